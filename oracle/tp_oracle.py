@@ -1,0 +1,335 @@
+"""fp64 CPU oracle of the tensor-parallel sharded linear block (GQA-aware).
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm may import this module. The library
+(``tensor_sharded_linear_gqa_gb300``) never imports it and has no CPU fallback;
+the two share no code. Inputs come from the seeded generators in
+``tensor_sharded_linear_gqa_gb300.inputs``, which hold none of the method.
+
+It is a plain, slow, obviously correct restatement of what the pages define:
+
+[MLX]  mlxcel manual, "텐서 병렬화" (Tensor parallelism)
+       - 개념 (Concept): every rank sees the same input, holds one shard of W.
+       - 가중치 샤딩 전략 (Weight-sharding strategies): Column Parallel splits the
+         output dimension, rank r holds W[:, r*D_out/N:(r+1)*D_out/N]; Row
+         Parallel splits the input dimension, rank r holds W[r*D_in/N:(r+1)*D_in/N, :];
+         Replicated keeps a full copy on every rank.
+       - 통신 패턴 (Communication patterns): ring all-reduce = reduce-scatter then
+         all-gather, 2*(N-1)/N*tensor_size sent per rank; in every step rank r
+         sends to (r+1)%N and receives from (r+N-1)%N, N-1 steps.
+       - 아키텍처 인식 샤드 플랜 (Architecture-aware shard plan): the standard
+         transformer table (q/k/v/gate/up ColumnParallel, o/down RowParallel +
+         AllReduce, q AllGather) and the GQA rule (shard K/V when
+         num_kv_heads >= tp_size, replicate otherwise), with its two examples.
+       - 설정 (Configuration): --tp-size is a power of two, default 1.
+[WIKI] railscraft wiki, "텐서 병렬 처리" (Tensor parallel processing)
+       - 상세 1 (Details 1, column & row parallel): Y_i = X W_i, Y = [Y_1..Y_n];
+         Y_i = X_i W_i, Y = sum_i Y_i.
+       - 예시 1 (Example 1): single-process column-parallel simulation; weights
+         are stored [out x in] and each shard computes X * W_i^T.
+
+Conventions (readings of the pages, each listed in the design notes):
+  * Weights are stored [out x in] (the simulation's layout), Y = X * W^T. A
+    "column shard" of the manual's W[D_in x D_out] is therefore a contiguous
+    block of stored rows, a "row shard" a block of stored columns.
+  * Ring chunks are contiguous flat ranges, chunk c = [floor(c*S/N), floor((c+1)*S/N)).
+  * Reduce-scatter step s: rank r sends chunk (r-1-s) mod N to rank (r+1)%N, which
+    adds it to its own copy; afterwards rank r holds the reduced chunk r.
+    All-gather step s: rank r sends chunk (r-s) mod N, the receiver overwrites.
+    A chunk received in step s is the one sent in step s+1.
+  * The collectives compute in the dtype of the buffers they are given: float64
+    by default, float32 when a caller wants the bit pattern of an fp32 ring
+    (each add is one IEEE add in that precision, in the order above).
+  * Activation of the MLP block: SwiGLU, silu(g) * u with silu(x) = x / (1 + e^-x)
+    (the pages name no activation).
+  * The o_proj input (attention context A) is an explicit input; attention
+    itself is not part of this block.
+
+Parity status: every public function is pinned by a CPU test against facts the
+pages and the mathematics fix (closed forms, worked examples, invariants,
+brute force on tiny inputs); see tests/test_oracle_*.py. None is unpinned.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Plan vocabulary ([MLX] 가중치 샤딩 전략 / 통신 패턴 / 아키텍처 인식 샤드 플랜)
+# ---------------------------------------------------------------------------
+COLUMN, ROW, VOCAB, REPLICATED = "ColumnParallel", "RowParallel", "VocabParallel", "Replicated"
+NO_COMM, ALL_REDUCE, ALL_GATHER, REDUCE_SCATTER = "None", "AllReduce", "AllGather", "ReduceScatter"
+
+WEIGHTS = ("q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj")
+
+
+class PlanError(ValueError):
+    """Raised for a configuration the plan rule does not accept. ``kind`` names why."""
+
+    def __init__(self, kind: str, msg: str):
+        super().__init__(msg)
+        self.kind = kind
+
+
+@dataclass
+class RankShard:
+    rank: int
+    q_heads: tuple            # [begin, end) of global q heads on this rank
+    kv_heads: tuple           # [begin, end) of global kv heads on this rank
+    kv_replicated: bool
+    strategy: dict = field(default_factory=dict)   # weight -> strategy
+    comm: dict = field(default_factory=dict)       # weight -> comm pattern after it
+    # weight -> [begin, end): output features (column weights) or input features
+    # (row weights) of the manual's W[D_in x D_out] that this rank holds.
+    ranges: dict = field(default_factory=dict)
+    q_to_kv: list = field(default_factory=list)    # local q head -> local kv head
+
+
+def _is_pow2(n: int) -> bool:
+    return n >= 1 and (n & (n - 1)) == 0
+
+
+def shard_plan(tp_size: int, hidden: int, num_q_heads: int, num_kv_heads: int,
+               head_dim: int, ffn: int) -> list:
+    """Per-rank shard plan of one decoder layer.
+
+    [MLX] 설정: tp_size must be a power of two (default 1).
+    [MLX] 아키텍처 인식 샤드 플랜, standard-transformer table: q/k/v ColumnParallel
+    (q followed by AllGather), o RowParallel + AllReduce, gate/up ColumnParallel
+    with no communication, down RowParallel + AllReduce.
+    [MLX] GQA-aware attention sharding: num_kv_heads >= tp_size -> K/V sharded;
+    num_kv_heads < tp_size -> K/V replicated on every rank (no rank gets a
+    fraction of a KV head).
+    Divisibility the pages leave open is required: q heads and ffn split evenly,
+    q heads group evenly over kv heads, sharded kv heads split evenly.
+    """
+    N = tp_size
+    if not _is_pow2(N):
+        raise PlanError("tp_size_not_pow2", f"tp_size {N} is not a power of two")
+    for name, v in (("hidden", hidden), ("num_q_heads", num_q_heads),
+                    ("num_kv_heads", num_kv_heads), ("head_dim", head_dim), ("ffn", ffn)):
+        if v < 1:
+            raise PlanError("invalid", f"{name} must be >= 1")
+    if num_q_heads % num_kv_heads != 0:
+        raise PlanError("gqa_shape", "num_q_heads must be a multiple of num_kv_heads")
+    if num_q_heads % N != 0:
+        raise PlanError("gqa_shape", "num_q_heads must divide evenly over tp_size")
+    replicated = num_kv_heads < N
+    if not replicated and num_kv_heads % N != 0:
+        raise PlanError("gqa_shape", "sharded num_kv_heads must divide evenly over tp_size")
+    if ffn % N != 0:
+        raise PlanError("not_divisible", "ffn must divide evenly over tp_size")
+
+    q_per = num_q_heads // N
+    group = num_q_heads // num_kv_heads          # q heads sharing one kv head
+    plan = []
+    for r in range(N):
+        qb, qe = r * q_per, (r + 1) * q_per
+        if replicated:
+            kb, ke = 0, num_kv_heads
+        else:
+            kv_per = num_kv_heads // N
+            kb, ke = r * kv_per, (r + 1) * kv_per
+        fb, fe = r * (ffn // N), (r + 1) * (ffn // N)
+        kv_strategy = REPLICATED if replicated else COLUMN
+        s = RankShard(rank=r, q_heads=(qb, qe), kv_heads=(kb, ke), kv_replicated=replicated)
+        s.strategy = {"q_proj": COLUMN, "k_proj": kv_strategy, "v_proj": kv_strategy,
+                      "o_proj": ROW, "gate_proj": COLUMN, "up_proj": COLUMN,
+                      "down_proj": ROW}
+        s.comm = {"q_proj": ALL_GATHER, "k_proj": NO_COMM, "v_proj": NO_COMM,
+                  "o_proj": ALL_REDUCE, "gate_proj": NO_COMM, "up_proj": NO_COMM,
+                  "down_proj": ALL_REDUCE}
+        s.ranges = {"q_proj": (qb * head_dim, qe * head_dim),
+                    "k_proj": (kb * head_dim, ke * head_dim),
+                    "v_proj": (kb * head_dim, ke * head_dim),
+                    "o_proj": (qb * head_dim, qe * head_dim),
+                    "gate_proj": (fb, fe), "up_proj": (fb, fe), "down_proj": (fb, fe)}
+        # Local q head j is global head qb+j; it reads global kv head (qb+j)//group,
+        # which sits at local index (that - kb) on this rank.
+        s.q_to_kv = [(qb + j) // group - kb for j in range(q_per)]
+        plan.append(s)
+    return plan
+
+
+# ---------------------------------------------------------------------------
+# Linear algebra ([WIKI] 상세 1, 예시 1; [MLX] Column Parallel / Row Parallel)
+# ---------------------------------------------------------------------------
+def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """Unsharded Y = X * W^T with W stored [out x in] ([WIKI] 예시 1)."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    return x @ w.T
+
+
+def split_rows(w: np.ndarray, n: int) -> list:
+    """Column-parallel shards: contiguous blocks of stored rows (output features)."""
+    out = w.shape[0]
+    assert out % n == 0
+    k = out // n
+    return [w[r * k:(r + 1) * k, :] for r in range(n)]
+
+
+def split_cols(a: np.ndarray, n: int) -> list:
+    """Row-parallel shards: contiguous blocks of stored columns (input features)."""
+    inn = a.shape[1]
+    assert inn % n == 0
+    k = inn // n
+    return [a[:, r * k:(r + 1) * k] for r in range(n)]
+
+
+def column_parallel(x: np.ndarray, w_shards: list) -> list:
+    """Per-rank Y_r = X * W_r^T, X replicated ([MLX] Column Parallel; [WIKI] 상세 1)."""
+    return [linear(x, w) for w in w_shards]
+
+
+def all_gather_columns(ys: list) -> np.ndarray:
+    """All-gather as concatenation along features, Y = [Y_1, ..., Y_N] ([WIKI] 상세 1)."""
+    return np.concatenate([np.asarray(y, dtype=np.float64) for y in ys], axis=1)
+
+
+def row_parallel(x_shards: list, w_shards: list) -> list:
+    """Per-rank partial P_r = X_r * W_r^T ([MLX] Row Parallel; [WIKI] 상세 1)."""
+    assert len(x_shards) == len(w_shards)
+    return [linear(x, w) for x, w in zip(x_shards, w_shards)]
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """silu(x) = x * sigmoid(x) = x / (1 + e^-x), in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """SwiGLU gating of the MLP block: silu(g) * u."""
+    return silu(g) * np.asarray(u, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Ring collectives ([MLX] 통신 패턴)
+# ---------------------------------------------------------------------------
+@dataclass
+class RingLog:
+    """What a simulated ring did: every send with its step, ends, chunk and bytes."""
+    n: int
+    sends: list = field(default_factory=list)  # (phase, step, src, dst, chunk, nbytes)
+
+    def bytes_sent(self, rank: int, phase: str | None = None) -> int:
+        return sum(b for (p, _s, src, _d, _c, b) in self.sends
+                   if src == rank and (phase is None or p == phase))
+
+    def steps(self, phase: str) -> int:
+        st = {s for (p, s, *_rest) in self.sends if p == phase}
+        return len(st)
+
+
+def chunk_bounds(size: int, n: int, c: int) -> tuple:
+    """Flat element range of ring chunk c of a buffer of ``size`` elements."""
+    return (c * size) // n, ((c + 1) * size) // n
+
+
+def ring_reduce_scatter(bufs: list, log: RingLog | None = None) -> list:
+    """Ring reduce-scatter, in place on copies of ``bufs`` (flat per-rank buffers).
+
+    N-1 steps; in step s every rank r sends chunk (r-1-s) mod N to (r+1)%N, which
+    adds what it receives to its own copy of that chunk. All sends of a step are
+    taken from the buffers as they stand before the step. Afterwards rank r holds
+    the fully reduced chunk r ([MLX] 통신 패턴: All-reduce (ring), Reduce-scatter,
+    ring topology).
+    """
+    n = len(bufs)
+    out = [np.array(b, copy=True).reshape(-1) for b in bufs]
+    size = out[0].size
+    for s in range(n - 1):
+        msgs = []
+        for r in range(n):
+            c = (r - 1 - s) % n
+            lo, hi = chunk_bounds(size, n, c)
+            msgs.append(((r + 1) % n, c, out[r][lo:hi].copy(), r))
+        for dst, c, data, src in msgs:
+            lo, hi = chunk_bounds(size, n, c)
+            out[dst][lo:hi] = data + out[dst][lo:hi]
+            if log is not None:
+                log.sends.append(("reduce_scatter", s, src, dst, c, data.nbytes))
+    return out
+
+
+def ring_all_gather(bufs: list, log: RingLog | None = None) -> list:
+    """Ring all-gather of chunk-owned buffers: rank r starts owning chunk r.
+
+    N-1 steps; in step s rank r sends chunk (r-s) mod N to (r+1)%N, which
+    overwrites its copy. Afterwards every rank holds every chunk
+    ([MLX] 통신 패턴: All-gather, ring forwarding).
+    """
+    n = len(bufs)
+    out = [np.array(b, copy=True).reshape(-1) for b in bufs]
+    size = out[0].size
+    for s in range(n - 1):
+        msgs = []
+        for r in range(n):
+            c = (r - s) % n
+            lo, hi = chunk_bounds(size, n, c)
+            msgs.append(((r + 1) % n, c, out[r][lo:hi].copy(), r))
+        for dst, c, data, src in msgs:
+            lo, hi = chunk_bounds(size, n, c)
+            out[dst][lo:hi] = data
+            if log is not None:
+                log.sends.append(("all_gather", s, src, dst, c, data.nbytes))
+    return out
+
+
+def ring_all_reduce(bufs: list, log: RingLog | None = None) -> list:
+    """Ring all-reduce = reduce-scatter followed by all-gather ([MLX] 통신 패턴)."""
+    return ring_all_gather(ring_reduce_scatter(bufs, log), log)
+
+
+def gather_flat_shards(shards: list) -> np.ndarray:
+    """Full tensor assembled from per-rank flat shards (rank r contributes chunk r)."""
+    return np.concatenate([np.asarray(s).reshape(-1) for s in shards])
+
+
+# ---------------------------------------------------------------------------
+# Blocks ([MLX] 아키텍처 인식 샤드 플랜; [WIKI] 상세 1, last paragraph)
+# ---------------------------------------------------------------------------
+def mlp_unsharded(x, wg, wu, wd) -> np.ndarray:
+    """Y = (silu(X Wg^T) * (X Wu^T)) Wd^T, the plain definition."""
+    return linear(swiglu(linear(x, wg), linear(x, wu)), wd)
+
+
+def mlp_sharded(x, wg, wu, wd, tp_size: int, log: RingLog | None = None) -> dict:
+    """MLP block sharded per the plan table: gate/up ColumnParallel (no comm),
+    down RowParallel + ring AllReduce. Returns per-rank H_r, partials P_r and
+    the all-reduced per-rank outputs (each [T x D])."""
+    T = x.shape[0]
+    D = wd.shape[0]
+    g = column_parallel(x, split_rows(wg, tp_size))
+    u = column_parallel(x, split_rows(wu, tp_size))
+    h = [swiglu(gr, ur) for gr, ur in zip(g, u)]
+    p = row_parallel(h, split_cols(wd, tp_size))
+    y = ring_all_reduce([pr.reshape(-1) for pr in p], log)
+    return {"h": h, "partials": p, "y": [yr.reshape(T, D) for yr in y]}
+
+
+def attn_proj_unsharded(x, wq, wk, wv, a, wo) -> dict:
+    """q/k/v = X W^T for each projection; Y = A Wo^T."""
+    return {"q": linear(x, wq), "k": linear(x, wk), "v": linear(x, wv), "y": linear(a, wo)}
+
+
+def attn_proj_sharded(x, wq, wk, wv, a, wo, plan: list, head_dim: int,
+                      log: RingLog | None = None) -> dict:
+    """Attention projections sharded per the plan: q/k/v column-parallel on the
+    rank's heads (K/V whole on every rank when replicated), o_proj row-parallel on
+    the rank's slice of A + ring all-reduce."""
+    q, k, v, parts = [], [], [], []
+    for s in plan:
+        qb, qe = s.ranges["q_proj"]
+        kb, ke = s.ranges["k_proj"]
+        q.append(linear(x, wq[qb:qe, :]))
+        k.append(linear(x, wk[kb:ke, :]))
+        v.append(linear(x, wv[kb:ke, :]))
+        ob, oe = s.ranges["o_proj"]
+        parts.append(linear(a[:, ob:oe], wo[:, ob:oe]))
+    T, D = a.shape[0], wo.shape[0]
+    y = ring_all_reduce([p.reshape(-1) for p in parts], log)
+    return {"q": q, "k": k, "v": v, "partials": parts, "y": [yr.reshape(T, D) for yr in y]}

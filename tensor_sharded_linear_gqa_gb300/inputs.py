@@ -1,0 +1,141 @@
+"""Seeded synthetic inputs and workload shapes for the tensor-parallel linear block.
+
+This module is shared by the tests, the benchmark and ``smoke()``. It draws
+random numbers, rounds them to bf16 bit patterns and describes the shapes of
+the workloads. It holds none of the block's arithmetic (no products, sums,
+activations, shard plans or collectives), so both the CUDA path and the fp64
+oracle can take their inputs from it without sharing any of the method.
+
+Generator: numpy PCG64 through ``SeedSequence(seed, spawn_key=(stream,))``; one
+independent stream per tensor (see ``STREAM``). Values are drawn as float64
+normals, narrowed to float32 and rounded to bf16 by round-to-nearest-even on
+the bit pattern. The oracle widens the same bits exactly to float64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# One independent random stream per tensor role.
+STREAM = {
+    "x": 0,      # activations X [T x hidden]
+    "a": 1,      # attention context A [T x q_heads*head_dim] (input of o_proj)
+    "wq": 2, "wk": 3, "wv": 4, "wo": 5,
+    "wg": 6, "wu": 7, "wd": 8,
+    "w": 9,      # plain linear weight of the fp32 worked example
+    "buf": 10,   # raw collective buffers
+}
+
+# Workloads, named by what they are. Weight tensors are stored [out x in]
+# row-major (K-major). ``w_std`` is the standard deviation of the weights,
+# activations are N(0, 1).
+WORKLOADS = {
+    # Column-parallel simulation worked example of the railscraft wiki page
+    # (in 1024, out 2048, two virtual GPUs, batch 32), run in fp32 both as a
+    # column-parallel and as a row-parallel layer.
+    "wiki_linear_fp32_tp2": dict(kind="linear_fp32", T=32, d_in=1024, d_out=2048,
+                                 tp=2, seed=101, w_std=1.0),
+    # Llama-style MLP block, TP=2, bf16.
+    "mlp_tp2_t512": dict(kind="mlp", T=512, hidden=2048, ffn=8192, tp=2,
+                         seed=102, w_std=0.02),
+    # Attention projections with GQA sharding, TP=4, bf16.
+    "attn_gqa_tp4_t2048": dict(kind="attn", T=2048, hidden=4096, q_heads=32,
+                               kv_heads=8, head_dim=128, tp=4, seed=103,
+                               w_std=0.02),
+    # Decode-shaped step: 4 KV heads replicated over 8 ranks, bf16.
+    "decode_gqa_rep_tp8_t64": dict(kind="layer", T=64, hidden=4096, q_heads=32,
+                                   kv_heads=4, head_dim=128, ffn=14336, tp=8,
+                                   seed=104, w_std=0.02),
+    # Large decoder-layer projections + MLP prefill, TP=8, bf16.
+    "prefill_layer_tp8_t4096": dict(kind="layer", T=4096, hidden=8192, q_heads=64,
+                                    kv_heads=8, head_dim=128, ffn=28672, tp=8,
+                                    seed=105, w_std=0.02, oracle_rows=64),
+}
+
+
+def rng(seed: int, stream: int) -> np.random.Generator:
+    """Independent PCG64 generator for (seed, stream)."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(stream,))))
+
+
+def normal_f32(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
+    """N(0, std^2) samples as float32."""
+    g = rng(seed, stream)
+    out = g.standard_normal(size=shape, dtype=np.float64)
+    if std != 1.0:
+        out *= std
+    return out.astype(np.float32)
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even); return uint16 bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    bias = ((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF)
+    return ((u + bias) >> np.uint64(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float32 exactly."""
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    """Widen bf16 bit patterns to float64 exactly."""
+    return bf16_bits_to_f32(b).astype(np.float64)
+
+
+def normal_bf16(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
+    """N(0, std^2) samples rounded to bf16, as uint16 bit patterns."""
+    return f32_to_bf16_bits(normal_f32(seed, stream, shape, std))
+
+
+def small_int_bf16(seed: int, stream: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """Uniform integers in [lo, hi] as bf16 bits (exact in bf16; used for bit-exact cases)."""
+    g = rng(seed, stream)
+    v = g.integers(lo, hi + 1, size=shape).astype(np.float32)
+    return f32_to_bf16_bits(v)
+
+
+def small_int_f32(seed: int, stream: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """Uniform integers in [lo, hi] as float32."""
+    g = rng(seed, stream)
+    return g.integers(lo, hi + 1, size=shape).astype(np.float32)
+
+
+def weight_shapes(w: dict) -> dict:
+    """Full (unsharded) weight shapes [out x in] of a workload."""
+    kind = w["kind"]
+    if kind == "linear_fp32":
+        return {"w": (w["d_out"], w["d_in"])}
+    D = w["hidden"]
+    out = {}
+    if kind in ("attn", "layer"):
+        hd = w["head_dim"]
+        out.update(wq=(w["q_heads"] * hd, D), wk=(w["kv_heads"] * hd, D),
+                   wv=(w["kv_heads"] * hd, D), wo=(D, w["q_heads"] * hd))
+    if kind in ("mlp", "layer"):
+        F = w["ffn"]
+        out.update(wg=(F, D), wu=(F, D), wd=(D, F))
+    return out
+
+
+def make_bf16_inputs(w: dict, rows: int | None = None) -> dict:
+    """Full bf16 inputs (uint16 bits) of a bf16 workload.
+
+    ``x`` and ``a`` are [T x .] N(0,1); weights are N(0, w_std^2). ``rows`` limits
+    nothing here: activations are always drawn whole so that a row sample of them
+    is the same bits the GPU sees.
+    """
+    seed, T = w["seed"], w["T"]
+    out = {"x": normal_bf16(seed, STREAM["x"], (T, w["hidden"]))}
+    if w["kind"] in ("attn", "layer"):
+        out["a"] = normal_bf16(seed, STREAM["a"], (T, w["q_heads"] * w["head_dim"]))
+    for name, shp in weight_shapes(w).items():
+        out[name] = normal_bf16(seed, STREAM[name], shp, w["w_std"])
+    return out
+
+
+def make_fp32_linear_inputs(w: dict) -> dict:
+    """fp32 inputs of the worked fp32 linear example: X [T x d_in], W [d_out x d_in]."""
+    seed = w["seed"]
+    return {"x": normal_f32(seed, STREAM["x"], (w["T"], w["d_in"])),
+            "w": normal_f32(seed, STREAM["w"], (w["d_out"], w["d_in"]), w["w_std"])}
