@@ -1,0 +1,309 @@
+/*
+ * tpgqa.h - C ABI of the tensor-parallel sharded linear block (GQA-aware) on
+ * one GB300 (sm_103a).
+ *
+ * Execution model. All N logical tensor-parallel ranks live in one GPU's HBM
+ * and run in lockstep in one process (mlxcel manual "텐서 병렬화", section
+ * 현재 런타임 지원 범위 / Current runtime support: in-process multi-rank). A
+ * rank's shard is a tp_tensor; a "collective" is a kernel that moves or reduces
+ * shard buffers on this one device. No peer-to-peer or network traffic exists.
+ *
+ * Weights are stored [out x in], row-major (K-major), and every linear
+ * computes Y = X * W^T (railscraft wiki "텐서 병렬 처리", 예시 1 / Example 1). A
+ * column shard of the manual's W[D_in x D_out] is therefore a contiguous block
+ * of stored rows; a row shard is a block of stored columns.
+ *
+ * Conventions shared by every call:
+ *  - Ownership: the caller owns every tensor buffer and every workspace; the
+ *    library allocates no device memory in these calls. The only object the
+ *    library owns is tp_plan (host memory, freed by tp_plan_destroy).
+ *  - Streams: every call that touches device memory only enqueues work on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream) and returns
+ *    without synchronising. Buffers must stay valid until that work is done.
+ *  - Pointers: tp_tensor.ptr is a device pointer. Arrays of tp_tensor
+ *    (per-rank arguments) are host arrays, read during the call only.
+ *  - Errors: every call returns a tp_status and never aborts. Arguments are
+ *    checked before any launch; on an error nothing is enqueued. TP_ERR_CUDA
+ *    means a CUDA runtime call failed; tp_last_cuda_error() gives its code.
+ *    Device-side errors (a bounded wait that ran out) are recorded in a device
+ *    status word and reported by tp_device_status().
+ *  - Alignment: tensors handed to the tensor-core (bf16) path need a 16-byte
+ *    aligned base and a row pitch (ld * element size) that is a multiple of 16
+ *    bytes, else TP_ERR_ALIGNMENT. Collective buffers need a 16-byte aligned
+ *    base.
+ *  - Empty inputs: zero rows (tokens) or zero elements is valid and enqueues
+ *    nothing.
+ *  - Thread safety: calls on different streams may run concurrently; a plan
+ *    is immutable after creation and may be shared.
+ */
+#ifndef TPGQA_H
+#define TPGQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *tp_stream_t;
+
+typedef enum tp_status {
+  TP_OK = 0,
+  TP_ERR_INVALID_ARG = 1,      /* null pointer, bad shape, bad mode, ...            */
+  TP_ERR_TP_SIZE_NOT_POW2 = 2, /* tp_size is not a power of two (설정 / --tp-size)   */
+  TP_ERR_NOT_DIVISIBLE = 3,    /* ffn (or another split dimension) not divisible by N */
+  TP_ERR_GQA_SHAPE = 4,        /* head counts the GQA rule cannot shard             */
+  TP_ERR_DTYPE = 5,            /* dtype combination not supported                    */
+  TP_ERR_ALIGNMENT = 6,        /* base or pitch not 16-byte aligned                  */
+  TP_ERR_RANK_FAILED = 7,      /* a rank is marked unhealthy (tp_set_rank_health)    */
+  TP_ERR_TIMEOUT = 8,          /* a bounded device-side wait ran out                 */
+  TP_ERR_CUDA = 9,             /* a CUDA runtime call failed; see tp_last_cuda_error */
+  TP_ERR_WORKSPACE = 10,       /* workspace missing or too small                     */
+  TP_ERR_UNSUPPORTED = 11      /* valid request this build does not implement        */
+} tp_status;
+
+typedef enum tp_dtype { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
+
+/* A 2-D row-major view: element (i, j) lives at ptr + (i * ld + j) * size(dtype).
+ * ld >= cols. rows or cols may be 0 (empty). */
+typedef struct tp_tensor {
+  void *ptr;
+  int32_t dtype; /* tp_dtype */
+  int32_t reserved;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
+} tp_tensor;
+
+/* ---------------------------------------------------------------------------
+ * Shard plan (mlxcel manual "텐서 병렬화": 가중치 샤딩 전략 / Weight-sharding
+ * strategies; 아키텍처 인식 샤드 플랜 / Architecture-aware shard plan, its
+ * standard-transformer table and the GQA-aware attention sharding rule).
+ * ------------------------------------------------------------------------- */
+typedef struct tp_dims {
+  int32_t tp_size;      /* N, a power of two >= 1                      */
+  int32_t hidden;       /* D                                           */
+  int32_t num_q_heads;  /* Hq                                          */
+  int32_t num_kv_heads; /* Hkv; Hq must be a multiple of Hkv           */
+  int32_t head_dim;     /* hd                                          */
+  int32_t ffn;          /* F, divisible by N                           */
+} tp_dims;
+
+typedef enum tp_shard_strategy {
+  TP_SHARD_COLUMN = 0,
+  TP_SHARD_ROW = 1,
+  TP_SHARD_VOCAB = 2,
+  TP_SHARD_REPLICATED = 3
+} tp_shard_strategy;
+
+typedef enum tp_comm_pattern {
+  TP_COMM_NONE = 0,
+  TP_COMM_ALL_REDUCE = 1,
+  TP_COMM_ALL_GATHER = 2,
+  TP_COMM_REDUCE_SCATTER = 3
+} tp_comm_pattern;
+
+typedef enum tp_weight {
+  TP_W_Q = 0, TP_W_K = 1, TP_W_V = 2, TP_W_O = 3,
+  TP_W_GATE = 4, TP_W_UP = 5, TP_W_DOWN = 6,
+  TP_W_COUNT = 7
+} tp_weight;
+
+typedef struct tp_rank_shard {
+  int32_t rank;
+  int32_t q_head_begin, q_head_end;   /* global q heads [begin, end) on this rank        */
+  int32_t kv_head_begin, kv_head_end; /* global kv heads on this rank (all when replicated) */
+  int32_t kv_replicated;              /* 1 when num_kv_heads < tp_size                   */
+  int32_t strategy[TP_W_COUNT];       /* tp_shard_strategy per weight                    */
+  int32_t comm[TP_W_COUNT];           /* tp_comm_pattern that follows the weight         */
+  /* Feature range [begin, end) this rank holds: output features for column
+   * weights (q, k, v, gate, up), input features for row weights (o, down),
+   * in the manual's W[D_in x D_out] terms (rows of the [out x in] storage for
+   * column weights, columns of it for row weights). */
+  int64_t range_begin[TP_W_COUNT];
+  int64_t range_end[TP_W_COUNT];
+} tp_rank_shard;
+
+typedef struct tp_plan tp_plan;
+
+/* Builds the plan of one decoder layer. Rule: q heads split evenly; K/V sharded
+ * when num_kv_heads >= tp_size (num_kv_heads % tp_size must be 0), replicated
+ * on every rank otherwise; q/k/v/gate/up ColumnParallel, o/down RowParallel +
+ * AllReduce, q followed by AllGather (the manual's table). On success *out owns
+ * a new plan. Errors: TP_ERR_INVALID_ARG (null, non-positive dims),
+ * TP_ERR_TP_SIZE_NOT_POW2, TP_ERR_GQA_SHAPE, TP_ERR_NOT_DIVISIBLE. Host only. */
+tp_status tp_plan_create(const tp_dims *dims, tp_plan **out);
+
+/* Frees a plan created by tp_plan_create. NULL is accepted. */
+tp_status tp_plan_destroy(tp_plan *plan);
+
+/* Copies the dims the plan was built from. */
+tp_status tp_plan_dims(const tp_plan *plan, tp_dims *out);
+
+/* Fills *out with rank `rank`'s shard description. TP_ERR_INVALID_ARG for a
+ * rank outside [0, tp_size). Host only. */
+tp_status tp_plan_query_rank(const tp_plan *plan, int32_t rank, tp_rank_shard *out);
+
+/* Local GQA map of rank `rank`: out[j] = local kv head read by local q head j,
+ * j in [0, q_head_end - q_head_begin). `capacity` is the length of `out`;
+ * TP_ERR_INVALID_ARG when it is too small. Host only. */
+tp_status tp_plan_q_to_kv(const tp_plan *plan, int32_t rank, int32_t *out, int32_t capacity);
+
+/* ---------------------------------------------------------------------------
+ * Linear layers (mlxcel manual: Column Parallel / Row Parallel; railscraft
+ * wiki 상세 1: Y_i = X W_i with Y = [Y_1..Y_n], and Y_i = X_i W_i with Y = sum Y_i).
+ * ------------------------------------------------------------------------- */
+
+/* Column-parallel linear: Y_r = X * W_r^T for r in [0, tp_size), X replicated.
+ *  x       : [T x K]. bf16 (tensor cores, fp32 accumulation) or f32 (exact fp32 FMA).
+ *  w[r]    : [n_r x K], same dtype as x.
+ *  gather=1: y[0] is one [T x sum_r n_r] tensor; shard r is written straight into
+ *            columns [sum_{q<r} n_q, ...) (the all-gather is the concatenation
+ *            and moves no extra bytes).
+ *  gather=0: y[r] is rank r's own [T x n_r] output.
+ *  y dtype : f32 or bf16 for bf16 inputs (rounded to nearest even); f32 for f32.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_CUDA. */
+tp_status tp_column_linear(int32_t tp_size, const tp_tensor *x, const tp_tensor *w,
+                           tp_tensor *y, int32_t gather, tp_stream_t stream);
+
+typedef enum tp_combine {
+  TP_COMBINE_NONE = 0,       /* y[r] = partial P_r (no reduction)                           */
+  TP_COMBINE_FUSED = 1,      /* y[0] = sum_r P_r, summed in the tensor-core accumulator over
+                                shards 0..N-1 in order; no partial is written              */
+  TP_COMBINE_RING = 2,       /* y[r] = P_r, then the ring all-reduce as N-1 reduce-scatter and
+                                N-1 all-gather step launches; every y[r] ends equal to the sum */
+  TP_COMBINE_RING_FUSED = 3  /* as TP_COMBINE_RING, one pass that folds the partials in the
+                                ring's order (bit-identical to TP_COMBINE_RING)            */
+} tp_combine;
+
+/* Row-parallel linear: P_r = X_r * W_r^T, then the combine above.
+ *  x[r] : [T x k_r] (rank r's slice of the input features), bf16 or f32.
+ *  w[r] : [n x k_r] (rank r's block of stored columns), same dtype as x[r].
+ *  y    : f32; y[0] alone for TP_COMBINE_FUSED, y[0..N-1] otherwise, each [T x n].
+ * The partials are the f32 accumulators. f32 inputs support NONE, RING and
+ * RING_FUSED. Errors: as tp_column_linear. */
+tp_status tp_row_linear(int32_t tp_size, const tp_tensor *x, const tp_tensor *w,
+                        tp_tensor *y, int32_t combine, tp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Ring collectives (mlxcel manual, 통신 패턴 / Communication patterns).
+ * buf[r] is rank r's f32 buffer; all N have the same rows x cols and are viewed
+ * flat in row-major order (S elements). Chunk c is the flat element range
+ * [floor(c*S/N), floor((c+1)*S/N)). Reduce-scatter step s: rank r sends chunk
+ * (r-1-s) mod N to rank (r+1) % N, which adds it to its copy; after N-1 steps
+ * rank r holds the reduced chunk r, summed in the order c+1, c+2, ..., c.
+ * All-gather step s: rank r sends chunk (r-s) mod N to (r+1) % N, which
+ * overwrites its copy. Buffers must be contiguous (ld == cols) and 16-byte
+ * aligned.
+ * ------------------------------------------------------------------------- */
+typedef enum tp_ring_mode {
+  TP_RING_STEPS = 0, /* one launch per ring step, N-1 per phase                       */
+  TP_RING_FUSED = 1  /* one launch per phase; same fold order, bit-identical results   */
+} tp_ring_mode;
+
+/* In-place reduce-scatter; afterwards chunk r of buf[r] is reduced. The other
+ * chunks of every buffer are unspecified afterwards (the step mode leaves
+ * intermediate sums there, the fused mode the original partials). */
+tp_status tp_reduce_scatter(int32_t tp_size, tp_tensor *buf, int32_t mode, tp_stream_t stream);
+
+/* In-place ring all-gather: on entry chunk r of buf[r] is rank r's chunk; on
+ * return every buffer holds every chunk. */
+tp_status tp_ring_all_gather(int32_t tp_size, tp_tensor *buf, int32_t mode, tp_stream_t stream);
+
+/* In-place all-reduce = reduce-scatter + all-gather; every buf[r] ends equal. */
+tp_status tp_allreduce_ring(int32_t tp_size, tp_tensor *buf, int32_t mode, tp_stream_t stream);
+
+/* Concatenating all-gather of separate shards (all-gather as concatenation).
+ *  shard[r] : [rows_r x cols_r], one dtype for all, f32 or bf16.
+ *  axis = 1 : columns; every shard has the same rows, out is [rows x sum cols_r].
+ *  axis = 0 : rows; every shard has the same cols, out is [sum rows_r x cols].
+ *  out[0..n_out-1]: n_out = 1 (one copy shared by all ranks) or tp_size (a copy
+ *  per rank). */
+tp_status tp_all_gather(int32_t tp_size, const tp_tensor *shard, tp_tensor *out, int32_t n_out,
+                        int32_t axis, tp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Blocks (mlxcel manual, 아키텍처 인식 샤드 플랜: gate/up ColumnParallel with no
+ * communication, down RowParallel + AllReduce; q/k/v ColumnParallel, o
+ * RowParallel + AllReduce).
+ * ------------------------------------------------------------------------- */
+
+/* Workspace bytes tp_mlp_block needs for `tokens` tokens (H_r of every rank,
+ * bf16, T x F in total). */
+size_t tp_mlp_block_workspace_size(const tp_plan *plan, int64_t tokens);
+
+/* MLP block: H_r = silu(X G_r^T) * (X U_r^T) (SwiGLU fused into the gate/up
+ * GEMM's epilogue, H_r rounded to bf16), then Y = sum_r H_r D_r^T.
+ *  x         : [T x D] bf16.
+ *  w_gate[r] : [F/N x D] bf16; w_up[r] likewise (rows plan.range(GATE/UP) of G, U).
+ *  w_down[r] : [D x F/N] bf16 (columns plan.range(DOWN) of Down [D x F]).
+ *  y         : f32 [T x D]; y[0] for TP_COMBINE_FUSED, y[0..N-1] otherwise
+ *              (TP_COMBINE_NONE leaves the partials).
+ *  workspace : device memory of at least tp_mlp_block_workspace_size bytes,
+ *              16-byte aligned; its contents on entry do not matter.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_WORKSPACE,
+ * TP_ERR_RANK_FAILED, TP_ERR_CUDA. */
+tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_gate,
+                       const tp_tensor *w_up, const tp_tensor *w_down, tp_tensor *y,
+                       int32_t combine, void *workspace, size_t workspace_bytes,
+                       tp_stream_t stream);
+
+/* Attention projections with GQA sharding.
+ *  x        : [T x D] bf16.
+ *  w_q[r]   : [(q heads of r) * hd x D] bf16;  q[r]: [T x same] bf16 out.
+ *  w_k, w_v : sharded -> N tensors [(kv heads of r) * hd x D];
+ *             replicated -> ONE tensor [Hkv * hd x D] shared by every rank (it is
+ *             computed once); k, v outputs likewise (N or 1 tensors, bf16).
+ *  a[r]     : [T x (q heads of r) * hd] bf16, rank r's slice of the attention
+ *             context that feeds o_proj (attention itself is not part of this call).
+ *  w_o[r]   : [D x (q heads of r) * hd] bf16 (columns plan.range(O) of Wo).
+ *  y        : f32 [T x D]; y[0] for TP_COMBINE_FUSED, y[0..N-1] otherwise.
+ * Errors: as tp_mlp_block (no workspace). */
+tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_q,
+                       const tp_tensor *w_k, const tp_tensor *w_v, tp_tensor *q, tp_tensor *k,
+                       tp_tensor *v, const tp_tensor *a, const tp_tensor *w_o, tp_tensor *y,
+                       int32_t combine, tp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Status, health and diagnostics.
+ * ------------------------------------------------------------------------- */
+
+/* Static string naming a status. */
+const char *tp_status_str(tp_status s);
+
+/* cudaError_t of the last failed CUDA runtime call made by this library in the
+ * calling thread (0 if none). */
+int32_t tp_last_cuda_error(void);
+
+/* Marks logical rank `rank` healthy (1) or failed (0), process-wide. While any
+ * rank that a call involves is failed, the call returns TP_ERR_RANK_FAILED
+ * before enqueuing anything, so the whole TP group stops together (mlxcel
+ * manual, TP 실행기 / TP executor: health reporting and error propagation). */
+tp_status tp_set_rank_health(int32_t rank, int32_t healthy);
+
+/* Synchronises `stream`, then reads and clears the device status word that
+ * kernels set when a bounded wait runs out. Returns TP_OK, TP_ERR_TIMEOUT or
+ * TP_ERR_CUDA. *detail (optional) receives the raw word (0 = none). */
+tp_status tp_device_status(tp_stream_t stream, int32_t *detail);
+
+/* Sets the time budget, in nanoseconds, of every bounded device-side wait of
+ * kernels enqueued afterwards (0 restores the default of 2 s). Process-wide;
+ * meant for tests of the timeout path. */
+tp_status tp_set_wait_budget(int64_t nanoseconds);
+
+/* Enqueues one kernel whose bounded wait is on an mbarrier that no thread
+ * completes, so it always runs out; the kernel records TP_ERR_TIMEOUT in the
+ * device status word and returns. Used to test the timeout path without a
+ * GPU fault or hang. */
+tp_status tp_debug_wait_timeout(tp_stream_t stream);
+
+/* Library version string. */
+const char *tp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPGQA_H */

@@ -1,0 +1,104 @@
+"""Builds the in-tree shared library ``libtpgqa.so`` for sm_103a with nvcc.
+
+Each translation unit is compiled in parallel into ``_build/`` and linked into
+``tensor_sharded_linear_gqa_gb300/libtpgqa.so`` (static CUDA runtime; the driver
+API is reached through cudaGetDriverEntryPointByVersion, so libcuda is not a
+link dependency). A stamp records the machine and the source hashes, so a
+library built for another machine or from other sources is rebuilt.
+
+Usage: ``python -m tensor_sharded_linear_gqa_gb300.build [--force] [-v]``.
+"""
+from __future__ import annotations
+
+import hashlib
+import json
+import os
+import platform
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libtpgqa.so")
+STAMP = os.path.join(BUILD, "stamp.json")
+
+SOURCES = ["plan.cpp", "tp_api.cu", "gemm_tcgen05.cu", "gemm_f32.cu", "combine.cu"]
+HEADERS = ["tp_internal.h", "sm100_ptx.cuh"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found; the CUDA 13 toolkit is required to build libtpgqa.so")
+
+
+def _digest() -> str:
+    h = hashlib.sha256()
+    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "tpgqa.h"),
+                                                                  os.path.abspath(__file__)]
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _stamp() -> dict:
+    return {"machine": platform.machine(), "digest": _digest()}
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+        return False
+    try:
+        with open(STAMP) as fh:
+            return json.load(fh) == _stamp()
+    except (OSError, ValueError):
+        return False
+
+
+def _compile(src: str, verbose: bool) -> str:
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+           "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, src), "-o", obj]
+    if src.endswith(".cpp"):
+        cmd[1:1] = ["-x", "c++"]
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+    if verbose and (r.stdout or r.stderr):
+        print(r.stdout + r.stderr, flush=True)
+    return obj
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles and links libtpgqa.so if it is missing or stale; returns its path."""
+    if not force and up_to_date():
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    with ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
+    tmp = LIB + ".tmp"
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB)
+    with open(STAMP, "w") as fh:
+        json.dump(_stamp(), fh)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

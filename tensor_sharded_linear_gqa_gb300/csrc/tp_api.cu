@@ -1,0 +1,695 @@
+// C ABI of the library: argument checks, launch sequencing and status codes.
+// Every entry point validates everything before it enqueues anything; on an
+// error nothing is launched. No entry point allocates device memory.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "tp_internal.h"
+
+namespace tpgqa {
+namespace {
+
+__device__ int g_dev_status = 0;
+
+constexpr long long kDefaultWaitNs = 2000000000LL;  // 2 s
+std::atomic<long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<unsigned long long> g_failed_ranks{0};
+thread_local int t_last_cuda_error = 0;
+
+std::mutex g_dev_mu;
+int *g_status_addr[64] = {nullptr};
+int g_sm_count[64] = {0};
+
+size_t esize(int32_t dt) { return dt == TP_F32 ? 4 : (dt == TP_BF16 ? 2 : 0); }
+
+bool shape_ok(const tp_tensor &t) {
+  if (esize(t.dtype) == 0) return false;
+  if (t.rows < 0 || t.cols < 0 || t.ld < t.cols || t.ld < 1) return false;
+  if (t.rows > 0 && t.cols > 0 && t.ptr == nullptr) return false;
+  return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Base and row pitch on 16-byte boundaries (tensor maps, vector stores).
+bool pitch_ok(const tp_tensor &t) {
+  return aligned16(t.ptr) && ((t.ld * static_cast<long long>(esize(t.dtype))) % 16) == 0;
+}
+
+bool pow2_in_range(int32_t n) { return n >= 1 && n <= kMaxRanks && (n & (n - 1)) == 0; }
+
+tp_status check_health(int32_t n) {
+  const unsigned long long mask = g_failed_ranks.load();
+  if (!mask) return TP_OK;
+  for (int32_t r = 0; r < n && r < 64; ++r)
+    if (mask & (1ULL << r)) return TP_ERR_RANK_FAILED;
+  return TP_OK;
+}
+
+char *byte_ptr(void *p, long long elems, int32_t dt) {
+  return static_cast<char *>(p) + elems * static_cast<long long>(esize(dt));
+}
+
+tp_status zero_fill(const tp_tensor &t, long long col0, long long cols, cudaStream_t s) {
+  if (t.rows == 0 || cols == 0) return TP_OK;
+  const size_t es = esize(t.dtype);
+  const cudaError_t e = cudaMemset2DAsync(byte_ptr(t.ptr, col0, t.dtype), t.ld * es, 0, cols * es,
+                                          t.rows, s);
+  return e == cudaSuccess ? TP_OK : cuda_fail(e);
+}
+
+// ---- ring collectives over y[0..n-1] ----
+tp_status check_ring_bufs(int32_t n, const tp_tensor *buf) {
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (!buf) return TP_ERR_INVALID_ARG;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(buf[r])) return TP_ERR_INVALID_ARG;
+    if (buf[r].dtype != TP_F32) return TP_ERR_DTYPE;
+    if (buf[r].rows != buf[0].rows || buf[r].cols != buf[0].cols) return TP_ERR_INVALID_ARG;
+    if (buf[r].rows > 1 && buf[r].ld != buf[r].cols) return TP_ERR_INVALID_ARG;
+    if (buf[r].rows * buf[r].cols > 0 && !aligned16(buf[r].ptr)) return TP_ERR_ALIGNMENT;
+    for (int32_t q = 0; q < r; ++q)
+      if (buf[q].ptr == buf[r].ptr && buf[r].rows * buf[r].cols > 0) return TP_ERR_INVALID_ARG;
+  }
+  return TP_OK;
+}
+
+RankPtrs rank_ptrs(int32_t n, const tp_tensor *buf) {
+  RankPtrs p;
+  std::memset(&p, 0, sizeof(p));
+  for (int32_t r = 0; r < n; ++r) p.p[r] = static_cast<float *>(buf[r].ptr);
+  return p;
+}
+
+tp_status run_reduce_scatter(int32_t n, const tp_tensor *buf, int32_t mode, cudaStream_t s) {
+  const long long size = buf[0].rows * buf[0].cols;
+  if (n == 1 || size == 0) return TP_OK;
+  const RankPtrs p = rank_ptrs(n, buf);
+  if (mode == TP_RING_FUSED) return launch_ring_fused(p, n, size, 0, s);
+  for (int step = 0; step < n - 1; ++step) {
+    const tp_status st = launch_ring_rs_step(p, n, size, step, s);
+    if (st != TP_OK) return st;
+  }
+  return TP_OK;
+}
+
+tp_status run_all_gather_ring(int32_t n, const tp_tensor *buf, int32_t mode, cudaStream_t s) {
+  const long long size = buf[0].rows * buf[0].cols;
+  if (n == 1 || size == 0) return TP_OK;
+  const RankPtrs p = rank_ptrs(n, buf);
+  if (mode == TP_RING_FUSED) return launch_ring_ag_fused(p, n, size, s);
+  for (int step = 0; step < n - 1; ++step) {
+    const tp_status st = launch_ring_ag_step(p, n, size, step, s);
+    if (st != TP_OK) return st;
+  }
+  return TP_OK;
+}
+
+tp_status run_allreduce(int32_t n, const tp_tensor *buf, int32_t mode, cudaStream_t s) {
+  const long long size = buf[0].rows * buf[0].cols;
+  if (n == 1 || size == 0) return TP_OK;
+  if (mode == TP_RING_FUSED) return launch_ring_fused(rank_ptrs(n, buf), n, size, 1, s);
+  tp_status st = run_reduce_scatter(n, buf, TP_RING_STEPS, s);
+  if (st != TP_OK) return st;
+  return run_all_gather_ring(n, buf, TP_RING_STEPS, s);
+}
+
+// ---- GEMM sequencing ----
+// Column-parallel problems: one per rank, A = x, B = w[r], output to outs[r].
+struct ColOut {
+  void *ptr;
+  long long ld;
+};
+
+tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, const ColOut *outs,
+                           int epi, cudaStream_t s) {
+  const long long T = x.rows, K = x.cols;
+  long long t256 = 0, t128 = 0;
+  for (int32_t r = 0; r < nb; ++r) {
+    t256 += ((T + 127) / 128) * ((w[r].rows + 255) / 256);
+    t128 += ((T + 127) / 128) * ((w[r].rows + 127) / 128);
+  }
+  GemmBuilder b;
+  b.epi = epi;
+  b.bn = choose_bn(t256, t128, epi);
+  tp_status err = TP_OK;
+  const int am = b.add_map(x.ptr, T, K, x.ld, 128, &err);
+  if (am < 0) return err;
+  for (int32_t r = 0; r < nb; ++r) {
+    if (w[r].rows == 0) continue;
+    const int bm = b.add_map(w[r].ptr, w[r].rows, K, w[r].ld, b.bn, &err);
+    if (bm < 0) return err;
+    const long long ks = K;
+    if (!b.add_problem(static_cast<int>(T), static_cast<int>(w[r].rows), outs[r].ptr, outs[r].ld,
+                       &am, &bm, nullptr, &ks, 1))
+      return TP_ERR_UNSUPPORTED;
+  }
+  return b.launch(s);
+}
+
+// Row-parallel: fused = one problem whose segments are the ranks; else one problem per rank.
+tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
+                        bool fused, cudaStream_t s) {
+  const long long T = x[0].rows, nout = w[0].rows;
+  const long long mt = (T + 127) / 128;
+  const long long probs = fused ? 1 : n;
+  GemmBuilder b;
+  b.epi = kEpiF32;
+  b.bn = choose_bn(probs * mt * ((nout + 255) / 256), probs * mt * ((nout + 127) / 128), kEpiF32);
+  tp_status err = TP_OK;
+  std::vector<int> am(n), bm(n);
+  std::vector<long long> ks(n);
+  for (int32_t r = 0; r < n; ++r) {
+    am[r] = b.add_map(x[r].ptr, T, x[r].cols, x[r].ld, 128, &err);
+    if (am[r] < 0) return err;
+    bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, b.bn, &err);
+    if (bm[r] < 0) return err;
+    ks[r] = x[r].cols;
+  }
+  if (fused) {
+    if (!b.add_problem(static_cast<int>(T), static_cast<int>(nout), y[0].ptr, y[0].ld, am.data(),
+                       bm.data(), nullptr, ks.data(), n))
+      return TP_ERR_UNSUPPORTED;
+  } else {
+    for (int32_t r = 0; r < n; ++r)
+      if (!b.add_problem(static_cast<int>(T), static_cast<int>(nout), y[r].ptr, y[r].ld, &am[r],
+                         &bm[r], nullptr, &ks[r], 1))
+        return TP_ERR_UNSUPPORTED;
+  }
+  return b.launch(s);
+}
+
+tp_status gemm_f32_column(const tp_tensor &x, int32_t n, const tp_tensor *w, const ColOut *outs,
+                          cudaStream_t s) {
+  F32Params p;
+  std::memset(&p, 0, sizeof(p));
+  int np = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    if (w[r].rows == 0) continue;
+    if (np >= kMaxF32Problems) return TP_ERR_UNSUPPORTED;
+    F32Problem &pr = p.prob[np];
+    pr.m = static_cast<int>(x.rows);
+    pr.n = static_cast<int>(w[r].rows);
+    pr.m_tiles = (pr.m + 31) / 32;
+    pr.n_tiles = (pr.n + 63) / 64;
+    pr.tile_begin = p.total_tiles;
+    pr.seg_begin = np;
+    pr.seg_count = 1;
+    pr.out = static_cast<float *>(outs[r].ptr);
+    pr.ldc = outs[r].ld;
+    p.seg[np] = F32Seg{static_cast<const float *>(x.ptr), x.ld, static_cast<const float *>(w[r].ptr),
+                       w[r].ld, static_cast<int>(x.cols)};
+    p.total_tiles += pr.m_tiles * pr.n_tiles;
+    ++np;
+  }
+  p.num_problems = np;
+  return launch_gemm_f32(p, s);
+}
+
+tp_status gemm_f32_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
+                       bool fused, cudaStream_t s) {
+  F32Params p;
+  std::memset(&p, 0, sizeof(p));
+  const int T = static_cast<int>(x[0].rows), nout = static_cast<int>(w[0].rows);
+  const int probs = fused ? 1 : n;
+  for (int q = 0; q < probs; ++q) {
+    F32Problem &pr = p.prob[q];
+    pr.m = T;
+    pr.n = nout;
+    pr.m_tiles = (T + 31) / 32;
+    pr.n_tiles = (nout + 63) / 64;
+    pr.tile_begin = p.total_tiles;
+    pr.seg_begin = fused ? 0 : q;
+    pr.seg_count = fused ? n : 1;
+    pr.out = static_cast<float *>(y[q].ptr);
+    pr.ldc = y[q].ld;
+    p.total_tiles += pr.m_tiles * pr.n_tiles;
+  }
+  for (int32_t r = 0; r < n; ++r)
+    p.seg[r] = F32Seg{static_cast<const float *>(x[r].ptr), x[r].ld,
+                      static_cast<const float *>(w[r].ptr), w[r].ld, static_cast<int>(x[r].cols)};
+  p.num_problems = probs;
+  return launch_gemm_f32(p, s);
+}
+
+// Validates a row-parallel argument set; on success fills T, n.
+tp_status check_row_args(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
+                         int32_t combine, int32_t *in_dtype) {
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (!x || !w || !y) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  const int32_t dt = x[0].dtype;
+  const long long T = x[0].rows, nout = w[0].rows;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(x[r]) || !shape_ok(w[r])) return TP_ERR_INVALID_ARG;
+    if (x[r].dtype != dt || w[r].dtype != dt) return TP_ERR_DTYPE;
+    if (x[r].rows != T || w[r].rows != nout || w[r].cols != x[r].cols) return TP_ERR_INVALID_ARG;
+    if (dt == TP_BF16 && T > 0 && (!pitch_ok(x[r]) || !pitch_ok(w[r]))) return TP_ERR_ALIGNMENT;
+  }
+  const int32_t ny = combine == TP_COMBINE_FUSED ? 1 : n;
+  for (int32_t q = 0; q < ny; ++q) {
+    if (!shape_ok(y[q])) return TP_ERR_INVALID_ARG;
+    if (y[q].dtype != TP_F32) return TP_ERR_DTYPE;
+    if (y[q].rows != T || y[q].cols != nout) return TP_ERR_INVALID_ARG;
+    if (T > 0 && nout > 0 && !pitch_ok(y[q])) return TP_ERR_ALIGNMENT;
+  }
+  if (combine == TP_COMBINE_RING || combine == TP_COMBINE_RING_FUSED) {
+    const tp_status st = check_ring_bufs(n, y);
+    if (st != TP_OK) return st;
+  }
+  *in_dtype = dt;
+  return TP_OK;
+}
+
+tp_status row_linear_impl(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
+                          int32_t combine, int32_t dt, cudaStream_t s) {
+  const long long T = x[0].rows, nout = w[0].rows;
+  if (T == 0 || nout == 0) return TP_OK;
+  const bool fused = combine == TP_COMBINE_FUSED;
+  bool all_k_zero = true;
+  for (int32_t r = 0; r < n; ++r) all_k_zero = all_k_zero && x[r].cols == 0;
+  tp_status st = TP_OK;
+  if (all_k_zero) {
+    for (int32_t q = 0; q < (fused ? 1 : n) && st == TP_OK; ++q) st = zero_fill(y[q], 0, nout, s);
+    return st;
+  }
+  for (int32_t r = 0; r < n; ++r)
+    if (x[r].cols == 0) return TP_ERR_UNSUPPORTED;  // a rank with an empty K slice
+  if (dt == TP_BF16)
+    st = gemm_bf16_row(n, x, w, y, fused, s);
+  else
+    st = gemm_f32_row(n, x, w, y, fused, s);
+  if (st != TP_OK) return st;
+  if (combine == TP_COMBINE_RING) return run_allreduce(n, y, TP_RING_STEPS, s);
+  if (combine == TP_COMBINE_RING_FUSED) return run_allreduce(n, y, TP_RING_FUSED, s);
+  return TP_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Shared helpers declared in tp_internal.h
+// ---------------------------------------------------------------------------
+cudaError_t get_dev_ctx(DevCtx *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  if (!g_status_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dev_status);
+    if (e != cudaSuccess) return e;
+    g_status_addr[dev] = static_cast<int *>(p);
+  }
+  out->status = g_status_addr[dev];
+  out->wait_ns = g_wait_ns.load();
+  return cudaSuccess;
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  if (!g_sm_count[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1)
+      v = 148;
+    g_sm_count[dev] = v;
+  }
+  return g_sm_count[dev];
+}
+
+tp_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return TP_ERR_CUDA;
+}
+
+}  // namespace tpgqa
+
+using namespace tpgqa;
+
+// ---------------------------------------------------------------------------
+// Linear layers
+// ---------------------------------------------------------------------------
+extern "C" tp_status tp_column_linear(int32_t n, const tp_tensor *x, const tp_tensor *w,
+                                      tp_tensor *y, int32_t gather, tp_stream_t stream) {
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (!x || !w || !y || (gather != 0 && gather != 1)) return TP_ERR_INVALID_ARG;
+  if (!shape_ok(*x)) return TP_ERR_INVALID_ARG;
+  const int32_t dt = x->dtype;
+  const long long T = x->rows, K = x->cols;
+  long long total = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(w[r])) return TP_ERR_INVALID_ARG;
+    if (w[r].dtype != dt) return TP_ERR_DTYPE;
+    if (w[r].cols != K) return TP_ERR_INVALID_ARG;
+    total += w[r].rows;
+  }
+  const int32_t ny = gather ? 1 : n;
+  for (int32_t q = 0; q < ny; ++q) {
+    if (!shape_ok(y[q])) return TP_ERR_INVALID_ARG;
+    if (y[q].rows != T || y[q].cols != (gather ? total : w[q].rows)) return TP_ERR_INVALID_ARG;
+    if (dt == TP_F32 && y[q].dtype != TP_F32) return TP_ERR_DTYPE;
+  }
+  const int32_t ydt = y[0].dtype;
+  for (int32_t q = 1; q < ny; ++q)
+    if (y[q].dtype != ydt) return TP_ERR_DTYPE;
+  if (dt == TP_BF16 && T > 0 && K > 0) {
+    if (!pitch_ok(*x)) return TP_ERR_ALIGNMENT;
+    for (int32_t r = 0; r < n; ++r)
+      if (w[r].rows > 0 && !pitch_ok(w[r])) return TP_ERR_ALIGNMENT;
+  }
+  if (T > 0) {
+    for (int32_t q = 0; q < ny; ++q)
+      if (y[q].cols > 0 && !pitch_ok(y[q])) return TP_ERR_ALIGNMENT;
+    if (gather)
+      for (int32_t r = 0; r < n; ++r)
+        if ((w[r].rows * static_cast<long long>(esize(ydt))) % 16) return TP_ERR_ALIGNMENT;
+  }
+  tp_status st = check_health(n);
+  if (st != TP_OK) return st;
+  if (T == 0 || total == 0) return TP_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  std::vector<ColOut> outs(n);
+  long long off = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    if (gather)
+      outs[r] = ColOut{byte_ptr(y[0].ptr, off, ydt), y[0].ld};
+    else
+      outs[r] = ColOut{y[r].ptr, y[r].ld};
+    off += w[r].rows;
+  }
+  if (K == 0) {
+    off = 0;
+    for (int32_t r = 0; r < n && st == TP_OK; ++r) {
+      st = gather ? zero_fill(y[0], off, w[r].rows, s) : zero_fill(y[r], 0, w[r].rows, s);
+      off += w[r].rows;
+    }
+    return st;
+  }
+  if (dt == TP_F32) return gemm_f32_column(*x, n, w, outs.data(), s);
+  return gemm_bf16_column(*x, n, w, outs.data(), ydt == TP_F32 ? kEpiF32 : kEpiBF16, s);
+}
+
+extern "C" tp_status tp_row_linear(int32_t n, const tp_tensor *x, const tp_tensor *w, tp_tensor *y,
+                                   int32_t combine, tp_stream_t stream) {
+  int32_t dt = 0;
+  tp_status st = check_row_args(n, x, w, y, combine, &dt);
+  if (st != TP_OK) return st;
+  st = check_health(n);
+  if (st != TP_OK) return st;
+  return row_linear_impl(n, x, w, y, combine, dt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Collectives
+// ---------------------------------------------------------------------------
+extern "C" tp_status tp_reduce_scatter(int32_t n, tp_tensor *buf, int32_t mode, tp_stream_t stream) {
+  tp_status st = check_ring_bufs(n, buf);
+  if (st != TP_OK) return st;
+  if (mode != TP_RING_STEPS && mode != TP_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if ((st = check_health(n)) != TP_OK) return st;
+  return run_reduce_scatter(n, buf, mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_ring_all_gather(int32_t n, tp_tensor *buf, int32_t mode, tp_stream_t stream) {
+  tp_status st = check_ring_bufs(n, buf);
+  if (st != TP_OK) return st;
+  if (mode != TP_RING_STEPS && mode != TP_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if ((st = check_health(n)) != TP_OK) return st;
+  return run_all_gather_ring(n, buf, mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_allreduce_ring(int32_t n, tp_tensor *buf, int32_t mode, tp_stream_t stream) {
+  tp_status st = check_ring_bufs(n, buf);
+  if (st != TP_OK) return st;
+  if (mode != TP_RING_STEPS && mode != TP_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if ((st = check_health(n)) != TP_OK) return st;
+  return run_allreduce(n, buf, mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_all_gather(int32_t n, const tp_tensor *shard, tp_tensor *out, int32_t n_out,
+                                   int32_t axis, tp_stream_t stream) {
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (!shard || !out || (n_out != 1 && n_out != n) || (axis != 0 && axis != 1))
+    return TP_ERR_INVALID_ARG;
+  const int32_t dt = shard[0].dtype;
+  long long sum = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(shard[r])) return TP_ERR_INVALID_ARG;
+    if (shard[r].dtype != dt) return TP_ERR_DTYPE;
+    if (axis == 1 && shard[r].rows != shard[0].rows) return TP_ERR_INVALID_ARG;
+    if (axis == 0 && shard[r].cols != shard[0].cols) return TP_ERR_INVALID_ARG;
+    sum += axis == 1 ? shard[r].cols : shard[r].rows;
+  }
+  const long long orows = axis == 1 ? shard[0].rows : sum;
+  const long long ocols = axis == 1 ? sum : shard[0].cols;
+  for (int32_t o = 0; o < n_out; ++o) {
+    if (!shape_ok(out[o])) return TP_ERR_INVALID_ARG;
+    if (out[o].dtype != dt) return TP_ERR_DTYPE;
+    if (out[o].rows != orows || out[o].cols != ocols) return TP_ERR_INVALID_ARG;
+  }
+  tp_status st = check_health(n);
+  if (st != TP_OK) return st;
+  const long long es = static_cast<long long>(esize(dt));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  CopyBatch b;
+  std::memset(&b, 0, sizeof(b));
+  for (int32_t o = 0; o < n_out; ++o) {
+    long long off = 0;
+    for (int32_t r = 0; r < n; ++r) {
+      const tp_tensor &sh = shard[r];
+      Copy2D c;
+      c.src = static_cast<const char *>(sh.ptr);
+      c.src_pitch = sh.ld * es;
+      c.dst_pitch = out[o].ld * es;
+      c.rows = sh.rows;
+      c.row_bytes = sh.cols * es;
+      c.dst = axis == 1 ? byte_ptr(out[o].ptr, off, dt) : byte_ptr(out[o].ptr, off * out[o].ld, dt);
+      off += axis == 1 ? sh.cols : sh.rows;
+      if (c.rows == 0 || c.row_bytes == 0) continue;
+      b.c[b.n++] = c;
+      if (b.n == kMaxCopies) {
+        if ((st = launch_copy_batch(b, s)) != TP_OK) return st;
+        b.n = 0;
+      }
+    }
+  }
+  return launch_copy_batch(b, s);
+}
+
+// ---------------------------------------------------------------------------
+// Blocks
+// ---------------------------------------------------------------------------
+extern "C" size_t tp_mlp_block_workspace_size(const tp_plan *plan, int64_t tokens) {
+  tp_dims d;
+  if (tp_plan_dims(plan, &d) != TP_OK || tokens < 0) return 0;
+  return static_cast<size_t>(tokens) * static_cast<size_t>(d.ffn) * 2;
+}
+
+extern "C" tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_gate,
+                                  const tp_tensor *w_up, const tp_tensor *w_down, tp_tensor *y,
+                                  int32_t combine, void *workspace, size_t workspace_bytes,
+                                  tp_stream_t stream) {
+  tp_dims d;
+  if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
+  if (!x || !w_gate || !w_up || !w_down || !y) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  const int32_t n = d.tp_size;
+  const long long D = d.hidden, Fr = d.ffn / n, T = x->rows;
+  if (!shape_ok(*x) || x->cols != D) return TP_ERR_INVALID_ARG;
+  if (x->dtype != TP_BF16) return TP_ERR_DTYPE;
+  for (int32_t r = 0; r < n; ++r) {
+    const tp_tensor *ws[3] = {&w_gate[r], &w_up[r], &w_down[r]};
+    for (const tp_tensor *t : ws) {
+      if (!shape_ok(*t)) return TP_ERR_INVALID_ARG;
+      if (t->dtype != TP_BF16) return TP_ERR_DTYPE;
+      if (!pitch_ok(*t)) return TP_ERR_ALIGNMENT;
+    }
+    if (w_gate[r].rows != Fr || w_gate[r].cols != D || w_up[r].rows != Fr || w_up[r].cols != D ||
+        w_down[r].rows != D || w_down[r].cols != Fr)
+      return TP_ERR_INVALID_ARG;
+  }
+  // H_r is rank r's column block of one [T x F] bf16 buffer in the workspace.
+  if ((Fr * 2) % 16) return TP_ERR_ALIGNMENT;
+  std::vector<tp_tensor> h(n);
+  for (int32_t r = 0; r < n; ++r)
+    h[r] = tp_tensor{byte_ptr(workspace, r * Fr, TP_BF16), TP_BF16, 0, T, Fr, static_cast<int64_t>(d.ffn)};
+  int32_t dt = 0;
+  if (T > 0) {
+    if (!pitch_ok(*x)) return TP_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < tp_mlp_block_workspace_size(plan, T)) return TP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TP_ERR_ALIGNMENT;
+  } else {
+    for (int32_t r = 0; r < n; ++r) h[r].ptr = nullptr, h[r].rows = 0;
+  }
+  tp_status st = check_row_args(n, h.data(), w_down, y, combine, &dt);
+  if (st != TP_OK) return st;
+  if ((st = check_health(n)) != TP_OK) return st;
+  if (T == 0) return TP_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // gate/up column-parallel GEMM with SwiGLU in the epilogue: H_r = silu(X G_r^T) * (X U_r^T).
+  {
+    GemmBuilder b;
+    b.epi = kEpiSwiGLU;
+    const long long mt = (T + 127) / 128;
+    b.bn = choose_bn(n * mt * ((Fr + 127) / 128), n * mt * ((Fr + 63) / 64), kEpiSwiGLU);
+    tp_status err = TP_OK;
+    const int am = b.add_map(x->ptr, T, D, x->ld, 128, &err);
+    if (am < 0) return err;
+    for (int32_t r = 0; r < n; ++r) {
+      const int gm = b.add_map(w_gate[r].ptr, Fr, D, w_gate[r].ld, b.bn / 2, &err);
+      if (gm < 0) return err;
+      const int um = b.add_map(w_up[r].ptr, Fr, D, w_up[r].ld, b.bn / 2, &err);
+      if (um < 0) return err;
+      const long long ks = D;
+      if (!b.add_problem(static_cast<int>(T), static_cast<int>(Fr), h[r].ptr, h[r].ld, &am, &gm,
+                         &um, &ks, 1))
+        return TP_ERR_UNSUPPORTED;
+    }
+    if ((st = b.launch(s)) != TP_OK) return st;
+  }
+  // down row-parallel GEMM + combine.
+  return row_linear_impl(n, h.data(), w_down, y, combine, TP_BF16, s);
+}
+
+extern "C" tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_q,
+                                  const tp_tensor *w_k, const tp_tensor *w_v, tp_tensor *q,
+                                  tp_tensor *k, tp_tensor *v, const tp_tensor *a,
+                                  const tp_tensor *w_o, tp_tensor *y, int32_t combine,
+                                  tp_stream_t stream) {
+  tp_dims d;
+  if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
+  if (!x || !w_q || !w_k || !w_v || !q || !k || !v || !a || !w_o || !y) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  const int32_t n = d.tp_size;
+  const long long D = d.hidden, hd = d.head_dim, T = x->rows;
+  if (!shape_ok(*x) || x->cols != D) return TP_ERR_INVALID_ARG;
+  if (x->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (T > 0 && !pitch_ok(*x)) return TP_ERR_ALIGNMENT;
+  tp_rank_shard s0;
+  tp_plan_query_rank(plan, 0, &s0);
+  const bool rep = s0.kv_replicated != 0;
+  const int32_t nkv = rep ? 1 : n;
+  const long long qcols = (s0.q_head_end - s0.q_head_begin) * hd;
+  const long long kvcols = (s0.kv_head_end - s0.kv_head_begin) * hd;
+  auto check_w = [&](const tp_tensor &t, long long rows, long long cols) -> tp_status {
+    if (!shape_ok(t)) return TP_ERR_INVALID_ARG;
+    if (t.dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (t.rows != rows || t.cols != cols) return TP_ERR_INVALID_ARG;
+    if (!pitch_ok(t)) return TP_ERR_ALIGNMENT;
+    return TP_OK;
+  };
+  auto check_out = [&](const tp_tensor &t, long long cols) -> tp_status {
+    if (!shape_ok(t)) return TP_ERR_INVALID_ARG;
+    if (t.dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (t.rows != T || t.cols != cols) return TP_ERR_INVALID_ARG;
+    if (T > 0 && !pitch_ok(t)) return TP_ERR_ALIGNMENT;
+    return TP_OK;
+  };
+  tp_status st;
+  for (int32_t r = 0; r < n; ++r) {
+    if ((st = check_w(w_q[r], qcols, D)) != TP_OK) return st;
+    if ((st = check_out(q[r], qcols)) != TP_OK) return st;
+    if ((st = check_w(w_o[r], D, qcols)) != TP_OK) return st;
+  }
+  for (int32_t r = 0; r < nkv; ++r) {
+    if ((st = check_w(w_k[r], kvcols, D)) != TP_OK) return st;
+    if ((st = check_w(w_v[r], kvcols, D)) != TP_OK) return st;
+    if ((st = check_out(k[r], kvcols)) != TP_OK) return st;
+    if ((st = check_out(v[r], kvcols)) != TP_OK) return st;
+  }
+  int32_t dt = 0;
+  if ((st = check_row_args(n, a, w_o, y, combine, &dt)) != TP_OK) return st;
+  if (dt != TP_BF16) return TP_ERR_DTYPE;
+  if (a[0].rows != T) return TP_ERR_INVALID_ARG;
+  if ((st = check_health(n)) != TP_OK) return st;
+  if (T == 0) return TP_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // q/k/v column-parallel as one grouped launch (K/V once when replicated).
+  {
+    std::vector<tp_tensor> ws;
+    std::vector<ColOut> outs;
+    for (int32_t r = 0; r < n; ++r) {
+      ws.push_back(w_q[r]);
+      outs.push_back(ColOut{q[r].ptr, q[r].ld});
+    }
+    for (int32_t r = 0; r < nkv; ++r) {
+      ws.push_back(w_k[r]);
+      outs.push_back(ColOut{k[r].ptr, k[r].ld});
+      ws.push_back(w_v[r]);
+      outs.push_back(ColOut{v[r].ptr, v[r].ld});
+    }
+    st = gemm_bf16_column(*x, static_cast<int32_t>(ws.size()), ws.data(), outs.data(), kEpiBF16, s);
+    if (st != TP_OK) return st;
+  }
+  // o_proj row-parallel + combine.
+  return row_linear_impl(n, a, w_o, y, combine, TP_BF16, s);
+}
+
+// ---------------------------------------------------------------------------
+// Status, health, diagnostics
+// ---------------------------------------------------------------------------
+extern "C" const char *tp_status_str(tp_status s) {
+  switch (s) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_INVALID_ARG: return "TP_ERR_INVALID_ARG";
+    case TP_ERR_TP_SIZE_NOT_POW2: return "TP_ERR_TP_SIZE_NOT_POW2";
+    case TP_ERR_NOT_DIVISIBLE: return "TP_ERR_NOT_DIVISIBLE";
+    case TP_ERR_GQA_SHAPE: return "TP_ERR_GQA_SHAPE";
+    case TP_ERR_DTYPE: return "TP_ERR_DTYPE";
+    case TP_ERR_ALIGNMENT: return "TP_ERR_ALIGNMENT";
+    case TP_ERR_RANK_FAILED: return "TP_ERR_RANK_FAILED";
+    case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA";
+    case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
+  }
+  return "TP_ERR_UNKNOWN";
+}
+
+extern "C" int32_t tp_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" tp_status tp_set_rank_health(int32_t rank, int32_t healthy) {
+  if (rank < 0 || rank >= 64) return TP_ERR_INVALID_ARG;
+  const unsigned long long bit = 1ULL << rank;
+  if (healthy)
+    g_failed_ranks.fetch_and(~bit);
+  else
+    g_failed_ranks.fetch_or(bit);
+  return TP_OK;
+}
+
+extern "C" tp_status tp_device_status(tp_stream_t stream, int32_t *detail) {
+  if (detail) *detail = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_dev_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (detail) *detail = word;
+  return word == 0 ? TP_OK : TP_ERR_TIMEOUT;
+}
+
+extern "C" tp_status tp_set_wait_budget(int64_t nanoseconds) {
+  if (nanoseconds < 0) return TP_ERR_INVALID_ARG;
+  g_wait_ns.store(nanoseconds == 0 ? kDefaultWaitNs : nanoseconds);
+  return TP_OK;
+}
+
+extern "C" tp_status tp_debug_wait_timeout(tp_stream_t stream) {
+  return launch_debug_wait(reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" const char *tp_version(void) { return "tpgqa 0.1 (sm_103a)"; }

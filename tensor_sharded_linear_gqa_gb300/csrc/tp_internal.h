@@ -1,0 +1,159 @@
+// Internal declarations shared by the library's translation units (not part of
+// the public ABI). Kernels of different translation units reach the device
+// status word through a pointer argument, so no relocatable device code is
+// needed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tpgqa.h"
+
+namespace tpgqa {
+
+// ---------------------------------------------------------------------------
+// Device status word and bounded waits
+// ---------------------------------------------------------------------------
+// Codes written to the device status word (first writer wins).
+enum : int {
+  kDevOk = 0,
+  kDevTimeoutProducer = 0x101,  // TMA producer gave up waiting for a free stage
+  kDevTimeoutMma = 0x102,       // MMA issuer gave up waiting for a full stage
+  kDevTimeoutEpilogue = 0x103,  // epilogue gave up waiting for the accumulator
+  kDevTimeoutDrain = 0x104,     // teardown gave up waiting for in-flight copies
+  kDevTimeoutDebug = 0x1FF,     // tp_debug_wait_timeout's wait
+};
+
+struct DevCtx {
+  int *status;           // device status word
+  long long wait_ns;     // budget of every bounded wait, nanoseconds
+};
+
+// Returns the context for kernels launched now (status word address is
+// resolved once per device). Returns cudaSuccess or the failing error.
+cudaError_t get_dev_ctx(DevCtx *out);
+
+int num_sms();
+
+// Records a failed CUDA call for tp_last_cuda_error() and returns TP_ERR_CUDA.
+tp_status cuda_fail(cudaError_t e);
+
+// ---------------------------------------------------------------------------
+// bf16 tensor-core grouped GEMM (tcgen05 + TMA), C = A * B^T, both K-major.
+// ---------------------------------------------------------------------------
+constexpr int kMaxMaps = 48;
+constexpr int kMaxProblems = 40;
+constexpr int kMaxSegs = 48;
+
+enum Epilogue : int {
+  kEpiF32 = 0,     // store fp32 accumulators
+  kEpiBF16 = 1,    // store bf16 (round to nearest even)
+  kEpiSwiGLU = 2,  // B tile = [gate rows ; up rows]; store bf16 silu(g) * u
+};
+
+// One K segment of a problem: the accumulator runs over every segment of its
+// problem in order (a row-parallel fused sum runs one segment per rank).
+struct GemmSeg {
+  int a_map;    // tensor map of A (rows = output rows)
+  int b_map;    // tensor map of B (rows = output cols; gate rows for SwiGLU)
+  int b2_map;   // up rows for SwiGLU, else -1
+  int k_tiles;  // ceil(K / 64)
+};
+
+struct GemmProblem {
+  int m, n;              // output rows / cols of this problem (n counts outputs)
+  int m_tiles, n_tiles;
+  int tile_begin;        // first linear tile id of this problem
+  int seg_begin, seg_count;
+  int pad;
+  void *out;             // output base (row-major)
+  long long ldc;         // elements
+};
+
+struct GemmParams {
+  CUtensorMap maps[kMaxMaps];
+  GemmProblem prob[kMaxProblems];
+  GemmSeg seg[kMaxSegs];
+  int num_problems;
+  int total_tiles;
+  int *status;
+  long long wait_ns;
+};
+
+// Host-side builder of a GemmParams.
+struct GemmBuilder {
+  GemmParams p;
+  int n_maps = 0, n_probs = 0, n_segs = 0;
+  int bn = 256;       // CTA tile width in accumulator columns (128 or 256)
+  int epi = kEpiF32;
+  GemmBuilder();
+  // Tensor map of a bf16 [rows x k] matrix with row pitch ld (elements), boxes
+  // of 64 x box_rows, 128-byte swizzle. Returns the map index or -1.
+  int add_map(const void *base, long long rows, long long k, long long ld, int box_rows,
+              tp_status *err);
+  // Adds a problem with segments [(a_map, b_map, b2_map, k)...]; returns false
+  // if the tables are full.
+  bool add_problem(int m, int n, void *out, long long ldc, const int *a_maps, const int *b_maps,
+                   const int *b2_maps, const long long *ks, int nseg);
+  tp_status launch(cudaStream_t stream);
+};
+
+// Picks the tile width for a set of problems with these output shapes.
+int choose_bn(long long total_tiles_256, long long total_tiles_128, int epi);
+
+// ---------------------------------------------------------------------------
+// Exact fp32 SIMT grouped GEMM, C = A * B^T with per-problem K segments.
+// ---------------------------------------------------------------------------
+constexpr int kMaxF32Problems = 16;
+constexpr int kMaxF32Segs = 32;
+
+struct F32Seg {
+  const float *a; long long lda;
+  const float *b; long long ldb;
+  int k;
+};
+struct F32Problem {
+  int m, n, m_tiles, n_tiles, tile_begin, seg_begin, seg_count;
+  float *out; long long ldc;
+};
+struct F32Params {
+  F32Problem prob[kMaxF32Problems];
+  F32Seg seg[kMaxF32Segs];
+  int num_problems, total_tiles;
+};
+tp_status launch_gemm_f32(const F32Params &p, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Collectives on shard buffers of one device.
+// ---------------------------------------------------------------------------
+constexpr int kMaxRanks = 64;
+struct RankPtrs {
+  float *p[kMaxRanks];
+};
+// One reduce-scatter / all-gather ring step over every rank.
+tp_status launch_ring_rs_step(const RankPtrs &b, int n, long long size, int step, cudaStream_t s);
+tp_status launch_ring_ag_step(const RankPtrs &b, int n, long long size, int step, cudaStream_t s);
+// One pass that folds each chunk in the ring's order; write_all = 1 gives the
+// all-reduce, 0 the reduce-scatter (only chunk c of buffer c is written).
+tp_status launch_ring_fused(const RankPtrs &b, int n, long long size, int write_all, cudaStream_t s);
+// In-place all-gather in one pass: chunk c of buffer c is copied to every other buffer.
+tp_status launch_ring_ag_fused(const RankPtrs &b, int n, long long size, cudaStream_t s);
+
+// Strided 2-D copy of a shard into an output (all-gather as concatenation).
+struct Copy2D {
+  const char *src; long long src_pitch;   // bytes
+  char *dst; long long dst_pitch;         // bytes
+  long long rows, row_bytes;
+};
+constexpr int kMaxCopies = 128;
+struct CopyBatch {
+  Copy2D c[kMaxCopies];
+  int n;
+};
+tp_status launch_copy_batch(const CopyBatch &b, cudaStream_t s);
+
+// Kernel that always times out its bounded wait (tests of the timeout path).
+tp_status launch_debug_wait(cudaStream_t s);
+
+}  // namespace tpgqa

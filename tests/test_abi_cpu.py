@@ -1,0 +1,211 @@
+"""CPU tests of the C ABI: the library loads, exports every declared symbol, its
+plan is bit-exact against the oracle's, and argument / health checks return
+their status before any CUDA call (so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+import tensor_sharded_linear_gqa_gb300 as tp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tpgqa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(tp_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("tp_plan_create", "tp_column_linear", "tp_row_linear", "tp_reduce_scatter",
+                     "tp_all_gather", "tp_allreduce_ring", "tp_mlp_block", "tp_attn_proj"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = tp.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in tp.EXPORTED, name
+
+
+def test_status_strings():
+    for i, name in enumerate(tp.STATUS_NAMES):
+        assert tp.tp_status_str(i) == name
+    assert tp.tp_version().startswith("tpgqa")
+
+
+STRAT = {O.COLUMN: tp.TP_SHARD_COLUMN, O.ROW: tp.TP_SHARD_ROW, O.VOCAB: tp.TP_SHARD_VOCAB,
+         O.REPLICATED: tp.TP_SHARD_REPLICATED}
+COMM = {O.NO_COMM: tp.TP_COMM_NONE, O.ALL_REDUCE: tp.TP_COMM_ALL_REDUCE,
+        O.ALL_GATHER: tp.TP_COMM_ALL_GATHER, O.REDUCE_SCATTER: tp.TP_COMM_REDUCE_SCATTER}
+
+PLAN_CASES = [(tp_, hkv * g, hkv, hd, ffn)
+              for tp_ in (1, 2, 4, 8, 16) for hkv in (1, 2, 3, 4, 8, 16) for g in (1, 2, 4)
+              for hd, ffn in ((64, 256), (128, 14336))
+              if (hkv * g) % tp_ == 0 and (hkv < tp_ or hkv % tp_ == 0) and ffn % tp_ == 0]
+PLAN_CASES += [(4, 32, 8, 128, 14336), (8, 32, 4, 128, 14336), (8, 64, 8, 128, 28672),
+               (2, 16, 8, 128, 8192)]
+
+
+@pytest.mark.parametrize("tp_size,hq,hkv,hd,ffn", PLAN_CASES)
+def test_plan_bit_exact_vs_oracle(tp_size, hq, hkv, hd, ffn):
+    hidden = 512
+    ref = O.shard_plan(tp_size, hidden, hq, hkv, hd, ffn)
+    plan = tp.tp_plan_create(tp_size, hidden, hq, hkv, hd, ffn)
+    for s in ref:
+        got = tp.tp_plan_query_rank(plan, s.rank)
+        assert got["q_heads"] == s.q_heads
+        assert got["kv_heads"] == s.kv_heads
+        assert got["kv_replicated"] == s.kv_replicated
+        for w in O.WEIGHTS:
+            assert got["strategy"][w] == STRAT[s.strategy[w]], w
+            assert got["comm"][w] == COMM[s.comm[w]], w
+            assert got["ranges"][w] == tuple(s.ranges[w]), w
+        assert tp.tp_plan_q_to_kv(plan, s.rank) == list(s.q_to_kv)
+
+
+ERR = {"tp_size_not_pow2": tp.TP_ERR_TP_SIZE_NOT_POW2, "gqa_shape": tp.TP_ERR_GQA_SHAPE,
+       "not_divisible": tp.TP_ERR_NOT_DIVISIBLE, "invalid": tp.TP_ERR_INVALID_ARG}
+
+
+@pytest.mark.parametrize("args", [(3, 64, 32, 8, 128, 1024), (0, 64, 32, 8, 128, 1024),
+                                  (8, 64, 48, 12, 128, 1024), (4, 64, 30, 6, 128, 1024),
+                                  (2, 64, 12, 5, 128, 1024), (4, 64, 8, 4, 8, 30),
+                                  (4, 0, 8, 4, 8, 32), (4, 64, 8, 4, 0, 32)])
+def test_plan_errors_match_oracle(args):
+    with pytest.raises(O.PlanError) as e:
+        O.shard_plan(*args)
+    with pytest.raises(tp.TPError) as g:
+        tp.tp_plan_create(*args)
+    assert g.value.status == ERR[e.value.kind]
+
+
+def test_query_rank_out_of_range():
+    plan = tp.tp_plan_create(4, 64, 8, 4, 8, 32)
+    s = tp.TpRankShard()
+    assert tp.raw_status("tp_plan_query_rank", plan.handle, 4, ctypes.byref(s)) == tp.TP_ERR_INVALID_ARG
+    assert tp.raw_status("tp_plan_query_rank", plan.handle, -1, ctypes.byref(s)) == tp.TP_ERR_INVALID_ARG
+    small = (ctypes.c_int32 * 1)()
+    assert tp.raw_status("tp_plan_q_to_kv", plan.handle, 0, small, 1) == tp.TP_ERR_INVALID_ARG
+
+
+def test_workspace_size():
+    plan = tp.tp_plan_create(2, 2048, 16, 8, 128, 8192)
+    assert tp.tp_mlp_block_workspace_size(plan, 512) == 512 * 8192 * 2
+    assert tp.tp_mlp_block_workspace_size(plan, 0) == 0
+
+
+# ---- argument checks that return before any CUDA call -------------------------
+FAKE = 1 << 40  # never dereferenced: every case below fails validation first
+
+
+def T(ptr, dtype, rows, cols, ld=None):
+    return tp.TpTensor(ptr, dtype, 0, rows, cols, ld if ld is not None else cols)
+
+
+def arr(*ts):
+    a = (tp.TpTensor * len(ts))()
+    for i, t in enumerate(ts):
+        a[i] = t
+    return a
+
+
+BF, F32 = tp.TP_BF16, tp.TP_F32
+
+
+def col_status(n, x, ws, ys, gather=1):
+    return tp.raw_status("tp_column_linear", n, ctypes.byref(x), arr(*ws), arr(*ys), gather, None)
+
+
+def test_column_linear_rejects_bad_arguments():
+    x = T(FAKE, BF, 64, 128)
+    w = [T(FAKE, BF, 32, 128), T(FAKE, BF, 32, 128)]
+    y = [T(FAKE, BF, 64, 64)]
+    assert col_status(3, x, w + [w[0]], y) == tp.TP_ERR_TP_SIZE_NOT_POW2
+    assert col_status(2, x, [w[0], T(FAKE, BF, 32, 100)], y) == tp.TP_ERR_INVALID_ARG
+    assert col_status(2, x, [w[0], T(FAKE, F32, 32, 128)], y) == tp.TP_ERR_DTYPE
+    assert col_status(2, x, w, [T(FAKE, BF, 64, 65)]) == tp.TP_ERR_INVALID_ARG
+    assert col_status(2, T(FAKE + 2, BF, 64, 128), w, y) == tp.TP_ERR_ALIGNMENT
+    assert col_status(2, T(FAKE, BF, 64, 100, 100), [T(FAKE, BF, 32, 100)] * 2, y) == \
+        tp.TP_ERR_ALIGNMENT  # row pitch of 200 bytes
+    assert col_status(2, T(None, BF, 64, 128), w, y) == tp.TP_ERR_INVALID_ARG
+    assert col_status(2, x, w, y, gather=2) == tp.TP_ERR_INVALID_ARG
+
+
+def test_row_linear_rejects_bad_arguments():
+    xs = [T(FAKE, BF, 64, 64), T(FAKE, BF, 64, 64)]
+    ws = [T(FAKE, BF, 128, 64), T(FAKE, BF, 128, 64)]
+    ys = [T(FAKE, F32, 64, 128), T(FAKE + 4096, F32, 64, 128)]
+
+    def st(xs_, ws_, ys_, combine):
+        return tp.raw_status("tp_row_linear", 2, arr(*xs_), arr(*ws_), arr(*ys_), combine, None)
+    assert st(xs, ws, ys, 7) == tp.TP_ERR_INVALID_ARG
+    assert st(xs, ws, [T(FAKE, BF, 64, 128)] * 2, tp.TP_COMBINE_NONE) == tp.TP_ERR_DTYPE
+    assert st(xs, [ws[0], T(FAKE, BF, 128, 32)], ys, tp.TP_COMBINE_NONE) == tp.TP_ERR_INVALID_ARG
+    # ring combine needs distinct, contiguous buffers
+    assert st(xs, ws, [ys[0], ys[0]], tp.TP_COMBINE_RING) == tp.TP_ERR_INVALID_ARG
+    assert st(xs, ws, [T(FAKE, F32, 64, 128, 256), ys[1]], tp.TP_COMBINE_RING) == tp.TP_ERR_INVALID_ARG
+
+
+def test_collectives_reject_bad_arguments():
+    good = [T(FAKE, F32, 8, 8), T(FAKE + 1024, F32, 8, 8)]
+
+    def st(fn, bufs, mode=0, n=2):
+        return tp.raw_status(fn, n, arr(*bufs), mode, None)
+    for fn in ("tp_reduce_scatter", "tp_ring_all_gather", "tp_allreduce_ring"):
+        assert st(fn, good, mode=5) == tp.TP_ERR_INVALID_ARG
+        assert st(fn, [good[0], T(FAKE + 1024, BF, 8, 8)]) == tp.TP_ERR_DTYPE
+        assert st(fn, [good[0], T(FAKE + 1028, F32, 8, 8)]) == tp.TP_ERR_ALIGNMENT
+        assert st(fn, [good[0], T(FAKE + 1024, F32, 8, 9)]) == tp.TP_ERR_INVALID_ARG
+        assert st(fn, good + [good[0]], n=3) == tp.TP_ERR_TP_SIZE_NOT_POW2
+
+
+def test_all_gather_rejects_bad_arguments():
+    sh = [T(FAKE, F32, 8, 4), T(FAKE + 512, F32, 8, 4)]
+    out = [T(FAKE + 4096, F32, 8, 8)]
+
+    def st(shards, outs, axis, n_out=None):
+        return tp.raw_status("tp_all_gather", 2, arr(*shards), arr(*outs),
+                             n_out if n_out is not None else len(outs), axis, None)
+    assert st(sh, out, 2) == tp.TP_ERR_INVALID_ARG
+    assert st(sh, out, 0) == tp.TP_ERR_INVALID_ARG          # rows would be 16
+    assert st(sh, [T(FAKE + 4096, BF, 8, 8)], 1) == tp.TP_ERR_DTYPE
+    assert st(sh, out * 3, 1, 3) == tp.TP_ERR_INVALID_ARG    # n_out must be 1 or tp_size
+
+
+def test_failed_rank_stops_the_group_before_any_launch():
+    # Host-side fault injection: rank 1 reports unhealthy; every call that involves
+    # it returns TP_ERR_RANK_FAILED before enqueuing work (no GPU needed).
+    x = T(FAKE, BF, 64, 128)
+    w = [T(FAKE, BF, 32, 128), T(FAKE, BF, 32, 128)]
+    y = [T(FAKE, BF, 64, 64)]
+    bufs = [T(FAKE, F32, 8, 8), T(FAKE + 1024, F32, 8, 8)]
+    tp.tp_set_rank_health(1, False)
+    try:
+        assert col_status(2, x, w, y) == tp.TP_ERR_RANK_FAILED
+        assert tp.raw_status("tp_allreduce_ring", 2, arr(*bufs), 0, None) == tp.TP_ERR_RANK_FAILED
+        # a single-rank call does not involve rank 1
+        assert tp.raw_status("tp_allreduce_ring", 1, arr(bufs[0]), 0, None) == tp.TP_OK
+    finally:
+        tp.tp_set_rank_health(1, True)
+    assert tp.raw_status("tp_set_rank_health", 64, 0) == tp.TP_ERR_INVALID_ARG
+
+
+def test_empty_inputs_enqueue_nothing():
+    # zero tokens: valid, returns TP_OK without touching CUDA
+    x = T(None, BF, 0, 128)
+    w = [T(FAKE, BF, 32, 128), T(FAKE, BF, 32, 128)]
+    y = [T(None, BF, 0, 64)]
+    assert col_status(2, x, w, y) == tp.TP_OK
+    empty = [T(None, F32, 0, 0, 1), T(None, F32, 0, 0, 1)]
+    assert tp.raw_status("tp_allreduce_ring", 2, arr(*empty), 0, None) == tp.TP_OK
+
+
+def test_wait_budget_argument():
+    assert tp.raw_status("tp_set_wait_budget", -1) == tp.TP_ERR_INVALID_ARG
+    assert tp.raw_status("tp_set_wait_budget", 0) == tp.TP_OK

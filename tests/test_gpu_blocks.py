@@ -1,0 +1,179 @@
+"""GPU parity of the MLP and attention-projection blocks at the workload sizes,
+against the fp64 oracle (bf16 inputs: max|Y_gpu - Y_ref| <= 1e-2 * max|Y_ref|).
+
+The prefill layer is checked on a seeded sample of 64 token rows: every output
+row depends only on its own input row, so the oracle evaluates just those rows.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import tensor_sharded_linear_gqa_gb300 as tp
+from tensor_sharded_linear_gqa_gb300 import inputs
+from gpu_util import BF16_TOL, assert_close, dev_bf16, host_bits_f32, host_f64, need_gpu
+
+pytestmark = pytest.mark.gpu
+COMBINES = [tp.TP_COMBINE_FUSED, tp.TP_COMBINE_RING, tp.TP_COMBINE_RING_FUSED]
+
+
+def torch():
+    import torch as t
+    return t
+
+
+class Layer:
+    """Device copies of a workload's bf16 inputs, sharded per the library's plan."""
+
+    def __init__(self, w, data):
+        t = torch()
+        self.w, self.n, self.T = w, w["tp"], w["T"]
+        self.plan = tp.tp_plan_create(w["tp"], w["hidden"], w.get("q_heads", 8), w.get("kv_heads", 8),
+                                      w.get("head_dim", 128), w.get("ffn", 8 * w["tp"]))
+        self.shards = [tp.tp_plan_query_rank(self.plan, r) for r in range(self.n)]
+        self.x = dev_bf16(data["x"])
+        self.dev = {}
+        for name in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "a"):
+            if name in data:
+                self.dev[name] = dev_bf16(data[name])
+        self.t = t
+
+    def rng(self, r, wname):
+        return self.shards[r]["ranges"][wname]
+
+    def mlp(self, combine):
+        t, n, T = self.t, self.n, self.T
+        D = self.w["hidden"]
+        g = [self.dev["wg"][slice(*self.rng(r, "gate_proj"))] for r in range(n)]
+        u = [self.dev["wu"][slice(*self.rng(r, "up_proj"))] for r in range(n)]
+        d = [self.dev["wd"][:, slice(*self.rng(r, "down_proj"))] for r in range(n)]
+        ys = [t.full((T, D), float("nan"), device="cuda")
+              for _ in range(1 if combine == tp.TP_COMBINE_FUSED else n)]
+        ws = t.empty(tp.tp_mlp_block_workspace_size(self.plan, T), dtype=t.uint8, device="cuda")
+        tp.tp_mlp_block(self.plan, self.x, g, u, d, ys, combine, ws)
+        h = ws.view(t.bfloat16).view(T, self.w["ffn"])
+        return ys, h
+
+    def attn(self, combine):
+        t, n, T = self.t, self.n, self.T
+        D = self.w["hidden"]
+        rep = self.shards[0]["kv_replicated"]
+        wq = [self.dev["wq"][slice(*self.rng(r, "q_proj"))] for r in range(n)]
+        kv_ranks = 1 if rep else n
+        wk = [self.dev["wk"][slice(*self.rng(r, "k_proj"))] for r in range(kv_ranks)]
+        wv = [self.dev["wv"][slice(*self.rng(r, "v_proj"))] for r in range(kv_ranks)]
+        a = [self.dev["a"][:, slice(*self.rng(r, "o_proj"))] for r in range(n)]
+        wo = [self.dev["wo"][:, slice(*self.rng(r, "o_proj"))] for r in range(n)]
+        q = [t.empty((T, x.shape[0]), dtype=t.bfloat16, device="cuda") for x in wq]
+        k = [t.empty((T, x.shape[0]), dtype=t.bfloat16, device="cuda") for x in wk]
+        v = [t.empty((T, x.shape[0]), dtype=t.bfloat16, device="cuda") for x in wv]
+        ys = [t.full((T, D), float("nan"), device="cuda")
+              for _ in range(1 if combine == tp.TP_COMBINE_FUSED else n)]
+        tp.tp_attn_proj(self.plan, self.x, wq, wk, wv, q, k, v, a, wo, ys, combine)
+        return q, k, v, ys
+
+
+_cache = {}
+
+
+def layer(name):
+    if name not in _cache:
+        w = inputs.WORKLOADS[name]
+        data = inputs.make_bf16_inputs(w)
+        _cache.clear()
+        _cache[name] = (Layer(w, data), {k: inputs.bf16_bits_to_f64(v) for k, v in data.items()})
+    return _cache[name]
+
+
+def _oracle_plan(w):
+    return O.shard_plan(w["tp"], w["hidden"], w["q_heads"], w["kv_heads"], w["head_dim"],
+                        w.get("ffn", 8 * w["tp"]))
+
+
+# ---- MLP block ------------------------------------------------------------------------
+@pytest.mark.parametrize("combine", COMBINES)
+def test_mlp_block_tp2_t512(combine):
+    need_gpu()
+    L, f = layer("mlp_tp2_t512")
+    ys, h = L.mlp(combine)
+    ref = O.mlp_sharded(f["x"], f["wg"], f["wu"], f["wd"], L.n)
+    assert_close(host_f64(h), np.concatenate(ref["h"], axis=1), BF16_TOL, "H (SwiGLU)")
+    for y in ys:
+        assert_close(host_f64(y), ref["y"][0], BF16_TOL, "Y")
+    if combine != tp.TP_COMBINE_FUSED:
+        for y in ys[1:]:
+            assert np.array_equal(host_bits_f32(y), host_bits_f32(ys[0]))
+
+
+@pytest.mark.parametrize("combine", [tp.TP_COMBINE_NONE] + COMBINES)
+def test_mlp_block_small_ragged(combine):
+    need_gpu()
+    w = dict(kind="mlp", T=200, hidden=256, ffn=1024, tp=4, seed=9, w_std=0.05)
+    data = inputs.make_bf16_inputs(w)
+    L = Layer(w, data)
+    f = {k: inputs.bf16_bits_to_f64(v) for k, v in data.items()}
+    ys, h = L.mlp(combine)
+    ref = O.mlp_sharded(f["x"], f["wg"], f["wu"], f["wd"], 4)
+    assert_close(host_f64(h), np.concatenate(ref["h"], axis=1), BF16_TOL, "H")
+    if combine == tp.TP_COMBINE_NONE:
+        for y, p in zip(ys, ref["partials"]):
+            assert_close(host_f64(y), p, BF16_TOL, "partial")
+    else:
+        for y in ys:
+            assert_close(host_f64(y), ref["y"][0], BF16_TOL, "Y")
+
+
+# ---- attention projections ----------------------------------------------------------
+def _check_attn(L, f, q, k, v, ys):
+    w = L.w
+    ref = O.attn_proj_sharded(f["x"], f["wq"], f["wk"], f["wv"], f["a"], f["wo"], _oracle_plan(w),
+                              w["head_dim"])
+    for r in range(L.n):
+        assert_close(host_f64(q[r]), ref["q"][r], BF16_TOL, f"q[{r}]")
+    for r in range(len(k)):
+        assert_close(host_f64(k[r]), ref["k"][r], BF16_TOL, f"k[{r}]")
+        assert_close(host_f64(v[r]), ref["v"][r], BF16_TOL, f"v[{r}]")
+    for y in ys:
+        assert_close(host_f64(y), ref["y"][0], BF16_TOL, "Y")
+
+
+@pytest.mark.parametrize("combine", COMBINES)
+def test_attn_proj_gqa_tp4_t2048(combine):
+    need_gpu()
+    L, f = layer("attn_gqa_tp4_t2048")
+    assert [s["kv_heads"] for s in L.shards] == [(0, 2), (2, 4), (4, 6), (6, 8)]
+    q, k, v, ys = L.attn(combine)
+    assert len(k) == 4
+    _check_attn(L, f, q, k, v, ys)
+
+
+@pytest.mark.parametrize("combine", COMBINES)
+def test_decode_replicated_kv_tp8_t64(combine):
+    need_gpu()
+    L, f = layer("decode_gqa_rep_tp8_t64")
+    assert all(s["kv_replicated"] and s["kv_heads"] == (0, 4) for s in L.shards)
+    q, k, v, ys = L.attn(combine)
+    assert len(k) == 1                     # replicated K/V computed once
+    _check_attn(L, f, q, k, v, ys)
+    ys, h = L.mlp(combine)
+    ref = O.mlp_sharded(f["x"], f["wg"], f["wu"], f["wd"], L.n)
+    for y in ys:
+        assert_close(host_f64(y), ref["y"][0], BF16_TOL, "MLP Y")
+
+
+def test_prefill_layer_tp8_t4096_sampled_rows():
+    need_gpu()
+    L, f = layer("prefill_layer_tp8_t4096")
+    rows = np.sort(inputs.rng(L.w["seed"], 99).choice(L.T, size=L.w["oracle_rows"], replace=False))
+    q, k, v, ys = L.attn(tp.TP_COMBINE_RING_FUSED)
+    plan = _oracle_plan(L.w)
+    ref = O.attn_proj_sharded(f["x"][rows], f["wq"], f["wk"], f["wv"], f["a"][rows], f["wo"], plan,
+                              L.w["head_dim"])
+    for r in range(L.n):
+        assert_close(host_f64(q[r])[rows], ref["q"][r], BF16_TOL, f"q[{r}]")
+        assert_close(host_f64(k[r])[rows], ref["k"][r], BF16_TOL, f"k[{r}]")
+    for y in ys:
+        assert_close(host_f64(y)[rows], ref["y"][0], BF16_TOL, "attn Y")
+    del q, k, v
+    ys, h = L.mlp(tp.TP_COMBINE_FUSED)
+    ref = O.mlp_sharded(f["x"][rows], f["wg"], f["wu"], f["wd"], L.n)
+    assert_close(host_f64(ys[0])[rows], ref["y"][0], BF16_TOL, "MLP Y")
