@@ -234,6 +234,18 @@ tp_status tp_all_gather(int32_t tp_size, const tp_tensor *shard, tp_tensor *out,
  * bf16, T x F in total). */
 size_t tp_mlp_block_workspace_size(const tp_plan *plan, int64_t tokens);
 
+/* Column-parallel gate/up projection of the MLP with SwiGLU fused into the
+ * GEMM epilogue: H_r = silu(X G_r^T) * (X U_r^T), rounded to bf16, for every
+ * rank in one launch (the first half of tp_mlp_block; the manual's table lists
+ * no communication after gate/up).
+ *  x         : [T x D] bf16.
+ *  w_gate[r] : [F/N x D] bf16; w_up[r] likewise.
+ *  h[r]      : [T x F/N] bf16 output of rank r.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_RANK_FAILED,
+ * TP_ERR_CUDA. */
+tp_status tp_gate_up_swiglu(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_gate,
+                            const tp_tensor *w_up, tp_tensor *h, tp_stream_t stream);
+
 /* MLP block: H_r = silu(X G_r^T) * (X U_r^T) (SwiGLU fused into the gate/up
  * GEMM's epilogue, H_r rounded to bf16), then Y = sum_r H_r D_r^T.
  *  x         : [T x D] bf16.

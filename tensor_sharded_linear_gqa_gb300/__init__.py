@@ -83,6 +83,7 @@ _SIGS = {
     "tp_ring_all_gather": ([ctypes.c_int32, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_allreduce_ring": ([ctypes.c_int32, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_all_gather": ([ctypes.c_int32, _T, _T, ctypes.c_int32, ctypes.c_int32, _S], ctypes.c_int),
+    "tp_gate_up_swiglu": ([ctypes.c_void_p, _T, _T, _T, _T, _S], ctypes.c_int),
     "tp_mlp_block_workspace_size": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_size_t),
     "tp_mlp_block": ([ctypes.c_void_p, _T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_void_p,
                       ctypes.c_size_t, _S], ctypes.c_int),
@@ -259,6 +260,12 @@ def tp_all_gather(tp_size: int, shards, outs, axis: int, stream=None) -> None:
            "tp_all_gather")
 
 
+def tp_gate_up_swiglu(plan: Plan, x, w_gate, w_up, h, stream=None) -> None:
+    xs = tensor(x)
+    _check(_lib.tp_gate_up_swiglu(plan.handle, ctypes.byref(xs), _arr(w_gate), _arr(w_up), _arr(h),
+                                  _stream(stream)), "tp_gate_up_swiglu")
+
+
 def tp_mlp_block_workspace_size(plan: Plan, tokens: int) -> int:
     return int(_lib.tp_mlp_block_workspace_size(plan.handle, tokens))
 
@@ -315,6 +322,26 @@ def tp_debug_wait_timeout(stream=None) -> None:
 
 def tp_version() -> str:
     return _lib.tp_version().decode()
+
+
+def arr(seq):
+    """ctypes array of TpTensor for a per-rank argument (kept alive by the caller)."""
+    return _arr(seq)
+
+
+class Prepared:
+    """A C entry point with its arguments marshalled once, for tight loops: calling
+    it makes only the ctypes call. Raises TPError on a non-OK status."""
+
+    def __init__(self, fn_name: str, *args):
+        self.fn = getattr(_lib, fn_name)
+        self.name = fn_name
+        self.args = args  # keeps the ctypes objects alive
+
+    def __call__(self) -> None:
+        st = self.fn(*self.args)
+        if st != TP_OK:
+            raise TPError(st, self.name)
 
 
 def raw_status(fn_name: str, *args) -> int:

@@ -491,6 +491,76 @@ extern "C" size_t tp_mlp_block_workspace_size(const tp_plan *plan, int64_t token
   return static_cast<size_t>(tokens) * static_cast<size_t>(d.ffn) * 2;
 }
 
+namespace {
+
+// Checks the gate/up weights against the plan; Fr = ffn / tp_size.
+tp_status check_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *w_gate,
+                        const tp_tensor *w_up) {
+  const int32_t n = d.tp_size;
+  const long long D = d.hidden, Fr = d.ffn / n, T = x->rows;
+  if (!shape_ok(*x) || x->cols != D) return TP_ERR_INVALID_ARG;
+  if (x->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (T > 0 && !pitch_ok(*x)) return TP_ERR_ALIGNMENT;
+  for (int32_t r = 0; r < n; ++r) {
+    const tp_tensor *ws[2] = {&w_gate[r], &w_up[r]};
+    for (const tp_tensor *t : ws) {
+      if (!shape_ok(*t)) return TP_ERR_INVALID_ARG;
+      if (t->dtype != TP_BF16) return TP_ERR_DTYPE;
+      if (t->rows != Fr || t->cols != D) return TP_ERR_INVALID_ARG;
+      if (!pitch_ok(*t)) return TP_ERR_ALIGNMENT;
+    }
+  }
+  return TP_OK;
+}
+
+// One grouped launch: problem r = (X, G_r | U_r) -> h[r] with the SwiGLU epilogue.
+tp_status launch_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *w_gate,
+                         const tp_tensor *w_up, const tp_tensor *h, cudaStream_t s) {
+  const int32_t n = d.tp_size;
+  const long long D = d.hidden, Fr = d.ffn / n, T = x->rows;
+  GemmBuilder b;
+  b.epi = kEpiSwiGLU;
+  const long long mt = (T + 127) / 128;
+  b.bn = choose_bn(n * mt * ((Fr + 127) / 128), n * mt * ((Fr + 63) / 64), kEpiSwiGLU);
+  tp_status err = TP_OK;
+  const int am = b.add_map(x->ptr, T, D, x->ld, 128, &err);
+  if (am < 0) return err;
+  for (int32_t r = 0; r < n; ++r) {
+    const int gm = b.add_map(w_gate[r].ptr, Fr, D, w_gate[r].ld, b.bn / 2, &err);
+    if (gm < 0) return err;
+    const int um = b.add_map(w_up[r].ptr, Fr, D, w_up[r].ld, b.bn / 2, &err);
+    if (um < 0) return err;
+    const long long ks = D;
+    if (!b.add_problem(static_cast<int>(T), static_cast<int>(Fr), h[r].ptr, h[r].ld, &am, &gm, &um,
+                       &ks, 1))
+      return TP_ERR_UNSUPPORTED;
+  }
+  return b.launch(s);
+}
+
+}  // namespace
+
+extern "C" tp_status tp_gate_up_swiglu(const tp_plan *plan, const tp_tensor *x,
+                                       const tp_tensor *w_gate, const tp_tensor *w_up, tp_tensor *h,
+                                       tp_stream_t stream) {
+  tp_dims d;
+  if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
+  if (!x || !w_gate || !w_up || !h) return TP_ERR_INVALID_ARG;
+  tp_status st = check_gate_up(d, x, w_gate, w_up);
+  if (st != TP_OK) return st;
+  const int32_t n = d.tp_size;
+  const long long Fr = d.ffn / n, T = x->rows;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(h[r])) return TP_ERR_INVALID_ARG;
+    if (h[r].dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (h[r].rows != T || h[r].cols != Fr) return TP_ERR_INVALID_ARG;
+    if (T > 0 && !pitch_ok(h[r])) return TP_ERR_ALIGNMENT;
+  }
+  if ((st = check_health(n)) != TP_OK) return st;
+  if (T == 0) return TP_OK;
+  return launch_gate_up(d, x, w_gate, w_up, h, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_gate,
                                   const tp_tensor *w_up, const tp_tensor *w_down, tp_tensor *y,
                                   int32_t combine, void *workspace, size_t workspace_bytes,
@@ -499,61 +569,34 @@ extern "C" tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const
   if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
   if (!x || !w_gate || !w_up || !w_down || !y) return TP_ERR_INVALID_ARG;
   if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  tp_status st = check_gate_up(d, x, w_gate, w_up);
+  if (st != TP_OK) return st;
   const int32_t n = d.tp_size;
   const long long D = d.hidden, Fr = d.ffn / n, T = x->rows;
-  if (!shape_ok(*x) || x->cols != D) return TP_ERR_INVALID_ARG;
-  if (x->dtype != TP_BF16) return TP_ERR_DTYPE;
   for (int32_t r = 0; r < n; ++r) {
-    const tp_tensor *ws[3] = {&w_gate[r], &w_up[r], &w_down[r]};
-    for (const tp_tensor *t : ws) {
-      if (!shape_ok(*t)) return TP_ERR_INVALID_ARG;
-      if (t->dtype != TP_BF16) return TP_ERR_DTYPE;
-      if (!pitch_ok(*t)) return TP_ERR_ALIGNMENT;
-    }
-    if (w_gate[r].rows != Fr || w_gate[r].cols != D || w_up[r].rows != Fr || w_up[r].cols != D ||
-        w_down[r].rows != D || w_down[r].cols != Fr)
-      return TP_ERR_INVALID_ARG;
+    if (!shape_ok(w_down[r])) return TP_ERR_INVALID_ARG;
+    if (w_down[r].dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (w_down[r].rows != D || w_down[r].cols != Fr) return TP_ERR_INVALID_ARG;
+    if (!pitch_ok(w_down[r])) return TP_ERR_ALIGNMENT;
   }
   // H_r is rank r's column block of one [T x F] bf16 buffer in the workspace.
   if ((Fr * 2) % 16) return TP_ERR_ALIGNMENT;
   std::vector<tp_tensor> h(n);
   for (int32_t r = 0; r < n; ++r)
-    h[r] = tp_tensor{byte_ptr(workspace, r * Fr, TP_BF16), TP_BF16, 0, T, Fr, static_cast<int64_t>(d.ffn)};
-  int32_t dt = 0;
+    h[r] = tp_tensor{byte_ptr(workspace, r * Fr, TP_BF16), TP_BF16, 0, T, Fr,
+                     static_cast<int64_t>(d.ffn)};
   if (T > 0) {
-    if (!pitch_ok(*x)) return TP_ERR_ALIGNMENT;
     if (!workspace || workspace_bytes < tp_mlp_block_workspace_size(plan, T)) return TP_ERR_WORKSPACE;
     if (!aligned16(workspace)) return TP_ERR_ALIGNMENT;
   } else {
-    for (int32_t r = 0; r < n; ++r) h[r].ptr = nullptr, h[r].rows = 0;
+    for (int32_t r = 0; r < n; ++r) h[r].ptr = nullptr;
   }
-  tp_status st = check_row_args(n, h.data(), w_down, y, combine, &dt);
-  if (st != TP_OK) return st;
+  int32_t dt = 0;
+  if ((st = check_row_args(n, h.data(), w_down, y, combine, &dt)) != TP_OK) return st;
   if ((st = check_health(n)) != TP_OK) return st;
   if (T == 0) return TP_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-  // gate/up column-parallel GEMM with SwiGLU in the epilogue: H_r = silu(X G_r^T) * (X U_r^T).
-  {
-    GemmBuilder b;
-    b.epi = kEpiSwiGLU;
-    const long long mt = (T + 127) / 128;
-    b.bn = choose_bn(n * mt * ((Fr + 127) / 128), n * mt * ((Fr + 63) / 64), kEpiSwiGLU);
-    tp_status err = TP_OK;
-    const int am = b.add_map(x->ptr, T, D, x->ld, 128, &err);
-    if (am < 0) return err;
-    for (int32_t r = 0; r < n; ++r) {
-      const int gm = b.add_map(w_gate[r].ptr, Fr, D, w_gate[r].ld, b.bn / 2, &err);
-      if (gm < 0) return err;
-      const int um = b.add_map(w_up[r].ptr, Fr, D, w_up[r].ld, b.bn / 2, &err);
-      if (um < 0) return err;
-      const long long ks = D;
-      if (!b.add_problem(static_cast<int>(T), static_cast<int>(Fr), h[r].ptr, h[r].ld, &am, &gm,
-                         &um, &ks, 1))
-        return TP_ERR_UNSUPPORTED;
-    }
-    if ((st = b.launch(s)) != TP_OK) return st;
-  }
+  if ((st = launch_gate_up(d, x, w_gate, w_up, h.data(), s)) != TP_OK) return st;
   // down row-parallel GEMM + combine.
   return row_linear_impl(n, h.data(), w_down, y, combine, TP_BF16, s);
 }

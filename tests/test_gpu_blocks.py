@@ -104,6 +104,22 @@ def test_mlp_block_tp2_t512(combine):
             assert np.array_equal(host_bits_f32(y), host_bits_f32(ys[0]))
 
 
+def test_gate_up_swiglu_matches_oracle_h():
+    need_gpu()
+    t = torch()
+    w = dict(kind="mlp", T=333, hidden=512, ffn=2048, tp=4, seed=12, w_std=0.05)
+    data = inputs.make_bf16_inputs(w)
+    L = Layer(w, data)
+    f = {k: inputs.bf16_bits_to_f64(v) for k, v in data.items()}
+    g = [L.dev["wg"][slice(*L.rng(r, "gate_proj"))] for r in range(4)]
+    u = [L.dev["wu"][slice(*L.rng(r, "up_proj"))] for r in range(4)]
+    h = [t.full((333, 512), float("nan"), dtype=t.bfloat16, device="cuda") for _ in range(4)]
+    tp.tp_gate_up_swiglu(L.plan, L.x, g, u, h)
+    ref = O.mlp_sharded(f["x"], f["wg"], f["wu"], f["wd"], 4)["h"]
+    for r in range(4):
+        assert_close(host_f64(h[r]), ref[r], BF16_TOL, f"H[{r}]")
+
+
 @pytest.mark.parametrize("combine", [tp.TP_COMBINE_NONE] + COMBINES)
 def test_mlp_block_small_ragged(combine):
     need_gpu()
