@@ -262,6 +262,38 @@ tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const tp_tensor 
                        int32_t combine, void *workspace, size_t workspace_bytes,
                        tp_stream_t stream);
 
+/* tp_mlp_block without a caller-provided workspace. The pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory: for example a plug-in inside a framework that owns all device
+ * memory through its own allocator and lends none of it, or a serving process
+ * that reserved all free HBM at start-up and must not call cudaMalloc (which
+ * can fail, or stall other streams) while requests are in flight.
+ *
+ * It computes exactly what tp_mlp_block computes, with the same arguments
+ * except the workspace: H (tokens x ffn bf16 values) is kept in one fixed
+ * scratch array inside the library, tp_mlp_block_static_max_bytes() = 16 MiB
+ * long. Every GPU that loads the library reserves that array when the library's
+ * device code is loaded and keeps it until the process exits.
+ *  - Size limit: x->rows * ffn * 2 bytes must not exceed the maximum, else
+ *    TP_ERR_WORKSPACE is returned and nothing is enqueued.
+ *  - Allocation: the call allocates nothing (no cudaMalloc / cudaFree, no
+ *    allocating library routine).
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *    first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the last
+ *    call's H. Each call overwrites H in full before reading it, so nothing has
+ *    to be cleared; but calls that can overlap on the GPU (different streams
+ *    without ordering between them) race on the array and give wrong results.
+ * The caller still passes and owns x, the weights and y. Other errors: as
+ * tp_mlp_block. */
+tp_status tp_mlp_block_static(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_gate,
+                              const tp_tensor *w_up, const tp_tensor *w_down, tp_tensor *y,
+                              int32_t combine, tp_stream_t stream);
+
+/* Size in bytes of tp_mlp_block_static's fixed scratch array (16 MiB). */
+size_t tp_mlp_block_static_max_bytes(void);
+
 /* Attention projections with GQA sharding.
  *  x        : [T x D] bf16.
  *  w_q[r]   : [(q heads of r) * hd x D] bf16;  q[r]: [T x same] bf16 out.

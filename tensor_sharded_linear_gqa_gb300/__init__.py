@@ -87,6 +87,8 @@ _SIGS = {
     "tp_mlp_block_workspace_size": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_size_t),
     "tp_mlp_block": ([ctypes.c_void_p, _T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_void_p,
                       ctypes.c_size_t, _S], ctypes.c_int),
+    "tp_mlp_block_static": ([ctypes.c_void_p, _T, _T, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
+    "tp_mlp_block_static_max_bytes": ([], ctypes.c_size_t),
     "tp_attn_proj": ([ctypes.c_void_p, _T, _T, _T, _T, _T, _T, _T, _T, _T, _T, ctypes.c_int32,
                       _S], ctypes.c_int),
     "tp_status_str": ([ctypes.c_int], ctypes.c_char_p),
@@ -282,6 +284,20 @@ def tp_mlp_block(plan: Plan, x, w_gate, w_up, w_down, y, combine: int, workspace
     _check(_lib.tp_mlp_block(plan.handle, ctypes.byref(xs), _arr(w_gate), _arr(w_up),
                              _arr(w_down), _arr(y), combine, wptr, wbytes, _stream(stream)),
            "tp_mlp_block")
+
+
+def tp_mlp_block_static(plan: Plan, x, w_gate, w_up, w_down, y, combine: int, stream=None) -> None:
+    """tp_mlp_block without a workspace argument, for callers that cannot allocate
+    device memory: H lives in the library's fixed 16 MiB scratch array. Calls on
+    one device share that array, so calls that overlap on the GPU race."""
+    xs = tensor(x)
+    _check(_lib.tp_mlp_block_static(plan.handle, ctypes.byref(xs), _arr(w_gate), _arr(w_up),
+                                    _arr(w_down), _arr(y), combine, _stream(stream)),
+           "tp_mlp_block_static")
+
+
+def tp_mlp_block_static_max_bytes() -> int:
+    return int(_lib.tp_mlp_block_static_max_bytes())
 
 
 def tp_attn_proj(plan: Plan, x, w_q, w_k, w_v, q, k, v, a, w_o, y, combine: int,
