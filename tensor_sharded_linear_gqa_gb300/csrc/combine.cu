@@ -100,9 +100,13 @@ __global__ void __launch_bounds__(kThreads) k_ring_ag_step(RankPtrs b, int n, lo
 }
 
 // Folds chunk c (grid.y) over all ranks in ring order; writes every buffer
-// (all-reduce) or buffer c only (reduce-scatter).
-__global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n, long long size,
+// (all-reduce) or buffer c only (reduce-scatter). NT = N when N is 2, 4 or 8
+// (fully unrolled, two float4 per thread per pass with every load issued before
+// the first add); NT = 0 handles any N.
+template <int NT>
+__global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n_rt, long long size,
                                                          int write_all) {
+  const int n = NT ? NT : n_rt;
   const int c = blockIdx.y;
   long long lo, hi, vlo, vhi;
   chunk_range(size, n, c, lo, hi);
@@ -121,14 +125,59 @@ __global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n, long
   if (t < vlo - lo) scalar(lo + t);
   if (t < hi - vhi) scalar(vhi + t);
   const long long v0 = vlo >> 2, nv = (vhi - vlo) >> 2;
-  for (long long i = t; i < nv; i += stride) {
-    float4 acc = reinterpret_cast<const float4 *>(b.p[(c + 1) % n])[v0 + i];
-    for (int j = 2; j <= n; ++j)
-      acc = add4(acc, reinterpret_cast<const float4 *>(b.p[(c + j) % n])[v0 + i]);
-    if (write_all) {
-      for (int r = 0; r < n; ++r) reinterpret_cast<float4 *>(b.p[r])[v0 + i] = acc;
-    } else {
-      reinterpret_cast<float4 *>(b.p[c])[v0 + i] = acc;
+  if constexpr (NT > 0) {
+    const float4 *src[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) src[j] = reinterpret_cast<const float4 *>(b.p[(c + 1 + j) % NT]) + v0;
+    long long i = t;
+    for (; i + stride < nv; i += 2 * stride) {
+      float4 x0[NT], x1[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        x0[j] = src[j][i];
+        x1[j] = src[j][i + stride];
+      }
+      float4 a0 = x0[0], a1 = x1[0];
+#pragma unroll
+      for (int j = 1; j < NT; ++j) {
+        a0 = add4(a0, x0[j]);
+        a1 = add4(a1, x1[j]);
+      }
+      if (write_all) {
+#pragma unroll
+        for (int r = 0; r < NT; ++r) {
+          reinterpret_cast<float4 *>(b.p[r])[v0 + i] = a0;
+          reinterpret_cast<float4 *>(b.p[r])[v0 + i + stride] = a1;
+        }
+      } else {
+        reinterpret_cast<float4 *>(b.p[c])[v0 + i] = a0;
+        reinterpret_cast<float4 *>(b.p[c])[v0 + i + stride] = a1;
+      }
+    }
+    for (; i < nv; i += stride) {
+      float4 x[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) x[j] = src[j][i];
+      float4 a = x[0];
+#pragma unroll
+      for (int j = 1; j < NT; ++j) a = add4(a, x[j]);
+      if (write_all) {
+#pragma unroll
+        for (int r = 0; r < NT; ++r) reinterpret_cast<float4 *>(b.p[r])[v0 + i] = a;
+      } else {
+        reinterpret_cast<float4 *>(b.p[c])[v0 + i] = a;
+      }
+    }
+  } else {
+    for (long long i = t; i < nv; i += stride) {
+      float4 acc = reinterpret_cast<const float4 *>(b.p[(c + 1) % n])[v0 + i];
+      for (int j = 2; j <= n; ++j)
+        acc = add4(acc, reinterpret_cast<const float4 *>(b.p[(c + j) % n])[v0 + i]);
+      if (write_all) {
+        for (int r = 0; r < n; ++r) reinterpret_cast<float4 *>(b.p[r])[v0 + i] = acc;
+      } else {
+        reinterpret_cast<float4 *>(b.p[c])[v0 + i] = acc;
+      }
     }
   }
 }
@@ -214,9 +263,11 @@ __global__ void k_debug_wait(int *status, long long wait_ns) {
   }
 }
 
+// Blocks per grid row: enough threads for about four float4 each (so every
+// thread has several loads in flight), at most four blocks per SM in total.
 int blocks_for(long long elems, int ranks_in_grid) {
-  const long long vec_threads = (elems / 4 + kThreads - 1) / kThreads;
-  long long cap = static_cast<long long>(num_sms()) * 8 / (ranks_in_grid > 0 ? ranks_in_grid : 1);
+  const long long vec_threads = (elems / 4 + 4 * kThreads - 1) / (4 * kThreads);
+  long long cap = static_cast<long long>(num_sms()) * 4 / (ranks_in_grid > 0 ? ranks_in_grid : 1);
   if (cap < 1) cap = 1;
   long long g = vec_threads < cap ? vec_threads : cap;
   return static_cast<int>(g < 1 ? 1 : g);
@@ -244,7 +295,12 @@ tp_status launch_ring_ag_step(const RankPtrs &b, int n, long long size, int step
 tp_status launch_ring_fused(const RankPtrs &b, int n, long long size, int write_all,
                             cudaStream_t s) {
   const dim3 grid(blocks_for(size / n + 4, n), n);
-  k_ring_fused<<<grid, kThreads, 0, s>>>(b, n, size, write_all);
+  switch (n) {
+    case 2: k_ring_fused<2><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
+    case 4: k_ring_fused<4><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
+    case 8: k_ring_fused<8><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
+    default: k_ring_fused<0><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
+  }
   return check_launch();
 }
 

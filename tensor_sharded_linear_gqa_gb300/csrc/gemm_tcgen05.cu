@@ -2,20 +2,25 @@
 // [M x K] and B [N x K] both K-major (weights stored [out x in]), fp32
 // accumulation in tensor memory.
 //
-// One CTA computes one 128 x BN output tile of one problem. Warp roles:
+// Persistent: one CTA per SM walks 128 x BN output tiles of all problems
+// (tile t goes to CTA t mod gridDim.x). Warp roles:
 //   warp 0      TMA producer: one thread streams 128x64 A and BNx64 B tiles
-//               into a ring of shared-memory stages (128-byte swizzle).
-//   warp 1      owns the TMEM accumulator (alloc / dealloc); one thread issues
-//               tcgen05.mma (M=128, N=BN, K=16, four per 64-wide stage) and
-//               frees each stage with tcgen05.commit.
+//               into a ring of shared-memory stages (128-byte swizzle), and
+//               prefetches B tiles a few k-blocks further ahead into L2.
+//   warp 1      owns TMEM (two BN-column fp32 accumulators; alloc / dealloc);
+//               one thread issues tcgen05.mma (M=128, N=BN, K=16, four per
+//               64-wide stage), frees each stage with tcgen05.commit and hands
+//               each finished accumulator to the epilogue.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp reads its
-//               32-lane quarter), fused output transform, global stores.
+//               32-lane quarter), fused output transform, global stores; the
+//               accumulator is released as soon as it has been read.
 // A problem's K loop runs over its segments in order, so a row-parallel layer
 // can sum every rank's shard in the same accumulator (segments = ranks).
 // Every mbarrier wait is bounded; a wait that runs out records a code in the
 // device status word, the CTA drains its in-flight copies, frees TMEM and exits.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -42,7 +47,9 @@ struct TileCfg {
 
 __device__ __forceinline__ void record(int *status, int code) { atomicCAS(status, 0, code); }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g * sigmoid(g); for g < -87 the denominator exceeds 2^126 and the
+// fast division returns 0, the correctly signed limit to within 1e-36.
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ void store_f32_row32(float *out, long long ldc, int row, int col0, int n,
                                                 const float (&f)[32]) {
@@ -80,11 +87,63 @@ __device__ __forceinline__ void store_bf16_row32(__nv_bfloat16 *out, long long l
   }
 }
 
+// Walks this CTA's (tile, segment, k-tile) sequence: tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ...; within a tile every segment of its problem in
+// order, within a segment its k-tiles.
+struct Cursor {
+  int tile, prob, mt, nt, seg, kt, kt_in_tile;
+  bool valid;
+};
+
+__device__ __forceinline__ int find_problem(const GemmParams &p, int tile) {
+  int pi = 0;
+  for (int i = 1; i < p.num_problems; ++i)
+    if (tile >= p.prob[i].tile_begin) pi = i;
+  return pi;
+}
+
+__device__ __forceinline__ void cursor_tile(const GemmParams &p, Cursor &c, int tile) {
+  c.tile = tile;
+  c.valid = tile < p.total_tiles;
+  if (!c.valid) return;
+  c.prob = find_problem(p, tile);
+  const GemmProblem &pr = p.prob[c.prob];
+  const int local = tile - pr.tile_begin;
+  c.mt = local % pr.m_tiles;
+  c.nt = local / pr.m_tiles;
+  c.seg = 0;
+  c.kt = 0;
+  c.kt_in_tile = 0;
+}
+
+__device__ __forceinline__ void cursor_next(const GemmParams &p, Cursor &c) {
+  const GemmProblem &pr = p.prob[c.prob];
+  ++c.kt;
+  ++c.kt_in_tile;
+  if (c.kt < p.seg[pr.seg_begin + c.seg].k_tiles) return;
+  c.kt = 0;
+  if (++c.seg < pr.seg_count) return;
+  cursor_tile(p, c, c.tile + gridDim.x);
+}
+
+__device__ __forceinline__ int tile_k_tiles(const GemmParams &p, int prob) {
+  const GemmProblem &pr = p.prob[prob];
+  int n = 0;
+  for (int s = 0; s < pr.seg_count; ++s) n += p.seg[pr.seg_begin + s].k_tiles;
+  return n;
+}
+
+// Persistent kernel: one CTA per SM walks tiles blockIdx.x + j * gridDim.x.
+// TMEM holds two accumulators, so the epilogue of tile j overlaps the MMAs of
+// tile j+1. The producer also prefetches B tiles kPrefetch k-blocks ahead into
+// L2, so the shared-memory ring waits on L2 rather than on DRAM.
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant__ GemmParams p) {
   using C = TileCfg<BN>;
   constexpr int kBRows = (EPI == kEpiSwiGLU) ? BN / 2 : BN;  // rows per B map box
   constexpr int kOutCols = (EPI == kEpiSwiGLU) ? BN / 2 : BN;
+  const int kPrefetch = p.prefetch;
+  constexpr uint32_t kTmemCols = 2 * BN;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -93,23 +152,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   const uint32_t sB0 = sA0 + C::kStages * C::kABytes;
   uint8_t *bar_area = smem + C::kStages * C::kStageBytes;
   const uint32_t bar0 = ptx::smem_addr(bar_area);
-  const uint32_t accum_bar = bar0 + 16 * C::kStages;
-  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 16 * C::kStages + 8);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 16 * C::kStages + 16);
+  // layout: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, then slot / flag words
   auto full_bar = [&](int i) { return bar0 + 8u * i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (C::kStages + i); };
-
-  // ---- which tile of which problem ----
-  const int tile = blockIdx.x;
-  int pi = 0;
-  for (int i = 1; i < p.num_problems; ++i)
-    if (tile >= p.prob[i].tile_begin) pi = i;
-  const GemmProblem &pr = p.prob[pi];
-  const int local = tile - pr.tile_begin;
-  const int mt = local % pr.m_tiles;
-  const int nt = local / pr.m_tiles;
-  int total_kt = 0;
-  for (int s = 0; s < pr.seg_count; ++s) total_kt += p.seg[pr.seg_begin + s].k_tiles;
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::kStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::kStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 4);
+  volatile uint32_t *tmem_slot =
+      reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * C::kStages + 5));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * C::kStages + 5) + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -119,88 +170,128 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
       ptx::mbar_init(full_bar(i), 1);
       ptx::mbar_init(empty_bar(i), 1);
     }
-    ptx::mbar_init(accum_bar, 1);
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), 4);  // one arrival per epilogue warp
+    }
+    ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < pr.seg_count; ++s) {
-      const GemmSeg &sg = p.seg[pr.seg_begin + s];
-      ptx::prefetch_tensormap(&p.maps[sg.a_map]);
-      ptx::prefetch_tensormap(&p.maps[sg.b_map]);
-      if (EPI == kEpiSwiGLU) ptx::prefetch_tensormap(&p.maps[sg.b2_map]);
-    }
+    for (int i = 0; i < p.n_maps_used; ++i) ptx::prefetch_tensormap(&p.maps[i]);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), BN);
+    ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem_d = *tmem_slot;
+  const uint32_t tmem_base = *tmem_slot;
 
   int issued = 0;  // k-blocks whose loads the producer started (thread 0 only)
   if (warp == 0) {
     if (lane == 0) {
-      const int a_row = mt * BM;
-      const int b_row = nt * kBRows;
-      bool ok = true;
+      Cursor ld, pf;
+      cursor_tile(p, ld, blockIdx.x);
+      cursor_tile(p, pf, blockIdx.x);
+      auto prefetch = [&](const Cursor &c) {
+        const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
+        ptx::tma_prefetch_l2_2d(&p.maps[sg.b_map], c.kt * BK, c.nt * kBRows);
+        if (EPI == kEpiSwiGLU) ptx::tma_prefetch_l2_2d(&p.maps[sg.b2_map], c.kt * BK, c.nt * kBRows);
+      };
+      for (int i = 0; i < kPrefetch && pf.valid; ++i) {
+        prefetch(pf);
+        cursor_next(p, pf);
+      }
       int kb = 0;
-      for (int s = 0; ok && s < pr.seg_count; ++s) {
-        const GemmSeg sg = p.seg[pr.seg_begin + s];
-        for (int kt = 0; kt < sg.k_tiles; ++kt, ++kb) {
-          const int st = kb % C::kStages;
-          const uint32_t ph = (kb / C::kStages) & 1;
-          if (*abort_flag) { ok = false; break; }
-          if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
-            record(p.status, kDevTimeoutProducer);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(full_bar(st), C::kStageBytes);
-          ptx::tma_load_2d(sA0 + st * C::kABytes, &p.maps[sg.a_map], kt * BK, a_row, full_bar(st));
-          ptx::tma_load_2d(sB0 + st * C::kBBytes, &p.maps[sg.b_map], kt * BK, b_row, full_bar(st));
-          if (EPI == kEpiSwiGLU)
-            ptx::tma_load_2d(sB0 + st * C::kBBytes + kBRows * 128, &p.maps[sg.b2_map], kt * BK,
-                             b_row, full_bar(st));
-          issued = kb + 1;
+      while (ld.valid) {
+        if (pf.valid) {
+          prefetch(pf);
+          cursor_next(p, pf);
         }
+        const int st = kb % C::kStages;
+        const uint32_t ph = (kb / C::kStages) & 1;
+        if (*abort_flag) break;
+        if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
+          record(p.status, kDevTimeoutProducer);
+          *abort_flag = 1;
+          break;
+        }
+        const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
+        ptx::mbar_arrive_expect_tx(full_bar(st), C::kStageBytes);
+        ptx::tma_load_2d(sA0 + st * C::kABytes, &p.maps[sg.a_map], ld.kt * BK, ld.mt * BM,
+                         full_bar(st));
+        ptx::tma_load_2d(sB0 + st * C::kBBytes, &p.maps[sg.b_map], ld.kt * BK, ld.nt * kBRows,
+                         full_bar(st));
+        if (EPI == kEpiSwiGLU)
+          ptx::tma_load_2d(sB0 + st * C::kBBytes + kBRows * 128, &p.maps[sg.b2_map], ld.kt * BK,
+                           ld.nt * kBRows, full_bar(st));
+        issued = ++kb;
+        cursor_next(p, ld);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
-      for (int kb = 0; kb < total_kt; ++kb) {
-        const int st = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
-        if (*abort_flag) break;
-        if (!ptx::mbar_wait(full_bar(st), ph, p.wait_ns)) {
-          record(p.status, kDevTimeoutMma);
+      int kb = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x, j = 0; ok && tile < p.total_tiles; tile += gridDim.x, ++j) {
+        const int a = j & 1;
+        const uint32_t use = static_cast<uint32_t>(j >> 1);
+        if (*abort_flag || !ptx::mbar_wait(tempty_bar(a), (use & 1) ^ 1, p.wait_ns)) {
+          if (!*abort_flag) record(p.status, kDevTimeoutMma);
           *abort_flag = 1;
           break;
         }
         ptx::tc_fence_after();
-        const uint64_t ad = ptx::smem_desc_sw128(sA0 + st * C::kABytes);
-        const uint64_t bd = ptx::smem_desc_sw128(sB0 + st * C::kBBytes);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(a * BN);
+        const int nk = tile_k_tiles(p, find_problem(p, tile));
+        for (int k0 = 0; k0 < nk; ++k0, ++kb) {
+          const int st = kb % C::kStages;
+          const uint32_t ph = (kb / C::kStages) & 1;
+          if (*abort_flag) { ok = false; break; }
+          if (!ptx::mbar_wait(full_bar(st), ph, p.wait_ns)) {
+            record(p.status, kDevTimeoutMma);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t ad = ptx::smem_desc_sw128(sA0 + st * C::kABytes);
+          const uint64_t bd = ptx::smem_desc_sw128(sB0 + st * C::kBBytes);
 #pragma unroll
-        for (int k = 0; k < BK / UMMA_K; ++k)
-          ptx::mma_bf16(tmem_d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-        ptx::mma_commit(empty_bar(st));
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (k0 | k) != 0 ? 1u : 0u);
+          ptx::mma_commit(empty_bar(st));
+        }
+        ptx::mma_commit(tfull_bar(a));
       }
-      ptx::mma_commit(accum_bar);
+      // Every MMA this thread issued has completed once the drain barrier fires.
+      ptx::mma_commit(drain_bar);
+      if (!ptx::mbar_wait(drain_bar, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
     }
   } else {
     // ---- epilogue: warps 2..5, warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32) ----
     const int q = warp & 3;
-    const bool ready = ptx::mbar_wait(accum_bar, 0, p.wait_ns);
-    if (!ready && lane == 0) record(p.status, kDevTimeoutEpilogue);
-    ptx::tc_fence_after();
-    const bool go = __all_sync(0xffffffffu, ready && (*abort_flag == 0));
-    if (go) {
+    for (int tile = blockIdx.x, j = 0; tile < p.total_tiles; tile += gridDim.x, ++j) {
+      const int a = j & 1;
+      const uint32_t use = static_cast<uint32_t>(j >> 1);
+      const bool ready = ptx::mbar_wait(tfull_bar(a), use & 1, p.wait_ns);
+      if (!ready && lane == 0) record(p.status, kDevTimeoutEpilogue);
+      ptx::tc_fence_after();
+      if (!__all_sync(0xffffffffu, ready && (*abort_flag == 0))) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      const GemmProblem &pr = p.prob[find_problem(p, tile)];
+      const int local = tile - pr.tile_begin;
+      const int mt = local % pr.m_tiles;
+      const int nt = local / pr.m_tiles;
       const int row = mt * BM + q * 32 + lane;
-      const uint32_t tbase = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * BN) +
+                             (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (EPI == kEpiSwiGLU) {
         __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(pr.out);
 #pragma unroll 1
@@ -209,9 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
           ptx::tmem_ld_32cols(tbase + c, g);
           ptx::tmem_ld_32cols(tbase + BN / 2 + c, u);
           ptx::tmem_ld_wait();
+          if (c + 32 == BN / 2) {  // accumulator fully read: hand it back to the MMA warp
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty_bar(a));
+          }
           float h[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) h[j] = silu(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+          for (int jj = 0; jj < 32; ++jj) h[jj] = silu(__uint_as_float(g[jj])) * __uint_as_float(u[jj]);
           if (row < pr.m) store_bf16_row32(out, pr.ldc, row, nt * kOutCols + c, pr.n, h);
         }
       } else {
@@ -220,9 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
           uint32_t v[32];
           ptx::tmem_ld_32cols(tbase + c, v);
           ptx::tmem_ld_wait();
+          if (c + 32 == BN) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty_bar(a));
+          }
           float f[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+          for (int jj = 0; jj < 32; ++jj) f[jj] = __uint_as_float(v[jj]);
           if (row < pr.m) {
             if constexpr (EPI == kEpiF32)
               store_f32_row32(static_cast<float *>(pr.out), pr.ldc, row, nt * kOutCols + c, pr.n, f);
@@ -247,7 +348,640 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_d, BN);
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Pair kernel: two CTAs of a cluster (an SM pair) compute one 256 x 256 tile
+// with tcgen05.mma.cta_group::2 (M=256, N=256, K=16). CTA r of the pair loads
+// A rows [128r, 128r+128) of the tile and one 128-row half of B (for SwiGLU:
+// the gate rows in CTA 0, the up rows in CTA 1), so each SM streams half the B
+// bytes of the single-CTA kernel per MMA flop. Only CTA 0 issues MMAs; its
+// commits arrive on the stage and accumulator barriers of both CTAs. Each CTA
+// holds its own 128 accumulator rows in TMEM (two 256-column buffers) and runs
+// its own epilogue; the epilogue warps of both CTAs release an accumulator on
+// CTA 0's barrier.
+// ---------------------------------------------------------------------------
+// A stage holds KSUB consecutive 64-wide k-tiles (KSUB boxes of A and of B per
+// CTA under one barrier): the TMA unit of an SM delivers more bytes per clock
+// with more boxes in flight per barrier phase, so 128-wide stages (KSUB = 2)
+// keep the tensor pipe fed better than 64-wide ones.
+constexpr int kPairABytes = 128 * BK * 2;  // one 64-wide k-tile of this CTA's 128 A rows
+constexpr int kPairBBytes = 128 * BK * 2;  // one 64-wide k-tile of this CTA's 128 B rows
+template <int KSUB>
+struct PairCfg {
+  static constexpr int kStages = 6 / KSUB;
+  static constexpr int kStageBytes = KSUB * (kPairABytes + kPairBBytes);
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+};
+
+template <int KSUB>
+__device__ __forceinline__ int seg_stages(const GemmSeg &sg) { return (sg.k_tiles + KSUB - 1) / KSUB; }
+
+template <int KSUB>
+__device__ __forceinline__ int tile_stages(const GemmParams &p, int prob) {
+  const GemmProblem &pr = p.prob[prob];
+  int n = 0;
+  for (int s = 0; s < pr.seg_count; ++s) n += seg_stages<KSUB>(p.seg[pr.seg_begin + s]);
+  return n;
+}
+
+template <int EPI, int KSUB>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_bf16_pair(const __grid_constant__ GemmParams p) {
+  constexpr int kPairSub = KSUB;
+  constexpr int kPairStages = PairCfg<KSUB>::kStages;
+  constexpr int kPairStageBytes = PairCfg<KSUB>::kStageBytes;
+  constexpr int BN = 256;
+  constexpr int kOutCols = (EPI == kEpiSwiGLU) ? BN / 2 : BN;
+  const int kPrefetch = p.prefetch;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr int S = kPairStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  // stage st: A k-tiles at sA0 + (st*KSUB + j)*kPairABytes, B at sB0 + (st*KSUB + j)*kPairBBytes
+  const uint32_t sA0 = ptx::smem_addr(smem);
+  const uint32_t sB0 = sA0 + S * kPairSub * kPairABytes;
+  uint8_t *bar_area = smem + S * kPairStageBytes;
+  const uint32_t bar0 = ptx::smem_addr(bar_area);
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (S + i); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * S + 5));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * S + 5) + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0 or 1 within the pair
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(full_bar(i), 1);
+      ptx::mbar_init(empty_bar(i), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.n_maps_used; ++i) ptx::prefetch_tensormap(&p.maps[i]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // Cursor over this pair's tiles: tiles pair, pair + npairs, ...
+      auto first = [&](Cursor &c) {
+        c.tile = pair;
+        c.valid = pair < p.total_tiles;
+        if (!c.valid) return;
+        c.prob = find_problem(p, pair);
+        const GemmProblem &pr = p.prob[c.prob];
+        c.mt = (pair - pr.tile_begin) % pr.m_tiles;
+        c.nt = (pair - pr.tile_begin) / pr.m_tiles;
+        c.seg = c.kt = c.kt_in_tile = 0;
+      };
+      auto next = [&](Cursor &c) {
+        const GemmProblem &pr = p.prob[c.prob];
+        ++c.kt;
+        ++c.kt_in_tile;
+        if (c.kt < seg_stages<KSUB>(p.seg[pr.seg_begin + c.seg])) return;
+        c.kt = 0;
+        if (++c.seg < pr.seg_count) return;
+        const int t = c.tile + npairs;
+        c.tile = t;
+        c.valid = t < p.total_tiles;
+        if (!c.valid) return;
+        c.prob = find_problem(p, t);
+        const GemmProblem &q = p.prob[c.prob];
+        c.mt = (t - q.tile_begin) % q.m_tiles;
+        c.nt = (t - q.tile_begin) / q.m_tiles;
+        c.seg = c.kt = c.kt_in_tile = 0;
+      };
+      // This CTA's half of B: rows of its own map and offset.
+      auto b_src = [&](const Cursor &c, int &map, int &row) {
+        const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
+        if (EPI == kEpiSwiGLU) {
+          map = leader ? sg.b_map : sg.b2_map;
+          row = c.nt * 128;
+        } else {
+          map = sg.b_map;
+          row = c.nt * BN + static_cast<int>(rank) * 128;
+        }
+      };
+      Cursor ld, pf;
+      first(ld);
+      first(pf);
+      for (int i = 0; i < kPrefetch && pf.valid; ++i) {
+        int m, r;
+        b_src(pf, m, r);
+        ptx::tma_prefetch_l2_2d(&p.maps[m], pf.kt * kPairSub * BK, r);
+        next(pf);
+      }
+      int kb = 0;
+      while (ld.valid) {
+        if (pf.valid) {
+          int m, r;
+          b_src(pf, m, r);
+          ptx::tma_prefetch_l2_2d(&p.maps[m], pf.kt * kPairSub * BK, r);
+          next(pf);
+        }
+        const int st = kb % S;
+        const uint32_t ph = (kb / S) & 1;
+        if (*abort_flag) break;
+        if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
+          record(p.status, kDevTimeoutProducer);
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t lead_full = ptx::mapa_shared(full_bar(st), 0);
+        if (leader) ptx::mbar_arrive_expect_tx(full_bar(st), 2 * kPairStageBytes);
+        const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
+        int m, r;
+        b_src(ld, m, r);
+#pragma unroll
+        for (int j = 0; j < kPairSub; ++j) {
+          // a k-tile past the segment's end reads zeros (out-of-range TMA fill)
+          const int x = (ld.kt * kPairSub + j) * BK;
+          ptx::tma_load_2d_pair(sA0 + (st * kPairSub + j) * kPairABytes, &p.maps[sg.a_map], x,
+                                ld.mt * 256 + static_cast<int>(rank) * 128, lead_full);
+          ptx::tma_load_2d_pair(sB0 + (st * kPairSub + j) * kPairBBytes, &p.maps[m], x, r, lead_full);
+        }
+        ++kb;
+        next(ld);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, BN);
+      int kb = 0;
+      bool ok = true;
+      for (int tile = pair, j = 0; ok && tile < p.total_tiles; tile += npairs, ++j) {
+        const int a = j & 1;
+        const uint32_t use = static_cast<uint32_t>(j >> 1);
+        if (*abort_flag || !ptx::mbar_wait(tempty_bar(a), (use & 1) ^ 1, p.wait_ns)) {
+          if (!*abort_flag) record(p.status, kDevTimeoutMma);
+          *abort_flag = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(a * BN);
+        const int nk = tile_stages<KSUB>(p, find_problem(p, tile));
+        for (int k0 = 0; k0 < nk; ++k0, ++kb) {
+          const int st = kb % S;
+          const uint32_t ph = (kb / S) & 1;
+          if (*abort_flag) { ok = false; break; }
+          if (!ptx::mbar_wait(full_bar(st), ph, p.wait_ns)) {
+            record(p.status, kDevTimeoutMma);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < kPairSub; ++j) {
+            const uint64_t ad = ptx::smem_desc_sw128(sA0 + (st * kPairSub + j) * kPairABytes);
+            const uint64_t bd = ptx::smem_desc_sw128(sB0 + (st * kPairSub + j) * kPairBBytes);
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k)
+              ptx::mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (k0 | j | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_multicast(empty_bar(st), 0x3);
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_multicast(tfull_bar(a), 0x3);
+      }
+      ptx::mma_commit_pair_multicast(drain_bar, 0x1);
+      if (!ptx::mbar_wait(drain_bar, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    }
+  } else {
+    const int q = warp & 3;
+    for (int tile = pair, j = 0; tile < p.total_tiles; tile += npairs, ++j) {
+      const int a = j & 1;
+      const uint32_t use = static_cast<uint32_t>(j >> 1);
+      const bool ready = ptx::mbar_wait(tfull_bar(a), use & 1, p.wait_ns);
+      if (!ready && lane == 0) record(p.status, kDevTimeoutEpilogue);
+      ptx::tc_fence_after();
+      if (!__all_sync(0xffffffffu, ready && (*abort_flag == 0))) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      const GemmProblem &pr = p.prob[find_problem(p, tile)];
+      const int local = tile - pr.tile_begin;
+      const int mt = local % pr.m_tiles;
+      const int nt = local / pr.m_tiles;
+      const int row = mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * BN) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t lead_tempty = ptx::mapa_shared(tempty_bar(a), 0);
+      if constexpr (EPI == kEpiSwiGLU) {
+        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(pr.out);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld_32cols(tbase + c, g);
+          ptx::tmem_ld_32cols(tbase + BN / 2 + c, u);
+          ptx::tmem_ld_wait();
+          if (c + 32 == BN / 2) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_remote(lead_tempty);
+          }
+          float h[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) h[jj] = silu(__uint_as_float(g[jj])) * __uint_as_float(u[jj]);
+          if (row < pr.m) store_bf16_row32(out, pr.ldc, row, nt * kOutCols + c, pr.n, h);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32cols(tbase + c, v);
+          ptx::tmem_ld_wait();
+          if (c + 32 == BN) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_remote(lead_tempty);
+          }
+          float f[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) f[jj] = __uint_as_float(v[jj]);
+          if (row < pr.m) {
+            if constexpr (EPI == kEpiF32)
+              store_f32_row32(static_cast<float *>(pr.out), pr.ldc, row, nt * kOutCols + c, pr.n, f);
+            else
+              store_bf16_row32(static_cast<__nv_bfloat16 *>(pr.out), pr.ldc, row, nt * kOutCols + c,
+                               pr.n, f);
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // A wait ran out somewhere in the pair: give copies already in flight (into
+    // either CTA) time to land before the pair's shared memory goes away.
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  ptx::cluster_sync();  // neither CTA leaves while the other may still touch its smem
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K cluster kernel for problems with too few output tiles to fill the
+// GPU (small-token row-parallel layers, decode). A cluster computes one tile:
+// CTA ranks are (split, member), member = the M-half for SM pairs. Split s
+// accumulates k-stages [s*ns/S, (s+1)*ns/S) of the tile in TMEM, writes its fp32
+// accumulator to its own shared memory, and after a cluster barrier reduces a
+// slice of the tile's rows by reading that slice from every split's shared
+// memory (DSMEM) and adding in split order 0, 1, ..., S-1. The sum order is
+// fixed, so the result does not depend on timing; no global workspace is used.
+// ---------------------------------------------------------------------------
+template <bool PAIR>
+struct SplitCfg {
+  static constexpr int kSub = PAIR ? 2 : 1;  // 64-wide k-tiles per stage
+  static constexpr int kStages = PAIR ? 3 : 4;
+  static constexpr int kABytes = 128 * BK * 2;
+  static constexpr int kBRows = PAIR ? 128 : 256;  // B rows per CTA per k-tile
+  static constexpr int kBBytes = kBRows * BK * 2;
+  static constexpr int kStageBytes = kSub * (kABytes + kBBytes);
+  static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+};
+
+template <bool PAIR, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_constant__ GemmParams p) {
+  using C = SplitCfg<PAIR>;
+  constexpr int BN = 256;
+  constexpr int KS = C::kSub;
+  constexpr int S = C::kStages;
+  constexpr uint32_t kTmemCols = BN;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sA0 = ptx::smem_addr(smem);
+  const uint32_t sB0 = sA0 + S * KS * C::kABytes;
+  uint8_t *bar_area = smem + S * C::kStageBytes;
+  const uint32_t bar0 = ptx::smem_addr(bar_area);
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (S + i); };
+  const uint32_t accum_bar = bar0 + 8u * (2 * S);
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 1);
+  const uint32_t recv_bar = bar0 + 8u * (2 * S + 2);
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * S + 3));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * S + 3) + 4);
+  // Receive buffer, reusing the stage ring once every CTA of the cluster has
+  // finished its main loop: recv[t][rl] holds split t's partial of owned row rl
+  // (256 fp32). Unit c4 of a row sits at ((c4 ^ (rl & 7)) * 16) so that the
+  // row-wise writes and the column-wise reads are free of bank conflicts.
+  const uint32_t red0 = sA0;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = ptx::cluster_ctarank();
+  const int csize = static_cast<int>(ptx::cluster_nctarank());
+  const int member = PAIR ? static_cast<int>(crank & 1) : 0;
+  const int split = PAIR ? static_cast<int>(crank >> 1) : static_cast<int>(crank);
+  const int nsplit = PAIR ? csize / 2 : csize;
+  const uint32_t lead = PAIR ? (crank & ~1u) : crank;  // CTA that issues this pair's MMAs
+  const bool issuer = !PAIR || member == 0;
+  const int tile = blockIdx.x / csize;
+
+  const int pi = find_problem(p, tile);
+  const GemmProblem &pr = p.prob[pi];
+  const int local = tile - pr.tile_begin;
+  const int mt = local % pr.m_tiles;
+  const int nt = local / pr.m_tiles;
+  int ns = 0;
+  for (int q = 0; q < pr.seg_count; ++q) ns += (p.seg[pr.seg_begin + q].k_tiles + KS - 1) / KS;
+  const int k_begin = (split * ns) / nsplit;
+  const int k_end = ((split + 1) * ns) / nsplit;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(full_bar(i), 1);
+      ptx::mbar_init(empty_bar(i), 1);
+    }
+    ptx::mbar_init(accum_bar, 1);
+    ptx::mbar_init(drain_bar, 1);
+    ptx::mbar_init(recv_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int q = 0; q < pr.seg_count; ++q) {
+      const GemmSeg &sg = p.seg[pr.seg_begin + q];
+      ptx::prefetch_tensormap(&p.maps[sg.a_map]);
+      ptx::prefetch_tensormap(&p.maps[sg.b_map]);
+      if (EPI == kEpiSwiGLU) ptx::prefetch_tensormap(&p.maps[sg.b2_map]);
+    }
+  }
+  if (warp == 1) {
+    if constexpr (PAIR)
+      ptx::tmem_alloc_pair(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    else
+      ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    if constexpr (PAIR)
+      ptx::tmem_relinquish_pair();
+    else
+      ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // position (segment, stage within segment) of global stage k_begin
+      int seg = 0, kt = k_begin;
+      while (seg < pr.seg_count) {
+        const int n = (p.seg[pr.seg_begin + seg].k_tiles + KS - 1) / KS;
+        if (kt < n) break;
+        kt -= n;
+        ++seg;
+      }
+      for (int kb = 0; kb < k_end - k_begin; ++kb) {
+        const int st = kb % S;
+        const uint32_t ph = (kb / S) & 1;
+        if (*abort_flag) break;
+        if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
+          record(p.status, kDevTimeoutProducer);
+          *abort_flag = 1;
+          break;
+        }
+        const GemmSeg &sg = p.seg[pr.seg_begin + seg];
+        if (issuer) ptx::mbar_arrive_expect_tx(full_bar(st), (PAIR ? 2 : 1) * C::kStageBytes);
+        const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(st), lead) : full_bar(st);
+        const int a_row = PAIR ? mt * 256 + member * 128 : mt * 128;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          const int x = (kt * KS + j) * BK;  // past the segment's K: zero fill
+          const uint32_t da = sA0 + (st * KS + j) * C::kABytes;
+          const uint32_t db = sB0 + (st * KS + j) * C::kBBytes;
+          if constexpr (PAIR) {
+            ptx::tma_load_2d_pair(da, &p.maps[sg.a_map], x, a_row, fb);
+            if (EPI == kEpiSwiGLU)
+              ptx::tma_load_2d_pair(db, &p.maps[member == 0 ? sg.b_map : sg.b2_map], x, nt * 128, fb);
+            else
+              ptx::tma_load_2d_pair(db, &p.maps[sg.b_map], x, nt * BN + member * 128, fb);
+          } else {
+            ptx::tma_load_2d(da, &p.maps[sg.a_map], x, a_row, fb);
+            if (EPI == kEpiSwiGLU) {
+              ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * 128, fb);
+              ptx::tma_load_2d(db + 128 * 128, &p.maps[sg.b2_map], x, nt * 128, fb);
+            } else {
+              ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * BN, fb);
+            }
+          }
+        }
+        if (++kt == (sg.k_tiles + KS - 1) / KS) {
+          kt = 0;
+          ++seg;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && issuer) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 256 : 128, BN);
+      const uint16_t mask = static_cast<uint16_t>(3u << lead);
+      for (int kb = 0; kb < k_end - k_begin; ++kb) {
+        const int st = kb % S;
+        const uint32_t ph = (kb / S) & 1;
+        if (*abort_flag) break;
+        if (!ptx::mbar_wait(full_bar(st), ph, p.wait_ns)) {
+          record(p.status, kDevTimeoutMma);
+          *abort_flag = 1;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+          const uint64_t ad = ptx::smem_desc_sw128(sA0 + (st * KS + j) * C::kABytes);
+          const uint64_t bd = ptx::smem_desc_sw128(sB0 + (st * KS + j) * C::kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint32_t acc = (kb | j | k) != 0 ? 1u : 0u;
+            if constexpr (PAIR)
+              ptx::mma_bf16_pair(tmem_d, ad + 2 * k, bd + 2 * k, idesc, acc);
+            else
+              ptx::mma_bf16(tmem_d, ad + 2 * k, bd + 2 * k, idesc, acc);
+          }
+        }
+        if constexpr (PAIR)
+          ptx::mma_commit_pair_multicast(empty_bar(st), mask);
+        else
+          ptx::mma_commit(empty_bar(st));
+      }
+      if constexpr (PAIR) {
+        ptx::mma_commit_pair_multicast(accum_bar, mask);
+        ptx::mma_commit_pair_multicast(drain_bar, static_cast<uint16_t>(1u << lead));
+      } else {
+        ptx::mma_commit(accum_bar);
+        ptx::mma_commit(drain_bar);
+      }
+      if (!ptx::mbar_wait(drain_bar, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    }
+  } else {
+    const bool ready = ptx::mbar_wait(accum_bar, 0, p.wait_ns);
+    if (!ready && lane == 0) record(p.status, kDevTimeoutEpilogue);
+    if (!__all_sync(0xffffffffu, ready)) {
+      if (lane == 0) *abort_flag = 1;
+    }
+  }
+
+  // Every CTA of the cluster has finished its main loop (and its stage ring is
+  // idle) before any partial is pushed into another CTA's shared memory.
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+
+  const int rows_per = 128 / nsplit;  // rows of this member's half owned by each split
+  if (warp >= 2) {
+    const int q = warp & 3;
+    const int tid = threadIdx.x - 64;
+    if (tid == 0) ptx::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((nsplit - 1) * rows_per * 1024));
+    // push: row r of this CTA's accumulator goes to the split that owns it
+    if (*abort_flag == 0) {
+      const int r = q * 32 + lane;
+      const int owner = r / rows_per;
+      const int rl = r - owner * rows_per;
+      const uint32_t dst_rank = PAIR ? static_cast<uint32_t>(2 * owner + member) : static_cast<uint32_t>(owner);
+      const uint32_t row_off = red0 + static_cast<uint32_t>((split * rows_per + rl) * 1024);
+      const bool local_row = owner == split;
+      const uint32_t rbar = ptx::mapa_shared(recv_bar, dst_rank);
+      const uint32_t tbase = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
+      const bool has_work = k_end > k_begin;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32cols(tbase + c, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c4 = c / 4 + j;
+          const float4 f = has_work ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+          const uint32_t a = row_off + static_cast<uint32_t>((c4 ^ (rl & 7)) * 16);
+          if (local_row)
+            *reinterpret_cast<float4 *>(smem + (a - red0)) = f;
+          else
+            ptx::st_async_f4(ptx::mapa_shared(a, dst_rank), f, rbar);
+        }
+      }
+    }
+    // wait for the other splits' partials of the rows this CTA owns
+    const bool got = ptx::mbar_wait(recv_bar, 0, p.wait_ns);
+    if (!got && lane == 0) record(p.status, kDevTimeoutEpilogue);
+    ptx::named_barrier(1, 128);  // local partial writes of all four epilogue warps
+    if (got && *abort_flag == 0) {
+      // rows [lo, lo + rows_per) of this member's half, summed over splits in order 0..S-1
+      const int lo = split * rows_per;
+      const int row0 = PAIR ? mt * 256 + member * 128 : mt * 128;
+      constexpr int kUnits = (EPI == kEpiSwiGLU) ? 32 : 64;  // output 16-byte units per row
+      const int total = rows_per * kUnits;
+      for (int idx = tid; idx < total; idx += 128) {
+        const int rl = idx / kUnits;
+        const int c4 = idx % kUnits;
+        const int grow = row0 + lo + rl;
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int t = 0; t < nsplit; ++t) {
+          const uint8_t *rowp = smem + (t * rows_per + rl) * 1024;
+          const float4 vg = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (rl & 7)) * 16));
+          if (t == 0) {
+            g = vg;
+          } else {
+            g.x += vg.x; g.y += vg.y; g.z += vg.z; g.w += vg.w;
+          }
+          if (EPI == kEpiSwiGLU) {
+            const float4 vu = *reinterpret_cast<const float4 *>(rowp + (((c4 + 32) ^ (rl & 7)) * 16));
+            if (t == 0) {
+              u = vu;
+            } else {
+              u.x += vu.x; u.y += vu.y; u.z += vu.z; u.w += vu.w;
+            }
+          }
+        }
+        if (grow >= pr.m) continue;
+        const float f[4] = {g.x, g.y, g.z, g.w};
+        if (EPI == kEpiF32) {
+          const int col = nt * BN + c4 * 4;
+          float *dst = static_cast<float *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
+          if (col + 4 <= pr.n) {
+            *reinterpret_cast<float4 *>(dst) = g;
+          } else {
+            for (int e = 0; e < 4; ++e)
+              if (col + e < pr.n) dst[e] = f[e];
+          }
+        } else {
+          float o[4];
+          int col;
+          if (EPI == kEpiSwiGLU) {
+            const float uu[4] = {u.x, u.y, u.z, u.w};
+            for (int e = 0; e < 4; ++e) o[e] = silu(f[e]) * uu[e];
+            col = nt * (BN / 2) + c4 * 4;
+          } else {
+            for (int e = 0; e < 4; ++e) o[e] = f[e];
+            col = nt * BN + c4 * 4;
+          }
+          __nv_bfloat16 *dst =
+              static_cast<__nv_bfloat16 *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
+          if (col + 4 <= pr.n) {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(o[2], o[3]);
+            uint2 w;
+            memcpy(&w.x, &h0, 4);
+            memcpy(&w.y, &h1, 4);
+            *reinterpret_cast<uint2 *>(dst) = w;
+          } else {
+            for (int e = 0; e < 4; ++e)
+              if (col + e < pr.n) dst[e] = __float2bfloat16_rn(o[e]);
+          }
+        }
+      }
+    }
+  }
+
+  if (*abort_flag && threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem_d, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem_d, kTmemCols);
   }
 }
 
@@ -286,8 +1020,86 @@ tp_status launch_one(const GemmParams &p, cudaStream_t stream) {
       if (dev < 32) configured_mask |= (1 << dev);
     }
   }
-  k_gemm_bf16<BN, EPI><<<p.total_tiles, kThreads, TileCfg<BN>::kSmem, stream>>>(p);
+  const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+  k_gemm_bf16<BN, EPI><<<grid, kThreads, TileCfg<BN>::kSmem, stream>>>(p);
   e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_fail(e);
+}
+
+template <int EPI, int KSUB>
+tp_status launch_pair_ks(const GemmParams &p, cudaStream_t stream) {
+  static int configured_mask = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 32 || !(configured_mask & (1 << dev))) {
+      e = cudaFuncSetAttribute(k_gemm_bf16_pair<EPI, KSUB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PairCfg<KSUB>::kSmem);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (dev < 32) configured_mask |= (1 << dev);
+    }
+  }
+  const int pairs_max = num_sms() / 2;
+  const int pairs = p.total_tiles < pairs_max ? p.total_tiles : pairs_max;
+  k_gemm_bf16_pair<EPI, KSUB><<<2 * pairs, kThreads, PairCfg<KSUB>::kSmem, stream>>>(p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_fail(e);
+}
+
+// 64-wide k-tiles per pipeline stage of the pair kernel (TPGQA_KSUB=2|3 overrides).
+// Two (three 64 KB stages) measured faster than three (two 96 KB stages): the
+// TMA unit delivers more bytes per clock with more boxes per barrier phase, but
+// two stages leave the loads and the MMAs too little overlap.
+int pair_ksub() {
+  static const int k = [] {
+    const char *e = getenv("TPGQA_KSUB");
+    const int v = e ? atoi(e) : 2;
+    return (v == 2 || v == 3) ? v : 2;
+  }();
+  return k;
+}
+
+template <int EPI>
+tp_status launch_pair(const GemmParams &p, cudaStream_t stream) {
+  return pair_ksub() == 2 ? launch_pair_ks<EPI, 2>(p, stream) : launch_pair_ks<EPI, 3>(p, stream);
+}
+
+template <bool PAIR, int EPI>
+tp_status launch_splitk(const GemmParams &p, cudaStream_t stream) {
+  using C = SplitCfg<PAIR>;
+  static int configured_mask = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 32 || !(configured_mask & (1 << dev))) {
+      e = cudaFuncSetAttribute(k_gemm_bf16_splitk<PAIR, EPI>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (dev < 32) configured_mask |= (1 << dev);
+    }
+  }
+  const int csize = (PAIR ? 2 : 1) * p.split;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(p.total_tiles * csize), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_gemm_bf16_splitk<PAIR, EPI>, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
@@ -325,10 +1137,11 @@ bool GemmBuilder::add_problem(int m, int n, void *out, long long ldc, const int 
                               const int *b_maps, const int *b2_maps, const long long *ks, int nseg) {
   if (n_probs >= kMaxProblems || n_segs + nseg > kMaxSegs) return false;
   const int out_cols = (epi == kEpiSwiGLU) ? bn / 2 : bn;
+  const int tile_m = pair ? 2 * BM : BM;
   GemmProblem &pr = p.prob[n_probs];
   pr.m = m;
   pr.n = n;
-  pr.m_tiles = (m + BM - 1) / BM;
+  pr.m_tiles = (m + tile_m - 1) / tile_m;
   pr.n_tiles = (n + out_cols - 1) / out_cols;
   pr.tile_begin = p.total_tiles;
   pr.seg_begin = n_segs;
@@ -350,12 +1163,48 @@ bool GemmBuilder::add_problem(int m, int n, void *out, long long ldc, const int 
 
 tp_status GemmBuilder::launch(cudaStream_t stream) {
   p.num_problems = n_probs;
+  p.n_maps_used = n_maps;
   if (p.total_tiles == 0) return TP_OK;
   DevCtx ctx;
   cudaError_t e = get_dev_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e);
   p.status = ctx.status;
   p.wait_ns = ctx.wait_ns;
+  // L2 prefetch depth of B tiles in k-blocks (TPGQA_PREFETCH overrides).
+  static const int prefetch = [] {
+    const char *e = getenv("TPGQA_PREFETCH");
+    return e ? atoi(e) : 8;
+  }();
+  p.prefetch = prefetch;
+  if (split == 0 && bn == 256) {
+    // fewest k-stages of any problem decides how far K can be split
+    const int ksub = pair ? 2 : 1;
+    long long min_stages = -1;
+    for (int i = 0; i < n_probs; ++i) {
+      long long st = 0;
+      for (int q = 0; q < p.prob[i].seg_count; ++q)
+        st += (p.seg[p.prob[i].seg_begin + q].k_tiles + ksub - 1) / ksub;
+      if (min_stages < 0 || st < min_stages) min_stages = st;
+    }
+    split = choose_split(p.total_tiles, pair, min_stages < 0 ? 0 : min_stages);
+  }
+  if (split < 1) split = 1;
+  p.split = split;
+  if (split > 1) {
+    if (pair) {
+      if (epi == kEpiF32) return launch_splitk<true, kEpiF32>(p, stream);
+      if (epi == kEpiBF16) return launch_splitk<true, kEpiBF16>(p, stream);
+      return launch_splitk<true, kEpiSwiGLU>(p, stream);
+    }
+    if (epi == kEpiF32) return launch_splitk<false, kEpiF32>(p, stream);
+    if (epi == kEpiBF16) return launch_splitk<false, kEpiBF16>(p, stream);
+    return launch_splitk<false, kEpiSwiGLU>(p, stream);
+  }
+  if (pair) {
+    if (epi == kEpiF32) return launch_pair<kEpiF32>(p, stream);
+    if (epi == kEpiBF16) return launch_pair<kEpiBF16>(p, stream);
+    return launch_pair<kEpiSwiGLU>(p, stream);
+  }
   if (bn == 256) {
     if (epi == kEpiF32) return launch_one<256, kEpiF32>(p, stream);
     if (epi == kEpiBF16) return launch_one<256, kEpiBF16>(p, stream);
@@ -366,12 +1215,48 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   return launch_one<128, kEpiSwiGLU>(p, stream);
 }
 
+bool choose_pair(long long rows) {
+  // TPGQA_PAIR=0|1 forces the single-CTA / SM-pair kernel (tuning override).
+  static const int forced = [] {
+    const char *e = getenv("TPGQA_PAIR");
+    return e ? atoi(e) : -1;
+  }();
+  if (forced == 0 || forced == 1) return forced == 1;
+  // Pairs compute 256-row tiles; at 128 rows or fewer half of every pair MMA
+  // would be padding, so the single-CTA kernel runs those.
+  return rows > 128;
+}
+
+int choose_split(long long tiles, bool pair, long long stages_per_tile) {
+  // TPGQA_SPLIT=n forces the split factor (tuning override; 1 disables).
+  static const int forced = [] {
+    const char *e = getenv("TPGQA_SPLIT");
+    return e ? atoi(e) : 0;
+  }();
+  const int per_tile = pair ? 2 : 1;
+  const int max_split = 8 / per_tile;  // portable cluster size limit
+  if (forced >= 1) return forced <= max_split ? forced : max_split;
+  const long long sms = num_sms();
+  int s = 1;
+  // Double the split while the grid still fits in one wave and each split keeps
+  // at least four k-stages to pipeline.
+  while (2 * s <= max_split && tiles * per_tile * 2 * s <= sms && stages_per_tile >= 8LL * s) s *= 2;
+  return s;
+}
+
 int choose_bn(long long tiles_256, long long tiles_128, int epi) {
   (void)tiles_128;
   (void)epi;
-  // Wide tiles halve the A re-reads; fall back to narrow ones when the wide
-  // grid would leave most SMs idle.
-  return tiles_256 >= num_sms() ? 256 : 128;
+  // TPGQA_BN=128|256 forces the tile width (tuning override).
+  static const int forced = [] {
+    const char *e = getenv("TPGQA_BN");
+    return e ? atoi(e) : 0;
+  }();
+  if (forced == 128 || forced == 256) return forced;
+  // 128-column tiles need twice the operand bytes per MMA flop and starve the
+  // tensor pipe; problems with few 256-column tiles are split along K instead.
+  (void)tiles_256;
+  return 256;
 }
 
 }  // namespace tpgqa

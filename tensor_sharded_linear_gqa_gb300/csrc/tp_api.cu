@@ -134,12 +134,14 @@ tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, c
   GemmBuilder b;
   b.epi = epi;
   b.bn = choose_bn(t256, t128, epi);
+  b.pair = choose_pair(T);
+  if (b.pair) b.bn = 256;
   tp_status err = TP_OK;
   const int am = b.add_map(x.ptr, T, K, x.ld, 128, &err);
   if (am < 0) return err;
   for (int32_t r = 0; r < nb; ++r) {
     if (w[r].rows == 0) continue;
-    const int bm = b.add_map(w[r].ptr, w[r].rows, K, w[r].ld, b.bn, &err);
+    const int bm = b.add_map(w[r].ptr, w[r].rows, K, w[r].ld, b.pair ? 128 : b.bn, &err);
     if (bm < 0) return err;
     const long long ks = K;
     if (!b.add_problem(static_cast<int>(T), static_cast<int>(w[r].rows), outs[r].ptr, outs[r].ld,
@@ -158,13 +160,15 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
   GemmBuilder b;
   b.epi = kEpiF32;
   b.bn = choose_bn(probs * mt * ((nout + 255) / 256), probs * mt * ((nout + 127) / 128), kEpiF32);
+  b.pair = choose_pair(T);
+  if (b.pair) b.bn = 256;
   tp_status err = TP_OK;
   std::vector<int> am(n), bm(n);
   std::vector<long long> ks(n);
   for (int32_t r = 0; r < n; ++r) {
     am[r] = b.add_map(x[r].ptr, T, x[r].cols, x[r].ld, 128, &err);
     if (am[r] < 0) return err;
-    bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, b.bn, &err);
+    bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, b.pair ? 128 : b.bn, &err);
     if (bm[r] < 0) return err;
     ks[r] = x[r].cols;
   }
@@ -522,6 +526,8 @@ tp_status launch_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *
   b.epi = kEpiSwiGLU;
   const long long mt = (T + 127) / 128;
   b.bn = choose_bn(n * mt * ((Fr + 127) / 128), n * mt * ((Fr + 63) / 64), kEpiSwiGLU);
+  b.pair = choose_pair(T);
+  if (b.pair) b.bn = 256;
   tp_status err = TP_OK;
   const int am = b.add_map(x->ptr, T, D, x->ld, 128, &err);
   if (am < 0) return err;

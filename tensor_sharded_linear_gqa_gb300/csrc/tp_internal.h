@@ -77,6 +77,9 @@ struct GemmParams {
   GemmSeg seg[kMaxSegs];
   int num_problems;
   int total_tiles;
+  int n_maps_used;
+  int prefetch;  // L2 prefetch distance of B tiles, in k-blocks (0 = none)
+  int split;     // split-K factor of the cluster kernel (1 = persistent kernels)
   int *status;
   long long wait_ns;
 };
@@ -87,6 +90,9 @@ struct GemmBuilder {
   int n_maps = 0, n_probs = 0, n_segs = 0;
   int bn = 256;       // CTA tile width in accumulator columns (128 or 256)
   int epi = kEpiF32;
+  bool pair = false;  // SM-pair kernel: 256 x 256 tiles, cta_group::2 (bn must be 256)
+  int split = 0;      // 0: chosen at launch; >1: split-K over a cluster, reduced in fixed
+                      // order through DSMEM; 1: the persistent kernels
   GemmBuilder();
   // Tensor map of a bf16 [rows x k] matrix with row pitch ld (elements), boxes
   // of 64 x box_rows, 128-byte swizzle. Returns the map index or -1.
@@ -101,6 +107,11 @@ struct GemmBuilder {
 
 // Picks the tile width for a set of problems with these output shapes.
 int choose_bn(long long total_tiles_256, long long total_tiles_128, int epi);
+// Whether to run the SM-pair kernel for problems of this many rows.
+bool choose_pair(long long rows);
+// Split-K factor for `tiles` output tiles of `stages_per_tile` k-stages each
+// (1 = no split).
+int choose_split(long long tiles, bool pair, long long stages_per_tile);
 
 // ---------------------------------------------------------------------------
 // Exact fp32 SIMT grouped GEMM, C = A * B^T with per-problem K segments.
