@@ -39,7 +39,8 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default: about one second of GPU time for the workload)")
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="mlp_tp2_t512")
@@ -245,6 +246,95 @@ def cpu_baseline(w, workload: str, seconds: float) -> dict:
 
 
 # ---- native arm ----------------------------------------------------------------------
+class DeviceSet:
+    """One copy of a workload's inputs, weights and outputs in HBM, sharded per the plan,
+    with the step's C calls marshalled once."""
+
+    def __init__(self, tp, torch, w, data, plan, shards, dev, sptr, mode):
+        import numpy as np
+        n, T = w["tp"], w["T"]
+        D = w["hidden"]
+        self.keep = []
+
+        def to_dev(bits):
+            t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+            self.keep.append(t)
+            return t
+
+        def rng(r, name):
+            return slice(*shards[r]["ranges"][name])
+
+        self.calls = []  # (phase name, callable)
+        combine_ring = {"ring": tp.TP_RING_STEPS, "ring_fused": tp.TP_RING_FUSED}.get(mode)
+        self.x = to_dev(data["x"])
+        self.e2e = {}
+        if w["kind"] in ("attn", "layer"):
+            hd = w["head_dim"]
+            rep = shards[0]["kv_replicated"]
+            nkv = 1 if rep else n
+            wq, wk, wv, wo = (to_dev(data[k]) for k in ("wq", "wk", "wv", "wo"))
+            self.a = to_dev(data["a"])
+            q_w = [wq[rng(r, "q_proj")] for r in range(n)]
+            k_w = [wk[rng(r, "k_proj")] for r in range(nkv)]
+            v_w = [wv[rng(r, "v_proj")] for r in range(nkv)]
+            a_r = [self.a[:, rng(r, "o_proj")] for r in range(n)]
+            o_w = [wo[:, rng(r, "o_proj")] for r in range(n)]
+            q = [torch.empty((T, t.shape[0]), dtype=torch.bfloat16, device=dev) for t in q_w]
+            k = [torch.empty((T, t.shape[0]), dtype=torch.bfloat16, device=dev) for t in k_w]
+            v = [torch.empty((T, t.shape[0]), dtype=torch.bfloat16, device=dev) for t in v_w]
+            yo = [torch.empty((T, D), device=dev) for _ in range(1 if mode == "fused" else n)]
+            self.keep += q + k + v + yo
+            self.calls.append(("qkv", ("tp_qkv_proj", tp.arr([self.x]), tp.arr(q_w), tp.arr(k_w), tp.arr(v_w),
+                                       tp.arr(q), tp.arr(k), tp.arr(v))))
+            self.calls.append(("o_proj", tp.Prepared(
+                "tp_row_linear", n, tp.arr(a_r), tp.arr(o_w), tp.arr(yo),
+                tp.TP_COMBINE_FUSED if mode == "fused" else tp.TP_COMBINE_NONE, sptr)))
+            if combine_ring is not None and n > 1:
+                self.calls.append(("combine_o", tp.Prepared("tp_allreduce_ring", n, tp.arr(yo), combine_ring, sptr)))
+            self.e2e["attn"] = (q_w, k_w, v_w, q, k, v, a_r, o_w, yo)
+        if w["kind"] in ("mlp", "layer"):
+            F = w["ffn"]
+            Fr = F // n
+            wg, wu, wd = (to_dev(data[k]) for k in ("wg", "wu", "wd"))
+            g = [wg[rng(r, "gate_proj")] for r in range(n)]
+            u = [wu[rng(r, "up_proj")] for r in range(n)]
+            dn = [wd[:, rng(r, "down_proj")] for r in range(n)]
+            hbuf = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
+            h = [hbuf[:, r * Fr:(r + 1) * Fr] for r in range(n)]
+            ym = [torch.empty((T, D), device=dev) for _ in range(1 if mode == "fused" else n)]
+            self.keep += [hbuf] + ym
+            self.calls.append(("gate_up", ("tp_gate_up_swiglu", tp.arr([self.x]), tp.arr(g), tp.arr(u),
+                                           tp.arr(h))))
+            self.calls.append(("down", tp.Prepared(
+                "tp_row_linear", n, tp.arr(h), tp.arr(dn), tp.arr(ym),
+                tp.TP_COMBINE_FUSED if mode == "fused" else tp.TP_COMBINE_NONE, sptr)))
+            if combine_ring is not None and n > 1:
+                self.calls.append(("combine_mlp", tp.Prepared("tp_allreduce_ring", n, tp.arr(ym), combine_ring,
+                                                             sptr)))
+            self.e2e["mlp"] = (g, u, dn, ym)
+
+
+def phase_costs(w, mode):
+    """Algorithmic flops and HBM bytes of every phase of one step (weights counted once;
+    a replicated K/V projection is computed once)."""
+    n, T, D = w["tp"], w["T"], w["hidden"]
+    out = {}
+    part = T * D * 4
+    nparts = 1 if mode == "fused" else n
+    if w["kind"] in ("attn", "layer"):
+        hd, hq, hkv = w["head_dim"], w["q_heads"], w["kv_heads"]
+        cols = (hq + 2 * hkv) * hd
+        out["qkv"] = (2.0 * T * D * cols, cols * D * 2 + T * D * 2 + T * cols * 2)
+        out["o_proj"] = (2.0 * T * hq * hd * D, D * hq * hd * 2 + T * hq * hd * 2 + nparts * part)
+        out["combine_o"] = (0.0, ring_bytes(mode, n, part))
+    if w["kind"] in ("mlp", "layer"):
+        F = w["ffn"]
+        out["gate_up"] = (4.0 * T * D * F, 2 * F * D * 2 + T * D * 2 + T * F * 2)
+        out["down"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + nparts * part)
+        out["combine_mlp"] = (0.0, ring_bytes(mode, n, part))
+    return out
+
+
 def run_native(args):
     import numpy as np
     import torch
@@ -256,67 +346,38 @@ def run_native(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = inputs.WORKLOADS[args.workload]
-    if w["kind"] != "mlp":
-        raise SystemExit("bench.py times the MLP block workloads; see --workload")
-    n, T, D, F = w["tp"], w["T"], w["hidden"], w["ffn"]
-    Fr = F // n
+    if w["kind"] == "linear_fp32":
+        raise SystemExit("bench.py times the bf16 block workloads")
+    n, T, D = w["tp"], w["T"], w["hidden"]
     mode = args.combine
-    combine = COMBINE_NAMES[mode]
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
-
-    # -- inputs: one seeded host draw, copied into R device sets ---------------------------
-    data = inputs.make_bf16_inputs(w)
-
-    def to_dev(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    set_bytes = (2 * F * D + D * F) * 2 + T * D * 2 + T * F * 2 + n * T * D * 4
-    R = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
-    plan0 = tp.tp_plan_create(n, D, 8 * n, 8, 128, F)
+    plan_args = (n, D, w.get("q_heads", 8 * n), w.get("kv_heads", 8), w.get("head_dim", 128),
+                 w.get("ffn", 8 * n))
+    plan0 = tp.tp_plan_create(*plan_args)
     shards = [tp.tp_plan_query_rank(plan0, r) for r in range(n)]
-    sets = []
-    for i in range(R):
-        x = to_dev(data["x"])
-        wg, wu, wd = to_dev(data["wg"]), to_dev(data["wu"]), to_dev(data["wd"])
-        g = [wg[slice(*shards[r]["ranges"]["gate_proj"])] for r in range(n)]
-        u = [wu[slice(*shards[r]["ranges"]["up_proj"])] for r in range(n)]
-        dn = [wd[:, slice(*shards[r]["ranges"]["down_proj"])] for r in range(n)]
-        hbuf = torch.empty((T, F), dtype=torch.bfloat16, device=dev)
-        h = [hbuf[:, r * Fr:(r + 1) * Fr] for r in range(n)]
-        ys = [torch.empty((T, D), dtype=torch.float32, device=dev)
-              for _ in range(1 if mode == "fused" else n)]
-        s = {"x": x, "keep": (wg, wu, wd, hbuf), "g": g, "u": u, "d": dn, "h": h, "y": ys}
-        s["gate_up"] = ("tp_gate_up_swiglu", tp.arr([x]), tp.arr(g), tp.arr(u), tp.arr(h))
-        if mode == "fused":
-            s["down"] = tp.Prepared("tp_row_linear", n, tp.arr(h), tp.arr(dn), tp.arr(ys),
-                                    tp.TP_COMBINE_FUSED, sptr)
-            s["ring"] = None
-        else:
-            s["down"] = tp.Prepared("tp_row_linear", n, tp.arr(h), tp.arr(dn), tp.arr(ys),
-                                    tp.TP_COMBINE_NONE, sptr)
-            s["ring"] = tp.Prepared("tp_allreduce_ring", n, tp.arr(ys),
-                                    tp.TP_RING_STEPS if mode == "ring" else tp.TP_RING_FUSED, sptr)
-        sets.append(s)
+
+    data = inputs.make_bf16_inputs(w)
+    costs = phase_costs(w, mode)
+    set_bytes = sum(b for (_f, b) in costs.values() if b) + T * D * 2
+    R = max(1, -(-2 * L2_BYTES // set_bytes) + (1 if set_bytes < 2 * L2_BYTES else 0))
+    sets = [DeviceSet(tp, torch, w, data, plan0, shards, dev, sptr, mode) for _ in range(R)]
+    names = [nm for (nm, _c) in sets[0].calls]
 
     def step(s, ev=None):
-        # a1: the shard plan (host), then the device path of the block
-        plan = tp.tp_plan_create(n, D, 8 * n, 8, 128, F)
-        name, xa, ga, ua, ha = s["gate_up"]
+        # a1: the shard plan (host), then every device phase of the step in order
+        plan = tp.tp_plan_create(*plan_args)
+        for i, (name, call) in enumerate(s.calls):
+            if ev:
+                ev[i].record(stream)
+            if isinstance(call, tuple):  # plan-bound call: marshal the fresh plan handle
+                st = tp.raw_status(call[0], plan.handle, *call[1:], sptr)
+                if st != tp.TP_OK:
+                    raise tp.TPError(st, call[0])
+            else:
+                call()
         if ev:
-            ev[0].record(stream)
-        st = tp.raw_status(name, plan.handle, xa, ga, ua, ha, sptr)
-        if st != tp.TP_OK:
-            raise tp.TPError(st, name)
-        if ev:
-            ev[1].record(stream)
-        s["down"]()
-        if ev:
-            ev[2].record(stream)
-        if s["ring"] is not None:
-            s["ring"]()
-        if ev:
-            ev[3].record(stream)
+            ev[len(s.calls)].record(stream)
         tp.tp_plan_destroy(plan)
 
     for i in range(args.warmup):
@@ -327,7 +388,8 @@ def run_native(args):
         raise SystemExit(f"device status {word:#x} after warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    nev = len(names) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     out_dir = os.path.join(ROOT, "gpurun_out")
     if not os.path.isdir(out_dir):
@@ -347,84 +409,115 @@ def run_native(args):
     if st != tp.TP_OK:
         raise SystemExit(f"device status {word:#x} after the timed region")
     total_ms = t_start.elapsed_time(t_end)
-    gate_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    down_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    ring_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    phase_ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, nm in enumerate(names)}
+    step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs)
     max_ms = dist_max(total_ms, world)
 
-    fl = mlp_flops(w)
-    value = world * fl["total"] * K / (max_ms / 1e3) / 1e12
+    flops_step = sum(f for (f, _b) in costs.values())
+    value = world * flops_step * K / (max_ms / 1e3) / 1e12
     peaks, peak_src = load_peaks()
-    gate_mean_s = statistics.mean(gate_ms) / 1e3
-    achieved = fl["gate_up"] / gate_mean_s / 1e12
-    part_bytes = T * D * 4
-    rb = ring_bytes(mode, n, part_bytes)
-    ring_mean_s = statistics.mean(ring_ms) / 1e3
-    combine_gbs = rb / ring_mean_s / 1e9 if rb and ring_mean_s > 0 else None
 
-    # -- end to end through the public block call with host buffers ------------------------
+    # roofline of the dominant kernel: the gate/up GEMM where there is an MLP, else q/k/v
+    rk = "gate_up" if "gate_up" in phase_ms else "qkv"
+    rf, rb = costs[rk]
+    r_s = phase_ms[rk] / 1e3
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if rf / rb >= ridge:
+        roof = {"kernel": f"k_gemm_bf16* ({rk})", "bound": "tensor", "achieved": round(rf / r_s / 1e12, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(rf / r_s / 1e12 / peaks["bf16_tflops"], 4),
+                "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic_flops_per_launch": rf}
+    else:
+        roof = {"kernel": f"k_gemm_bf16* ({rk})", "bound": "hbm", "achieved": round(rb / r_s / 1e9, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(rb / r_s / 1e9 / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": rb}
+    roof["traffic"] = committed_traffic(args.workload) if rk == "gate_up" else None
+
+    comb = {}
+    for nm in names:
+        if nm.startswith("combine"):
+            b = costs[nm][1]
+            gbs = b / (phase_ms[nm] / 1e3) / 1e9 if phase_ms[nm] > 0 else None
+            comb[nm] = {"gbs": round(gbs, 1), "bytes_per_step": b,
+                        "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+
+    # -- end to end through the public block calls with host buffers ---------------------
+    s0 = sets[0]
     xh = torch.from_numpy(np.ascontiguousarray(data["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    yh = torch.empty((T, D), dtype=torch.float32).pin_memory()
-    ws = torch.empty(tp.tp_mlp_block_workspace_size(plan0, T), dtype=torch.uint8, device=dev)
-    es = sets[0]
-    for i in range(3 + args.e2e_steps):
-        if i == 3:
-            torch.cuda.synchronize(dev)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        es["x"].copy_(xh, non_blocking=True)
-        tp.tp_mlp_block(plan0, es["x"], es["g"], es["u"], es["d"], es["y"], combine, ws, stream=sptr)
-        yh.copy_(es["y"][0], non_blocking=True)
+    ah = (torch.from_numpy(np.ascontiguousarray(data["a"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+          if "a" in data else None)
+    outs_h = []
+    h2d = xh.numel() * 2 + (ah.numel() * 2 if ah is not None else 0)
+    d2h = 0
+    if "attn" in s0.e2e:
+        outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
+        d2h += T * D * 4
+    if "mlp" in s0.e2e:
+        outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
+        d2h += T * D * 4
+        ws = torch.empty(tp.tp_mlp_block_workspace_size(plan0, T), dtype=torch.uint8, device=dev)
+    combine_id = COMBINE_NAMES[mode]
+
+    def e2e_step():
+        s0.x.copy_(xh, non_blocking=True)
+        j = 0
+        if "attn" in s0.e2e:
+            s0.a.copy_(ah, non_blocking=True)
+            q_w, k_w, v_w, q, k, v, a_r, o_w, yo = s0.e2e["attn"]
+            tp.tp_attn_proj(plan0, s0.x, q_w, k_w, v_w, q, k, v, a_r, o_w, yo, combine_id, stream=sptr)
+            outs_h[j].copy_(yo[0], non_blocking=True)
+            j += 1
+        if "mlp" in s0.e2e:
+            g, u, dn, ym = s0.e2e["mlp"]
+            tp.tp_mlp_block(plan0, s0.x, g, u, dn, ym, combine_id, ws, stream=sptr)
+            outs_h[j].copy_(ym[0], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = dist_max(e0.elapsed_time(e1), world)
-    e2e_value = world * fl["total"] * args.e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_value = world * flops_step * args.e2e_steps / (e2e_ms / 1e3) / 1e12
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w["kind"] == "mlp":
         try:
             cpu = cpu_baseline(w, args.workload, args.cpu_seconds)
         except Exception as exc:  # reported, not fatal
             cpu = {"error": str(exc)[-300:]}
 
-    traffic = committed_traffic(args.workload)
-    peak = peaks["bf16_tflops"]
+    launches = 0
+    for nm in names:
+        if nm.startswith("combine"):
+            launches += 2 * (n - 1) if mode == "ring" else 1
+        else:
+            launches += 1
+    config = {"workload": args.workload, "tokens": T, "hidden": D, "tp_size": n, "combine": mode,
+              "flops_per_step": flops_step,
+              "l2": (f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2x L2 in total)" if R > 1 else
+                     f"one input set of {set_bytes / 1e6:.1f} MB (> 2x L2)"),
+              "parallelism": f"tp{n} logical ranks on one GPU; replicas across GPUs"}
+    for k in ("ffn", "q_heads", "kv_heads", "head_dim"):
+        if k in w:
+            config[k] = w[k]
     line = {
         "metric": "TP MLP/attn-proj block TFLOP/s and combine GB/s on 1 GB300, % of roofline",
-        "value": round(value, 3),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": round(max_ms / K, 6),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(max_ms / K, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights, rounded to bf16)",
-        "config": {
-            "workload": args.workload, "tokens": T, "hidden": D, "ffn": F, "tp_size": n,
-            "combine": mode, "flops_per_step": fl["total"],
-            "l2": f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2x L2 in total)",
-            "parallelism": f"tp{n} logical ranks on one GPU; replicas across GPUs",
-        },
-        "phases_ms": {"gate_up_swiglu": round(statistics.mean(gate_ms), 5),
-                      "down": round(statistics.mean(down_ms), 5),
-                      "combine": round(statistics.mean(ring_ms), 5),
-                      "step_sum": round(statistics.mean(step_ms), 5)},
-        "combine": {"mode": mode, "gbs": round(combine_gbs, 1) if combine_gbs else None,
-                    "bytes_per_step": rb, "frac_of_hbm": round(combine_gbs / peaks["hbm_gbs"], 4)
-                    if combine_gbs else None, "bus_bytes_per_rank": int(2 * (n - 1) / n * part_bytes)},
-        "roofline": {"kernel": "k_gemm_bf16 (gate/up + SwiGLU epilogue)", "bound": "tensor",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16_tflops (burst)",
-                     "algorithmic_flops_per_launch": fl["gate_up"]},
-        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": T * D * 2, "d2h_bytes_per_step": T * D * 4},
-        "gpu_launches": launches_per_step(mode, n) * K,
+        "config": config,
+        "phases_ms": {**{nm: round(v, 5) for nm, v in phase_ms.items()}, "step_sum": round(step_ms, 5)},
+        "combine": comb,
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches * K,
         "clocks": clk.summary(),
     }
     if cpu is not None:
@@ -469,8 +562,14 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+DEFAULT_STEPS = {"mlp_tp2_t512": 10000, "attn_gqa_tp4_t2048": 3000, "decode_gqa_rep_tp8_t64": 6000,
+                 "prefill_layer_tp8_t4096": 200}
+
+
 def main():
     args = parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS.get(args.workload, 1000) if args.impl == "native" else 20
     if args.impl == "reference":
         run_reference(args)
     else:

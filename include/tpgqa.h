@@ -294,6 +294,19 @@ tp_status tp_mlp_block_static(const tp_plan *plan, const tp_tensor *x, const tp_
 /* Size in bytes of tp_mlp_block_static's fixed scratch array (16 MiB). */
 size_t tp_mlp_block_static_max_bytes(void);
 
+/* Column-parallel q/k/v projections with the GQA rule, as one grouped launch
+ * (the first half of tp_attn_proj; the manual's table puts q/k/v in
+ * ColumnParallel, with K/V replicated when num_kv_heads < tp_size).
+ *  x        : [T x D] bf16.
+ *  w_q[r]   : [(q heads of r) * hd x D] bf16;  q[r]: [T x same] bf16 out.
+ *  w_k, w_v : N tensors when sharded, ONE shared tensor when replicated (computed
+ *             once); k, v outputs likewise (bf16).
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_RANK_FAILED,
+ * TP_ERR_CUDA. */
+tp_status tp_qkv_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_q,
+                      const tp_tensor *w_k, const tp_tensor *w_v, tp_tensor *q, tp_tensor *k,
+                      tp_tensor *v, tp_stream_t stream);
+
 /* Attention projections with GQA sharding.
  *  x        : [T x D] bf16.
  *  w_q[r]   : [(q heads of r) * hd x D] bf16;  q[r]: [T x same] bf16 out.

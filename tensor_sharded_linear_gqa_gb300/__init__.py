@@ -89,6 +89,7 @@ _SIGS = {
                       ctypes.c_size_t, _S], ctypes.c_int),
     "tp_mlp_block_static": ([ctypes.c_void_p, _T, _T, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_mlp_block_static_max_bytes": ([], ctypes.c_size_t),
+    "tp_qkv_proj": ([ctypes.c_void_p, _T, _T, _T, _T, _T, _T, _T, _S], ctypes.c_int),
     "tp_attn_proj": ([ctypes.c_void_p, _T, _T, _T, _T, _T, _T, _T, _T, _T, _T, ctypes.c_int32,
                       _S], ctypes.c_int),
     "tp_status_str": ([ctypes.c_int], ctypes.c_char_p),
@@ -298,6 +299,12 @@ def tp_mlp_block_static(plan: Plan, x, w_gate, w_up, w_down, y, combine: int, st
 
 def tp_mlp_block_static_max_bytes() -> int:
     return int(_lib.tp_mlp_block_static_max_bytes())
+
+
+def tp_qkv_proj(plan: Plan, x, w_q, w_k, w_v, q, k, v, stream=None) -> None:
+    xs = tensor(x)
+    _check(_lib.tp_qkv_proj(plan.handle, ctypes.byref(xs), _arr(w_q), _arr(w_k), _arr(w_v), _arr(q),
+                            _arr(k), _arr(v), _stream(stream)), "tp_qkv_proj")
 
 
 def tp_attn_proj(plan: Plan, x, w_q, w_k, w_v, q, k, v, a, w_o, y, combine: int,

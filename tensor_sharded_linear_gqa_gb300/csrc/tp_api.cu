@@ -607,24 +607,18 @@ extern "C" tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const
   return row_linear_impl(n, h.data(), w_down, y, combine, TP_BF16, s);
 }
 
-extern "C" tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_q,
-                                  const tp_tensor *w_k, const tp_tensor *w_v, tp_tensor *q,
-                                  tp_tensor *k, tp_tensor *v, const tp_tensor *a,
-                                  const tp_tensor *w_o, tp_tensor *y, int32_t combine,
-                                  tp_stream_t stream) {
-  tp_dims d;
-  if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
-  if (!x || !w_q || !w_k || !w_v || !q || !k || !v || !a || !w_o || !y) return TP_ERR_INVALID_ARG;
-  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+namespace {
+
+// Checks x, the q/k/v weights and outputs against the plan; sets T.
+tp_status check_qkv(const tp_dims &d, const tp_rank_shard &s0, const tp_tensor *x, const tp_tensor *w_q,
+                    const tp_tensor *w_k, const tp_tensor *w_v, const tp_tensor *q, const tp_tensor *k,
+                    const tp_tensor *v) {
   const int32_t n = d.tp_size;
   const long long D = d.hidden, hd = d.head_dim, T = x->rows;
   if (!shape_ok(*x) || x->cols != D) return TP_ERR_INVALID_ARG;
   if (x->dtype != TP_BF16) return TP_ERR_DTYPE;
   if (T > 0 && !pitch_ok(*x)) return TP_ERR_ALIGNMENT;
-  tp_rank_shard s0;
-  tp_plan_query_rank(plan, 0, &s0);
-  const bool rep = s0.kv_replicated != 0;
-  const int32_t nkv = rep ? 1 : n;
+  const int32_t nkv = s0.kv_replicated ? 1 : n;
   const long long qcols = (s0.q_head_end - s0.q_head_begin) * hd;
   const long long kvcols = (s0.kv_head_end - s0.kv_head_begin) * hd;
   auto check_w = [&](const tp_tensor &t, long long rows, long long cols) -> tp_status {
@@ -645,13 +639,75 @@ extern "C" tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const
   for (int32_t r = 0; r < n; ++r) {
     if ((st = check_w(w_q[r], qcols, D)) != TP_OK) return st;
     if ((st = check_out(q[r], qcols)) != TP_OK) return st;
-    if ((st = check_w(w_o[r], D, qcols)) != TP_OK) return st;
   }
   for (int32_t r = 0; r < nkv; ++r) {
     if ((st = check_w(w_k[r], kvcols, D)) != TP_OK) return st;
     if ((st = check_w(w_v[r], kvcols, D)) != TP_OK) return st;
     if ((st = check_out(k[r], kvcols)) != TP_OK) return st;
     if ((st = check_out(v[r], kvcols)) != TP_OK) return st;
+  }
+  return TP_OK;
+}
+
+// q/k/v column-parallel as one grouped launch (K/V once when replicated).
+tp_status launch_qkv(const tp_dims &d, const tp_rank_shard &s0, const tp_tensor *x, const tp_tensor *w_q,
+                     const tp_tensor *w_k, const tp_tensor *w_v, const tp_tensor *q, const tp_tensor *k,
+                     const tp_tensor *v, cudaStream_t s) {
+  const int32_t n = d.tp_size;
+  const int32_t nkv = s0.kv_replicated ? 1 : n;
+  std::vector<tp_tensor> ws;
+  std::vector<ColOut> outs;
+  for (int32_t r = 0; r < n; ++r) {
+    ws.push_back(w_q[r]);
+    outs.push_back(ColOut{q[r].ptr, q[r].ld});
+  }
+  for (int32_t r = 0; r < nkv; ++r) {
+    ws.push_back(w_k[r]);
+    outs.push_back(ColOut{k[r].ptr, k[r].ld});
+    ws.push_back(w_v[r]);
+    outs.push_back(ColOut{v[r].ptr, v[r].ld});
+  }
+  return gemm_bf16_column(*x, static_cast<int32_t>(ws.size()), ws.data(), outs.data(), kEpiBF16, s);
+}
+
+}  // namespace
+
+extern "C" tp_status tp_qkv_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_q,
+                                 const tp_tensor *w_k, const tp_tensor *w_v, tp_tensor *q, tp_tensor *k,
+                                 tp_tensor *v, tp_stream_t stream) {
+  tp_dims d;
+  if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
+  if (!x || !w_q || !w_k || !w_v || !q || !k || !v) return TP_ERR_INVALID_ARG;
+  tp_rank_shard s0;
+  tp_plan_query_rank(plan, 0, &s0);
+  tp_status st = check_qkv(d, s0, x, w_q, w_k, w_v, q, k, v);
+  if (st != TP_OK) return st;
+  if ((st = check_health(d.tp_size)) != TP_OK) return st;
+  if (x->rows == 0) return TP_OK;
+  return launch_qkv(d, s0, x, w_q, w_k, w_v, q, k, v, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_q,
+                                  const tp_tensor *w_k, const tp_tensor *w_v, tp_tensor *q,
+                                  tp_tensor *k, tp_tensor *v, const tp_tensor *a,
+                                  const tp_tensor *w_o, tp_tensor *y, int32_t combine,
+                                  tp_stream_t stream) {
+  tp_dims d;
+  if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
+  if (!x || !w_q || !w_k || !w_v || !q || !k || !v || !a || !w_o || !y) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  const int32_t n = d.tp_size;
+  const long long D = d.hidden, hd = d.head_dim, T = x->rows;
+  tp_rank_shard s0;
+  tp_plan_query_rank(plan, 0, &s0);
+  tp_status st = check_qkv(d, s0, x, w_q, w_k, w_v, q, k, v);
+  if (st != TP_OK) return st;
+  const long long qcols = (s0.q_head_end - s0.q_head_begin) * hd;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(w_o[r])) return TP_ERR_INVALID_ARG;
+    if (w_o[r].dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (w_o[r].rows != D || w_o[r].cols != qcols) return TP_ERR_INVALID_ARG;
+    if (!pitch_ok(w_o[r])) return TP_ERR_ALIGNMENT;
   }
   int32_t dt = 0;
   if ((st = check_row_args(n, a, w_o, y, combine, &dt)) != TP_OK) return st;
@@ -660,24 +716,7 @@ extern "C" tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const
   if ((st = check_health(n)) != TP_OK) return st;
   if (T == 0) return TP_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-  // q/k/v column-parallel as one grouped launch (K/V once when replicated).
-  {
-    std::vector<tp_tensor> ws;
-    std::vector<ColOut> outs;
-    for (int32_t r = 0; r < n; ++r) {
-      ws.push_back(w_q[r]);
-      outs.push_back(ColOut{q[r].ptr, q[r].ld});
-    }
-    for (int32_t r = 0; r < nkv; ++r) {
-      ws.push_back(w_k[r]);
-      outs.push_back(ColOut{k[r].ptr, k[r].ld});
-      ws.push_back(w_v[r]);
-      outs.push_back(ColOut{v[r].ptr, v[r].ld});
-    }
-    st = gemm_bf16_column(*x, static_cast<int32_t>(ws.size()), ws.data(), outs.data(), kEpiBF16, s);
-    if (st != TP_OK) return st;
-  }
+  if ((st = launch_qkv(d, s0, x, w_q, w_k, w_v, q, k, v, s)) != TP_OK) return st;
   // o_proj row-parallel + combine.
   return row_linear_impl(n, a, w_o, y, combine, TP_BF16, s);
 }

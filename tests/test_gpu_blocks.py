@@ -176,6 +176,32 @@ def test_decode_replicated_kv_tp8_t64(combine):
         assert_close(host_f64(y), ref["y"][0], BF16_TOL, "MLP Y")
 
 
+@pytest.mark.parametrize("tp_size,hq,hkv", [(4, 8, 4), (8, 16, 2)])
+def test_qkv_proj_matches_oracle(tp_size, hq, hkv):
+    need_gpu()
+    t = torch()
+    w = dict(kind="attn", T=150, hidden=256, q_heads=hq, kv_heads=hkv, head_dim=64, tp=tp_size, seed=31,
+             w_std=0.05)
+    data = inputs.make_bf16_inputs(w)
+    L = Layer(w, data)
+    f = {k: inputs.bf16_bits_to_f64(v) for k, v in data.items()}
+    rep = L.shards[0]["kv_replicated"]
+    nkv = 1 if rep else tp_size
+    wq = [L.dev["wq"][slice(*L.rng(r, "q_proj"))] for r in range(tp_size)]
+    wk = [L.dev["wk"][slice(*L.rng(r, "k_proj"))] for r in range(nkv)]
+    wv = [L.dev["wv"][slice(*L.rng(r, "v_proj"))] for r in range(nkv)]
+    q = [t.full((150, x.shape[0]), float("nan"), dtype=t.bfloat16, device="cuda") for x in wq]
+    k = [t.full((150, x.shape[0]), float("nan"), dtype=t.bfloat16, device="cuda") for x in wk]
+    v = [t.full((150, x.shape[0]), float("nan"), dtype=t.bfloat16, device="cuda") for x in wv]
+    tp.tp_qkv_proj(L.plan, L.x, wq, wk, wv, q, k, v)
+    ref = O.attn_proj_sharded(f["x"], f["wq"], f["wk"], f["wv"], f["a"], f["wo"], _oracle_plan(w), 64)
+    for r in range(tp_size):
+        assert_close(host_f64(q[r]), ref["q"][r], BF16_TOL, f"q[{r}]")
+    for r in range(nkv):
+        assert_close(host_f64(k[r]), ref["k"][r], BF16_TOL, f"k[{r}]")
+        assert_close(host_f64(v[r]), ref["v"][r], BF16_TOL, f"v[{r}]")
+
+
 def test_prefill_layer_tp8_t4096_sampled_rows():
     need_gpu()
     L, f = layer("prefill_layer_tp8_t4096")
