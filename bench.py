@@ -44,7 +44,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="mlp_tp2_t512")
-    p.add_argument("--combine", choices=sorted(COMBINE_NAMES), default="ring")
+    p.add_argument("--combine", choices=sorted(COMBINE_NAMES), default="ring_fused",
+                   help="ring_fused: the ring all-reduce in one pass, bit-identical to ring (N-1 step launches per phase)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -389,7 +390,6 @@ def run_native(args):
 
     K = args.steps
     nev = len(names) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     out_dir = os.path.join(ROOT, "gpurun_out")
     if not os.path.isdir(out_dir):
@@ -401,7 +401,7 @@ def run_native(args):
         torch.cuda.synchronize(dev)
         t_start.record(stream)
         for i in range(K):
-            step(sets[i % R], evs[i])
+            step(sets[i % R])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
@@ -409,9 +409,17 @@ def run_native(args):
     if st != tp.TP_OK:
         raise SystemExit(f"device status {word:#x} after the timed region")
     total_ms = t_start.elapsed_time(t_end)
+    max_ms = dist_max(total_ms, world)
+    # Per-phase breakdown: a second pass of the same steps with CUDA events between
+    # the phases (events between kernels also stop the next kernel's early launch,
+    # so this pass runs slightly slower than the timed region above).
+    P = min(K, 500)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(P)]
+    for i in range(P):
+        step(sets[i % R], evs[i])
+    torch.cuda.synchronize(dev)
     phase_ms = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, nm in enumerate(names)}
     step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs)
-    max_ms = dist_max(total_ms, world)
 
     flops_step = sum(f for (f, _b) in costs.values())
     value = world * flops_step * K / (max_ms / 1e3) / 1e12
@@ -512,7 +520,8 @@ def run_native(args):
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights, rounded to bf16)",
         "config": config,
-        "phases_ms": {**{nm: round(v, 5) for nm, v in phase_ms.items()}, "step_sum": round(step_ms, 5)},
+        "phases_ms": {**{nm: round(v, 5) for nm, v in phase_ms.items()}, "step_sum": round(step_ms, 5),
+                      "pass_steps": P},
         "combine": comb,
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

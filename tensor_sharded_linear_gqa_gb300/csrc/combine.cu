@@ -23,6 +23,11 @@ namespace {
 
 constexpr int kThreads = 256;
 
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void chunk_range(long long size, int n, int c, long long &lo,
                                             long long &hi) {
   lo = (static_cast<long long>(c) * size) / n;
@@ -45,6 +50,8 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
 // One reduce-scatter step; grid.y = sending rank.
 __global__ void __launch_bounds__(kThreads) k_ring_rs_step(RankPtrs b, int n, long long size,
                                                            int step) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int r = blockIdx.y;
   const int c = ((r - 1 - step) % n + n) % n;
   const float *__restrict__ src = b.p[r];
@@ -74,6 +81,8 @@ __global__ void __launch_bounds__(kThreads) k_ring_rs_step(RankPtrs b, int n, lo
 // One all-gather step; grid.y = sending rank.
 __global__ void __launch_bounds__(kThreads) k_ring_ag_step(RankPtrs b, int n, long long size,
                                                            int step) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int r = blockIdx.y;
   const int c = ((r - step) % n + n) % n;
   const float *__restrict__ src = b.p[r];
@@ -106,6 +115,8 @@ __global__ void __launch_bounds__(kThreads) k_ring_ag_step(RankPtrs b, int n, lo
 template <int NT>
 __global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n_rt, long long size,
                                                          int write_all) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int n = NT ? NT : n_rt;
   const int c = blockIdx.y;
   long long lo, hi, vlo, vhi;
@@ -184,6 +195,8 @@ __global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n_rt, l
 
 // In-place all-gather in one pass: chunk c (grid.y) of buffer c to every other buffer.
 __global__ void __launch_bounds__(kThreads) k_ring_ag_fused(RankPtrs b, int n, long long size) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int c = blockIdx.y;
   long long lo, hi, vlo, vhi;
   chunk_range(size, n, c, lo, hi);
@@ -218,6 +231,8 @@ __device__ __forceinline__ void copy_rows(const Copy2D &cp) {
 // grid.y = copy index; each copy moves `rows` rows of `row_bytes` bytes in the
 // widest unit that divides every address, pitch and row length.
 __global__ void __launch_bounds__(kThreads) k_copy_batch(const __grid_constant__ CopyBatch b) {
+  griddep_wait();
+  griddep_launch_dependents();
   const Copy2D &cp = b.c[blockIdx.y];
   const unsigned long long bits = reinterpret_cast<unsigned long long>(cp.src) |
                                   reinterpret_cast<unsigned long long>(cp.dst) |
@@ -263,11 +278,14 @@ __global__ void k_debug_wait(int *status, long long wait_ns) {
   }
 }
 
-// Blocks per grid row: enough threads for about four float4 each (so every
-// thread has several loads in flight), at most four blocks per SM in total.
+// Blocks per grid row: about four float4 per thread when the buffers are large
+// (several loads in flight per thread), one per thread when that would leave SMs
+// idle, at most four blocks per SM in total.
 int blocks_for(long long elems, int ranks_in_grid) {
-  const long long vec_threads = (elems / 4 + 4 * kThreads - 1) / (4 * kThreads);
-  long long cap = static_cast<long long>(num_sms()) * 4 / (ranks_in_grid > 0 ? ranks_in_grid : 1);
+  const long long rows = ranks_in_grid > 0 ? ranks_in_grid : 1;
+  long long vec_threads = (elems / 4 + 4 * kThreads - 1) / (4 * kThreads);
+  if (vec_threads * rows < 2LL * num_sms()) vec_threads = (elems / 4 + kThreads - 1) / kThreads;
+  long long cap = static_cast<long long>(num_sms()) * 4 / rows;
   if (cap < 1) cap = 1;
   long long g = vec_threads < cap ? vec_threads : cap;
   return static_cast<int>(g < 1 ? 1 : g);
@@ -278,36 +296,36 @@ tp_status check_launch() {
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
+tp_status launch_checked(cudaError_t e) {
+  if (e != cudaSuccess) return cuda_fail(e);
+  return check_launch();
+}
+
 }  // namespace
 
 tp_status launch_ring_rs_step(const RankPtrs &b, int n, long long size, int step, cudaStream_t s) {
   const dim3 grid(blocks_for(size / n + 4, n), n);
-  k_ring_rs_step<<<grid, kThreads, 0, s>>>(b, n, size, step);
-  return check_launch();
+  return launch_checked(launch_kernel(k_ring_rs_step, grid, dim3(kThreads), 0, s, 1, b, n, size, step));
 }
 
 tp_status launch_ring_ag_step(const RankPtrs &b, int n, long long size, int step, cudaStream_t s) {
   const dim3 grid(blocks_for(size / n + 4, n), n);
-  k_ring_ag_step<<<grid, kThreads, 0, s>>>(b, n, size, step);
-  return check_launch();
+  return launch_checked(launch_kernel(k_ring_ag_step, grid, dim3(kThreads), 0, s, 1, b, n, size, step));
 }
 
 tp_status launch_ring_fused(const RankPtrs &b, int n, long long size, int write_all,
                             cudaStream_t s) {
   const dim3 grid(blocks_for(size / n + 4, n), n);
-  switch (n) {
-    case 2: k_ring_fused<2><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
-    case 4: k_ring_fused<4><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
-    case 8: k_ring_fused<8><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
-    default: k_ring_fused<0><<<grid, kThreads, 0, s>>>(b, n, size, write_all); break;
-  }
-  return check_launch();
+  void (*k)(RankPtrs, int, long long, int) = n == 2   ? k_ring_fused<2>
+                                            : n == 4 ? k_ring_fused<4>
+                                            : n == 8 ? k_ring_fused<8>
+                                                     : k_ring_fused<0>;
+  return launch_checked(launch_kernel(k, grid, dim3(kThreads), 0, s, 1, b, n, size, write_all));
 }
 
 tp_status launch_ring_ag_fused(const RankPtrs &b, int n, long long size, cudaStream_t s) {
   const dim3 grid(blocks_for(size / n + 4, n), n);
-  k_ring_ag_fused<<<grid, kThreads, 0, s>>>(b, n, size);
-  return check_launch();
+  return launch_checked(launch_kernel(k_ring_ag_fused, grid, dim3(kThreads), 0, s, 1, b, n, size));
 }
 
 tp_status launch_copy_batch(const CopyBatch &b, cudaStream_t s) {
@@ -317,8 +335,8 @@ tp_status launch_copy_batch(const CopyBatch &b, cudaStream_t s) {
   long long gx = static_cast<long long>(num_sms()) * 4 / b.n;
   if (gx < 1) gx = 1;
   if (gx > rows) gx = rows;
-  k_copy_batch<<<dim3(static_cast<unsigned>(gx), b.n), kThreads, 0, s>>>(b);
-  return check_launch();
+  return launch_checked(
+      launch_kernel(k_copy_batch, dim3(static_cast<unsigned>(gx), b.n), dim3(kThreads), 0, s, 1, b));
 }
 
 tp_status launch_debug_wait(cudaStream_t s) {

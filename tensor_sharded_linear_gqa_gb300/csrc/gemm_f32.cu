@@ -13,6 +13,8 @@ constexpr int FBM = 32, FBN = 64, FBK = 32, FTHREADS = 256;
 __global__ void __launch_bounds__(FTHREADS) k_gemm_f32(const __grid_constant__ F32Params p) {
   __shared__ float As[FBK][FBM + 1];
   __shared__ float Bs[FBK][FBN + 1];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tile = blockIdx.x;
   int pi = 0;
@@ -75,8 +77,8 @@ __global__ void __launch_bounds__(FTHREADS) k_gemm_f32(const __grid_constant__ F
 
 tp_status launch_gemm_f32(const F32Params &p, cudaStream_t stream) {
   if (p.total_tiles == 0) return TP_OK;
-  k_gemm_f32<<<p.total_tiles, FTHREADS, 0, stream>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(k_gemm_f32, dim3(p.total_tiles), dim3(FTHREADS), 0, stream, 1, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 

@@ -189,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Prologue done: wait for the previous kernel in the stream, then let the next one launch.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   int issued = 0;  // k-blocks whose loads the producer started (thread 0 only)
   if (warp == 0) {
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
           break;
         }
         const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
-        ptx::mbar_arrive_expect_tx(full_bar(st), C::kStageBytes);
+        ptx::mbar_arrive_expect_tx(full_bar(st), static_cast<uint32_t>(p.a_rows * 128 + C::kBBytes));
         ptx::tma_load_2d(sA0 + st * C::kABytes, &p.maps[sg.a_map], ld.kt * BK, ld.mt * BM,
                          full_bar(st));
         ptx::tma_load_2d(sB0 + st * C::kBBytes, &p.maps[sg.b_map], ld.kt * BK, ld.nt * kBRows,
@@ -446,6 +449,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -663,21 +668,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // memory (DSMEM) and adding in split order 0, 1, ..., S-1. The sum order is
 // fixed, so the result does not depend on timing; no global workspace is used.
 // ---------------------------------------------------------------------------
-template <bool PAIR>
+template <bool PAIR, int BN>
 struct SplitCfg {
   static constexpr int kSub = PAIR ? 2 : 1;  // 64-wide k-tiles per stage
-  static constexpr int kStages = PAIR ? 3 : 4;
   static constexpr int kABytes = 128 * BK * 2;
-  static constexpr int kBRows = PAIR ? 128 : 256;  // B rows per CTA per k-tile
+  static constexpr int kBRows = PAIR ? 128 : BN;  // B rows per CTA per k-tile
   static constexpr int kBBytes = kBRows * BK * 2;
   static constexpr int kStageBytes = kSub * (kABytes + kBBytes);
+  static constexpr int kStages = (6 * 32768) / kStageBytes;  // 192 KB of stages
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
 };
 
-template <bool PAIR, int EPI>
+template <bool PAIR, int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_constant__ GemmParams p) {
-  using C = SplitCfg<PAIR>;
-  constexpr int BN = 256;
+  using C = SplitCfg<PAIR, BN>;
+  static_assert(!PAIR || BN == 256, "SM pairs run 256-column tiles");
   constexpr int KS = C::kSub;
   constexpr int S = C::kStages;
   constexpr uint32_t kTmemCols = BN;
@@ -698,9 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * S + 3) + 4);
   // Receive buffer, reusing the stage ring once every CTA of the cluster has
   // finished its main loop: recv[t][rl] holds split t's partial of owned row rl
-  // (256 fp32). Unit c4 of a row sits at ((c4 ^ (rl & 7)) * 16) so that the
-  // row-wise writes and the column-wise reads are free of bank conflicts.
+  // (BN fp32, kRowBytes). Unit c4 of a row sits at ((c4 ^ (rl & 7)) * 16) so that
+  // the row-wise writes and the column-wise reads are free of bank conflicts.
   const uint32_t red0 = sA0;
+  constexpr int kRowBytes = BN * 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -756,6 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_d = *tmem_slot;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -777,7 +785,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
           break;
         }
         const GemmSeg &sg = p.seg[pr.seg_begin + seg];
-        if (issuer) ptx::mbar_arrive_expect_tx(full_bar(st), (PAIR ? 2 : 1) * C::kStageBytes);
+        if (issuer)
+          ptx::mbar_arrive_expect_tx(full_bar(st), PAIR ? 2 * C::kStageBytes
+                                                        : static_cast<uint32_t>(KS * (p.a_rows * 128 + C::kBBytes)));
         const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(st), lead) : full_bar(st);
         const int a_row = PAIR ? mt * 256 + member * 128 : mt * 128;
 #pragma unroll
@@ -794,8 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
           } else {
             ptx::tma_load_2d(da, &p.maps[sg.a_map], x, a_row, fb);
             if (EPI == kEpiSwiGLU) {
-              ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * 128, fb);
-              ptx::tma_load_2d(db + 128 * 128, &p.maps[sg.b2_map], x, nt * 128, fb);
+              ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * (BN / 2), fb);
+              ptx::tma_load_2d(db + (BN / 2) * 128, &p.maps[sg.b2_map], x, nt * (BN / 2), fb);
             } else {
               ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * BN, fb);
             }
@@ -867,14 +877,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   if (warp >= 2) {
     const int q = warp & 3;
     const int tid = threadIdx.x - 64;
-    if (tid == 0) ptx::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((nsplit - 1) * rows_per * 1024));
+    if (tid == 0)
+      ptx::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((nsplit - 1) * rows_per * kRowBytes));
     // push: row r of this CTA's accumulator goes to the split that owns it
     if (*abort_flag == 0) {
       const int r = q * 32 + lane;
       const int owner = r / rows_per;
       const int rl = r - owner * rows_per;
       const uint32_t dst_rank = PAIR ? static_cast<uint32_t>(2 * owner + member) : static_cast<uint32_t>(owner);
-      const uint32_t row_off = red0 + static_cast<uint32_t>((split * rows_per + rl) * 1024);
+      const uint32_t row_off = red0 + static_cast<uint32_t>((split * rows_per + rl) * kRowBytes);
       const bool local_row = owner == split;
       const uint32_t rbar = ptx::mapa_shared(recv_bar, dst_rank);
       const uint32_t tbase = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
@@ -906,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
       // rows [lo, lo + rows_per) of this member's half, summed over splits in order 0..S-1
       const int lo = split * rows_per;
       const int row0 = PAIR ? mt * 256 + member * 128 : mt * 128;
-      constexpr int kUnits = (EPI == kEpiSwiGLU) ? 32 : 64;  // output 16-byte units per row
+      constexpr int kUnits = (EPI == kEpiSwiGLU) ? BN / 8 : BN / 4;  // output 16-byte units per row
       const int total = rows_per * kUnits;
       for (int idx = tid; idx < total; idx += 128) {
         const int rl = idx / kUnits;
@@ -914,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
         const int grow = row0 + lo + rl;
         float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
         for (int t = 0; t < nsplit; ++t) {
-          const uint8_t *rowp = smem + (t * rows_per + rl) * 1024;
+          const uint8_t *rowp = smem + (t * rows_per + rl) * kRowBytes;
           const float4 vg = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (rl & 7)) * 16));
           if (t == 0) {
             g = vg;
@@ -922,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
             g.x += vg.x; g.y += vg.y; g.z += vg.z; g.w += vg.w;
           }
           if (EPI == kEpiSwiGLU) {
-            const float4 vu = *reinterpret_cast<const float4 *>(rowp + (((c4 + 32) ^ (rl & 7)) * 16));
+            const float4 vu = *reinterpret_cast<const float4 *>(rowp + (((c4 + BN / 8) ^ (rl & 7)) * 16));
             if (t == 0) {
               u = vu;
             } else {
@@ -1021,8 +1032,8 @@ tp_status launch_one(const GemmParams &p, cudaStream_t stream) {
     }
   }
   const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
-  k_gemm_bf16<BN, EPI><<<grid, kThreads, TileCfg<BN>::kSmem, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_kernel(k_gemm_bf16<BN, EPI>, dim3(grid), dim3(kThreads), TileCfg<BN>::kSmem, stream, 1, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
@@ -1044,8 +1055,9 @@ tp_status launch_pair_ks(const GemmParams &p, cudaStream_t stream) {
   }
   const int pairs_max = num_sms() / 2;
   const int pairs = p.total_tiles < pairs_max ? p.total_tiles : pairs_max;
-  k_gemm_bf16_pair<EPI, KSUB><<<2 * pairs, kThreads, PairCfg<KSUB>::kSmem, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_kernel(k_gemm_bf16_pair<EPI, KSUB>, dim3(2 * pairs), dim3(kThreads), PairCfg<KSUB>::kSmem,
+                    stream, 1, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
@@ -1067,9 +1079,9 @@ tp_status launch_pair(const GemmParams &p, cudaStream_t stream) {
   return pair_ksub() == 2 ? launch_pair_ks<EPI, 2>(p, stream) : launch_pair_ks<EPI, 3>(p, stream);
 }
 
-template <bool PAIR, int EPI>
+template <bool PAIR, int EPI, int BN>
 tp_status launch_splitk(const GemmParams &p, cudaStream_t stream) {
-  using C = SplitCfg<PAIR>;
+  using C = SplitCfg<PAIR, BN>;
   static int configured_mask = 0;
   static std::mutex mu;
   int dev = 0;
@@ -1078,27 +1090,15 @@ tp_status launch_splitk(const GemmParams &p, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> g(mu);
     if (dev >= 32 || !(configured_mask & (1 << dev))) {
-      e = cudaFuncSetAttribute(k_gemm_bf16_splitk<PAIR, EPI>,
+      e = cudaFuncSetAttribute(k_gemm_bf16_splitk<PAIR, EPI, BN>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 32) configured_mask |= (1 << dev);
     }
   }
   const int csize = (PAIR ? 2 : 1) * p.split;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(p.total_tiles * csize), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_gemm_bf16_splitk<PAIR, EPI>, p);
+  e = launch_kernel(k_gemm_bf16_splitk<PAIR, EPI, BN>, dim3(static_cast<unsigned>(p.total_tiles * csize)),
+                    dim3(kThreads), C::kSmem, stream, static_cast<unsigned>(csize), p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
@@ -1176,7 +1176,8 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     return e ? atoi(e) : 8;
   }();
   p.prefetch = prefetch;
-  if (split == 0 && bn == 256) {
+  p.a_rows = pair ? 128 : a_rows;
+  if (split == 0) {
     // fewest k-stages of any problem decides how far K can be split
     const int ksub = pair ? 2 : 1;
     long long min_stages = -1;
@@ -1192,13 +1193,18 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   p.split = split;
   if (split > 1) {
     if (pair) {
-      if (epi == kEpiF32) return launch_splitk<true, kEpiF32>(p, stream);
-      if (epi == kEpiBF16) return launch_splitk<true, kEpiBF16>(p, stream);
-      return launch_splitk<true, kEpiSwiGLU>(p, stream);
+      if (epi == kEpiF32) return launch_splitk<true, kEpiF32, 256>(p, stream);
+      if (epi == kEpiBF16) return launch_splitk<true, kEpiBF16, 256>(p, stream);
+      return launch_splitk<true, kEpiSwiGLU, 256>(p, stream);
     }
-    if (epi == kEpiF32) return launch_splitk<false, kEpiF32>(p, stream);
-    if (epi == kEpiBF16) return launch_splitk<false, kEpiBF16>(p, stream);
-    return launch_splitk<false, kEpiSwiGLU>(p, stream);
+    if (bn == 128) {
+      if (epi == kEpiF32) return launch_splitk<false, kEpiF32, 128>(p, stream);
+      if (epi == kEpiBF16) return launch_splitk<false, kEpiBF16, 128>(p, stream);
+      return launch_splitk<false, kEpiSwiGLU, 128>(p, stream);
+    }
+    if (epi == kEpiF32) return launch_splitk<false, kEpiF32, 256>(p, stream);
+    if (epi == kEpiBF16) return launch_splitk<false, kEpiBF16, 256>(p, stream);
+    return launch_splitk<false, kEpiSwiGLU, 256>(p, stream);
   }
   if (pair) {
     if (epi == kEpiF32) return launch_pair<kEpiF32>(p, stream);
@@ -1244,9 +1250,7 @@ int choose_split(long long tiles, bool pair, long long stages_per_tile) {
   return s;
 }
 
-int choose_bn(long long tiles_256, long long tiles_128, int epi) {
-  (void)tiles_128;
-  (void)epi;
+int choose_bn(long long rows) {
   // TPGQA_BN=128|256 forces the tile width (tuning override).
   static const int forced = [] {
     const char *e = getenv("TPGQA_BN");
@@ -1254,9 +1258,14 @@ int choose_bn(long long tiles_256, long long tiles_128, int epi) {
   }();
   if (forced == 128 || forced == 256) return forced;
   // 128-column tiles need twice the operand bytes per MMA flop and starve the
-  // tensor pipe; problems with few 256-column tiles are split along K instead.
-  (void)tiles_256;
-  return 256;
+  // tensor pipe on compute-bound shapes. At 64 tokens or fewer every GEMM streams
+  // its weights from HBM, and narrower tiles double the number of CTAs doing so.
+  return rows <= 64 ? 128 : 256;
+}
+
+int a_box_rows(long long rows) {
+  const long long r = ((rows + 7) / 8) * 8;
+  return static_cast<int>(r < 128 ? (r < 8 ? 8 : r) : 128);
 }
 
 }  // namespace tpgqa

@@ -2,6 +2,7 @@
 // Every entry point validates everything before it enqueues anything; on an
 // error nothing is launched. No entry point allocates device memory.
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -133,11 +134,14 @@ tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, c
   }
   GemmBuilder b;
   b.epi = epi;
-  b.bn = choose_bn(t256, t128, epi);
+  (void)t256;
+  (void)t128;
+  b.bn = choose_bn(T);
   b.pair = choose_pair(T);
   if (b.pair) b.bn = 256;
+  b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
-  const int am = b.add_map(x.ptr, T, K, x.ld, 128, &err);
+  const int am = b.add_map(x.ptr, T, K, x.ld, b.a_rows, &err);
   if (am < 0) return err;
   for (int32_t r = 0; r < nb; ++r) {
     if (w[r].rows == 0) continue;
@@ -159,14 +163,17 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
   const long long probs = fused ? 1 : n;
   GemmBuilder b;
   b.epi = kEpiF32;
-  b.bn = choose_bn(probs * mt * ((nout + 255) / 256), probs * mt * ((nout + 127) / 128), kEpiF32);
+  (void)probs;
+  (void)mt;
+  b.bn = choose_bn(T);
   b.pair = choose_pair(T);
   if (b.pair) b.bn = 256;
+  b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
   std::vector<int> am(n), bm(n);
   std::vector<long long> ks(n);
   for (int32_t r = 0; r < n; ++r) {
-    am[r] = b.add_map(x[r].ptr, T, x[r].cols, x[r].ld, 128, &err);
+    am[r] = b.add_map(x[r].ptr, T, x[r].cols, x[r].ld, b.a_rows, &err);
     if (am[r] < 0) return err;
     bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, b.pair ? 128 : b.bn, &err);
     if (bm[r] < 0) return err;
@@ -324,6 +331,14 @@ int num_sms() {
     g_sm_count[dev] = v;
   }
   return g_sm_count[dev];
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *e = getenv("TPGQA_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 tp_status cuda_fail(cudaError_t e) {
@@ -525,11 +540,13 @@ tp_status launch_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *
   GemmBuilder b;
   b.epi = kEpiSwiGLU;
   const long long mt = (T + 127) / 128;
-  b.bn = choose_bn(n * mt * ((Fr + 127) / 128), n * mt * ((Fr + 63) / 64), kEpiSwiGLU);
+  (void)mt;
+  b.bn = choose_bn(T);
   b.pair = choose_pair(T);
   if (b.pair) b.bn = 256;
+  b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
-  const int am = b.add_map(x->ptr, T, D, x->ld, 128, &err);
+  const int am = b.add_map(x->ptr, T, D, x->ld, b.a_rows, &err);
   if (am < 0) return err;
   for (int32_t r = 0; r < n; ++r) {
     const int gm = b.add_map(w_gate[r].ptr, Fr, D, w_gate[r].ld, b.bn / 2, &err);

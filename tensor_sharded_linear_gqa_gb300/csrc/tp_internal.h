@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "tpgqa.h"
 
 namespace tpgqa {
@@ -38,6 +40,42 @@ int num_sms();
 
 // Records a failed CUDA call for tp_last_cuda_error() and returns TP_ERR_CUDA.
 tp_status cuda_fail(cudaError_t e);
+
+// Whether kernels are launched with programmatic stream serialization (PDL):
+// every kernel of the library waits (griddepcontrol.wait) before it touches
+// global memory, so the next kernel in a stream may launch and run its prologue
+// while the previous one finishes. TPGQA_PDL=0 turns it off.
+bool pdl_enabled();
+
+// Launches `kernel` on `stream`, with PDL when enabled and with a cluster of
+// `cluster_x` CTAs when cluster_x > 1 (kernels whose cluster shape is fixed at
+// compile time pass 1).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster_x > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster_x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------------------
 // bf16 tensor-core grouped GEMM (tcgen05 + TMA), C = A * B^T, both K-major.
@@ -80,6 +118,8 @@ struct GemmParams {
   int n_maps_used;
   int prefetch;  // L2 prefetch distance of B tiles, in k-blocks (0 = none)
   int split;     // split-K factor of the cluster kernel (1 = persistent kernels)
+  int a_rows;    // rows of every A box (128, or the token count rounded up to 8 when
+                 // it is smaller: accumulator rows past it are never stored)
   int *status;
   long long wait_ns;
 };
@@ -91,6 +131,7 @@ struct GemmBuilder {
   int bn = 256;       // CTA tile width in accumulator columns (128 or 256)
   int epi = kEpiF32;
   bool pair = false;  // SM-pair kernel: 256 x 256 tiles, cta_group::2 (bn must be 256)
+  int a_rows = 128;   // A box rows of the single-CTA kernels (see a_box_rows)
   int split = 0;      // 0: chosen at launch; >1: split-K over a cluster, reduced in fixed
                       // order through DSMEM; 1: the persistent kernels
   GemmBuilder();
@@ -105,8 +146,10 @@ struct GemmBuilder {
   tp_status launch(cudaStream_t stream);
 };
 
-// Picks the tile width for a set of problems with these output shapes.
-int choose_bn(long long total_tiles_256, long long total_tiles_128, int epi);
+// Picks the tile width (128 or 256 accumulator columns) for problems of `rows` rows.
+int choose_bn(long long rows);
+// Rows of an A box for problems of `rows` rows on the single-CTA kernels.
+int a_box_rows(long long rows);
 // Whether to run the SM-pair kernel for problems of this many rows.
 bool choose_pair(long long rows);
 // Split-K factor for `tiles` output tiles of `stages_per_tile` k-stages each
