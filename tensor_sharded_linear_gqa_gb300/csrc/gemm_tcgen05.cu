@@ -1258,9 +1258,10 @@ int choose_bn(long long rows) {
   }();
   if (forced == 128 || forced == 256) return forced;
   // 128-column tiles need twice the operand bytes per MMA flop and starve the
-  // tensor pipe on compute-bound shapes. At 64 tokens or fewer every GEMM streams
-  // its weights from HBM, and narrower tiles double the number of CTAs doing so.
-  return rows <= 64 ? 128 : 256;
+  // tensor pipe; they also measured slower on decode shapes (three small TMA
+  // boxes per stage), where 256-column tiles with split-K stream weights faster.
+  (void)rows;
+  return 256;
 }
 
 int a_box_rows(long long rows) {
