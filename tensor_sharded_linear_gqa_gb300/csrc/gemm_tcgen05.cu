@@ -668,6 +668,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // memory (DSMEM) and adding in split order 0, 1, ..., S-1. The sum order is
 // fixed, so the result does not depend on timing; no global workspace is used.
 // ---------------------------------------------------------------------------
+// Stores one 16-byte unit (4 fp32 sums g, and for SwiGLU the matching up sums u)
+// of output row `grow` at unit c4 of tile column block nt, with the epilogue
+// transform of EPI; columns past the problem's n are dropped.
+struct OutDesc {
+  void *out;
+  long long ldc;
+  int n;
+};
+
+template <int EPI, int BN>
+__device__ __forceinline__ void store_unit(const OutDesc &pr, int grow, int nt, int c4, float4 g, float4 u) {
+  const float f[4] = {g.x, g.y, g.z, g.w};
+  if (EPI == kEpiF32) {
+    const int col = nt * BN + c4 * 4;
+    float *dst = static_cast<float *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
+    if (col + 4 <= pr.n) {
+      *reinterpret_cast<float4 *>(dst) = g;
+    } else {
+      for (int e = 0; e < 4; ++e)
+        if (col + e < pr.n) dst[e] = f[e];
+    }
+    return;
+  }
+  float o[4];
+  int col;
+  if (EPI == kEpiSwiGLU) {
+    const float uu[4] = {u.x, u.y, u.z, u.w};
+    for (int e = 0; e < 4; ++e) o[e] = silu(f[e]) * uu[e];
+    col = nt * (BN / 2) + c4 * 4;
+  } else {
+    for (int e = 0; e < 4; ++e) o[e] = f[e];
+    col = nt * BN + c4 * 4;
+  }
+  __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
+  if (col + 4 <= pr.n) {
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 w;
+    memcpy(&w.x, &h0, 4);
+    memcpy(&w.y, &h1, 4);
+    *reinterpret_cast<uint2 *>(dst) = w;
+  } else {
+    for (int e = 0; e < 4; ++e)
+      if (col + e < pr.n) dst[e] = __float2bfloat16_rn(o[e]);
+  }
+}
+
 template <bool PAIR, int BN>
 struct SplitCfg {
   static constexpr int kSub = PAIR ? 2 : 1;  // 64-wide k-tiles per stage
@@ -874,107 +921,208 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   ptx::tc_fence_after();
 
   const int rows_per = 128 / nsplit;  // rows of this member's half owned by each split
-  if (warp >= 2) {
-    const int q = warp & 3;
-    const int tid = threadIdx.x - 64;
-    if (tid == 0)
-      ptx::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((nsplit - 1) * rows_per * kRowBytes));
-    // push: row r of this CTA's accumulator goes to the split that owns it
-    if (*abort_flag == 0) {
-      const int r = q * 32 + lane;
-      const int owner = r / rows_per;
-      const int rl = r - owner * rows_per;
-      const uint32_t dst_rank = PAIR ? static_cast<uint32_t>(2 * owner + member) : static_cast<uint32_t>(owner);
-      const uint32_t row_off = red0 + static_cast<uint32_t>((split * rows_per + rl) * kRowBytes);
-      const bool local_row = owner == split;
-      const uint32_t rbar = ptx::mapa_shared(recv_bar, dst_rank);
-      const uint32_t tbase = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
-      const bool has_work = k_end > k_begin;
+  // Bulk path: stage the whole accumulator in own shared memory, then send each
+  // owner its contiguous block of rows with one bulk copy; the owner receives the
+  // other splits' blocks after its own staging area. Needs room for both.
+  const bool bulk = (128 + (nsplit - 1) * rows_per) * kRowBytes <= S * C::kStageBytes;
+  if (bulk) {
+    const uint32_t recv0 = red0 + 128u * kRowBytes;  // slot j: rows_per rows of split (j < split ? j : j + 1)
+    if (warp >= 2) {
+      const int q = warp & 3;
+      const int tid = threadIdx.x - 64;
+      if (tid == 0)
+        ptx::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((nsplit - 1) * rows_per * kRowBytes));
+      if (*abort_flag == 0) {
+        const int r = q * 32 + lane;
+        const uint32_t tbase = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
+        const bool has_work = k_end > k_begin;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32cols(tbase + c, v);
-        ptx::tmem_ld_wait();
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32cols(tbase + c, v);
+          ptx::tmem_ld_wait();
+          float4 *row = reinterpret_cast<float4 *>(smem + r * kRowBytes);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int c4 = c / 4 + j;
-          const float4 f = has_work ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-          const uint32_t a = row_off + static_cast<uint32_t>((c4 ^ (rl & 7)) * 16);
-          if (local_row)
-            *reinterpret_cast<float4 *>(smem + (a - red0)) = f;
-          else
-            ptx::st_async_f4(ptx::mapa_shared(a, dst_rank), f, rbar);
+          for (int j = 0; j < 8; ++j) {
+            const int c4 = c / 4 + j;
+            row[c4 ^ (r & 7)] = has_work ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                       __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+      ptx::fence_proxy_async_smem();  // staged rows visible to the bulk-copy engine
+      ptx::named_barrier(1, 128);
+      if (tid < nsplit && tid != split && *abort_flag == 0) {
+        const int o = tid;  // destination split
+        const uint32_t dst_rank = PAIR ? static_cast<uint32_t>(2 * o + member) : static_cast<uint32_t>(o);
+        const int slot = split < o ? split : split - 1;
+        ptx::bulk_copy_to_cluster(
+            ptx::mapa_shared(recv0 + static_cast<uint32_t>(slot * rows_per * kRowBytes), dst_rank),
+            red0 + static_cast<uint32_t>(o * rows_per * kRowBytes),
+            static_cast<uint32_t>(rows_per * kRowBytes), ptx::mapa_shared(recv_bar, dst_rank));
+      }
+      const bool got = ptx::mbar_wait(recv_bar, 0, p.wait_ns);
+      if (!got && lane == 0) record(p.status, kDevTimeoutEpilogue);
+      if (got && *abort_flag == 0) {
+        // Sum the owned rows over splits in order 0..S-1. Problem fields live in
+        // registers; each thread takes kBatch units and issues every shared load
+        // of a split before adding, so loads overlap.
+        const int lo = split * rows_per;
+        const int row0 = PAIR ? mt * 256 + member * 128 : mt * 128;
+        const OutDesc od{pr.out, pr.ldc, pr.n};
+        const int m_rows = pr.m;
+        constexpr int kUnits = (EPI == kEpiSwiGLU) ? BN / 8 : BN / 4;
+        constexpr int kBatch = 4;
+        constexpr int kMaxSplit = PAIR ? 4 : 8;
+        const int total = rows_per * kUnits;
+        for (int base = tid; base < total; base += 128 * kBatch) {
+          float4 g[kBatch], u[kBatch];
+#pragma unroll
+          for (int t = 0; t < kMaxSplit; ++t) {
+            if (t >= nsplit) break;
+            float4 vg[kBatch], vu[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+              const int idx = base + b * 128 < total ? base + b * 128 : base;
+              const int rl = idx / kUnits;
+              const int c4 = idx % kUnits;
+              const int prow = (t == split) ? lo + rl : 128 + (t < split ? t : t - 1) * rows_per + rl;
+              const uint32_t rowa = red0 + static_cast<uint32_t>(prow * kRowBytes);
+              vg[b] = ptx::ld_shared_f4(rowa + static_cast<uint32_t>(((c4 ^ (rl & 7)) * 16)));
+              if (EPI == kEpiSwiGLU)
+                vu[b] = ptx::ld_shared_f4(rowa + static_cast<uint32_t>((((c4 + BN / 8) ^ (rl & 7)) * 16)));
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+              if (t == 0) {
+                g[b] = vg[b];
+                if (EPI == kEpiSwiGLU) u[b] = vu[b];
+              } else {
+                g[b].x += vg[b].x; g[b].y += vg[b].y; g[b].z += vg[b].z; g[b].w += vg[b].w;
+                if (EPI == kEpiSwiGLU) {
+                  u[b].x += vu[b].x; u[b].y += vu[b].y; u[b].z += vu[b].z; u[b].w += vu[b].w;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int idx = base + b * 128;
+            if (idx >= total) break;
+            const int rl = idx / kUnits;
+            const int grow = row0 + lo + rl;
+            if (grow < m_rows) store_unit<EPI, BN>(od, grow, nt, idx % kUnits, g[b], u[b]);
+          }
         }
       }
     }
-    // wait for the other splits' partials of the rows this CTA owns
-    const bool got = ptx::mbar_wait(recv_bar, 0, p.wait_ns);
-    if (!got && lane == 0) record(p.status, kDevTimeoutEpilogue);
-    ptx::named_barrier(1, 128);  // local partial writes of all four epilogue warps
-    if (got && *abort_flag == 0) {
-      // rows [lo, lo + rows_per) of this member's half, summed over splits in order 0..S-1
-      const int lo = split * rows_per;
-      const int row0 = PAIR ? mt * 256 + member * 128 : mt * 128;
-      constexpr int kUnits = (EPI == kEpiSwiGLU) ? BN / 8 : BN / 4;  // output 16-byte units per row
-      const int total = rows_per * kUnits;
-      for (int idx = tid; idx < total; idx += 128) {
-        const int rl = idx / kUnits;
-        const int c4 = idx % kUnits;
-        const int grow = row0 + lo + rl;
-        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
-        for (int t = 0; t < nsplit; ++t) {
-          const uint8_t *rowp = smem + (t * rows_per + rl) * kRowBytes;
-          const float4 vg = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (rl & 7)) * 16));
-          if (t == 0) {
-            g = vg;
-          } else {
-            g.x += vg.x; g.y += vg.y; g.z += vg.z; g.w += vg.w;
-          }
-          if (EPI == kEpiSwiGLU) {
-            const float4 vu = *reinterpret_cast<const float4 *>(rowp + (((c4 + BN / 8) ^ (rl & 7)) * 16));
-            if (t == 0) {
-              u = vu;
-            } else {
-              u.x += vu.x; u.y += vu.y; u.z += vu.z; u.w += vu.w;
-            }
+    // Outgoing bulk copies read this CTA's staging area until the owner's barrier
+    // has seen their bytes: nobody leaves before every owner has received.
+    ptx::cluster_sync();
+  } else {
+    if (warp >= 2) {
+      const int q = warp & 3;
+      const int tid = threadIdx.x - 64;
+      if (tid == 0)
+        ptx::mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((nsplit - 1) * rows_per * kRowBytes));
+      // push: row r of this CTA's accumulator goes to the split that owns it
+      if (*abort_flag == 0) {
+        const int r = q * 32 + lane;
+        const int owner = r / rows_per;
+        const int rl = r - owner * rows_per;
+        const uint32_t dst_rank = PAIR ? static_cast<uint32_t>(2 * owner + member) : static_cast<uint32_t>(owner);
+        const uint32_t row_off = red0 + static_cast<uint32_t>((split * rows_per + rl) * kRowBytes);
+        const bool local_row = owner == split;
+        const uint32_t rbar = ptx::mapa_shared(recv_bar, dst_rank);
+        const uint32_t tbase = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
+        const bool has_work = k_end > k_begin;
+  #pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32cols(tbase + c, v);
+          ptx::tmem_ld_wait();
+  #pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int c4 = c / 4 + j;
+            const float4 f = has_work ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            const uint32_t a = row_off + static_cast<uint32_t>((c4 ^ (rl & 7)) * 16);
+            if (local_row)
+              *reinterpret_cast<float4 *>(smem + (a - red0)) = f;
+            else
+              ptx::st_async_f4(ptx::mapa_shared(a, dst_rank), f, rbar);
           }
         }
-        if (grow >= pr.m) continue;
-        const float f[4] = {g.x, g.y, g.z, g.w};
-        if (EPI == kEpiF32) {
-          const int col = nt * BN + c4 * 4;
-          float *dst = static_cast<float *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
-          if (col + 4 <= pr.n) {
-            *reinterpret_cast<float4 *>(dst) = g;
-          } else {
-            for (int e = 0; e < 4; ++e)
-              if (col + e < pr.n) dst[e] = f[e];
+      }
+      // wait for the other splits' partials of the rows this CTA owns
+      const bool got = ptx::mbar_wait(recv_bar, 0, p.wait_ns);
+      if (!got && lane == 0) record(p.status, kDevTimeoutEpilogue);
+      ptx::named_barrier(1, 128);  // local partial writes of all four epilogue warps
+      if (got && *abort_flag == 0) {
+        // rows [lo, lo + rows_per) of this member's half, summed over splits in order 0..S-1
+        const int lo = split * rows_per;
+        const int row0 = PAIR ? mt * 256 + member * 128 : mt * 128;
+        constexpr int kUnits = (EPI == kEpiSwiGLU) ? BN / 8 : BN / 4;  // output 16-byte units per row
+        const int total = rows_per * kUnits;
+        for (int idx = tid; idx < total; idx += 128) {
+          const int rl = idx / kUnits;
+          const int c4 = idx % kUnits;
+          const int grow = row0 + lo + rl;
+          float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+          for (int t = 0; t < nsplit; ++t) {
+            const uint8_t *rowp = smem + (t * rows_per + rl) * kRowBytes;
+            const float4 vg = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (rl & 7)) * 16));
+            if (t == 0) {
+              g = vg;
+            } else {
+              g.x += vg.x; g.y += vg.y; g.z += vg.z; g.w += vg.w;
+            }
+            if (EPI == kEpiSwiGLU) {
+              const float4 vu = *reinterpret_cast<const float4 *>(rowp + (((c4 + BN / 8) ^ (rl & 7)) * 16));
+              if (t == 0) {
+                u = vu;
+              } else {
+                u.x += vu.x; u.y += vu.y; u.z += vu.z; u.w += vu.w;
+              }
+            }
           }
-        } else {
-          float o[4];
-          int col;
-          if (EPI == kEpiSwiGLU) {
-            const float uu[4] = {u.x, u.y, u.z, u.w};
-            for (int e = 0; e < 4; ++e) o[e] = silu(f[e]) * uu[e];
-            col = nt * (BN / 2) + c4 * 4;
+          if (grow >= pr.m) continue;
+          const float f[4] = {g.x, g.y, g.z, g.w};
+          if (EPI == kEpiF32) {
+            const int col = nt * BN + c4 * 4;
+            float *dst = static_cast<float *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
+            if (col + 4 <= pr.n) {
+              *reinterpret_cast<float4 *>(dst) = g;
+            } else {
+              for (int e = 0; e < 4; ++e)
+                if (col + e < pr.n) dst[e] = f[e];
+            }
           } else {
-            for (int e = 0; e < 4; ++e) o[e] = f[e];
-            col = nt * BN + c4 * 4;
-          }
-          __nv_bfloat16 *dst =
-              static_cast<__nv_bfloat16 *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
-          if (col + 4 <= pr.n) {
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(o[2], o[3]);
-            uint2 w;
-            memcpy(&w.x, &h0, 4);
-            memcpy(&w.y, &h1, 4);
-            *reinterpret_cast<uint2 *>(dst) = w;
-          } else {
-            for (int e = 0; e < 4; ++e)
-              if (col + e < pr.n) dst[e] = __float2bfloat16_rn(o[e]);
+            float o[4];
+            int col;
+            if (EPI == kEpiSwiGLU) {
+              const float uu[4] = {u.x, u.y, u.z, u.w};
+              for (int e = 0; e < 4; ++e) o[e] = silu(f[e]) * uu[e];
+              col = nt * (BN / 2) + c4 * 4;
+            } else {
+              for (int e = 0; e < 4; ++e) o[e] = f[e];
+              col = nt * BN + c4 * 4;
+            }
+            __nv_bfloat16 *dst =
+                static_cast<__nv_bfloat16 *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
+            if (col + 4 <= pr.n) {
+              __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]);
+              __nv_bfloat162 h1 = __floats2bfloat162_rn(o[2], o[3]);
+              uint2 w;
+              memcpy(&w.x, &h0, 4);
+              memcpy(&w.y, &h1, 4);
+              *reinterpret_cast<uint2 *>(dst) = w;
+            } else {
+              for (int e = 0; e < 4; ++e)
+                if (col + e < pr.n) dst[e] = __float2bfloat16_rn(o[e]);
+            }
           }
         }
       }

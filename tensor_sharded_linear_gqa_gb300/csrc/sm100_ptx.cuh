@@ -151,6 +151,27 @@ __device__ __forceinline__ void st_async_f4(uint32_t cluster_addr, float4 v, uin
       : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into the
+// shared memory of a CTA of the cluster, counted (complete_tx) on an mbarrier in
+// the destination CTA. Both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// 16-byte load from this CTA's shared memory (shared::cta address).
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // Barrier among `nthreads` threads of the CTA on hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
