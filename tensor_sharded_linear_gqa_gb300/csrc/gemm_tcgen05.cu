@@ -499,7 +499,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kPrefetch && pf.valid; ++i) {
         int m, r;
         b_src(pf, m, r);
-        ptx::tma_prefetch_l2_2d(&p.maps[m], pf.kt * kPairSub * BK, r);
+        if (p.box_kt > 1)
+          ptx::tma_prefetch_l2_3d(&p.maps[m], 0, r, pf.kt * kPairSub);
+        else
+          ptx::tma_prefetch_l2_2d(&p.maps[m], pf.kt * kPairSub * BK, r);
         next(pf);
       }
       int kb = 0;
@@ -507,7 +510,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (pf.valid) {
           int m, r;
           b_src(pf, m, r);
-          ptx::tma_prefetch_l2_2d(&p.maps[m], pf.kt * kPairSub * BK, r);
+          if (p.box_kt > 1)
+            ptx::tma_prefetch_l2_3d(&p.maps[m], 0, r, pf.kt * kPairSub);
+          else
+            ptx::tma_prefetch_l2_2d(&p.maps[m], pf.kt * kPairSub * BK, r);
           next(pf);
         }
         const int st = kb % S;
@@ -523,13 +529,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
         int m, r;
         b_src(ld, m, r);
+        const int a_row = ld.mt * 256 + static_cast<int>(rank) * 128;
+        if (p.box_kt > 1) {
+          // one copy per operand brings the stage's KSUB k-tiles (3-D maps)
+          ptx::tma_load_3d_pair(sA0 + st * kPairSub * kPairABytes, &p.maps[sg.a_map], 0, a_row,
+                                ld.kt * kPairSub, lead_full);
+          ptx::tma_load_3d_pair(sB0 + st * kPairSub * kPairBBytes, &p.maps[m], 0, r, ld.kt * kPairSub,
+                                lead_full);
+        } else {
 #pragma unroll
-        for (int j = 0; j < kPairSub; ++j) {
-          // a k-tile past the segment's end reads zeros (out-of-range TMA fill)
-          const int x = (ld.kt * kPairSub + j) * BK;
-          ptx::tma_load_2d_pair(sA0 + (st * kPairSub + j) * kPairABytes, &p.maps[sg.a_map], x,
-                                ld.mt * 256 + static_cast<int>(rank) * 128, lead_full);
-          ptx::tma_load_2d_pair(sB0 + (st * kPairSub + j) * kPairBBytes, &p.maps[m], x, r, lead_full);
+          for (int j = 0; j < kPairSub; ++j) {
+            // a k-tile past the segment's end reads zeros (out-of-range TMA fill)
+            const int x = (ld.kt * kPairSub + j) * BK;
+            ptx::tma_load_2d_pair(sA0 + (st * kPairSub + j) * kPairABytes, &p.maps[sg.a_map], x, a_row,
+                                  lead_full);
+            ptx::tma_load_2d_pair(sB0 + (st * kPairSub + j) * kPairBBytes, &p.maps[m], x, r, lead_full);
+          }
         }
         ++kb;
         next(ld);
@@ -837,24 +852,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
                                                         : static_cast<uint32_t>(KS * (p.a_rows * 128 + C::kBBytes)));
         const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(st), lead) : full_bar(st);
         const int a_row = PAIR ? mt * 256 + member * 128 : mt * 128;
+        if (PAIR && p.box_kt > 1) {
+          // 3-D maps: one copy per operand brings the stage's KS k-tiles
+          const int z = kt * KS;  // past the segment's K: zero fill
+          ptx::tma_load_3d_pair(sA0 + st * KS * C::kABytes, &p.maps[sg.a_map], 0, a_row, z, fb);
+          if (EPI == kEpiSwiGLU)
+            ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[member == 0 ? sg.b_map : sg.b2_map], 0,
+                                  nt * 128, z, fb);
+          else
+            ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[sg.b_map], 0, nt * BN + member * 128, z,
+                                  fb);
+        } else {
 #pragma unroll
-        for (int j = 0; j < KS; ++j) {
-          const int x = (kt * KS + j) * BK;  // past the segment's K: zero fill
-          const uint32_t da = sA0 + (st * KS + j) * C::kABytes;
-          const uint32_t db = sB0 + (st * KS + j) * C::kBBytes;
-          if constexpr (PAIR) {
-            ptx::tma_load_2d_pair(da, &p.maps[sg.a_map], x, a_row, fb);
-            if (EPI == kEpiSwiGLU)
-              ptx::tma_load_2d_pair(db, &p.maps[member == 0 ? sg.b_map : sg.b2_map], x, nt * 128, fb);
-            else
-              ptx::tma_load_2d_pair(db, &p.maps[sg.b_map], x, nt * BN + member * 128, fb);
-          } else {
-            ptx::tma_load_2d(da, &p.maps[sg.a_map], x, a_row, fb);
-            if (EPI == kEpiSwiGLU) {
-              ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * (BN / 2), fb);
-              ptx::tma_load_2d(db + (BN / 2) * 128, &p.maps[sg.b2_map], x, nt * (BN / 2), fb);
+          for (int j = 0; j < KS; ++j) {
+            const int x = (kt * KS + j) * BK;  // past the segment's K: zero fill
+            const uint32_t da = sA0 + (st * KS + j) * C::kABytes;
+            const uint32_t db = sB0 + (st * KS + j) * C::kBBytes;
+            if constexpr (PAIR) {
+              ptx::tma_load_2d_pair(da, &p.maps[sg.a_map], x, a_row, fb);
+              if (EPI == kEpiSwiGLU)
+                ptx::tma_load_2d_pair(db, &p.maps[member == 0 ? sg.b_map : sg.b2_map], x, nt * 128, fb);
+              else
+                ptx::tma_load_2d_pair(db, &p.maps[sg.b_map], x, nt * BN + member * 128, fb);
             } else {
-              ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * BN, fb);
+              ptx::tma_load_2d(da, &p.maps[sg.a_map], x, a_row, fb);
+              if (EPI == kEpiSwiGLU) {
+                ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * (BN / 2), fb);
+                ptx::tma_load_2d(db + (BN / 2) * 128, &p.maps[sg.b2_map], x, nt * (BN / 2), fb);
+              } else {
+                ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * BN, fb);
+              }
             }
           }
         }
@@ -936,18 +963,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
         const int r = q * 32 + lane;
         const uint32_t tbase = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
         const bool has_work = k_end > k_begin;
+        float4 *row = reinterpret_cast<float4 *>(smem + r * kRowBytes);
+        // 128 columns per wait: four TMEM loads in flight instead of one
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32cols(tbase + c, v);
-          ptx::tmem_ld_wait();
-          float4 *row = reinterpret_cast<float4 *>(smem + r * kRowBytes);
+        for (int c = 0; c < BN; c += 128) {
+          uint32_t v[4][32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int c4 = c / 4 + j;
-            row[c4 ^ (r & 7)] = has_work ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                       __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int h = 0; h < 4; ++h) ptx::tmem_ld_32cols(tbase + c + 32 * h, v[h]);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 4; ++h) ptx::tmem_regs_ready(v[h]);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int c4 = (c + 32 * h) / 4 + j;
+              row[c4 ^ (r & 7)] =
+                  has_work ? make_float4(__uint_as_float(v[h][4 * j]), __uint_as_float(v[h][4 * j + 1]),
+                                         __uint_as_float(v[h][4 * j + 2]), __uint_as_float(v[h][4 * j + 3]))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
           }
         }
       }
@@ -973,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
         const OutDesc od{pr.out, pr.ldc, pr.n};
         const int m_rows = pr.m;
         constexpr int kUnits = (EPI == kEpiSwiGLU) ? BN / 8 : BN / 4;
-        constexpr int kBatch = 4;
+        constexpr int kBatch = (EPI == kEpiSwiGLU) ? 4 : 8;
         constexpr int kMaxSplit = PAIR ? 4 : 8;
         const int total = rows_per * kUnits;
         for (int base = tid; base < total; base += 128 * kBatch) {
@@ -1129,6 +1164,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
     }
   }
 
+
   if (*abort_flag && threadIdx.x == 0) {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < 2000000ull) {
@@ -1251,6 +1287,41 @@ tp_status launch_splitk(const GemmParams &p, cudaStream_t stream) {
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
+// Clusters of `csize` split-K CTAs that can be resident at once, or -1 if the
+// runtime cannot say. A cluster has to fit inside one GPC, so this can be well
+// below SMs / csize (on GB300: 36 clusters of 4 and 15 of 8 for 152 SMs). All
+// split-K instantiations use the same shared memory and block size, so one of
+// them stands for all.
+int max_active_clusters(int csize) {
+  static std::mutex mu;
+  static int cache[32][17] = {};  // [device][cluster size], 0 = not queried yet
+  int dev = 0;
+  if (csize < 1 || csize > 16 || cudaGetDevice(&dev) != cudaSuccess || dev >= 32) return -1;
+  std::lock_guard<std::mutex> g(mu);
+  if (cache[dev][csize] == 0) {
+    using C = SplitCfg<true, 256>;
+    auto kern = k_gemm_bf16_splitk<true, kEpiF32, 256>;
+    int n = -1;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(csize));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = C::kSmem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = static_cast<unsigned>(csize);
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = -1;
+    }
+    cudaGetLastError();  // a failed query leaves no sticky error behind
+    cache[dev][csize] = n;
+  }
+  return cache[dev][csize];
+}
+
 }  // namespace
 
 GemmBuilder::GemmBuilder() { std::memset(&p, 0, sizeof(p)); }
@@ -1278,7 +1349,41 @@ int GemmBuilder::add_map(const void *base, long long rows, long long k, long lon
     *err = TP_ERR_INVALID_ARG;
     return -1;
   }
+  margs[n_maps] = MapArgs{base, rows, k, ld, box_rows};
   return n_maps++;
+}
+
+int GemmBuilder::use_3d_boxes(int kt) {
+  // TPGQA_TMA3D=0 keeps the 2-D maps (tuning override).
+  static const int enabled = [] {
+    const char *e = getenv("TPGQA_TMA3D");
+    return e ? atoi(e) : 1;
+  }();
+  if (kt <= 1 || !enabled) return 1;
+  for (int i = 0; i < n_maps; ++i)
+    if (margs[i].k % BK != 0 || margs[i].k / BK < kt) return 1;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return 1;
+  // View a [rows x k] matrix as [k/64][rows][64]: element (x, y, z) is column
+  // z*64 + x of row y, so dim 2 steps by 128 bytes inside a row. A box of
+  // {64, box_rows, kt} lands as kt swizzled [box_rows x 128 B] k-tiles back to
+  // back, the same shared-memory layout that kt 2-D copies produce.
+  CUtensorMap tmp[kMaxMaps];
+  for (int i = 0; i < n_maps; ++i) {
+    const MapArgs &m = margs[i];
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(m.rows),
+                                static_cast<cuuint64_t>(m.k / BK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(m.ld) * 2, static_cast<cuuint64_t>(BK) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(m.box_rows),
+                               static_cast<cuuint32_t>(kt)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&tmp[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(m.base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return 1;  // keep the 2-D maps, all of them
+  }
+  for (int i = 0; i < n_maps; ++i) p.maps[i] = tmp[i];
+  return kt;
 }
 
 bool GemmBuilder::add_problem(int m, int n, void *out, long long ldc, const int *a_maps,
@@ -1339,6 +1444,10 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   }
   if (split < 1) split = 1;
   p.split = split;
+  // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand
+  // and stage replaces KSUB 2-D copies. The single-CTA kernels load one k-tile
+  // per stage and keep the 2-D maps.
+  p.box_kt = pair ? use_3d_boxes(split > 1 ? SplitCfg<true, 256>::kSub : pair_ksub()) : 1;
   if (split > 1) {
     if (pair) {
       if (epi == kEpiF32) return launch_splitk<true, kEpiF32, 256>(p, stream);
@@ -1395,6 +1504,12 @@ int choose_split(long long tiles, bool pair, long long stages_per_tile) {
   // Double the split while the grid still fits in one wave and each split keeps
   // at least four k-stages to pipeline.
   while (2 * s <= max_split && tiles * per_tile * 2 * s <= sms && stages_per_tile >= 8LL * s) s *= 2;
+  // One wave also needs every cluster (one tile's splits) resident at once.
+  while (s > 1) {
+    const int m = max_active_clusters(per_tile * s);
+    if (m < 0 || tiles <= m) break;
+    s /= 2;
+  }
   return s;
 }
 

@@ -120,6 +120,8 @@ struct GemmParams {
   int split;     // split-K factor of the cluster kernel (1 = persistent kernels)
   int a_rows;    // rows of every A box (128, or the token count rounded up to 8 when
                  // it is smaller: accumulator rows past it are never stored)
+  int box_kt;    // 64-wide k-tiles per TMA copy: 1 = 2-D maps (one copy per k-tile),
+                 // >1 = 3-D maps whose box spans that many k-tiles (a whole stage)
   int *status;
   long long wait_ns;
 };
@@ -134,11 +136,22 @@ struct GemmBuilder {
   int a_rows = 128;   // A box rows of the single-CTA kernels (see a_box_rows)
   int split = 0;      // 0: chosen at launch; >1: split-K over a cluster, reduced in fixed
                       // order through DSMEM; 1: the persistent kernels
+  // What each map was made from, so launch() can re-encode them as 3-D maps.
+  struct MapArgs {
+    const void *base;
+    long long rows, k, ld;
+    int box_rows;
+  };
+  MapArgs margs[kMaxMaps];
   GemmBuilder();
   // Tensor map of a bf16 [rows x k] matrix with row pitch ld (elements), boxes
   // of 64 x box_rows, 128-byte swizzle. Returns the map index or -1.
   int add_map(const void *base, long long rows, long long k, long long ld, int box_rows,
               tp_status *err);
+  // Re-encodes every map as a 3-D map whose box spans kt k-tiles, if every
+  // map's K is a multiple of 64 with at least kt k-tiles; returns kt, or 1 (the
+  // 2-D maps kept) otherwise.
+  int use_3d_boxes(int kt);
   // Adds a problem with segments [(a_map, b_map, b2_map, k)...]; returns false
   // if the tables are full.
   bool add_problem(int m, int n, void *out, long long ldc, const int *a_maps, const int *b_maps,

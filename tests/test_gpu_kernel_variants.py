@@ -3,8 +3,11 @@
 The library picks a kernel per call: a persistent single-CTA kernel, a
 persistent SM-pair kernel (tcgen05 cta_group::2) with two or three 64-wide
 k-tiles per pipeline stage, and a split-K cluster kernel for either, depending
-on the shape. The tuning overrides TPGQA_PAIR, TPGQA_KSUB and TPGQA_SPLIT force
-one variant, so each variant here reruns the linear-layer and
+on the shape. The SM-pair kernels fetch each stage with one 3-D TMA copy per
+operand when every K is a multiple of 64, else with one 2-D copy per k-tile.
+Split-K reduces the splits' partials through the cluster's shared memory in a
+fixed order. The tuning overrides TPGQA_PAIR, TPGQA_KSUB, TPGQA_SPLIT and
+TPGQA_TMA3D force one variant, so each variant here reruns the linear-layer and
 MLP parity tests in a child process with the override set.
 """
 import os
@@ -21,13 +24,54 @@ TESTS = ["tests/test_gpu_linear.py",
          "tests/test_gpu_blocks.py::test_mlp_block_small_ragged"]
 
 
-@pytest.mark.parametrize("pair,split,ksub", [("0", "1", "2"), ("1", "1", "2"), ("1", "1", "3"),
-                                             ("0", "2", "2"), ("0", "4", "2"), ("1", "2", "2"),
-                                             ("1", "4", "2")])
-def test_kernel_variant_parity(pair, split, ksub):
+@pytest.mark.parametrize("pair,split,ksub,tma3d", [
+    ("0", "1", "2", "1"), ("1", "1", "2", "1"), ("1", "1", "3", "1"), ("1", "1", "2", "0"),
+    ("1", "1", "3", "0"), ("0", "2", "2", "1"), ("0", "4", "2", "1"), ("1", "2", "2", "1"),
+    ("1", "4", "2", "1"), ("1", "2", "2", "0")])
+def test_kernel_variant_parity(pair, split, ksub, tma3d):
     from gpu_util import need_gpu
     need_gpu()
-    env = dict(os.environ, TPGQA_PAIR=pair, TPGQA_SPLIT=split, TPGQA_KSUB=ksub)
+    env = dict(os.environ, TPGQA_PAIR=pair, TPGQA_SPLIT=split, TPGQA_KSUB=ksub, TPGQA_TMA3D=tma3d)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
                         *TESTS], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+# Runs row-parallel GEMMs that split K three times each and checks that the
+# fp32 outputs are the same bits every time: ragged shapes (partial last row and
+# column tiles) on the SM-pair and the single-CTA kernels.
+_REPEAT = r"""
+import sys
+sys.path.insert(0, "tests")
+import numpy as np, torch
+import tensor_sharded_linear_gqa_gb300 as tp
+from tensor_sharded_linear_gqa_gb300 import inputs
+from gpu_util import dev_bf16
+for T, per, nout, n in [(200, 1024, 264, 2), (70, 2048, 520, 4), (512, 2048, 1024, 2)]:
+    x = inputs.normal_bf16(61, 0, (T, n * per))
+    w = inputs.normal_bf16(61, 1, (nout, n * per), 0.02)
+    xs = [dev_bf16(x[:, r * per:(r + 1) * per]) for r in range(n)]
+    ws = [dev_bf16(w[:, r * per:(r + 1) * per]) for r in range(n)]
+    first = None
+    for rep in range(3):
+        ys = [torch.full((T, nout), float("nan"), device="cuda") for _ in range(n)]
+        tp.tp_row_linear(n, xs, ws, ys, tp.TP_COMBINE_NONE)
+        got = np.stack([y.cpu().numpy() for y in ys]).view(np.uint32)
+        if first is None:
+            first = got
+        assert np.array_equal(got, first), (T, per, nout, n, rep)
+assert tp.tp_device_status() == (tp.TP_OK, 0)
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("split", ["2", "4"])
+def test_split_k_reduction_is_deterministic(split):
+    """The splits' partials are added in split order 0..S-1 whatever order the
+    CTAs finish in, so repeated runs give the same bits."""
+    from gpu_util import need_gpu
+    need_gpu()
+    env = dict(os.environ, TPGQA_SPLIT=split)
+    r = subprocess.run([sys.executable, "-c", _REPEAT], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]

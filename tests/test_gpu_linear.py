@@ -74,10 +74,13 @@ def test_wiki_example_fp32_row_parallel(combine):
 # ---- bf16: exact small-integer cases (several tiles and a ragged tail) -------
 @pytest.mark.parametrize("n", [1, 2, 4, 8])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
-def test_column_exact_small_integers(n, out_dtype):
+@pytest.mark.parametrize("K", [192, 200])
+def test_column_exact_small_integers(n, out_dtype, K):
     need_gpu()
     t = torch()
-    T, K, per = 200, 192, 136          # 2 m-tiles (ragged), 3 k-tiles, ragged n
+    # 2 m-tiles (ragged), ragged n; K = 192 is 3 whole k-tiles (the last stage of
+    # two k-tiles half past the end), K = 200 ends inside a k-tile
+    T, per = 200, 136
     lo, hi = (-1, 1) if out_dtype == "bf16" else (-4, 4)   # bf16 holds integers <= 256 exactly
     x = inputs.small_int_bf16(21, 0, (T, K), lo, hi)
     wf = inputs.small_int_bf16(21, 1, (n * per, K), lo, hi)
