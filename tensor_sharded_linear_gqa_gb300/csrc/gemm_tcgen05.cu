@@ -87,6 +87,29 @@ __device__ __forceinline__ void store_bf16_row32(__nv_bfloat16 *out, long long l
   }
 }
 
+__device__ __forceinline__ void store_bf16_row16(__nv_bfloat16 *out, long long ldc, int row, int col0,
+                                                 int n, const float (&f)[16]) {
+  __nv_bfloat16 *dst = out + static_cast<long long>(row) * ldc + col0;
+  if (col0 + 16 <= n) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 8) {
+      uint4 w;
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(f[j + 0], f[j + 1]);
+      __nv_bfloat162 h1 = __floats2bfloat162_rn(f[j + 2], f[j + 3]);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(f[j + 4], f[j + 5]);
+      __nv_bfloat162 h3 = __floats2bfloat162_rn(f[j + 6], f[j + 7]);
+      memcpy(&w.x, &h0, 4);
+      memcpy(&w.y, &h1, 4);
+      memcpy(&w.z, &h2, 4);
+      memcpy(&w.w, &h3, 4);
+      *reinterpret_cast<uint4 *>(dst + j) = w;
+    }
+  } else {
+    for (int j = 0; j < 16; ++j)
+      if (col0 + j < n) dst[j] = __float2bfloat16_rn(f[j]);
+  }
+}
+
 // Walks this CTA's (tile, segment, k-tile) sequence: tiles blockIdx.x,
 // blockIdx.x + gridDim.x, ...; within a tile every segment of its problem in
 // order, within a segment its k-tiles.
@@ -210,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
       }
       int kb = 0;
       while (ld.valid) {
-        if (pf.valid) {
+        if (kPrefetch > 0 && pf.valid) {
           prefetch(pf);
           cursor_next(p, pf);
         }
@@ -371,12 +394,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
 // with more boxes in flight per barrier phase, so 128-wide stages (KSUB = 2)
 // keep the tensor pipe fed better than 64-wide ones.
 constexpr int kPairABytes = 128 * BK * 2;  // one 64-wide k-tile of this CTA's 128 A rows
-constexpr int kPairBBytes = 128 * BK * 2;  // one 64-wide k-tile of this CTA's 128 B rows
-template <int KSUB>
+// BN accumulator columns per tile: each CTA holds BN/2 rows of B (for SwiGLU,
+// BN/2 gate rows in CTA 0 and BN/2 up rows in CTA 1). BN is 256, or 224 when
+// narrower tiles fill the last wave better.
+template <int KSUB, int BN>
 struct PairCfg {
+  static constexpr int kBRows = BN / 2;
+  static constexpr int kBBytes = kBRows * BK * 2;  // one 64-wide k-tile of this CTA's B rows
   static constexpr int kStages = 6 / KSUB;
-  static constexpr int kStageBytes = KSUB * (kPairABytes + kPairBBytes);
+  static constexpr int kStageBytes = KSUB * (kPairABytes + kBBytes);
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
+  static_assert(kBBytes % 1024 == 0, "B k-tiles must keep the 1024-byte swizzle alignment");
 };
 
 template <int KSUB>
@@ -390,16 +418,18 @@ __device__ __forceinline__ int tile_stages(const GemmParams &p, int prob) {
   return n;
 }
 
-template <int EPI, int KSUB>
+template <int EPI, int KSUB, int BN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_gemm_bf16_pair(const __grid_constant__ GemmParams p) {
+  using PC = PairCfg<KSUB, BN>;
   constexpr int kPairSub = KSUB;
-  constexpr int kPairStages = PairCfg<KSUB>::kStages;
-  constexpr int kPairStageBytes = PairCfg<KSUB>::kStageBytes;
-  constexpr int BN = 256;
+  constexpr int kPairStages = PC::kStages;
+  constexpr int kPairStageBytes = PC::kStageBytes;
+  constexpr int kPairBBytes = PC::kBBytes;
+  constexpr int kHalfB = PC::kBRows;  // B rows per CTA
   constexpr int kOutCols = (EPI == kEpiSwiGLU) ? BN / 2 : BN;
   const int kPrefetch = p.prefetch;
-  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kTmemCols = 512;  // two accumulators, at columns 0 and 256
   constexpr int S = kPairStages;
 
   extern __shared__ uint8_t smem_raw[];
@@ -487,10 +517,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
         if (EPI == kEpiSwiGLU) {
           map = leader ? sg.b_map : sg.b2_map;
-          row = c.nt * 128;
+          row = c.nt * kHalfB;
         } else {
           map = sg.b_map;
-          row = c.nt * BN + static_cast<int>(rank) * 128;
+          row = c.nt * BN + static_cast<int>(rank) * kHalfB;
         }
       };
       Cursor ld, pf;
@@ -507,7 +537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       int kb = 0;
       while (ld.valid) {
-        if (pf.valid) {
+        if (kPrefetch > 0 && pf.valid) {
           int m, r;
           b_src(pf, m, r);
           if (p.box_kt > 1)
@@ -564,7 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(a * BN);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(a * 256);
         const int nk = tile_stages<KSUB>(p, find_problem(p, tile));
         for (int k0 = 0; k0 < nk; ++k0, ++kb) {
           const int st = kb % S;
@@ -610,17 +640,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int mt = local % pr.m_tiles;
       const int nt = local / pr.m_tiles;
       const int row = mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
-      const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * BN) +
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * 256) +
                              (static_cast<uint32_t>(q * 32) << 16);
       const uint32_t lead_tempty = ptx::mapa_shared(tempty_bar(a), 0);
       if constexpr (EPI == kEpiSwiGLU) {
+        // gate sums in accumulator columns [0, BN/2), up sums in [BN/2, BN)
         __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(pr.out);
+        constexpr int kFull = (BN / 2) / 32 * 32;  // columns handled 32 at a time
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = 0; c < kFull; c += 32) {
           uint32_t g[32], u[32];
           ptx::tmem_ld_32cols(tbase + c, g);
           ptx::tmem_ld_32cols(tbase + BN / 2 + c, u);
           ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(g);
+          ptx::tmem_regs_ready(u);
           if (c + 32 == BN / 2) {
             ptx::tc_fence_before();
             __syncwarp();
@@ -631,7 +665,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 32; ++jj) h[jj] = silu(__uint_as_float(g[jj])) * __uint_as_float(u[jj]);
           if (row < pr.m) store_bf16_row32(out, pr.ldc, row, nt * kOutCols + c, pr.n, h);
         }
+        if constexpr (BN / 2 > kFull) {
+          static_assert(BN / 2 - kFull == 16, "a 16-column tail");
+          uint32_t g[16], u[16];
+          ptx::tmem_ld_16cols(tbase + kFull, g);
+          ptx::tmem_ld_16cols(tbase + BN / 2 + kFull, u);
+          ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(g);
+          ptx::tmem_regs_ready(u);
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(lead_tempty);
+          float h[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) h[jj] = silu(__uint_as_float(g[jj])) * __uint_as_float(u[jj]);
+          if (row < pr.m) store_bf16_row16(out, pr.ldc, row, nt * kOutCols + kFull, pr.n, h);
+        }
       } else {
+        static_assert(BN % 32 == 0, "32-column epilogue chunks");
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t v[32];
@@ -1221,7 +1272,7 @@ tp_status launch_one(const GemmParams &p, cudaStream_t stream) {
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
-template <int EPI, int KSUB>
+template <int EPI, int KSUB, int BN>
 tp_status launch_pair_ks(const GemmParams &p, cudaStream_t stream) {
   static int configured_mask = 0;
   static std::mutex mu;
@@ -1231,15 +1282,15 @@ tp_status launch_pair_ks(const GemmParams &p, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> g(mu);
     if (dev >= 32 || !(configured_mask & (1 << dev))) {
-      e = cudaFuncSetAttribute(k_gemm_bf16_pair<EPI, KSUB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               PairCfg<KSUB>::kSmem);
+      e = cudaFuncSetAttribute(k_gemm_bf16_pair<EPI, KSUB, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PairCfg<KSUB, BN>::kSmem);
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 32) configured_mask |= (1 << dev);
     }
   }
   const int pairs_max = num_sms() / 2;
   const int pairs = p.total_tiles < pairs_max ? p.total_tiles : pairs_max;
-  e = launch_kernel(k_gemm_bf16_pair<EPI, KSUB>, dim3(2 * pairs), dim3(kThreads), PairCfg<KSUB>::kSmem,
+  e = launch_kernel(k_gemm_bf16_pair<EPI, KSUB, BN>, dim3(2 * pairs), dim3(kThreads), PairCfg<KSUB, BN>::kSmem,
                     stream, 1, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
@@ -1259,8 +1310,9 @@ int pair_ksub() {
 }
 
 template <int EPI>
-tp_status launch_pair(const GemmParams &p, cudaStream_t stream) {
-  return pair_ksub() == 2 ? launch_pair_ks<EPI, 2>(p, stream) : launch_pair_ks<EPI, 3>(p, stream);
+tp_status launch_pair(const GemmParams &p, int bn, cudaStream_t stream) {
+  if (bn == 224) return launch_pair_ks<EPI, 2, 224>(p, stream);
+  return pair_ksub() == 2 ? launch_pair_ks<EPI, 2, 256>(p, stream) : launch_pair_ks<EPI, 3, 256>(p, stream);
 }
 
 template <bool PAIR, int EPI, int BN>
@@ -1423,10 +1475,13 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e);
   p.status = ctx.status;
   p.wait_ns = ctx.wait_ns;
-  // L2 prefetch depth of B tiles in k-blocks (TPGQA_PREFETCH overrides).
+  // L2 prefetch depth of B tiles in k-blocks, issued by the TMA producer
+  // (TPGQA_PREFETCH overrides). Off by default: every prefetch costs the single
+  // producer thread about as much as a load, and the T=512 MLP block ran 4%
+  // slower with a depth of 8 and 10% slower with 32.
   static const int prefetch = [] {
     const char *e = getenv("TPGQA_PREFETCH");
-    return e ? atoi(e) : 8;
+    return e ? atoi(e) : 0;
   }();
   p.prefetch = prefetch;
   p.a_rows = pair ? 128 : a_rows;
@@ -1442,12 +1497,12 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     }
     split = choose_split(p.total_tiles, pair, min_stages < 0 ? 0 : min_stages);
   }
-  if (split < 1) split = 1;
+  if (split < 1 || (pair && bn != 256)) split = 1;  // split-K pairs run 256-column tiles
   p.split = split;
   // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand
   // and stage replaces KSUB 2-D copies. The single-CTA kernels load one k-tile
   // per stage and keep the 2-D maps.
-  p.box_kt = pair ? use_3d_boxes(split > 1 ? SplitCfg<true, 256>::kSub : pair_ksub()) : 1;
+  p.box_kt = pair ? use_3d_boxes(split > 1 || bn != 256 ? SplitCfg<true, 256>::kSub : pair_ksub()) : 1;
   if (split > 1) {
     if (pair) {
       if (epi == kEpiF32) return launch_splitk<true, kEpiF32, 256>(p, stream);
@@ -1464,9 +1519,9 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     return launch_splitk<false, kEpiSwiGLU, 256>(p, stream);
   }
   if (pair) {
-    if (epi == kEpiF32) return launch_pair<kEpiF32>(p, stream);
-    if (epi == kEpiBF16) return launch_pair<kEpiBF16>(p, stream);
-    return launch_pair<kEpiSwiGLU>(p, stream);
+    if (epi == kEpiF32) return launch_pair<kEpiF32>(p, bn, stream);
+    if (epi == kEpiBF16) return launch_pair<kEpiBF16>(p, bn, stream);
+    return launch_pair<kEpiSwiGLU>(p, bn, stream);
   }
   if (bn == 256) {
     if (epi == kEpiF32) return launch_one<256, kEpiF32>(p, stream);
@@ -1525,6 +1580,41 @@ int choose_bn(long long rows) {
   // boxes per stage), where 256-column tiles with split-K stream weights faster.
   (void)rows;
   return 256;
+}
+
+int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, int *b_rows) {
+  // TPGQA_PAIR_BN=224|256 forces the SM-pair tile width (tuning override).
+  static const int forced = [] {
+    const char *e = getenv("TPGQA_PAIR_BN");
+    return e ? atoi(e) : 0;
+  }();
+  int best = 256;
+  if (forced == 224 || forced == 256) {
+    best = forced;
+  } else {
+    // A tile's time goes with its stage bytes (the loads bound the pair's
+    // k-loop), the kernel's with the number of waves of tiles over the SM
+    // pairs. Narrower tiles win when they save a wave. Grids small enough for
+    // split-K keep 256 columns (the split-K pair kernel runs only those).
+    const long long pairs = num_sms() / 2;
+    const long long mt = (m + 255) / 256;
+    long long cost256 = 0;
+    for (int bn : {256, 224}) {
+      const int out_cols = swiglu ? bn / 2 : bn;
+      long long tiles = 0;
+      for (int i = 0; i < nprob; ++i) tiles += mt * ((ncols[i] + out_cols - 1) / out_cols);
+      const long long waves = (tiles + pairs - 1) / pairs;
+      const long long cost = waves * (2 * (16384 + (bn / 2) * 128));
+      if (bn == 256) {
+        cost256 = cost;
+        if (tiles * 4 <= num_sms()) break;  // split-K territory
+      } else if (cost < cost256) {
+        best = bn;
+      }
+    }
+  }
+  *b_rows = best / 2;
+  return best;
 }
 
 int a_box_rows(long long rows) {

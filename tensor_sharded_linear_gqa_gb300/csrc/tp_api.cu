@@ -138,14 +138,19 @@ tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, c
   (void)t128;
   b.bn = choose_bn(T);
   b.pair = choose_pair(T);
-  if (b.pair) b.bn = 256;
+  int b_rows = b.bn;
+  if (b.pair) {
+    std::vector<long long> nc(nb);
+    for (int32_t r = 0; r < nb; ++r) nc[r] = w[r].rows;
+    b.bn = choose_pair_bn(T, nc.data(), nb, false, &b_rows);
+  }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
   const int am = b.add_map(x.ptr, T, K, x.ld, b.a_rows, &err);
   if (am < 0) return err;
   for (int32_t r = 0; r < nb; ++r) {
     if (w[r].rows == 0) continue;
-    const int bm = b.add_map(w[r].ptr, w[r].rows, K, w[r].ld, b.pair ? 128 : b.bn, &err);
+    const int bm = b.add_map(w[r].ptr, w[r].rows, K, w[r].ld, b_rows, &err);
     if (bm < 0) return err;
     const long long ks = K;
     if (!b.add_problem(static_cast<int>(T), static_cast<int>(w[r].rows), outs[r].ptr, outs[r].ld,
@@ -167,7 +172,11 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
   (void)mt;
   b.bn = choose_bn(T);
   b.pair = choose_pair(T);
-  if (b.pair) b.bn = 256;
+  int b_rows = b.bn;
+  if (b.pair) {
+    const std::vector<long long> nc(static_cast<size_t>(probs), nout);
+    b.bn = choose_pair_bn(T, nc.data(), static_cast<int>(probs), false, &b_rows);
+  }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
   std::vector<int> am(n), bm(n);
@@ -175,7 +184,7 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
   for (int32_t r = 0; r < n; ++r) {
     am[r] = b.add_map(x[r].ptr, T, x[r].cols, x[r].ld, b.a_rows, &err);
     if (am[r] < 0) return err;
-    bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, b.pair ? 128 : b.bn, &err);
+    bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, b_rows, &err);
     if (bm[r] < 0) return err;
     ks[r] = x[r].cols;
   }
@@ -543,12 +552,17 @@ tp_status launch_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *
   (void)mt;
   b.bn = choose_bn(T);
   b.pair = choose_pair(T);
-  if (b.pair) b.bn = 256;
+  if (b.pair) {
+    const std::vector<long long> nc(static_cast<size_t>(n), Fr);
+    int b_rows = 0;
+    b.bn = choose_pair_bn(T, nc.data(), n, true, &b_rows);
+  }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
   const int am = b.add_map(x->ptr, T, D, x->ld, b.a_rows, &err);
   if (am < 0) return err;
   for (int32_t r = 0; r < n; ++r) {
+    // gate and up each fill half of a tile's accumulator columns
     const int gm = b.add_map(w_gate[r].ptr, Fr, D, w_gate[r].ld, b.bn / 2, &err);
     if (gm < 0) return err;
     const int um = b.add_map(w_up[r].ptr, Fr, D, w_up[r].ld, b.bn / 2, &err);

@@ -130,9 +130,10 @@ struct GemmParams {
 struct GemmBuilder {
   GemmParams p;
   int n_maps = 0, n_probs = 0, n_segs = 0;
-  int bn = 256;       // CTA tile width in accumulator columns (128 or 256)
+  int bn = 256;       // tile width in accumulator columns (single CTA: 128 or 256;
+                      // SM pair: 256 or 224)
   int epi = kEpiF32;
-  bool pair = false;  // SM-pair kernel: 256 x 256 tiles, cta_group::2 (bn must be 256)
+  bool pair = false;  // SM-pair kernel: 256 x bn tiles, cta_group::2
   int a_rows = 128;   // A box rows of the single-CTA kernels (see a_box_rows)
   int split = 0;      // 0: chosen at launch; >1: split-K over a cluster, reduced in fixed
                       // order through DSMEM; 1: the persistent kernels
@@ -163,6 +164,10 @@ struct GemmBuilder {
 int choose_bn(long long rows);
 // Rows of an A box for problems of `rows` rows on the single-CTA kernels.
 int a_box_rows(long long rows);
+// Tile width of the SM-pair kernel (256 or 224 accumulator columns) for
+// problems of m rows and ncols[i] output columns; *b_rows receives the rows of
+// a B box (bn / 2: each CTA of the pair loads half of B).
+int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, int *b_rows);
 // Whether to run the SM-pair kernel for problems of this many rows.
 bool choose_pair(long long rows);
 // Split-K factor for `tiles` output tiles of `stages_per_tile` k-stages each
