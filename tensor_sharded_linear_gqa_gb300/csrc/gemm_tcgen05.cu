@@ -35,15 +35,27 @@ constexpr int BK = 64;  // bf16 elements in one 128-byte swizzled row
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;
 
+// Single-CTA tiles: 128 x BN, one 64-wide k-tile per pipeline stage. A stage
+// holds a_rows x 128 bytes of A (the rows loaded) followed by BN x 128 bytes of
+// B, so the number of stages, and with it the bytes in flight per SM, follows
+// a_rows: at T = 64, five 40 KB stages instead of four 48 KB ones. The host
+// computes the count (one_stages_for) and the kernel reads it from its params.
 template <int BN>
 struct TileCfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
-  static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kStages * kStageBytes + kBarBytes;
 };
+constexpr int kMaxOneStages = 8;
+constexpr int kSmemLimit = 227 * 1024;  // dynamic shared memory per CTA on sm_100-class GPUs
+
+// Stages of the single-CTA kernels for A boxes of a_rows rows and BN-column tiles.
+inline int one_stages_for(int a_rows, int bn) {
+  const int stage = a_rows * BK * 2 + bn * BK * 2;
+  int s = (kSmemLimit - 1024 - 256) / stage;
+  return s > kMaxOneStages ? kMaxOneStages : s;
+}
+inline int one_smem_bytes(int a_rows, int bn, int stages) {
+  return 1024 + stages * (a_rows * BK * 2 + bn * BK * 2) + 256;
+}
 
 __device__ __forceinline__ void record(int *status, int code) { atomicCAS(status, 0, code); }
 
@@ -171,25 +183,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  const uint32_t sA0 = ptx::smem_addr(smem);
-  const uint32_t sB0 = sA0 + C::kStages * C::kABytes;
-  uint8_t *bar_area = smem + C::kStages * C::kStageBytes;
+  // stage st: A (a_rows x 128 B) at sbase + st*kStage, B right after it
+  const int kStagesRt = p.one_stages;
+  const uint32_t kAT = static_cast<uint32_t>(p.a_rows) * 128u;
+  const uint32_t kStage = kAT + C::kBBytes;
+  const uint32_t sbase = ptx::smem_addr(smem);
+  auto a_slot = [&](int st) { return sbase + static_cast<uint32_t>(st) * kStage; };
+  auto b_slot = [&](int st) { return sbase + static_cast<uint32_t>(st) * kStage + kAT; };
+  uint8_t *bar_area = smem + static_cast<uint32_t>(kStagesRt) * kStage;
   const uint32_t bar0 = ptx::smem_addr(bar_area);
   // layout: full[S], empty[S], tmem_full[2], tmem_empty[2], drain, then slot / flag words
   auto full_bar = [&](int i) { return bar0 + 8u * i; };
-  auto empty_bar = [&](int i) { return bar0 + 8u * (C::kStages + i); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::kStages + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::kStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 4);
-  volatile uint32_t *tmem_slot =
-      reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * C::kStages + 5));
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * C::kStages + 5) + 4);
+  auto empty_bar = [&](int i) { return bar0 + 8u * (kStagesRt + i); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStagesRt + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStagesRt + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStagesRt + 4);
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * kStagesRt + 5));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * kStagesRt + 5) + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < kStagesRt; ++i) {
       ptx::mbar_init(full_bar(i), 1);
       ptx::mbar_init(empty_bar(i), 1);
     }
@@ -237,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
           prefetch(pf);
           cursor_next(p, pf);
         }
-        const int st = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
+        const int st = kb % kStagesRt;
+        const uint32_t ph = (kb / kStagesRt) & 1;
         if (*abort_flag) break;
         if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
           record(p.status, kDevTimeoutProducer);
@@ -247,13 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
         }
         const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
         ptx::mbar_arrive_expect_tx(full_bar(st), static_cast<uint32_t>(p.a_rows * 128 + C::kBBytes));
-        ptx::tma_load_2d(sA0 + st * C::kABytes, &p.maps[sg.a_map], ld.kt * BK, ld.mt * BM,
-                         full_bar(st));
-        ptx::tma_load_2d(sB0 + st * C::kBBytes, &p.maps[sg.b_map], ld.kt * BK, ld.nt * kBRows,
-                         full_bar(st));
+        ptx::tma_load_2d(a_slot(st), &p.maps[sg.a_map], ld.kt * BK, ld.mt * BM, full_bar(st));
+        ptx::tma_load_2d(b_slot(st), &p.maps[sg.b_map], ld.kt * BK, ld.nt * kBRows, full_bar(st));
         if (EPI == kEpiSwiGLU)
-          ptx::tma_load_2d(sB0 + st * C::kBBytes + kBRows * 128, &p.maps[sg.b2_map], ld.kt * BK,
-                           ld.nt * kBRows, full_bar(st));
+          ptx::tma_load_2d(b_slot(st) + kBRows * 128, &p.maps[sg.b2_map], ld.kt * BK, ld.nt * kBRows,
+                           full_bar(st));
         issued = ++kb;
         cursor_next(p, ld);
       }
@@ -275,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
         const uint32_t d = tmem_base + static_cast<uint32_t>(a * BN);
         const int nk = tile_k_tiles(p, find_problem(p, tile));
         for (int k0 = 0; k0 < nk; ++k0, ++kb) {
-          const int st = kb % C::kStages;
-          const uint32_t ph = (kb / C::kStages) & 1;
+          const int st = kb % kStagesRt;
+          const uint32_t ph = (kb / kStagesRt) & 1;
           if (*abort_flag) { ok = false; break; }
           if (!ptx::mbar_wait(full_bar(st), ph, p.wait_ns)) {
             record(p.status, kDevTimeoutMma);
@@ -285,8 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t ad = ptx::smem_desc_sw128(sA0 + st * C::kABytes);
-          const uint64_t bd = ptx::smem_desc_sw128(sB0 + st * C::kBBytes);
+          // A rows past a_rows read the next bytes of the stage (B): their
+          // accumulator rows are never stored
+          const uint64_t ad = ptx::smem_desc_sw128(a_slot(st));
+          const uint64_t bd = ptx::smem_desc_sw128(b_slot(st));
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k)
             ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (k0 | k) != 0 ? 1u : 0u);
@@ -366,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   __syncthreads();
   if (*abort_flag && threadIdx.x == 0) {
     // Loads the producer started must land before the CTA's shared memory goes away.
-    const int first = issued > C::kStages ? issued - C::kStages : 0;
+    const int first = issued > kStagesRt ? issued - kStagesRt : 0;
     for (int kb = first; kb < issued; ++kb)
-      if (!ptx::mbar_wait(full_bar(kb % C::kStages), (kb / C::kStages) & 1, p.wait_ns))
+      if (!ptx::mbar_wait(full_bar(kb % kStagesRt), (kb / kStagesRt) & 1, p.wait_ns))
         record(p.status, kDevTimeoutDrain);
   }
   __syncthreads();
@@ -797,15 +813,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   using C = SplitCfg<PAIR, BN>;
   static_assert(!PAIR || BN == 256, "SM pairs run 256-column tiles");
   constexpr int KS = C::kSub;
-  constexpr int S = C::kStages;
+  // SM pairs: fixed stages of 128-row A k-tiles. Single CTAs: an A k-tile holds
+  // the a_rows rows loaded and the stage count comes from the host.
+  const int S = PAIR ? C::kStages : p.one_stages;
+  const uint32_t kAT = PAIR ? static_cast<uint32_t>(C::kABytes) : static_cast<uint32_t>(p.a_rows) * 128u;
+  const uint32_t kStageArea = static_cast<uint32_t>(S * KS) * (kAT + C::kBBytes);
   constexpr uint32_t kTmemCols = BN;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sA0 = ptx::smem_addr(smem);
-  const uint32_t sB0 = sA0 + S * KS * C::kABytes;
-  uint8_t *bar_area = smem + S * C::kStageBytes;
+  const uint32_t sB0 = sA0 + static_cast<uint32_t>(S * KS) * kAT;
+  uint8_t *bar_area = smem + kStageArea;
   const uint32_t bar0 = ptx::smem_addr(bar_area);
   auto full_bar = [&](int i) { return bar0 + 8u * i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (S + i); };
@@ -906,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
         if (PAIR && p.box_kt > 1) {
           // 3-D maps: one copy per operand brings the stage's KS k-tiles
           const int z = kt * KS;  // past the segment's K: zero fill
-          ptx::tma_load_3d_pair(sA0 + st * KS * C::kABytes, &p.maps[sg.a_map], 0, a_row, z, fb);
+          ptx::tma_load_3d_pair(sA0 + st * KS * kAT, &p.maps[sg.a_map], 0, a_row, z, fb);
           if (EPI == kEpiSwiGLU)
             ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[member == 0 ? sg.b_map : sg.b2_map], 0,
                                   nt * 128, z, fb);
@@ -917,7 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
 #pragma unroll
           for (int j = 0; j < KS; ++j) {
             const int x = (kt * KS + j) * BK;  // past the segment's K: zero fill
-            const uint32_t da = sA0 + (st * KS + j) * C::kABytes;
+            const uint32_t da = sA0 + (st * KS + j) * kAT;
             const uint32_t db = sB0 + (st * KS + j) * C::kBBytes;
             if constexpr (PAIR) {
               ptx::tma_load_2d_pair(da, &p.maps[sg.a_map], x, a_row, fb);
@@ -958,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
         ptx::tc_fence_after();
 #pragma unroll
         for (int j = 0; j < KS; ++j) {
-          const uint64_t ad = ptx::smem_desc_sw128(sA0 + (st * KS + j) * C::kABytes);
+          const uint64_t ad = ptx::smem_desc_sw128(sA0 + (st * KS + j) * kAT);
           const uint64_t bd = ptx::smem_desc_sw128(sB0 + (st * KS + j) * C::kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
@@ -1002,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   // Bulk path: stage the whole accumulator in own shared memory, then send each
   // owner its contiguous block of rows with one bulk copy; the owner receives the
   // other splits' blocks after its own staging area. Needs room for both.
-  const bool bulk = (128 + (nsplit - 1) * rows_per) * kRowBytes <= S * C::kStageBytes;
+  const bool bulk = static_cast<uint32_t>((128 + (nsplit - 1) * rows_per) * kRowBytes) <= kStageArea;
   if (bulk) {
     const uint32_t recv0 = red0 + 128u * kRowBytes;  // slot j: rows_per rows of split (j < split ? j : j + 1)
     if (warp >= 2) {
@@ -1260,14 +1280,14 @@ tp_status launch_one(const GemmParams &p, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> g(mu);
     if (dev >= 32 || !(configured_mask & (1 << dev))) {
-      e = cudaFuncSetAttribute(k_gemm_bf16<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               TileCfg<BN>::kSmem);
+      e = cudaFuncSetAttribute(k_gemm_bf16<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 32) configured_mask |= (1 << dev);
     }
   }
   const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
-  e = launch_kernel(k_gemm_bf16<BN, EPI>, dim3(grid), dim3(kThreads), TileCfg<BN>::kSmem, stream, 1, p);
+  e = launch_kernel(k_gemm_bf16<BN, EPI>, dim3(grid), dim3(kThreads), one_smem_bytes(p.a_rows, BN, p.one_stages),
+                    stream, 1, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
@@ -1327,14 +1347,15 @@ tp_status launch_splitk(const GemmParams &p, cudaStream_t stream) {
     std::lock_guard<std::mutex> g(mu);
     if (dev >= 32 || !(configured_mask & (1 << dev))) {
       e = cudaFuncSetAttribute(k_gemm_bf16_splitk<PAIR, EPI, BN>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR ? C::kSmem : kSmemLimit);
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 32) configured_mask |= (1 << dev);
     }
   }
   const int csize = (PAIR ? 2 : 1) * p.split;
+  const int smem = PAIR ? C::kSmem : one_smem_bytes(p.a_rows, BN, p.one_stages);
   e = launch_kernel(k_gemm_bf16_splitk<PAIR, EPI, BN>, dim3(static_cast<unsigned>(p.total_tiles * csize)),
-                    dim3(kThreads), C::kSmem, stream, static_cast<unsigned>(csize), p);
+                    dim3(kThreads), smem, stream, static_cast<unsigned>(csize), p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
@@ -1485,6 +1506,7 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   }();
   p.prefetch = prefetch;
   p.a_rows = pair ? 128 : a_rows;
+  p.one_stages = one_stages_for(p.a_rows, bn);
   if (split == 0) {
     // fewest k-stages of any problem decides how far K can be split
     const int ksub = pair ? 2 : 1;

@@ -122,6 +122,7 @@ struct GemmParams {
                  // it is smaller: accumulator rows past it are never stored)
   int box_kt;    // 64-wide k-tiles per TMA copy: 1 = 2-D maps (one copy per k-tile),
                  // >1 = 3-D maps whose box spans that many k-tiles (a whole stage)
+  int one_stages;  // pipeline stages of the single-CTA kernels (sized from a_rows)
   int *status;
   long long wait_ns;
 };
