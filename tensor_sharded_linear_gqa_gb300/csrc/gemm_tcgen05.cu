@@ -178,7 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   constexpr int kBRows = (EPI == kEpiSwiGLU) ? BN / 2 : BN;  // rows per B map box
   constexpr int kOutCols = (EPI == kEpiSwiGLU) ? BN / 2 : BN;
   const int kPrefetch = p.prefetch;
-  constexpr uint32_t kTmemCols = 2 * BN;
+  // Two accumulators; TMEM is allocated in powers of two, so BN in (128, 256]
+  // takes 512 columns with the accumulators at columns 0 and 256.
+  constexpr uint32_t kAccStride = BN <= 128 ? 128 : 256;
+  constexpr uint32_t kTmemCols = 2 * kAccStride;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(a * BN);
+        const uint32_t d = tmem_base + static_cast<uint32_t>(a) * kAccStride;
         const int nk = tile_k_tiles(p, find_problem(p, tile));
         for (int k0 = 0; k0 < nk; ++k0, ++kb) {
           const int st = kb % kStagesRt;
@@ -332,12 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
       const int mt = local % pr.m_tiles;
       const int nt = local / pr.m_tiles;
       const int row = mt * BM + q * 32 + lane;
-      const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * BN) +
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(a) * kAccStride +
                              (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (EPI == kEpiSwiGLU) {
+        // gate sums in accumulator columns [0, BN/2), up sums in [BN/2, BN)
         __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(pr.out);
+        constexpr int kFull = (BN / 2) / 32 * 32;  // columns handled 32 at a time
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = 0; c < kFull; c += 32) {
           uint32_t g[32], u[32];
           ptx::tmem_ld_32cols(tbase + c, g);
           ptx::tmem_ld_32cols(tbase + BN / 2 + c, u);
@@ -352,7 +357,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
           for (int jj = 0; jj < 32; ++jj) h[jj] = silu(__uint_as_float(g[jj])) * __uint_as_float(u[jj]);
           if (row < pr.m) store_bf16_row32(out, pr.ldc, row, nt * kOutCols + c, pr.n, h);
         }
+        if constexpr (BN / 2 > kFull) {
+          static_assert(BN / 2 - kFull == 16, "a 16-column tail");
+          uint32_t g[16], u[16];
+          ptx::tmem_ld_16cols(tbase + kFull, g);
+          ptx::tmem_ld_16cols(tbase + BN / 2 + kFull, u);
+          ptx::tmem_ld_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(tempty_bar(a));
+          float h[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) h[jj] = silu(__uint_as_float(g[jj])) * __uint_as_float(u[jj]);
+          if (row < pr.m) store_bf16_row16(out, pr.ldc, row, nt * kOutCols + kFull, pr.n, h);
+        }
       } else {
+        static_assert(BN % 32 == 0, "32-column epilogue chunks");
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t v[32];
@@ -1068,8 +1088,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
             red0 + static_cast<uint32_t>(o * rows_per * kRowBytes),
             static_cast<uint32_t>(rows_per * kRowBytes), ptx::mapa_shared(recv_bar, dst_rank));
       }
+    }
+    // All six warps (the producer and MMA warps are idle by now) wait for the
+    // other splits' rows and share the summation and the stores.
+    {
+      const int tid = threadIdx.x;
       const bool got = ptx::mbar_wait(recv_bar, 0, p.wait_ns);
-      if (!got && lane == 0) record(p.status, kDevTimeoutEpilogue);
+      if (!got && tid == 0) record(p.status, kDevTimeoutEpilogue);
       if (got && *abort_flag == 0) {
         // Sum the owned rows over splits in order 0..S-1. Problem fields live in
         // registers; each thread takes kBatch units and issues every shared load
@@ -1082,7 +1107,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
         constexpr int kBatch = (EPI == kEpiSwiGLU) ? 4 : 8;
         constexpr int kMaxSplit = PAIR ? 4 : 8;
         const int total = rows_per * kUnits;
-        for (int base = tid; base < total; base += 128 * kBatch) {
+        for (int base = tid; base < total; base += kThreads * kBatch) {
           float4 g[kBatch], u[kBatch];
 #pragma unroll
           for (int t = 0; t < kMaxSplit; ++t) {
@@ -1090,7 +1115,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
             float4 vg[kBatch], vu[kBatch];
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
-              const int idx = base + b * 128 < total ? base + b * 128 : base;
+              const int idx = base + b * kThreads < total ? base + b * kThreads : base;
               const int rl = idx / kUnits;
               const int c4 = idx % kUnits;
               const int prow = (t == split) ? lo + rl : 128 + (t < split ? t : t - 1) * rows_per + rl;
@@ -1114,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
           }
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
-            const int idx = base + b * 128;
+            const int idx = base + b * kThreads;
             if (idx >= total) break;
             const int rl = idx / kUnits;
             const int grow = row0 + lo + rl;
@@ -1519,7 +1544,8 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     }
     split = choose_split(p.total_tiles, pair, min_stages < 0 ? 0 : min_stages);
   }
-  if (split < 1 || (pair && bn != 256)) split = 1;  // split-K pairs run 256-column tiles
+  if (split < 1 || (pair && bn != 256) || (!pair && bn != 256 && bn != 128))
+    split = 1;  // split-K runs 256-column pair tiles and 128/256-column single-CTA tiles
   p.split = split;
   // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand
   // and stage replaces KSUB 2-D copies. The single-CTA kernels load one k-tile
@@ -1549,6 +1575,16 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     if (epi == kEpiF32) return launch_one<256, kEpiF32>(p, stream);
     if (epi == kEpiBF16) return launch_one<256, kEpiBF16>(p, stream);
     return launch_one<256, kEpiSwiGLU>(p, stream);
+  }
+  if (bn == 224) {
+    if (epi == kEpiF32) return launch_one<224, kEpiF32>(p, stream);
+    if (epi == kEpiBF16) return launch_one<224, kEpiBF16>(p, stream);
+    return launch_one<224, kEpiSwiGLU>(p, stream);
+  }
+  if (bn == 192) {
+    if (epi == kEpiF32) return launch_one<192, kEpiF32>(p, stream);
+    if (epi == kEpiBF16) return launch_one<192, kEpiBF16>(p, stream);
+    return launch_one<192, kEpiSwiGLU>(p, stream);
   }
   if (epi == kEpiF32) return launch_one<128, kEpiF32>(p, stream);
   if (epi == kEpiBF16) return launch_one<128, kEpiBF16>(p, stream);
@@ -1590,18 +1626,33 @@ int choose_split(long long tiles, bool pair, long long stages_per_tile) {
   return s;
 }
 
-int choose_bn(long long rows) {
-  // TPGQA_BN=128|256 forces the tile width (tuning override).
+int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu) {
+  // TPGQA_BN=128|192|224|256 forces the tile width (tuning override).
   static const int forced = [] {
     const char *e = getenv("TPGQA_BN");
     return e ? atoi(e) : 0;
   }();
-  if (forced == 128 || forced == 256) return forced;
-  // 128-column tiles need twice the operand bytes per MMA flop and starve the
-  // tensor pipe; they also measured slower on decode shapes (three small TMA
-  // boxes per stage), where 256-column tiles with split-K stream weights faster.
-  (void)rows;
-  return 256;
+  if (forced == 128 || forced == 192 || forced == 224 || forced == 256) return forced;
+  // Single-CTA tiles stream the weights (few rows of activations): a tile's time
+  // goes with its width, the kernel's with the waves of tiles over the SMs.
+  // 128-column tiles need twice the operand bytes per MMA flop; grids small
+  // enough for split-K keep 256 columns.
+  const long long sms = num_sms();
+  const long long mt = (rows + 127) / 128;
+  int best = 256;
+  long long best_cost = -1;
+  for (int bn : {256, 224, 192}) {
+    const int out_cols = swiglu ? bn / 2 : bn;
+    long long tiles = 0;
+    for (int i = 0; i < nprob; ++i) tiles += mt * ((ncols[i] + out_cols - 1) / out_cols);
+    if (bn == 256 && tiles * 2 <= sms) return 256;  // split-K territory
+    const long long cost = ((tiles + sms - 1) / sms) * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, int *b_rows) {

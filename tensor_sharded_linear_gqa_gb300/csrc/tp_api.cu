@@ -136,13 +136,17 @@ tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, c
   b.epi = epi;
   (void)t256;
   (void)t128;
-  b.bn = choose_bn(T);
   b.pair = choose_pair(T);
-  int b_rows = b.bn;
-  if (b.pair) {
+  int b_rows = 0;
+  {
     std::vector<long long> nc(nb);
     for (int32_t r = 0; r < nb; ++r) nc[r] = w[r].rows;
-    b.bn = choose_pair_bn(T, nc.data(), nb, false, &b_rows);
+    if (b.pair) {
+      b.bn = choose_pair_bn(T, nc.data(), nb, false, &b_rows);
+    } else {
+      b.bn = choose_bn(T, nc.data(), nb, false);
+      b_rows = b.bn;
+    }
   }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
@@ -170,12 +174,16 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
   b.epi = kEpiF32;
   (void)probs;
   (void)mt;
-  b.bn = choose_bn(T);
   b.pair = choose_pair(T);
-  int b_rows = b.bn;
-  if (b.pair) {
+  int b_rows = 0;
+  {
     const std::vector<long long> nc(static_cast<size_t>(probs), nout);
-    b.bn = choose_pair_bn(T, nc.data(), static_cast<int>(probs), false, &b_rows);
+    if (b.pair) {
+      b.bn = choose_pair_bn(T, nc.data(), static_cast<int>(probs), false, &b_rows);
+    } else {
+      b.bn = choose_bn(T, nc.data(), static_cast<int>(probs), false);
+      b_rows = b.bn;
+    }
   }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
@@ -550,12 +558,11 @@ tp_status launch_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *
   b.epi = kEpiSwiGLU;
   const long long mt = (T + 127) / 128;
   (void)mt;
-  b.bn = choose_bn(T);
   b.pair = choose_pair(T);
-  if (b.pair) {
+  {
     const std::vector<long long> nc(static_cast<size_t>(n), Fr);
     int b_rows = 0;
-    b.bn = choose_pair_bn(T, nc.data(), n, true, &b_rows);
+    b.bn = b.pair ? choose_pair_bn(T, nc.data(), n, true, &b_rows) : choose_bn(T, nc.data(), n, true);
   }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;

@@ -131,8 +131,8 @@ struct GemmParams {
 struct GemmBuilder {
   GemmParams p;
   int n_maps = 0, n_probs = 0, n_segs = 0;
-  int bn = 256;       // tile width in accumulator columns (single CTA: 128 or 256;
-                      // SM pair: 256 or 224)
+  int bn = 256;       // tile width in accumulator columns (single CTA: 128, 192,
+                      // 224 or 256; SM pair: 256 or 224)
   int epi = kEpiF32;
   bool pair = false;  // SM-pair kernel: 256 x bn tiles, cta_group::2
   int a_rows = 128;   // A box rows of the single-CTA kernels (see a_box_rows)
@@ -161,8 +161,9 @@ struct GemmBuilder {
   tp_status launch(cudaStream_t stream);
 };
 
-// Picks the tile width (128 or 256 accumulator columns) for problems of `rows` rows.
-int choose_bn(long long rows);
+// Tile width of the single-CTA kernels (256, 224 or 192 accumulator columns)
+// for problems of `rows` rows and ncols[i] output columns.
+int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu);
 // Rows of an A box for problems of `rows` rows on the single-CTA kernels.
 int a_box_rows(long long rows);
 // Tile width of the SM-pair kernel (256 or 224 accumulator columns) for

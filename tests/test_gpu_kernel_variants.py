@@ -6,10 +6,11 @@ k-tiles per pipeline stage, and a split-K cluster kernel for either, depending
 on the shape. The SM-pair kernels fetch each stage with one 3-D TMA copy per
 operand when every K is a multiple of 64, else with one 2-D copy per k-tile.
 Split-K reduces the splits' partials through the cluster's shared memory in a
-fixed order. The persistent SM-pair kernel runs 256- or 224-column tiles. The
-tuning overrides TPGQA_PAIR, TPGQA_KSUB, TPGQA_SPLIT, TPGQA_TMA3D and
-TPGQA_PAIR_BN force one variant, so each variant here reruns the linear-layer
-and MLP parity tests in a child process with the override set.
+fixed order. The persistent SM-pair kernel runs 256- or 224-column tiles, the
+single-CTA kernel 128- to 256-column ones. The tuning overrides TPGQA_PAIR,
+TPGQA_KSUB, TPGQA_SPLIT, TPGQA_TMA3D, TPGQA_PAIR_BN and TPGQA_BN force one
+variant, so each variant here reruns the linear-layer and MLP parity tests in a
+child process with the override set.
 """
 import os
 import subprocess
@@ -25,16 +26,17 @@ TESTS = ["tests/test_gpu_linear.py",
          "tests/test_gpu_blocks.py::test_mlp_block_small_ragged"]
 
 
-@pytest.mark.parametrize("pair,split,ksub,tma3d,pair_bn", [
-    ("0", "1", "2", "1", "256"), ("1", "1", "2", "1", "256"), ("1", "1", "3", "1", "256"),
-    ("1", "1", "2", "0", "256"), ("1", "1", "3", "0", "256"), ("1", "1", "2", "1", "224"),
-    ("1", "1", "2", "0", "224"), ("0", "2", "2", "1", "256"), ("0", "4", "2", "1", "256"),
-    ("1", "2", "2", "1", "256"), ("1", "4", "2", "1", "256"), ("1", "2", "2", "0", "256")])
-def test_kernel_variant_parity(pair, split, ksub, tma3d, pair_bn):
+@pytest.mark.parametrize("pair,split,ksub,tma3d,pair_bn,bn", [
+    ("0", "1", "2", "1", "256", "256"), ("0", "1", "2", "1", "256", "224"), ("0", "1", "2", "1", "256", "192"),
+    ("0", "1", "2", "1", "256", "128"), ("1", "1", "2", "1", "256", "256"), ("1", "1", "3", "1", "256", "256"),
+    ("1", "1", "2", "0", "256", "256"), ("1", "1", "3", "0", "256", "256"), ("1", "1", "2", "1", "224", "256"),
+    ("1", "1", "2", "0", "224", "256"), ("0", "2", "2", "1", "256", "256"), ("0", "4", "2", "1", "256", "256"),
+    ("1", "2", "2", "1", "256", "256"), ("1", "4", "2", "1", "256", "256"), ("1", "2", "2", "0", "256", "256")])
+def test_kernel_variant_parity(pair, split, ksub, tma3d, pair_bn, bn):
     from gpu_util import need_gpu
     need_gpu()
     env = dict(os.environ, TPGQA_PAIR=pair, TPGQA_SPLIT=split, TPGQA_KSUB=ksub, TPGQA_TMA3D=tma3d,
-               TPGQA_PAIR_BN=pair_bn)
+               TPGQA_PAIR_BN=pair_bn, TPGQA_BN=bn)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
                         *TESTS], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
