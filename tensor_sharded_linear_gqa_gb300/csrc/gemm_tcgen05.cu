@@ -2,15 +2,21 @@
 // [M x K] and B [N x K] both K-major (weights stored [out x in]), fp32
 // accumulation in tensor memory.
 //
-// Persistent: one CTA per SM walks 128 x BN output tiles of all problems
-// (tile t goes to CTA t mod gridDim.x). Warp roles:
-//   warp 0      TMA producer: one thread streams 128x64 A and BNx64 B tiles
-//               into a ring of shared-memory stages (128-byte swizzle), and
-//               prefetches B tiles a few k-blocks further ahead into L2.
-//   warp 1      owns TMEM (two BN-column fp32 accumulators; alloc / dealloc);
-//               one thread issues tcgen05.mma (M=128, N=BN, K=16, four per
-//               64-wide stage), frees each stage with tcgen05.commit and hands
-//               each finished accumulator to the epilogue.
+// Three kernels share one problem/segment model and one warp layout:
+//   k_gemm_bf16        persistent, one CTA per SM, 128 x BN tiles (BN 128..256),
+//                      used for at most 128 rows (decode);
+//   k_gemm_bf16_pair   persistent over 2-CTA clusters, 256 x BN tiles with
+//                      tcgen05.mma.cta_group::2 (BN 256 or 224);
+//   k_gemm_bf16_splitk one tile per cluster, K split over the cluster's CTAs and
+//                      reduced through distributed shared memory in fixed order.
+// Warp roles:
+//   warp 0      TMA producer: one thread streams A and B k-tiles into a ring of
+//               shared-memory stages (128-byte swizzle), one copy per operand
+//               per k-tile, or per stage with 3-D tensor maps.
+//   warp 1      owns TMEM (two fp32 accumulators; alloc / dealloc); one thread
+//               issues tcgen05.mma (K=16, four per 64-wide k-tile), frees each
+//               stage with tcgen05.commit and hands each finished accumulator
+//               to the epilogue.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp reads its
 //               32-lane quarter), fused output transform, global stores; the
 //               accumulator is released as soon as it has been read.
@@ -170,8 +176,8 @@ __device__ __forceinline__ int tile_k_tiles(const GemmParams &p, int prob) {
 
 // Persistent kernel: one CTA per SM walks tiles blockIdx.x + j * gridDim.x.
 // TMEM holds two accumulators, so the epilogue of tile j overlaps the MMAs of
-// tile j+1. The producer also prefetches B tiles kPrefetch k-blocks ahead into
-// L2, so the shared-memory ring waits on L2 rather than on DRAM.
+// tile j+1. The producer can also prefetch B tiles kPrefetch k-blocks ahead into
+// L2 (off by default: it slowed every measured shape).
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant__ GemmParams p) {
   using C = TileCfg<BN>;
@@ -415,15 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
 }
 
 // ---------------------------------------------------------------------------
-// Pair kernel: two CTAs of a cluster (an SM pair) compute one 256 x 256 tile
-// with tcgen05.mma.cta_group::2 (M=256, N=256, K=16). CTA r of the pair loads
-// A rows [128r, 128r+128) of the tile and one 128-row half of B (for SwiGLU:
-// the gate rows in CTA 0, the up rows in CTA 1), so each SM streams half the B
-// bytes of the single-CTA kernel per MMA flop. Only CTA 0 issues MMAs; its
-// commits arrive on the stage and accumulator barriers of both CTAs. Each CTA
-// holds its own 128 accumulator rows in TMEM (two 256-column buffers) and runs
-// its own epilogue; the epilogue warps of both CTAs release an accumulator on
-// CTA 0's barrier.
+// Pair kernel: two CTAs of a cluster (an SM pair) compute one 256 x BN tile
+// with tcgen05.mma.cta_group::2 (M=256, N=BN, K=16). CTA r of the pair loads
+// A rows [128r, 128r+128) of the tile and BN/2 rows of B (for SwiGLU: the gate
+// rows in CTA 0, the up rows in CTA 1), so each SM streams half the B bytes of
+// the single-CTA kernel per MMA flop. Only CTA 0 issues MMAs; its commits arrive
+// on the stage and accumulator barriers of both CTAs. Each CTA holds its own 128
+// accumulator rows in TMEM (two buffers, at columns 0 and 256) and runs its own
+// epilogue; the epilogue warps of both CTAs release an accumulator on CTA 0's
+// barrier.
 // ---------------------------------------------------------------------------
 // A stage holds KSUB consecutive 64-wide k-tiles (KSUB boxes of A and of B per
 // CTA under one barrier): the TMA unit of an SM delivers more bytes per clock
@@ -764,11 +770,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Split-K cluster kernel for problems with too few output tiles to fill the
 // GPU (small-token row-parallel layers, decode). A cluster computes one tile:
 // CTA ranks are (split, member), member = the M-half for SM pairs. Split s
-// accumulates k-stages [s*ns/S, (s+1)*ns/S) of the tile in TMEM, writes its fp32
-// accumulator to its own shared memory, and after a cluster barrier reduces a
-// slice of the tile's rows by reading that slice from every split's shared
-// memory (DSMEM) and adding in split order 0, 1, ..., S-1. The sum order is
-// fixed, so the result does not depend on timing; no global workspace is used.
+// accumulates k-stages [s*ns/S, (s+1)*ns/S) of the tile in TMEM. After a
+// cluster barrier each split owns a slice of the tile's rows: every CTA stages
+// its fp32 accumulator in its own shared memory and sends each owner that
+// owner's rows with one bulk copy into the owner's shared memory (DSMEM). The
+// owner adds the partials in split order 0, 1, ..., S-1 and stores. The sum
+// order is fixed, so the result does not depend on timing; no global workspace
+// is used. When the shared memory cannot hold the staged tile and the received
+// rows together, rows are pushed from registers with st.async instead.
 // ---------------------------------------------------------------------------
 // Stores one 16-byte unit (4 fp32 sums g, and for SwiGLU the matching up sums u)
 // of output row `grow` at unit c4 of tile column block nt, with the epilogue
