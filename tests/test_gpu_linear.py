@@ -160,6 +160,29 @@ def test_row_ring_modes_bitwise_equal():
         assert np.array_equal(host_bits_f32(a[r]), host_bits_f32(a[0]))
 
 
+@pytest.mark.parametrize("n,T,per,nout", [(2, 512, 4096, 2048), (4, 200, 2048, 264), (8, 64, 2048, 1000)])
+def test_row_ring_modes_bitwise_equal_split_k(n, T, per, nout):
+    """Shapes small enough in T for the split-K GEMM (pair and single-CTA,
+    ragged rows and columns): the one-pass ring all-reduce must give the step
+    ring's bits on every rank, on repeated calls, and the oracle's value."""
+    need_gpu()
+    x = inputs.normal_bf16(62, 0, (T, n * per))
+    wf = inputs.normal_bf16(62, 1, (nout, n * per), 0.02)
+    xs = [dev_bf16(x[:, r * per:(r + 1) * per]) for r in range(n)]
+    ws = [dev_bf16(wf[:, r * per:(r + 1) * per]) for r in range(n)]
+    a = _row_outputs(n, T, nout, tp.TP_COMBINE_RING)
+    tp.tp_row_linear(n, xs, ws, a, tp.TP_COMBINE_RING)
+    for rep in range(2):
+        b = _row_outputs(n, T, nout, tp.TP_COMBINE_RING_FUSED)
+        tp.tp_row_linear(n, xs, ws, b, tp.TP_COMBINE_RING_FUSED)
+        for r in range(n):
+            assert np.array_equal(host_bits_f32(a[r]), host_bits_f32(b[r])), (rep, r)
+    parts = O.row_parallel(O.split_cols(inputs.bf16_bits_to_f64(x), n),
+                           O.split_cols(inputs.bf16_bits_to_f64(wf), n))
+    assert_close(host_f64(b[0]), sum(parts), BF16_TOL, "ring fold vs oracle")
+    assert tp.tp_device_status() == (tp.TP_OK, 0)
+
+
 def test_column_gather_into_strided_output():
     need_gpu()
     t = torch()
