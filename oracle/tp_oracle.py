@@ -289,6 +289,40 @@ def gather_flat_shards(shards: list) -> np.ndarray:
     return np.concatenate([np.asarray(s).reshape(-1) for s in shards])
 
 
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bfloat16 (ties to even), returned as
+    float64. bfloat16 keeps the top 16 bits of an IEEE float32 (8 exponent bits,
+    7 stored mantissa bits); rounding adds half an ulp of the kept part, plus the
+    kept part's lowest bit for ties, then truncates."""
+    b = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).view(np.uint32).astype(np.uint64)
+    r = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def reduce_scatter_then_column(partials: list, w_shards: list, round_bf16: bool = False,
+                               log: RingLog | None = None) -> dict:
+    """A row-parallel result feeding a column-parallel op directly ([MLX] 통신 패턴,
+    Reduce-scatter: used when a row-parallel result goes straight into a
+    column-parallel op; the all-gather step is avoided).
+
+    The per-rank partials [T x K] are reduce-scattered on the ring (rank c ends
+    holding reduced chunk c); optionally the reduced values are rounded to
+    bfloat16, the operand type of the next GEMM. The column-parallel op then
+    multiplies the input made of the N reduced chunks, taken where they lie, by
+    each rank's weight shard. Returns the chunks, that input and the outputs.
+    """
+    n = len(partials)
+    t, k = np.asarray(partials[0]).shape
+    rs = ring_reduce_scatter(partials, log)
+    chunks = []
+    for c in range(n):
+        lo, hi = chunk_bounds(t * k, n, c)
+        v = rs[c][lo:hi]
+        chunks.append(round_to_bf16(v) if round_bf16 else v)
+    x = gather_flat_shards(chunks).reshape(t, k)
+    return {"chunks": chunks, "x": x, "y": column_parallel(x.astype(np.float64), w_shards)}
+
+
 # ---------------------------------------------------------------------------
 # Blocks ([MLX] 아키텍처 인식 샤드 플랜; [WIKI] 상세 1, last paragraph)
 # ---------------------------------------------------------------------------
