@@ -225,6 +225,42 @@ tp_status tp_all_gather(int32_t tp_size, const tp_tensor *shard, tp_tensor *out,
                         int32_t axis, tp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Row-parallel -> column-parallel pipeline without the all-gather (mlxcel
+ * manual, 통신 패턴 / Communication patterns, Reduce-scatter: used when the
+ * result of a row-parallel op goes straight into a column-parallel op; the
+ * all-gather step is avoided).
+ * ------------------------------------------------------------------------- */
+
+/* One-pass ring reduce-scatter of f32 partials into bf16 chunks.
+ *  partial[r] : rank r's f32 [T x n] partial, contiguous (ld == cols), 16-byte
+ *               aligned; read only.
+ *  out[r]     : rank r's bf16 [T x n] buffer (any ld, a multiple of 8); only
+ *               chunk r (flat range [floor(r*S/N), floor((r+1)*S/N)) of the
+ *               row-major [T x n] view) is written, with the sum of chunk r
+ *               over the ranks in the ring's order r+1, r+2, ..., r, in f32,
+ *               rounded once to bf16 (nearest even). The rest of out[r] is
+ *               left as it was.
+ * The f32 sums are bit-identical to tp_reduce_scatter's. bf16 is the operand
+ * type of the column-parallel GEMM that reads the chunks next.
+ * Errors: TP_ERR_INVALID_ARG (sizes differ, N not a power of two), TP_ERR_DTYPE,
+ * TP_ERR_ALIGNMENT, TP_ERR_RANK_FAILED, TP_ERR_CUDA. */
+tp_status tp_reduce_scatter_bf16(int32_t tp_size, const tp_tensor *partial, tp_tensor *out,
+                                 tp_stream_t stream);
+
+/* Column-parallel linear whose input is the N reduced chunks where they lie:
+ * rank c's buffer holds rows [c*T/N, (c+1)*T/N) of X (chunk c of a reduce-
+ * scatter), and the GEMM reads each block of rows from its chunk's buffer, so
+ * no all-gather runs. Y_r = X * W_r^T as in tp_column_linear.
+ *  x_chunks[c] : bf16 [T x K] buffer of rank c; rows [c*T/N, (c+1)*T/N) are
+ *                read, the rest is ignored. T must be a multiple of N (chunk
+ *                boundaries on rows), else TP_ERR_NOT_DIVISIBLE.
+ *  w[r], y, gather : as tp_column_linear (bf16 weights).
+ * Results are bit-identical to tp_column_linear on the assembled X.
+ * Errors: as tp_column_linear, plus TP_ERR_NOT_DIVISIBLE. */
+tp_status tp_column_linear_chunks(int32_t tp_size, const tp_tensor *x_chunks, const tp_tensor *w,
+                                  tp_tensor *y, int32_t gather, tp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Blocks (mlxcel manual, 아키텍처 인식 샤드 플랜: gate/up ColumnParallel with no
  * communication, down RowParallel + AllReduce; q/k/v ColumnParallel, o
  * RowParallel + AllReduce).

@@ -80,6 +80,8 @@ _SIGS = {
     "tp_column_linear": ([ctypes.c_int32, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_row_linear": ([ctypes.c_int32, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_reduce_scatter": ([ctypes.c_int32, _T, ctypes.c_int32, _S], ctypes.c_int),
+    "tp_reduce_scatter_bf16": ([ctypes.c_int32, _T, _T, _S], ctypes.c_int),
+    "tp_column_linear_chunks": ([ctypes.c_int32, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_ring_all_gather": ([ctypes.c_int32, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_allreduce_ring": ([ctypes.c_int32, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_all_gather": ([ctypes.c_int32, _T, _T, ctypes.c_int32, ctypes.c_int32, _S], ctypes.c_int),
@@ -246,6 +248,18 @@ def tp_row_linear(tp_size: int, x, w, y, combine: int, stream=None) -> None:
 
 def tp_reduce_scatter(tp_size: int, bufs, mode: int = TP_RING_STEPS, stream=None) -> None:
     _check(_lib.tp_reduce_scatter(tp_size, _arr(bufs), mode, _stream(stream)), "tp_reduce_scatter")
+
+
+def tp_reduce_scatter_bf16(tp_size: int, partials, out, stream=None) -> None:
+    """Ring reduce-scatter of f32 partials; chunk r of out[r] receives the bf16 sum."""
+    _check(_lib.tp_reduce_scatter_bf16(tp_size, _arr(partials), _arr(out), _stream(stream)),
+           "tp_reduce_scatter_bf16")
+
+
+def tp_column_linear_chunks(tp_size: int, x_chunks, w, y, gather: bool, stream=None) -> None:
+    """Column-parallel linear whose input rows [c*T/N, (c+1)*T/N) are read from x_chunks[c]."""
+    _check(_lib.tp_column_linear_chunks(tp_size, _arr(x_chunks), _arr(w), _arr(y), int(gather),
+                                        _stream(stream)), "tp_column_linear_chunks")
 
 
 def tp_ring_all_gather(tp_size: int, bufs, mode: int = TP_RING_STEPS, stream=None) -> None:

@@ -16,6 +16,8 @@
 // same order, c+1, c+2, ..., c (mod N), in registers, so their results are
 // bit-identical to the step kernels (IEEE addition is commutative; the
 // association is the ring's left fold).
+#include <cuda_bf16.h>
+
 #include "tp_internal.h"
 
 namespace tpgqa {
@@ -301,6 +303,72 @@ tp_status launch_checked(cudaError_t e) {
   return check_launch();
 }
 
+
+// One-pass reduce-scatter into bf16 (grid.y = chunk): every element of chunk c
+// is folded over the ranks in the ring's order c+1, c+2, ..., c in f32, exactly
+// as k_ring_fused does, then rounded once to bf16 (nearest even) and stored in
+// buffer c's row-major [rows x cols] matrix with row pitch ld. Flat element e
+// sits at row e / cols, column e % cols.
+template <int NT>
+__global__ void __launch_bounds__(kThreads) k_ring_rs_bf16(RankPtrs b, Bf16Outs o, int n_rt, long long size) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int n = NT ? NT : n_rt;
+  const int c = blockIdx.y;
+  long long lo, hi;
+  chunk_range(size, n, c, lo, hi);
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(o.p[c]);
+  const bool small = size < (1LL << 31);
+  auto at = [&](long long e) {
+    long long row, col;
+    if (small) {
+      const unsigned int ue = static_cast<unsigned int>(e), uc = static_cast<unsigned int>(o.cols);
+      row = ue / uc;
+      col = ue - static_cast<unsigned int>(row) * uc;
+    } else {
+      row = e / o.cols;
+      col = e - row * o.cols;
+    }
+    return out + row * o.ld + col;
+  };
+  auto fold1 = [&](long long e) {
+    float acc = b.p[(c + 1) % n][e];
+    for (int j = 2; j <= n; ++j) acc = acc + b.p[(c + j) % n][e];
+    return acc;
+  };
+  if ((o.cols & 3) != 0) {  // rows not in whole float4 units: scalar throughout
+    for (long long e = lo + t; e < hi; e += stride) *at(e) = __float2bfloat16_rn(fold1(e));
+    return;
+  }
+  long long vlo, vhi;
+  split_vec(lo, hi, vlo, vhi);
+  if (t < vlo - lo) *at(lo + t) = __float2bfloat16_rn(fold1(lo + t));
+  if (t < hi - vhi) *at(vhi + t) = __float2bfloat16_rn(fold1(vhi + t));
+  const long long v0 = vlo >> 2, v1 = vhi >> 2;
+  for (long long i = v0 + t; i < v1; i += stride) {
+    float4 a;
+    if constexpr (NT > 0) {
+      float4 x[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) x[j] = reinterpret_cast<const float4 *>(b.p[(c + 1 + j) % NT])[i];
+      a = x[0];
+#pragma unroll
+      for (int j = 1; j < NT; ++j) a = add4(a, x[j]);
+    } else {
+      a = reinterpret_cast<const float4 *>(b.p[(c + 1) % n])[i];
+      for (int j = 2; j <= n; ++j) a = add4(a, reinterpret_cast<const float4 *>(b.p[(c + j) % n])[i]);
+    }
+    // four elements of one row (cols is a multiple of 4): one 8-byte store
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+    uint2 w;
+    w.x = *reinterpret_cast<const unsigned int *>(&h0);
+    w.y = *reinterpret_cast<const unsigned int *>(&h1);
+    *reinterpret_cast<uint2 *>(at(i * 4)) = w;
+  }
+}
+
 }  // namespace
 
 tp_status launch_ring_rs_step(const RankPtrs &b, int n, long long size, int step, cudaStream_t s) {
@@ -321,6 +389,15 @@ tp_status launch_ring_fused(const RankPtrs &b, int n, long long size, int write_
                                             : n == 8 ? k_ring_fused<8>
                                                      : k_ring_fused<0>;
   return launch_checked(launch_kernel(k, grid, dim3(kThreads), 0, s, 1, b, n, size, write_all));
+}
+
+tp_status launch_ring_rs_bf16(const RankPtrs &b, const Bf16Outs &o, int n, long long size, cudaStream_t s) {
+  const dim3 grid(blocks_for(size / n + 4, n), n);
+  void (*k)(RankPtrs, Bf16Outs, int, long long) = n == 2   ? k_ring_rs_bf16<2>
+                                                  : n == 4 ? k_ring_rs_bf16<4>
+                                                  : n == 8 ? k_ring_rs_bf16<8>
+                                                           : k_ring_rs_bf16<0>;
+  return launch_checked(launch_kernel(k, grid, dim3(kThreads), 0, s, 1, b, o, n, size));
 }
 
 tp_status launch_ring_ag_fused(const RankPtrs &b, int n, long long size, cudaStream_t s) {

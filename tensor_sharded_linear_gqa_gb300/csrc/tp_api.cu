@@ -164,6 +164,53 @@ tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, c
   return b.launch(s);
 }
 
+// Column-parallel GEMM whose input rows come from N chunk buffers: rows
+// [c*T/N, (c+1)*T/N) live in x_chunks[c]. Every (chunk, rank) pair is one problem
+// of the grouped GEMM: T/N rows read from chunk c's buffer times rank r's
+// weights, written at row offset c*T/N of rank r's output.
+tp_status gemm_bf16_column_chunks(int32_t n, const tp_tensor *x_chunks, const tp_tensor *w, const ColOut *outs,
+                                  int32_t ydt, int epi, cudaStream_t s) {
+  const long long T = x_chunks[0].rows, K = x_chunks[0].cols, Tc = T / n;
+  GemmBuilder b;
+  b.epi = epi;
+  b.pair = choose_pair(Tc);
+  int b_rows = 0;
+  {
+    std::vector<long long> nc;
+    for (int32_t c = 0; c < n; ++c)
+      for (int32_t r = 0; r < n; ++r) nc.push_back(w[r].rows);
+    if (b.pair) {
+      b.bn = choose_pair_bn(Tc, nc.data(), static_cast<int>(nc.size()), false, &b_rows);
+    } else {
+      b.bn = choose_bn(Tc, nc.data(), static_cast<int>(nc.size()), false);
+      b_rows = b.bn;
+    }
+  }
+  b.a_rows = b.pair ? 128 : a_box_rows(Tc);
+  tp_status err = TP_OK;
+  std::vector<int> am(n), bm(n, -1);
+  for (int32_t c = 0; c < n; ++c) {
+    am[c] = b.add_map(byte_ptr(x_chunks[c].ptr, c * Tc * x_chunks[c].ld, TP_BF16), Tc, K, x_chunks[c].ld,
+                      b.a_rows, &err);
+    if (am[c] < 0) return err;
+  }
+  for (int32_t r = 0; r < n; ++r) {
+    if (w[r].rows == 0) continue;
+    bm[r] = b.add_map(w[r].ptr, w[r].rows, K, w[r].ld, b_rows, &err);
+    if (bm[r] < 0) return err;
+  }
+  for (int32_t c = 0; c < n; ++c)
+    for (int32_t r = 0; r < n; ++r) {
+      if (w[r].rows == 0) continue;
+      const long long ks = K;
+      if (!b.add_problem(static_cast<int>(Tc), static_cast<int>(w[r].rows),
+                         byte_ptr(outs[r].ptr, c * Tc * outs[r].ld, ydt), outs[r].ld, &am[c], &bm[r], nullptr,
+                         &ks, 1))
+        return TP_ERR_UNSUPPORTED;
+    }
+  return b.launch(s);
+}
+
 // Row-parallel: fused = one problem whose segments are the ranks; else one problem per rank.
 tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
                         bool fused, cudaStream_t s) {
@@ -450,6 +497,89 @@ extern "C" tp_status tp_reduce_scatter(int32_t n, tp_tensor *buf, int32_t mode, 
   if (mode != TP_RING_STEPS && mode != TP_RING_FUSED) return TP_ERR_INVALID_ARG;
   if ((st = check_health(n)) != TP_OK) return st;
   return run_reduce_scatter(n, buf, mode, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_reduce_scatter_bf16(int32_t n, const tp_tensor *partial, tp_tensor *out,
+                                            tp_stream_t stream) {
+  tp_status st = check_ring_bufs(n, partial);
+  if (st != TP_OK) return st;
+  if (!out) return TP_ERR_INVALID_ARG;
+  const long long rows = partial[0].rows, cols = partial[0].cols;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(out[r])) return TP_ERR_INVALID_ARG;
+    if (out[r].dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (out[r].rows != rows || out[r].cols != cols || out[r].ld != out[0].ld) return TP_ERR_INVALID_ARG;
+    if (rows * cols > 0 && !pitch_ok(out[r])) return TP_ERR_ALIGNMENT;
+  }
+  if ((st = check_health(n)) != TP_OK) return st;
+  const long long size = rows * cols;
+  if (size == 0) return TP_OK;
+  Bf16Outs o;
+  std::memset(&o, 0, sizeof(o));
+  for (int32_t r = 0; r < n; ++r) o.p[r] = out[r].ptr;
+  o.ld = out[0].ld;
+  o.cols = cols;
+  return launch_ring_rs_bf16(rank_ptrs(n, partial), o, n, size, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_column_linear_chunks(int32_t n, const tp_tensor *x_chunks, const tp_tensor *w,
+                                             tp_tensor *y, int32_t gather, tp_stream_t stream) {
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (!x_chunks || !w || !y || (gather != 0 && gather != 1)) return TP_ERR_INVALID_ARG;
+  const long long T = x_chunks[0].rows, K = x_chunks[0].cols;
+  for (int32_t c = 0; c < n; ++c) {
+    if (!shape_ok(x_chunks[c])) return TP_ERR_INVALID_ARG;
+    if (x_chunks[c].dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (x_chunks[c].rows != T || x_chunks[c].cols != K) return TP_ERR_INVALID_ARG;
+  }
+  if (T % n != 0) return TP_ERR_NOT_DIVISIBLE;
+  long long total = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(w[r])) return TP_ERR_INVALID_ARG;
+    if (w[r].dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (w[r].cols != K) return TP_ERR_INVALID_ARG;
+    total += w[r].rows;
+  }
+  const int32_t ny = gather ? 1 : n;
+  for (int32_t q = 0; q < ny; ++q) {
+    if (!shape_ok(y[q])) return TP_ERR_INVALID_ARG;
+    if (y[q].rows != T || y[q].cols != (gather ? total : w[q].rows)) return TP_ERR_INVALID_ARG;
+  }
+  const int32_t ydt = y[0].dtype;
+  for (int32_t q = 1; q < ny; ++q)
+    if (y[q].dtype != ydt) return TP_ERR_DTYPE;
+  if (T > 0 && K > 0) {
+    for (int32_t c = 0; c < n; ++c)
+      if (!pitch_ok(x_chunks[c])) return TP_ERR_ALIGNMENT;
+    for (int32_t r = 0; r < n; ++r)
+      if (w[r].rows > 0 && !pitch_ok(w[r])) return TP_ERR_ALIGNMENT;
+  }
+  if (T > 0) {
+    for (int32_t q = 0; q < ny; ++q)
+      if (y[q].cols > 0 && !pitch_ok(y[q])) return TP_ERR_ALIGNMENT;
+    if (gather)
+      for (int32_t r = 0; r < n; ++r)
+        if ((w[r].rows * static_cast<long long>(esize(ydt))) % 16) return TP_ERR_ALIGNMENT;
+  }
+  tp_status st = check_health(n);
+  if (st != TP_OK) return st;
+  if (T == 0 || total == 0) return TP_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<ColOut> outs(n);
+  long long off = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    outs[r] = gather ? ColOut{byte_ptr(y[0].ptr, off, ydt), y[0].ld} : ColOut{y[r].ptr, y[r].ld};
+    off += w[r].rows;
+  }
+  if (K == 0) {
+    off = 0;
+    for (int32_t r = 0; r < n && st == TP_OK; ++r) {
+      st = gather ? zero_fill(y[0], off, w[r].rows, s) : zero_fill(y[r], 0, w[r].rows, s);
+      off += w[r].rows;
+    }
+    return st;
+  }
+  return gemm_bf16_column_chunks(n, x_chunks, w, outs.data(), ydt, ydt == TP_F32 ? kEpiF32 : kEpiBF16, s);
 }
 
 extern "C" tp_status tp_ring_all_gather(int32_t n, tp_tensor *buf, int32_t mode, tp_stream_t stream) {

@@ -81,8 +81,8 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // bf16 tensor-core grouped GEMM (tcgen05 + TMA), C = A * B^T, both K-major.
 // ---------------------------------------------------------------------------
 constexpr int kMaxMaps = 48;
-constexpr int kMaxProblems = 40;
-constexpr int kMaxSegs = 48;
+constexpr int kMaxProblems = 72;  // a column GEMM over reduce-scatter chunks has N*N problems
+constexpr int kMaxSegs = 80;
 
 enum Epilogue : int {
   kEpiF32 = 0,     // store fp32 accumulators
@@ -213,6 +213,15 @@ tp_status launch_ring_ag_step(const RankPtrs &b, int n, long long size, int step
 tp_status launch_ring_fused(const RankPtrs &b, int n, long long size, int write_all, cudaStream_t s);
 // In-place all-gather in one pass: chunk c of buffer c is copied to every other buffer.
 tp_status launch_ring_ag_fused(const RankPtrs &b, int n, long long size, cudaStream_t s);
+// bf16 destinations of a reduce-scatter: buffer r is a [rows x cols] bf16 matrix
+// with row pitch ld (elements) at p[r].
+struct Bf16Outs {
+  void *p[kMaxRanks];
+  long long ld, cols;
+};
+// One-pass reduce-scatter of the f32 buffers b into bf16: chunk c, folded in the
+// ring's order in f32, is rounded to bf16 and written to o.p[c] only.
+tp_status launch_ring_rs_bf16(const RankPtrs &b, const Bf16Outs &o, int n, long long size, cudaStream_t s);
 
 // Strided 2-D copy of a shard into an output (all-gather as concatenation).
 struct Copy2D {

@@ -165,6 +165,37 @@ def test_collectives_reject_bad_arguments():
         assert st(fn, good + [good[0]], n=3) == tp.TP_ERR_TP_SIZE_NOT_POW2
 
 
+def test_reduce_scatter_bf16_rejects_bad_arguments():
+    parts = [T(FAKE, F32, 8, 8), T(FAKE + 1024, F32, 8, 8)]
+    outs = [T(FAKE + 4096, BF, 8, 8), T(FAKE + 8192, BF, 8, 8)]
+
+    def st(p_, o_, n=2):
+        return tp.raw_status("tp_reduce_scatter_bf16", n, arr(*p_), arr(*o_), None)
+    assert st(parts, [outs[0], T(FAKE + 8192, F32, 8, 8)]) == tp.TP_ERR_DTYPE
+    assert st(parts, [outs[0], T(FAKE + 8192, BF, 8, 16)]) == tp.TP_ERR_INVALID_ARG
+    assert st(parts, [outs[0], T(FAKE + 8194, BF, 8, 8)]) == tp.TP_ERR_ALIGNMENT
+    assert st([parts[0], T(FAKE + 1024, BF, 8, 8)], outs) == tp.TP_ERR_DTYPE
+    assert st(parts + [parts[0]], outs + [outs[0]], n=3) == tp.TP_ERR_TP_SIZE_NOT_POW2
+
+
+def test_column_linear_chunks_rejects_bad_arguments():
+    xs = [T(FAKE, BF, 64, 128), T(FAKE + (1 << 20), BF, 64, 128)]
+    w = [T(FAKE, BF, 32, 128), T(FAKE, BF, 32, 128)]
+    y = [T(FAKE, BF, 64, 64)]
+
+    def st(x_, w_, y_, gather=1, n=2):
+        return tp.raw_status("tp_column_linear_chunks", n, arr(*x_), arr(*w_), arr(*y_), gather, None)
+    # the chunk boundary of 63 rows over 2 ranks falls inside a row of the flat buffer
+    assert st([T(FAKE, BF, 63, 128)] * 2, w, [T(FAKE, BF, 63, 64)]) == tp.TP_ERR_NOT_DIVISIBLE
+    assert st([xs[0], T(FAKE, BF, 64, 120)], w, y) == tp.TP_ERR_INVALID_ARG
+    assert st([xs[0], T(FAKE, F32, 64, 128)], w, y) == tp.TP_ERR_DTYPE
+    assert st(xs, [w[0], T(FAKE, F32, 32, 128)], y) == tp.TP_ERR_DTYPE
+    assert st(xs, w, [T(FAKE, BF, 64, 65)]) == tp.TP_ERR_INVALID_ARG
+    assert st([xs[0], T(FAKE + 2, BF, 64, 128)], w, y) == tp.TP_ERR_ALIGNMENT
+    assert st(xs, w, y, gather=2) == tp.TP_ERR_INVALID_ARG
+    assert st(xs + [xs[0]], w + [w[0]], y, n=3) == tp.TP_ERR_TP_SIZE_NOT_POW2
+
+
 def test_all_gather_rejects_bad_arguments():
     sh = [T(FAKE, F32, 8, 4), T(FAKE + 512, F32, 8, 4)]
     out = [T(FAKE + 4096, F32, 8, 8)]
