@@ -32,6 +32,8 @@ sys.path.insert(0, ROOT)
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 COMBINE_NAMES = {"fused": 1, "ring": 2, "ring_fused": 3}
+# Modes of the row-parallel -> reduce-scatter -> column-parallel pipeline workload.
+PIPELINE_MODES = ("deferred", "gathered")
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -45,8 +47,10 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
     p.add_argument("--workload", default="mlp_tp2_t512")
-    p.add_argument("--combine", choices=sorted(COMBINE_NAMES), default="ring_fused",
-                   help="ring_fused: the ring all-reduce in one pass, bit-identical to ring (N-1 step launches per phase)")
+    p.add_argument("--combine", choices=sorted(COMBINE_NAMES) + sorted(PIPELINE_MODES), default=None,
+                   help="ring_fused (default): the ring all-reduce in one pass, bit-identical to ring (N-1 step "
+                        "launches per phase). The reduce-scatter pipeline workload takes deferred (default: the "
+                        "column GEMM reads the reduced chunks) or gathered (an all-gather first)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -314,6 +318,45 @@ class DeviceSet:
                 self.calls.append(("combine_mlp", tp.Prepared("tp_allreduce_ring", n, tp.arr(ym), combine_ring,
                                                              sptr)))
             self.e2e["mlp"] = (g, u, dn, ym)
+        if w["kind"] == "rs_column":
+            F = w["ffn"]
+            Fr = F // n
+            self.h = to_dev(data["h"])
+            wd, wqkv = to_dev(data["wd"]), to_dev(data["wqkv"])
+            per = wqkv.shape[0] // n
+            wd_r = [wd[:, r * Fr:(r + 1) * Fr] for r in range(n)]
+            wc_r = [wqkv[r * per:(r + 1) * per] for r in range(n)]
+            parts = [torch.empty((T, D), device=dev) for _ in range(n)]
+            chunks = [torch.empty((T, D), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+            xfull = torch.empty((T, D), dtype=torch.bfloat16, device=dev) if mode == "gathered" else None
+            self.keep += parts + chunks + [xfull]
+            self._xs = tp.tensor(xfull) if xfull is not None else None
+
+            def pipeline_calls(hbuf, ys):
+                """Row-parallel partials, the ring reduce-scatter into bf16 chunks, then the
+                column-parallel GEMM: over the chunks in place (deferred) or over an
+                all-gathered copy (gathered). The intermediates are shared: every call
+                runs on one stream."""
+                h_r = [hbuf[:, r * Fr:(r + 1) * Fr] for r in range(n)]
+                calls = [("row", tp.Prepared("tp_row_linear", n, tp.arr(h_r), tp.arr(wd_r), tp.arr(parts),
+                                             tp.TP_COMBINE_NONE, sptr)),
+                         ("combine_rs", tp.Prepared("tp_reduce_scatter_bf16", n, tp.arr(parts), tp.arr(chunks),
+                                                    sptr))]
+                if mode == "gathered":
+                    shards_rs = [chunks[r][r * T // n:(r + 1) * T // n] for r in range(n)]
+                    calls.append(("combine_ag", tp.Prepared("tp_all_gather", n, tp.arr(shards_rs),
+                                                            tp.arr([xfull]), 1, 0, sptr)))
+                    calls.append(("column", tp.Prepared("tp_column_linear", n, ctypes.byref(self._xs),
+                                                        tp.arr(wc_r), tp.arr(ys), 0, sptr)))
+                else:
+                    calls.append(("column", tp.Prepared("tp_column_linear_chunks", n, tp.arr(chunks),
+                                                        tp.arr(wc_r), tp.arr(ys), 0, sptr)))
+                return calls
+
+            ys = [torch.empty((T, per), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+            self.keep += ys
+            self.calls += pipeline_calls(self.h, ys)
+            self.e2e["rs_column"] = (pipeline_calls, ys)
 
 
 def phase_costs(w, mode):
@@ -334,6 +377,15 @@ def phase_costs(w, mode):
         out["gate_up"] = (4.0 * T * D * F, 2 * F * D * 2 + T * D * 2 + T * F * 2)
         out["down"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + nparts * part)
         out["combine_mlp"] = (0.0, ring_bytes(mode, n, part))
+    if w["kind"] == "rs_column":
+        F, hd = w["ffn"], w["head_dim"]
+        per = (w["q_heads"] // n + 2 * max(1, w["kv_heads"] // n)) * hd
+        S = T * D
+        out["row"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + n * part)
+        out["combine_rs"] = (0.0, n * S * 4 + S * 2)          # every partial read once, bf16 chunks written
+        if mode == "gathered":
+            out["combine_ag"] = (0.0, S * 2 * 2)               # bf16 chunks read, full copy written
+        out["column"] = (2.0 * T * D * n * per, n * per * D * 2 + S * 2 + T * n * per * 2)
     return out
 
 
@@ -427,7 +479,7 @@ def run_native(args):
     peaks, peak_src = load_peaks()
 
     # roofline of the dominant kernel: the gate/up GEMM where there is an MLP, else q/k/v
-    rk = "gate_up" if "gate_up" in phase_ms else "qkv"
+    rk = "gate_up" if "gate_up" in phase_ms else ("qkv" if "qkv" in phase_ms else "row")
     rf, rb = costs[rk]
     r_s = phase_ms[rk] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -452,7 +504,9 @@ def run_native(args):
 
     # -- end to end through the public block calls with host buffers ---------------------
     s0 = sets[0]
-    xh = torch.from_numpy(np.ascontiguousarray(data["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    in_key = "h" if "rs_column" in s0.e2e else "x"
+    x0 = s0.h if in_key == "h" else s0.x
+    xh = torch.from_numpy(np.ascontiguousarray(data[in_key]).view(np.int16)).view(torch.bfloat16).pin_memory()
     ah = (torch.from_numpy(np.ascontiguousarray(data["a"]).view(np.int16)).view(torch.bfloat16).pin_memory()
           if "a" in data else None)
     outs_h = []
@@ -465,20 +519,28 @@ def run_native(args):
         outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
         d2h += T * D * 4
         ws = torch.empty(tp.tp_mlp_block_workspace_size(plan0, T), dtype=torch.uint8, device=dev)
-    combine_id = COMBINE_NAMES[mode]
+    if "rs_column" in s0.e2e:
+        # every rank's column-parallel output comes back: each holds its own heads
+        for t in s0.e2e["rs_column"][1]:
+            outs_h.append(torch.empty(tuple(t.shape), dtype=torch.bfloat16).pin_memory())
+            d2h += t.numel() * 2
+    combine_id = COMBINE_NAMES.get(mode)
 
     # Two activation slots (inputs, outputs, workspace) over the same weights, so
     # that step i's compute overlaps step i+1's input copy and step i-1's output
     # copy, each on its own copy stream: what a serving loop does with the public
     # calls. Every step's copies still run inside the timed region.
     def make_slot(first):
-        sl = {"x": s0.x if first else torch.empty_like(s0.x)}
+        sl = {"x": x0 if first else torch.empty_like(x0)}
         if "attn" in s0.e2e:
             sl["a"] = s0.a if first else torch.empty_like(s0.a)
             sl["yo"] = s0.e2e["attn"][8] if first else [torch.empty_like(t) for t in s0.e2e["attn"][8]]
         if "mlp" in s0.e2e:
             sl["ym"] = s0.e2e["mlp"][3] if first else [torch.empty_like(t) for t in s0.e2e["mlp"][3]]
             sl["ws"] = ws if first else torch.empty_like(ws)
+        if "rs_column" in s0.e2e:
+            ys0 = s0.e2e["rs_column"][1]
+            sl["ys"] = ys0 if first else [torch.empty_like(t) for t in ys0]
         sl["outs_h"] = outs_h if first else [torch.empty_like(t).pin_memory() for t in outs_h]
         return sl
 
@@ -500,13 +562,16 @@ def run_native(args):
             sl["calls"].append(tp.Prepared(
                 "tp_mlp_block", plan0.handle, ctypes.byref(xs), tp.arr(g), tp.arr(u), tp.arr(dn),
                 tp.arr(sl["ym"]), combine_id, sl["ws"].data_ptr(), sl["ws"].numel(), sptr))
+        if "rs_column" in s0.e2e:
+            sl["calls"] += [c for (_nm, c) in s0.e2e["rs_column"][0](sl["x"], sl["ys"])]
 
     def compute(sl):
         for call in sl["calls"]:
             call()
 
     def results(sl):
-        return ([sl["yo"][0]] if "attn" in s0.e2e else []) + ([sl["ym"][0]] if "mlp" in s0.e2e else [])
+        return (([sl["yo"][0]] if "attn" in s0.e2e else []) + ([sl["ym"][0]] if "mlp" in s0.e2e else []) +
+                (list(sl["ys"]) if "rs_column" in s0.e2e else []))
 
     def serial_step():
         sl = slots[0]
@@ -647,11 +712,17 @@ def run_reference(args):
 
 
 DEFAULT_STEPS = {"mlp_tp2_t512": 10000, "attn_gqa_tp4_t2048": 3000, "decode_gqa_rep_tp8_t64": 6000,
-                 "prefill_layer_tp8_t4096": 200}
+                 "prefill_layer_tp8_t4096": 200, "rs_column_tp8_t4096": 600}
 
 
 def main():
     args = parse_args()
+    from tensor_sharded_linear_gqa_gb300 import inputs as _inputs
+    kind = _inputs.WORKLOADS.get(args.workload, {}).get("kind")
+    if args.combine is None:
+        args.combine = "deferred" if kind == "rs_column" else "ring_fused"
+    if (kind == "rs_column") != (args.combine in PIPELINE_MODES):
+        raise SystemExit(f"--combine {args.combine} does not apply to workload {args.workload}")
     if args.steps is None:
         args.steps = DEFAULT_STEPS.get(args.workload, 1000) if args.impl == "native" else 20
     if args.impl == "reference":

@@ -308,7 +308,9 @@ tp_status launch_checked(cudaError_t e) {
 // is folded over the ranks in the ring's order c+1, c+2, ..., c in f32, exactly
 // as k_ring_fused does, then rounded once to bf16 (nearest even) and stored in
 // buffer c's row-major [rows x cols] matrix with row pitch ld. Flat element e
-// sits at row e / cols, column e % cols.
+// sits at row e / cols, column e % cols. The partials are read once, with
+// streaming (evict-first) loads, so that they do not push the bf16 chunks just
+// written out of L2: the next kernel, a GEMM over the chunks, reads them there.
 template <int NT>
 __global__ void __launch_bounds__(kThreads) k_ring_rs_bf16(RankPtrs b, Bf16Outs o, int n_rt, long long size) {
   griddep_wait();
@@ -352,13 +354,13 @@ __global__ void __launch_bounds__(kThreads) k_ring_rs_bf16(RankPtrs b, Bf16Outs 
     if constexpr (NT > 0) {
       float4 x[NT];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) x[j] = reinterpret_cast<const float4 *>(b.p[(c + 1 + j) % NT])[i];
+      for (int j = 0; j < NT; ++j) x[j] = __ldcs(reinterpret_cast<const float4 *>(b.p[(c + 1 + j) % NT]) + i);
       a = x[0];
 #pragma unroll
       for (int j = 1; j < NT; ++j) a = add4(a, x[j]);
     } else {
-      a = reinterpret_cast<const float4 *>(b.p[(c + 1) % n])[i];
-      for (int j = 2; j <= n; ++j) a = add4(a, reinterpret_cast<const float4 *>(b.p[(c + j) % n])[i]);
+      a = __ldcs(reinterpret_cast<const float4 *>(b.p[(c + 1) % n]) + i);
+      for (int j = 2; j <= n; ++j) a = add4(a, __ldcs(reinterpret_cast<const float4 *>(b.p[(c + j) % n]) + i));
     }
     // four elements of one row (cols is a multiple of 4): one 8-byte store
     const __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);

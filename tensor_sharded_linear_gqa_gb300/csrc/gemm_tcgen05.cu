@@ -136,11 +136,16 @@ struct Cursor {
   bool valid;
 };
 
+// The problem holding a tile: the last one whose tile_begin is <= tile (problems
+// are laid out in tile order), by binary search over up to kMaxProblems.
 __device__ __forceinline__ int find_problem(const GemmParams &p, int tile) {
-  int pi = 0;
-  for (int i = 1; i < p.num_problems; ++i)
-    if (tile >= p.prob[i].tile_begin) pi = i;
-  return pi;
+  int lo = 0, hi = p.num_problems - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile >= p.prob[mid].tile_begin) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 __device__ __forceinline__ void cursor_tile(const GemmParams &p, Cursor &c, int tile) {

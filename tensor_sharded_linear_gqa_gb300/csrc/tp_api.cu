@@ -199,8 +199,11 @@ tp_status gemm_bf16_column_chunks(int32_t n, const tp_tensor *x_chunks, const tp
     bm[r] = b.add_map(w[r].ptr, w[r].rows, K, w[r].ld, b_rows, &err);
     if (bm[r] < 0) return err;
   }
-  for (int32_t c = 0; c < n; ++c)
-    for (int32_t r = 0; r < n; ++r) {
+  // Rank-major: the tiles that run together (consecutive tile indices) share one
+  // rank's weight block over all chunks, as one problem over the gathered X would.
+  // Chunk-major order has every wave touch all N weight blocks.
+  for (int32_t r = 0; r < n; ++r)
+    for (int32_t c = 0; c < n; ++c) {
       if (w[r].rows == 0) continue;
       const long long ks = K;
       if (!b.add_problem(static_cast<int>(Tc), static_cast<int>(w[r].rows),

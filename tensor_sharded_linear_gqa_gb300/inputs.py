@@ -23,6 +23,8 @@ STREAM = {
     "wg": 6, "wu": 7, "wd": 8,
     "w": 9,      # plain linear weight of the fp32 worked example
     "buf": 10,   # raw collective buffers
+    "h": 11,     # row-parallel input H [T x ffn] of the reduce-scatter pipeline
+    "wqkv": 12,  # fused per-rank q/k/v weight of the reduce-scatter pipeline
 }
 
 # Workloads, named by what they are. Weight tensors are stored [out x in]
@@ -49,6 +51,13 @@ WORKLOADS = {
     "prefill_layer_tp8_t4096": dict(kind="layer", T=4096, hidden=8192, q_heads=64,
                                     kv_heads=8, head_dim=128, ffn=28672, tp=8,
                                     seed=105, w_std=0.02, oracle_rows=64),
+    # Row-parallel down projection whose result feeds the next layer's q/k/v
+    # projection (column-parallel) through a reduce-scatter, TP=8, bf16. The
+    # q/k/v weights are stored fused per rank: rank r's rows are its q heads,
+    # then its k head, then its v head.
+    "rs_column_tp8_t4096": dict(kind="rs_column", T=4096, hidden=8192, q_heads=64,
+                                kv_heads=8, head_dim=128, ffn=28672, tp=8,
+                                seed=106, w_std=0.02),
 }
 
 
@@ -115,6 +124,10 @@ def weight_shapes(w: dict) -> dict:
     if kind in ("mlp", "layer"):
         F = w["ffn"]
         out.update(wg=(F, D), wu=(F, D), wd=(D, F))
+    if kind == "rs_column":
+        n, hd = w["tp"], w["head_dim"]
+        per = (w["q_heads"] // n + 2 * max(1, w["kv_heads"] // n)) * hd
+        out.update(wd=(D, w["ffn"]), wqkv=(n * per, D))
     return out
 
 
@@ -127,6 +140,8 @@ def make_bf16_inputs(w: dict, rows: int | None = None) -> dict:
     """
     seed, T = w["seed"], w["T"]
     out = {"x": normal_bf16(seed, STREAM["x"], (T, w["hidden"]))}
+    if w["kind"] == "rs_column":
+        out["h"] = normal_bf16(seed, STREAM["h"], (T, w["ffn"]))
     if w["kind"] in ("attn", "layer"):
         out["a"] = normal_bf16(seed, STREAM["a"], (T, w["q_heads"] * w["head_dim"]))
     for name, shp in weight_shapes(w).items():

@@ -135,3 +135,43 @@ def test_row_reduce_scatter_column_pipeline(n, t, k_row, d, per):
     for r in range(n):
         assert_close(host_f64(ys[r]), ref["y"][r], BF16_TOL, f"rank {r}")
     assert tp.tp_device_status() == (tp.TP_OK, 0)
+
+
+def test_rs_column_tp8_t4096_sampled_rows():
+    """The full-size pipeline in the launch configuration the benchmark times (TP=8,
+    T=4096, down projection 28672 -> 8192 feeding the fused q/k/v projection of
+    1280 columns per rank), checked on a seeded sample of token rows: every output
+    row depends only on its own input row. The all-gathered variant is run on the
+    same partials and must agree with the deferred one bit for bit."""
+    need_gpu()
+    torch = _torch()
+    w = inputs.WORKLOADS["rs_column_tp8_t4096"]
+    n, t, d, f = w["tp"], w["T"], w["hidden"], w["ffn"]
+    data = inputs.make_bf16_inputs(w)
+    fr = f // n
+    h, wd, wqkv = dev_bf16(data["h"]), dev_bf16(data["wd"]), dev_bf16(data["wqkv"])
+    per = wqkv.shape[0] // n
+    parts = [torch.empty((t, d), device="cuda") for _ in range(n)]
+    tp.tp_row_linear(n, [h[:, r * fr:(r + 1) * fr] for r in range(n)],
+                     [wd[:, r * fr:(r + 1) * fr] for r in range(n)], parts, tp.TP_COMBINE_NONE)
+    chunks = [torch.empty((t, d), dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    tp.tp_reduce_scatter_bf16(n, parts, chunks)
+    del parts
+    wc = [wqkv[r * per:(r + 1) * per] for r in range(n)]
+    ys = [torch.full((t, per), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    tp.tp_column_linear_chunks(n, chunks, wc, ys, gather=False)
+    xfull = torch.empty((t, d), dtype=torch.bfloat16, device="cuda")
+    tp.tp_all_gather(n, [chunks[r][r * t // n:(r + 1) * t // n] for r in range(n)], [xfull], axis=0)
+    yg = [torch.empty((t, per), dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    tp.tp_column_linear(n, xfull, wc, yg, gather=False)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == (tp.TP_OK, 0)
+    for r in range(n):
+        assert torch.equal(ys[r].view(torch.int16), yg[r].view(torch.int16)), f"rank {r}"
+    rows = np.sort(inputs.rng(w["seed"], 99).choice(t, size=48, replace=False))
+    hf = inputs.bf16_bits_to_f64(data["h"][rows])
+    part_ref = O.row_parallel(O.split_cols(hf, n), O.split_cols(inputs.bf16_bits_to_f64(data["wd"]), n))
+    ref = O.reduce_scatter_then_column(part_ref, O.split_rows(inputs.bf16_bits_to_f64(data["wqkv"]), n),
+                                       round_bf16=True)
+    for r in range(n):
+        assert_close(host_f64(ys[r])[rows], ref["y"][r], BF16_TOL, f"rank {r}")
