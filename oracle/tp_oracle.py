@@ -22,6 +22,11 @@ It is a plain, slow, obviously correct restatement of what the pages define:
          AllReduce, q AllGather) and the GQA rule (shard K/V when
          num_kv_heads >= tp_size, replicate otherwise), with its two examples.
        - 설정 (Configuration): --tp-size is a power of two, default 1.
+       - Vocab Parallel (a weight-sharding strategy) and 임베딩 및 LM Head 샤딩
+         (Embedding and LM-head sharding): the vocabulary dimension of the
+         embedding table and the LM head is split into contiguous per-rank
+         slices; in vocab_parallel mode the lookup and the logits need an
+         all-gather.
 [WIKI] railscraft wiki, "텐서 병렬 처리" (Tensor parallel processing)
        - 상세 1 (Details 1, column & row parallel): Y_i = X W_i, Y = [Y_1..Y_n];
          Y_i = X_i W_i, Y = sum_i Y_i.
@@ -44,6 +49,9 @@ Conventions (readings of the pages, each listed in the design notes):
     (the pages name no activation).
   * The o_proj input (attention context A) is an explicit input; attention
     itself is not part of this block.
+  * Vocab slices are equal (V divisible by N). The embedding all-gather moves
+    each rank's looked-up rows ("piece") around the ring like any all-gather;
+    every token's row comes from the one rank whose slice holds its id.
 
 Parity status: every public function is pinned by a CPU test against facts the
 pages and the mathematics fix (closed forms, worked examples, invariants,
@@ -321,6 +329,90 @@ def reduce_scatter_then_column(partials: list, w_shards: list, round_bf16: bool 
         chunks.append(round_to_bf16(v) if round_bf16 else v)
     x = gather_flat_shards(chunks).reshape(t, k)
     return {"chunks": chunks, "x": x, "y": column_parallel(x.astype(np.float64), w_shards)}
+
+
+# ---------------------------------------------------------------------------
+# Vocab parallel ([MLX] 가중치 샤딩 전략, Vocab Parallel; 임베딩 및 LM Head 샤딩)
+# ---------------------------------------------------------------------------
+def vocab_ranges(vocab: int, n: int) -> list:
+    """[begin, end) of the token ids each rank holds: the vocabulary dimension
+    is split into N contiguous slices of V/N ids ([MLX] Vocab Parallel: every
+    rank owns one contiguous slice of the token vocabulary). V must divide by N,
+    as every other split dimension must."""
+    if not _is_pow2(n):
+        raise PlanError("tp_size", f"tp_size {n} is not a power of two")
+    if vocab <= 0 or vocab % n:
+        raise PlanError("not_divisible", f"vocab {vocab} does not split over {n} ranks")
+    per = vocab // n
+    return [(r * per, (r + 1) * per) for r in range(n)]
+
+
+def embedding(ids, table) -> np.ndarray:
+    """The plain lookup: row i of the result is row ids[i] of the table [V x D]."""
+    ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+    table = np.asarray(table, dtype=np.float64)
+    if ids.size and (ids.min() < 0 or ids.max() >= table.shape[0]):
+        raise ValueError("token id outside the vocabulary")
+    out = np.empty((ids.size, table.shape[1]))
+    for i, t in enumerate(ids):
+        out[i] = table[t]
+    return out
+
+
+def vocab_parallel_embedding(ids, table_shards: list, log: RingLog | None = None) -> dict:
+    """Embedding lookup over a vocab-sharded table ([MLX] 임베딩 및 LM Head 샤딩,
+    vocab_parallel: the vocabulary dimension is sharded and the lookup needs an
+    all-gather).
+
+    Rank r holds table rows [r*V/N, (r+1)*V/N) as its shard. It looks up the
+    tokens whose ids fall in its slice, at local row id - r*V/N, and contributes
+    those rows (its "piece", keyed by token position). The pieces are all-gathered
+    on the ring (step s: rank r forwards piece (r-s) mod N to (r+1)%N), after
+    which every rank holds every token's row, taken from the one rank owning it.
+    """
+    ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+    n = len(table_shards)
+    per = np.asarray(table_shards[0]).shape[0]
+    d = np.asarray(table_shards[0]).shape[1]
+    rng_ = vocab_ranges(per * n, n)
+    if ids.size and (ids.min() < 0 or ids.max() >= per * n):
+        raise ValueError("token id outside the vocabulary")
+    pieces = []
+    for r, (lo, hi) in enumerate(rng_):
+        shard = np.asarray(table_shards[r], dtype=np.float64)
+        pos = [i for i in range(ids.size) if lo <= ids[i] < hi]
+        rows = np.array([shard[ids[i] - lo] for i in pos]).reshape(len(pos), d)
+        pieces.append((pos, rows))
+    # ring all-gather of the pieces: held[r] = {owner: piece} that rank r has
+    held = [{r: pieces[r]} for r in range(n)]
+    for s in range(n - 1):
+        msgs = []
+        for r in range(n):
+            owner = (r - s) % n
+            msgs.append(((r + 1) % n, owner, held[r][owner], r))
+        for dst, owner, piece, src in msgs:
+            held[dst][owner] = piece
+            if log is not None:
+                log.sends.append(("all_gather", s, src, dst, owner, piece[1].nbytes))
+    outs = []
+    for r in range(n):
+        y = np.full((ids.size, d), np.nan)
+        for owner in range(n):
+            pos, rows = held[r][owner]
+            for j, i in enumerate(pos):
+                y[i] = rows[j]
+        outs.append(y)
+    return {"pieces": pieces, "y": outs}
+
+
+def vocab_parallel_lm_head(x, w_shards: list) -> dict:
+    """LM-head logits over a vocab-sharded weight ([MLX] 임베딩 및 LM Head 샤딩,
+    vocab_parallel: the logits need an all-gather). Weights are stored [V x D];
+    rank r's shard is rows [r*V/N, (r+1)*V/N), so its logits X W_r^T are the
+    columns of its vocabulary slice, and the all-gather concatenates them in
+    rank order into the full [T x V] logits."""
+    parts = column_parallel(x, w_shards)
+    return {"parts": parts, "logits": all_gather_columns(parts)}
 
 
 # ---------------------------------------------------------------------------

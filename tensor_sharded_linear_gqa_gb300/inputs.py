@@ -93,8 +93,27 @@ def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
 
 
 def normal_bf16(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
-    """N(0, std^2) samples rounded to bf16, as uint16 bit patterns."""
-    return f32_to_bf16_bits(normal_f32(seed, stream, shape, std))
+    """N(0, std^2) samples rounded to bf16, as uint16 bit patterns.
+
+    Large tensors are drawn in blocks of leading rows from one generator: the
+    values are the same as from one draw of the whole shape (the generator is
+    consumed in order), with a bounded peak of host memory."""
+    shape = tuple(shape) if isinstance(shape, (tuple, list)) else (shape,)
+    total = int(np.prod(shape))
+    if total <= _BLOCK or len(shape) < 2:
+        return f32_to_bf16_bits(normal_f32(seed, stream, shape, std))
+    g = rng(seed, stream)
+    out = np.empty(shape, dtype=np.uint16)
+    step = max(1, _BLOCK // int(np.prod(shape[1:])))
+    for r0 in range(0, shape[0], step):
+        blk = g.standard_normal(size=(min(step, shape[0] - r0),) + shape[1:], dtype=np.float64)
+        if std != 1.0:
+            blk *= std
+        out[r0:r0 + blk.shape[0]] = f32_to_bf16_bits(blk.astype(np.float32))
+    return out
+
+
+_BLOCK = 1 << 24  # elements per block of normal_bf16
 
 
 def small_int_bf16(seed: int, stream: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
