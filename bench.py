@@ -318,6 +318,30 @@ class DeviceSet:
                 self.calls.append(("combine_mlp", tp.Prepared("tp_allreduce_ring", n, tp.arr(ym), combine_ring,
                                                              sptr)))
             self.e2e["mlp"] = (g, u, dn, ym)
+        if w["kind"] == "vocab":
+            V = w["vocab"]
+            per_v = V // n
+            emb, wlm = to_dev(data["emb"]), to_dev(data["wlm"])
+            emb_r = [emb[r * per_v:(r + 1) * per_v] for r in range(n)]
+            wlm_r = [wlm[r * per_v:(r + 1) * per_v] for r in range(n)]
+            self.ids = torch.from_numpy(data["ids"]).to(dev)
+            self.keep.append(self.ids)
+
+            def vocab_calls(ids, xbuf, x0, logits):
+                """The lookup of the token ids (one shared output copy), then the LM-head
+                logits of the hidden states, gathered into one [T x V] f32 tensor."""
+                xs = tp.tensor(xbuf)
+                self.keep.append(xs)
+                return [("embed", tp.Prepared("tp_vocab_embedding", n, tp.ids_ptr(ids), ids.numel(),
+                                              tp.arr(emb_r), tp.arr([x0]), 1, sptr)),
+                        ("lm_head", tp.Prepared("tp_vocab_lm_head", n, ctypes.byref(xs), tp.arr(wlm_r),
+                                                tp.arr([logits]), 1, sptr))]
+
+            x0 = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+            logits = torch.empty((T, V), device=dev)
+            self.keep += [x0, logits]
+            self.calls += vocab_calls(self.ids, self.x, x0, logits)
+            self.e2e["vocab"] = (vocab_calls, x0, logits)
         if w["kind"] == "rs_column":
             F = w["ffn"]
             Fr = F // n
@@ -377,6 +401,10 @@ def phase_costs(w, mode):
         out["gate_up"] = (4.0 * T * D * F, 2 * F * D * 2 + T * D * 2 + T * F * 2)
         out["down"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + nparts * part)
         out["combine_mlp"] = (0.0, ring_bytes(mode, n, part))
+    if w["kind"] == "vocab":
+        V = w["vocab"]
+        out["embed"] = (0.0, T * D * 2 * 2 + T * 4)        # rows read once and written once, ids
+        out["lm_head"] = (2.0 * T * D * V, V * D * 2 + T * D * 2 + T * V * 4)
     if w["kind"] == "rs_column":
         F, hd = w["ffn"], w["head_dim"]
         per = (w["q_heads"] // n + 2 * max(1, w["kv_heads"] // n)) * hd
@@ -479,7 +507,7 @@ def run_native(args):
     peaks, peak_src = load_peaks()
 
     # roofline of the dominant kernel: the gate/up GEMM where there is an MLP, else q/k/v
-    rk = "gate_up" if "gate_up" in phase_ms else ("qkv" if "qkv" in phase_ms else "row")
+    rk = next(k for k in ("gate_up", "qkv", "row", "lm_head") if k in phase_ms)
     rf, rb = costs[rk]
     r_s = phase_ms[rk] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -494,9 +522,9 @@ def run_native(args):
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": rb}
     roof["traffic"] = committed_traffic(args.workload) if rk == "gate_up" else None
 
-    comb = {}
+    comb = {}  # every data-movement phase (the collectives, the lookup) against HBM
     for nm in names:
-        if nm.startswith("combine"):
+        if costs[nm][0] == 0:
             b = costs[nm][1]
             gbs = b / (phase_ms[nm] / 1e3) / 1e9 if phase_ms[nm] > 0 else None
             comb[nm] = {"gbs": round(gbs, 1), "bytes_per_step": b,
@@ -510,7 +538,8 @@ def run_native(args):
     ah = (torch.from_numpy(np.ascontiguousarray(data["a"]).view(np.int16)).view(torch.bfloat16).pin_memory()
           if "a" in data else None)
     outs_h = []
-    h2d = xh.numel() * 2 + (ah.numel() * 2 if ah is not None else 0)
+    idh = torch.from_numpy(data["ids"]).pin_memory() if "vocab" in s0.e2e else None
+    h2d = xh.numel() * 2 + (ah.numel() * 2 if ah is not None else 0) + (idh.numel() * 4 if idh is not None else 0)
     d2h = 0
     if "attn" in s0.e2e:
         outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
@@ -519,6 +548,11 @@ def run_native(args):
         outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
         d2h += T * D * 4
         ws = torch.empty(tp.tp_mlp_block_workspace_size(plan0, T), dtype=torch.uint8, device=dev)
+    if "vocab" in s0.e2e:
+        # the looked-up rows and the full f32 logits come back
+        for t in s0.e2e["vocab"][1:]:
+            outs_h.append(torch.empty(tuple(t.shape), dtype=t.dtype).pin_memory())
+            d2h += t.numel() * t.element_size()
     if "rs_column" in s0.e2e:
         # every rank's column-parallel output comes back: each holds its own heads
         for t in s0.e2e["rs_column"][1]:
@@ -538,6 +572,10 @@ def run_native(args):
         if "mlp" in s0.e2e:
             sl["ym"] = s0.e2e["mlp"][3] if first else [torch.empty_like(t) for t in s0.e2e["mlp"][3]]
             sl["ws"] = ws if first else torch.empty_like(ws)
+        if "vocab" in s0.e2e:
+            _f, x00, lg0 = s0.e2e["vocab"]
+            sl["ids"] = s0.ids if first else torch.empty_like(s0.ids)
+            sl["vo"] = [x00, lg0] if first else [torch.empty_like(x00), torch.empty_like(lg0)]
         if "rs_column" in s0.e2e:
             ys0 = s0.e2e["rs_column"][1]
             sl["ys"] = ys0 if first else [torch.empty_like(t) for t in ys0]
@@ -564,6 +602,8 @@ def run_native(args):
                 tp.arr(sl["ym"]), combine_id, sl["ws"].data_ptr(), sl["ws"].numel(), sptr))
         if "rs_column" in s0.e2e:
             sl["calls"] += [c for (_nm, c) in s0.e2e["rs_column"][0](sl["x"], sl["ys"])]
+        if "vocab" in s0.e2e:
+            sl["calls"] += [c for (_nm, c) in s0.e2e["vocab"][0](sl["ids"], sl["x"], *sl["vo"])]
 
     def compute(sl):
         for call in sl["calls"]:
@@ -571,13 +611,16 @@ def run_native(args):
 
     def results(sl):
         return (([sl["yo"][0]] if "attn" in s0.e2e else []) + ([sl["ym"][0]] if "mlp" in s0.e2e else []) +
-                (list(sl["ys"]) if "rs_column" in s0.e2e else []))
+                (list(sl["ys"]) if "rs_column" in s0.e2e else []) +
+                (list(sl["vo"]) if "vocab" in s0.e2e else []))
 
     def serial_step():
         sl = slots[0]
         sl["x"].copy_(xh, non_blocking=True)
         if "a" in sl:
             sl["a"].copy_(ah, non_blocking=True)
+        if "ids" in sl:
+            sl["ids"].copy_(idh, non_blocking=True)
         compute(sl)
         for hbuf, dbuf in zip(sl["outs_h"], results(sl)):
             hbuf.copy_(dbuf, non_blocking=True)
@@ -596,6 +639,8 @@ def run_native(args):
             sl["x"].copy_(xh, non_blocking=True)
             if "a" in sl:
                 sl["a"].copy_(ah, non_blocking=True)
+            if "ids" in sl:
+                sl["ids"].copy_(idh, non_blocking=True)
             ev_in[b].record(h2d_s)
         stream.wait_event(ev_in[b])
         if i >= 2:
@@ -649,7 +694,9 @@ def run_native(args):
               "l2": (f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2x L2 in total)" if R > 1 else
                      f"one input set of {set_bytes / 1e6:.1f} MB (> 2x L2)"),
               "parallelism": f"tp{n} logical ranks on one GPU; replicas across GPUs"}
-    for k in ("ffn", "q_heads", "kv_heads", "head_dim"):
+    if w["kind"] == "vocab":
+        config["combine"] = "all-gather of the looked-up rows and of the logits (in the kernels)"
+    for k in ("ffn", "q_heads", "kv_heads", "head_dim", "vocab"):
         if k in w:
             config[k] = w[k]
     line = {
@@ -712,7 +759,7 @@ def run_reference(args):
 
 
 DEFAULT_STEPS = {"mlp_tp2_t512": 10000, "attn_gqa_tp4_t2048": 3000, "decode_gqa_rep_tp8_t64": 6000,
-                 "prefill_layer_tp8_t4096": 200, "rs_column_tp8_t4096": 600}
+                 "prefill_layer_tp8_t4096": 200, "rs_column_tp8_t4096": 600, "vocab_tp8_t4096": 200}
 
 
 def main():

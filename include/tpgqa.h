@@ -61,7 +61,8 @@ typedef enum tp_status {
   TP_ERR_TIMEOUT = 8,          /* a bounded device-side wait ran out                 */
   TP_ERR_CUDA = 9,             /* a CUDA runtime call failed; see tp_last_cuda_error */
   TP_ERR_WORKSPACE = 10,       /* workspace missing or too small                     */
-  TP_ERR_UNSUPPORTED = 11      /* valid request this build does not implement        */
+  TP_ERR_UNSUPPORTED = 11,     /* valid request this build does not implement        */
+  TP_ERR_BAD_TOKEN = 12        /* an embedding lookup met a token id outside [0, V)  */
 } tp_status;
 
 typedef enum tp_dtype { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
@@ -261,6 +262,46 @@ tp_status tp_column_linear_chunks(int32_t tp_size, const tp_tensor *x_chunks, co
                                   tp_tensor *y, int32_t gather, tp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Vocab parallel (mlxcel manual, 가중치 샤딩 전략 / Weight-sharding strategies,
+ * Vocab Parallel: the vocabulary dimension of the embedding table and of the
+ * LM head is split into contiguous per-rank slices; 임베딩 및 LM Head 샤딩 /
+ * Embedding and LM-head sharding, vocab_parallel: the lookup and the logits
+ * need an all-gather).
+ * ------------------------------------------------------------------------- */
+
+/* Embedding lookup over a vocab-sharded table, with the all-gather of the rows
+ * looked up: row i of every output is row ids[i] of the full table [V x D],
+ * V = tp_size * table[0].rows. Rank r holds ids [r*V/N, (r+1)*V/N) as table[r]
+ * (id at local row id - r*V/N). Each token's row is read once, from the rank
+ * owning its id, and written to every output.
+ *  ids      : device pointer to n_tokens int32 token ids (n_tokens >= 0).
+ *  table[r] : [V/N x D] f32 or bf16; every shard has the same shape and dtype.
+ *  out[o]   : [n_tokens x D] in the table's dtype; n_out = 1 (one copy shared
+ *             by all ranks) or tp_size (a copy per rank).
+ * An id outside [0, V) is not looked up: its rows are written as zeros and the
+ * device status word records it (tp_device_status then returns
+ * TP_ERR_BAD_TOKEN). 16-byte aligned bases, pitches and rows take a vector
+ * path; anything else is copied element by element. Bases must be aligned to
+ * the element size and ids to 4 bytes, else TP_ERR_ALIGNMENT.
+ * Errors: TP_ERR_INVALID_ARG (null, shapes differ, n_out), TP_ERR_TP_SIZE_NOT_POW2,
+ * TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_RANK_FAILED, TP_ERR_CUDA. */
+tp_status tp_vocab_embedding(int32_t tp_size, const int32_t *ids, int64_t n_tokens,
+                             const tp_tensor *table, tp_tensor *out, int32_t n_out,
+                             tp_stream_t stream);
+
+/* LM-head logits over a vocab-sharded weight, with their all-gather: rank r's
+ * logits are X W_r^T for its vocabulary slice W_r = rows [r*V/N, (r+1)*V/N) of
+ * the LM-head weight [V x D]. gather = 1 writes them as column blocks, in rank
+ * order, of one [T x V] logits tensor (the all-gather as concatenation, no
+ * copy); gather = 0 leaves logits[r] = [T x V/N] per rank.
+ *  x      : [T x D] bf16 (f32 with f32 weights, as tp_column_linear).
+ *  w[r]   : [V/N x D]; every shard has the same number of rows.
+ *  logits : f32 or bf16 (f32 for f32 inputs).
+ * Errors: as tp_column_linear; TP_ERR_INVALID_ARG when the shards differ in rows. */
+tp_status tp_vocab_lm_head(int32_t tp_size, const tp_tensor *x, const tp_tensor *w,
+                           tp_tensor *logits, int32_t gather, tp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Blocks (mlxcel manual, 아키텍처 인식 샤드 플랜: gate/up ColumnParallel with no
  * communication, down RowParallel + AllReduce; q/k/v ColumnParallel, o
  * RowParallel + AllReduce).
@@ -377,8 +418,10 @@ int32_t tp_last_cuda_error(void);
 tp_status tp_set_rank_health(int32_t rank, int32_t healthy);
 
 /* Synchronises `stream`, then reads and clears the device status word that
- * kernels set when a bounded wait runs out. Returns TP_OK, TP_ERR_TIMEOUT or
- * TP_ERR_CUDA. *detail (optional) receives the raw word (0 = none). */
+ * kernels set when a bounded wait runs out or an embedding lookup meets a bad
+ * token id (the first such event is kept). Returns TP_OK, TP_ERR_TIMEOUT,
+ * TP_ERR_BAD_TOKEN or TP_ERR_CUDA. *detail (optional) receives the raw word
+ * (0 = none). */
 tp_status tp_device_status(tp_stream_t stream, int32_t *detail);
 
 /* Sets the time budget, in nanoseconds, of every bounded device-side wait of

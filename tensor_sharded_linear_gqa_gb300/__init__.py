@@ -24,7 +24,8 @@ LIB_PATH = os.path.join(_PKG, "libtpgqa.so")
 TP_OK = 0
 STATUS_NAMES = ["TP_OK", "TP_ERR_INVALID_ARG", "TP_ERR_TP_SIZE_NOT_POW2", "TP_ERR_NOT_DIVISIBLE",
                 "TP_ERR_GQA_SHAPE", "TP_ERR_DTYPE", "TP_ERR_ALIGNMENT", "TP_ERR_RANK_FAILED",
-                "TP_ERR_TIMEOUT", "TP_ERR_CUDA", "TP_ERR_WORKSPACE", "TP_ERR_UNSUPPORTED"]
+                "TP_ERR_TIMEOUT", "TP_ERR_CUDA", "TP_ERR_WORKSPACE", "TP_ERR_UNSUPPORTED",
+                "TP_ERR_BAD_TOKEN"]
 for _i, _n in enumerate(STATUS_NAMES):
     globals()[_n] = _i
 TP_F32, TP_BF16 = 0, 1
@@ -85,6 +86,9 @@ _SIGS = {
     "tp_ring_all_gather": ([ctypes.c_int32, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_allreduce_ring": ([ctypes.c_int32, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_all_gather": ([ctypes.c_int32, _T, _T, ctypes.c_int32, ctypes.c_int32, _S], ctypes.c_int),
+    "tp_vocab_embedding": ([ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, _T, _T, ctypes.c_int32, _S],
+                           ctypes.c_int),
+    "tp_vocab_lm_head": ([ctypes.c_int32, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
     "tp_gate_up_swiglu": ([ctypes.c_void_p, _T, _T, _T, _T, _S], ctypes.c_int),
     "tp_mlp_block_workspace_size": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_size_t),
     "tp_mlp_block": ([ctypes.c_void_p, _T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_void_p,
@@ -275,6 +279,27 @@ def tp_all_gather(tp_size: int, shards, outs, axis: int, stream=None) -> None:
     outs = list(outs)
     _check(_lib.tp_all_gather(tp_size, _arr(shards), _arr(outs), len(outs), axis, _stream(stream)),
            "tp_all_gather")
+
+
+def ids_ptr(ids) -> int:
+    """Device address of a contiguous int32 CUDA tensor of token ids (0 when empty)."""
+    if str(ids.dtype) != "torch.int32" or not ids.is_contiguous():
+        raise TypeError("token ids must be a contiguous int32 tensor")
+    return ids.data_ptr() if ids.numel() else 0
+
+
+def tp_vocab_embedding(tp_size: int, ids, table, outs, stream=None) -> None:
+    """Rows ids[i] of the vocab-sharded table (table[r] = rank r's slice) into
+    every output (1 shared copy or tp_size copies)."""
+    outs = list(outs)
+    _check(_lib.tp_vocab_embedding(tp_size, ids_ptr(ids), ids.numel(), _arr(table), _arr(outs), len(outs),
+                                   _stream(stream)), "tp_vocab_embedding")
+
+
+def tp_vocab_lm_head(tp_size: int, x, w, logits, gather: bool, stream=None) -> None:
+    xs = tensor(x)
+    _check(_lib.tp_vocab_lm_head(tp_size, ctypes.byref(xs), _arr(w), _arr(logits), int(gather),
+                                 _stream(stream)), "tp_vocab_lm_head")
 
 
 def tp_gate_up_swiglu(plan: Plan, x, w_gate, w_up, h, stream=None) -> None:

@@ -585,6 +585,67 @@ extern "C" tp_status tp_column_linear_chunks(int32_t n, const tp_tensor *x_chunk
   return gemm_bf16_column_chunks(n, x_chunks, w, outs.data(), ydt, ydt == TP_F32 ? kEpiF32 : kEpiBF16, s);
 }
 
+extern "C" tp_status tp_vocab_embedding(int32_t n, const int32_t *ids, int64_t n_tokens, const tp_tensor *table,
+                                        tp_tensor *out, int32_t n_out, tp_stream_t stream) {
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (!table || !out || (n_out != 1 && n_out != n) || n_tokens < 0 || (n_tokens > 0 && !ids))
+    return TP_ERR_INVALID_ARG;
+  const int32_t dt = table[0].dtype;
+  const long long rows = table[0].rows, D = table[0].cols;
+  for (int32_t r = 0; r < n; ++r) {
+    if (!shape_ok(table[r])) return TP_ERR_INVALID_ARG;
+    if (table[r].dtype != dt) return TP_ERR_DTYPE;
+    if (table[r].rows != rows || table[r].cols != D) return TP_ERR_INVALID_ARG;
+  }
+  if (rows == 0 && n_tokens > 0) return TP_ERR_INVALID_ARG;  // no id can be valid
+  for (int32_t o = 0; o < n_out; ++o) {
+    if (!shape_ok(out[o])) return TP_ERR_INVALID_ARG;
+    if (out[o].dtype != dt) return TP_ERR_DTYPE;
+    if (out[o].rows != n_tokens || out[o].cols != D) return TP_ERR_INVALID_ARG;
+  }
+  // element-aligned bases and pitches (the element path), 4-byte aligned ids
+  const long long es = static_cast<long long>(esize(dt));
+  auto elem_ok = [&](const tp_tensor &t) { return (reinterpret_cast<uintptr_t>(t.ptr) % es) == 0; };
+  if (n_tokens > 0 && (reinterpret_cast<uintptr_t>(ids) & 3) != 0) return TP_ERR_ALIGNMENT;
+  for (int32_t r = 0; r < n; ++r)
+    if (!elem_ok(table[r])) return TP_ERR_ALIGNMENT;
+  for (int32_t o = 0; o < n_out; ++o)
+    if (!elem_ok(out[o])) return TP_ERR_ALIGNMENT;
+  tp_status st = check_health(n);
+  if (st != TP_OK) return st;
+  if (n_tokens == 0 || D == 0) return TP_OK;
+  EmbedArgs a;
+  std::memset(&a, 0, sizeof(a));
+  bool vec16 = (D * es) % 16 == 0;  // ids are read one int at a time
+  for (int32_t r = 0; r < n; ++r) {
+    a.tab[r] = static_cast<const char *>(table[r].ptr);
+    a.tab_pitch[r] = table[r].ld * es;
+    vec16 = vec16 && pitch_ok(table[r]);
+  }
+  for (int32_t o = 0; o < n_out; ++o) {
+    a.out[o] = static_cast<char *>(out[o].ptr);
+    a.out_pitch[o] = out[o].ld * es;
+    vec16 = vec16 && pitch_ok(out[o]);
+  }
+  a.ids = ids;
+  a.n_tokens = n_tokens;
+  a.rows_per_rank = rows;
+  a.row_bytes = D * es;
+  a.n = n;
+  a.n_outs = n_out;
+  a.esize = static_cast<int>(es);
+  return launch_vocab_embed(a, vec16, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tp_status tp_vocab_lm_head(int32_t n, const tp_tensor *x, const tp_tensor *w, tp_tensor *logits,
+                                      int32_t gather, tp_stream_t stream) {
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (!w) return TP_ERR_INVALID_ARG;
+  for (int32_t r = 1; r < n; ++r)
+    if (w[r].rows != w[0].rows) return TP_ERR_INVALID_ARG;  // slices of V/N ids each
+  return tp_column_linear(n, x, w, logits, gather, stream);
+}
+
 extern "C" tp_status tp_ring_all_gather(int32_t n, tp_tensor *buf, int32_t mode, tp_stream_t stream) {
   tp_status st = check_ring_bufs(n, buf);
   if (st != TP_OK) return st;
@@ -909,6 +970,7 @@ extern "C" const char *tp_status_str(tp_status s) {
     case TP_ERR_CUDA: return "TP_ERR_CUDA";
     case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE";
     case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
+    case TP_ERR_BAD_TOKEN: return "TP_ERR_BAD_TOKEN";
   }
   return "TP_ERR_UNKNOWN";
 }
@@ -938,7 +1000,7 @@ extern "C" tp_status tp_device_status(tp_stream_t stream, int32_t *detail) {
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if (detail) *detail = word;
-  return word == 0 ? TP_OK : TP_ERR_TIMEOUT;
+  return word == 0 ? TP_OK : (word == kDevBadToken ? TP_ERR_BAD_TOKEN : TP_ERR_TIMEOUT);
 }
 
 extern "C" tp_status tp_set_wait_budget(int64_t nanoseconds) {

@@ -25,6 +25,7 @@ enum : int {
   kDevTimeoutEpilogue = 0x103,  // epilogue gave up waiting for the accumulator
   kDevTimeoutDrain = 0x104,     // teardown gave up waiting for in-flight copies
   kDevTimeoutDebug = 0x1FF,     // tp_debug_wait_timeout's wait
+  kDevBadToken = 0x201,         // an embedding lookup met a token id outside [0, V)
 };
 
 struct DevCtx {
@@ -235,6 +236,22 @@ struct CopyBatch {
   int n;
 };
 tp_status launch_copy_batch(const CopyBatch &b, cudaStream_t s);
+
+// Vocab-parallel embedding lookup with its all-gather: token i's row comes from
+// shard r = ids[i] / rows_per_rank (its row ids[i] - r * rows_per_rank) and is
+// stored to every output. Bad ids give zero rows and kDevBadToken.
+struct EmbedArgs {
+  const char *tab[kMaxRanks];
+  long long tab_pitch[kMaxRanks];   // bytes between rows of shard r
+  char *out[kMaxRanks];
+  long long out_pitch[kMaxRanks];   // bytes between rows of output o
+  const int *ids;
+  long long n_tokens, rows_per_rank, row_bytes;
+  int n, n_outs, esize;
+  int *status;
+};
+// vec16: every base, pitch and the row length are multiples of 16 bytes.
+tp_status launch_vocab_embed(const EmbedArgs &a, bool vec16, cudaStream_t s);
 
 // Kernel that always times out its bounded wait (tests of the timeout path).
 tp_status launch_debug_wait(cudaStream_t s);

@@ -25,6 +25,9 @@ STREAM = {
     "buf": 10,   # raw collective buffers
     "h": 11,     # row-parallel input H [T x ffn] of the reduce-scatter pipeline
     "wqkv": 12,  # fused per-rank q/k/v weight of the reduce-scatter pipeline
+    "ids": 13,   # token ids of the vocab-parallel lookup
+    "emb": 14,   # embedding table [V x D]
+    "wlm": 15,   # LM-head weight [V x D]
 }
 
 # Workloads, named by what they are. Weight tensors are stored [out x in]
@@ -58,6 +61,12 @@ WORKLOADS = {
     "rs_column_tp8_t4096": dict(kind="rs_column", T=4096, hidden=8192, q_heads=64,
                                 kv_heads=8, head_dim=128, ffn=28672, tp=8,
                                 seed=106, w_std=0.02),
+    # Vocab-parallel embedding lookup and LM head of a 128256-token vocabulary
+    # (above the 100k tokens where vocab sharding pays), hidden 8192, TP=8, bf16
+    # with f32 logits: 4096 uniformly drawn token ids are looked up, and the
+    # logits of 4096 hidden states are computed over the whole vocabulary.
+    "vocab_tp8_t4096": dict(kind="vocab", T=4096, hidden=8192, vocab=128256, tp=8,
+                            seed=107, w_std=0.02),
 }
 
 
@@ -116,6 +125,11 @@ def normal_bf16(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
 _BLOCK = 1 << 24  # elements per block of normal_bf16
 
 
+def token_ids(seed: int, stream: int, n: int, vocab: int) -> np.ndarray:
+    """n token ids drawn uniformly from [0, vocab), as int32."""
+    return rng(seed, stream).integers(0, vocab, size=n).astype(np.int32)
+
+
 def small_int_bf16(seed: int, stream: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
     """Uniform integers in [lo, hi] as bf16 bits (exact in bf16; used for bit-exact cases)."""
     g = rng(seed, stream)
@@ -143,6 +157,8 @@ def weight_shapes(w: dict) -> dict:
     if kind in ("mlp", "layer"):
         F = w["ffn"]
         out.update(wg=(F, D), wu=(F, D), wd=(D, F))
+    if kind == "vocab":
+        out.update(emb=(w["vocab"], D), wlm=(w["vocab"], D))
     if kind == "rs_column":
         n, hd = w["tp"], w["head_dim"]
         per = (w["q_heads"] // n + 2 * max(1, w["kv_heads"] // n)) * hd
@@ -161,6 +177,8 @@ def make_bf16_inputs(w: dict, rows: int | None = None) -> dict:
     out = {"x": normal_bf16(seed, STREAM["x"], (T, w["hidden"]))}
     if w["kind"] == "rs_column":
         out["h"] = normal_bf16(seed, STREAM["h"], (T, w["ffn"]))
+    if w["kind"] == "vocab":
+        out["ids"] = token_ids(seed, STREAM["ids"], T, w["vocab"])
     if w["kind"] in ("attn", "layer"):
         out["a"] = normal_bf16(seed, STREAM["a"], (T, w["q_heads"] * w["head_dim"]))
     for name, shp in weight_shapes(w).items():

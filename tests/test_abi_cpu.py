@@ -209,6 +209,48 @@ def test_all_gather_rejects_bad_arguments():
     assert st(sh, out * 3, 1, 3) == tp.TP_ERR_INVALID_ARG    # n_out must be 1 or tp_size
 
 
+def test_vocab_embedding_rejects_bad_arguments():
+    tab = [T(FAKE, BF, 16, 64), T(FAKE + 4096, BF, 16, 64)]
+    out = [T(FAKE + 8192, BF, 5, 64)]
+    ids = FAKE + (1 << 16)
+
+    def st(t_, o_, n_tok=5, n=2, ids_=ids, n_out=None):
+        return tp.raw_status("tp_vocab_embedding", n, ids_, n_tok, arr(*t_), arr(*o_),
+                             n_out if n_out is not None else len(o_), None)
+    assert st(tab, out, ids_=0) == tp.TP_ERR_INVALID_ARG          # no ids
+    assert st(tab, out, n_tok=-1) == tp.TP_ERR_INVALID_ARG
+    assert st([tab[0], T(FAKE + 4096, BF, 15, 64)], out) == tp.TP_ERR_INVALID_ARG  # slices differ
+    assert st([tab[0], T(FAKE + 4096, F32, 16, 64)], out) == tp.TP_ERR_DTYPE
+    assert st(tab, [T(FAKE + 8192, F32, 5, 64)]) == tp.TP_ERR_DTYPE
+    assert st(tab, [T(FAKE + 8192, BF, 4, 64)]) == tp.TP_ERR_INVALID_ARG  # rows != n_tokens
+    assert st(tab, [T(FAKE + 8192, BF, 5, 32)]) == tp.TP_ERR_INVALID_ARG  # cols != D
+    assert st(tab, out * 3, n_out=3) == tp.TP_ERR_INVALID_ARG          # n_out must be 1 or tp_size
+    assert st(tab + [tab[0]], out, n=3) == tp.TP_ERR_TP_SIZE_NOT_POW2
+    assert st(tab, out, ids_=ids + 2) == tp.TP_ERR_ALIGNMENT
+    assert st([tab[0], T(FAKE + 4097, BF, 16, 64)], out) == tp.TP_ERR_ALIGNMENT
+    f32tab = [T(FAKE, F32, 16, 64), T(FAKE + 4096, F32, 16, 64)]
+    assert st(f32tab, [T(FAKE + 8194, F32, 5, 64)]) == tp.TP_ERR_ALIGNMENT
+    assert st(tab, [T(FAKE + 8192, BF, 0, 64)], n_tok=0, ids_=0) == tp.TP_OK  # nothing to look up
+    tp.tp_set_rank_health(1, False)
+    try:
+        assert st(tab, out) == tp.TP_ERR_RANK_FAILED
+    finally:
+        tp.tp_set_rank_health(1, True)
+
+
+def test_vocab_lm_head_rejects_bad_arguments():
+    x = T(FAKE, BF, 64, 128)
+    w = [T(FAKE, BF, 32, 128), T(FAKE + 8192, BF, 32, 128)]
+    logits = [T(FAKE, F32, 64, 64)]
+
+    def st(w_, y_, gather=1, n=2):
+        return tp.raw_status("tp_vocab_lm_head", n, ctypes.byref(x), arr(*w_), arr(*y_), gather, None)
+    assert st([w[0], T(FAKE + 8192, BF, 24, 128)], [T(FAKE, F32, 64, 56)]) == tp.TP_ERR_INVALID_ARG
+    assert st(w, [T(FAKE, F32, 64, 60)]) == tp.TP_ERR_INVALID_ARG
+    assert st(w, [T(FAKE + 4, F32, 64, 64)]) == tp.TP_ERR_ALIGNMENT
+    assert st(w, logits, gather=3) == tp.TP_ERR_INVALID_ARG
+
+
 def test_failed_rank_stops_the_group_before_any_launch():
     # Host-side fault injection: rank 1 reports unhealthy; every call that involves
     # it returns TP_ERR_RANK_FAILED before enqueuing work (no GPU needed).
