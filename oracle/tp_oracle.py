@@ -22,6 +22,10 @@ It is a plain, slow, obviously correct restatement of what the pages define:
          AllReduce, q AllGather) and the GQA rule (shard K/V when
          num_kv_heads >= tp_size, replicate otherwise), with its two examples.
        - 설정 (Configuration): --tp-size is a power of two, default 1.
+       - MoE 전문가 병렬화 (MoE expert parallelism): Expert Parallel puts
+         expert i whole on rank i % tp_size; Within-Expert Parallel shards every
+         expert's FFN over all ranks with the dense FFN's column-parallel
+         gate/up and row-parallel down projections.
        - Vocab Parallel (a weight-sharding strategy) and 임베딩 및 LM Head 샤딩
          (Embedding and LM-head sharding): the vocabulary dimension of the
          embedding table and the LM head is split into contiguous per-rank
@@ -49,6 +53,9 @@ Conventions (readings of the pages, each listed in the design notes):
     (the pages name no activation).
   * The o_proj input (attention context A) is an explicit input; attention
     itself is not part of this block.
+  * MoE: the routing (top-k expert ids and weights per token) is an input; a
+    rank's partial output sums, in slot order, the weighted contributions of the
+    slots it runs, and the partials are all-reduced on the ring.
   * Vocab slices are equal (V divisible by N). The embedding all-gather moves
     each rank's looked-up rows ("piece") around the ring like any all-gather;
     every token's row comes from the one rank whose slice holds its id.
@@ -435,6 +442,74 @@ def mlp_sharded(x, wg, wu, wd, tp_size: int, log: RingLog | None = None) -> dict
     p = row_parallel(h, split_cols(wd, tp_size))
     y = ring_all_reduce([pr.reshape(-1) for pr in p], log)
     return {"h": h, "partials": p, "y": [yr.reshape(T, D) for yr in y]}
+
+
+# ---------------------------------------------------------------------------
+# Mixture of experts ([MLX] MoE 전문가 병렬화: Expert Parallel, Within-Expert Parallel)
+# ---------------------------------------------------------------------------
+MOE_EXPERT_PARALLEL, MOE_WITHIN_EXPERT = "expert_parallel", "within_expert"
+
+
+def expert_rank(expert: int, tp_size: int) -> int:
+    """Rank holding expert i whole in expert-parallel mode: experts are dealt to
+    the ranks round-robin, expert i on rank i % tp_size ([MLX] Expert Parallel)."""
+    return expert % tp_size
+
+
+def moe_unsharded(x, topk_ids, topk_w, wg, wu, wd) -> np.ndarray:
+    """The plain top-k mixture: token t's output is the sum over its k routing
+    slots j of topk_w[t, j] times expert topk_ids[t, j]'s FFN (the dense MLP's
+    SwiGLU definition with that expert's weights) applied to x[t]. The routing
+    (ids and weights) is an input; the router itself is not part of the block."""
+    x = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    w = np.asarray(topk_w, dtype=np.float64)
+    y = np.zeros((x.shape[0], np.asarray(wd[0]).shape[0]))
+    for t in range(x.shape[0]):
+        for j in range(ids.shape[1]):
+            e = ids[t, j]
+            y[t] += w[t, j] * mlp_unsharded(x[t:t + 1], wg[e], wu[e], wd[e])[0]
+    return y
+
+
+def moe_sharded(x, topk_ids, topk_w, wg, wu, wd, tp_size: int, mode: str,
+                log: RingLog | None = None) -> dict:
+    """MoE block over tp_size ranks ([MLX] MoE 전문가 병렬화).
+
+    expert_parallel: rank r runs, whole, the experts i with i % tp_size == r and
+    only the routing slots that chose them; no communication inside an expert.
+    within_expert: every expert's FFN is sharded over all ranks like the dense
+    FFN (gate/up column-parallel, down row-parallel), so rank r runs every slot
+    with its slice of every expert.
+    Either way rank r's partial output sums its slots' weighted contributions,
+    and the partials are combined by the ring all-reduce (the row-parallel
+    down projection's all-reduce, as in the dense FFN; the router runs on every
+    rank, so every rank sees the same routing).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    w = np.asarray(topk_w, dtype=np.float64)
+    n, T = tp_size, x.shape[0]
+    D = np.asarray(wd[0]).shape[0]
+    if mode not in (MOE_EXPERT_PARALLEL, MOE_WITHIN_EXPERT):
+        raise ValueError(f"unknown MoE mode {mode}")
+    partials = [np.zeros((T, D)) for _ in range(n)]
+    for r in range(n):
+        for t in range(T):
+            for j in range(ids.shape[1]):
+                e = ids[t, j]
+                if mode == MOE_EXPERT_PARALLEL:
+                    if expert_rank(e, n) != r:
+                        continue
+                    contrib = mlp_unsharded(x[t:t + 1], wg[e], wu[e], wd[e])[0]
+                else:
+                    g_r = split_rows(np.asarray(wg[e], dtype=np.float64), n)[r]
+                    u_r = split_rows(np.asarray(wu[e], dtype=np.float64), n)[r]
+                    d_r = split_cols(np.asarray(wd[e], dtype=np.float64), n)[r]
+                    contrib = linear(swiglu(linear(x[t:t + 1], g_r), linear(x[t:t + 1], u_r)), d_r)[0]
+                partials[r][t] += w[t, j] * contrib
+    y = ring_all_reduce([p.reshape(-1) for p in partials], log)
+    return {"partials": partials, "y": [yr.reshape(T, D) for yr in y]}
 
 
 def attn_proj_unsharded(x, wq, wk, wv, a, wo) -> dict:
