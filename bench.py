@@ -51,6 +51,8 @@ def parse_args():
                    help="ring_fused (default): the ring all-reduce in one pass, bit-identical to ring (N-1 step "
                         "launches per phase). The reduce-scatter pipeline workload takes deferred (default: the "
                         "column GEMM reads the reduced chunks) or gathered (an all-gather first)")
+    p.add_argument("--moe-mode", choices=["within_expert", "expert_parallel"], default="within_expert",
+                   help="MoE sharding of the moe workloads")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -256,7 +258,7 @@ class DeviceSet:
     """One copy of a workload's inputs, weights and outputs in HBM, sharded per the plan,
     with the step's C calls marshalled once."""
 
-    def __init__(self, tp, torch, w, data, plan, shards, dev, sptr, mode):
+    def __init__(self, tp, torch, w, data, plan, shards, dev, sptr, mode, moe_mode="within_expert"):
         import numpy as np
         n, T = w["tp"], w["T"]
         D = w["hidden"]
@@ -318,6 +320,40 @@ class DeviceSet:
                 self.calls.append(("combine_mlp", tp.Prepared("tp_allreduce_ring", n, tp.arr(ym), combine_ring,
                                                              sptr)))
             self.e2e["mlp"] = (g, u, dn, ym)
+        if w["kind"] == "moe":
+            E, F, k = w["experts"], w["ffn"], w["top_k"]
+            within = moe_mode == "within_expert"
+            eg, eu, ed = data["eg"], data["eu"], data["ed"]
+            if within:  # rank r: every expert's F/N slice, stacked by expert
+                fs = F // n
+                g = [np.concatenate([eg[e, r * fs:(r + 1) * fs] for e in range(E)]) for r in range(n)]
+                u = [np.concatenate([eu[e, r * fs:(r + 1) * fs] for e in range(E)]) for r in range(n)]
+                dn = [np.concatenate([ed[e][:, r * fs:(r + 1) * fs] for e in range(E)]) for r in range(n)]
+            else:       # rank r: experts r, r+N, ... whole
+                g = [np.concatenate([eg[e] for e in range(r, E, n)]) for r in range(n)]
+                u = [np.concatenate([eu[e] for e in range(r, E, n)]) for r in range(n)]
+                dn = [np.concatenate([ed[e] for e in range(r, E, n)]) for r in range(n)]
+            g, u, dn = [to_dev(t) for t in g], [to_dev(t) for t in u], [to_dev(t) for t in dn]
+            self.rid = torch.from_numpy(data["topk_ids"]).to(dev)
+            self.rw = torch.from_numpy(data["topk_w"]).to(dev)
+            self.dims = tp.moe_dims(n, tp.TP_MOE_WITHIN_EXPERT if within else tp.TP_MOE_EXPERT_PARALLEL, E, k, D, F)
+            ws = torch.empty(tp.tp_moe_workspace_size(self.dims, T), dtype=torch.uint8, device=dev)
+            self.keep += [self.rid, self.rw, ws]
+            combine_id = COMBINE_NAMES[mode]
+
+            def moe_calls(xbuf, rid, rw, ys):
+                """The public MoE block call: routing, gather, expert GEMMs, weighted
+                combine and the all-reduce, all on the device."""
+                xs = tp.tensor(xbuf)
+                self.keep.append(xs)
+                return [("moe_block", tp.Prepared(
+                    "tp_moe_block", ctypes.byref(self.dims), ctypes.byref(xs), rid.data_ptr(), rw.data_ptr(),
+                    tp.arr(g), tp.arr(u), tp.arr(dn), tp.arr(ys), combine_id, ws.data_ptr(), ws.numel(), sptr))]
+
+            ys = [torch.empty((T, D), device=dev) for _ in range(1 if mode == "fused" else n)]
+            self.keep += ys
+            self.calls += moe_calls(self.x, self.rid, self.rw, ys)
+            self.e2e["moe"] = (moe_calls, ys)
         if w["kind"] == "vocab":
             V = w["vocab"]
             per_v = V // n
@@ -401,6 +437,12 @@ def phase_costs(w, mode):
         out["gate_up"] = (4.0 * T * D * F, 2 * F * D * 2 + T * D * 2 + T * F * 2)
         out["down"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + nparts * part)
         out["combine_mlp"] = (0.0, ring_bytes(mode, n, part))
+    if w["kind"] == "moe":
+        E, F, k = w["experts"], w["ffn"], w["top_k"]
+        a = T * k
+        # weights once, X, the routed copy of X and H written and read, f32 partials and outputs
+        out["moe_block"] = (6.0 * a * D * F, 3 * E * F * D * 2 + T * D * 2 + 2 * a * D * 2 + 2 * a * F * 2 +
+                            2 * (n if mode != "fused" else 1) * a * D * 4 + ring_bytes(mode, n, part))
     if w["kind"] == "vocab":
         V = w["vocab"]
         out["embed"] = (0.0, T * D * 2 * 2 + T * 4)        # rows read once and written once, ids
@@ -443,7 +485,7 @@ def run_native(args):
     costs = phase_costs(w, mode)
     set_bytes = sum(b for (_f, b) in costs.values() if b) + T * D * 2
     R = max(1, -(-2 * L2_BYTES // set_bytes) + (1 if set_bytes < 2 * L2_BYTES else 0))
-    sets = [DeviceSet(tp, torch, w, data, plan0, shards, dev, sptr, mode) for _ in range(R)]
+    sets = [DeviceSet(tp, torch, w, data, plan0, shards, dev, sptr, mode, args.moe_mode) for _ in range(R)]
     names = [nm for (nm, _c) in sets[0].calls]
 
     def step(s, ev=None):
@@ -507,7 +549,7 @@ def run_native(args):
     peaks, peak_src = load_peaks()
 
     # roofline of the dominant kernel: the gate/up GEMM where there is an MLP, else q/k/v
-    rk = next(k for k in ("gate_up", "qkv", "row", "lm_head") if k in phase_ms)
+    rk = next(k for k in ("gate_up", "qkv", "row", "lm_head", "moe_block") if k in phase_ms)
     rf, rb = costs[rk]
     r_s = phase_ms[rk] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -540,6 +582,10 @@ def run_native(args):
     outs_h = []
     idh = torch.from_numpy(data["ids"]).pin_memory() if "vocab" in s0.e2e else None
     h2d = xh.numel() * 2 + (ah.numel() * 2 if ah is not None else 0) + (idh.numel() * 4 if idh is not None else 0)
+    if "moe" in s0.e2e:
+        rih = torch.from_numpy(data["topk_ids"]).pin_memory()
+        rwh = torch.from_numpy(data["topk_w"]).pin_memory()
+        h2d += rih.numel() * 4 + rwh.numel() * 4
     d2h = 0
     if "attn" in s0.e2e:
         outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
@@ -548,6 +594,9 @@ def run_native(args):
         outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
         d2h += T * D * 4
         ws = torch.empty(tp.tp_mlp_block_workspace_size(plan0, T), dtype=torch.uint8, device=dev)
+    if "moe" in s0.e2e:
+        outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())  # the layer output
+        d2h += T * D * 4
     if "vocab" in s0.e2e:
         # the looked-up rows and the full f32 logits come back
         for t in s0.e2e["vocab"][1:]:
@@ -572,6 +621,11 @@ def run_native(args):
         if "mlp" in s0.e2e:
             sl["ym"] = s0.e2e["mlp"][3] if first else [torch.empty_like(t) for t in s0.e2e["mlp"][3]]
             sl["ws"] = ws if first else torch.empty_like(ws)
+        if "moe" in s0.e2e:
+            sl["rid"] = s0.rid if first else torch.empty_like(s0.rid)
+            sl["rw"] = s0.rw if first else torch.empty_like(s0.rw)
+            ym0 = s0.e2e["moe"][1]
+            sl["ymoe"] = ym0 if first else [torch.empty_like(t) for t in ym0]
         if "vocab" in s0.e2e:
             _f, x00, lg0 = s0.e2e["vocab"]
             sl["ids"] = s0.ids if first else torch.empty_like(s0.ids)
@@ -604,6 +658,8 @@ def run_native(args):
             sl["calls"] += [c for (_nm, c) in s0.e2e["rs_column"][0](sl["x"], sl["ys"])]
         if "vocab" in s0.e2e:
             sl["calls"] += [c for (_nm, c) in s0.e2e["vocab"][0](sl["ids"], sl["x"], *sl["vo"])]
+        if "moe" in s0.e2e:
+            sl["calls"] += [c for (_nm, c) in s0.e2e["moe"][0](sl["x"], sl["rid"], sl["rw"], sl["ymoe"])]
 
     def compute(sl):
         for call in sl["calls"]:
@@ -612,7 +668,8 @@ def run_native(args):
     def results(sl):
         return (([sl["yo"][0]] if "attn" in s0.e2e else []) + ([sl["ym"][0]] if "mlp" in s0.e2e else []) +
                 (list(sl["ys"]) if "rs_column" in s0.e2e else []) +
-                (list(sl["vo"]) if "vocab" in s0.e2e else []))
+                (list(sl["vo"]) if "vocab" in s0.e2e else []) +
+                ([sl["ymoe"][0]] if "moe" in s0.e2e else []))
 
     def serial_step():
         sl = slots[0]
@@ -621,6 +678,9 @@ def run_native(args):
             sl["a"].copy_(ah, non_blocking=True)
         if "ids" in sl:
             sl["ids"].copy_(idh, non_blocking=True)
+        if "rid" in sl:
+            sl["rid"].copy_(rih, non_blocking=True)
+            sl["rw"].copy_(rwh, non_blocking=True)
         compute(sl)
         for hbuf, dbuf in zip(sl["outs_h"], results(sl)):
             hbuf.copy_(dbuf, non_blocking=True)
@@ -641,6 +701,9 @@ def run_native(args):
                 sl["a"].copy_(ah, non_blocking=True)
             if "ids" in sl:
                 sl["ids"].copy_(idh, non_blocking=True)
+            if "rid" in sl:
+                sl["rid"].copy_(rih, non_blocking=True)
+                sl["rw"].copy_(rwh, non_blocking=True)
             ev_in[b].record(h2d_s)
         stream.wait_event(ev_in[b])
         if i >= 2:
@@ -696,7 +759,9 @@ def run_native(args):
               "parallelism": f"tp{n} logical ranks on one GPU; replicas across GPUs"}
     if w["kind"] == "vocab":
         config["combine"] = "all-gather of the looked-up rows and of the logits (in the kernels)"
-    for k in ("ffn", "q_heads", "kv_heads", "head_dim", "vocab"):
+    if w["kind"] == "moe":
+        config["moe_mode"] = args.moe_mode
+    for k in ("ffn", "q_heads", "kv_heads", "head_dim", "vocab", "experts", "top_k"):
         if k in w:
             config[k] = w[k]
     line = {
@@ -759,7 +824,8 @@ def run_reference(args):
 
 
 DEFAULT_STEPS = {"mlp_tp2_t512": 10000, "attn_gqa_tp4_t2048": 3000, "decode_gqa_rep_tp8_t64": 6000,
-                 "prefill_layer_tp8_t4096": 200, "rs_column_tp8_t4096": 600, "vocab_tp8_t4096": 200}
+                 "prefill_layer_tp8_t4096": 200, "rs_column_tp8_t4096": 600, "vocab_tp8_t4096": 200,
+                 "moe_mixtral_tp8_t4096": 400}
 
 
 def main():

@@ -302,6 +302,63 @@ tp_status tp_vocab_lm_head(int32_t tp_size, const tp_tensor *x, const tp_tensor 
                            tp_tensor *logits, int32_t gather, tp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Mixture of experts (mlxcel manual, MoE 전문가 병렬화 / MoE expert parallelism:
+ * Expert Parallel puts expert i whole on rank i % tp_size, with no
+ * communication inside an expert; Within-Expert Parallel shards every expert's
+ * FFN over all ranks with the dense FFN's column-parallel gate/up and
+ * row-parallel down projections).
+ * ------------------------------------------------------------------------- */
+typedef enum tp_moe_mode {
+  TP_MOE_EXPERT_PARALLEL = 0,
+  TP_MOE_WITHIN_EXPERT = 1
+} tp_moe_mode;
+
+typedef struct tp_moe_dims {
+  int32_t tp_size;      /* N, a power of two                                       */
+  int32_t mode;         /* tp_moe_mode                                             */
+  int32_t num_experts;  /* E, 1..256; a multiple of N for expert parallel          */
+  int32_t top_k;        /* k routing slots per token, >= 1                         */
+  int64_t hidden;       /* D, a multiple of 8                                      */
+  int64_t ffn;          /* F per expert; F/N a multiple of 8 for within-expert      */
+} tp_moe_dims;
+
+/* Workspace bytes tp_moe_block needs for `tokens` tokens: the routed layout of
+ * T*k rows (each expert's rows padded to whole GEMM tiles), the gathered
+ * inputs, H and the f32 down-projection rows of every rank. 0 for bad dims. */
+size_t tp_moe_workspace_size(const tp_moe_dims *dims, int64_t tokens);
+
+/* MoE block: Y = sum_r Y_r, where rank r's partial output is, per token t, the
+ * sum over its slots j (in slot order) of topk_w[t,j] times the FFN (SwiGLU,
+ * silu(X G^T) * (X U^T) then D^T, H rounded to bf16) of expert topk_ids[t,j]
+ * restricted to what rank r holds of it:
+ *  - expert parallel: the whole expert when expert % N == r, else nothing;
+ *  - within-expert: rows [r*F/N, (r+1)*F/N) of its gate and up weights and the
+ *    same columns of its down weight.
+ * The routing is an input (the router runs on every rank, so all ranks share
+ * it); the block routes, gathers, runs the expert GEMMs and combines on the
+ * device, with no host synchronisation.
+ *  x         : [T x D] bf16.
+ *  topk_ids  : device int32 [T x k], row-major. An id outside [0, E) drops that
+ *              slot and is reported by tp_device_status as TP_ERR_BAD_TOKEN.
+ *  topk_w    : device f32 [T x k], row-major.
+ *  w_gate[r], w_up[r] : rank r's expert weights stacked by slot, bf16:
+ *              within-expert [E*F/N x D], expert e's slice at rows [e*F/N, ...);
+ *              expert parallel [(E/N)*F x D], slot s = expert r + s*N at rows [s*F, ...).
+ *  w_down[r] : within-expert [E*D x F/N], expert e at rows [e*D, (e+1)*D);
+ *              expert parallel [(E/N)*D x F], slot s at rows [s*D, (s+1)*D).
+ *  y         : f32 [T x D]; y[0] for TP_COMBINE_FUSED (the sum over ranks),
+ *              y[0..N-1] otherwise (TP_COMBINE_NONE leaves the partials, RING
+ *              and RING_FUSED all-reduce them on the ring).
+ *  workspace : device memory of at least tp_moe_workspace_size bytes, 256-byte
+ *              aligned; its contents on entry do not matter.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_TP_SIZE_NOT_POW2, TP_ERR_NOT_DIVISIBLE,
+ * TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_WORKSPACE, TP_ERR_RANK_FAILED, TP_ERR_CUDA. */
+tp_status tp_moe_block(const tp_moe_dims *dims, const tp_tensor *x, const int32_t *topk_ids,
+                       const float *topk_w, const tp_tensor *w_gate, const tp_tensor *w_up,
+                       const tp_tensor *w_down, tp_tensor *y, int32_t combine, void *workspace,
+                       size_t workspace_bytes, tp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Blocks (mlxcel manual, 아키텍처 인식 샤드 플랜: gate/up ColumnParallel with no
  * communication, down RowParallel + AllReduce; q/k/v ColumnParallel, o
  * RowParallel + AllReduce).

@@ -35,6 +35,7 @@ TP_W_Q, TP_W_K, TP_W_V, TP_W_O, TP_W_GATE, TP_W_UP, TP_W_DOWN, TP_W_COUNT = rang
 WEIGHT_NAMES = ["q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj"]
 TP_COMBINE_NONE, TP_COMBINE_FUSED, TP_COMBINE_RING, TP_COMBINE_RING_FUSED = 0, 1, 2, 3
 TP_RING_STEPS, TP_RING_FUSED = 0, 1
+TP_MOE_EXPERT_PARALLEL, TP_MOE_WITHIN_EXPERT = 0, 1
 
 
 class TpTensor(ctypes.Structure):
@@ -55,6 +56,11 @@ class TpRankShard(ctypes.Structure):
                 ("strategy", ctypes.c_int32 * TP_W_COUNT), ("comm", ctypes.c_int32 * TP_W_COUNT),
                 ("range_begin", ctypes.c_int64 * TP_W_COUNT),
                 ("range_end", ctypes.c_int64 * TP_W_COUNT)]
+
+
+class TpMoeDims(ctypes.Structure):
+    _fields_ = [("tp_size", ctypes.c_int32), ("mode", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64)]
 
 
 class TPError(RuntimeError):
@@ -89,6 +95,9 @@ _SIGS = {
     "tp_vocab_embedding": ([ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, _T, _T, ctypes.c_int32, _S],
                            ctypes.c_int),
     "tp_vocab_lm_head": ([ctypes.c_int32, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
+    "tp_moe_workspace_size": ([_P(TpMoeDims), ctypes.c_int64], ctypes.c_size_t),
+    "tp_moe_block": ([_P(TpMoeDims), _T, ctypes.c_void_p, ctypes.c_void_p, _T, _T, _T, _T, ctypes.c_int32,
+                      ctypes.c_void_p, ctypes.c_size_t, _S], ctypes.c_int),
     "tp_gate_up_swiglu": ([ctypes.c_void_p, _T, _T, _T, _T, _S], ctypes.c_int),
     "tp_mlp_block_workspace_size": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_size_t),
     "tp_mlp_block": ([ctypes.c_void_p, _T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_void_p,
@@ -300,6 +309,31 @@ def tp_vocab_lm_head(tp_size: int, x, w, logits, gather: bool, stream=None) -> N
     xs = tensor(x)
     _check(_lib.tp_vocab_lm_head(tp_size, ctypes.byref(xs), _arr(w), _arr(logits), int(gather),
                                  _stream(stream)), "tp_vocab_lm_head")
+
+
+def moe_dims(tp_size: int, mode: int, num_experts: int, top_k: int, hidden: int, ffn: int) -> TpMoeDims:
+    return TpMoeDims(tp_size, mode, num_experts, top_k, hidden, ffn)
+
+
+def tp_moe_workspace_size(dims: TpMoeDims, tokens: int) -> int:
+    return int(_lib.tp_moe_workspace_size(ctypes.byref(dims), tokens))
+
+
+def _dev_ptr(t, dtype: str) -> int:
+    if str(t.dtype) != dtype or not t.is_contiguous():
+        raise TypeError(f"expected a contiguous {dtype} tensor")
+    return t.data_ptr() if t.numel() else 0
+
+
+def tp_moe_block(dims: TpMoeDims, x, topk_ids, topk_w, w_gate, w_up, w_down, y, combine: int, workspace,
+                 stream=None) -> None:
+    """topk_ids: int32 [T x k] CUDA tensor; topk_w: float32 [T x k]; workspace: a
+    CUDA byte tensor of at least tp_moe_workspace_size bytes."""
+    xs = tensor(x)
+    _check(_lib.tp_moe_block(ctypes.byref(dims), ctypes.byref(xs), _dev_ptr(topk_ids, "torch.int32"),
+                             _dev_ptr(topk_w, "torch.float32"), _arr(w_gate), _arr(w_up), _arr(w_down),
+                             _arr(y), combine, workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "tp_moe_block")
 
 
 def tp_gate_up_swiglu(plan: Plan, x, w_gate, w_up, h, stream=None) -> None:

@@ -133,6 +133,7 @@ __device__ __forceinline__ void store_bf16_row16(__nv_bfloat16 *out, long long l
 // order, within a segment its k-tiles.
 struct Cursor {
   int tile, prob, mt, nt, seg, kt, kt_in_tile;
+  int moff, brow;  // B map offset and first B row of the tile (block tables)
   bool valid;
 };
 
@@ -148,7 +149,28 @@ __device__ __forceinline__ int find_problem(const GemmParams &p, int tile) {
   return lo;
 }
 
+// First tile at or after `tile`, stepping by `stride`, that its problem's block
+// table does not skip (every tile when there is no table). The producer, the
+// MMA issuer and the epilogue all step with it, so they see the same tiles.
+__device__ __forceinline__ int live_tile(const GemmParams &p, int tile, int stride) {
+  for (; tile < p.total_tiles; tile += stride) {
+    const GemmProblem &pr = p.prob[find_problem(p, tile)];
+    if (!pr.blk) break;
+    const int v = __ldg(pr.blk + (tile - pr.tile_begin) % pr.m_tiles);
+    if (v >= 0 && (v >> 16) < pr.n_moff) break;
+  }
+  return tile;
+}
+
+// B map offset and first B row of m-tile mt of a problem.
+__device__ __forceinline__ void tile_b_origin(const GemmProblem &pr, int mt, int &moff, int &brow) {
+  const int v = pr.blk ? __ldg(pr.blk + mt) : 0;
+  moff = v >> 16;
+  brow = (v & 0xFFFF) * pr.b_rows_per_blk;
+}
+
 __device__ __forceinline__ void cursor_tile(const GemmParams &p, Cursor &c, int tile) {
+  tile = live_tile(p, tile, gridDim.x);
   c.tile = tile;
   c.valid = tile < p.total_tiles;
   if (!c.valid) return;
@@ -157,6 +179,7 @@ __device__ __forceinline__ void cursor_tile(const GemmParams &p, Cursor &c, int 
   const int local = tile - pr.tile_begin;
   c.mt = local % pr.m_tiles;
   c.nt = local / pr.m_tiles;
+  tile_b_origin(pr, c.mt, c.moff, c.brow);
   c.seg = 0;
   c.kt = 0;
   c.kt_in_tile = 0;
@@ -254,8 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
       cursor_tile(p, pf, blockIdx.x);
       auto prefetch = [&](const Cursor &c) {
         const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
-        ptx::tma_prefetch_l2_2d(&p.maps[sg.b_map], c.kt * BK, c.nt * kBRows);
-        if (EPI == kEpiSwiGLU) ptx::tma_prefetch_l2_2d(&p.maps[sg.b2_map], c.kt * BK, c.nt * kBRows);
+        ptx::tma_prefetch_l2_2d(&p.maps[sg.b_map + c.moff], c.kt * BK, c.brow + c.nt * kBRows);
+        if (EPI == kEpiSwiGLU)
+          ptx::tma_prefetch_l2_2d(&p.maps[sg.b2_map + c.moff], c.kt * BK, c.brow + c.nt * kBRows);
       };
       for (int i = 0; i < kPrefetch && pf.valid; ++i) {
         prefetch(pf);
@@ -278,10 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
         const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
         ptx::mbar_arrive_expect_tx(full_bar(st), static_cast<uint32_t>(p.a_rows * 128 + C::kBBytes));
         ptx::tma_load_2d(a_slot(st), &p.maps[sg.a_map], ld.kt * BK, ld.mt * BM, full_bar(st));
-        ptx::tma_load_2d(b_slot(st), &p.maps[sg.b_map], ld.kt * BK, ld.nt * kBRows, full_bar(st));
+        ptx::tma_load_2d(b_slot(st), &p.maps[sg.b_map + ld.moff], ld.kt * BK, ld.brow + ld.nt * kBRows,
+                         full_bar(st));
         if (EPI == kEpiSwiGLU)
-          ptx::tma_load_2d(b_slot(st) + kBRows * 128, &p.maps[sg.b2_map], ld.kt * BK, ld.nt * kBRows,
-                           full_bar(st));
+          ptx::tma_load_2d(b_slot(st) + kBRows * 128, &p.maps[sg.b2_map + ld.moff], ld.kt * BK,
+                           ld.brow + ld.nt * kBRows, full_bar(st));
         issued = ++kb;
         cursor_next(p, ld);
       }
@@ -291,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
       int kb = 0;
       bool ok = true;
-      for (int tile = blockIdx.x, j = 0; ok && tile < p.total_tiles; tile += gridDim.x, ++j) {
+      for (int tile = live_tile(p, blockIdx.x, gridDim.x), j = 0; ok && tile < p.total_tiles;
+           tile = live_tile(p, tile + gridDim.x, gridDim.x), ++j) {
         const int a = j & 1;
         const uint32_t use = static_cast<uint32_t>(j >> 1);
         if (*abort_flag || !ptx::mbar_wait(tempty_bar(a), (use & 1) ^ 1, p.wait_ns)) {
@@ -331,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   } else {
     // ---- epilogue: warps 2..5, warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32) ----
     const int q = warp & 3;
-    for (int tile = blockIdx.x, j = 0; tile < p.total_tiles; tile += gridDim.x, ++j) {
+    for (int tile = live_tile(p, blockIdx.x, gridDim.x), j = 0; tile < p.total_tiles;
+         tile = live_tile(p, tile + gridDim.x, gridDim.x), ++j) {
       const int a = j & 1;
       const uint32_t use = static_cast<uint32_t>(j >> 1);
       const bool ready = ptx::mbar_wait(tfull_bar(a), use & 1, p.wait_ns);
@@ -533,13 +560,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // Cursor over this pair's tiles: tiles pair, pair + npairs, ...
       auto first = [&](Cursor &c) {
-        c.tile = pair;
-        c.valid = pair < p.total_tiles;
+        const int t = live_tile(p, pair, npairs);
+        c.tile = t;
+        c.valid = t < p.total_tiles;
         if (!c.valid) return;
-        c.prob = find_problem(p, pair);
+        c.prob = find_problem(p, t);
         const GemmProblem &pr = p.prob[c.prob];
-        c.mt = (pair - pr.tile_begin) % pr.m_tiles;
-        c.nt = (pair - pr.tile_begin) / pr.m_tiles;
+        c.mt = (t - pr.tile_begin) % pr.m_tiles;
+        c.nt = (t - pr.tile_begin) / pr.m_tiles;
+        tile_b_origin(pr, c.mt, c.moff, c.brow);
         c.seg = c.kt = c.kt_in_tile = 0;
       };
       auto next = [&](Cursor &c) {
@@ -549,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (c.kt < seg_stages<KSUB>(p.seg[pr.seg_begin + c.seg])) return;
         c.kt = 0;
         if (++c.seg < pr.seg_count) return;
-        const int t = c.tile + npairs;
+        const int t = live_tile(p, c.tile + npairs, npairs);
         c.tile = t;
         c.valid = t < p.total_tiles;
         if (!c.valid) return;
@@ -557,17 +586,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const GemmProblem &q = p.prob[c.prob];
         c.mt = (t - q.tile_begin) % q.m_tiles;
         c.nt = (t - q.tile_begin) / q.m_tiles;
+        tile_b_origin(q, c.mt, c.moff, c.brow);
         c.seg = c.kt = c.kt_in_tile = 0;
       };
       // This CTA's half of B: rows of its own map and offset.
       auto b_src = [&](const Cursor &c, int &map, int &row) {
         const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
         if (EPI == kEpiSwiGLU) {
-          map = leader ? sg.b_map : sg.b2_map;
-          row = c.nt * kHalfB;
+          map = (leader ? sg.b_map : sg.b2_map) + c.moff;
+          row = c.brow + c.nt * kHalfB;
         } else {
-          map = sg.b_map;
-          row = c.nt * BN + static_cast<int>(rank) * kHalfB;
+          map = sg.b_map + c.moff;
+          row = c.brow + c.nt * BN + static_cast<int>(rank) * kHalfB;
         }
       };
       Cursor ld, pf;
@@ -632,7 +662,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, BN);
       int kb = 0;
       bool ok = true;
-      for (int tile = pair, j = 0; ok && tile < p.total_tiles; tile += npairs, ++j) {
+      for (int tile = live_tile(p, pair, npairs), j = 0; ok && tile < p.total_tiles;
+           tile = live_tile(p, tile + npairs, npairs), ++j) {
         const int a = j & 1;
         const uint32_t use = static_cast<uint32_t>(j >> 1);
         if (*abort_flag || !ptx::mbar_wait(tempty_bar(a), (use & 1) ^ 1, p.wait_ns)) {
@@ -672,7 +703,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     const int q = warp & 3;
-    for (int tile = pair, j = 0; tile < p.total_tiles; tile += npairs, ++j) {
+    for (int tile = live_tile(p, pair, npairs), j = 0; tile < p.total_tiles;
+         tile = live_tile(p, tile + npairs, npairs), ++j) {
       const int a = j & 1;
       const uint32_t use = static_cast<uint32_t>(j >> 1);
       const bool ready = ptx::mbar_wait(tfull_bar(a), use & 1, p.wait_ns);
@@ -1499,7 +1531,8 @@ int GemmBuilder::use_3d_boxes(int kt) {
 }
 
 bool GemmBuilder::add_problem(int m, int n, void *out, long long ldc, const int *a_maps,
-                              const int *b_maps, const int *b2_maps, const long long *ks, int nseg) {
+                              const int *b_maps, const int *b2_maps, const long long *ks, int nseg,
+                              const int *blk, int b_rows_per_blk, int n_moff) {
   if (n_probs >= kMaxProblems || n_segs + nseg > kMaxSegs) return false;
   const int out_cols = (epi == kEpiSwiGLU) ? bn / 2 : bn;
   const int tile_m = pair ? 2 * BM : BM;
@@ -1513,6 +1546,10 @@ bool GemmBuilder::add_problem(int m, int n, void *out, long long ldc, const int 
   pr.seg_count = nseg;
   pr.out = out;
   pr.ldc = ldc;
+  pr.blk = blk;
+  pr.b_rows_per_blk = b_rows_per_blk;
+  pr.n_moff = n_moff;
+  if (blk) split = 1;  // block tables run on the persistent kernels only
   for (int s = 0; s < nseg; ++s) {
     GemmSeg &sg = p.seg[n_segs + s];
     sg.a_map = a_maps[s];

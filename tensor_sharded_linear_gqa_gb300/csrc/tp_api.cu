@@ -646,6 +646,104 @@ extern "C" tp_status tp_vocab_lm_head(int32_t n, const tp_tensor *x, const tp_te
   return tp_column_linear(n, x, w, logits, gather, stream);
 }
 
+namespace {
+
+tp_status moe_check_dims(const tp_moe_dims *d) {
+  if (!d) return TP_ERR_INVALID_ARG;
+  const int32_t n = d->tp_size;
+  if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
+  if (d->mode != TP_MOE_EXPERT_PARALLEL && d->mode != TP_MOE_WITHIN_EXPERT) return TP_ERR_INVALID_ARG;
+  if (d->num_experts < 1 || d->num_experts > kMaxExperts || d->top_k < 1 || d->hidden < 1 || d->ffn < 1)
+    return TP_ERR_INVALID_ARG;
+  const bool within = d->mode == TP_MOE_WITHIN_EXPERT;
+  if (!within && d->num_experts % n) return TP_ERR_NOT_DIVISIBLE;
+  if (within && d->ffn % n) return TP_ERR_NOT_DIVISIBLE;
+  if (d->hidden % 8 || (within ? d->ffn / n : d->ffn) % 8) return TP_ERR_ALIGNMENT;  // 16-byte rows
+  return TP_OK;
+}
+
+bool moe_tokens_ok(const tp_moe_dims *d, int64_t tokens) {
+  // assignments and rows of the routed layout are indexed with 32-bit ints
+  return tokens >= 0 && tokens <= (0x7fffffffLL - 256LL * kMaxExperts) / d->top_k;
+}
+
+}  // namespace
+
+extern "C" size_t tp_moe_workspace_size(const tp_moe_dims *d, int64_t tokens) {
+  if (moe_check_dims(d) != TP_OK || !moe_tokens_ok(d, tokens)) return 0;
+  return moe_layout(d->tp_size, d->mode, d->num_experts, d->top_k, tokens, d->hidden, d->ffn).total;
+}
+
+extern "C" tp_status tp_moe_block(const tp_moe_dims *d, const tp_tensor *x, const int32_t *topk_ids,
+                                  const float *topk_w, const tp_tensor *w_gate, const tp_tensor *w_up,
+                                  const tp_tensor *w_down, tp_tensor *y, int32_t combine, void *workspace,
+                                  size_t workspace_bytes, tp_stream_t stream) {
+  tp_status st = moe_check_dims(d);
+  if (st != TP_OK) return st;
+  if (!x || !w_gate || !w_up || !w_down || !y) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  const int32_t n = d->tp_size, E = d->num_experts;
+  const bool within = d->mode == TP_MOE_WITHIN_EXPERT;
+  const long long D = d->hidden, F = d->ffn, T = x->rows;
+  const long long e_loc = within ? E : E / n, Fs = within ? F / n : F;
+  if (!shape_ok(*x) || x->cols != D) return TP_ERR_INVALID_ARG;
+  if (x->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (!moe_tokens_ok(d, T)) return TP_ERR_INVALID_ARG;
+  auto check_w = [&](const tp_tensor &t, long long rows, long long cols) -> tp_status {
+    if (!shape_ok(t)) return TP_ERR_INVALID_ARG;
+    if (t.dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (t.rows != rows || t.cols != cols) return TP_ERR_INVALID_ARG;
+    if (!pitch_ok(t)) return TP_ERR_ALIGNMENT;
+    return TP_OK;
+  };
+  for (int32_t r = 0; r < n; ++r) {
+    if ((st = check_w(w_gate[r], e_loc * Fs, D)) != TP_OK) return st;
+    if ((st = check_w(w_up[r], e_loc * Fs, D)) != TP_OK) return st;
+    if ((st = check_w(w_down[r], e_loc * D, Fs)) != TP_OK) return st;
+  }
+  const int32_t ny = combine == TP_COMBINE_FUSED ? 1 : n;
+  for (int32_t q = 0; q < ny; ++q) {
+    if (!shape_ok(y[q])) return TP_ERR_INVALID_ARG;
+    if (y[q].dtype != TP_F32) return TP_ERR_DTYPE;
+    if (y[q].rows != T || y[q].cols != D) return TP_ERR_INVALID_ARG;
+    if (T > 0 && !pitch_ok(y[q])) return TP_ERR_ALIGNMENT;
+  }
+  if ((combine == TP_COMBINE_RING || combine == TP_COMBINE_RING_FUSED) && n > 1)
+    for (int32_t q = 0; q < n; ++q)
+      if (y[q].ld != D) return TP_ERR_INVALID_ARG;  // the ring reduces contiguous buffers
+  if (T > 0) {
+    if (!pitch_ok(*x)) return TP_ERR_ALIGNMENT;
+    if (!topk_ids || !topk_w) return TP_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(topk_ids) & 3) || (reinterpret_cast<uintptr_t>(topk_w) & 3))
+      return TP_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < tp_moe_workspace_size(d, T)) return TP_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return TP_ERR_ALIGNMENT;
+  }
+  if ((st = check_health(n)) != TP_OK) return st;
+  if (T == 0) return TP_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MoeCall c;
+  c.n = n;
+  c.mode = d->mode;
+  c.experts = E;
+  c.k = d->top_k;
+  c.combine = combine;
+  c.hidden = D;
+  c.ffn = F;
+  c.x = x;
+  c.ids = topk_ids;
+  c.weights = topk_w;
+  c.w_gate = w_gate;
+  c.w_up = w_up;
+  c.w_down = w_down;
+  c.y = y;
+  c.workspace = workspace;
+  if ((st = moe_forward(c, s)) != TP_OK) return st;
+  if (combine == TP_COMBINE_RING) return run_allreduce(n, y, TP_RING_STEPS, s);
+  if (combine == TP_COMBINE_RING_FUSED) return run_allreduce(n, y, TP_RING_FUSED, s);
+  return TP_OK;
+}
+
 extern "C" tp_status tp_ring_all_gather(int32_t n, tp_tensor *buf, int32_t mode, tp_stream_t stream) {
   tp_status st = check_ring_bufs(n, buf);
   if (st != TP_OK) return st;

@@ -105,9 +105,17 @@ struct GemmProblem {
   int m_tiles, n_tiles;
   int tile_begin;        // first linear tile id of this problem
   int seg_begin, seg_count;
+  int b_rows_per_blk;    // with a block table: B rows per block slot
+  int n_moff;            // with a block table: B maps per segment (entries whose
+                         // map offset is not below it are skipped like -1)
   int pad;
   void *out;             // output base (row-major)
   long long ldc;         // elements
+  // Optional device table, one entry per m-tile, written by an earlier kernel
+  // (the MoE routing): -1 skips the tile; otherwise (map_offset << 16) | slot
+  // takes B from map b_map + map_offset (b2_map + map_offset for SwiGLU), rows
+  // from slot * b_rows_per_blk on. Null: every tile, B rows from 0.
+  const int *blk;
 };
 
 struct GemmParams {
@@ -158,7 +166,8 @@ struct GemmBuilder {
   // Adds a problem with segments [(a_map, b_map, b2_map, k)...]; returns false
   // if the tables are full.
   bool add_problem(int m, int n, void *out, long long ldc, const int *a_maps, const int *b_maps,
-                   const int *b2_maps, const long long *ks, int nseg);
+                   const int *b2_maps, const long long *ks, int nseg, const int *blk = nullptr,
+                   int b_rows_per_blk = 0, int n_moff = 1);
   tp_status launch(cudaStream_t stream);
 };
 
@@ -252,6 +261,31 @@ struct EmbedArgs {
 };
 // vec16: every base, pitch and the row length are multiples of 16 bytes.
 tp_status launch_vocab_embed(const EmbedArgs &a, bool vec16, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Mixture-of-experts block (moe.cu).
+// ---------------------------------------------------------------------------
+constexpr int kMaxExperts = 256;
+// Rows of the routed layout and the workspace regions of tp_moe_block.
+struct MoeLayout {
+  bool pair;         // SM-pair GEMMs (256-row tiles) or single-CTA (128)
+  int bm;            // rows per tile; every expert's rows start on a tile
+  long long rows;    // capacity of the layout: T*k + E*(bm-1), rounded up to bm
+  long long nblk;    // tiles of rows (entries of the block table)
+  size_t off_pos, off_inv, off_blk, off_xp, off_h, off_yp, total;
+};
+MoeLayout moe_layout(int n, int mode, int experts, int k, long long tokens, long long hidden, long long ffn);
+// A validated tp_moe_block call (the combine's all-reduce is left to the caller).
+struct MoeCall {
+  int n, mode, experts, k, combine;
+  long long hidden, ffn;
+  const tp_tensor *x;
+  const int *ids;
+  const float *weights;
+  const tp_tensor *w_gate, *w_up, *w_down, *y;
+  void *workspace;
+};
+tp_status moe_forward(const MoeCall &c, cudaStream_t s);
 
 // Kernel that always times out its bounded wait (tests of the timeout path).
 tp_status launch_debug_wait(cudaStream_t s);

@@ -28,6 +28,8 @@ STREAM = {
     "ids": 13,   # token ids of the vocab-parallel lookup
     "emb": 14,   # embedding table [V x D]
     "wlm": 15,   # LM-head weight [V x D]
+    "route": 16,  # MoE routing: expert ids and weights per token
+    "eg": 17, "eu": 18, "ed": 19,  # MoE expert weights [E x F x D], [E x F x D], [E x D x F]
 }
 
 # Workloads, named by what they are. Weight tensors are stored [out x in]
@@ -67,6 +69,11 @@ WORKLOADS = {
     # logits of 4096 hidden states are computed over the whole vocabulary.
     "vocab_tp8_t4096": dict(kind="vocab", T=4096, hidden=8192, vocab=128256, tp=8,
                             seed=107, w_std=0.02),
+    # Mixtral-8x7B-shaped MoE layer: 8 experts of hidden 4096 and FFN 14336, top-2
+    # routing drawn uniformly (two distinct experts a token, softmax weights over
+    # the two), 4096 tokens, TP=8; within-expert sharding (F/N = 1792 per rank).
+    "moe_mixtral_tp8_t4096": dict(kind="moe", T=4096, hidden=4096, ffn=14336, experts=8, top_k=2,
+                                  tp=8, seed=108, w_std=0.02),
 }
 
 
@@ -130,6 +137,17 @@ def token_ids(seed: int, stream: int, n: int, vocab: int) -> np.ndarray:
     return rng(seed, stream).integers(0, vocab, size=n).astype(np.int32)
 
 
+def routing(seed: int, stream: int, tokens: int, experts: int, k: int) -> tuple:
+    """Synthetic top-k routing: k distinct experts per token drawn uniformly
+    (int32 [T x k]) and weights that are the softmax of k N(0,1) draws (float32)."""
+    g = rng(seed, stream)
+    keys = g.random((tokens, experts))
+    ids = np.argsort(keys, axis=1)[:, :k].astype(np.int32)  # a uniform k-subset, in random order
+    z = g.standard_normal((tokens, k))
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    return ids, (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
 def small_int_bf16(seed: int, stream: int, shape, lo: int = -4, hi: int = 4) -> np.ndarray:
     """Uniform integers in [lo, hi] as bf16 bits (exact in bf16; used for bit-exact cases)."""
     g = rng(seed, stream)
@@ -159,6 +177,9 @@ def weight_shapes(w: dict) -> dict:
         out.update(wg=(F, D), wu=(F, D), wd=(D, F))
     if kind == "vocab":
         out.update(emb=(w["vocab"], D), wlm=(w["vocab"], D))
+    if kind == "moe":
+        E, F = w["experts"], w["ffn"]
+        out.update(eg=(E, F, D), eu=(E, F, D), ed=(E, D, F))
     if kind == "rs_column":
         n, hd = w["tp"], w["head_dim"]
         per = (w["q_heads"] // n + 2 * max(1, w["kv_heads"] // n)) * hd
@@ -179,6 +200,8 @@ def make_bf16_inputs(w: dict, rows: int | None = None) -> dict:
         out["h"] = normal_bf16(seed, STREAM["h"], (T, w["ffn"]))
     if w["kind"] == "vocab":
         out["ids"] = token_ids(seed, STREAM["ids"], T, w["vocab"])
+    if w["kind"] == "moe":
+        out["topk_ids"], out["topk_w"] = routing(seed, STREAM["route"], T, w["experts"], w["top_k"])
     if w["kind"] in ("attn", "layer"):
         out["a"] = normal_bf16(seed, STREAM["a"], (T, w["q_heads"] * w["head_dim"]))
     for name, shp in weight_shapes(w).items():

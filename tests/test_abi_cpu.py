@@ -251,6 +251,49 @@ def test_vocab_lm_head_rejects_bad_arguments():
     assert st(w, logits, gather=3) == tp.TP_ERR_INVALID_ARG
 
 
+def test_moe_rejects_bad_arguments():
+    n, E, k, D, F, Tt = 2, 4, 2, 64, 128, 16
+    within = tp.moe_dims(n, tp.TP_MOE_WITHIN_EXPERT, E, k, D, F)
+    x = T(FAKE, BF, Tt, D)
+    g = [T(FAKE, BF, E * F // n, D)] * n
+    d = [T(FAKE, BF, E * D, F // n)] * n
+    y = [T(FAKE, F32, Tt, D)] * n
+    ws_need = tp.tp_moe_workspace_size(within, Tt)
+    assert ws_need > 0
+
+    def st(dims, x_=x, g_=g, u_=g, d_=d, y_=y, combine=tp.TP_COMBINE_RING_FUSED, ws=FAKE, wsb=None, ids=FAKE,
+           wts=FAKE):
+        return tp.raw_status("tp_moe_block", ctypes.byref(dims), ctypes.byref(x_), ids, wts, arr(*g_), arr(*u_),
+                             arr(*d_), arr(*y_), combine, ws, ws_need if wsb is None else wsb, None)
+    assert st(tp.moe_dims(3, 1, E, k, D, F)) == tp.TP_ERR_TP_SIZE_NOT_POW2
+    assert st(tp.moe_dims(n, 2, E, k, D, F)) == tp.TP_ERR_INVALID_ARG          # mode
+    assert st(tp.moe_dims(n, 1, 0, k, D, F)) == tp.TP_ERR_INVALID_ARG          # no experts
+    assert st(tp.moe_dims(n, 1, 257, k, D, F)) == tp.TP_ERR_INVALID_ARG        # over 256 experts
+    assert st(tp.moe_dims(n, 0, 3, k, D, F)) == tp.TP_ERR_NOT_DIVISIBLE        # E % N (expert parallel)
+    assert st(tp.moe_dims(n, 1, E, k, D, 129)) == tp.TP_ERR_NOT_DIVISIBLE      # F % N (within expert)
+    assert st(tp.moe_dims(n, 1, E, k, 60, F)) == tp.TP_ERR_ALIGNMENT           # D not a multiple of 8
+    assert st(within, g_=[T(FAKE, BF, E * F // n - 8, D)] * n) == tp.TP_ERR_INVALID_ARG
+    assert st(within, d_=[T(FAKE, F32, E * D, F // n)] * n) == tp.TP_ERR_DTYPE
+    assert st(within, y_=[T(FAKE, BF, Tt, D)] * n) == tp.TP_ERR_DTYPE
+    assert st(within, ws=FAKE + 16) == tp.TP_ERR_ALIGNMENT
+    assert st(within, wsb=ws_need - 1) == tp.TP_ERR_WORKSPACE
+    assert st(within, ids=0) == tp.TP_ERR_INVALID_ARG
+    assert st(within, ids=FAKE + 2) == tp.TP_ERR_ALIGNMENT
+    assert st(within, combine=7) == tp.TP_ERR_INVALID_ARG
+    assert st(within, y_=[T(FAKE, F32, Tt, D, ld=D + 8)] * n) == tp.TP_ERR_INVALID_ARG  # ring needs ld == D
+    # expert parallel takes [(E/N)*F x D] gate/up and [(E/N)*D x F] down per rank
+    ep = tp.moe_dims(n, tp.TP_MOE_EXPERT_PARALLEL, E, k, D, F)
+    ws_need = tp.tp_moe_workspace_size(ep, Tt)
+    assert st(ep, g_=[T(FAKE, BF, E // n * F, D)] * n, d_=[T(FAKE, BF, E // n * D, F)] * n,
+              ids=FAKE + 2) == tp.TP_ERR_ALIGNMENT  # shapes accepted, then the ids pointer is checked
+    assert tp.tp_moe_workspace_size(tp.moe_dims(n, 0, 3, k, D, F), Tt) == 0
+    tp.tp_set_rank_health(1, False)
+    try:
+        assert st(within, wsb=tp.tp_moe_workspace_size(within, Tt)) == tp.TP_ERR_RANK_FAILED
+    finally:
+        tp.tp_set_rank_health(1, True)
+
+
 def test_failed_rank_stops_the_group_before_any_launch():
     # Host-side fault injection: rank 1 reports unhealthy; every call that involves
     # it returns TP_ERR_RANK_FAILED before enqueuing work (no GPU needed).
