@@ -51,8 +51,11 @@ Conventions (readings of the pages, each listed in the design notes):
     (each add is one IEEE add in that precision, in the order above).
   * Activation of the MLP block: SwiGLU, silu(g) * u with silu(x) = x / (1 + e^-x)
     (the pages name no activation).
-  * The o_proj input (attention context A) is an explicit input; attention
-    itself is not part of this block.
+  * The o_proj input (attention context A) is an explicit input of the
+    projection block. The attention core that produces it (attention_core_sharded)
+    is scaled dot-product attention, causal for prefill, 1/sqrt(d) scale, no
+    position encoding (the pages name none); each local q head uses the kv head
+    the plan's q->kv map gives it.
   * MoE: the routing (top-k expert ids and weights per token) is an input; a
     rank's partial output sums, in slot order, the weighted contributions of the
     slots it runs, and the partials are all-reduced on the ring.
@@ -442,6 +445,50 @@ def mlp_sharded(x, wg, wu, wd, tp_size: int, log: RingLog | None = None) -> dict
     p = row_parallel(h, split_cols(wd, tp_size))
     y = ring_all_reduce([pr.reshape(-1) for pr in p], log)
     return {"h": h, "partials": p, "y": [yr.reshape(T, D) for yr in y]}
+
+
+# ---------------------------------------------------------------------------
+# Attention core between q/k/v and o_proj ([MLX] GQA 인식 어텐션 샤딩: each rank
+# attends with its own q heads over the kv heads the plan gives it)
+# ---------------------------------------------------------------------------
+def softmax_rows(s: np.ndarray) -> np.ndarray:
+    """Row-wise softmax exp(s - max) / sum exp(s - max); -inf entries get 0."""
+    s = np.asarray(s, dtype=np.float64)
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=1, keepdims=True)
+
+
+def attention_head(q, k, v, causal: bool) -> np.ndarray:
+    """Scaled dot-product attention of one head: softmax(q k^T / sqrt(d)) v,
+    with query i seeing keys j <= i when causal. q [T x d], k and v [T x d]."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = (q @ k.T) / np.sqrt(q.shape[1])
+    if causal:
+        t = s.shape[0]
+        s = np.where(np.arange(t)[None, :] <= np.arange(t)[:, None], s, -np.inf)
+    return softmax_rows(s) @ v
+
+
+def attention_core_sharded(q, k, v, plan: list, head_dim: int, causal: bool = True) -> list:
+    """Rank r's attention output A_r [T x Hq_r*d]: for each of its local q heads h,
+    attention_head of q head h with the kv head q_to_kv[h] of the rank's K/V
+    (its own kv heads when sharded, all of them when replicated). q[r] is
+    [T x Hq_r*d]; k[r], v[r] are [T x Hkv_r*d] (one shared entry when the plan
+    replicates K/V). A_r's columns are the rank's slice of the o_proj input."""
+    out = []
+    d = head_dim
+    for r, s in enumerate(plan):
+        kr = k[0] if s.kv_replicated else k[r]
+        vr = v[0] if s.kv_replicated else v[r]
+        heads = []
+        for h, g in enumerate(s.q_to_kv):
+            heads.append(attention_head(q[r][:, h * d:(h + 1) * d], kr[:, g * d:(g + 1) * d],
+                                        vr[:, g * d:(g + 1) * d], causal))
+        out.append(np.concatenate(heads, axis=1))
+    return out
 
 
 # ---------------------------------------------------------------------------
