@@ -320,6 +320,28 @@ class DeviceSet:
                 self.calls.append(("combine_mlp", tp.Prepared("tp_allreduce_ring", n, tp.arr(ym), combine_ring,
                                                              sptr)))
             self.e2e["mlp"] = (g, u, dn, ym)
+        if w["kind"] == "attn_core":
+            hd = w["head_dim"]
+            rep = shards[0]["kv_replicated"]
+            self.aq, self.ak, self.av = to_dev(data["q"]), to_dev(data["k"]), to_dev(data["v"])
+            ws = torch.empty(tp.tp_attn_core_workspace_size(plan, T), dtype=torch.uint8, device=dev)
+            aout = torch.empty((T, w["q_heads"] * hd), dtype=torch.bfloat16, device=dev)
+            self.keep += [ws, aout]
+
+            def cols(t, heads):
+                return t[:, heads[0] * hd:heads[1] * hd]
+
+            def attn_calls(qb, kb, vb, ob):
+                """The public attention-core call over every rank's q heads (causal)."""
+                qs = [cols(qb, shards[r]["q_heads"]) for r in range(n)]
+                outs = [cols(ob, shards[r]["q_heads"]) for r in range(n)]
+                ks = [kb] if rep else [cols(kb, shards[r]["kv_heads"]) for r in range(n)]
+                vs = [vb] if rep else [cols(vb, shards[r]["kv_heads"]) for r in range(n)]
+                return [("attn_core", tp.Prepared("tp_attn_core", plan.handle, tp.arr(qs), tp.arr(ks), tp.arr(vs),
+                                                  tp.arr(outs), 1, ws.data_ptr(), ws.numel(), sptr))]
+
+            self.calls += attn_calls(self.aq, self.ak, self.av, aout)
+            self.e2e["attn_core"] = (attn_calls, aout)
         if w["kind"] == "moe":
             E, F, k = w["experts"], w["ffn"], w["top_k"]
             within = moe_mode == "within_expert"
@@ -437,6 +459,11 @@ def phase_costs(w, mode):
         out["gate_up"] = (4.0 * T * D * F, 2 * F * D * 2 + T * D * 2 + T * F * 2)
         out["down"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + nparts * part)
         out["combine_mlp"] = (0.0, ring_bytes(mode, n, part))
+    if w["kind"] == "attn_core":
+        hd, hq, hkv = w["head_dim"], w["q_heads"], w["kv_heads"]
+        # causal: query i meets keys 0..i; QK^T and PV, 2 flops a multiply-add each
+        out["attn_core"] = (4.0 * hd * hq * T * (T + 1) / 2,
+                            T * hq * hd * 2 * 2 + T * hkv * hd * 2 * 2 + 2 * T * hkv * hd * 2)
     if w["kind"] == "moe":
         E, F, k = w["experts"], w["ffn"], w["top_k"]
         a = T * k
@@ -549,7 +576,7 @@ def run_native(args):
     peaks, peak_src = load_peaks()
 
     # roofline of the dominant kernel: the gate/up GEMM where there is an MLP, else q/k/v
-    rk = next(k for k in ("gate_up", "qkv", "row", "lm_head", "moe_block") if k in phase_ms)
+    rk = next(k for k in ("gate_up", "qkv", "row", "lm_head", "moe_block", "attn_core") if k in phase_ms)
     rf, rb = costs[rk]
     r_s = phase_ms[rk] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -582,6 +609,11 @@ def run_native(args):
     outs_h = []
     idh = torch.from_numpy(data["ids"]).pin_memory() if "vocab" in s0.e2e else None
     h2d = xh.numel() * 2 + (ah.numel() * 2 if ah is not None else 0) + (idh.numel() * 4 if idh is not None else 0)
+    copy_x = "attn_core" not in s0.e2e  # the attention core takes q, k, v instead of x
+    if "attn_core" in s0.e2e:
+        qkvh = [torch.from_numpy(np.ascontiguousarray(data[key]).view(np.int16)).view(torch.bfloat16).pin_memory()
+                for key in ("q", "k", "v")]
+        h2d = sum(t.numel() * 2 for t in qkvh)
     if "moe" in s0.e2e:
         rih = torch.from_numpy(data["topk_ids"]).pin_memory()
         rwh = torch.from_numpy(data["topk_w"]).pin_memory()
@@ -594,6 +626,10 @@ def run_native(args):
         outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())
         d2h += T * D * 4
         ws = torch.empty(tp.tp_mlp_block_workspace_size(plan0, T), dtype=torch.uint8, device=dev)
+    if "attn_core" in s0.e2e:
+        ao = s0.e2e["attn_core"][1]
+        outs_h.append(torch.empty(tuple(ao.shape), dtype=torch.bfloat16).pin_memory())  # every rank's A
+        d2h += ao.numel() * 2
     if "moe" in s0.e2e:
         outs_h.append(torch.empty((T, D), dtype=torch.float32).pin_memory())  # the layer output
         d2h += T * D * 4
@@ -621,6 +657,10 @@ def run_native(args):
         if "mlp" in s0.e2e:
             sl["ym"] = s0.e2e["mlp"][3] if first else [torch.empty_like(t) for t in s0.e2e["mlp"][3]]
             sl["ws"] = ws if first else torch.empty_like(ws)
+        if "attn_core" in s0.e2e:
+            sl["qkv"] = [s0.aq, s0.ak, s0.av] if first else [torch.empty_like(t) for t in (s0.aq, s0.ak, s0.av)]
+            ao = s0.e2e["attn_core"][1]
+            sl["aout"] = ao if first else torch.empty_like(ao)
         if "moe" in s0.e2e:
             sl["rid"] = s0.rid if first else torch.empty_like(s0.rid)
             sl["rw"] = s0.rw if first else torch.empty_like(s0.rw)
@@ -660,6 +700,8 @@ def run_native(args):
             sl["calls"] += [c for (_nm, c) in s0.e2e["vocab"][0](sl["ids"], sl["x"], *sl["vo"])]
         if "moe" in s0.e2e:
             sl["calls"] += [c for (_nm, c) in s0.e2e["moe"][0](sl["x"], sl["rid"], sl["rw"], sl["ymoe"])]
+        if "attn_core" in s0.e2e:
+            sl["calls"] += [c for (_nm, c) in s0.e2e["attn_core"][0](*sl["qkv"], sl["aout"])]
 
     def compute(sl):
         for call in sl["calls"]:
@@ -669,11 +711,13 @@ def run_native(args):
         return (([sl["yo"][0]] if "attn" in s0.e2e else []) + ([sl["ym"][0]] if "mlp" in s0.e2e else []) +
                 (list(sl["ys"]) if "rs_column" in s0.e2e else []) +
                 (list(sl["vo"]) if "vocab" in s0.e2e else []) +
-                ([sl["ymoe"][0]] if "moe" in s0.e2e else []))
+                ([sl["ymoe"][0]] if "moe" in s0.e2e else []) +
+                ([sl["aout"]] if "attn_core" in s0.e2e else []))
 
     def serial_step():
         sl = slots[0]
-        sl["x"].copy_(xh, non_blocking=True)
+        if copy_x:
+            sl["x"].copy_(xh, non_blocking=True)
         if "a" in sl:
             sl["a"].copy_(ah, non_blocking=True)
         if "ids" in sl:
@@ -681,6 +725,9 @@ def run_native(args):
         if "rid" in sl:
             sl["rid"].copy_(rih, non_blocking=True)
             sl["rw"].copy_(rwh, non_blocking=True)
+        if "qkv" in sl:
+            for dbuf, hbuf in zip(sl["qkv"], qkvh):
+                dbuf.copy_(hbuf, non_blocking=True)
         compute(sl)
         for hbuf, dbuf in zip(sl["outs_h"], results(sl)):
             hbuf.copy_(dbuf, non_blocking=True)
@@ -696,7 +743,8 @@ def run_native(args):
         if i >= 2:
             h2d_s.wait_event(ev_done[b])  # step i-2 has finished reading this slot's inputs
         with torch.cuda.stream(h2d_s):
-            sl["x"].copy_(xh, non_blocking=True)
+            if copy_x:
+                sl["x"].copy_(xh, non_blocking=True)
             if "a" in sl:
                 sl["a"].copy_(ah, non_blocking=True)
             if "ids" in sl:
@@ -704,6 +752,9 @@ def run_native(args):
             if "rid" in sl:
                 sl["rid"].copy_(rih, non_blocking=True)
                 sl["rw"].copy_(rwh, non_blocking=True)
+            if "qkv" in sl:
+                for dbuf, hbuf in zip(sl["qkv"], qkvh):
+                    dbuf.copy_(hbuf, non_blocking=True)
             ev_in[b].record(h2d_s)
         stream.wait_event(ev_in[b])
         if i >= 2:
@@ -828,7 +879,7 @@ def run_reference(args):
 
 DEFAULT_STEPS = {"mlp_tp2_t512": 10000, "attn_gqa_tp4_t2048": 3000, "decode_gqa_rep_tp8_t64": 6000,
                  "prefill_layer_tp8_t4096": 200, "rs_column_tp8_t4096": 600, "vocab_tp8_t4096": 200,
-                 "moe_mixtral_tp8_t4096": 400}
+                 "moe_mixtral_tp8_t4096": 400, "attn_core_tp8_t4096": 1000}
 
 
 def main():

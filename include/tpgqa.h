@@ -302,6 +302,34 @@ tp_status tp_vocab_lm_head(int32_t tp_size, const tp_tensor *x, const tp_tensor 
                            tp_tensor *logits, int32_t gather, tp_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Attention core between q/k/v and o_proj (mlxcel manual, GQA 인식 어텐션 샤딩 /
+ * GQA-aware attention sharding: each rank's q heads attend with the kv heads
+ * the plan gives it, its own when K/V are sharded, all of them when replicated).
+ * ------------------------------------------------------------------------- */
+
+/* Workspace bytes tp_attn_core needs for `tokens` tokens (the transposed V of
+ * every kv source, bf16). 0 for a null plan or negative tokens. */
+size_t tp_attn_core_workspace_size(const tp_plan *plan, int64_t tokens);
+
+/* A_r = per local q head h of rank r: softmax(Q_h K_g^T / sqrt(d)) V_g with g
+ * the plan's q->kv map (tp_plan_q_to_kv), query i seeing keys j <= i when
+ * causal = 1, every key when causal = 0. No position encoding is applied.
+ * S and the running output are f32 (tensor cores, TMEM); P is rounded to bf16
+ * for the P V product; A is written as bf16.
+ *  q[r]  : [T x Hq_r*d] bf16 (tp_qkv_proj's q output of rank r).
+ *  k[r], v[r] : [T x Hkv_r*d] bf16; one shared entry (k[0], v[0], all kv heads)
+ *          when the plan replicates K/V, else one per rank.
+ *  a[r]  : [T x Hq_r*d] bf16 output, rank r's slice of the o_proj input.
+ *  workspace : at least tp_attn_core_workspace_size bytes, 16-byte aligned.
+ * d must be 128 and tp_size at most 32, with at most 256 q heads in all,
+ * else TP_ERR_UNSUPPORTED.
+ * Errors: TP_ERR_INVALID_ARG, TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_WORKSPACE,
+ * TP_ERR_UNSUPPORTED, TP_ERR_RANK_FAILED, TP_ERR_CUDA. */
+tp_status tp_attn_core(const tp_plan *plan, const tp_tensor *q, const tp_tensor *k, const tp_tensor *v,
+                       tp_tensor *a, int32_t causal, void *workspace, size_t workspace_bytes,
+                       tp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Mixture of experts (mlxcel manual, MoE 전문가 병렬화 / MoE expert parallelism:
  * Expert Parallel puts expert i whole on rank i % tp_size, with no
  * communication inside an expert; Within-Expert Parallel shards every expert's

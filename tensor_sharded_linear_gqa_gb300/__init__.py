@@ -95,6 +95,9 @@ _SIGS = {
     "tp_vocab_embedding": ([ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, _T, _T, ctypes.c_int32, _S],
                            ctypes.c_int),
     "tp_vocab_lm_head": ([ctypes.c_int32, _T, _T, _T, ctypes.c_int32, _S], ctypes.c_int),
+    "tp_attn_core_workspace_size": ([ctypes.c_void_p, ctypes.c_int64], ctypes.c_size_t),
+    "tp_attn_core": ([ctypes.c_void_p, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, _S],
+                     ctypes.c_int),
     "tp_moe_workspace_size": ([_P(TpMoeDims), ctypes.c_int64], ctypes.c_size_t),
     "tp_moe_block": ([_P(TpMoeDims), _T, ctypes.c_void_p, ctypes.c_void_p, _T, _T, _T, _T, ctypes.c_int32,
                       ctypes.c_void_p, ctypes.c_size_t, _S], ctypes.c_int),
@@ -309,6 +312,17 @@ def tp_vocab_lm_head(tp_size: int, x, w, logits, gather: bool, stream=None) -> N
     xs = tensor(x)
     _check(_lib.tp_vocab_lm_head(tp_size, ctypes.byref(xs), _arr(w), _arr(logits), int(gather),
                                  _stream(stream)), "tp_vocab_lm_head")
+
+
+def tp_attn_core_workspace_size(plan: Plan, tokens: int) -> int:
+    return int(_lib.tp_attn_core_workspace_size(plan.handle, tokens))
+
+
+def tp_attn_core(plan: Plan, q, k, v, a, causal: bool, workspace, stream=None) -> None:
+    """q[r], a[r]: rank r's [T x Hq_r*d] bf16; k, v: one entry per rank, or one
+    shared entry when the plan replicates K/V; workspace: a CUDA byte tensor."""
+    _check(_lib.tp_attn_core(plan.handle, _arr(q), _arr(k), _arr(v), _arr(a), int(causal),
+                             workspace.data_ptr(), workspace.numel(), _stream(stream)), "tp_attn_core")
 
 
 def moe_dims(tp_size: int, mode: int, num_experts: int, top_k: int, hidden: int, ffn: int) -> TpMoeDims:

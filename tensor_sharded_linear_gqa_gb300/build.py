@@ -27,7 +27,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtpgqa.so")
 STAMP = os.path.join(BUILD, "stamp.json")
 
-SOURCES = ["plan.cpp", "tp_api.cu", "gemm_tcgen05.cu", "gemm_f32.cu", "combine.cu", "mlp_static.cu", "vocab.cu", "moe.cu"]
+SOURCES = ["plan.cpp", "tp_api.cu", "gemm_tcgen05.cu", "gemm_f32.cu", "combine.cu", "mlp_static.cu", "vocab.cu", "moe.cu", "attention.cu"]
 HEADERS = ["tp_internal.h", "sm100_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -2,6 +2,7 @@
 // Every entry point validates everything before it enqueues anything; on an
 // error nothing is launched. No entry point allocates device memory.
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -644,6 +645,108 @@ extern "C" tp_status tp_vocab_lm_head(int32_t n, const tp_tensor *x, const tp_te
   for (int32_t r = 1; r < n; ++r)
     if (w[r].rows != w[0].rows) return TP_ERR_INVALID_ARG;  // slices of V/N ids each
   return tp_column_linear(n, x, w, logits, gather, stream);
+}
+
+namespace {
+
+size_t attn_vt_bytes(long long cols, long long tokens) {
+  const long long tp8 = (tokens + 7) / 8 * 8;  // V^T row pitch: 16-byte multiple
+  return static_cast<size_t>((cols * tp8 * 2 + 255) / 256 * 256);
+}
+
+}  // namespace
+
+extern "C" size_t tp_attn_core_workspace_size(const tp_plan *plan, int64_t tokens) {
+  tp_dims d;
+  tp_rank_shard s0;
+  if (!plan || tokens < 0 || tp_plan_dims(plan, &d) != TP_OK || tp_plan_query_rank(plan, 0, &s0) != TP_OK)
+    return 0;
+  const int nkv = s0.kv_replicated ? 1 : d.tp_size;
+  return nkv * attn_vt_bytes((s0.kv_head_end - s0.kv_head_begin) * static_cast<long long>(d.head_dim), tokens);
+}
+
+extern "C" tp_status tp_attn_core(const tp_plan *plan, const tp_tensor *q, const tp_tensor *k, const tp_tensor *v,
+                                  tp_tensor *a, int32_t causal, void *workspace, size_t workspace_bytes,
+                                  tp_stream_t stream) {
+  tp_dims d;
+  if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
+  if (!q || !k || !v || !a || (causal != 0 && causal != 1)) return TP_ERR_INVALID_ARG;
+  const int32_t n = d.tp_size;
+  const long long hd = d.head_dim;
+  if (hd != 128 || n > kMaxAttnRanks) return TP_ERR_UNSUPPORTED;
+  std::vector<tp_rank_shard> sh(n);
+  for (int32_t r = 0; r < n; ++r)
+    if (tp_plan_query_rank(plan, r, &sh[r]) != TP_OK) return TP_ERR_INVALID_ARG;
+  const bool rep = sh[0].kv_replicated != 0;
+  const int32_t nkv = rep ? 1 : n;
+  const long long T = q[0].rows;
+  auto check = [&](const tp_tensor &t, long long cols) -> tp_status {
+    if (!shape_ok(t)) return TP_ERR_INVALID_ARG;
+    if (t.dtype != TP_BF16) return TP_ERR_DTYPE;
+    if (t.rows != T || t.cols != cols) return TP_ERR_INVALID_ARG;
+    if (T > 0 && !pitch_ok(t)) return TP_ERR_ALIGNMENT;
+    return TP_OK;
+  };
+  tp_status st;
+  int total_heads = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    const long long qc = (sh[r].q_head_end - sh[r].q_head_begin) * hd;
+    if ((st = check(q[r], qc)) != TP_OK) return st;
+    if ((st = check(a[r], qc)) != TP_OK) return st;
+    total_heads += sh[r].q_head_end - sh[r].q_head_begin;
+  }
+  const long long kvc = (sh[0].kv_head_end - sh[0].kv_head_begin) * hd;
+  for (int32_t r = 0; r < nkv; ++r) {
+    if ((st = check(k[r], kvc)) != TP_OK) return st;
+    if ((st = check(v[r], kvc)) != TP_OK) return st;
+  }
+  if (total_heads > kMaxAttnHeads || T > 0x7fffffffLL - 256) return TP_ERR_UNSUPPORTED;
+  const size_t vt = attn_vt_bytes(kvc, T);
+  if (T > 0) {
+    if (!workspace || workspace_bytes < nkv * vt) return TP_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return TP_ERR_ALIGNMENT;
+  }
+  if ((st = check_health(n)) != TP_OK) return st;
+  if (T == 0 || total_heads == 0) return TP_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long tp8 = (T + 7) / 8 * 8;
+  // V -> V^T per kv source, so that P V reads K-major tiles
+  for (int32_t r = 0; r < nkv; ++r)
+    if ((st = launch_transpose_bf16(v[r].ptr, v[r].ld, static_cast<char *>(workspace) + r * vt, tp8,
+                                    static_cast<int>(T), static_cast<int>(kvc), s)) != TP_OK)
+      return st;
+  static thread_local AttnParams prm;  // ~22 KB: kept off the stack
+  std::memset(&prm, 0, sizeof(prm));
+  for (int32_t r = 0; r < n; ++r)
+    if (!encode_bf16_map_2d(&prm.maps[r], q[r].ptr, T, q[r].cols, q[r].ld, 128)) return TP_ERR_INVALID_ARG;
+  for (int32_t r = 0; r < nkv; ++r) {
+    if (!encode_bf16_map_2d(&prm.maps[n + r], k[r].ptr, T, kvc, k[r].ld, 128)) return TP_ERR_INVALID_ARG;
+    if (!encode_bf16_map_2d(&prm.maps[n + nkv + r], static_cast<char *>(workspace) + r * vt, kvc, T, tp8, 128))
+      return TP_ERR_INVALID_ARG;
+  }
+  int h = 0;
+  std::vector<int32_t> q2kv;
+  for (int32_t r = 0; r < n; ++r) {
+    const int nq = sh[r].q_head_end - sh[r].q_head_begin;
+    q2kv.assign(nq, 0);
+    if (nq > 0 && tp_plan_q_to_kv(plan, r, q2kv.data(), nq) != TP_OK) return TP_ERR_INVALID_ARG;
+    const int src = rep ? 0 : r;
+    for (int j = 0; j < nq; ++j, ++h) {
+      AttnHead &e = prm.heads[h];
+      e.q_map = r;
+      e.k_map = n + src;
+      e.v_map = n + nkv + src;
+      e.q_col = static_cast<int>(j * hd);
+      e.kv_col = static_cast<int>(q2kv[j] * hd);
+      e.out = byte_ptr(a[r].ptr, j * hd, TP_BF16);
+      e.out_ld = a[r].ld;
+    }
+  }
+  prm.tokens = static_cast<int>(T);
+  prm.q_tiles = static_cast<int>((T + 127) / 128);
+  prm.causal = causal;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(hd)));
+  return launch_attention(prm, total_heads, s);
 }
 
 namespace {

@@ -262,6 +262,38 @@ struct EmbedArgs {
 // vec16: every base, pitch and the row length are multiples of 16 bytes.
 tp_status launch_vocab_embed(const EmbedArgs &a, bool vec16, cudaStream_t s);
 
+// Tensor map of a bf16 [rows x cols] matrix with row pitch ld (elements):
+// boxes of 64 columns x box_rows rows, 128-byte swizzle, zero fill out of range.
+bool encode_bf16_map_2d(CUtensorMap *map, const void *base, long long rows, long long cols, long long ld,
+                        int box_rows);
+
+// ---------------------------------------------------------------------------
+// Attention core (attention.cu): one CTA per (128-query tile, q head).
+// ---------------------------------------------------------------------------
+constexpr int kMaxAttnRanks = 32;
+constexpr int kMaxAttnMaps = 3 * kMaxAttnRanks;
+constexpr int kMaxAttnHeads = 256;
+struct AttnHead {
+  int q_map, k_map, v_map;  // map indices: Q of the rank, K and V^T of its kv source
+  int q_col;                // first column of this q head in Q (= local head * d)
+  int kv_col;               // first column of its kv head in K (= first row in V^T)
+  int pad;
+  void *out;                // bf16 A_r + q_col: this head's output columns
+  long long out_ld;
+};
+struct AttnParams {
+  CUtensorMap maps[kMaxAttnMaps];
+  AttnHead heads[kMaxAttnHeads];
+  int tokens, q_tiles, causal, pad;
+  float scale_log2;         // log2(e) / sqrt(d)
+  int *status;
+  long long wait_ns;
+};
+tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s);
+// V [rows x cols] (pitch ld_in) -> V^T [cols x rows] (pitch ld_out), bf16.
+tp_status launch_transpose_bf16(const void *in, long long ld_in, void *out, long long ld_out, int rows, int cols,
+                                cudaStream_t s);
+
 // ---------------------------------------------------------------------------
 // Mixture-of-experts block (moe.cu).
 // ---------------------------------------------------------------------------

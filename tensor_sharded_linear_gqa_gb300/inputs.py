@@ -30,6 +30,7 @@ STREAM = {
     "wlm": 15,   # LM-head weight [V x D]
     "route": 16,  # MoE routing: expert ids and weights per token
     "eg": 17, "eu": 18, "ed": 19,  # MoE expert weights [E x F x D], [E x F x D], [E x D x F]
+    "aq": 20, "ak": 21, "av": 22,  # attention core inputs Q [T x Hq*d], K and V [T x Hkv*d]
 }
 
 # Workloads, named by what they are. Weight tensors are stored [out x in]
@@ -72,6 +73,11 @@ WORKLOADS = {
     # Mixtral-8x7B-shaped MoE layer: 8 experts of hidden 4096 and FFN 14336, top-2
     # routing drawn uniformly (two distinct experts a token, softmax weights over
     # the two), 4096 tokens, TP=8; within-expert sharding (F/N = 1792 per rank).
+    # Attention core of the prefill layer: causal attention of 4096 tokens,
+    # 64 q heads and 8 kv heads of 128 over 8 ranks (8 q heads and 1 kv head
+    # each); Q, K, V drawn N(0,1).
+    "attn_core_tp8_t4096": dict(kind="attn_core", T=4096, hidden=8192, q_heads=64, kv_heads=8,
+                                head_dim=128, tp=8, seed=109),
     "moe_mixtral_tp8_t4096": dict(kind="moe", T=4096, hidden=4096, ffn=14336, experts=8, top_k=2,
                                   tp=8, seed=108, w_std=0.02),
 }
@@ -202,6 +208,11 @@ def make_bf16_inputs(w: dict, rows: int | None = None) -> dict:
         out["ids"] = token_ids(seed, STREAM["ids"], T, w["vocab"])
     if w["kind"] == "moe":
         out["topk_ids"], out["topk_w"] = routing(seed, STREAM["route"], T, w["experts"], w["top_k"])
+    if w["kind"] == "attn_core":
+        hd = w["head_dim"]
+        out["q"] = normal_bf16(seed, STREAM["aq"], (T, w["q_heads"] * hd))
+        out["k"] = normal_bf16(seed, STREAM["ak"], (T, w["kv_heads"] * hd))
+        out["v"] = normal_bf16(seed, STREAM["av"], (T, w["kv_heads"] * hd))
     if w["kind"] in ("attn", "layer"):
         out["a"] = normal_bf16(seed, STREAM["a"], (T, w["q_heads"] * w["head_dim"]))
     for name, shp in weight_shapes(w).items():

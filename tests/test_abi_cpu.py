@@ -294,6 +294,32 @@ def test_moe_rejects_bad_arguments():
         tp.tp_set_rank_health(1, True)
 
 
+def test_attn_core_rejects_bad_arguments():
+    plan = tp.tp_plan_create(2, 256, 8, 2, 128, 16)   # 4 q heads and 1 kv head per rank
+    Tt = 64
+    q = [T(FAKE, BF, Tt, 512), T(FAKE + 65536, BF, Tt, 512)]
+    kv = [T(FAKE, BF, Tt, 128), T(FAKE + 65536, BF, Tt, 128)]
+    need = tp.tp_attn_core_workspace_size(plan, Tt)
+    assert need == 2 * 128 * 64 * 2
+
+    def st(q_=q, k_=kv, v_=kv, a_=q, causal=1, ws=FAKE, wsb=need, pl=plan):
+        return tp.raw_status("tp_attn_core", pl.handle, arr(*q_), arr(*k_), arr(*v_), arr(*a_), causal, ws, wsb,
+                             None)
+    assert st(causal=2) == tp.TP_ERR_INVALID_ARG
+    assert st(q_=[q[0], T(FAKE, BF, Tt, 384)]) == tp.TP_ERR_INVALID_ARG        # rank 1 holds 4 heads
+    assert st(k_=[kv[0], T(FAKE, F32, Tt, 128)]) == tp.TP_ERR_DTYPE
+    assert st(a_=[q[0], T(FAKE + 2, BF, Tt, 512)]) == tp.TP_ERR_ALIGNMENT
+    assert st(wsb=need - 1) == tp.TP_ERR_WORKSPACE
+    assert st(ws=FAKE + 8) == tp.TP_ERR_ALIGNMENT
+    p64 = tp.tp_plan_create(2, 256, 8, 2, 64, 16)                     # head_dim 64 is not built
+    assert st(pl=p64) == tp.TP_ERR_UNSUPPORTED
+    tp.tp_set_rank_health(1, False)
+    try:
+        assert st() == tp.TP_ERR_RANK_FAILED
+    finally:
+        tp.tp_set_rank_health(1, True)
+
+
 def test_failed_rank_stops_the_group_before_any_launch():
     # Host-side fault injection: rank 1 reports unhealthy; every call that involves
     # it returns TP_ERR_RANK_FAILED before enqueuing work (no GPU needed).
