@@ -7,15 +7,19 @@
 //
 // k_attention: one CTA per (128-query tile, q head); causal grids run the
 // longest query tiles first. Warp roles:
-//   warp 0     TMA producer: the Q tile once, then K and V^T tiles of 128 keys
-//              through a 2-stage ring (V is transposed beforehand, so every MMA
-//              operand is a K-major, 128-byte-swizzled tile);
+//   warp 0     TMA producers: lane 0 loads the Q tile once and K tiles of 128
+//              keys through a 2-stage ring, lane 1 V^T tiles through another (V
+//              is transposed beforehand, so every MMA operand is a K-major,
+//              128-byte-swizzled tile). A K stage frees when its S = Q K^T is
+//              done, two blocks before the V stage beside it;
 //   warp 1     MMA issuer: S_j = Q K_j^T (M=128, N=128 keys, K=128) into one of
 //              two TMEM buffers, then O += P_j V_j (N=128, K=128 keys) into a
 //              third that accumulates over the key blocks; S_{j+1} is issued
 //              before P_j V_j so it overlaps the softmax;
-//   warps 2-5  softmax: one thread per query row (TMEM lane). Pass 1 takes the
-//              row maximum of S_j; the row's reference maximum m moves only when
+//   warps 2-9  softmax: two threads per query row (TMEM lane), warps w and w+4
+//              taking keys and output columns [0, 64) and [64, 128). They take the
+//              row maximum of S_j and combine it through shared memory (a named
+//              barrier per warp pair); the row's reference maximum m moves only when
 //              the block's maximum exceeds it by more than 8 (in log2 units),
 //              and then the row of O is rescaled in TMEM by 2^(m_old - m_new)
 //              after the previous P V has landed; so p = exp2(s*c - m) <= 2^8.
@@ -35,16 +39,25 @@
 namespace tpgqa {
 namespace {
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 320;  // producer warp, MMA warp, 8 softmax warps
 constexpr int kTileQ = 128, kTileK = 128, kHd = 128;
 constexpr uint32_t kSub = 128u * 128u;            // one [128 rows x 64 bf16] swizzled k-tile
 constexpr uint32_t kTile = 2 * kSub;              // a [128 x 128] bf16 operand tile
-constexpr uint32_t kSmemQ = 0, kSmemK = kTile, kSmemV = 3 * kTile, kSmemP = 5 * kTile;
-constexpr uint32_t kSmemBar = 6 * kTile;          // barriers after the six tiles
-constexpr size_t kAttnSmem = 6 * kTile + 1024 + 256;  // + alignment slack + barriers
+constexpr uint32_t kSmemQ = 0, kSmemK = kTile, kSmemV = 3 * kTile, kSmemP = 5 * kTile;  // P: 2 tiles
+constexpr uint32_t kSmemBar = 7 * kTile;          // barriers after the seven tiles (160 bytes)
+constexpr uint32_t kSmemRed = kSmemBar + 160;      // row-maximum / row-sum exchange, [2][128] f32
+constexpr size_t kAttnSmem = kSmemRed + 1024 + 1024;  // + the exchange + alignment slack (226.1 KB)
 constexpr uint32_t kTmemCols = 512;               // S0, S1, O at columns 0, 128, 256
 
 __device__ __forceinline__ void record(int *status, int code) { atomicCAS(status, 0, code); }
+
+// 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32):
+// relative error of order 2^-22, far below the bf16 rounding P goes through next.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 tp_status launch_checked(cudaError_t e) {
   if (e != cudaSuccess) return cuda_fail(e);
@@ -60,10 +73,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
   const uint32_t sQ = sbase + kSmemQ, sK0 = sbase + kSmemK, sV0 = sbase + kSmemV, sP = sbase + kSmemP;
   uint8_t *bar_area = smem + kSmemBar;
   const uint32_t bar0 = ptx::smem_addr(bar_area);
-  const uint32_t q_full = bar0, kv_full0 = bar0 + 8, kv_empty0 = bar0 + 24, s_full0 = bar0 + 40,
-                 p_full = bar0 + 56, o_full = bar0 + 64, drain = bar0 + 72;
-  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 96);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 100);
+  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40,
+                 v_empty0 = bar0 + 56, s_full0 = bar0 + 72, p_full = bar0 + 88, p_empty0 = bar0 + 96,
+                 drain = bar0 + 112;
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 120);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 124);
+  const uint32_t xbar0 = bar0 + 128;  // one exchange barrier per softmax warp pair
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // work item: causal grids start with the last (longest) query tiles
@@ -76,13 +91,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(kv_full0 + 8 * s, 1);
-      ptx::mbar_init(kv_empty0 + 8 * s, 1);
+      ptx::mbar_init(k_full0 + 8 * s, 1);
+      ptx::mbar_init(k_empty0 + 8 * s, 1);
+      ptx::mbar_init(v_full0 + 8 * s, 1);
+      ptx::mbar_init(v_empty0 + 8 * s, 1);
       ptx::mbar_init(s_full0 + 8 * s, 1);
     }
-    ptx::mbar_init(p_full, 128);
-    ptx::mbar_init(o_full, 1);
+    ptx::mbar_init(p_full, 256);
+    ptx::mbar_init(p_empty0, 1);
+    ptx::mbar_init(p_empty0 + 8, 1);
     ptx::mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) ptx::mbar_init(xbar0 + 8 * q, 64);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -102,29 +121,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
-  int issued[2] = {0, 0};  // loads started per KV stage (producer thread)
+  int issued[2] = {0, 0};  // loads started per stage of this producer lane's ring
   bool q_issued = false;
   if (warp == 0) {
-    if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(q_full, kTile);
-      for (int c = 0; c < 2; ++c)
-        ptx::tma_load_2d(sQ + c * kSub, &p.maps[hd.q_map], hd.q_col + c * 64, q0, q_full);
-      q_issued = true;
+    if (lane < 2) {
+      // lane 0: Q, then the K ring; lane 1: the V^T ring
+      const uint32_t full0 = lane == 0 ? k_full0 : v_full0, empty0 = lane == 0 ? k_empty0 : v_empty0;
+      const uint32_t dst0 = lane == 0 ? sK0 : sV0;
+      const CUtensorMap *map = &p.maps[lane == 0 ? hd.k_map : hd.v_map];
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(q_full, kTile);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_2d(sQ + c * kSub, &p.maps[hd.q_map], hd.q_col + c * 64, q0, q_full);
+        q_issued = true;
+      }
       for (int j = 0; j < nb; ++j) {
         const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
         if (*abort_flag) break;
-        if (!ptx::mbar_wait(kv_empty0 + 8 * s, ph ^ 1, p.wait_ns)) {
+        if (!ptx::mbar_wait(empty0 + 8 * s, ((j >> 1) & 1) ^ 1, p.wait_ns)) {
           record(p.status, kDevTimeoutProducer);
           *abort_flag = 1;
           break;
         }
-        ptx::mbar_arrive_expect_tx(kv_full0 + 8 * s, 2 * kTile);
+        ptx::mbar_arrive_expect_tx(full0 + 8 * s, kTile);
         for (int c = 0; c < 2; ++c) {
-          ptx::tma_load_2d(sK0 + s * kTile + c * kSub, &p.maps[hd.k_map], hd.kv_col + c * 64, j * kTileK,
-                           kv_full0 + 8 * s);
-          ptx::tma_load_2d(sV0 + s * kTile + c * kSub, &p.maps[hd.v_map], j * kTileK + c * 64, hd.kv_col,
-                           kv_full0 + 8 * s);
+          if (lane == 0)
+            ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, hd.kv_col + c * 64, j * kTileK, full0 + 8 * s);
+          else
+            ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, j * kTileK + c * 64, hd.kv_col, full0 + 8 * s);
         }
         ++issued[s];
       }
@@ -136,7 +160,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
       if (!ok) record(p.status, kDevTimeoutMma);
       auto issue_s = [&](int j) -> bool {
         const int s = j & 1;
-        if (*abort_flag || !ptx::mbar_wait(kv_full0 + 8 * s, (j >> 1) & 1, p.wait_ns)) {
+        if (*abort_flag || !ptx::mbar_wait(k_full0 + 8 * s, (j >> 1) & 1, p.wait_ns)) {
           if (!*abort_flag) record(p.status, kDevTimeoutMma);
           return false;
         }
@@ -149,13 +173,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
           ptx::mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(s_full0 + 8 * s);
+        ptx::mma_commit(k_empty0 + 8 * s);
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < nb; ++j) {
         if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
         // O += P_j V_j once the softmax has written P_j (and rescaled O if needed)
-        if (*abort_flag || !ptx::mbar_wait(p_full, j & 1, p.wait_ns)) {
+        if (*abort_flag || !ptx::mbar_wait(p_full, j & 1, p.wait_ns) ||
+            !ptx::mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, p.wait_ns)) {
           if (!*abort_flag) record(p.status, kDevTimeoutMma);
           ok = false;
           break;
@@ -165,29 +191,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
         const uint32_t d = tmem + 256u;
 #pragma unroll
         for (int kk = 0; kk < kTileK / 16; ++kk) {
-          const uint64_t ad = ptx::smem_desc_sw128(sP + (kk >> 2) * kSub) + 2 * (kk & 3);
+          const uint64_t ad = ptx::smem_desc_sw128(sP + s * kTile + (kk >> 2) * kSub) + 2 * (kk & 3);
           const uint64_t bd = ptx::smem_desc_sw128(sV0 + s * kTile + (kk >> 2) * kSub) + 2 * (kk & 3);
           ptx::mma_bf16(d, ad, bd, idesc, (j | kk) > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(o_full);
-        ptx::mma_commit(kv_empty0 + 8 * s);
+        ptx::mma_commit(p_empty0 + 8 * s);  // P_j read, O current up to block j
+        ptx::mma_commit(v_empty0 + 8 * s);
       }
       if (!ok) *abort_flag = 1;
       ptx::mma_commit(drain);
       if (!ptx::mbar_wait(drain, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
     }
   } else {
-    // ---- softmax: warp w reads TMEM lanes [32*(w%4), +32); one query row per thread ----
+    // ---- softmax: warps w and w+4 read TMEM lanes [32*(w%4), +32); a thread pair per row ----
     const int qw = warp & 3;
+    const int half = (warp - 2) >> 2;  // 0: keys / output columns [0, 64), 1: [64, 128)
     const int row = qw * 32 + lane;
     const int qrow = q0 + row;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    const uint32_t ob = tmem + lane_off + 256u;
+    const uint32_t ob = tmem + lane_off + 256u + 64u * half;
+    const uint32_t xbar = xbar0 + 8 * qw;  // the two warps sharing these rows
+    volatile float *red = reinterpret_cast<volatile float *>(smem + kSmemRed);
+    // The partner's value of this row through shared memory. Each exchange takes
+    // two phases of the pair's barrier: both values written, then both read (so
+    // the next exchange cannot overwrite a value not yet read). Bounded waits.
+    auto exchange = [&](float x, float &y) -> bool {
+      red[half * 128 + row] = x;
+      ptx::mbar_arrive(xbar);
+      bool ready = ptx::mbar_wait(xbar, 0, p.wait_ns);
+      y = red[(half ^ 1) * 128 + row];
+      ptx::mbar_arrive(xbar);
+      ready = ptx::mbar_wait(xbar, 1, p.wait_ns) && ready;
+      if (!__all_sync(0xffffffffu, ready && *abort_flag == 0)) {
+        if (lane == 0) {
+          if (!ready) record(p.status, kDevTimeoutEpilogue);
+          *abort_flag = 1;
+        }
+        return false;
+      }
+      return true;
+    };
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    // waits for O += P_{j} V_{j} to land (the P tile is free again, O is current)
-    auto wait_o = [&](int j) -> bool {
-      const bool ready = ptx::mbar_wait(o_full, j & 1, p.wait_ns);
+    // waits for O += P_i V_i to land: P tile i % 2 is free again and O is current
+    // up to block i (tcgen05 operations complete in issue order)
+    auto wait_pv = [&](int i) -> bool {
+      const bool ready = ptx::mbar_wait(p_empty0 + 8 * (i & 1), (i >> 1) & 1, p.wait_ns);
       if (!__all_sync(0xffffffffu, ready && *abort_flag == 0)) {
         if (lane == 0) {
           if (!ready) record(p.status, kDevTimeoutEpilogue);
@@ -198,6 +247,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
       ptx::tc_fence_after();
       return true;
     };
+    const int c0 = 64 * half;  // first key of this thread's half
     for (int j = 0; j < nb; ++j) {
       const int s = j & 1;
       const bool ready = ptx::mbar_wait(s_full0 + 8 * s, (j >> 1) & 1, p.wait_ns);
@@ -210,67 +260,72 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(s * 128);
+      const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(s * 128 + c0);
       const int k0 = j * kTileK;
       // keys past the query (causal) or past the sequence are masked
-      const int lim = min(p.causal ? qrow - k0 + 1 : kTileK, p.tokens - k0);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32cols(sb + c * 32, v);
+      const int lim = min(p.causal ? qrow - k0 + 1 : kTileK, p.tokens - k0) - c0;
+      uint32_t v[64];
+      {
+        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        ptx::tmem_ld_32cols(sb, v0);
+        ptx::tmem_ld_32cols(sb + 32, v1);
         ptx::tmem_ld_wait();
         ptx::tmem_regs_ready(v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (c * 32 + i < lim) mx = fmaxf(mx, __uint_as_float(v[i]));
       }
+      const bool full = __all_sync(0xffffffffu, lim >= 64);  // no masked key in this warp's half
+      if (!full) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i >= lim) v[i] = __float_as_uint(-INFINITY);
+      }
+      float mx = __uint_as_float(v[0]);
+#pragma unroll
+      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+      float mx2;
+      if (!exchange(mx, mx2)) { ok = false; break; }
+      mx = fmaxf(mx, mx2);
       const float m_blk = mx * p.scale_log2;
       const bool move = m_blk > m + 8.f;  // always on the first block (m = -inf)
       const float m_new = move ? m_blk : m;
       const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
-      if (j > 0) {
-        if (!wait_o(j - 1)) { ok = false; break; }
-        if (__any_sync(0xffffffffu, move)) {
-          // rescale this warp's rows of O (lanes that keep their maximum scale by 1)
+      bool pv1_done = false;
+      if (j > 0 && __any_sync(0xffffffffu, move)) {
+        if (!wait_pv(j - 1)) { ok = false; break; }
+        pv1_done = true;
+        // rescale this thread's half of the row of O (rows keeping their maximum scale by 1)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            ptx::tmem_ld_32cols(ob + c * 32, v);
-            ptx::tmem_ld_wait();
-            ptx::tmem_regs_ready(v);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld_32cols(ob + c * 32, o);
+          ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            ptx::tmem_st_32cols(ob + c * 32, v);
-          }
-          ptx::tmem_st_wait();
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          ptx::tmem_st_32cols(ob + c * 32, o);
         }
+        ptx::tmem_st_wait();
       }
+      // P tile s was last read by P_{j-2} V_{j-2}
+      if (j >= 2 && !pv1_done && !wait_pv(j - 2)) { ok = false; break; }
       float lsum = 0.f;
+      // k-tile `half` of the P tile holds this thread's 64 keys
+      const uint32_t pbase = sP + s * kTile + half * kSub + row * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld_32cols(sb + c * 32, v);
-        ptx::tmem_ld_wait();
-        ptx::tmem_regs_ready(v);
-        uint32_t packed[16];
+      for (int g = 0; g < 8; ++g) {  // keys [8g, 8g+8) of the half: one 16-byte chunk
+        uint32_t packed[4];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float a0 = c * 32 + i < lim ? exp2f(__uint_as_float(v[i]) * p.scale_log2 - m_new) : 0.f;
-          const float a1 = c * 32 + i + 1 < lim ? exp2f(__uint_as_float(v[i + 1]) * p.scale_log2 - m_new) : 0.f;
+        for (int i = 0; i < 8; i += 2) {
+          const float a0 = ex2_approx(fmaf(__uint_as_float(v[8 * g + i]), p.scale_log2, -m_new));
+          const float a1 = ex2_approx(fmaf(__uint_as_float(v[8 * g + i + 1]), p.scale_log2, -m_new));
           lsum += a0 + a1;
           const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
           memcpy(&packed[i >> 1], &h, 4);
         }
-        // keys [32c, 32c+32) of this row: k-tile c/2, 16-byte chunks (c%2)*4 .. +3, swizzled by row
-        const uint32_t rbase = sP + (c >> 1) * kSub + row * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t chunk = static_cast<uint32_t>(((c & 1) * 4 + u) ^ (row & 7));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rbase + chunk * 16),
-                       "r"(packed[4 * u]), "r"(packed[4 * u + 1]), "r"(packed[4 * u + 2]), "r"(packed[4 * u + 3])
-                       : "memory");
-        }
+        const uint32_t addr = pbase + static_cast<uint32_t>((g ^ (row & 7)) * 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[0]), "r"(packed[1]),
+                     "r"(packed[2]), "r"(packed[3])
+                     : "memory");
       }
       l = l * alpha + lsum;
       m = m_new;
@@ -278,16 +333,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
       ptx::tc_fence_before();
       ptx::mbar_arrive(p_full);
     }
-    if (ok && wait_o(nb - 1)) {
-      const float inv = 1.f / l;
+    float l2 = 0.f;
+    if (ok && wait_pv(nb - 1) && exchange(l, l2)) {
+      const float inv = 1.f / (l + l2);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
         ptx::tmem_ld_32cols(ob + c * 32, v);
         ptx::tmem_ld_wait();
         ptx::tmem_regs_ready(v);
         if (qrow < p.tokens) {
-          __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(hd.out) + static_cast<long long>(qrow) * hd.out_ld + c * 32;
+          __nv_bfloat16 *dst =
+              static_cast<__nv_bfloat16 *>(hd.out) + static_cast<long long>(qrow) * hd.out_ld + c0 + c * 32;
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
@@ -308,10 +365,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
 
   // ---- teardown: every TMA load this CTA started has landed before it exits ----
   __syncthreads();
-  if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane < 2) {
     if (q_issued && !ptx::mbar_wait(q_full, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    const uint32_t full0 = lane == 0 ? k_full0 : v_full0;
     for (int s = 0; s < 2; ++s)
-      if (issued[s] > 0 && !ptx::mbar_wait(kv_full0 + 8 * s, (issued[s] - 1) & 1, p.wait_ns))
+      if (issued[s] > 0 && !ptx::mbar_wait(full0 + 8 * s, (issued[s] - 1) & 1, p.wait_ns))
         record(p.status, kDevTimeoutDrain);
   }
   __syncthreads();
