@@ -801,6 +801,8 @@ def run_native(args):
     for nm in names:
         if nm.startswith("combine"):
             launches += 2 * (n - 1) if mode == "ring" else 1
+        elif nm == "attn_core":
+            launches += 2  # the transpose of every kv source's V, then the attention kernel
         elif nm == "moe_block":
             # routing, gather, gate/up, down and combine kernels, then the all-reduce
             launches += 5 + ({"ring": 2 * (n - 1), "ring_fused": 1}.get(mode, 0) if n > 1 else 0)

@@ -5,9 +5,11 @@
 // A_h = softmax(Q_h K_g^T / sqrt(d)) V_g, causal (query i sees keys j <= i) or
 // full, d = 128.
 //
-// k_attention: one CTA per (128-query tile, q head); causal grids run the
-// longest query tiles first. Warp roles:
-//   warp 0     TMA producers: lane 0 loads the Q tile once and K tiles of 128
+// k_attention: persistent, one CTA per SM walking (128-query tile, q head) work
+// items, the longest causal query tiles first; TMEM, barriers and the pipeline
+// phases carry over from item to item. Warp roles:
+//   warp 0     TMA producers: lane 0 loads each item's Q tile (as soon as the
+//              previous item's last S = Q K^T has read the last one) and K tiles of 128
 //              keys through a 2-stage ring, lane 1 V^T tiles through another (V
 //              is transposed beforehand, so every MMA operand is a K-major,
 //              128-byte-swizzled tile). A K stage frees when its S = Q K^T is
@@ -18,13 +20,14 @@
 //              before P_j V_j so it overlaps the softmax;
 //   warps 2-9  softmax: two threads per query row (TMEM lane), warps w and w+4
 //              taking keys and output columns [0, 64) and [64, 128). They take the
-//              row maximum of S_j and combine it through shared memory (a named
-//              barrier per warp pair); the row's reference maximum m moves only when
+//              row maximum of S_j and combine it through shared memory (a bounded
+//              mbarrier handshake per warp pair); the row's reference maximum m moves only when
 //              the block's maximum exceeds it by more than 8 (in log2 units),
 //              and then the row of O is rescaled in TMEM by 2^(m_old - m_new)
 //              after the previous P V has landed; so p = exp2(s*c - m) <= 2^8.
 //              Pass 2 writes p as bf16 into the shared-memory P tile (K-major,
-//              swizzled) and sums it into the row sum l. At the end O / l.
+//              swizzled) and sums it into the row sum l. At the end of an item
+//              O / l is stored and the MMA warp is told O is free again.
 // Every wait is bounded; on a timeout the kernel records it, stops issuing,
 // drains its TMA loads, frees TMEM and returns.
 //
@@ -44,8 +47,8 @@ constexpr int kTileQ = 128, kTileK = 128, kHd = 128;
 constexpr uint32_t kSub = 128u * 128u;            // one [128 rows x 64 bf16] swizzled k-tile
 constexpr uint32_t kTile = 2 * kSub;              // a [128 x 128] bf16 operand tile
 constexpr uint32_t kSmemQ = 0, kSmemK = kTile, kSmemV = 3 * kTile, kSmemP = 5 * kTile;  // P: 2 tiles
-constexpr uint32_t kSmemBar = 7 * kTile;          // barriers after the seven tiles (160 bytes)
-constexpr uint32_t kSmemRed = kSmemBar + 160;      // row-maximum / row-sum exchange, [2][128] f32
+constexpr uint32_t kSmemBar = 7 * kTile;          // barriers after the seven tiles (176 bytes)
+constexpr uint32_t kSmemRed = kSmemBar + 192;      // row-maximum / row-sum exchange, [2][128] f32
 constexpr size_t kAttnSmem = kSmemRed + 1024 + 1024;  // + the exchange + alignment slack (226.1 KB)
 constexpr uint32_t kTmemCols = 512;               // S0, S1, O at columns 0, 128, 256
 
@@ -73,42 +76,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
   const uint32_t sQ = sbase + kSmemQ, sK0 = sbase + kSmemK, sV0 = sbase + kSmemV, sP = sbase + kSmemP;
   uint8_t *bar_area = smem + kSmemBar;
   const uint32_t bar0 = ptx::smem_addr(bar_area);
-  const uint32_t q_full = bar0, k_full0 = bar0 + 8, k_empty0 = bar0 + 24, v_full0 = bar0 + 40,
-                 v_empty0 = bar0 + 56, s_full0 = bar0 + 72, p_full = bar0 + 88, p_empty0 = bar0 + 96,
-                 drain = bar0 + 112;
-  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 120);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 124);
-  const uint32_t xbar0 = bar0 + 128;  // one exchange barrier per softmax warp pair
+  const uint32_t q_full = bar0, q_empty = bar0 + 8, k_full0 = bar0 + 16, k_empty0 = bar0 + 32,
+                 v_full0 = bar0 + 48, v_empty0 = bar0 + 64, s_full0 = bar0 + 80, p_full = bar0 + 96,
+                 p_empty0 = bar0 + 104, o_free = bar0 + 120, drain = bar0 + 128;
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 136);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 140);
+  const uint32_t xbar0 = bar0 + 144;  // one exchange barrier per softmax warp pair
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work item: causal grids start with the last (longest) query tiles
-  const int qt = p.causal ? p.q_tiles - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int head = blockIdx.y;
-  const AttnHead hd = p.heads[head];
-  const int q0 = qt * kTileQ;
-  const int nb = p.causal ? qt + 1 : (p.tokens + kTileK - 1) / kTileK;
+  const int items = p.q_tiles * p.heads_total;
+  // work item -> (query tile, head); causal runs the longest query tiles first
+  auto item = [&](int it, int &qt, int &nb) -> const AttnHead & {
+    const int r = it / p.heads_total;
+    qt = p.causal ? p.q_tiles - 1 - r : r;
+    nb = p.causal ? qt + 1 : (p.tokens + kTileK - 1) / kTileK;
+    return p.heads[it % p.heads_total];
+  };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(k_full0 + 8 * s, 1);
       ptx::mbar_init(k_empty0 + 8 * s, 1);
       ptx::mbar_init(v_full0 + 8 * s, 1);
       ptx::mbar_init(v_empty0 + 8 * s, 1);
       ptx::mbar_init(s_full0 + 8 * s, 1);
+      ptx::mbar_init(p_empty0 + 8 * s, 1);
     }
     ptx::mbar_init(p_full, 256);
-    ptx::mbar_init(p_empty0, 1);
-    ptx::mbar_init(p_empty0 + 8, 1);
+    ptx::mbar_init(o_free, 256);
     ptx::mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) ptx::mbar_init(xbar0 + 8 * q, 64);
     *abort_flag = 0;
     ptx::fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    ptx::prefetch_tensormap(&p.maps[hd.q_map]);
-    ptx::prefetch_tensormap(&p.maps[hd.k_map]);
-    ptx::prefetch_tensormap(&p.maps[hd.v_map]);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
@@ -121,49 +122,65 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
+  // Pipeline phases run on counters over this CTA's whole sequence of items:
+  // ic (items started) and g (key blocks, over all items).
   int issued[2] = {0, 0};  // loads started per stage of this producer lane's ring
-  bool q_issued = false;
+  int q_loads = 0;
   if (warp == 0) {
     if (lane < 2) {
-      // lane 0: Q, then the K ring; lane 1: the V^T ring
+      // lane 0: Q of each item, then the K ring; lane 1: the V^T ring
       const uint32_t full0 = lane == 0 ? k_full0 : v_full0, empty0 = lane == 0 ? k_empty0 : v_empty0;
       const uint32_t dst0 = lane == 0 ? sK0 : sV0;
-      const CUtensorMap *map = &p.maps[lane == 0 ? hd.k_map : hd.v_map];
-      if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(q_full, kTile);
-        for (int c = 0; c < 2; ++c)
-          ptx::tma_load_2d(sQ + c * kSub, &p.maps[hd.q_map], hd.q_col + c * 64, q0, q_full);
-        q_issued = true;
-      }
-      for (int j = 0; j < nb; ++j) {
-        const int s = j & 1;
-        if (*abort_flag) break;
-        if (!ptx::mbar_wait(empty0 + 8 * s, ((j >> 1) & 1) ^ 1, p.wait_ns)) {
-          record(p.status, kDevTimeoutProducer);
-          *abort_flag = 1;
-          break;
+      bool run = true;
+      int g = 0;
+      for (int it = blockIdx.x, ic = 0; run && it < items; it += gridDim.x, ++ic) {
+        int qt, nb;
+        const AttnHead &hd = item(it, qt, nb);
+        if (lane == 0) {
+          // the previous item's last S = Q K^T has read Q
+          if (*abort_flag || !ptx::mbar_wait(q_empty, (ic & 1) ^ 1, p.wait_ns)) {
+            if (!*abort_flag) record(p.status, kDevTimeoutProducer);
+            *abort_flag = 1;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(q_full, kTile);
+          for (int c = 0; c < 2; ++c)
+            ptx::tma_load_2d(sQ + c * kSub, &p.maps[hd.q_map], hd.q_col + c * 64, qt * kTileQ, q_full);
+          ++q_loads;
         }
-        ptx::mbar_arrive_expect_tx(full0 + 8 * s, kTile);
-        for (int c = 0; c < 2; ++c) {
-          if (lane == 0)
-            ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, hd.kv_col + c * 64, j * kTileK, full0 + 8 * s);
-          else
-            ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, j * kTileK + c * 64, hd.kv_col, full0 + 8 * s);
+        const CUtensorMap *map = &p.maps[lane == 0 ? hd.k_map : hd.v_map];
+        for (int j = 0; j < nb; ++j, ++g) {
+          const int s = g & 1;
+          if (*abort_flag || !ptx::mbar_wait(empty0 + 8 * s, ((g >> 1) & 1) ^ 1, p.wait_ns)) {
+            if (!*abort_flag) record(p.status, kDevTimeoutProducer);
+            *abort_flag = 1;
+            run = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(full0 + 8 * s, kTile);
+          for (int c = 0; c < 2; ++c) {
+            if (lane == 0)
+              ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, hd.kv_col + c * 64, j * kTileK, full0 + 8 * s);
+            else
+              ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, j * kTileK + c * 64, hd.kv_col, full0 + 8 * s);
+          }
+          ++issued[s];
         }
-        ++issued[s];
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileQ, 128);
-      bool ok = ptx::mbar_wait(q_full, 0, p.wait_ns);
-      if (!ok) record(p.status, kDevTimeoutMma);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (*abort_flag || !ptx::mbar_wait(k_full0 + 8 * s, (j >> 1) & 1, p.wait_ns)) {
-          if (!*abort_flag) record(p.status, kDevTimeoutMma);
-          return false;
-        }
+      bool ok = true;
+      auto fail = [&]() {
+        if (!*abort_flag) record(p.status, kDevTimeoutMma);
+        ok = false;
+      };
+      // S_g = Q K_g^T into TMEM buffer g % 2 (free: its previous S was read before
+      // the softmax signalled p_full for that block, which this thread waited on)
+      auto issue_s = [&](int g) {
+        const int s = g & 1;
+        if (*abort_flag || !ptx::mbar_wait(k_full0 + 8 * s, (g >> 1) & 1, p.wait_ns)) return fail();
         ptx::tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(s * 128);
 #pragma unroll
@@ -174,29 +191,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
         }
         ptx::mma_commit(s_full0 + 8 * s);
         ptx::mma_commit(k_empty0 + 8 * s);
-        return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < nb; ++j) {
-        if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
-        // O += P_j V_j once the softmax has written P_j (and rescaled O if needed)
-        if (*abort_flag || !ptx::mbar_wait(p_full, j & 1, p.wait_ns) ||
-            !ptx::mbar_wait(v_full0 + 8 * (j & 1), (j >> 1) & 1, p.wait_ns)) {
-          if (!*abort_flag) record(p.status, kDevTimeoutMma);
-          ok = false;
+      int g = 0;
+      for (int it = blockIdx.x, ic = 0; ok && it < items; it += gridDim.x, ++ic) {
+        int qt, nb;
+        item(it, qt, nb);
+        // this item's Q has landed
+        if (*abort_flag || !ptx::mbar_wait(q_full, ic & 1, p.wait_ns)) {
+          fail();
           break;
         }
-        ptx::tc_fence_after();
-        const int s = j & 1;
-        const uint32_t d = tmem + 256u;
+        issue_s(g);
+        if (ok && nb == 1) ptx::mma_commit(q_empty);
+        for (int j = 0; ok && j < nb; ++j, ++g) {
+          if (j + 1 < nb) {
+            issue_s(g + 1);
+            if (!ok) break;
+            if (j + 2 == nb) ptx::mma_commit(q_empty);  // the item's last S is issued
+          }
+          // O += P_g V_g once the softmax has written P_g (and rescaled O if needed);
+          // the item's first one overwrites O, so the previous item's output must
+          // have been read from it
+          if (*abort_flag || !ptx::mbar_wait(p_full, g & 1, p.wait_ns) ||
+              !ptx::mbar_wait(v_full0 + 8 * (g & 1), (g >> 1) & 1, p.wait_ns) ||
+              (j == 0 && !ptx::mbar_wait(o_free, (ic & 1) ^ 1, p.wait_ns))) {
+            fail();
+            break;
+          }
+          ptx::tc_fence_after();
+          const int s = g & 1;
+          const uint32_t d = tmem + 256u;
 #pragma unroll
-        for (int kk = 0; kk < kTileK / 16; ++kk) {
-          const uint64_t ad = ptx::smem_desc_sw128(sP + s * kTile + (kk >> 2) * kSub) + 2 * (kk & 3);
-          const uint64_t bd = ptx::smem_desc_sw128(sV0 + s * kTile + (kk >> 2) * kSub) + 2 * (kk & 3);
-          ptx::mma_bf16(d, ad, bd, idesc, (j | kk) > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kTileK / 16; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(sP + s * kTile + (kk >> 2) * kSub) + 2 * (kk & 3);
+            const uint64_t bd = ptx::smem_desc_sw128(sV0 + s * kTile + (kk >> 2) * kSub) + 2 * (kk & 3);
+            ptx::mma_bf16(d, ad, bd, idesc, (j | kk) > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(p_empty0 + 8 * s);  // P_g read, O current up to block g
+          ptx::mma_commit(v_empty0 + 8 * s);
         }
-        ptx::mma_commit(p_empty0 + 8 * s);  // P_j read, O current up to block j
-        ptx::mma_commit(v_empty0 + 8 * s);
       }
       if (!ok) *abort_flag = 1;
       ptx::mma_commit(drain);
@@ -207,21 +240,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
     const int qw = warp & 3;
     const int half = (warp - 2) >> 2;  // 0: keys / output columns [0, 64), 1: [64, 128)
     const int row = qw * 32 + lane;
-    const int qrow = q0 + row;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const uint32_t ob = tmem + lane_off + 256u + 64u * half;
     const uint32_t xbar = xbar0 + 8 * qw;  // the two warps sharing these rows
     volatile float *red = reinterpret_cast<volatile float *>(smem + kSmemRed);
-    // The partner's value of this row through shared memory. Each exchange takes
-    // two phases of the pair's barrier: both values written, then both read (so
-    // the next exchange cannot overwrite a value not yet read). Bounded waits.
-    auto exchange = [&](float x, float &y) -> bool {
-      red[half * 128 + row] = x;
-      ptx::mbar_arrive(xbar);
-      bool ready = ptx::mbar_wait(xbar, 0, p.wait_ns);
-      y = red[(half ^ 1) * 128 + row];
-      ptx::mbar_arrive(xbar);
-      ready = ptx::mbar_wait(xbar, 1, p.wait_ns) && ready;
+    bool ok = true;
+    // A bounded warp-wide wait; on a timeout (or another role's abort) the warp gives up.
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool ready = ptx::mbar_wait(bar, parity, p.wait_ns);
       if (!__all_sync(0xffffffffu, ready && *abort_flag == 0)) {
         if (lane == 0) {
           if (!ready) record(p.status, kDevTimeoutEpilogue);
@@ -231,110 +257,111 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
       }
       return true;
     };
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    // waits for O += P_i V_i to land: P tile i % 2 is free again and O is current
-    // up to block i (tcgen05 operations complete in issue order)
+    // The partner's value of this row through shared memory. Each exchange takes
+    // two phases of the pair's barrier: both values written, then both read (so
+    // the next exchange cannot overwrite a value not yet read).
+    auto exchange = [&](float x, float &y) -> bool {
+      red[half * 128 + row] = x;
+      ptx::mbar_arrive(xbar);
+      if (!wait_all(xbar, 0)) return false;
+      y = red[(half ^ 1) * 128 + row];
+      ptx::mbar_arrive(xbar);
+      return wait_all(xbar, 1);
+    };
+    // O += P_i V_i has landed: P tile i % 2 is free and O is current up to block i
+    // (tcgen05 operations complete in issue order)
     auto wait_pv = [&](int i) -> bool {
-      const bool ready = ptx::mbar_wait(p_empty0 + 8 * (i & 1), (i >> 1) & 1, p.wait_ns);
-      if (!__all_sync(0xffffffffu, ready && *abort_flag == 0)) {
-        if (lane == 0) {
-          if (!ready) record(p.status, kDevTimeoutEpilogue);
-          *abort_flag = 1;
-        }
-        return false;
-      }
+      if (!wait_all(p_empty0 + 8 * (i & 1), (i >> 1) & 1)) return false;
       ptx::tc_fence_after();
       return true;
     };
     const int c0 = 64 * half;  // first key of this thread's half
-    for (int j = 0; j < nb; ++j) {
-      const int s = j & 1;
-      const bool ready = ptx::mbar_wait(s_full0 + 8 * s, (j >> 1) & 1, p.wait_ns);
-      if (!__all_sync(0xffffffffu, ready && *abort_flag == 0)) {
-        if (lane == 0) {
-          if (!ready) record(p.status, kDevTimeoutEpilogue);
-          *abort_flag = 1;
-        }
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(s * 128 + c0);
-      const int k0 = j * kTileK;
-      // keys past the query (causal) or past the sequence are masked
-      const int lim = min(p.causal ? qrow - k0 + 1 : kTileK, p.tokens - k0) - c0;
-      uint32_t v[64];
-      {
-        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-        ptx::tmem_ld_32cols(sb, v0);
-        ptx::tmem_ld_32cols(sb + 32, v1);
-        ptx::tmem_ld_wait();
-        ptx::tmem_regs_ready(v);
-      }
-      const bool full = __all_sync(0xffffffffu, lim >= 64);  // no masked key in this warp's half
-      if (!full) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i >= lim) v[i] = __float_as_uint(-INFINITY);
-      }
-      float mx = __uint_as_float(v[0]);
-#pragma unroll
-      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
-      float mx2;
-      if (!exchange(mx, mx2)) { ok = false; break; }
-      mx = fmaxf(mx, mx2);
-      const float m_blk = mx * p.scale_log2;
-      const bool move = m_blk > m + 8.f;  // always on the first block (m = -inf)
-      const float m_new = move ? m_blk : m;
-      const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
-      bool pv1_done = false;
-      if (j > 0 && __any_sync(0xffffffffu, move)) {
-        if (!wait_pv(j - 1)) { ok = false; break; }
-        pv1_done = true;
-        // rescale this thread's half of the row of O (rows keeping their maximum scale by 1)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          ptx::tmem_ld_32cols(ob + c * 32, o);
+    int g = 0;
+    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      int qt, nb;
+      const AttnHead &hd = item(it, qt, nb);
+      const int qrow = qt * kTileQ + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nb; ++j, ++g) {
+        const int s = g & 1;
+        if (!wait_all(s_full0 + 8 * s, (g >> 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(s * 128 + c0);
+        const int k0 = j * kTileK;
+        // keys past the query (causal) or past the sequence are masked
+        const int lim = min(p.causal ? qrow - k0 + 1 : kTileK, p.tokens - k0) - c0;
+        uint32_t v[64];
+        {
+          uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+          uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+          ptx::tmem_ld_32cols(sb, v0);
+          ptx::tmem_ld_32cols(sb + 32, v1);
           ptx::tmem_ld_wait();
-          ptx::tmem_regs_ready(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          ptx::tmem_st_32cols(ob + c * 32, o);
+          ptx::tmem_regs_ready(v);
         }
-        ptx::tmem_st_wait();
-      }
-      // P tile s was last read by P_{j-2} V_{j-2}
-      if (j >= 2 && !pv1_done && !wait_pv(j - 2)) { ok = false; break; }
-      float lsum = 0.f;
-      // k-tile `half` of the P tile holds this thread's 64 keys
-      const uint32_t pbase = sP + s * kTile + half * kSub + row * 128;
+        if (!__all_sync(0xffffffffu, lim >= 64)) {  // a masked key in this warp's half
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {  // keys [8g, 8g+8) of the half: one 16-byte chunk
-        uint32_t packed[4];
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const float a0 = ex2_approx(fmaf(__uint_as_float(v[8 * g + i]), p.scale_log2, -m_new));
-          const float a1 = ex2_approx(fmaf(__uint_as_float(v[8 * g + i + 1]), p.scale_log2, -m_new));
-          lsum += a0 + a1;
-          const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-          memcpy(&packed[i >> 1], &h, 4);
+          for (int i = 0; i < 64; ++i)
+            if (i >= lim) v[i] = __float_as_uint(-INFINITY);
         }
-        const uint32_t addr = pbase + static_cast<uint32_t>((g ^ (row & 7)) * 16);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[0]), "r"(packed[1]),
-                     "r"(packed[2]), "r"(packed[3])
-                     : "memory");
+        float mx = __uint_as_float(v[0]);
+#pragma unroll
+        for (int i = 1; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+        float mx2;
+        if (!exchange(mx, mx2)) { ok = false; break; }
+        mx = fmaxf(mx, mx2);
+        const float m_blk = mx * p.scale_log2;
+        const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
+        const float m_new = move ? m_blk : m;
+        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
+        bool pv1_done = false;
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          if (!wait_pv(g - 1)) { ok = false; break; }
+          pv1_done = true;
+          // rescale this thread's half of the row of O (rows keeping their maximum scale by 1)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld_32cols(ob + c * 32, o);
+            ptx::tmem_ld_wait();
+            ptx::tmem_regs_ready(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st_32cols(ob + c * 32, o);
+          }
+          ptx::tmem_st_wait();
+        }
+        // P tile s was last read by P_{g-2} V_{g-2}
+        if (g >= 2 && !pv1_done && !wait_pv(g - 2)) { ok = false; break; }
+        float lsum = 0.f;
+        // k-tile `half` of the P tile holds this thread's 64 keys
+        const uint32_t pbase = sP + s * kTile + half * kSub + row * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // keys [8q, 8q+8) of the half: one 16-byte chunk
+          uint32_t packed[4];
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const float a0 = ex2_approx(fmaf(__uint_as_float(v[8 * q + i]), p.scale_log2, -m_new));
+            const float a1 = ex2_approx(fmaf(__uint_as_float(v[8 * q + i + 1]), p.scale_log2, -m_new));
+            lsum += a0 + a1;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+            memcpy(&packed[i >> 1], &h, 4);
+          }
+          const uint32_t addr = pbase + static_cast<uint32_t>((q ^ (row & 7)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[0]), "r"(packed[1]),
+                       "r"(packed[2]), "r"(packed[3])
+                       : "memory");
+        }
+        l = l * alpha + lsum;
+        m = m_new;
+        ptx::fence_proxy_async_smem();  // P visible to the tensor core
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(p_full);
       }
-      l = l * alpha + lsum;
-      m = m_new;
-      ptx::fence_proxy_async_smem();  // P visible to the tensor core
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(p_full);
-    }
-    float l2 = 0.f;
-    if (ok && wait_pv(nb - 1) && exchange(l, l2)) {
+      if (!ok) break;
+      // the item's output: O / l once its last P V has landed
+      float l2 = 0.f;
+      if (!wait_pv(g - 1) || !exchange(l, l2)) { ok = false; break; }
       const float inv = 1.f / (l + l2);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -360,13 +387,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
           }
         }
       }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(o_free);  // O may be overwritten by the next item's first P V
     }
   }
 
   // ---- teardown: every TMA load this CTA started has landed before it exits ----
   __syncthreads();
   if (warp == 0 && lane < 2) {
-    if (q_issued && !ptx::mbar_wait(q_full, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    if (q_loads > 0 && !ptx::mbar_wait(q_full, (q_loads - 1) & 1, p.wait_ns)) record(p.status, kDevTimeoutDrain);
     const uint32_t full0 = lane == 0 ? k_full0 : v_full0;
     for (int s = 0; s < 2; ++s)
       if (issued[s] > 0 && !ptx::mbar_wait(full0 + 8 * s, (issued[s] - 1) & 1, p.wait_ns))
@@ -379,34 +408,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
   }
 }
 
-// V [T x C] (row pitch ld_in) -> V^T [C x T] (row pitch ld_out), 64 x 64 tiles.
-__global__ void __launch_bounds__(256) k_transpose_bf16(const __nv_bfloat16 *in, long long ld_in,
-                                                        __nv_bfloat16 *out, long long ld_out, int rows,
-                                                        int cols) {
+// V [T x C] (row pitch ld_in) -> V^T [C x T] (row pitch ld_out) for every kv
+// source in one launch (grid z = source), 64 x 64 tiles through shared memory.
+__global__ void __launch_bounds__(256) k_transpose_bf16(TransposeArgs a) {
   __shared__ __nv_bfloat16 tile[64][66];
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
+  const __nv_bfloat16 *in = static_cast<const __nv_bfloat16 *>(a.in[blockIdx.z]);
+  __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out[blockIdx.z]);
+  const long long ld_in = a.ld_in[blockIdx.z];
   const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int r = i / 64, c = i % 64;
-    if (r0 + r < rows && c0 + c < cols) tile[r][c] = in[static_cast<long long>(r0 + r) * ld_in + c0 + c];
+    if (r0 + r < a.rows && c0 + c < a.cols) tile[r][c] = in[static_cast<long long>(r0 + r) * ld_in + c0 + c];
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 64 * 64; i += 256) {
     const int c = i / 64, r = i % 64;
-    if (r0 + r < rows && c0 + c < cols) out[static_cast<long long>(c0 + c) * ld_out + r0 + r] = tile[r][c];
+    if (r0 + r < a.rows && c0 + c < a.cols) out[static_cast<long long>(c0 + c) * a.ld_out + r0 + r] = tile[r][c];
   }
 }
 
 }  // namespace
 
-tp_status launch_transpose_bf16(const void *in, long long ld_in, void *out, long long ld_out, int rows, int cols,
-                                cudaStream_t s) {
-  if (rows == 0 || cols == 0) return TP_OK;
-  const dim3 grid((rows + 63) / 64, (cols + 63) / 64);
-  return launch_checked(launch_kernel(k_transpose_bf16, grid, dim3(256), 0, s, 1,
-                                      static_cast<const __nv_bfloat16 *>(in), ld_in,
-                                      static_cast<__nv_bfloat16 *>(out), ld_out, rows, cols));
+tp_status launch_transpose_bf16(const TransposeArgs &a, int sources, cudaStream_t s) {
+  if (a.rows == 0 || a.cols == 0 || sources == 0) return TP_OK;
+  const dim3 grid((a.rows + 63) / 64, (a.cols + 63) / 64, sources);
+  return launch_checked(launch_kernel(k_transpose_bf16, grid, dim3(256), 0, s, 1, a));
 }
 
 tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
@@ -422,7 +450,9 @@ tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
     if (e != cudaSuccess) return cuda_fail(e);
     attr_set = true;
   }
-  const dim3 grid(static_cast<unsigned>(p.q_tiles), static_cast<unsigned>(total_heads));
+  p.heads_total = total_heads;
+  const long long items = static_cast<long long>(p.q_tiles) * total_heads;
+  const dim3 grid(static_cast<unsigned>(items < num_sms() ? items : num_sms()));
   return launch_checked(launch_kernel(k_attention, grid, dim3(kAttnThreads), kAttnSmem, s, 1, p));
 }
 

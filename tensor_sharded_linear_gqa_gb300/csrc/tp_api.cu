@@ -710,11 +710,18 @@ extern "C" tp_status tp_attn_core(const tp_plan *plan, const tp_tensor *q, const
   if (T == 0 || total_heads == 0) return TP_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const long long tp8 = (T + 7) / 8 * 8;
-  // V -> V^T per kv source, so that P V reads K-major tiles
-  for (int32_t r = 0; r < nkv; ++r)
-    if ((st = launch_transpose_bf16(v[r].ptr, v[r].ld, static_cast<char *>(workspace) + r * vt, tp8,
-                                    static_cast<int>(T), static_cast<int>(kvc), s)) != TP_OK)
-      return st;
+  // V -> V^T for every kv source in one launch, so that P V reads K-major tiles
+  TransposeArgs ta;
+  std::memset(&ta, 0, sizeof(ta));
+  for (int32_t r = 0; r < nkv; ++r) {
+    ta.in[r] = v[r].ptr;
+    ta.ld_in[r] = v[r].ld;
+    ta.out[r] = static_cast<char *>(workspace) + r * vt;
+  }
+  ta.ld_out = tp8;
+  ta.rows = static_cast<int>(T);
+  ta.cols = static_cast<int>(kvc);
+  if ((st = launch_transpose_bf16(ta, nkv, s)) != TP_OK) return st;
   static thread_local AttnParams prm;  // ~22 KB: kept off the stack
   std::memset(&prm, 0, sizeof(prm));
   for (int32_t r = 0; r < n; ++r)

@@ -284,15 +284,22 @@ struct AttnHead {
 struct AttnParams {
   CUtensorMap maps[kMaxAttnMaps];
   AttnHead heads[kMaxAttnHeads];
-  int tokens, q_tiles, causal, pad;
+  int tokens, q_tiles, causal, heads_total;
   float scale_log2;         // log2(e) / sqrt(d)
   int *status;
   long long wait_ns;
 };
 tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s);
-// V [rows x cols] (pitch ld_in) -> V^T [cols x rows] (pitch ld_out), bf16.
-tp_status launch_transpose_bf16(const void *in, long long ld_in, void *out, long long ld_out, int rows, int cols,
-                                cudaStream_t s);
+// V [rows x cols] (pitch ld_in[z]) -> V^T [cols x rows] (pitch ld_out), bf16,
+// for sources z = 0..sources-1 in one launch.
+struct TransposeArgs {
+  const void *in[kMaxAttnRanks];
+  long long ld_in[kMaxAttnRanks];
+  void *out[kMaxAttnRanks];
+  long long ld_out;
+  int rows, cols;
+};
+tp_status launch_transpose_bf16(const TransposeArgs &a, int sources, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Mixture-of-experts block (moe.cu).
