@@ -854,6 +854,11 @@ def run_reference(args):
         return
     from tensor_sharded_linear_gqa_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
+    if w["kind"] != "mlp":
+        print(json.dumps({"impl": "reference", "unavailable": "the timed oracle arm covers the MLP block "
+                                                              f"workloads; {args.workload} is a {w['kind']} workload"}),
+              flush=True)
+        return
     K, W = args.steps, max(args.warmup, 0)
     # Each step is a row sample of the workload sized so that all K + W steps take
     # about two minutes on the host cores.

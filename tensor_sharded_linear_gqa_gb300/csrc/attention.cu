@@ -54,6 +54,33 @@ constexpr uint32_t kTmemCols = 512;               // S0, S1, O at columns 0, 128
 
 __device__ __forceinline__ void record(int *status, int code) { atomicCAS(status, 0, code); }
 
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two f32 lanes in one 64-bit register, and the packed (f32x2) add and fma.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32):
 // relative error of order 2^-22, far below the bf16 rounding P goes through next.
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -304,9 +331,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
           for (int i = 0; i < 64; ++i)
             if (i >= lim) v[i] = __float_as_uint(-INFINITY);
         }
-        float mx = __uint_as_float(v[0]);
+        float mx = __uint_as_float(v[63]);
 #pragma unroll
-        for (int i = 1; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+        for (int i = 0; i < 62; i += 2) mx = max3f(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+        mx = fmaxf(mx, __uint_as_float(v[62]));
         float mx2;
         if (!exchange(mx, mx2)) { ok = false; break; }
         mx = fmaxf(mx, mx2);
@@ -333,7 +361,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
         }
         // P tile s was last read by P_{g-2} V_{g-2}
         if (g >= 2 && !pv1_done && !wait_pv(g - 2)) { ok = false; break; }
-        float lsum = 0.f;
+        // p = 2^(s*c - m) two lanes at a time (packed f32x2 fma and sum)
+        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
+        uint64_t sum2 = pack2(0.f, 0.f);
         // k-tile `half` of the P tile holds this thread's 64 keys
         const uint32_t pbase = sP + s * kTile + half * kSub + row * 128;
 #pragma unroll
@@ -341,9 +371,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
           uint32_t packed[4];
 #pragma unroll
           for (int i = 0; i < 8; i += 2) {
-            const float a0 = ex2_approx(fmaf(__uint_as_float(v[8 * q + i]), p.scale_log2, -m_new));
-            const float a1 = ex2_approx(fmaf(__uint_as_float(v[8 * q + i + 1]), p.scale_log2, -m_new));
-            lsum += a0 + a1;
+            float y0, y1;
+            unpack2(fma2(pack2(__uint_as_float(v[8 * q + i]), __uint_as_float(v[8 * q + i + 1])), c2, nm2), y0, y1);
+            const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
+            sum2 = add2(sum2, pack2(a0, a1));
             const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
             memcpy(&packed[i >> 1], &h, 4);
           }
@@ -352,7 +383,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
                        "r"(packed[2]), "r"(packed[3])
                        : "memory");
         }
-        l = l * alpha + lsum;
+        float s0, s1;
+        unpack2(sum2, s0, s1);
+        l = l * alpha + (s0 + s1);
         m = m_new;
         ptx::fence_proxy_async_smem();  // P visible to the tensor core
         ptx::tc_fence_before();
