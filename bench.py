@@ -281,7 +281,11 @@ class DeviceSet:
             rep = shards[0]["kv_replicated"]
             nkv = 1 if rep else n
             wq, wk, wv, wo = (to_dev(data[k]) for k in ("wq", "wk", "wv", "wo"))
-            self.a = to_dev(data["a"])
+            # with the attention core, A is its output; else an explicit input
+            self.attention = bool(w.get("attention"))
+            self.a = (torch.empty((T, w["q_heads"] * hd), dtype=torch.bfloat16, device=dev) if self.attention
+                      else to_dev(data["a"]))
+            self.keep.append(self.a)
             q_w = [wq[rng(r, "q_proj")] for r in range(n)]
             k_w = [wk[rng(r, "k_proj")] for r in range(nkv)]
             v_w = [wv[rng(r, "v_proj")] for r in range(nkv)]
@@ -294,6 +298,13 @@ class DeviceSet:
             self.keep += q + k + v + yo
             self.calls.append(("qkv", ("tp_qkv_proj", tp.arr([self.x]), tp.arr(q_w), tp.arr(k_w), tp.arr(v_w),
                                        tp.arr(q), tp.arr(k), tp.arr(v))))
+            self.aws = None
+            if self.attention:
+                self.aws = torch.empty(tp.tp_attn_core_workspace_size(plan, T), dtype=torch.uint8, device=dev)
+                self.keep.append(self.aws)
+                self.calls.append(("attn_core", tp.Prepared(
+                    "tp_attn_core", plan.handle, tp.arr(q), tp.arr(k), tp.arr(v), tp.arr(a_r), 1,
+                    self.aws.data_ptr(), self.aws.numel(), sptr)))
             self.calls.append(("o_proj", tp.Prepared(
                 "tp_row_linear", n, tp.arr(a_r), tp.arr(o_w), tp.arr(yo),
                 tp.TP_COMBINE_FUSED if mode == "fused" else tp.TP_COMBINE_NONE, sptr)))
@@ -459,6 +470,10 @@ def phase_costs(w, mode):
         out["gate_up"] = (4.0 * T * D * F, 2 * F * D * 2 + T * D * 2 + T * F * 2)
         out["down"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + nparts * part)
         out["combine_mlp"] = (0.0, ring_bytes(mode, n, part))
+    if w["kind"] == "layer" and w.get("attention"):
+        hd, hq, hkv = w["head_dim"], w["q_heads"], w["kv_heads"]
+        out["attn_core"] = (4.0 * hd * hq * T * (T + 1) / 2,
+                            T * hq * hd * 2 * 2 + T * hkv * hd * 2 * 2 + 2 * T * hkv * hd * 2)
     if w["kind"] == "attn_core":
         hd, hq, hkv = w["head_dim"], w["q_heads"], w["kv_heads"]
         # causal: query i meets keys 0..i; QK^T and PV, 2 flops a multiply-add each
@@ -685,9 +700,21 @@ def run_native(args):
             q_w, k_w, v_w, q, k, v, _a_r, o_w, _yo = s0.e2e["attn"]
             a_r = [sl["a"][:, slice(*shards[r]["ranges"]["o_proj"])] for r in range(n)]
             xs = tp.tensor(sl["x"])
-            sl["calls"].append(tp.Prepared(
-                "tp_attn_proj", plan0.handle, ctypes.byref(xs), tp.arr(q_w), tp.arr(k_w), tp.arr(v_w), tp.arr(q),
-                tp.arr(k), tp.arr(v), tp.arr(a_r), tp.arr(o_w), tp.arr(sl["yo"]), combine_id, sptr))
+            sl["keep"] = [xs]
+            if s0.attention:
+                # q/k/v projections, the attention core into this slot's A, o_proj + combine
+                sl["calls"].append(tp.Prepared(
+                    "tp_qkv_proj", plan0.handle, ctypes.byref(xs), tp.arr(q_w), tp.arr(k_w), tp.arr(v_w),
+                    tp.arr(q), tp.arr(k), tp.arr(v), sptr))
+                sl["calls"].append(tp.Prepared(
+                    "tp_attn_core", plan0.handle, tp.arr(q), tp.arr(k), tp.arr(v), tp.arr(a_r), 1,
+                    s0.aws.data_ptr(), s0.aws.numel(), sptr))
+                sl["calls"].append(tp.Prepared(
+                    "tp_row_linear", n, tp.arr(a_r), tp.arr(o_w), tp.arr(sl["yo"]), combine_id, sptr))
+            else:
+                sl["calls"].append(tp.Prepared(
+                    "tp_attn_proj", plan0.handle, ctypes.byref(xs), tp.arr(q_w), tp.arr(k_w), tp.arr(v_w),
+                    tp.arr(q), tp.arr(k), tp.arr(v), tp.arr(a_r), tp.arr(o_w), tp.arr(sl["yo"]), combine_id, sptr))
         if "mlp" in s0.e2e:
             g, u, dn, _ym = s0.e2e["mlp"]
             xs = tp.tensor(sl["x"])
@@ -718,7 +745,7 @@ def run_native(args):
         sl = slots[0]
         if copy_x:
             sl["x"].copy_(xh, non_blocking=True)
-        if "a" in sl:
+        if ah is not None:
             sl["a"].copy_(ah, non_blocking=True)
         if "ids" in sl:
             sl["ids"].copy_(idh, non_blocking=True)
@@ -745,7 +772,7 @@ def run_native(args):
         with torch.cuda.stream(h2d_s):
             if copy_x:
                 sl["x"].copy_(xh, non_blocking=True)
-            if "a" in sl:
+            if ah is not None:
                 sl["a"].copy_(ah, non_blocking=True)
             if "ids" in sl:
                 sl["ids"].copy_(idh, non_blocking=True)
@@ -886,7 +913,7 @@ def run_reference(args):
 
 DEFAULT_STEPS = {"mlp_tp2_t512": 10000, "attn_gqa_tp4_t2048": 3000, "decode_gqa_rep_tp8_t64": 6000,
                  "prefill_layer_tp8_t4096": 200, "rs_column_tp8_t4096": 600, "vocab_tp8_t4096": 200,
-                 "moe_mixtral_tp8_t4096": 400, "attn_core_tp8_t4096": 1000}
+                 "moe_mixtral_tp8_t4096": 400, "attn_core_tp8_t4096": 1000, "decoder_layer_tp8_t4096": 200}
 
 
 def main():

@@ -57,6 +57,10 @@ WORKLOADS = {
     "prefill_layer_tp8_t4096": dict(kind="layer", T=4096, hidden=8192, q_heads=64,
                                     kv_heads=8, head_dim=128, ffn=28672, tp=8,
                                     seed=105, w_std=0.02, oracle_rows=64),
+    # The prefill layer with its attention: q/k/v projections, causal attention
+    # core, o_proj + all-reduce, then the MLP block (no explicit A input).
+    "decoder_layer_tp8_t4096": dict(kind="layer", attention=True, T=4096, hidden=8192, q_heads=64,
+                                    kv_heads=8, head_dim=128, ffn=28672, tp=8, seed=110, w_std=0.02),
     # Row-parallel down projection whose result feeds the next layer's q/k/v
     # projection (column-parallel) through a reduce-scatter, TP=8, bf16. The
     # q/k/v weights are stored fused per rank: rank r's rows are its q heads,
@@ -213,7 +217,7 @@ def make_bf16_inputs(w: dict, rows: int | None = None) -> dict:
         out["q"] = normal_bf16(seed, STREAM["aq"], (T, w["q_heads"] * hd))
         out["k"] = normal_bf16(seed, STREAM["ak"], (T, w["kv_heads"] * hd))
         out["v"] = normal_bf16(seed, STREAM["av"], (T, w["kv_heads"] * hd))
-    if w["kind"] in ("attn", "layer"):
+    if w["kind"] in ("attn", "layer") and not w.get("attention"):
         out["a"] = normal_bf16(seed, STREAM["a"], (T, w["q_heads"] * w["head_dim"]))
     for name, shp in weight_shapes(w).items():
         out[name] = normal_bf16(seed, STREAM[name], shp, w["w_std"])

@@ -137,3 +137,44 @@ def test_attn_core_tp8_t4096_sampled_rows():
             v = f(data["v"][r][:, g * HD:(g + 1) * HD])
             ref = np.stack([O.attention_head(q[i:i + 1], k[:i + 1], v[:i + 1], causal=False)[0] for i in rows])
             assert_close(got[rows, h * HD:(h + 1) * HD], ref, BF16_TOL, f"rank {r} head {h}")
+
+
+@pytest.mark.parametrize("tp_size,hq,hkv", [(4, 8, 2), (2, 4, 4)])
+def test_projection_attention_o_proj_chain(tp_size, hq, hkv):
+    """x -> q/k/v projections (column-parallel) -> causal attention core per rank ->
+    o_proj (row-parallel) with the ring all-reduce, against the oracle's chain of
+    the same three steps."""
+    need_gpu()
+    torch = _torch()
+    t, d = 200, 512
+    w = dict(kind="attn", T=t, hidden=d, q_heads=hq, kv_heads=hkv, head_dim=HD, tp=tp_size, seed=613,
+             w_std=0.05)
+    data = inputs.make_bf16_inputs(w)
+    plan = tp.tp_plan_create(tp_size, d, hq, hkv, HD, 8 * tp_size)
+    oplan = O.shard_plan(tp_size, d, hq, hkv, HD, 8 * tp_size)
+    sh = [tp.tp_plan_query_rank(plan, r) for r in range(tp_size)]
+    rep = sh[0]["kv_replicated"]
+    nkv = 1 if rep else tp_size
+    dev = {k: dev_bf16(data[k]) for k in ("x", "wq", "wk", "wv", "wo")}
+    wq = [dev["wq"][slice(*sh[r]["ranges"]["q_proj"])] for r in range(tp_size)]
+    wk = [dev["wk"][slice(*sh[r]["ranges"]["k_proj"])] for r in range(nkv)]
+    wv = [dev["wv"][slice(*sh[r]["ranges"]["v_proj"])] for r in range(nkv)]
+    wo = [dev["wo"][:, slice(*sh[r]["ranges"]["o_proj"])] for r in range(tp_size)]
+    q = [torch.empty((t, x.shape[0]), dtype=torch.bfloat16, device="cuda") for x in wq]
+    k = [torch.empty((t, x.shape[0]), dtype=torch.bfloat16, device="cuda") for x in wk]
+    v = [torch.empty((t, x.shape[0]), dtype=torch.bfloat16, device="cuda") for x in wv]
+    a = torch.empty((t, hq * HD), dtype=torch.bfloat16, device="cuda")
+    a_r = [a[:, slice(*sh[r]["ranges"]["o_proj"])] for r in range(tp_size)]
+    ys = [torch.empty((t, d), device="cuda") for _ in range(tp_size)]
+    ws = torch.empty(tp.tp_attn_core_workspace_size(plan, t), dtype=torch.uint8, device="cuda")
+    tp.tp_qkv_proj(plan, dev["x"], wq, wk, wv, q, k, v)
+    tp.tp_attn_core(plan, q, k, v, a_r, True, ws)
+    tp.tp_row_linear(tp_size, a_r, wo, ys, tp.TP_COMBINE_RING_FUSED)
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == (tp.TP_OK, 0)
+    f = {k: inputs.bf16_bits_to_f64(data[k]) for k in ("x", "wq", "wk", "wv", "wo")}
+    proj = O.attn_proj_sharded(f["x"], f["wq"], f["wk"], f["wv"], np.zeros((t, hq * HD)), f["wo"], oplan, HD)
+    att = O.attention_core_sharded(proj["q"], proj["k"], proj["v"], oplan, HD, True)
+    ref = sum(O.linear(att[r], f["wo"][:, slice(*oplan[r].ranges["o_proj"])]) for r in range(tp_size))
+    for r in range(tp_size):
+        assert_close(host_f64(ys[r]), ref, BF16_TOL, f"rank {r}")
