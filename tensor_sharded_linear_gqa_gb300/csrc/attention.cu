@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "sm100_ptx.cuh"
 #include "tp_internal.h"
@@ -476,12 +477,19 @@ tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
   if (e != cudaSuccess) return cuda_fail(e);
   p.status = ctx.status;
   p.wait_ns = ctx.wait_ns;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kAttnSmem));
-    if (e != cudaSuccess) return cuda_fail(e);
-    attr_set = true;
+  // the shared-memory opt-in is per device: set it once on each
+  static std::mutex mu;
+  static unsigned long long configured = 0;
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 64 || !(configured & (1ULL << dev))) {
+      e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kAttnSmem));
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (dev < 64) configured |= 1ULL << dev;
+    }
   }
   p.heads_total = total_heads;
   const long long items = static_cast<long long>(p.q_tiles) * total_heads;
