@@ -142,26 +142,40 @@ class ClockSampler:
 
 
 # ---- distributed plumbing (replicas only: NCCL carries only the timing max) ----------
-def dist_setup(args):
+def dist_setup(args, backend: str | None = None):
+    """One process per GPU from the launcher's environment. NCCL on GPUs; gloo
+    (host only, for the CPU tests of this plumbing) when no GPU is visible or
+    when asked for."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        backend = backend or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
 def dist_max(x: float, world: int) -> float:
+    """The largest of every rank's x (the job time is the slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tflops(world: int, flops_per_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: the work every replica did over the slowest rank's time."""
+    return world * flops_per_step * steps / (max_ms / 1e3) / 1e12
 
 
 def barrier(world: int):
@@ -590,7 +604,7 @@ def run_native(args):
     step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs)
 
     flops_step = sum(f for (f, _b) in costs.values())
-    value = world * flops_step * K / (max_ms / 1e3) / 1e12
+    value = aggregate_tflops(world, flops_step, K, max_ms)
     peaks, peak_src = load_peaks()
 
     # roofline of the dominant kernel: the gate/up GEMM where there is an MLP, else q/k/v
