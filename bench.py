@@ -612,13 +612,15 @@ def run_native(args):
     rf, rb = costs[rk]
     r_s = phase_ms[rk] / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    kname = {"attn_core": "k_attention (with the V transpose)",
+             "moe_block": "tp_moe_block (routing, gather, expert GEMMs, combine)"}.get(rk, f"k_gemm_bf16* ({rk})")
     if rf / rb >= ridge:
-        roof = {"kernel": f"k_gemm_bf16* ({rk})", "bound": "tensor", "achieved": round(rf / r_s / 1e12, 2),
+        roof = {"kernel": kname, "bound": "tensor", "achieved": round(rf / r_s / 1e12, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(rf / r_s / 1e12 / peaks["bf16_tflops"], 4),
                 "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic_flops_per_launch": rf}
     else:
-        roof = {"kernel": f"k_gemm_bf16* ({rk})", "bound": "hbm", "achieved": round(rb / r_s / 1e9, 1),
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(rb / r_s / 1e9, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(rb / r_s / 1e9 / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": rb}
     roof["traffic"] = committed_traffic(args.workload) if rk == "gate_up" else None
