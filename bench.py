@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-COMBINE_NAMES = {"fused": 1, "ring": 2, "ring_fused": 3}
+COMBINE_NAMES = {"fused": 1, "ring": 2, "ring_fused": 3, "ring_shared": 4}
 # Modes of the row-parallel -> reduce-scatter -> column-parallel pipeline workload.
 PIPELINE_MODES = ("deferred", "gathered")
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -49,8 +49,10 @@ def parse_args():
     p.add_argument("--workload", default="mlp_tp2_t512")
     p.add_argument("--combine", choices=sorted(COMBINE_NAMES) + sorted(PIPELINE_MODES), default=None,
                    help="ring_fused (default): the ring all-reduce in one pass, bit-identical to ring (N-1 step "
-                        "launches per phase). The reduce-scatter pipeline workload takes deferred (default: the "
-                        "column GEMM reads the reduced chunks) or gathered (an all-gather first)")
+                        "launches per phase); ring_shared: the same with the result stored once, for ranks that "
+                        "share one output on this device; fused: the ranks summed in the GEMM accumulator. The "
+                        "reduce-scatter pipeline workload takes deferred (default: the column GEMM reads the "
+                        "reduced chunks) or gathered (an all-gather first)")
     p.add_argument("--moe-mode", choices=["within_expert", "expert_parallel"], default="within_expert",
                    help="MoE sharding of the moe workloads")
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -83,11 +85,13 @@ def ring_bytes(mode: str, n: int, size_bytes: int) -> int:
         return 0
     if mode == "ring":
         return 3 * (n - 1) * size_bytes + 2 * (n - 1) * size_bytes
+    if mode == "ring_shared":
+        return (n + 1) * size_bytes  # each partial read once, the one shared result written
     return 2 * n * size_bytes  # ring_fused: each partial read once, every rank written once
 
 
 def launches_per_step(mode: str, n: int) -> int:
-    ring = {"ring": 2 * (n - 1), "ring_fused": 1, "fused": 0}[mode] if n > 1 else 0
+    ring = {"ring": 2 * (n - 1), "ring_fused": 1, "ring_shared": 1, "fused": 0}[mode] if n > 1 else 0
     return 2 + ring
 
 
@@ -287,7 +291,8 @@ class DeviceSet:
             return slice(*shards[r]["ranges"][name])
 
         self.calls = []  # (phase name, callable)
-        combine_ring = {"ring": tp.TP_RING_STEPS, "ring_fused": tp.TP_RING_FUSED}.get(mode)
+        combine_ring = {"ring": tp.TP_RING_STEPS, "ring_fused": tp.TP_RING_FUSED,
+                        "ring_shared": tp.TP_RING_FUSED_SHARED}.get(mode)
         self.x = to_dev(data["x"])
         self.e2e = {}
         if w["kind"] in ("attn", "layer"):
@@ -892,7 +897,7 @@ def run_native(args):
             launches += 2  # the transpose of every kv source's V, then the attention kernel
         elif nm == "moe_block":
             # routing, gather, gate/up, down and combine kernels, then the all-reduce
-            launches += 5 + ({"ring": 2 * (n - 1), "ring_fused": 1}.get(mode, 0) if n > 1 else 0)
+            launches += 5 + ({"ring": 2 * (n - 1), "ring_fused": 1, "ring_shared": 1}.get(mode, 0) if n > 1 else 0)
         else:
             launches += 1
     config = {"workload": args.workload, "tokens": T, "hidden": D, "tp_size": n, "combine": mode,

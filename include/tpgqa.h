@@ -175,8 +175,11 @@ typedef enum tp_combine {
                                 shards 0..N-1 in order; no partial is written              */
   TP_COMBINE_RING = 2,       /* y[r] = P_r, then the ring all-reduce as N-1 reduce-scatter and
                                 N-1 all-gather step launches; every y[r] ends equal to the sum */
-  TP_COMBINE_RING_FUSED = 3  /* as TP_COMBINE_RING, one pass that folds the partials in the
+  TP_COMBINE_RING_FUSED = 3, /* as TP_COMBINE_RING, one pass that folds the partials in the
                                 ring's order (bit-identical to TP_COMBINE_RING)            */
+  TP_COMBINE_RING_SHARED = 4 /* as TP_COMBINE_RING_FUSED, with the result stored once, in
+                                y[0] (bit-identical to it): for ranks that share one output
+                                on this device; y[1..N-1] keep their partials              */
 } tp_combine;
 
 /* Row-parallel linear: P_r = X_r * W_r^T, then the combine above.
@@ -201,7 +204,10 @@ tp_status tp_row_linear(int32_t tp_size, const tp_tensor *x, const tp_tensor *w,
  * ------------------------------------------------------------------------- */
 typedef enum tp_ring_mode {
   TP_RING_STEPS = 0, /* one launch per ring step, N-1 per phase                       */
-  TP_RING_FUSED = 1  /* one launch per phase; same fold order, bit-identical results   */
+  TP_RING_FUSED = 1, /* one launch per phase; same fold order, bit-identical results   */
+  TP_RING_FUSED_SHARED = 2 /* tp_allreduce_ring only: one pass, the sum written to buf[0]
+                              alone (the N equal results stored once); buf[1..N-1] keep
+                              their partials                                            */
 } tp_ring_mode;
 
 /* In-place reduce-scatter; afterwards chunk r of buf[r] is reduced. The other

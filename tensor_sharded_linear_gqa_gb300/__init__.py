@@ -33,8 +33,8 @@ TP_SHARD_COLUMN, TP_SHARD_ROW, TP_SHARD_VOCAB, TP_SHARD_REPLICATED = 0, 1, 2, 3
 TP_COMM_NONE, TP_COMM_ALL_REDUCE, TP_COMM_ALL_GATHER, TP_COMM_REDUCE_SCATTER = 0, 1, 2, 3
 TP_W_Q, TP_W_K, TP_W_V, TP_W_O, TP_W_GATE, TP_W_UP, TP_W_DOWN, TP_W_COUNT = range(8)
 WEIGHT_NAMES = ["q_proj", "k_proj", "v_proj", "o_proj", "gate_proj", "up_proj", "down_proj"]
-TP_COMBINE_NONE, TP_COMBINE_FUSED, TP_COMBINE_RING, TP_COMBINE_RING_FUSED = 0, 1, 2, 3
-TP_RING_STEPS, TP_RING_FUSED = 0, 1
+TP_COMBINE_NONE, TP_COMBINE_FUSED, TP_COMBINE_RING, TP_COMBINE_RING_FUSED, TP_COMBINE_RING_SHARED = 0, 1, 2, 3, 4
+TP_RING_STEPS, TP_RING_FUSED, TP_RING_FUSED_SHARED = 0, 1, 2
 TP_MOE_EXPERT_PARALLEL, TP_MOE_WITHIN_EXPERT = 0, 1
 
 

@@ -111,7 +111,10 @@ __global__ void __launch_bounds__(kThreads) k_ring_ag_step(RankPtrs b, int n, lo
 }
 
 // Folds chunk c (grid.y) over all ranks in ring order; writes every buffer
-// (all-reduce) or buffer c only (reduce-scatter). NT = N when N is 2, 4 or 8
+// (write_all = 1: all-reduce), buffer 0 only (2: the all-reduce's result stored
+// once, for ranks that share one output on this device; every element is read
+// and written by one thread, so buffer 0 can hold a partial on entry) or
+// buffer c only (0: reduce-scatter). NT = N when N is 2, 4 or 8
 // (fully unrolled, two float4 per thread per pass with every load issued before
 // the first add); NT = 0 handles any N.
 template <int NT>
@@ -129,10 +132,10 @@ __global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n_rt, l
   auto scalar = [&](long long e) {
     float acc = b.p[(c + 1) % n][e];
     for (int j = 2; j <= n; ++j) acc = acc + b.p[(c + j) % n][e];
-    if (write_all) {
+    if (write_all == 1) {
       for (int r = 0; r < n; ++r) b.p[r][e] = acc;
     } else {
-      b.p[c][e] = acc;
+      b.p[write_all == 2 ? 0 : c][e] = acc;
     }
   };
   if (t < vlo - lo) scalar(lo + t);
@@ -156,15 +159,16 @@ __global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n_rt, l
         a0 = add4(a0, x0[j]);
         a1 = add4(a1, x1[j]);
       }
-      if (write_all) {
+      if (write_all == 1) {
 #pragma unroll
         for (int r = 0; r < NT; ++r) {
           reinterpret_cast<float4 *>(b.p[r])[v0 + i] = a0;
           reinterpret_cast<float4 *>(b.p[r])[v0 + i + stride] = a1;
         }
       } else {
-        reinterpret_cast<float4 *>(b.p[c])[v0 + i] = a0;
-        reinterpret_cast<float4 *>(b.p[c])[v0 + i + stride] = a1;
+        float4 *dst = reinterpret_cast<float4 *>(b.p[write_all == 2 ? 0 : c]);
+        dst[v0 + i] = a0;
+        dst[v0 + i + stride] = a1;
       }
     }
     for (; i < nv; i += stride) {
@@ -174,11 +178,11 @@ __global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n_rt, l
       float4 a = x[0];
 #pragma unroll
       for (int j = 1; j < NT; ++j) a = add4(a, x[j]);
-      if (write_all) {
+      if (write_all == 1) {
 #pragma unroll
         for (int r = 0; r < NT; ++r) reinterpret_cast<float4 *>(b.p[r])[v0 + i] = a;
       } else {
-        reinterpret_cast<float4 *>(b.p[c])[v0 + i] = a;
+        reinterpret_cast<float4 *>(b.p[write_all == 2 ? 0 : c])[v0 + i] = a;
       }
     }
   } else {
@@ -186,10 +190,10 @@ __global__ void __launch_bounds__(kThreads) k_ring_fused(RankPtrs b, int n_rt, l
       float4 acc = reinterpret_cast<const float4 *>(b.p[(c + 1) % n])[v0 + i];
       for (int j = 2; j <= n; ++j)
         acc = add4(acc, reinterpret_cast<const float4 *>(b.p[(c + j) % n])[v0 + i]);
-      if (write_all) {
+      if (write_all == 1) {
         for (int r = 0; r < n; ++r) reinterpret_cast<float4 *>(b.p[r])[v0 + i] = acc;
       } else {
-        reinterpret_cast<float4 *>(b.p[c])[v0 + i] = acc;
+        reinterpret_cast<float4 *>(b.p[write_all == 2 ? 0 : c])[v0 + i] = acc;
       }
     }
   }

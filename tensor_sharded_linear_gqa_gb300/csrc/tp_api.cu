@@ -113,6 +113,7 @@ tp_status run_allreduce(int32_t n, const tp_tensor *buf, int32_t mode, cudaStrea
   const long long size = buf[0].rows * buf[0].cols;
   if (n == 1 || size == 0) return TP_OK;
   if (mode == TP_RING_FUSED) return launch_ring_fused(rank_ptrs(n, buf), n, size, 1, s);
+  if (mode == TP_RING_FUSED_SHARED) return launch_ring_fused(rank_ptrs(n, buf), n, size, 2, s);
   tp_status st = run_reduce_scatter(n, buf, TP_RING_STEPS, s);
   if (st != TP_OK) return st;
   return run_all_gather_ring(n, buf, TP_RING_STEPS, s);
@@ -318,7 +319,7 @@ tp_status check_row_args(int32_t n, const tp_tensor *x, const tp_tensor *w, cons
                          int32_t combine, int32_t *in_dtype) {
   if (!pow2_in_range(n)) return n >= 1 && n <= kMaxRanks ? TP_ERR_TP_SIZE_NOT_POW2 : TP_ERR_INVALID_ARG;
   if (!x || !w || !y) return TP_ERR_INVALID_ARG;
-  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_SHARED) return TP_ERR_INVALID_ARG;
   const int32_t dt = x[0].dtype;
   const long long T = x[0].rows, nout = w[0].rows;
   for (int32_t r = 0; r < n; ++r) {
@@ -334,7 +335,7 @@ tp_status check_row_args(int32_t n, const tp_tensor *x, const tp_tensor *w, cons
     if (y[q].rows != T || y[q].cols != nout) return TP_ERR_INVALID_ARG;
     if (T > 0 && nout > 0 && !pitch_ok(y[q])) return TP_ERR_ALIGNMENT;
   }
-  if (combine == TP_COMBINE_RING || combine == TP_COMBINE_RING_FUSED) {
+  if (combine == TP_COMBINE_RING || combine == TP_COMBINE_RING_FUSED || combine == TP_COMBINE_RING_SHARED) {
     const tp_status st = check_ring_bufs(n, y);
     if (st != TP_OK) return st;
   }
@@ -363,6 +364,7 @@ tp_status row_linear_impl(int32_t n, const tp_tensor *x, const tp_tensor *w, con
   if (st != TP_OK) return st;
   if (combine == TP_COMBINE_RING) return run_allreduce(n, y, TP_RING_STEPS, s);
   if (combine == TP_COMBINE_RING_FUSED) return run_allreduce(n, y, TP_RING_FUSED, s);
+  if (combine == TP_COMBINE_RING_SHARED) return run_allreduce(n, y, TP_RING_FUSED_SHARED, s);
   return TP_OK;
 }
 
@@ -791,7 +793,7 @@ extern "C" tp_status tp_moe_block(const tp_moe_dims *d, const tp_tensor *x, cons
   tp_status st = moe_check_dims(d);
   if (st != TP_OK) return st;
   if (!x || !w_gate || !w_up || !w_down || !y) return TP_ERR_INVALID_ARG;
-  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_SHARED) return TP_ERR_INVALID_ARG;
   const int32_t n = d->tp_size, E = d->num_experts;
   const bool within = d->mode == TP_MOE_WITHIN_EXPERT;
   const long long D = d->hidden, F = d->ffn, T = x->rows;
@@ -818,7 +820,7 @@ extern "C" tp_status tp_moe_block(const tp_moe_dims *d, const tp_tensor *x, cons
     if (y[q].rows != T || y[q].cols != D) return TP_ERR_INVALID_ARG;
     if (T > 0 && !pitch_ok(y[q])) return TP_ERR_ALIGNMENT;
   }
-  if ((combine == TP_COMBINE_RING || combine == TP_COMBINE_RING_FUSED) && n > 1)
+  if ((combine == TP_COMBINE_RING || combine == TP_COMBINE_RING_FUSED || combine == TP_COMBINE_RING_SHARED) && n > 1)
     for (int32_t q = 0; q < n; ++q)
       if (y[q].ld != D) return TP_ERR_INVALID_ARG;  // the ring reduces contiguous buffers
   if (T > 0) {
@@ -851,6 +853,7 @@ extern "C" tp_status tp_moe_block(const tp_moe_dims *d, const tp_tensor *x, cons
   if ((st = moe_forward(c, s)) != TP_OK) return st;
   if (combine == TP_COMBINE_RING) return run_allreduce(n, y, TP_RING_STEPS, s);
   if (combine == TP_COMBINE_RING_FUSED) return run_allreduce(n, y, TP_RING_FUSED, s);
+  if (combine == TP_COMBINE_RING_SHARED) return run_allreduce(n, y, TP_RING_FUSED_SHARED, s);
   return TP_OK;
 }
 
@@ -865,7 +868,7 @@ extern "C" tp_status tp_ring_all_gather(int32_t n, tp_tensor *buf, int32_t mode,
 extern "C" tp_status tp_allreduce_ring(int32_t n, tp_tensor *buf, int32_t mode, tp_stream_t stream) {
   tp_status st = check_ring_bufs(n, buf);
   if (st != TP_OK) return st;
-  if (mode != TP_RING_STEPS && mode != TP_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if (mode != TP_RING_STEPS && mode != TP_RING_FUSED && mode != TP_RING_FUSED_SHARED) return TP_ERR_INVALID_ARG;
   if ((st = check_health(n)) != TP_OK) return st;
   return run_allreduce(n, buf, mode, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1014,7 +1017,7 @@ extern "C" tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const
   tp_dims d;
   if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
   if (!x || !w_gate || !w_up || !w_down || !y) return TP_ERR_INVALID_ARG;
-  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_SHARED) return TP_ERR_INVALID_ARG;
   tp_status st = check_gate_up(d, x, w_gate, w_up);
   if (st != TP_OK) return st;
   const int32_t n = d.tp_size;
@@ -1135,7 +1138,7 @@ extern "C" tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const
   tp_dims d;
   if (!plan || tp_plan_dims(plan, &d) != TP_OK) return TP_ERR_INVALID_ARG;
   if (!x || !w_q || !w_k || !w_v || !q || !k || !v || !a || !w_o || !y) return TP_ERR_INVALID_ARG;
-  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_FUSED) return TP_ERR_INVALID_ARG;
+  if (combine < TP_COMBINE_NONE || combine > TP_COMBINE_RING_SHARED) return TP_ERR_INVALID_ARG;
   const int32_t n = d.tp_size;
   const long long D = d.hidden, hd = d.head_dim, T = x->rows;
   tp_rank_shard s0;

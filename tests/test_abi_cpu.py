@@ -163,6 +163,9 @@ def test_collectives_reject_bad_arguments():
         assert st(fn, [good[0], T(FAKE + 1028, F32, 8, 8)]) == tp.TP_ERR_ALIGNMENT
         assert st(fn, [good[0], T(FAKE + 1024, F32, 8, 9)]) == tp.TP_ERR_INVALID_ARG
         assert st(fn, good + [good[0]], n=3) == tp.TP_ERR_TP_SIZE_NOT_POW2
+    # the shared-result mode exists for the all-reduce only
+    assert st("tp_reduce_scatter", good, mode=tp.TP_RING_FUSED_SHARED) == tp.TP_ERR_INVALID_ARG
+    assert st("tp_ring_all_gather", good, mode=tp.TP_RING_FUSED_SHARED) == tp.TP_ERR_INVALID_ARG
 
 
 def test_reduce_scatter_bf16_rejects_bad_arguments():

@@ -40,6 +40,21 @@ def test_allreduce_bit_exact(n, shape, mode):
         assert np.array_equal(host_bits_f32(dev[r]).reshape(-1), _bits(ref[r])), (n, shape, mode, r)
 
 
+@pytest.mark.parametrize("n", NS)
+@pytest.mark.parametrize("shape", SHAPES)
+def test_allreduce_shared_result_bit_exact(n, shape):
+    """The one-pass ring all-reduce with its result stored once: buf[0] holds the
+    oracle ring's sum bit for bit, buf[1..N-1] keep their partials."""
+    need_gpu()
+    host = _host_bufs(n, shape, seed=17 + n)
+    dev = [dev_f32(h) for h in host]
+    tp.tp_allreduce_ring(n, dev, tp.TP_RING_FUSED_SHARED)
+    ref = O.ring_all_reduce([h.reshape(-1) for h in host])
+    assert np.array_equal(host_bits_f32(dev[0]).reshape(-1), _bits(ref[0])), (n, shape)
+    for r in range(1, n):
+        assert np.array_equal(host_bits_f32(dev[r]).reshape(-1), _bits(host[r])), (n, shape, r)
+
+
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("n", [2, 4, 8])
 @pytest.mark.parametrize("shape", [(1, 7), (37, 101), (512, 2048)])
