@@ -214,45 +214,178 @@ def committed_traffic(workload: str):
 
 
 # ---- CPU baseline (the oracle as it stands) --------------------------------------------
-CPU_SNIPPET = r"""
-import json, os, sys, time
-sys.path.insert(0, sys.argv[1])
-import oracle as O
-from tensor_sharded_linear_gqa_gb300 import inputs
-w = dict(inputs.WORKLOADS[sys.argv[2]])
-budget, max_reps, rows = float(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5])
-d = inputs.make_bf16_inputs(w)
-f = {k: inputs.bf16_bits_to_f64(v) for k, v in d.items()}
-if rows <= 0:
-    # size the per-pass row sample so that one pass takes about -rows/1000 seconds
-    target = -rows / 1000.0
-    t0 = time.perf_counter()
-    O.mlp_sharded(f["x"][:32], f["wg"], f["wu"], f["wd"], w["tp"])
-    t32 = max(time.perf_counter() - t0, 1e-4)
-    rows = int(max(1, min(w["T"], 32 * target / t32)))
-x = f["x"][:rows]
-times = []
-t_all = time.perf_counter()
-while True:
-    t0 = time.perf_counter()
-    O.mlp_sharded(x, f["wg"], f["wu"], f["wd"], w["tp"])
-    times.append(time.perf_counter() - t0)
-    if time.perf_counter() - t_all >= budget or len(times) >= max_reps:
-        break
-print(json.dumps({"reps": len(times), "seconds": sum(times), "times": times, "rows": rows}))
-"""
+# Host bytes of operands the timed oracle may hold; a workload above it is not timed.
+CPU_HOLD_CAP = 16 << 30
 
 
-def cpu_oracle_run(workload: str, seconds: float, max_reps: int, rows: int) -> dict:
-    """Runs the fp64 oracle MLP block in a child process on every core this process may use.
-    rows > 0: that many token rows per pass; rows <= 0: sized so a pass takes -rows ms."""
+def oracle_work(w) -> str:
+    """What one oracle pass computes, for the sample description."""
+    kind = w["kind"]
+    if kind == "layer" and w.get("attention"):
+        return ("q/k/v column-parallel, causal attention core, o_proj row-parallel with its ring all-reduce, "
+                "then the MLP block")
+    return {"mlp": "column gate/up, SwiGLU, row down, ring all-reduce",
+            "attn": "q/k/v column-parallel, o_proj row-parallel, ring all-reduce",
+            "layer": "attention projections then the MLP block, each with its ring all-reduce",
+            "attn_core": "causal attention of every rank's q heads with the kv heads the plan gives them",
+            "moe": "every rank's share of the routed expert FFNs, ring all-reduce",
+            "vocab": "vocab-parallel lookup with its ring all-gather, then the LM-head logits",
+            "rs_column": "row-parallel partials, ring reduce-scatter rounded to bf16, column-parallel GEMM",
+            }[kind]
+
+
+def oracle_hold_bytes(w) -> int:
+    """Host bytes of the inputs the timed oracle keeps widened: fp64 weights and
+    activations, except the embedding table, kept as float32 (the oracle widens it
+    one shard at a time)."""
+    from tensor_sharded_linear_gqa_gb300 import inputs
+    total = 0
+    for name, shp in inputs.weight_shapes(w).items():
+        count = 1
+        for s in shp:
+            count *= s
+        total += count * (4 if name == "emb" else 8)
+    T, D = w["T"], w["hidden"]
+    total += 8 * T * D * 2
+    if w["kind"] == "attn_core":
+        total += 8 * T * (w["q_heads"] + 2 * w["kv_heads"]) * w["head_dim"]
+    return total
+
+
+def sample_flops(w, rows: int) -> float:
+    """Algorithmic flops of one pass over the first `rows` token rows (for causal
+    attention, the first `rows` queries with their keys: the same problem at T = rows)."""
+    return sum(f for f, _ in phase_costs(dict(w, T=rows), "ring_fused").values())
+
+
+def oracle_pass(w, moe_mode: str):
+    """The workload's inputs (the same seeded bits the GPU path reads, widened
+    exactly), and pass(rows): the oracle over the first `rows` token rows, which
+    returns the step's outputs (rank 0's copy where every rank holds the result).
+    Also returns p, the power of rows that a pass's cost grows with."""
+    import numpy as np
+
+    import oracle as O
+    from tensor_sharded_linear_gqa_gb300 import inputs
+
+    d = inputs.make_bf16_inputs(w)
+    f = {}
+    for k in list(d):
+        if d[k].dtype == np.uint16:
+            bits = d.pop(k)
+            f[k] = inputs.bf16_bits_to_f64(bits).astype(np.float32 if k == "emb" else np.float64)
+            del bits
+    n, kind = w["tp"], w["kind"]
+    hd = w.get("head_dim", 128)
+    plan = None
+    if kind in ("attn", "layer", "attn_core"):
+        plan = O.shard_plan(n, w["hidden"], w["q_heads"], w["kv_heads"], hd, w.get("ffn", 8 * n))
+
+    def mlp(x):
+        return O.mlp_sharded(x, f["wg"], f["wu"], f["wd"], n)["y"][0]
+
+    def attn_projections(x, rows):
+        r = O.attn_proj_sharded(x, f["wq"], f["wk"], f["wv"], f["a"][:rows], f["wo"], plan, hd)
+        return r["q"] + r["k"] + r["v"] + [r["y"][0]]
+
+    def attention_layer(x):
+        q = [O.linear(x, f["wq"][slice(*s.ranges["q_proj"])]) for s in plan]
+        k = [O.linear(x, f["wk"][slice(*s.ranges["k_proj"])]) for s in plan]
+        v = [O.linear(x, f["wv"][slice(*s.ranges["v_proj"])]) for s in plan]
+        att = O.attention_core_sharded(q, k, v, plan, hd, causal=True)
+        parts = [O.linear(att[r], f["wo"][:, slice(*s.ranges["o_proj"])]) for r, s in enumerate(plan)]
+        y = O.ring_all_reduce([p.reshape(-1) for p in parts])[0].reshape(x.shape[0], -1)
+        return q + k + v + att + [y]
+
+    if kind == "mlp":
+        return (lambda rows: [mlp(f["x"][:rows])]), 1
+    if kind == "attn":
+        return (lambda rows: attn_projections(f["x"][:rows], rows)), 1
+    if kind == "layer":
+        def layer(rows):
+            x = f["x"][:rows]
+            out = attention_layer(x) if w.get("attention") else attn_projections(x, rows)
+            return out + [mlp(x)]
+        return layer, 1
+    if kind == "attn_core":
+        def heads(t, rng):
+            return t[:, rng[0] * hd:rng[1] * hd]
+        qs = [heads(f["q"], s.q_heads) for s in plan]
+        ks = [heads(f["k"], s.kv_heads) for s in plan]
+        vs = [heads(f["v"], s.kv_heads) for s in plan]
+        return (lambda rows: O.attention_core_sharded([t[:rows] for t in qs], [t[:rows] for t in ks],
+                                                      [t[:rows] for t in vs], plan, hd, causal=True)), 2
+    if kind == "moe":
+        mode = O.MOE_WITHIN_EXPERT if moe_mode == "within_expert" else O.MOE_EXPERT_PARALLEL
+        ids, wts = d["topk_ids"], d["topk_w"].astype(np.float64)
+        return (lambda rows: O.moe_sharded(f["x"][:rows], ids[:rows], wts[:rows], f["eg"], f["eu"], f["ed"], n,
+                                           mode)["y"][:1]), 1
+    if kind == "vocab":
+        emb, wlm, ids = O.split_rows(f["emb"], n), O.split_rows(f["wlm"], n), d["ids"]
+
+        def vocab(rows):
+            return [O.vocab_parallel_embedding(ids[:rows], emb)["y"][0],
+                    O.vocab_parallel_lm_head(f["x"][:rows], wlm)["logits"]]
+        return vocab, 1
+    if kind == "rs_column":
+        wd, wqkv = O.split_cols(f["wd"], n), O.split_rows(f["wqkv"], n)
+
+        def rs_column(rows):
+            parts = O.row_parallel(O.split_cols(f["h"][:rows], n), wd)
+            return O.reduce_scatter_then_column(parts, wqkv, round_bf16=True)["y"]
+        return rs_column, 1
+    raise ValueError(f"no timed oracle pass for workload kind {kind}")
+
+
+def cpu_child(workload: str, moe_mode: str, budget: str, max_reps: str, rows: str) -> None:
+    """Child-process body of cpu_oracle_run: times oracle passes, prints one JSON line."""
+    from tensor_sharded_linear_gqa_gb300 import inputs
+    w = dict(inputs.WORKLOADS[workload])
+    budget, max_reps, rows = float(budget), int(max_reps), int(rows)
+    one_pass, power = oracle_pass(w, moe_mode)
+    if rows <= 0:
+        # Size the row sample so that one pass takes about -rows/1000 seconds: fit
+        # cost = a + b * rows**power through two timed probes after a warm-up pass
+        # (a is the part of a pass that does not grow with the rows).
+        target = -rows / 1000.0
+        r1, r2 = min(w["T"], 8), min(w["T"], 32)
+        one_pass(r1)
+        cost = []
+        for r in (r1, r2):
+            t0 = time.perf_counter()
+            one_pass(r)
+            cost.append(time.perf_counter() - t0)
+        b = (cost[1] - cost[0]) / (r2 ** power - r1 ** power) if r2 > r1 else 0.0
+        a = cost[0] - b * r1 ** power
+        if b <= 0.0:  # the probes did not resolve a slope: scale the larger one
+            rows = int(r2 * (target / max(cost[1], 1e-4)) ** (1.0 / power))
+        elif target <= a:
+            rows = r1
+        else:
+            rows = int(((target - a) / b) ** (1.0 / power))
+    rows = max(1, min(w["T"], rows))
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        one_pass(rows)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all >= budget or len(times) >= max_reps:
+            break
+    print(json.dumps({"reps": len(times), "seconds": sum(times), "times": times, "rows": rows}))
+
+
+def cpu_oracle_run(workload: str, moe_mode: str, seconds: float, max_reps: int, rows: int) -> dict:
+    """Runs the fp64 oracle over a workload in a child process on every core this
+    process may use. rows > 0: that many token rows per pass (at most T); rows <= 0:
+    sized so that a pass takes about -rows ms."""
     cores = len(os.sched_getaffinity(0))
     env = dict(os.environ)
     for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(cores)
-    out = subprocess.run([sys.executable, "-c", CPU_SNIPPET, ROOT, workload, str(seconds),
-                          str(max_reps), str(rows)], capture_output=True, text=True, env=env,
-                         timeout=1800)
+    code = "import sys; sys.path.insert(0, sys.argv[1]); import bench; bench.cpu_child(*sys.argv[2:])"
+    out = subprocess.run([sys.executable, "-c", code, ROOT, workload, moe_mode, str(seconds), str(max_reps),
+                          str(rows)], capture_output=True, text=True, env=env, timeout=1800)
     if out.returncode != 0:
         raise RuntimeError(out.stderr[-2000:])
     r = json.loads(out.stdout.strip().splitlines()[-1])
@@ -260,15 +393,28 @@ def cpu_oracle_run(workload: str, seconds: float, max_reps: int, rows: int) -> d
     return r
 
 
-def cpu_baseline(w, workload: str, seconds: float) -> dict:
-    rows = w["T"]
-    r = cpu_oracle_run(workload, seconds, 1000, rows)
-    fl = mlp_flops(dict(w, T=r["rows"]))["total"]
-    val = fl * r["reps"] / r["seconds"] / 1e12
+def cpu_too_large(w):
+    """The reason the oracle is not timed on a workload, or None."""
+    need = oracle_hold_bytes(w)
+    if need > CPU_HOLD_CAP:
+        return (f"the oracle would hold {need / 2**30:.1f} GiB of widened inputs on the host "
+                f"(cap {CPU_HOLD_CAP / 2**30:.0f} GiB)")
+    return None
+
+
+def cpu_baseline(w, workload: str, moe_mode: str, seconds: float) -> dict:
+    """The oracle as it stands, timed for about `seconds` on a bounded row sample
+    (whole passes when a pass over all T rows takes under a quarter of that)."""
+    why = cpu_too_large(w)
+    if why:
+        return {"unavailable": why}
+    r = cpu_oracle_run(workload, moe_mode, seconds, 1000, -int(seconds * 250))
+    rows = r["rows"]
+    val = sample_flops(w, rows) * r["reps"] / r["seconds"] / 1e12
+    what = "full passes" if rows == w["T"] else f"passes over {rows} of its {w['T']} token rows"
     return {"value": round(val, 6), "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
-            "sample": f"{r['reps']} full passes of the fp64 oracle MLP block (T={r['rows']}, "
-                      f"D={w['hidden']}, F={w['ffn']}, TP={w['tp']}: column gate/up, SwiGLU, "
-                      f"row down, ring all-reduce) in {r['seconds']:.1f} s"}
+            "sample": f"{r['reps']} {what} of the fp64 oracle on {workload} ({oracle_work(w)}) "
+                      f"in {r['seconds']:.1f} s"}
 
 
 # ---- native arm ----------------------------------------------------------------------
@@ -883,9 +1029,9 @@ def run_native(args):
         raise SystemExit(f"device status {word:#x} after the end-to-end runs")
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and w["kind"] == "mlp":
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            cpu = cpu_baseline(w, args.workload, args.cpu_seconds)
+            cpu = cpu_baseline(w, args.workload, args.moe_mode, args.cpu_seconds)
         except Exception as exc:  # reported, not fatal
             cpu = {"error": str(exc)[-300:]}
 
@@ -947,29 +1093,35 @@ def run_reference(args):
         return
     from tensor_sharded_linear_gqa_gb300 import inputs
     w = inputs.WORKLOADS[args.workload]
-    if w["kind"] != "mlp":
-        print(json.dumps({"impl": "reference", "unavailable": "the timed oracle arm covers the MLP block "
-                                                              f"workloads; {args.workload} is a {w['kind']} workload"}),
-              flush=True)
+    if w["kind"] == "linear_fp32":
+        raise SystemExit("bench.py times the bf16 block workloads")
+    why = cpu_too_large(w)
+    if why:
+        print(json.dumps({"impl": "reference", "unavailable": why}), flush=True)
         return
     K, W = args.steps, max(args.warmup, 0)
     # Each step is a row sample of the workload sized so that all K + W steps take
     # about two minutes on the host cores.
     per_step_ms = max(5.0, 120_000.0 / (K + W))
-    r = cpu_oracle_run(args.workload, 1e9, K + W, -int(per_step_ms))
+    r = cpu_oracle_run(args.workload, args.moe_mode, 1e9, K + W, -int(per_step_ms))
     times = r["times"][W:] or r["times"]
     per_step = sum(times) / len(times)
     rows = r["rows"]
-    value = mlp_flops(dict(w, T=rows))["total"] / per_step / 1e12
-    sample = (f"{rows} of {w['T']} token rows of {args.workload} per step (fp64 oracle: column "
-              f"gate/up, SwiGLU, row down, ring all-reduce), {len(times)} timed passes")
+    value = sample_flops(w, rows) / per_step / 1e12
+    sample = (f"{rows} of {w['T']} token rows of {args.workload} per step (fp64 oracle: {oracle_work(w)}), "
+              f"{len(times)} timed passes")
+    config = {"workload": args.workload, "tokens": w["T"], "hidden": w["hidden"], "tp_size": w["tp"],
+              "rows_per_step": rows}
+    for key in ("ffn", "q_heads", "kv_heads", "head_dim", "experts", "top_k", "vocab"):
+        if key in w:
+            config[key] = w[key]
+    if w["kind"] == "moe":
+        config["moe_mode"] = args.moe_mode
     line = {"metric": "TP MLP/attn-proj block TFLOP/s and combine GB/s on 1 GB300, % of roofline",
             "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": len(times),
             "warmup": W, "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "tokens": w["T"], "hidden": w["hidden"],
-                       "ffn": w["ffn"], "tp_size": w["tp"], "rows_per_step": rows},
-            "impl": "reference",
+            "config": config, "impl": "reference",
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": r["cores"],
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

@@ -74,14 +74,14 @@ WORKLOADS = {
     # logits of 4096 hidden states are computed over the whole vocabulary.
     "vocab_tp8_t4096": dict(kind="vocab", T=4096, hidden=8192, vocab=128256, tp=8,
                             seed=107, w_std=0.02),
-    # Mixtral-8x7B-shaped MoE layer: 8 experts of hidden 4096 and FFN 14336, top-2
-    # routing drawn uniformly (two distinct experts a token, softmax weights over
-    # the two), 4096 tokens, TP=8; within-expert sharding (F/N = 1792 per rank).
     # Attention core of the prefill layer: causal attention of 4096 tokens,
     # 64 q heads and 8 kv heads of 128 over 8 ranks (8 q heads and 1 kv head
     # each); Q, K, V drawn N(0,1).
     "attn_core_tp8_t4096": dict(kind="attn_core", T=4096, hidden=8192, q_heads=64, kv_heads=8,
                                 head_dim=128, tp=8, seed=109),
+    # Mixtral-8x7B-shaped MoE layer: 8 experts of hidden 4096 and FFN 14336, top-2
+    # routing drawn uniformly (two distinct experts a token, softmax weights over
+    # the two), 4096 tokens, TP=8; within-expert sharding (F/N = 1792 per rank).
     "moe_mixtral_tp8_t4096": dict(kind="moe", T=4096, hidden=4096, ffn=14336, experts=8, top_k=2,
                                   tp=8, seed=108, w_std=0.02),
 }
