@@ -68,7 +68,8 @@ typedef enum tp_status {
 typedef enum tp_dtype { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
 
 /* A 2-D row-major view: element (i, j) lives at ptr + (i * ld + j) * size(dtype).
- * ld >= cols. rows or cols may be 0 (empty). */
+ * ld >= cols. rows or cols may be 0 (empty); each is below 2^31 (their product,
+ * and ld, are not limited). */
 typedef struct tp_tensor {
   void *ptr;
   int32_t dtype; /* tp_dtype */

@@ -26,9 +26,14 @@ int g_sm_count[64] = {0};
 
 size_t esize(int32_t dt) { return dt == TP_F32 ? 4 : (dt == TP_BF16 ? 2 : 0); }
 
+// Rows and columns each fit a 32-bit signed index (GEMM tile coordinates and TMA
+// box coordinates are 32-bit); element counts and offsets are 64-bit throughout.
+constexpr long long kMaxDim = 0x7fffffffLL;
+
 bool shape_ok(const tp_tensor &t) {
   if (esize(t.dtype) == 0) return false;
   if (t.rows < 0 || t.cols < 0 || t.ld < t.cols || t.ld < 1) return false;
+  if (t.rows > kMaxDim || t.cols > kMaxDim) return false;
   if (t.rows > 0 && t.cols > 0 && t.ptr == nullptr) return false;
   return true;
 }

@@ -405,6 +405,17 @@ def test_every_call_takes_zero_tokens():
         assert tp.raw_status("tp_row_linear", n, arr(*xs), arr(*ws), arr(*ys), ring, None) == tp.TP_ERR_CUDA
 
 
+def test_dimensions_fit_32_bit_indices():
+    # rows and cols each below 2^31 (GEMM and TMA coordinates are 32-bit)
+    big = 1 << 31
+    w = [T(FAKE, BF, 32, 128), T(FAKE + (1 << 24), BF, 32, 128)]
+    assert col_status(2, T(FAKE, BF, big, 128), w, [T(FAKE, BF, big, 64)] * 2, gather=0) == tp.TP_ERR_INVALID_ARG
+    assert col_status(2, T(FAKE, BF, 64, big), [T(FAKE, BF, 32, big)] * 2, [T(FAKE, BF, 64, 64)]) == \
+        tp.TP_ERR_INVALID_ARG
+    flat = [T(FAKE, F32, big, 1), T(FAKE + (1 << 36), F32, big, 1)]
+    assert tp.raw_status("tp_allreduce_ring", 2, arr(*flat), 0, None) == tp.TP_ERR_INVALID_ARG
+
+
 def test_wait_budget_argument():
     assert tp.raw_status("tp_set_wait_budget", -1) == tp.TP_ERR_INVALID_ARG
     assert tp.raw_status("tp_set_wait_budget", 0) == tp.TP_OK
