@@ -57,7 +57,10 @@ def parse_args():
                    help="MoE sharding of the moe workloads")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="host seconds of the CPU baseline timed beside the native arm")
+    p.add_argument("--reference-seconds", type=float, default=120.0,
+                   help="host seconds that all steps of --impl reference take together")
     return p.parse_args()
 
 
@@ -1101,8 +1104,8 @@ def run_reference(args):
         return
     K, W = args.steps, max(args.warmup, 0)
     # Each step is a row sample of the workload sized so that all K + W steps take
-    # about two minutes on the host cores.
-    per_step_ms = max(5.0, 120_000.0 / (K + W))
+    # about --reference-seconds (two minutes by default) on the host cores.
+    per_step_ms = max(5.0, 1000.0 * args.reference_seconds / (K + W))
     r = cpu_oracle_run(args.workload, args.moe_mode, 1e9, K + W, -int(per_step_ms))
     times = r["times"][W:] or r["times"]
     per_step = sum(times) / len(times)
