@@ -59,6 +59,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="host seconds of the CPU baseline timed beside the native arm")
+    p.add_argument("--clocks-csv", default=None,
+                   help="file for the nvidia-smi clock samples of the timed region, {rank} replaced by the "
+                        "rank (default: a temporary file)")
     p.add_argument("--reference-seconds", type=float, default=120.0,
                    help="host seconds that all steps of --impl reference take together")
     return p.parse_args()
@@ -727,11 +730,12 @@ def run_native(args):
     K = args.steps
     nev = len(names) + 1
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    out_dir = os.path.join(ROOT, "gpurun_out")
-    if not os.path.isdir(out_dir):
+    if args.clocks_csv:
+        clock_path = args.clocks_csv.replace("{rank}", str(rank))
+    else:
         import tempfile
-        out_dir = tempfile.gettempdir()
-    clock_path = os.path.join(out_dir, f"clocks_rank{rank}.csv")
+        fd, clock_path = tempfile.mkstemp(prefix=f"clocks_rank{rank}_", suffix=".csv")
+        os.close(fd)
     with ClockSampler(local, clock_path) as clk:
         barrier(world)
         torch.cuda.synchronize(dev)
