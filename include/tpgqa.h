@@ -61,7 +61,7 @@ typedef enum tp_status {
   TP_ERR_TIMEOUT = 8,          /* a bounded device-side wait ran out                 */
   TP_ERR_CUDA = 9,             /* a CUDA runtime call failed; see tp_last_cuda_error */
   TP_ERR_WORKSPACE = 10,       /* workspace missing or too small                     */
-  TP_ERR_UNSUPPORTED = 11,     /* valid request this build does not implement        */
+  TP_ERR_UNSUPPORTED = 11,     /* valid request the library does not implement       */
   TP_ERR_BAD_TOKEN = 12        /* an embedding lookup met a token id outside [0, V)  */
 } tp_status;
 
