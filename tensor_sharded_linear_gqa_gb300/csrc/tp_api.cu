@@ -77,9 +77,16 @@ tp_status check_ring_bufs(int32_t n, const tp_tensor *buf) {
     if (buf[r].rows != buf[0].rows || buf[r].cols != buf[0].cols) return TP_ERR_INVALID_ARG;
     if (buf[r].rows > 1 && buf[r].ld != buf[r].cols) return TP_ERR_INVALID_ARG;
     if (buf[r].rows * buf[r].cols > 0 && !aligned16(buf[r].ptr)) return TP_ERR_ALIGNMENT;
-    for (int32_t q = 0; q < r; ++q)
-      if (buf[q].ptr == buf[r].ptr && buf[r].rows * buf[r].cols > 0) return TP_ERR_INVALID_ARG;
   }
+  // Every rank's buffer is written by the ring: byte ranges that share even one
+  // element would race, so any overlap of two ranks' ranges is rejected.
+  const uintptr_t bytes = static_cast<uintptr_t>(buf[0].rows * buf[0].cols) * 4u;
+  if (bytes == 0) return TP_OK;
+  for (int32_t r = 0; r < n; ++r)
+    for (int32_t q = 0; q < r; ++q) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(buf[q].ptr), b = reinterpret_cast<uintptr_t>(buf[r].ptr);
+      if (a < b + bytes && b < a + bytes) return TP_ERR_INVALID_ARG;
+    }
   return TP_OK;
 }
 

@@ -150,6 +150,23 @@ def test_row_linear_rejects_bad_arguments():
     # ring combine needs distinct, contiguous buffers
     assert st(xs, ws, [ys[0], ys[0]], tp.TP_COMBINE_RING) == tp.TP_ERR_INVALID_ARG
     assert st(xs, ws, [T(FAKE, F32, 64, 128, 256), ys[1]], tp.TP_COMBINE_RING) == tp.TP_ERR_INVALID_ARG
+    # ranges that share elements would race in the ring: a second buffer four
+    # floats into the first (aligned, distinct base) is rejected as well
+    far = [T(FAKE, F32, 64, 128), T(FAKE + 64 * 128 * 4, F32, 64, 128)]
+    for combine in (tp.TP_COMBINE_RING, tp.TP_COMBINE_RING_FUSED, tp.TP_COMBINE_RING_SHARED):
+        assert st(xs, ws, [far[0], T(FAKE + 16, F32, 64, 128)], combine) == tp.TP_ERR_INVALID_ARG
+        assert st(xs, ws, [T(FAKE + 64 * 128 * 4 - 16, F32, 64, 128), far[0]], combine) == tp.TP_ERR_INVALID_ARG
+
+
+def test_collectives_reject_overlapping_rank_buffers():
+    def st(fn, bufs, mode=0, n=2):
+        return tp.raw_status(fn, n, arr(*bufs), mode, None)
+    a = T(FAKE, F32, 8, 8)                   # 256 bytes
+    for fn in ("tp_reduce_scatter", "tp_ring_all_gather", "tp_allreduce_ring"):
+        assert st(fn, [a, T(FAKE + 16, F32, 8, 8)]) == tp.TP_ERR_INVALID_ARG
+        assert st(fn, [T(FAKE + 240, F32, 8, 8), a]) == tp.TP_ERR_INVALID_ARG
+        four = [a, T(FAKE + 256, F32, 8, 8), T(FAKE + 512, F32, 8, 8), T(FAKE + 752, F32, 8, 8)]
+        assert st(fn, four, n=4) == tp.TP_ERR_INVALID_ARG   # the last two share one float4
 
 
 def test_collectives_reject_bad_arguments():

@@ -245,3 +245,123 @@ def test_prefill_layer_tp8_t4096_sampled_rows():
     ys, h = L.mlp(tp.TP_COMBINE_FUSED)
     ref = O.mlp_sharded(f["x"][rows], f["wg"], f["wu"], f["wd"], L.n)
     assert_close(host_f64(ys[0])[rows], ref["y"][0], BF16_TOL, "MLP Y")
+
+
+# ---- the benchmarked layers at their full size ----------------------------------------
+def _sampled_rows(w, count=64):
+    return np.sort(inputs.rng(w["seed"], 99).choice(w["T"], size=count, replace=False))
+
+
+_ring_fused_bits = {}
+
+
+@pytest.mark.parametrize("combine", [tp.TP_COMBINE_RING, tp.TP_COMBINE_RING_SHARED])
+def test_prefill_layer_tp8_t4096_ring_modes(combine):
+    """The step-by-step ring (N-1 reduce-scatter and N-1 all-gather launches) and the
+    ring whose result is stored once, on the benchmarked prefill layer (8 ranks, 128 MiB
+    f32 partials per rank): both blocks against the oracle on 64 sampled rows, and bit
+    for bit against TP_COMBINE_RING_FUSED, which folds every chunk in the same ring
+    order (mlxcel manual "텐서 병렬화", 통신 패턴: reduce-scatter then all-gather,
+    rank r sending to (r+1) % N)."""
+    need_gpu()
+    L, f = layer("prefill_layer_tp8_t4096")
+    rows = _sampled_rows(L.w, L.w["oracle_rows"])
+    if not _ring_fused_bits:
+        _q, _k, _v, ya = L.attn(tp.TP_COMBINE_RING_FUSED)
+        _ring_fused_bits["attn"] = host_bits_f32(ya[0])
+        del ya
+        ym, _h = L.mlp(tp.TP_COMBINE_RING_FUSED)
+        _ring_fused_bits["mlp"] = host_bits_f32(ym[0])
+        del ym
+    copies = L.n if combine == tp.TP_COMBINE_RING else 1
+    plan = _oracle_plan(L.w)
+    _q, _k, _v, ya = L.attn(combine)
+    ref = O.attn_proj_sharded(f["x"][rows], f["wq"], f["wk"], f["wv"], f["a"][rows], f["wo"], plan,
+                              L.w["head_dim"])
+    for r in range(copies):
+        assert np.array_equal(host_bits_f32(ya[r]), _ring_fused_bits["attn"]), f"attention rank {r}"
+    assert_close(host_f64(ya[0])[rows], ref["y"][0], BF16_TOL, "attn Y")
+    del ya, _q, _k, _v
+    ym, _h = L.mlp(combine)
+    for r in range(copies):
+        assert np.array_equal(host_bits_f32(ym[r]), _ring_fused_bits["mlp"]), f"MLP rank {r}"
+    ref = O.mlp_sharded(f["x"][rows], f["wg"], f["wu"], f["wd"], L.n)
+    assert_close(host_f64(ym[0])[rows], ref["y"][0], BF16_TOL, "MLP Y")
+
+
+_decoder_ref = {}
+
+
+def _decoder_oracle(w, f, rows):
+    """The decoder layer on the sampled rows, in the oracle: q/k/v column-parallel
+    per rank, causal attention of each sampled query over the keys of every earlier
+    token (keys and values of all T rows), o_proj row-parallel with the ring
+    all-reduce, then the MLP block on the same input rows."""
+    hd, n = w["head_dim"], w["tp"]
+    plan = _oracle_plan(w)
+    q, k, v, att = [], [], [], []
+    for s in plan:
+        q.append(O.linear(f["x"][rows], f["wq"][slice(*s.ranges["q_proj"])]))
+        k.append(O.linear(f["x"], f["wk"][slice(*s.ranges["k_proj"])]))
+        v.append(O.linear(f["x"], f["wv"][slice(*s.ranges["v_proj"])]))
+        a = np.empty_like(q[-1])
+        for h, g in enumerate(s.q_to_kv):
+            kh, vh = k[-1][:, g * hd:(g + 1) * hd], v[-1][:, g * hd:(g + 1) * hd]
+            for j, i in enumerate(rows):
+                a[j, h * hd:(h + 1) * hd] = O.attention_head(q[-1][j:j + 1, h * hd:(h + 1) * hd], kh[:i + 1],
+                                                             vh[:i + 1], causal=False)[0]
+        att.append(a)
+    parts = [O.linear(att[r], f["wo"][:, slice(*plan[r].ranges["o_proj"])]) for r in range(n)]
+    y_o = O.ring_all_reduce([p.reshape(-1) for p in parts])[0].reshape(len(rows), -1)
+    y_mlp = O.mlp_sharded(f["x"][rows], f["wg"], f["wu"], f["wd"], n)["y"][0]
+    return {"q": q, "k": [t[rows] for t in k], "v": [t[rows] for t in v], "a": att, "y_o": y_o, "y_mlp": y_mlp}
+
+
+@pytest.mark.parametrize("combine", [tp.TP_COMBINE_RING_FUSED, tp.TP_COMBINE_FUSED, tp.TP_COMBINE_RING_SHARED])
+def test_decoder_layer_tp8_t4096_sampled_rows(combine):
+    """The whole benchmarked decoder layer (T=4096, D=8192, 64 q / 8 kv heads, F=28672,
+    TP=8) through the public calls, as the benchmark chains them: tp_qkv_proj, the causal
+    tp_attn_core into the o_proj input, tp_row_linear with the combine, tp_mlp_block.
+    Checked on 64 seeded rows: q/k/v, the attention output, the o_proj result and the
+    MLP result against the oracle's chain of the same steps (mlxcel manual "텐서 병렬화",
+    아키텍처 인식 샤드 플랜 and GQA 인식 어텐션 샤딩)."""
+    need_gpu()
+    t = torch()
+    w = inputs.WORKLOADS["decoder_layer_tp8_t4096"]
+    L, f = layer("decoder_layer_tp8_t4096")
+    n, T, D, hd = L.n, L.T, w["hidden"], w["head_dim"]
+    rows = _sampled_rows(w)
+    if not _decoder_ref:
+        _decoder_ref.update(_decoder_oracle(w, f, rows))
+    ref = _decoder_ref
+    rep = L.shards[0]["kv_replicated"]
+    nkv = 1 if rep else n
+    wq = [L.dev["wq"][slice(*L.rng(r, "q_proj"))] for r in range(n)]
+    wk = [L.dev["wk"][slice(*L.rng(r, "k_proj"))] for r in range(nkv)]
+    wv = [L.dev["wv"][slice(*L.rng(r, "v_proj"))] for r in range(nkv)]
+    wo = [L.dev["wo"][:, slice(*L.rng(r, "o_proj"))] for r in range(n)]
+    q = [t.empty((T, x.shape[0]), dtype=t.bfloat16, device="cuda") for x in wq]
+    k = [t.empty((T, x.shape[0]), dtype=t.bfloat16, device="cuda") for x in wk]
+    v = [t.empty((T, x.shape[0]), dtype=t.bfloat16, device="cuda") for x in wv]
+    a = t.full((T, w["q_heads"] * hd), float("nan"), dtype=t.bfloat16, device="cuda")
+    a_r = [a[:, slice(*L.rng(r, "o_proj"))] for r in range(n)]
+    yo = [t.full((T, D), float("nan"), device="cuda") for _ in range(1 if combine == tp.TP_COMBINE_FUSED else n)]
+    ws = t.empty(tp.tp_attn_core_workspace_size(L.plan, T), dtype=t.uint8, device="cuda")
+    tp.tp_qkv_proj(L.plan, L.x, wq, wk, wv, q, k, v)
+    tp.tp_attn_core(L.plan, q, k, v, a_r, True, ws)
+    tp.tp_row_linear(n, a_r, wo, yo, combine)
+    t.cuda.synchronize()
+    assert tp.tp_device_status() == (tp.TP_OK, 0)
+    for r in range(n):
+        assert_close(host_f64(q[r])[rows], ref["q"][r], BF16_TOL, f"q[{r}]")
+        assert_close(host_f64(a_r[r])[rows], ref["a"][r], BF16_TOL, f"attention output of rank {r}")
+    for r in range(nkv):
+        assert_close(host_f64(k[r])[rows], ref["k"][r], BF16_TOL, f"k[{r}]")
+        assert_close(host_f64(v[r])[rows], ref["v"][r], BF16_TOL, f"v[{r}]")
+    copies = 1 if combine in (tp.TP_COMBINE_FUSED, tp.TP_COMBINE_RING_SHARED) else n
+    for r in range(copies):
+        assert_close(host_f64(yo[r])[rows], ref["y_o"], BF16_TOL, f"o_proj Y, rank {r}")
+    del q, k, v, a, a_r, yo, ws
+    ym, _h = L.mlp(combine)
+    for r in range(copies):
+        assert_close(host_f64(ym[r])[rows], ref["y_mlp"], BF16_TOL, f"MLP Y, rank {r}")
