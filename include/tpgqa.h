@@ -176,12 +176,22 @@ typedef enum tp_combine {
                                 shards 0..N-1 in order; no partial is written              */
   TP_COMBINE_RING = 2,       /* y[r] = P_r, then the ring all-reduce as N-1 reduce-scatter and
                                 N-1 all-gather step launches; every y[r] ends equal to the sum */
-  TP_COMBINE_RING_FUSED = 3, /* as TP_COMBINE_RING, one pass that folds the partials in the
+  TP_COMBINE_RING_FUSED = 3, /* as TP_COMBINE_RING, the partials folded in one pass in the
                                 ring's order (bit-identical to TP_COMBINE_RING)            */
   TP_COMBINE_RING_SHARED = 4 /* as TP_COMBINE_RING_FUSED, with the result stored once, in
                                 y[0] (bit-identical to it): for ranks that share one output
-                                on this device; y[1..N-1] keep their partials              */
+                                on this device; y[1..N-1] are scratch, unspecified after   */
 } tp_combine;
+/* With bf16 inputs, RING_FUSED and RING_SHARED fold the ring into the GEMM when
+ * every 256-row tile lies inside one ring chunk (T % N == 0, T/N a multiple of
+ * 256, more than 128 tokens, an output width n that is a multiple of 4 with
+ * y[r].ld == n, N <= 16, and a shape that the
+ * GEMM without a combine runs without split-K): each rank's partial is computed
+ * exactly as TP_COMBINE_NONE computes it, then added in its chunk's ring order
+ * in the epilogue, so no partial is written and no second pass runs. The bits
+ * are those of the GEMM followed by the one-pass ring. Other shapes run the GEMM
+ * and then the one-pass ring. The environment variable TPGQA_RING_EPILOGUE=0
+ * (read on every call) turns the fold off. */
 
 /* Row-parallel linear: P_r = X_r * W_r^T, then the combine above.
  *  x[r] : [T x k_r] (rank r's slice of the input features), bf16 or f32.
@@ -526,6 +536,12 @@ tp_status tp_set_wait_budget(int64_t nanoseconds);
  * device status word and returns. Used to test the timeout path without a
  * GPU fault or hang. */
 tp_status tp_debug_wait_timeout(tp_stream_t stream);
+
+/* Kernel launches this library has enqueued in this process so far, on every
+ * stream and device (each successful kernel launch of every call counts one;
+ * memsets and copies do not count). A caller reads it before and after a region
+ * of work to count that region's launches. Never fails. */
+uint64_t tp_launch_count(void);
 
 /* Library version string. */
 const char *tp_version(void);

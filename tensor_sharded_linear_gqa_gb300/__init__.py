@@ -116,6 +116,7 @@ _SIGS = {
     "tp_device_status": ([_S, _P(ctypes.c_int32)], ctypes.c_int),
     "tp_set_wait_budget": ([ctypes.c_int64], ctypes.c_int),
     "tp_debug_wait_timeout": ([_S], ctypes.c_int),
+    "tp_launch_count": ([], ctypes.c_uint64),
     "tp_version": ([], ctypes.c_char_p),
 }
 EXPORTED = tuple(_SIGS)
@@ -428,6 +429,11 @@ def tp_set_wait_budget(nanoseconds: int) -> None:
 
 def tp_debug_wait_timeout(stream=None) -> None:
     _check(_lib.tp_debug_wait_timeout(_stream(stream)), "tp_debug_wait_timeout")
+
+
+def tp_launch_count() -> int:
+    """Kernel launches the library has enqueued in this process so far."""
+    return int(_lib.tp_launch_count())
 
 
 def tp_version() -> str:

@@ -427,6 +427,7 @@ tp_status launch_debug_wait(cudaStream_t s) {
   const cudaError_t e = get_dev_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e);
   k_debug_wait<<<1, 32, 0, s>>>(ctx.status, ctx.wait_ns);
+  note_launch();
   return check_launch();
 }
 

@@ -804,6 +804,293 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Ring-folding row-parallel pair kernel: the row-parallel GEMM and the ring
+// all-reduce of its partials in one pass (mlxcel manual "텐서 병렬화", 통신 패턴:
+// the reduced chunk c is the fold x_{c+1} + x_{c+2} + ... + x_c of the ranks'
+// partials, indices mod N). One problem holds the N ranks' K slices as
+// segments. Each 256 x BN tile lies inside one ring chunk c; its SM pair runs
+// the segments in that chunk's fold order, rank c+1 first, each from a zeroed
+// accumulator, so every per-rank partial has exactly the bits the GEMM without
+// a combine writes (same tile width, same k-stage sequence). The epilogue adds
+// each partial to the running sum in TMEM in the same order as the one-pass
+// ring kernel adds them, then stores the sum to every rank's output (or to
+// y[0] alone) with TMA stores. The result is bit-identical to the GEMM
+// followed by the ring, and no partial ever reaches global memory.
+//
+// TMEM holds two 256-column regions. Tile jt of this pair keeps its running
+// sum in region jt & 1 (the first partial lands there directly) and receives
+// the later partials in the other region; after the last add the sum is
+// written back to its region, the partial's region goes back to the MMA warp
+// (it becomes the next tile's sum region) and the stores drain from the sum
+// region while the next tile's first partial is computed.
+// ---------------------------------------------------------------------------
+constexpr int kRingStagingBytes = 4 * 2 * 32 * 128;  // 4 epilogue warps x 2 buffers x [32 rows x 128 B]
+
+template <int KSUB, int BN>
+struct PairRingCfg {
+  using PC = PairCfg<KSUB, BN>;
+  static constexpr int kSmem = 1024 + PC::kStages * PC::kStageBytes + kRingStagingBytes + 256;
+  static_assert(kSmem <= kSmemLimit, "stages, staging buffers and barriers fit in shared memory");
+  static_assert(PC::kStageBytes % 1024 == 0, "staging buffers keep the 1024-byte swizzle alignment");
+};
+
+template <int KSUB, int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_bf16_pair_ring(const __grid_constant__ GemmParams p) {
+  using PC = PairCfg<KSUB, BN>;
+  constexpr int S = PC::kStages;
+  constexpr int kHalfB = PC::kBRows;  // B rows per CTA
+  constexpr int kPairBBytes = PC::kBBytes;
+  constexpr uint32_t kTmemCols = 512;  // two regions, at columns 0 and 256
+  constexpr int kChunks = BN / 32;
+  static_assert(BN % 32 == 0, "32-column epilogue chunks");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sA0 = ptx::smem_addr(smem);
+  const uint32_t sB0 = sA0 + S * KSUB * kPairABytes;
+  uint8_t *staging = smem + S * PC::kStageBytes;
+  uint8_t *bar_area = staging + kRingStagingBytes;
+  const uint32_t bar0 = ptx::smem_addr(bar_area);
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (S + i); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * (2 * S + 5));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * (2 * S + 5) + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = ptx::cluster_ctarank();  // 0 or 1 within the SM pair
+  const bool leader = crank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const GemmProblem &pr = p.prob[0];
+  const int nrank = pr.seg_count;
+  // The tile's ring chunk, and with it the rank whose partial comes s-th.
+  auto fold_rank = [&](int mt, int s) { return ((mt * 256) / p.ring_rows + 1 + s) % nrank; };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(full_bar(i), 1);
+      ptx::mbar_init(empty_bar(i), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < p.n_maps_used; ++i) ptx::prefetch_tensormap(&p.maps[i]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int kb = 0;
+      bool go = true;
+      for (int t = pair; go && t < p.total_tiles; t += npairs) {
+        const int mt = t % pr.m_tiles, nt = t / pr.m_tiles;
+        const int a_row = mt * 256 + static_cast<int>(crank) * 128;
+        const int b_row = nt * BN + static_cast<int>(crank) * kHalfB;
+        for (int s = 0; go && s < nrank; ++s) {
+          const GemmSeg &sg = p.seg[pr.seg_begin + fold_rank(mt, s)];
+          const int nst = seg_stages<KSUB>(sg);
+          for (int kt = 0; kt < nst; ++kt, ++kb) {
+            const int st = kb % S;
+            const uint32_t ph = (kb / S) & 1;
+            if (*abort_flag) { go = false; break; }
+            if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
+              record(p.status, kDevTimeoutProducer);
+              *abort_flag = 1;
+              go = false;
+              break;
+            }
+            const uint32_t lead_full = ptx::mapa_shared(full_bar(st), 0);
+            if (leader) ptx::mbar_arrive_expect_tx(full_bar(st), 2 * PC::kStageBytes);
+            if (p.box_kt > 1) {
+              ptx::tma_load_3d_pair(sA0 + st * KSUB * kPairABytes, &p.maps[sg.a_map], 0, a_row, kt * KSUB,
+                                    lead_full);
+              ptx::tma_load_3d_pair(sB0 + st * KSUB * kPairBBytes, &p.maps[sg.b_map], 0, b_row, kt * KSUB,
+                                    lead_full);
+            } else {
+#pragma unroll
+              for (int j = 0; j < KSUB; ++j) {
+                const int x = (kt * KSUB + j) * BK;  // past the segment's K: zero fill
+                ptx::tma_load_2d_pair(sA0 + (st * KSUB + j) * kPairABytes, &p.maps[sg.a_map], x, a_row,
+                                      lead_full);
+                ptx::tma_load_2d_pair(sB0 + (st * KSUB + j) * kPairBBytes, &p.maps[sg.b_map], x, b_row,
+                                      lead_full);
+              }
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, BN);
+      int kb = 0;
+      uint32_t taken0 = 0, taken1 = 0;  // acquisitions of each TMEM region so far
+      bool ok = true;
+      for (int t = pair, jt = 0; ok && t < p.total_tiles; t += npairs, ++jt) {
+        const int mt = t % pr.m_tiles;
+        for (int s = 0; ok && s < nrank; ++s) {
+          const int reg = s == 0 ? (jt & 1) : ((jt & 1) ^ 1);
+          uint32_t &taken = reg ? taken1 : taken0;
+          if (*abort_flag || !ptx::mbar_wait(tempty_bar(reg), (taken & 1) ^ 1, p.wait_ns)) {
+            if (!*abort_flag) record(p.status, kDevTimeoutMma);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          ++taken;
+          ptx::tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(reg * 256);
+          const int nst = seg_stages<KSUB>(p.seg[pr.seg_begin + fold_rank(mt, s)]);
+          for (int k0 = 0; k0 < nst; ++k0, ++kb) {
+            const int st = kb % S;
+            const uint32_t ph = (kb / S) & 1;
+            if (*abort_flag) { ok = false; break; }
+            if (!ptx::mbar_wait(full_bar(st), ph, p.wait_ns)) {
+              record(p.status, kDevTimeoutMma);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < KSUB; ++j) {
+              const uint64_t ad = ptx::smem_desc_sw128(sA0 + (st * KSUB + j) * kPairABytes);
+              const uint64_t bd = ptx::smem_desc_sw128(sB0 + (st * KSUB + j) * kPairBBytes);
+#pragma unroll
+              for (int k = 0; k < BK / UMMA_K; ++k)
+                ptx::mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (k0 | j | k) != 0 ? 1u : 0u);
+            }
+            ptx::mma_commit_pair_multicast(empty_bar(st), 0x3);
+          }
+          if (!ok) break;
+          ptx::mma_commit_pair_multicast(tfull_bar(reg), 0x3);
+        }
+      }
+      ptx::mma_commit_pair_multicast(drain_bar, 0x1);
+      if (!ptx::mbar_wait(drain_bar, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    }
+  } else {
+    // ---- epilogue: warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32): rows of this CTA ----
+    const int q = warp & 3;
+    uint8_t *mine = staging + q * (2 * 32 * 128);  // this warp's two [32 x 128 B] buffers
+    uint32_t seen0 = 0, seen1 = 0;  // completions of each region consumed so far
+    const uint32_t lead_tempty0 = ptx::mapa_shared(tempty_bar(0), 0);
+    const uint32_t lead_tempty1 = ptx::mapa_shared(tempty_bar(1), 0);
+    int groups = 0;  // bulk store groups this warp has committed (lane 0 issues them)
+    bool alive = true;
+    auto await = [&](int reg) {
+      uint32_t &seen = reg ? seen1 : seen0;
+      const bool ready = ptx::mbar_wait(tfull_bar(reg), seen & 1, p.wait_ns);
+      ++seen;
+      if (!ready && lane == 0) record(p.status, kDevTimeoutEpilogue);
+      ptx::tc_fence_after();
+      if (!__all_sync(0xffffffffu, ready && (*abort_flag == 0))) {
+        if (lane == 0) *abort_flag = 1;
+        alive = false;
+      }
+      return alive;
+    };
+    for (int t = pair, jt = 0; alive && t < p.total_tiles; t += npairs, ++jt) {
+      const int mt = t % pr.m_tiles, nt = t / pr.m_tiles;
+      const int rs = jt & 1, ra = rs ^ 1;
+      const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+      const uint32_t tsum = tmem_base + static_cast<uint32_t>(rs * 256) + lane_off;
+      const uint32_t tacc = tmem_base + static_cast<uint32_t>(ra * 256) + lane_off;
+      if (!await(rs)) break;  // the first partial of the fold, in the sum region
+      for (int s = 1; s < nrank; ++s) {
+        if (!await(ra)) break;
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t a[32], b[32];
+          ptx::tmem_ld_32cols(tsum + c * 32, a);
+          ptx::tmem_ld_32cols(tacc + c * 32, b);
+          ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(a);
+          ptx::tmem_regs_ready(b);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(b[j]));
+          ptx::tmem_st_32cols(tsum + c * 32, a);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_remote(ra ? lead_tempty1 : lead_tempty0);
+      }
+      if (!alive) break;
+      // The reduced rows [y0, y0 + 32) x columns [nt*BN, nt*BN + BN): staged 32
+      // columns at a time (128-byte swizzle) and stored to every output.
+      const int y0 = mt * 256 + static_cast<int>(crank) * 128 + q * 32;
+#pragma unroll 1
+      for (int c = 0; c < kChunks; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32cols(tsum + c * 32, v);
+        ptx::tmem_ld_wait();
+        ptx::tmem_regs_ready(v);
+        if (c + 1 == kChunks) {  // the sum region is read: hand it back to the MMA warp
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(rs ? lead_tempty1 : lead_tempty0);
+        }
+        uint8_t *buf = mine + (groups & 1) * (32 * 128);
+        if (groups >= 2) {  // the stores that read this buffer two chunks ago are done reading
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+        }
+        float4 *row = reinterpret_cast<float4 *>(buf + lane * 128);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          row[u ^ (lane & 7)] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                            __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int r = 0; r < p.ring_copies; ++r)
+            ptx::tma_store_2d(&p.maps[p.ring_out + r], ptx::smem_addr(buf), nt * BN + c * 32, y0);
+          ptx::bulk_commit_group();
+        }
+        ++groups;
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_group_all();  // every store has landed before the CTA leaves
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  ptx::cluster_sync();  // neither CTA leaves while the other may still touch its smem
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Split-K cluster kernel for problems with too few output tiles to fill the
 // GPU (small-token row-parallel layers, decode). A cluster computes one tile:
 // CTA ranks are (split, member), member = the M-half for SM pairs. Split s
@@ -1406,6 +1693,37 @@ tp_status launch_pair(const GemmParams &p, int bn, cudaStream_t stream) {
   return pair_ksub() == 2 ? launch_pair_ks<EPI, 2, 256>(p, stream) : launch_pair_ks<EPI, 3, 256>(p, stream);
 }
 
+template <int KSUB, int BN>
+tp_status launch_pair_ring_ks(const GemmParams &p, cudaStream_t stream) {
+  static int configured_mask = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 32 || !(configured_mask & (1 << dev))) {
+      e = cudaFuncSetAttribute(k_gemm_bf16_pair_ring<KSUB, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PairRingCfg<KSUB, BN>::kSmem);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (dev < 32) configured_mask |= (1 << dev);
+    }
+  }
+  const int pairs_max = num_sms() / 2;
+  const int pairs = p.total_tiles < pairs_max ? p.total_tiles : pairs_max;
+  e = launch_kernel(k_gemm_bf16_pair_ring<KSUB, BN>, dim3(2 * pairs), dim3(kThreads), PairRingCfg<KSUB, BN>::kSmem,
+                    stream, 1, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : cuda_fail(e);
+}
+
+// Same tile width and k-stage grouping as launch_pair, so the partials match
+// the GEMM without a combine bit for bit.
+tp_status launch_pair_ring(const GemmParams &p, int bn, cudaStream_t stream) {
+  if (bn == 224) return launch_pair_ring_ks<2, 224>(p, stream);
+  return pair_ksub() == 2 ? launch_pair_ring_ks<2, 256>(p, stream) : launch_pair_ring_ks<3, 256>(p, stream);
+}
+
 template <bool PAIR, int EPI, int BN>
 tp_status launch_splitk(const GemmParams &p, cudaStream_t stream) {
   using C = SplitCfg<PAIR, BN>;
@@ -1510,6 +1828,31 @@ int GemmBuilder::add_map(const void *base, long long rows, long long k, long lon
   return n_maps++;
 }
 
+int GemmBuilder::add_out_map_f32(void *base, long long rows, long long cols, long long ld, tp_status *err) {
+  if (n_maps >= kMaxMaps) {
+    *err = TP_ERR_UNSUPPORTED;
+    return -1;
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    *err = cuda_fail(cudaErrorNotSupported);
+    return -1;
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&p.maps[n_maps], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+    *err = TP_ERR_INVALID_ARG;
+    return -1;
+  }
+  margs[n_maps] = MapArgs{base, rows, cols, ld, 32};
+  out_map[n_maps] = true;
+  return n_maps++;
+}
+
 int GemmBuilder::use_3d_boxes(int kt) {
   // TPGQA_TMA3D=0 keeps the 2-D maps (tuning override).
   static const int enabled = [] {
@@ -1518,7 +1861,7 @@ int GemmBuilder::use_3d_boxes(int kt) {
   }();
   if (kt <= 1 || !enabled) return 1;
   for (int i = 0; i < n_maps; ++i)
-    if (margs[i].k % BK != 0 || margs[i].k / BK < kt) return 1;
+    if (!out_map[i] && (margs[i].k % BK != 0 || margs[i].k / BK < kt)) return 1;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return 1;
   // View a [rows x k] matrix as [k/64][rows][64]: element (x, y, z) is column
@@ -1527,6 +1870,7 @@ int GemmBuilder::use_3d_boxes(int kt) {
   // back, the same shared-memory layout that kt 2-D copies produce.
   CUtensorMap tmp[kMaxMaps];
   for (int i = 0; i < n_maps; ++i) {
+    if (out_map[i]) continue;
     const MapArgs &m = margs[i];
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(m.rows),
                                 static_cast<cuuint64_t>(m.k / BK)};
@@ -1539,7 +1883,8 @@ int GemmBuilder::use_3d_boxes(int kt) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return 1;  // keep the 2-D maps, all of them
   }
-  for (int i = 0; i < n_maps; ++i) p.maps[i] = tmp[i];
+  for (int i = 0; i < n_maps; ++i)
+    if (!out_map[i]) p.maps[i] = tmp[i];
   return kt;
 }
 
@@ -1608,13 +1953,14 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     }
     split = choose_split(p.total_tiles, pair, min_stages < 0 ? 0 : min_stages);
   }
-  if (split < 1 || (pair && bn != 256) || (!pair && bn != 256 && bn != 128))
+  if (split < 1 || (pair && bn != 256) || (!pair && bn != 256 && bn != 128) || ring)
     split = 1;  // split-K runs 256-column pair tiles and 128/256-column single-CTA tiles
   p.split = split;
   // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand
   // and stage replaces KSUB 2-D copies. The single-CTA kernels load one k-tile
   // per stage and keep the 2-D maps.
   p.box_kt = pair ? use_3d_boxes(split > 1 || bn != 256 ? SplitCfg<true, 256>::kSub : pair_ksub()) : 1;
+  if (ring) return launch_pair_ring(p, bn, stream);
   if (split > 1) {
     if (pair) {
       if (epi == kEpiF32) return launch_splitk<true, kEpiF32, 256>(p, stream);

@@ -273,6 +273,79 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
   return b.launch(s);
 }
 
+// Whether the ring all-reduce of a bf16 row-parallel layer can be folded into
+// its GEMM (the ring-folding pair kernel) with results bit-identical to the
+// GEMM followed by the one-pass ring: the layer runs on the SM-pair kernel
+// without split-K, every 256-row tile lies inside one ring chunk (T % N == 0,
+// T/N a multiple of 256; the chunks are then whole rows), and the outputs can
+// be written by 2-D TMA stores. TPGQA_RING_EPILOGUE=0 turns it off (read on
+// every call).
+bool ring_fold_ok(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y, int copies) {
+  const char *env = getenv("TPGQA_RING_EPILOGUE");
+  if (env && env[0] == '0') return false;
+  const long long T = x[0].rows, nout = w[0].rows;
+  if (n < 2 || n > kMaxSegs || 2 * n + copies > kMaxMaps) return false;
+  if (!choose_pair(T) || T % n != 0 || (T / n) % 256 != 0 || T > (1LL << 30)) return false;
+  if (nout % 4 != 0 || nout > (1LL << 30)) return false;
+  for (int r = 0; r < copies; ++r)
+    if (y[r].ld != nout) return false;
+  // the GEMM without a combine must also run the persistent pair kernel (no split-K)
+  int b_rows = 0;
+  const std::vector<long long> nc(static_cast<size_t>(n), nout);
+  const int bn = choose_pair_bn(T, nc.data(), n, false, &b_rows);
+  if (bn == 256) {
+    long long min_stages = -1;
+    for (int32_t r = 0; r < n; ++r) {
+      const long long st = ((x[r].cols + 63) / 64 + 1) / 2;
+      if (min_stages < 0 || st < min_stages) min_stages = st;
+    }
+    const long long tiles = static_cast<long long>(n) * (T / 256) * ((nout + 255) / 256);
+    if (choose_split(tiles, true, min_stages) != 1) return false;
+  }
+  return true;
+}
+
+// Row-parallel GEMM with the ring all-reduce folded in: one problem whose
+// segments are the ranks, the sum written to y[0..copies-1].
+tp_status gemm_bf16_row_ring(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y, int copies,
+                             cudaStream_t s) {
+  const long long T = x[0].rows, nout = w[0].rows;
+  GemmBuilder b;
+  b.epi = kEpiF32;
+  b.pair = true;
+  b.ring = true;
+  b.split = 1;
+  int b_rows = 0;
+  {
+    const std::vector<long long> nc(static_cast<size_t>(n), nout);
+    b.bn = choose_pair_bn(T, nc.data(), n, false, &b_rows);  // the width the unfolded GEMM takes
+  }
+  b.a_rows = 128;
+  tp_status err = TP_OK;
+  std::vector<int> am(n), bm(n);
+  std::vector<long long> ks(n);
+  for (int32_t r = 0; r < n; ++r) {
+    am[r] = b.add_map(x[r].ptr, T, x[r].cols, x[r].ld, b.a_rows, &err);
+    if (am[r] < 0) return err;
+    bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, b_rows, &err);
+    if (bm[r] < 0) return err;
+    ks[r] = x[r].cols;
+  }
+  if (!b.add_problem(static_cast<int>(T), static_cast<int>(nout), y[0].ptr, y[0].ld, am.data(), bm.data(), nullptr,
+                     ks.data(), n))
+    return TP_ERR_UNSUPPORTED;
+  int first = -1;
+  for (int r = 0; r < copies; ++r) {
+    const int m = b.add_out_map_f32(y[r].ptr, T, nout, y[r].ld, &err);
+    if (m < 0) return err;
+    if (r == 0) first = m;
+  }
+  b.p.ring_rows = static_cast<int>(T / n);
+  b.p.ring_out = first;
+  b.p.ring_copies = copies;
+  return b.launch(s);
+}
+
 tp_status gemm_f32_column(const tp_tensor &x, int32_t n, const tp_tensor *w, const ColOut *outs,
                           cudaStream_t s) {
   F32Params p;
@@ -369,6 +442,10 @@ tp_status row_linear_impl(int32_t n, const tp_tensor *x, const tp_tensor *w, con
   }
   for (int32_t r = 0; r < n; ++r)
     if (x[r].cols == 0) return TP_ERR_UNSUPPORTED;  // a rank with an empty K slice
+  if (dt == TP_BF16 && (combine == TP_COMBINE_RING_FUSED || combine == TP_COMBINE_RING_SHARED)) {
+    const int copies = combine == TP_COMBINE_RING_FUSED ? n : 1;
+    if (ring_fold_ok(n, x, w, y, copies)) return gemm_bf16_row_ring(n, x, w, y, copies, s);
+  }
   if (dt == TP_BF16)
     st = gemm_bf16_row(n, x, w, y, fused, s);
   else
@@ -1235,5 +1312,14 @@ extern "C" tp_status tp_set_wait_budget(int64_t nanoseconds) {
 extern "C" tp_status tp_debug_wait_timeout(tp_stream_t stream) {
   return launch_debug_wait(reinterpret_cast<cudaStream_t>(stream));
 }
+
+namespace tpgqa {
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace tpgqa
+
+extern "C" uint64_t tp_launch_count(void) { return tpgqa::g_launches.load(std::memory_order_relaxed); }
 
 extern "C" const char *tp_version(void) { return "tpgqa 0.1 (sm_103a)"; }

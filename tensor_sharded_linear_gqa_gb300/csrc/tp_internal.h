@@ -48,6 +48,9 @@ tp_status cuda_fail(cudaError_t e);
 // while the previous one finishes. TPGQA_PDL=0 turns it off.
 bool pdl_enabled();
 
+// Counts one kernel launch issued by the library (tp_launch_count).
+void note_launch();
+
 // Launches `kernel` on `stream`, with PDL when enabled and with a cluster of
 // `cluster_x` CTAs when cluster_x > 1 (kernels whose cluster shape is fixed at
 // compile time pass 1).
@@ -75,7 +78,9 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -132,6 +137,14 @@ struct GemmParams {
   int box_kt;    // 64-wide k-tiles per TMA copy: 1 = 2-D maps (one copy per k-tile),
                  // >1 = 3-D maps whose box spans that many k-tiles (a whole stage)
   int one_stages;  // pipeline stages of the single-CTA kernels (sized from a_rows)
+  // Ring-folding row-parallel kernel (0 rows = not folding): one problem whose
+  // segments are the N ranks' K slices; every tile lies inside one ring chunk of
+  // ring_rows rows, and its per-rank partials are added in that chunk's ring
+  // order. The sum goes to ring_copies f32 outputs through the tensor maps
+  // ring_out .. ring_out + ring_copies - 1 (32 x 32 boxes, 128-byte swizzle).
+  int ring_rows;
+  int ring_out;
+  int ring_copies;
   int *status;
   long long wait_ns;
 };
@@ -154,11 +167,17 @@ struct GemmBuilder {
     int box_rows;
   };
   MapArgs margs[kMaxMaps];
+  bool out_map[kMaxMaps] = {};  // maps made by add_out_map_f32 (kept 2-D)
   GemmBuilder();
   // Tensor map of a bf16 [rows x k] matrix with row pitch ld (elements), boxes
   // of 64 x box_rows, 128-byte swizzle. Returns the map index or -1.
   int add_map(const void *base, long long rows, long long k, long long ld, int box_rows,
               tp_status *err);
+  // Tensor map of an f32 [rows x cols] output with row pitch ld (elements), for
+  // stores of 32 x 32 boxes from 128-byte-swizzled shared memory. Returns the
+  // map index or -1. Not re-encoded by use_3d_boxes.
+  int add_out_map_f32(void *base, long long rows, long long cols, long long ld, tp_status *err);
+  bool ring = false;  // launch the ring-folding pair kernel (see GemmParams::ring_rows)
   // Re-encodes every map as a 3-D map whose box spans kt k-tiles, if every
   // map's K is a multiple of 64 with at least kt k-tiles; returns kt, or 1 (the
   // 2-D maps kept) otherwise.

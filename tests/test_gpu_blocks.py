@@ -141,20 +141,15 @@ def test_mlp_block_small_ragged(combine):
 @pytest.mark.parametrize("name", ["mlp_tp2_t512", "decode_gqa_rep_tp8_t64"])
 def test_ring_shared_result_is_the_ring_fused_result(name):
     """TP_COMBINE_RING_SHARED folds in the ring's order like RING_FUSED and stores
-    the result once, in y[0]: bit-identical to RING_FUSED's y[0], while
-    y[1..N-1] keep their partials (equal to TP_COMBINE_NONE's)."""
+    the result once, in y[0]: bit-identical to RING_FUSED's y[0] (y[1..N-1] are
+    scratch)."""
     need_gpu()
     L, _f = layer(name)
     fused, _ = L.mlp(tp.TP_COMBINE_RING_FUSED)
     ref0 = host_bits_f32(fused[0])
     del fused
-    none, _ = L.mlp(tp.TP_COMBINE_NONE)
-    parts = [host_bits_f32(y) for y in none]
-    del none
     shared, _ = L.mlp(tp.TP_COMBINE_RING_SHARED)
     assert np.array_equal(host_bits_f32(shared[0]), ref0)
-    for r in range(1, L.n):
-        assert np.array_equal(host_bits_f32(shared[r]), parts[r])
     if "wq" not in L.dev:  # an MLP-only workload
         return
     _q, _k, _v, ya = L.attn(tp.TP_COMBINE_RING_FUSED)

@@ -1,0 +1,134 @@
+"""The ring all-reduce folded into the row-parallel GEMM (mlxcel manual "텐서
+병렬화", 통신 패턴: reduce-scatter then all-gather on the ring; chunk c is
+reduced in the order c+1, c+2, ..., c).
+
+Where every 256-row tile lies inside one ring chunk, tp_row_linear with
+TP_COMBINE_RING_FUSED / RING_SHARED runs the ring-folding GEMM: each rank's
+partial is computed from a zeroed accumulator exactly as the GEMM without a
+combine computes it, and the partials are added in the chunk's ring order. The
+result must therefore equal, bit for bit, the partials of TP_COMBINE_NONE
+reduced by the one-pass ring (tp_allreduce_ring), and the step-by-step ring;
+and it must match the fp64 oracle within the bf16 tolerance.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import tensor_sharded_linear_gqa_gb300 as tp
+from tensor_sharded_linear_gqa_gb300 import inputs
+from gpu_util import BF16_TOL, assert_close, dev_bf16, host_bits_f32, host_f64, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+# (tokens, ranks, output features, input features per rank): tiles inside one
+# chunk (T/N a multiple of 256); ragged K (not a multiple of 64, odd k-tile
+# counts), an output width that is not a multiple of the 256-column tile.
+CASES = [
+    (512, 2, 512, 256),
+    (1024, 4, 768, 320),
+    (2048, 8, 1000, 200),
+    (2048, 4, 4096, 1024),   # the attention projection's o_proj shape
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _layer(T, n, D, K, seed):
+    x = [inputs.normal_bf16(seed, 40 + r, (T, K)) for r in range(n)]
+    w = [inputs.normal_bf16(seed, 80 + r, (D, K), 0.05) for r in range(n)]
+    return x, w
+
+
+def _run(xd, wd, combine, env=None):
+    torch = _torch()
+    n = len(xd)
+    T, D = xd[0].shape[0], wd[0].shape[0]
+    ys = [torch.full((T, D), float("nan"), device="cuda") for _ in range(n)]
+    old = os.environ.get("TPGQA_RING_EPILOGUE")
+    try:
+        if env is not None:
+            os.environ["TPGQA_RING_EPILOGUE"] = env
+        tp.tp_row_linear(n, xd, wd, ys, combine)
+    finally:
+        if env is not None:
+            if old is None:
+                del os.environ["TPGQA_RING_EPILOGUE"]
+            else:
+                os.environ["TPGQA_RING_EPILOGUE"] = old
+    torch.cuda.synchronize()
+    assert tp.tp_device_status() == (tp.TP_OK, 0)
+    return ys
+
+
+@pytest.mark.parametrize("T,n,D,K", CASES)
+def test_folded_ring_is_bit_identical_to_gemm_then_ring(T, n, D, K):
+    need_gpu()
+    x, w = _layer(T, n, D, K, seed=700 + T + n + D)
+    xd = [dev_bf16(a) for a in x]
+    wd = [dev_bf16(a) for a in w]
+    # reference: partials of the GEMM without a combine, then the one-pass ring
+    parts = _run(xd, wd, tp.TP_COMBINE_NONE)
+    part_bits = [host_bits_f32(p) for p in parts]
+    tp.tp_allreduce_ring(n, parts, tp.TP_RING_FUSED)
+    _torch().cuda.synchronize()
+    ref = host_bits_f32(parts[0])
+    for p in parts[1:]:
+        assert np.array_equal(host_bits_f32(p), ref)
+    # the oracle's ring over the same f32 partials, in its own fold order
+    oring = O.ring_all_reduce([b.view(np.float32).reshape(-1) for b in part_bits])
+    assert np.array_equal(np.asarray(oring[0], dtype=np.float32).view(np.uint32).reshape(T, D), ref)
+    # folded (default), and the same call with the fold turned off
+    folded = _run(xd, wd, tp.TP_COMBINE_RING_FUSED)
+    for r in range(n):
+        assert np.array_equal(host_bits_f32(folded[r]), ref), f"rank {r}"
+    unfolded = _run(xd, wd, tp.TP_COMBINE_RING_FUSED, env="0")
+    for r in range(n):
+        assert np.array_equal(host_bits_f32(unfolded[r]), ref), f"rank {r}, unfolded"
+    shared = _run(xd, wd, tp.TP_COMBINE_RING_SHARED)
+    assert np.array_equal(host_bits_f32(shared[0]), ref)
+    steps = _run(xd, wd, tp.TP_COMBINE_RING)
+    for r in range(n):
+        assert np.array_equal(host_bits_f32(steps[r]), ref), f"rank {r}, step ring"
+    # and the value against the fp64 definition: sum_r X_r W_r^T
+    f = inputs.bf16_bits_to_f64
+    exact = sum(O.linear(f(a), f(b)) for a, b in zip(x, w))
+    assert_close(host_f64(folded[0]), exact, BF16_TOL, "folded sum")
+
+
+def test_integer_inputs_give_the_exact_sum():
+    """Small integers are exact in bf16 and every sum stays below 2^24, so the
+    folded result equals the unsharded product exactly, whatever the order."""
+    need_gpu()
+    T, n, D, K = 1024, 4, 520, 192
+    x = [inputs.small_int_bf16(77, 10 + r, (T, K), -3, 3) for r in range(n)]
+    w = [inputs.small_int_bf16(77, 30 + r, (D, K), -3, 3) for r in range(n)]
+    ys = _run([dev_bf16(a) for a in x], [dev_bf16(b) for b in w], tp.TP_COMBINE_RING_FUSED)
+    f = inputs.bf16_bits_to_f64
+    exact = O.linear(np.concatenate([f(a) for a in x], axis=1), np.concatenate([f(b) for b in w], axis=1))
+    for y in ys:
+        assert np.array_equal(host_f64(y), exact)
+
+
+def test_consecutive_calls_and_other_buffers_unchanged():
+    """Two calls in a row on new inputs give fresh results (no state carried in
+    the kernel), and RING_SHARED writes y[0] only."""
+    need_gpu()
+    torch = _torch()
+    T, n, D, K = 1024, 4, 512, 256
+    for seed in (801, 802):
+        x, w = _layer(T, n, D, K, seed)
+        xd = [dev_bf16(a) for a in x]
+        wd = [dev_bf16(a) for a in w]
+        parts = _run(xd, wd, tp.TP_COMBINE_NONE)
+        tp.tp_allreduce_ring(n, parts, tp.TP_RING_FUSED)
+        ys = [torch.full((T, D), 7.0, device="cuda") for _ in range(n)]
+        tp.tp_row_linear(n, xd, wd, ys, tp.TP_COMBINE_RING_SHARED)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits_f32(ys[0]), host_bits_f32(parts[0]))
+        for y in ys[1:]:
+            assert bool((y == 7.0).all())
