@@ -1,13 +1,15 @@
 #!/usr/bin/env python3
-"""Benchmark of the tensor-parallel MLP block on GB300 (one JSON line on stdout).
+"""Benchmark of the tensor-parallel sharded linear blocks on GB300 (one JSON line on stdout).
 
-One step = one pass of the block's hot path over one batch of synthetic input:
-the shard plan (host), the column-parallel gate/up GEMM with the fused SwiGLU
-for all ranks, the row-parallel down GEMM, and the ring all-reduce of the
-per-rank partials. Default workload: Llama-style MLP, T=512 tokens, D=2048,
-F=8192, TP=2, bf16 inputs with fp32 accumulation. Inputs are already resident in
-HBM; several input sets (each a full weight copy) are rotated so that the
-working set exceeds twice the L2 (no step reads another step's weights from L2).
+One step = one pass of the hot path over one batch of synthetic input. Default
+workload: the large decoder-layer projections and MLP in prefill, T=4096 tokens,
+D=8192, 64 q / 8 kv heads of 128, F=28672, TP=8, bf16 inputs with fp32
+accumulation. A step is the shard plan (host), the q/k/v column-parallel GEMM,
+the o_proj row-parallel GEMM with the ring all-reduce of its partials, the
+gate/up column-parallel GEMM with the fused SwiGLU, and the down row-parallel
+GEMM with its ring all-reduce. Inputs are already resident in HBM; when one
+input set is smaller than twice the L2, several sets (each a full weight copy)
+are rotated so that no step reads another step's weights from L2.
 
 `--impl reference` times the fp64 CPU oracle on the same workload instead (the
 CPU baseline arm). Under torchrun every rank runs an independent replica on its
@@ -46,7 +48,7 @@ def parse_args():
                    help="timed steps (default: about one second of GPU time for the workload)")
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--workload", default="mlp_tp2_t512")
+    p.add_argument("--workload", default="prefill_layer_tp8_t4096")
     p.add_argument("--combine", choices=sorted(COMBINE_NAMES) + sorted(PIPELINE_MODES), default=None,
                    help="ring_fused (default): the ring all-reduce in one pass, bit-identical to ring (N-1 step "
                         "launches per phase); ring_shared: the same with the result stored once, for ranks that "
@@ -94,11 +96,6 @@ def ring_bytes(mode: str, n: int, size_bytes: int) -> int:
     if mode == "ring_shared":
         return (n + 1) * size_bytes  # each partial read once, the one shared result written
     return 2 * n * size_bytes  # ring_fused: each partial read once, every rank written once
-
-
-def launches_per_step(mode: str, n: int) -> int:
-    ring = {"ring": 2 * (n - 1), "ring_fused": 1, "ring_shared": 1, "fused": 0}[mode] if n > 1 else 0
-    return 2 + ring
 
 
 # ---- clocks -------------------------------------------------------------------------
@@ -343,8 +340,43 @@ def oracle_pass(w, moe_mode: str):
     raise ValueError(f"no timed oracle pass for workload kind {kind}")
 
 
-def cpu_child(workload: str, moe_mode: str, budget: str, max_reps: str, rows: str) -> None:
-    """Child-process body of cpu_oracle_run: times oracle passes, prints one JSON line."""
+# Rows of every step result that the native arm saves for the oracle's check.
+PARITY_ROWS = 256
+PARITY_TOL = 1e-2  # max|gpu - oracle| <= 1e-2 * max|oracle| (bf16 inputs, fp32 accumulation)
+
+
+def oracle_results(w, out: list) -> list:
+    """The step results, in the order step_results gives the GPU's, out of one
+    oracle pass's outputs (see oracle_pass)."""
+    import numpy as np
+    kind = w["kind"]
+    if kind == "attn":
+        return [out[-1]]
+    if kind == "layer":
+        return out[-2:]
+    if kind == "attn_core":
+        return [np.concatenate(out, axis=1)]
+    return list(out)
+
+
+def parity_errors(gpu: list, ref: list) -> list:
+    """max|gpu - ref| / max|ref| over the rows both hold, per result."""
+    import numpy as np
+    errs = []
+    for g, r in zip(gpu, ref):
+        r = np.asarray(r, dtype=np.float64)
+        m = min(g.shape[0], r.shape[0])
+        g, r = np.asarray(g[:m], dtype=np.float64), r[:m]
+        scale = float(np.max(np.abs(r))) if r.size else 0.0
+        diff = float(np.max(np.abs(g - r))) if r.size else 0.0
+        errs.append(diff / scale if scale > 0 else diff)
+    return errs
+
+
+def cpu_child(workload: str, moe_mode: str, budget: str, max_reps: str, rows: str, check: str = "") -> None:
+    """Child-process body of cpu_oracle_run: times oracle passes, prints one JSON line.
+    With `check` (an .npz of the GPU's first rows of every step result), the last
+    pass's outputs are compared with them."""
     from tensor_sharded_linear_gqa_gb300 import inputs
     w = dict(inputs.WORKLOADS[workload])
     budget, max_reps, rows = float(budget), int(max_reps), int(rows)
@@ -374,14 +406,23 @@ def cpu_child(workload: str, moe_mode: str, budget: str, max_reps: str, rows: st
     t_all = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        one_pass(rows)
+        last = one_pass(rows)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_all >= budget or len(times) >= max_reps:
             break
-    print(json.dumps({"reps": len(times), "seconds": sum(times), "times": times, "rows": rows}))
+    res = {"reps": len(times), "seconds": sum(times), "times": times, "rows": rows}
+    if check:
+        import numpy as np
+        with np.load(check) as z:
+            gpu = [z[f"r{i}"] for i in range(len(z.files))]
+        errs = parity_errors(gpu, oracle_results(w, last))
+        res["parity"] = {"rows": min(rows, PARITY_ROWS), "max_rel_err": [float(f"{e:.3e}") for e in errs],
+                         "tol": PARITY_TOL, "pass": bool(all(e <= PARITY_TOL for e in errs))}
+    print(json.dumps(res))
 
 
-def cpu_oracle_run(workload: str, moe_mode: str, seconds: float, max_reps: int, rows: int) -> dict:
+def cpu_oracle_run(workload: str, moe_mode: str, seconds: float, max_reps: int, rows: int,
+                   check: str = "") -> dict:
     """Runs the fp64 oracle over a workload in a child process on every core this
     process may use. rows > 0: that many token rows per pass (at most T); rows <= 0:
     sized so that a pass takes about -rows ms."""
@@ -391,7 +432,7 @@ def cpu_oracle_run(workload: str, moe_mode: str, seconds: float, max_reps: int, 
         env[k] = str(cores)
     code = "import sys; sys.path.insert(0, sys.argv[1]); import bench; bench.cpu_child(*sys.argv[2:])"
     out = subprocess.run([sys.executable, "-c", code, ROOT, workload, moe_mode, str(seconds), str(max_reps),
-                          str(rows)], capture_output=True, text=True, env=env, timeout=1800)
+                          str(rows), check], capture_output=True, text=True, env=env, timeout=1800)
     if out.returncode != 0:
         raise RuntimeError(out.stderr[-2000:])
     r = json.loads(out.stdout.strip().splitlines()[-1])
@@ -408,19 +449,20 @@ def cpu_too_large(w):
     return None
 
 
-def cpu_baseline(w, workload: str, moe_mode: str, seconds: float) -> dict:
+def cpu_baseline(w, workload: str, moe_mode: str, seconds: float, check: str = "") -> tuple:
     """The oracle as it stands, timed for about `seconds` on a bounded row sample
-    (whole passes when a pass over all T rows takes under a quarter of that)."""
+    (whole passes when a pass over all T rows takes under a quarter of that).
+    Returns (the cpu_baseline object, the parity check of the GPU's saved rows or None)."""
     why = cpu_too_large(w)
     if why:
-        return {"unavailable": why}
-    r = cpu_oracle_run(workload, moe_mode, seconds, 1000, -int(seconds * 250))
+        return {"unavailable": why}, None
+    r = cpu_oracle_run(workload, moe_mode, seconds, 1000, -int(seconds * 250), check)
     rows = r["rows"]
     val = sample_flops(w, rows) * r["reps"] / r["seconds"] / 1e12
     what = "full passes" if rows == w["T"] else f"passes over {rows} of its {w['T']} token rows"
-    return {"value": round(val, 6), "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
-            "sample": f"{r['reps']} {what} of the fp64 oracle on {workload} ({oracle_work(w)}) "
-                      f"in {r['seconds']:.1f} s"}
+    return ({"value": round(val, 6), "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+             "sample": f"{r['reps']} {what} of the fp64 oracle on {workload} ({oracle_work(w)}) "
+                       f"in {r['seconds']:.1f} s"}, r.get("parity"))
 
 
 # ---- native arm ----------------------------------------------------------------------
@@ -443,8 +485,6 @@ class DeviceSet:
             return slice(*shards[r]["ranges"][name])
 
         self.calls = []  # (phase name, callable)
-        combine_ring = {"ring": tp.TP_RING_STEPS, "ring_fused": tp.TP_RING_FUSED,
-                        "ring_shared": tp.TP_RING_FUSED_SHARED}.get(mode)
         self.x = to_dev(data["x"])
         self.e2e = {}
         if w["kind"] in ("attn", "layer"):
@@ -476,11 +516,10 @@ class DeviceSet:
                 self.calls.append(("attn_core", tp.Prepared(
                     "tp_attn_core", plan.handle, tp.arr(q), tp.arr(k), tp.arr(v), tp.arr(a_r), 1,
                     self.aws.data_ptr(), self.aws.numel(), sptr)))
-            self.calls.append(("o_proj", tp.Prepared(
-                "tp_row_linear", n, tp.arr(a_r), tp.arr(o_w), tp.arr(yo),
-                tp.TP_COMBINE_FUSED if mode == "fused" else tp.TP_COMBINE_NONE, sptr)))
-            if combine_ring is not None and n > 1:
-                self.calls.append(("combine_o", tp.Prepared("tp_allreduce_ring", n, tp.arr(yo), combine_ring, sptr)))
+            # o_proj row-parallel with its combine, one public call (the library may
+            # fold the ring into the GEMM)
+            self.calls.append(("o_proj", tp.Prepared("tp_row_linear", n, tp.arr(a_r), tp.arr(o_w), tp.arr(yo),
+                                                     COMBINE_NAMES[mode], sptr)))
             self.e2e["attn"] = (q_w, k_w, v_w, q, k, v, a_r, o_w, yo)
         if w["kind"] in ("mlp", "layer"):
             F = w["ffn"]
@@ -495,12 +534,8 @@ class DeviceSet:
             self.keep += [hbuf] + ym
             self.calls.append(("gate_up", ("tp_gate_up_swiglu", tp.arr([self.x]), tp.arr(g), tp.arr(u),
                                            tp.arr(h))))
-            self.calls.append(("down", tp.Prepared(
-                "tp_row_linear", n, tp.arr(h), tp.arr(dn), tp.arr(ym),
-                tp.TP_COMBINE_FUSED if mode == "fused" else tp.TP_COMBINE_NONE, sptr)))
-            if combine_ring is not None and n > 1:
-                self.calls.append(("combine_mlp", tp.Prepared("tp_allreduce_ring", n, tp.arr(ym), combine_ring,
-                                                             sptr)))
+            self.calls.append(("down", tp.Prepared("tp_row_linear", n, tp.arr(h), tp.arr(dn), tp.arr(ym),
+                                                   COMBINE_NAMES[mode], sptr)))
             self.e2e["mlp"] = (g, u, dn, ym)
         if w["kind"] == "attn_core":
             hd = w["head_dim"]
@@ -623,24 +658,31 @@ class DeviceSet:
             self.e2e["rs_column"] = (pipeline_calls, ys)
 
 
+def result_copies(mode: str, n: int) -> int:
+    """f32 result tensors a row-parallel layer with its combine writes: one per rank
+    after a ring all-reduce, one for the fused sum or the shared ring result."""
+    return 1 if mode in ("fused", "ring_shared") or n == 1 else n
+
+
 def phase_costs(w, mode):
     """Algorithmic flops and HBM bytes of every phase of one step (weights counted once;
-    a replicated K/V projection is computed once)."""
+    a replicated K/V projection is computed once). A row-parallel phase includes its
+    combine: its bytes are its operands and the combined result (the ring's own
+    traffic, when it runs as a separate pass, is measured on its own; see
+    combine_loop)."""
     n, T, D = w["tp"], w["T"], w["hidden"]
     out = {}
     part = T * D * 4
-    nparts = 1 if mode == "fused" else n
+    nparts = result_copies(mode, n)
     if w["kind"] in ("attn", "layer"):
         hd, hq, hkv = w["head_dim"], w["q_heads"], w["kv_heads"]
         cols = (hq + 2 * hkv) * hd
         out["qkv"] = (2.0 * T * D * cols, cols * D * 2 + T * D * 2 + T * cols * 2)
         out["o_proj"] = (2.0 * T * hq * hd * D, D * hq * hd * 2 + T * hq * hd * 2 + nparts * part)
-        out["combine_o"] = (0.0, ring_bytes(mode, n, part))
     if w["kind"] in ("mlp", "layer"):
         F = w["ffn"]
         out["gate_up"] = (4.0 * T * D * F, 2 * F * D * 2 + T * D * 2 + T * F * 2)
         out["down"] = (2.0 * T * F * D, D * F * 2 + T * F * 2 + nparts * part)
-        out["combine_mlp"] = (0.0, ring_bytes(mode, n, part))
     if w["kind"] == "layer" and w.get("attention"):
         hd, hq, hkv = w["head_dim"], w["q_heads"], w["kv_heads"]
         out["attn_core"] = (4.0 * hd * hq * T * (T + 1) / 2,
@@ -670,6 +712,42 @@ def phase_costs(w, mode):
             out["combine_ag"] = (0.0, S * 2 * 2)               # bf16 chunks read, full copy written
         out["column"] = (2.0 * T * D * n * per, n * per * D * 2 + S * 2 + T * n * per * 2)
     return out
+
+
+def combine_loop(tp, torch, dev, stream, n, rows, cols, mode, hbm_gbs):
+    """The ring all-reduce alone: tp_allreduce_ring in the step's ring mode on N f32
+    buffers of one partial's shape, back to back over enough buffer sets that the
+    working set exceeds twice the L2 (so the figure is HBM's, not L2's), one pair
+    of CUDA events around the loop. Algorithmic bytes: ring_bytes."""
+    ring_mode = {"ring": tp.TP_RING_STEPS, "ring_fused": tp.TP_RING_FUSED,
+                 "ring_shared": tp.TP_RING_FUSED_SHARED}[mode]
+    part = rows * cols * 4
+    nsets = 1 if n * part >= 2 * L2_BYTES else -(-2 * L2_BYTES // (n * part)) + 1
+    bufs = [[torch.zeros((rows, cols), device=dev) for _ in range(n)] for _ in range(nsets)]
+    calls = [tp.Prepared("tp_allreduce_ring", n, tp.arr(b), ring_mode, stream.cuda_stream) for b in bufs]
+    for c in calls[:3]:
+        c()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    calls[0]()
+    torch.cuda.synchronize(dev)
+    once = max(time.perf_counter() - t0, 1e-6)
+    reps = max(len(calls), min(2000, int(0.3 / once)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = tp.tp_launch_count()
+    e0.record(stream)
+    for i in range(reps):
+        calls[i % nsets]()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / reps
+    b = ring_bytes(mode, n, part)
+    gbs = b / (ms / 1e3) / 1e9
+    del bufs, calls
+    return {"gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_gbs, 4), "bytes_per_call": b,
+            "launch_ms": round(ms, 5), "kernels_per_call": (tp.tp_launch_count() - l0) / reps,
+            "bus_bytes_per_rank": 2 * (n - 1) * part // n,
+            "timing": f"tp_allreduce_ring alone, {reps} calls over {nsets} set(s) of {n} x {part / 2**20:.0f} MiB"}
 
 
 def run_native(args):
@@ -736,6 +814,7 @@ def run_native(args):
         import tempfile
         fd, clock_path = tempfile.mkstemp(prefix=f"clocks_rank{rank}_", suffix=".csv")
         os.close(fd)
+    launches0 = tp.tp_launch_count()
     with ClockSampler(local, clock_path) as clk:
         barrier(world)
         torch.cuda.synchronize(dev)
@@ -745,14 +824,15 @@ def run_native(args):
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
+    launches = tp.tp_launch_count() - launches0  # every kernel the K timed steps enqueued
     st, word = tp.tp_device_status(sptr)
     if st != tp.TP_OK:
         raise SystemExit(f"device status {word:#x} after the timed region")
     total_ms = t_start.elapsed_time(t_end)
     max_ms = dist_max(total_ms, world)
-    # Per-phase breakdown: a second pass of the same steps with CUDA events between
-    # the phases (events between kernels also stop the next kernel's early launch,
-    # so this pass runs slightly slower than the timed region above).
+    # Per-phase breakdown, for the shares only: a second pass of the same steps
+    # with CUDA events between the phases (events between kernels also stop the
+    # next kernel's early launch, so this pass runs slower than the timed region).
     P = min(K, 500)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(P)]
     for i in range(P):
@@ -765,13 +845,41 @@ def run_native(args):
     value = aggregate_tflops(world, flops_step, K, max_ms)
     peaks, peak_src = load_peaks()
 
-    # roofline of the dominant kernel: the gate/up GEMM where there is an MLP, else q/k/v
+    # Roofline of the dominant kernel: its public call alone, back to back over the
+    # rotating input sets, one pair of events around the whole loop on the
+    # launching stream. The gate/up GEMM where there is an MLP, else q/k/v, the
+    # row GEMM, the LM head, the MoE block or the attention core.
     rk = next(k for k in ("gate_up", "qkv", "row", "lm_head", "moe_block", "attn_core") if k in phase_ms)
+    ri = names.index(rk)
     rf, rb = costs[rk]
-    r_s = phase_ms[rk] / 1e3
+    kr = max(20, min(K * 4, int(0.5e3 / max(phase_ms[rk], 1e-3))))  # about half a second
+
+    def call_phase(s_, i_):
+        name_, call_ = s_.calls[i_]
+        if isinstance(call_, tuple):
+            st_ = tp.raw_status(call_[0], plan0.handle, *call_[1:], sptr)
+            if st_ != tp.TP_OK:
+                raise tp.TPError(st_, call_[0])
+        else:
+            call_()
+
+    for i in range(3):
+        call_phase(sets[i % R], ri)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = tp.tp_launch_count()
+    e0.record(stream)
+    for i in range(kr):
+        call_phase(sets[i % R], ri)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    r_launch_calls = (tp.tp_launch_count() - l0) / kr
+    r_s = e0.elapsed_time(e1) / kr / 1e3
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     kname = {"attn_core": "k_attention (with the V transpose)",
              "moe_block": "tp_moe_block (routing, gather, expert GEMMs, combine)"}.get(rk, f"k_gemm_bf16* ({rk})")
+    timing = (f"{kr} back-to-back calls of the phase's public call over {R} input set(s), "
+              f"CUDA events around the loop on the launching stream")
     if rf / rb >= ridge:
         roof = {"kernel": kname, "bound": "tensor", "achieved": round(rf / r_s / 1e12, 2),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -782,14 +890,19 @@ def run_native(args):
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(rb / r_s / 1e9 / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": rb}
     roof["traffic"] = committed_traffic(args.workload) if rk == "gate_up" else None
+    roof["launch_ms"] = round(r_s * 1e3, 5)
+    roof["timing"] = timing
+    roof["kernels_per_call"] = r_launch_calls
 
-    comb = {}  # every data-movement phase (the collectives, the lookup) against HBM
+    comb = {}  # every data-movement phase of the step (the lookup, the pipeline's collectives) against HBM
     for nm in names:
         if costs[nm][0] == 0:
             b = costs[nm][1]
             gbs = b / (phase_ms[nm] / 1e3) / 1e9 if phase_ms[nm] > 0 else None
             comb[nm] = {"gbs": round(gbs, 1), "bytes_per_step": b,
                         "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    if w["kind"] in ("attn", "layer", "mlp") and n > 1 and mode != "fused":
+        comb["allreduce"] = combine_loop(tp, torch, dev, stream, n, T, D, mode, peaks["hbm_gbs"])
 
     # -- end to end through the public block calls with host buffers ---------------------
     s0 = sets[0]
@@ -987,8 +1100,8 @@ def run_native(args):
         return dist_max(e0.elapsed_time(e1), world)
 
     e2e_ms = timed(pipelined_step, args.e2e_steps)
+    # e2e.value is this loop's figure (the graph replay below is a side field)
     e2e_value = world * flops_step * args.e2e_steps / (e2e_ms / 1e3) / 1e12
-    e2e_stream_value = e2e_value
 
 
     serial_ms = timed(lambda i: serial_step(), args.e2e_steps)
@@ -1026,8 +1139,6 @@ def run_native(args):
         g_ms = dist_max(g0.elapsed_time(g1), world)
         e2e_graph = {"graph": True, "steps_per_graph": G,
                      "value": round(world * flops_step * reps * G / (g_ms / 1e3) / 1e12, 3)}
-        if e2e_graph["value"] > e2e_value:
-            e2e_value = e2e_graph["value"]
     except Exception as exc:  # the stream loop's figure stands
         e2e_graph = {"graph": False, "error": str(exc)[-200:]}
         torch.cuda.synchronize(dev)
@@ -1035,24 +1146,25 @@ def run_native(args):
     if st != tp.TP_OK:
         raise SystemExit(f"device status {word:#x} after the end-to-end runs")
 
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # The first rows of every step result of input set 0 (the last timed step's,
+        # rewritten with the same values by the end-to-end loop), for the oracle
+        # child to check against the same rows of its own pass.
+        import tempfile
+        fd, check = tempfile.mkstemp(prefix="bench_rows_", suffix=".npz")
+        os.close(fd)
         try:
-            cpu = cpu_baseline(w, args.workload, args.moe_mode, args.cpu_seconds)
+            rows_out = {}
+            for i, t in enumerate(results(slots[0])):
+                rows_out[f"r{i}"] = t[:PARITY_ROWS].float().cpu().numpy()
+            np.savez(check, **rows_out)
+            cpu, parity = cpu_baseline(w, args.workload, args.moe_mode, args.cpu_seconds, check)
         except Exception as exc:  # reported, not fatal
             cpu = {"error": str(exc)[-300:]}
+        finally:
+            os.unlink(check)
 
-    launches = 0
-    for nm in names:
-        if nm.startswith("combine"):
-            launches += 2 * (n - 1) if mode == "ring" else 1
-        elif nm == "attn_core":
-            launches += 2  # the transpose of every kv source's V, then the attention kernel
-        elif nm == "moe_block":
-            # routing, gather, gate/up, down and combine kernels, then the all-reduce
-            launches += 5 + ({"ring": 2 * (n - 1), "ring_fused": 1, "ring_shared": 1}.get(mode, 0) if n > 1 else 0)
-        else:
-            launches += 1
     config = {"workload": args.workload, "tokens": T, "hidden": D, "tp_size": n, "combine": mode,
               "flops_per_step": flops_step,
               "l2": (f"{R} rotating input sets of {set_bytes / 1e6:.1f} MB (> 2x L2 in total)" if R > 1 else
@@ -1077,14 +1189,17 @@ def run_native(args):
         "combine": comb,
         "roofline": roof,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "stream_loop_value": round(e2e_stream_value, 3), "cuda_graph": e2e_graph,
+                "loop": "pipelined stream loop (two activation slots, copies on two copy streams)",
+                "cuda_graph": e2e_graph,
                 "d2h_bytes_per_step": d2h, "pipelined": True,
                 "serial_value": round(serial_value, 3)},
-        "gpu_launches": launches * K,
+        "gpu_launches": launches,
+        "launches_per_step": launches / K,
         "clocks": clk.summary(),
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    line["parity"] = parity  # None when the oracle did not run beside this arm
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

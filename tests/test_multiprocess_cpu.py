@@ -91,7 +91,8 @@ def test_reference_arm_prints_only_on_rank_zero():
 
 def test_reference_arm_prints_the_contract_line():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
-                        "--warmup", "1", "--reference-seconds", "2"], capture_output=True, text=True, timeout=300,
+                        "--warmup", "1", "--reference-seconds", "2", "--workload", "mlp_tp2_t512"],
+                       capture_output=True, text=True, timeout=300,
                        env=dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0"))
     assert r.returncode == 0, r.stderr[-2000:]
     line = json.loads(r.stdout.strip().splitlines()[-1])
@@ -104,3 +105,17 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_default_workload_is_the_largest_single_gpu_layer():
+    """With no flags the bench times the prefill decoder layer (T=4096, D=8192,
+    64 q / 8 kv heads, F=28672, TP=8) with the one-pass ring combine."""
+    sys.path.insert(0, ROOT)
+    import bench
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        args = bench.parse_args()
+    finally:
+        sys.argv = old
+    assert args.workload == "prefill_layer_tp8_t4096" and args.combine is None and args.gpus == 1
