@@ -459,7 +459,9 @@ tp_status tp_mlp_block(const tp_plan *plan, const tp_tensor *x, const tp_tensor 
  *    allocating library routine).
  *  - Set-up: the first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture. The cached address belongs to the
+ *    device's context at that time: do not use the library across a
+ *    cudaDeviceReset of that device (see tp_device_status).
  *  - Sharing: every call on a device uses the same array, which keeps the last
  *    call's H. Each call overwrites H in full before reading it, so nothing has
  *    to be cleared; but calls that can overlap on the GPU (different streams
@@ -523,7 +525,12 @@ tp_status tp_set_rank_health(int32_t rank, int32_t healthy);
  * kernels set when a bounded wait runs out or an embedding lookup meets a bad
  * token id (the first such event is kept). Returns TP_OK, TP_ERR_TIMEOUT,
  * TP_ERR_BAD_TOKEN or TP_ERR_CUDA. *detail (optional) receives the raw word
- * (0 = none). */
+ * (0 = none).
+ * The library looks up the device addresses of its own device variables (this
+ * status word, the scratch array of tp_mlp_block_static) once per device and
+ * keeps them for the life of the process. A cudaDeviceReset destroys the
+ * context they belong to, so the library must not be used on a device after
+ * that device has been reset. */
 tp_status tp_device_status(tp_stream_t stream, int32_t *detail);
 
 /* Sets the time budget, in nanoseconds, of every bounded device-side wait of

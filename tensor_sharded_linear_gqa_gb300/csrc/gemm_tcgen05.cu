@@ -592,7 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // This CTA's half of B: rows of its own map and offset.
       auto b_src = [&](const Cursor &c, int &map, int &row) {
         const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
-        if (EPI == kEpiSwiGLU) {
+        if (EPI == kEpiSwiGLU || sg.b2_map >= 0) {  // two B matrices, one half of the tile each
           map = (leader ? sg.b_map : sg.b2_map) + c.moff;
           row = c.brow + c.nt * kHalfB;
         } else {
@@ -776,11 +776,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) f[jj] = __uint_as_float(v[jj]);
           if (row < pr.m) {
-            if constexpr (EPI == kEpiF32)
+            if constexpr (EPI == kEpiF32) {
               store_f32_row32(static_cast<float *>(pr.out), pr.ldc, row, nt * kOutCols + c, pr.n, f);
-            else
+            } else if (EPI == kEpiBF16 && BN == 256 && pr.out2 != nullptr) {
+              // two outputs: accumulator columns [0, 128) to out, [128, 256) to out2
+              const bool second = c >= BN / 2;
+              store_bf16_row32(static_cast<__nv_bfloat16 *>(second ? pr.out2 : pr.out), second ? pr.ldc2 : pr.ldc,
+                               row, nt * (BN / 2) + (second ? c - BN / 2 : c), pr.n, f);
+            } else {
               store_bf16_row32(static_cast<__nv_bfloat16 *>(pr.out), pr.ldc, row, nt * kOutCols + c,
                                pr.n, f);
+            }
           }
         }
       }
@@ -1921,6 +1927,21 @@ bool GemmBuilder::add_problem(int m, int n, void *out, long long ldc, const int 
   return true;
 }
 
+bool GemmBuilder::add_dual_problem(int m, int n, void *out, long long ldc, void *out2, long long ldc2, int a_map,
+                                   int b_map, int b2_map, long long k) {
+  if (!pair || bn != 256 || epi != kEpiBF16 || n > 128) return false;
+  const long long ks = k;
+  const int saved_epi = epi;
+  epi = kEpiSwiGLU;  // tile count: 128 output columns per 256-column tile
+  const bool ok = add_problem(m, n, out, ldc, &a_map, &b_map, &b2_map, &ks, 1);
+  epi = saved_epi;
+  if (!ok) return false;
+  p.prob[n_probs - 1].out2 = out2;
+  p.prob[n_probs - 1].ldc2 = ldc2;
+  dual = true;
+  return true;
+}
+
 tp_status GemmBuilder::launch(cudaStream_t stream) {
   p.num_problems = n_probs;
   p.n_maps_used = n_maps;
@@ -1953,7 +1974,7 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     }
     split = choose_split(p.total_tiles, pair, min_stages < 0 ? 0 : min_stages);
   }
-  if (split < 1 || (pair && bn != 256) || (!pair && bn != 256 && bn != 128) || ring)
+  if (split < 1 || (pair && bn != 256) || (!pair && bn != 256 && bn != 128) || ring || dual)
     split = 1;  // split-K runs 256-column pair tiles and 128/256-column single-CTA tiles
   p.split = split;
   // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand

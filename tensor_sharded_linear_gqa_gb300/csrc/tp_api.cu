@@ -1182,11 +1182,57 @@ tp_status check_qkv(const tp_dims &d, const tp_rank_shard &s0, const tp_tensor *
 }
 
 // q/k/v column-parallel as one grouped launch (K/V once when replicated).
+// q/k/v on the SM-pair kernel with each rank's k and v (at most 128 columns each)
+// sharing one 256-column tile: k's rows feed one CTA of the pair, v's the other,
+// and the two halves of the accumulator are stored to k and v. Separate k and v
+// problems of 128 columns would each fill only half of a 256-column tile.
+tp_status gemm_bf16_qkv_paired(int32_t n, int32_t nkv, const tp_tensor &x, const tp_tensor *w_q,
+                               const tp_tensor *w_k, const tp_tensor *w_v, const tp_tensor *q, const tp_tensor *k,
+                               const tp_tensor *v, cudaStream_t s) {
+  const long long T = x.rows, K = x.cols;
+  GemmBuilder b;
+  b.epi = kEpiBF16;
+  b.pair = true;
+  b.bn = 256;
+  b.split = 1;
+  b.a_rows = 128;
+  tp_status err = TP_OK;
+  const int am = b.add_map(x.ptr, T, K, x.ld, 128, &err);
+  if (am < 0) return err;
+  for (int32_t r = 0; r < n; ++r) {
+    if (w_q[r].rows == 0) continue;
+    const int bm = b.add_map(w_q[r].ptr, w_q[r].rows, K, w_q[r].ld, 128, &err);
+    if (bm < 0) return err;
+    if (!b.add_problem(static_cast<int>(T), static_cast<int>(w_q[r].rows), q[r].ptr, q[r].ld, &am, &bm, nullptr,
+                       &K, 1))
+      return TP_ERR_UNSUPPORTED;
+  }
+  for (int32_t r = 0; r < nkv; ++r) {
+    const int bk = b.add_map(w_k[r].ptr, w_k[r].rows, K, w_k[r].ld, 128, &err);
+    if (bk < 0) return err;
+    const int bv = b.add_map(w_v[r].ptr, w_v[r].rows, K, w_v[r].ld, 128, &err);
+    if (bv < 0) return err;
+    if (!b.add_dual_problem(static_cast<int>(T), static_cast<int>(w_k[r].rows), k[r].ptr, k[r].ld, v[r].ptr,
+                            v[r].ld, am, bk, bv, K))
+      return TP_ERR_UNSUPPORTED;
+  }
+  return b.launch(s);
+}
+
 tp_status launch_qkv(const tp_dims &d, const tp_rank_shard &s0, const tp_tensor *x, const tp_tensor *w_q,
                      const tp_tensor *w_k, const tp_tensor *w_v, const tp_tensor *q, const tp_tensor *k,
                      const tp_tensor *v, cudaStream_t s) {
   const int32_t n = d.tp_size;
   const int32_t nkv = s0.kv_replicated ? 1 : n;
+  {
+    // TPGQA_QKV_PAIRED=0 keeps k and v as separate problems (read on every call).
+    const char *env = getenv("TPGQA_QKV_PAIRED");
+    bool paired = !(env && env[0] == '0') && choose_pair(x->rows) && 1 + n + 2 * nkv <= kMaxMaps &&
+                  n + nkv <= kMaxProblems;
+    for (int32_t r = 0; paired && r < nkv; ++r)
+      paired = w_k[r].rows == w_v[r].rows && w_k[r].rows > 0 && w_k[r].rows <= 128;
+    if (paired) return gemm_bf16_qkv_paired(n, nkv, *x, w_q, w_k, w_v, q, k, v, s);
+  }
   std::vector<tp_tensor> ws;
   std::vector<ColOut> outs;
   for (int32_t r = 0; r < n; ++r) {

@@ -116,6 +116,11 @@ struct GemmProblem {
   int pad;
   void *out;             // output base (row-major)
   long long ldc;         // elements
+  // Two-output problem (SM-pair kernel, bf16 epilogue, 256-column tiles only):
+  // B comes from b_map (first 128 tile columns, stored to out) and b2_map (last
+  // 128, stored to out2), n columns each. Null: one output.
+  void *out2;
+  long long ldc2;
   // Optional device table, one entry per m-tile, written by an earlier kernel
   // (the MoE routing): -1 skips the tile; otherwise (map_offset << 16) | slot
   // takes B from map b_map + map_offset (b2_map + map_offset for SwiGLU), rows
@@ -187,6 +192,11 @@ struct GemmBuilder {
   bool add_problem(int m, int n, void *out, long long ldc, const int *a_maps, const int *b_maps,
                    const int *b2_maps, const long long *ks, int nseg, const int *blk = nullptr,
                    int b_rows_per_blk = 0, int n_moff = 1);
+  // A two-output problem (see GemmProblem::out2): C1 = A * B1^T to out, C2 =
+  // A * B2^T to out2, both [m x n], in shared 256-column pair tiles.
+  bool add_dual_problem(int m, int n, void *out, long long ldc, void *out2, long long ldc2, int a_map,
+                        int b_map, int b2_map, long long k);
+  bool dual = false;  // some problem has two outputs (forces the SM-pair kernel, no split)
   tp_status launch(cudaStream_t stream);
 };
 

@@ -360,3 +360,51 @@ def test_decoder_layer_tp8_t4096_sampled_rows(combine):
     ym, _h = L.mlp(combine)
     for r in range(copies):
         assert_close(host_f64(ym[r])[rows], ref["y_mlp"], BF16_TOL, f"MLP Y, rank {r}")
+
+
+@pytest.mark.parametrize("tp_size,hq,hkv,hd,T", [(8, 64, 8, 128, 600), (4, 16, 4, 64, 300), (8, 16, 2, 64, 257)])
+def test_qkv_paired_kv_tiles_equal_separate_problems(tp_size, hq, hkv, hd, T):
+    """Where each rank's k and v projections are at most 128 columns wide, the
+    SM-pair kernel computes them in one 256-column tile (k's weight rows in one
+    CTA, v's in the other). Each output element is the same MMA sequence as with
+    separate problems, so the bits agree with TPGQA_QKV_PAIRED=0; and q/k/v match
+    the oracle."""
+    import os
+    need_gpu()
+    t = torch()
+    w = dict(kind="attn", T=T, hidden=256, q_heads=hq, kv_heads=hkv, head_dim=hd, tp=tp_size, seed=41,
+             w_std=0.05)
+    data = inputs.make_bf16_inputs(w)
+    L = Layer(w, data)
+    f = {k: inputs.bf16_bits_to_f64(v) for k, v in data.items()}
+    nkv = 1 if L.shards[0]["kv_replicated"] else tp_size
+    wq = [L.dev["wq"][slice(*L.rng(r, "q_proj"))] for r in range(tp_size)]
+    wk = [L.dev["wk"][slice(*L.rng(r, "k_proj"))] for r in range(nkv)]
+    wv = [L.dev["wv"][slice(*L.rng(r, "v_proj"))] for r in range(nkv)]
+
+    def run(paired):
+        q = [t.full((T, x.shape[0]), float("nan"), dtype=t.bfloat16, device="cuda") for x in wq]
+        k = [t.full((T, x.shape[0]), float("nan"), dtype=t.bfloat16, device="cuda") for x in wk]
+        v = [t.full((T, x.shape[0]), float("nan"), dtype=t.bfloat16, device="cuda") for x in wv]
+        old = os.environ.get("TPGQA_QKV_PAIRED")
+        os.environ["TPGQA_QKV_PAIRED"] = "1" if paired else "0"
+        try:
+            tp.tp_qkv_proj(L.plan, L.x, wq, wk, wv, q, k, v)
+        finally:
+            if old is None:
+                del os.environ["TPGQA_QKV_PAIRED"]
+            else:
+                os.environ["TPGQA_QKV_PAIRED"] = old
+        t.cuda.synchronize()
+        return [host_bits_f32(a.view(t.int16).to(t.int32)) for a in q + k + v], (q, k, v)
+
+    bits_p, (q, k, v) = run(True)
+    bits_s, _ = run(False)
+    for i, (a, b) in enumerate(zip(bits_p, bits_s)):
+        assert np.array_equal(a, b), f"output {i}"
+    ref = O.attn_proj_sharded(f["x"], f["wq"], f["wk"], f["wv"], f["a"], f["wo"], _oracle_plan(w), hd)
+    for r in range(tp_size):
+        assert_close(host_f64(q[r]), ref["q"][r], BF16_TOL, f"q[{r}]")
+    for r in range(nkv):
+        assert_close(host_f64(k[r]), ref["k"][r], BF16_TOL, f"k[{r}]")
+        assert_close(host_f64(v[r]), ref["v"][r], BF16_TOL, f"v[{r}]")
