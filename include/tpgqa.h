@@ -20,6 +20,17 @@
  *  - Streams: every call that touches device memory only enqueues work on
  *    `stream` (a cudaStream_t; NULL = the legacy default stream) and returns
  *    without synchronising. Buffers must stay valid until that work is done.
+ *  - Overlap: kernels are launched with programmatic dependent launch, so a
+ *    call's kernels may start while the previous kernel on the stream is still
+ *    running; they wait for it before touching activations, outputs or
+ *    workspaces. Weights (the w arguments of the GEMM calls, which no earlier
+ *    kernel of a step writes) are read from the start, so the first weight
+ *    tiles stream in during the previous kernel's tail. A weight buffer must
+ *    therefore not be written by the kernel that immediately precedes its use
+ *    on the same stream (put an event wait, a host synchronisation or other
+ *    work in between), or set the environment variable TPGQA_EARLY_B=0 (read at
+ *    every launch) to make weight loads wait as well. Block-table (MoE) GEMMs
+ *    never read weights early.
  *  - Pointers: tp_tensor.ptr is a device pointer. Arrays of tp_tensor
  *    (per-rank arguments) are host arrays, read during the call only.
  *  - Errors: every call returns a tp_status and never aborts. Arguments are

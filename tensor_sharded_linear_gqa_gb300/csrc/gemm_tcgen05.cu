@@ -265,6 +265,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Weights do not come from the previous kernel: the producer starts the B
+  // loads of its first stages before the grid-dependency wait (each stage's
+  // barrier expects the A bytes too, which follow the wait).
+  int pre = 0;  // leading k-blocks whose B loads were issued early (thread 0 only)
+  if (warp == 0 && lane == 0 && p.early_b) {
+    Cursor c;
+    cursor_tile(p, c, blockIdx.x);
+    for (; pre < kStagesRt && c.valid; ++pre) {
+      const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
+      ptx::mbar_arrive_expect_tx(full_bar(pre), static_cast<uint32_t>(p.a_rows * 128 + C::kBBytes));
+      ptx::tma_load_2d(b_slot(pre), &p.maps[sg.b_map + c.moff], c.kt * BK, c.brow + c.nt * kBRows, full_bar(pre));
+      if (EPI == kEpiSwiGLU)
+        ptx::tma_load_2d(b_slot(pre) + kBRows * 128, &p.maps[sg.b2_map + c.moff], c.kt * BK,
+                         c.brow + c.nt * kBRows, full_bar(pre));
+      cursor_next(p, c);
+    }
+  }
   // Prologue done: wait for the previous kernel in the stream, then let the next one launch.
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
@@ -294,12 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
         const int st = kb % kStagesRt;
         const uint32_t ph = (kb / kStagesRt) & 1;
         if (*abort_flag) break;
+        const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
+        if (kb < pre) {  // B already in flight, the stage's barrier already armed: A only
+          ptx::tma_load_2d(a_slot(st), &p.maps[sg.a_map], ld.kt * BK, ld.mt * BM, full_bar(st));
+          issued = ++kb;
+          cursor_next(p, ld);
+          continue;
+        }
         if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
           record(p.status, kDevTimeoutProducer);
           *abort_flag = 1;
           break;
         }
-        const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
         ptx::mbar_arrive_expect_tx(full_bar(st), static_cast<uint32_t>(p.a_rows * 128 + C::kBBytes));
         ptx::tma_load_2d(a_slot(st), &p.maps[sg.a_map], ld.kt * BK, ld.mt * BM, full_bar(st));
         ptx::tma_load_2d(b_slot(st), &p.maps[sg.b_map + ld.moff], ld.kt * BK, ld.brow + ld.nt * kBRows,
@@ -444,6 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
     for (int kb = first; kb < issued; ++kb)
       if (!ptx::mbar_wait(full_bar(kb % kStagesRt), (kb / kStagesRt) & 1, p.wait_ns))
         record(p.status, kDevTimeoutDrain);
+    if (pre > issued) {
+      // early B loads whose stage never received its A: their barrier cannot
+      // complete, so give the copies time to land
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+      }
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -553,6 +583,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Weights do not come from the previous kernel: the B loads of the first
+  // tile's first stages start before the grid-dependency wait, their A loads
+  // after it (block tables, written by an earlier kernel, never load early).
+  int pre = 0;
+  if (warp == 0 && lane == 0 && p.early_b && pair < p.total_tiles) {
+    const GemmProblem &pr = p.prob[find_problem(p, pair)];
+    const int nt = (pair - pr.tile_begin) / pr.m_tiles;
+    for (int sgi = 0; sgi < pr.seg_count && pre < S; ++sgi) {
+      const GemmSeg &sg = p.seg[pr.seg_begin + sgi];
+      const bool two_b = EPI == kEpiSwiGLU || sg.b2_map >= 0;
+      const int map = two_b ? (leader ? sg.b_map : sg.b2_map) : sg.b_map;
+      const int row = two_b ? nt * kHalfB : nt * BN + static_cast<int>(rank) * kHalfB;
+      for (int kt = 0; kt < seg_stages<KSUB>(sg) && pre < S; ++kt, ++pre) {
+        const uint32_t lead_full = ptx::mapa_shared(full_bar(pre), 0);
+        if (leader) ptx::mbar_arrive_expect_tx(full_bar(pre), 2 * kPairStageBytes);
+        if (p.box_kt > 1) {
+          ptx::tma_load_3d_pair(sB0 + pre * kPairSub * kPairBBytes, &p.maps[map], 0, row, kt * kPairSub, lead_full);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kPairSub; ++j)
+            ptx::tma_load_2d_pair(sB0 + (pre * kPairSub + j) * kPairBBytes, &p.maps[map], (kt * kPairSub + j) * BK,
+                                  row, lead_full);
+        }
+      }
+    }
+  }
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
@@ -626,13 +682,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int st = kb % S;
         const uint32_t ph = (kb / S) & 1;
         if (*abort_flag) break;
-        if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
+        const bool early = kb < pre;  // B already in flight and the stage's barrier armed
+        if (!early && !ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
           record(p.status, kDevTimeoutProducer);
           *abort_flag = 1;
           break;
         }
         const uint32_t lead_full = ptx::mapa_shared(full_bar(st), 0);
-        if (leader) ptx::mbar_arrive_expect_tx(full_bar(st), 2 * kPairStageBytes);
+        if (leader && !early) ptx::mbar_arrive_expect_tx(full_bar(st), 2 * kPairStageBytes);
         const GemmSeg &sg = p.seg[p.prob[ld.prob].seg_begin + ld.seg];
         int m, r;
         b_src(ld, m, r);
@@ -641,8 +698,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // one copy per operand brings the stage's KSUB k-tiles (3-D maps)
           ptx::tma_load_3d_pair(sA0 + st * kPairSub * kPairABytes, &p.maps[sg.a_map], 0, a_row,
                                 ld.kt * kPairSub, lead_full);
-          ptx::tma_load_3d_pair(sB0 + st * kPairSub * kPairBBytes, &p.maps[m], 0, r, ld.kt * kPairSub,
-                                lead_full);
+          if (!early)
+            ptx::tma_load_3d_pair(sB0 + st * kPairSub * kPairBBytes, &p.maps[m], 0, r, ld.kt * kPairSub,
+                                  lead_full);
         } else {
 #pragma unroll
           for (int j = 0; j < kPairSub; ++j) {
@@ -650,7 +708,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int x = (ld.kt * kPairSub + j) * BK;
             ptx::tma_load_2d_pair(sA0 + (st * kPairSub + j) * kPairABytes, &p.maps[sg.a_map], x, a_row,
                                   lead_full);
-            ptx::tma_load_2d_pair(sB0 + (st * kPairSub + j) * kPairBBytes, &p.maps[m], x, r, lead_full);
+            if (!early)
+              ptx::tma_load_2d_pair(sB0 + (st * kPairSub + j) * kPairBBytes, &p.maps[m], x, r, lead_full);
           }
         }
         ++kb;
@@ -902,6 +961,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Weights do not come from the previous kernel: the B loads of the first
+  // tile's first stages start before the grid-dependency wait.
+  int pre = 0;
+  if (warp == 0 && lane == 0 && p.early_b && pair < p.total_tiles) {
+    const int mt = pair % pr.m_tiles, nt = pair / pr.m_tiles;
+    const int b_row = nt * BN + static_cast<int>(crank) * kHalfB;
+    for (int s = 0; s < nrank && pre < S; ++s) {
+      const GemmSeg &sg = p.seg[pr.seg_begin + fold_rank(mt, s)];
+      for (int kt = 0; kt < seg_stages<KSUB>(sg) && pre < S; ++kt, ++pre) {
+        const uint32_t lead_full = ptx::mapa_shared(full_bar(pre), 0);
+        if (leader) ptx::mbar_arrive_expect_tx(full_bar(pre), 2 * PC::kStageBytes);
+        if (p.box_kt > 1) {
+          ptx::tma_load_3d_pair(sB0 + pre * KSUB * kPairBBytes, &p.maps[sg.b_map], 0, b_row, kt * KSUB, lead_full);
+        } else {
+#pragma unroll
+          for (int j = 0; j < KSUB; ++j)
+            ptx::tma_load_2d_pair(sB0 + (pre * KSUB + j) * kPairBBytes, &p.maps[sg.b_map], (kt * KSUB + j) * BK,
+                                  b_row, lead_full);
+        }
+      }
+    }
+  }
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
@@ -920,27 +1001,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int st = kb % S;
             const uint32_t ph = (kb / S) & 1;
             if (*abort_flag) { go = false; break; }
-            if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
+            const bool early = kb < pre;  // B already in flight and the stage's barrier armed
+            if (!early && !ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
               record(p.status, kDevTimeoutProducer);
               *abort_flag = 1;
               go = false;
               break;
             }
             const uint32_t lead_full = ptx::mapa_shared(full_bar(st), 0);
-            if (leader) ptx::mbar_arrive_expect_tx(full_bar(st), 2 * PC::kStageBytes);
+            if (leader && !early) ptx::mbar_arrive_expect_tx(full_bar(st), 2 * PC::kStageBytes);
             if (p.box_kt > 1) {
               ptx::tma_load_3d_pair(sA0 + st * KSUB * kPairABytes, &p.maps[sg.a_map], 0, a_row, kt * KSUB,
                                     lead_full);
-              ptx::tma_load_3d_pair(sB0 + st * KSUB * kPairBBytes, &p.maps[sg.b_map], 0, b_row, kt * KSUB,
-                                    lead_full);
+              if (!early)
+                ptx::tma_load_3d_pair(sB0 + st * KSUB * kPairBBytes, &p.maps[sg.b_map], 0, b_row, kt * KSUB,
+                                      lead_full);
             } else {
 #pragma unroll
               for (int j = 0; j < KSUB; ++j) {
                 const int x = (kt * KSUB + j) * BK;  // past the segment's K: zero fill
                 ptx::tma_load_2d_pair(sA0 + (st * KSUB + j) * kPairABytes, &p.maps[sg.a_map], x, a_row,
                                       lead_full);
-                ptx::tma_load_2d_pair(sB0 + (st * KSUB + j) * kPairBBytes, &p.maps[sg.b_map], x, b_row,
-                                      lead_full);
+                if (!early)
+                  ptx::tma_load_2d_pair(sB0 + (st * KSUB + j) * kPairBBytes, &p.maps[sg.b_map], x, b_row,
+                                        lead_full);
               }
             }
           }
@@ -1254,67 +1338,100 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem_d = *tmem_slot;
+
+  // The producer's loads of one stage: A (activations, which may come from the
+  // previous kernel) and B (weights, which do not).
+  const uint32_t stage_tx = PAIR ? 2 * C::kStageBytes : static_cast<uint32_t>(KS * (p.a_rows * 128 + C::kBBytes));
+  const int a_row = PAIR ? mt * 256 + member * 128 : mt * 128;
+  auto load_a = [&](int st, const GemmSeg &sg, int kt, uint32_t fb) {
+    if (PAIR && p.box_kt > 1) {
+      ptx::tma_load_3d_pair(sA0 + st * KS * kAT, &p.maps[sg.a_map], 0, a_row, kt * KS, fb);  // past K: zero fill
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      const int x = (kt * KS + j) * BK;  // past the segment's K: zero fill
+      const uint32_t da = sA0 + (st * KS + j) * kAT;
+      if constexpr (PAIR)
+        ptx::tma_load_2d_pair(da, &p.maps[sg.a_map], x, a_row, fb);
+      else
+        ptx::tma_load_2d(da, &p.maps[sg.a_map], x, a_row, fb);
+    }
+  };
+  auto load_b = [&](int st, const GemmSeg &sg, int kt, uint32_t fb) {
+    if (PAIR && p.box_kt > 1) {
+      const int z = kt * KS;
+      if (EPI == kEpiSwiGLU)
+        ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[member == 0 ? sg.b_map : sg.b2_map], 0,
+                              nt * 128, z, fb);
+      else
+        ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[sg.b_map], 0, nt * BN + member * 128, z, fb);
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < KS; ++j) {
+      const int x = (kt * KS + j) * BK;
+      const uint32_t db = sB0 + (st * KS + j) * C::kBBytes;
+      if constexpr (PAIR) {
+        if (EPI == kEpiSwiGLU)
+          ptx::tma_load_2d_pair(db, &p.maps[member == 0 ? sg.b_map : sg.b2_map], x, nt * 128, fb);
+        else
+          ptx::tma_load_2d_pair(db, &p.maps[sg.b_map], x, nt * BN + member * 128, fb);
+      } else {
+        if (EPI == kEpiSwiGLU) {
+          ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * (BN / 2), fb);
+          ptx::tma_load_2d(db + (BN / 2) * 128, &p.maps[sg.b2_map], x, nt * (BN / 2), fb);
+        } else {
+          ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * BN, fb);
+        }
+      }
+    }
+  };
+  // (segment, stage within the segment) of this split's first stage
+  int seg0 = 0, kt0 = k_begin;
+  while (seg0 < pr.seg_count) {
+    const int n = (p.seg[pr.seg_begin + seg0].k_tiles + KS - 1) / KS;
+    if (kt0 < n) break;
+    kt0 -= n;
+    ++seg0;
+  }
+  // Weights do not come from the previous kernel: the B loads of the first
+  // stages start before the grid-dependency wait, their A loads after it.
+  int pre = 0;
+  if (warp == 0 && lane == 0 && p.early_b) {
+    int seg = seg0, kt = kt0;
+    for (; pre < S && pre < k_end - k_begin; ++pre) {
+      const GemmSeg &sg = p.seg[pr.seg_begin + seg];
+      if (issuer) ptx::mbar_arrive_expect_tx(full_bar(pre), stage_tx);
+      load_b(pre, sg, kt, PAIR ? ptx::mapa_shared(full_bar(pre), lead) : full_bar(pre));
+      if (++kt == (sg.k_tiles + KS - 1) / KS) {
+        kt = 0;
+        ++seg;
+      }
+    }
+  }
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
-      // position (segment, stage within segment) of global stage k_begin
-      int seg = 0, kt = k_begin;
-      while (seg < pr.seg_count) {
-        const int n = (p.seg[pr.seg_begin + seg].k_tiles + KS - 1) / KS;
-        if (kt < n) break;
-        kt -= n;
-        ++seg;
-      }
+      int seg = seg0, kt = kt0;
       for (int kb = 0; kb < k_end - k_begin; ++kb) {
         const int st = kb % S;
         const uint32_t ph = (kb / S) & 1;
         if (*abort_flag) break;
-        if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
-          record(p.status, kDevTimeoutProducer);
-          *abort_flag = 1;
-          break;
-        }
         const GemmSeg &sg = p.seg[pr.seg_begin + seg];
-        if (issuer)
-          ptx::mbar_arrive_expect_tx(full_bar(st), PAIR ? 2 * C::kStageBytes
-                                                        : static_cast<uint32_t>(KS * (p.a_rows * 128 + C::kBBytes)));
         const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(st), lead) : full_bar(st);
-        const int a_row = PAIR ? mt * 256 + member * 128 : mt * 128;
-        if (PAIR && p.box_kt > 1) {
-          // 3-D maps: one copy per operand brings the stage's KS k-tiles
-          const int z = kt * KS;  // past the segment's K: zero fill
-          ptx::tma_load_3d_pair(sA0 + st * KS * kAT, &p.maps[sg.a_map], 0, a_row, z, fb);
-          if (EPI == kEpiSwiGLU)
-            ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[member == 0 ? sg.b_map : sg.b2_map], 0,
-                                  nt * 128, z, fb);
-          else
-            ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[sg.b_map], 0, nt * BN + member * 128, z,
-                                  fb);
-        } else {
-#pragma unroll
-          for (int j = 0; j < KS; ++j) {
-            const int x = (kt * KS + j) * BK;  // past the segment's K: zero fill
-            const uint32_t da = sA0 + (st * KS + j) * kAT;
-            const uint32_t db = sB0 + (st * KS + j) * C::kBBytes;
-            if constexpr (PAIR) {
-              ptx::tma_load_2d_pair(da, &p.maps[sg.a_map], x, a_row, fb);
-              if (EPI == kEpiSwiGLU)
-                ptx::tma_load_2d_pair(db, &p.maps[member == 0 ? sg.b_map : sg.b2_map], x, nt * 128, fb);
-              else
-                ptx::tma_load_2d_pair(db, &p.maps[sg.b_map], x, nt * BN + member * 128, fb);
-            } else {
-              ptx::tma_load_2d(da, &p.maps[sg.a_map], x, a_row, fb);
-              if (EPI == kEpiSwiGLU) {
-                ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * (BN / 2), fb);
-                ptx::tma_load_2d(db + (BN / 2) * 128, &p.maps[sg.b2_map], x, nt * (BN / 2), fb);
-              } else {
-                ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * BN, fb);
-              }
-            }
+        if (kb >= pre) {
+          if (!ptx::mbar_wait(empty_bar(st), ph ^ 1, p.wait_ns)) {
+            record(p.status, kDevTimeoutProducer);
+            *abort_flag = 1;
+            break;
           }
+          if (issuer) ptx::mbar_arrive_expect_tx(full_bar(st), stage_tx);
+          load_b(st, sg, kt, fb);
         }
+        load_a(st, sg, kt, fb);
         if (++kt == (sg.k_tiles + KS - 1) / KS) {
           kt = 0;
           ++seg;
@@ -1962,6 +2079,16 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   p.prefetch = prefetch;
   p.a_rows = pair ? 128 : a_rows;
   p.one_stages = one_stages_for(p.a_rows, bn);
+  {
+    // TPGQA_EARLY_B=0 keeps every load behind the grid-dependency wait (read on
+    // every launch). Block tables are written by an earlier kernel and decide
+    // which weights a tile reads, so their problems never load early.
+    const char *env = getenv("TPGQA_EARLY_B");
+    bool early = !(env && env[0] == '0');
+    for (int i = 0; i < n_probs; ++i)
+      if (p.prob[i].blk) early = false;
+    p.early_b = early ? 1 : 0;
+  }
   if (split == 0) {
     // fewest k-stages of any problem decides how far K can be split
     const int ksub = pair ? 2 : 1;

@@ -142,6 +142,11 @@ struct GemmParams {
   int box_kt;    // 64-wide k-tiles per TMA copy: 1 = 2-D maps (one copy per k-tile),
                  // >1 = 3-D maps whose box spans that many k-tiles (a whole stage)
   int one_stages;  // pipeline stages of the single-CTA kernels (sized from a_rows)
+  // 1: the producer issues the weight (B) loads of its first stages before the
+  // grid-dependency wait, so they overlap the previous kernel's tail; the A
+  // loads follow the wait. Only when no problem has a block table (which an
+  // earlier kernel writes).
+  int early_b;
   // Ring-folding row-parallel kernel (0 rows = not folding): one problem whose
   // segments are the N ranks' K slices; every tile lies inside one ring chunk of
   // ring_rows rows, and its per-rank partials are added in that chunk's ring

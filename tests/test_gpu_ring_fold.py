@@ -132,3 +132,44 @@ def test_consecutive_calls_and_other_buffers_unchanged():
         assert np.array_equal(host_bits_f32(ys[0]), host_bits_f32(parts[0]))
         for y in ys[1:]:
             assert bool((y == 7.0).all())
+
+
+@pytest.mark.parametrize("kind", ["decode", "decode_splitk", "pair", "fold"])
+def test_early_weight_loads_change_no_bits(kind):
+    """The GEMM kernels start their first weight (B) loads before the wait on the
+    previous kernel; the arithmetic is unchanged, so every bit equals the run with
+    TPGQA_EARLY_B=0 (all loads after the wait), for the single-CTA, split-K,
+    SM-pair and ring-folding kernels."""
+    need_gpu()
+    torch = _torch()
+    if kind == "decode":          # 64 tokens: single-CTA persistent kernel, 152 tiles
+        T, n, D, K, combine = 64, 8, 4096, 512, tp.TP_COMBINE_NONE
+    elif kind == "decode_splitk":  # few output tiles: split-K clusters
+        T, n, D, K, combine = 64, 2, 512, 2048, tp.TP_COMBINE_NONE
+    elif kind == "pair":
+        T, n, D, K, combine = 640, 4, 1536, 384, tp.TP_COMBINE_NONE
+    else:
+        T, n, D, K, combine = 1024, 4, 768, 320, tp.TP_COMBINE_RING_FUSED
+    x, w = _layer(T, n, D, K, seed=900 + T + D)
+    xd = [dev_bf16(a) for a in x]
+    wd = [dev_bf16(a) for a in w]
+    outs = {}
+    for env in ("0", "1"):
+        old = os.environ.get("TPGQA_EARLY_B")
+        os.environ["TPGQA_EARLY_B"] = env
+        try:
+            ys = [torch.full((T, D), float("nan"), device="cuda") for _ in range(n)]
+            for _ in range(3):  # back to back, so the loads overlap the previous launch
+                tp.tp_row_linear(n, xd, wd, ys, combine)
+            torch.cuda.synchronize()
+        finally:
+            if old is None:
+                del os.environ["TPGQA_EARLY_B"]
+            else:
+                os.environ["TPGQA_EARLY_B"] = old
+        outs[env] = [host_bits_f32(y) for y in ys]
+    for r in range(n):
+        assert np.array_equal(outs["0"][r], outs["1"][r]), f"rank {r}"
+    f = inputs.bf16_bits_to_f64
+    assert_close(host_f64(ys[0]), O.linear(f(x[0]), f(w[0])) if combine == tp.TP_COMBINE_NONE else
+                 sum(O.linear(f(a), f(b)) for a, b in zip(x, w)), BF16_TOL, "result")
