@@ -505,8 +505,10 @@ template <int KSUB, int BN>
 struct PairCfg {
   static constexpr int kBRows = BN / 2;
   static constexpr int kBBytes = kBRows * BK * 2;  // one 64-wide k-tile of this CTA's B rows
-  static constexpr int kStages = 6 / KSUB;
   static constexpr int kStageBytes = KSUB * (kPairABytes + kBBytes);
+  // as many stages as fit beside the barriers: 3 for 256- and 224-column tiles
+  // of 128-deep stages, 4 for 128-column tiles
+  static constexpr int kStages = (kSmemLimit - 1280) / kStageBytes > 4 ? 4 : (kSmemLimit - 1280) / kStageBytes;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
   static_assert(kBBytes % 1024 == 0, "B k-tiles must keep the 1024-byte swizzle alignment");
 };
@@ -1813,6 +1815,8 @@ int pair_ksub() {
 template <int EPI>
 tp_status launch_pair(const GemmParams &p, int bn, cudaStream_t stream) {
   if (bn == 224) return launch_pair_ks<EPI, 2, 224>(p, stream);
+  if (bn == 128) return launch_pair_ks<EPI, 2, 128>(p, stream);
+  if (bn != 256) return TP_ERR_UNSUPPORTED;
   return pair_ksub() == 2 ? launch_pair_ks<EPI, 2, 256>(p, stream) : launch_pair_ks<EPI, 3, 256>(p, stream);
 }
 
@@ -1844,6 +1848,8 @@ tp_status launch_pair_ring_ks(const GemmParams &p, cudaStream_t stream) {
 // the GEMM without a combine bit for bit.
 tp_status launch_pair_ring(const GemmParams &p, int bn, cudaStream_t stream) {
   if (bn == 224) return launch_pair_ring_ks<2, 224>(p, stream);
+  if (bn == 128) return launch_pair_ring_ks<2, 128>(p, stream);
+  if (bn != 256) return TP_ERR_UNSUPPORTED;
   return pair_ksub() == 2 ? launch_pair_ring_ks<2, 256>(p, stream) : launch_pair_ring_ks<3, 256>(p, stream);
 }
 
@@ -2220,7 +2226,7 @@ int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, 
     return e ? atoi(e) : 0;
   }();
   int best = 256;
-  if (forced == 224 || forced == 256) {
+  if (forced == 128 || forced == 224 || forced == 256) {
     best = forced;
   } else {
     // A tile's time goes with its stage bytes (the loads bound the pair's
