@@ -34,6 +34,7 @@
 // k_transpose_bf16: V [T x C] -> V^T [C x T] through 64 x 64 shared tiles.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -442,6 +443,380 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
   }
 }
 
+// ---------------------------------------------------------------------------
+// k_attention2: two query tiles per work item. An item is a pair of adjacent
+// 128-query tiles (2i, 2i+1) of one q head, so the causal work of the two is
+// nearly equal and every K / V^T tile loaded serves both. Warp roles:
+//   warp 0     TMA producers: lane 0 loads the item's two Q tiles and the K
+//              ring (2 stages), lane 1 the V^T ring (2 stages);
+//   warp 1     MMA issuer, in the order S_A(0), S_B(0), P_A(0)V, S_A(1),
+//              P_B(0)V, S_B(1), ...: while one tile's softmax runs, the
+//              tensor core works on the other tile;
+//   warps 2-5  softmax of tile A, warps 6-9 of tile B: one thread per query
+//              row (its TMEM lane) over all 128 keys of a block, so no row
+//              value is exchanged between threads.
+// TMEM: S of tile A at columns 0-127, of tile B at 128-255, O of A at 256-383,
+// of B at 384-511. The softmax writes P as bf16 over the first 64 columns of its
+// S (two values per 32-bit column), and P V reads it from there as the A
+// operand (the tensor-memory form of tcgen05.mma), so P never goes through
+// shared memory. S of the next block is issued after P V of this one, which has
+// read P by then (the tensor core runs one issuer's MMAs in order). The
+// reference maximum moves only when a block's maximum exceeds it by more than
+// 8 (log2 units); then that row of O is rescaled in TMEM: O is current up to the
+// previous block whenever S of a block is complete, so no extra wait is needed.
+// Every wait is bounded, as in k_attention.
+// ---------------------------------------------------------------------------
+constexpr uint32_t k2SmemQ = 0, k2SmemK = 2 * kTile, k2SmemV = 4 * kTile;  // Q_A, Q_B; K ring; V^T ring
+constexpr uint32_t k2SmemBar = 6 * kTile;
+constexpr size_t kAttn2Smem = k2SmemBar + 256 + 1024;  // + barriers + alignment slack (193.3 KB)
+
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t sQ = sbase + k2SmemQ, sK0 = sbase + k2SmemK, sV0 = sbase + k2SmemV;
+  uint8_t *bar_area = smem + k2SmemBar;
+  const uint32_t bar0 = ptx::smem_addr(bar_area);
+  // barriers (8 bytes each): per tile X in {0 = A, 1 = B}: s_full, p_full, o_full, o_free
+  const uint32_t q_full = bar0, q_empty = bar0 + 8, k_full0 = bar0 + 16, k_empty0 = bar0 + 32,
+                 v_full0 = bar0 + 48, v_empty0 = bar0 + 64, s_full0 = bar0 + 80, p_full0 = bar0 + 96,
+                 o_full0 = bar0 + 112, o_free0 = bar0 + 128, drain = bar0 + 144;
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 152);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 156);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kv_blocks = (p.tokens + kTileK - 1) / kTileK;
+  const int pairs = (p.q_tiles + 1) / 2;
+  const int items = pairs * p.heads_total;
+  // work item -> (first query tile, blocks of tile A, blocks of tile B, head);
+  // causal runs the longest pairs first; a tile past the sequence has no blocks
+  auto item = [&](int it, int &qt0, int &nba, int &nbb) -> const AttnHead & {
+    const int r = it / p.heads_total;
+    const int pi = p.causal ? pairs - 1 - r : r;
+    qt0 = 2 * pi;
+    nba = p.causal ? qt0 + 1 : kv_blocks;
+    nbb = qt0 + 1 < p.q_tiles ? (p.causal ? qt0 + 2 : kv_blocks) : 0;
+    return p.heads[it % p.heads_total];
+  };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(k_full0 + 8 * s, 1);
+      ptx::mbar_init(k_empty0 + 8 * s, 1);
+      ptx::mbar_init(v_full0 + 8 * s, 1);
+      ptx::mbar_init(v_empty0 + 8 * s, 1);
+      ptx::mbar_init(s_full0 + 8 * s, 1);
+      ptx::mbar_init(p_full0 + 8 * s, 128);
+      ptx::mbar_init(o_full0 + 8 * s, 1);
+      ptx::mbar_init(o_free0 + 8 * s, 128);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+
+  int issued[2] = {0, 0};  // loads started per stage of this producer lane's ring
+  int q_loads = 0;
+  if (warp == 0) {
+    if (lane < 2) {
+      // lane 0: the Q tiles of each item, then the K ring; lane 1: the V^T ring
+      const uint32_t full0 = lane == 0 ? k_full0 : v_full0, empty0 = lane == 0 ? k_empty0 : v_empty0;
+      const uint32_t dst0 = lane == 0 ? sK0 : sV0;
+      bool run = true;
+      int g = 0;
+      for (int it = blockIdx.x, ic = 0; run && it < items; it += gridDim.x, ++ic) {
+        int qt0, nba, nbb;
+        const AttnHead &hd = item(it, qt0, nba, nbb);
+        const int nbm = nba > nbb ? nba : nbb;
+        if (lane == 0) {
+          // the previous item's last S has read both Q tiles
+          if (*abort_flag || !ptx::mbar_wait(q_empty, (ic & 1) ^ 1, p.wait_ns)) {
+            if (!*abort_flag) record(p.status, kDevTimeoutProducer);
+            *abort_flag = 1;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(q_full, nbb > 0 ? 2 * kTile : kTile);
+          for (int t = 0; t < (nbb > 0 ? 2 : 1); ++t)
+            for (int c = 0; c < 2; ++c)
+              ptx::tma_load_2d(sQ + t * kTile + c * kSub, &p.maps[hd.q_map], hd.q_col + c * 64,
+                               (qt0 + t) * kTileQ, q_full);
+          ++q_loads;
+        }
+        const CUtensorMap *map = &p.maps[lane == 0 ? hd.k_map : hd.v_map];
+        for (int j = 0; j < nbm; ++j, ++g) {
+          const int s = g & 1;
+          if (*abort_flag || !ptx::mbar_wait(empty0 + 8 * s, ((g >> 1) & 1) ^ 1, p.wait_ns)) {
+            if (!*abort_flag) record(p.status, kDevTimeoutProducer);
+            *abort_flag = 1;
+            run = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(full0 + 8 * s, kTile);
+          for (int c = 0; c < 2; ++c) {
+            if (lane == 0)
+              ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, hd.kv_col + c * 64, j * kTileK, full0 + 8 * s);
+            else
+              ptx::tma_load_2d(dst0 + s * kTile + c * kSub, map, j * kTileK + c * 64, hd.kv_col, full0 + 8 * s);
+          }
+          ++issued[s];
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileQ, 128);
+      bool ok = true;
+      auto fail = [&]() {
+        if (!*abort_flag) record(p.status, kDevTimeoutMma);
+        ok = false;
+      };
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (*abort_flag || !ptx::mbar_wait(bar, parity, p.wait_ns)) {
+          fail();
+          return false;
+        }
+        return true;
+      };
+      // S_X = Q_X K^T for the K stage of block g, into tile X's S columns
+      auto issue_s = [&](int x, int g) {
+        const uint32_t d = tmem + static_cast<uint32_t>(x * 128);
+        const uint32_t kq = sQ + static_cast<uint32_t>(x) * kTile, kk0 = sK0 + static_cast<uint32_t>(g & 1) * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kHd / 16; ++kk) {
+          const uint64_t ad = ptx::smem_desc_sw128(kq + (kk >> 2) * kSub) + 2 * (kk & 3);
+          const uint64_t bd = ptx::smem_desc_sw128(kk0 + (kk >> 2) * kSub) + 2 * (kk & 3);
+          ptx::mma_bf16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(s_full0 + 8 * x);
+      };
+      // O_X += P_X V^T_g, P_X read from tile X's S columns in tensor memory
+      auto issue_pv = [&](int x, int g, bool first) {
+        const uint32_t d = tmem + 256u + static_cast<uint32_t>(x * 128);
+        const uint32_t a = tmem + static_cast<uint32_t>(x * 128);
+        const uint32_t vv = sV0 + static_cast<uint32_t>(g & 1) * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kTileK / 16; ++kk) {
+          const uint64_t bd = ptx::smem_desc_sw128(vv + (kk >> 2) * kSub) + 2 * (kk & 3);
+          ptx::mma_bf16_ts(d, a + 8u * kk, bd, idesc, (!first || kk > 0) ? 1u : 0u);
+        }
+      };
+      int g = 0;                    // K / V blocks over all items
+      uint32_t np[2] = {0, 0};      // softmax hand-offs consumed per tile
+      uint32_t nact[2] = {0, 0};    // items in which the tile was active
+      for (int it = blockIdx.x, ic = 0; ok && it < items; it += gridDim.x, ++ic) {
+        int qt0, nba, nbb;
+        item(it, qt0, nba, nbb);
+        const int nb[2] = {nba, nbb};
+        const int nbm = nba > nbb ? nba : nbb;
+        if (!wait(q_full, ic & 1)) break;
+        // S of block 0 of both tiles
+        if (!wait(k_full0 + 8 * (g & 1), (g >> 1) & 1)) break;
+        ptx::tc_fence_after();
+        for (int x = 0; x < 2; ++x)
+          if (nb[x] > 0) issue_s(x, g);
+        ptx::mma_commit(k_empty0 + 8 * (g & 1));
+        if (nbm == 1) ptx::mma_commit(q_empty);
+        for (int j = 0; ok && j < nbm; ++j) {
+          const int gj = g + j;
+          if (!wait(v_full0 + 8 * (gj & 1), (gj >> 1) & 1)) break;
+          bool next_k = false;  // K of block j+1 waited for
+          for (int x = 0; ok && x < 2; ++x) {
+            if (j >= nb[x]) continue;
+            // P_X(j) is in TMEM; the item's first P V overwrites O_X, so its previous
+            // item's output must have been read
+            if (!wait(p_full0 + 8 * x, np[x] & 1)) break;
+            ++np[x];
+            if (j == 0 && !wait(o_free0 + 8 * x, (nact[x] & 1) ^ 1)) break;
+            ptx::tc_fence_after();
+            issue_pv(x, gj, j == 0);
+            if (j + 1 == nb[x]) {
+              ptx::mma_commit(o_full0 + 8 * x);  // O_X complete for this item
+            } else {
+              if (!next_k) {
+                if (!wait(k_full0 + 8 * ((gj + 1) & 1), ((gj + 1) >> 1) & 1)) break;
+                ptx::tc_fence_after();
+                next_k = true;
+              }
+              issue_s(x, gj + 1);
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit(v_empty0 + 8 * (gj & 1));  // V of block j read by every P V of it
+          if (next_k) {
+            ptx::mma_commit(k_empty0 + 8 * ((gj + 1) & 1));  // K of block j+1 read by every S of it
+            if (j + 2 == nbm) ptx::mma_commit(q_empty);        // the item's last S is issued
+          }
+        }
+        for (int x = 0; x < 2; ++x)
+          if (nb[x] > 0) ++nact[x];
+        g += nbm;
+      }
+      if (!ok) *abort_flag = 1;
+      ptx::mma_commit(drain);
+      if (!ptx::mbar_wait(drain, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    }
+  } else {
+    // ---- softmax: warps 2-5 tile A, 6-9 tile B; warp w reads TMEM lanes [32*(w%4), +32) ----
+    const int x = (warp - 2) >> 2;  // 0 = tile A, 1 = tile B
+    const int qw = warp & 3;
+    const int row = qw * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(x * 128);   // S, then P over its first half
+    const uint32_t ob = tmem + lane_off + 256u + static_cast<uint32_t>(x * 128);
+    const uint32_t s_full = s_full0 + 8 * x, p_full = p_full0 + 8 * x, o_full = o_full0 + 8 * x,
+                   o_free = o_free0 + 8 * x;
+    bool ok = true;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool ready = ptx::mbar_wait(bar, parity, p.wait_ns);
+      if (!__all_sync(0xffffffffu, ready && *abort_flag == 0)) {
+        if (lane == 0) {
+          if (!ready) record(p.status, kDevTimeoutEpilogue);
+          *abort_flag = 1;
+        }
+        return false;
+      }
+      return true;
+    };
+    uint32_t gs = 0, nact = 0;  // S blocks of this tile consumed; items it was active in
+    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      int qt0, nba, nbb;
+      const AttnHead &hd = item(it, qt0, nba, nbb);
+      const int nb = x == 0 ? nba : nbb;
+      if (nb == 0) continue;
+      const int qrow = (qt0 + x) * kTileQ + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nb; ++j, ++gs) {
+        if (!wait_all(s_full, gs & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const int k0 = j * kTileK;
+        // keys past the query (causal) or past the sequence are masked
+        const int lim = min(p.causal ? qrow - k0 + 1 : kTileK, p.tokens - k0);
+        uint32_t v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t (&vc)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]);
+          ptx::tmem_ld_32cols(sb + 32 * c, vc);
+        }
+        ptx::tmem_ld_wait();
+        ptx::tmem_regs_ready(v);
+        if (!__all_sync(0xffffffffu, lim >= kTileK)) {  // a masked key in this warp's rows
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) v[i] = __float_as_uint(-INFINITY);
+        }
+        float mx = __uint_as_float(v[127]);
+#pragma unroll
+        for (int i = 0; i < 126; i += 2) mx = max3f(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+        mx = fmaxf(mx, __uint_as_float(v[126]));
+        const float m_blk = mx * p.scale_log2;
+        const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
+        const float m_new = move ? m_blk : m;
+        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
+        // p = 2^(s*c - m), two keys at a time (packed f32x2 fma and sum), packed as
+        // bf16 pairs into the first 64 columns of S, 16 columns at a time
+        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
+        uint64_t sum2 = pack2(0.f, 0.f);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float y0, y1;
+            unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
+                    y1);
+            const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
+            sum2 = add2(sum2, pack2(a0, a1));
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
+            memcpy(&pk[i >> 1], &hb, 4);
+          }
+          ptx::tmem_st_16cols(sb + 16 * h, pk);
+        }
+        float s0, s1;
+        unpack2(sum2, s0, s1);
+        l = l * alpha + (s0 + s1);
+        m = m_new;
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          // O holds P V up to block j-1 (S_j completes after that P V) and block j's
+          // P V waits for this thread's hand-off; rows keeping their maximum scale by 1
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld_32cols(ob + c * 32, o);
+            ptx::tmem_ld_wait();
+            ptx::tmem_regs_ready(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st_32cols(ob + c * 32, o);
+          }
+        }
+        ptx::tmem_st_wait();   // P (and a rescaled O) in tensor memory before the hand-off
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      // the item's output: O / l once its last P V has landed
+      if (!wait_all(o_full, nact & 1)) { ok = false; break; }
+      ++nact;
+      ptx::tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32cols(ob + c * 32, v);
+        ptx::tmem_ld_wait();
+        ptx::tmem_regs_ready(v);
+        if (qrow < p.tokens) {
+          __nv_bfloat16 *dst =
+              static_cast<__nv_bfloat16 *>(hd.out) + static_cast<long long>(qrow) * hd.out_ld + c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
+            memcpy(&w.x, &h0, 4);
+            memcpy(&w.y, &h1, 4);
+            memcpy(&w.z, &h2, 4);
+            memcpy(&w.w, &h3, 4);
+            *reinterpret_cast<uint4 *>(dst + i) = w;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(o_free);  // O_X may be overwritten by the next item's first P V
+    }
+  }
+
+  // ---- teardown: every TMA load this CTA started has landed before it exits ----
+  __syncthreads();
+  if (warp == 0 && lane < 2) {
+    if (q_loads > 0 && !ptx::mbar_wait(q_full, (q_loads - 1) & 1, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    const uint32_t full0 = lane == 0 ? k_full0 : v_full0;
+    for (int s = 0; s < 2; ++s)
+      if (issued[s] > 0 && !ptx::mbar_wait(full0 + 8 * s, (issued[s] - 1) & 1, p.wait_ns))
+        record(p.status, kDevTimeoutDrain);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // V [T x C] (row pitch ld_in) -> V^T [C x T] (row pitch ld_out) for every kv
 // source in one launch (grid z = source), 64 x 64 tiles through shared memory.
 __global__ void __launch_bounds__(256) k_transpose_bf16(TransposeArgs a) {
@@ -487,14 +862,25 @@ tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
     if (dev >= 64 || !(configured & (1ULL << dev))) {
       e = cudaFuncSetAttribute(k_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kAttnSmem));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attention2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kAttn2Smem));
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 64) configured |= 1ULL << dev;
     }
   }
   p.heads_total = total_heads;
-  const long long items = static_cast<long long>(p.q_tiles) * total_heads;
+  // Two query tiles per work item by default; TPGQA_ATTN=1 runs the kernel with
+  // one query tile per item (read on every call).
+  const char *env = getenv("TPGQA_ATTN");
+  if (env && env[0] == '1') {
+    const long long items = static_cast<long long>(p.q_tiles) * total_heads;
+    const dim3 grid(static_cast<unsigned>(items < num_sms() ? items : num_sms()));
+    return launch_checked(launch_kernel(k_attention, grid, dim3(kAttnThreads), kAttnSmem, s, 1, p));
+  }
+  const long long items = static_cast<long long>((p.q_tiles + 1) / 2) * total_heads;
   const dim3 grid(static_cast<unsigned>(items < num_sms() ? items : num_sms()));
-  return launch_checked(launch_kernel(k_attention, grid, dim3(kAttnThreads), kAttnSmem, s, 1, p));
+  return launch_checked(launch_kernel(k_attention2, grid, dim3(kAttnThreads), kAttn2Smem, s, 1, p));
 }
 
 }  // namespace tpgqa
