@@ -489,8 +489,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
   const int kv_blocks = (p.tokens + kTileK - 1) / kTileK;
   const int pairs = (p.q_tiles + 1) / 2;
   const int items = pairs * p.heads_total;
+  // This CTA's r-th item: ranks in snake order over the CTAs (r-th round forward
+  // when r is even, backward when odd), so with the longest items ranked first
+  // every CTA's total stays close to the mean. -1 past the last item.
+  auto rank_of = [&](int r) {
+    const int pos = (r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                            : static_cast<int>(blockIdx.x);
+    const int k = r * static_cast<int>(gridDim.x) + pos;
+    return k < items ? k : -1;
+  };
   // work item -> (first query tile, blocks of tile A, blocks of tile B, head);
-  // causal runs the longest pairs first; a tile past the sequence has no blocks
+  // causal ranks the longest pairs first; a tile past the sequence has no blocks
   auto item = [&](int it, int &qt0, int &nba, int &nbb) -> const AttnHead & {
     const int r = it / p.heads_total;
     const int pi = p.causal ? pairs - 1 - r : r;
@@ -537,7 +546,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
       const uint32_t dst0 = lane == 0 ? sK0 : sV0;
       bool run = true;
       int g = 0;
-      for (int it = blockIdx.x, ic = 0; run && it < items; it += gridDim.x, ++ic) {
+      for (int ic = 0, it = rank_of(0); run && it >= 0; it = rank_of(++ic)) {
         int qt0, nba, nbb;
         const AttnHead &hd = item(it, qt0, nba, nbb);
         const int nbm = nba > nbb ? nba : nbb;
@@ -616,7 +625,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
       int g = 0;                    // K / V blocks over all items
       uint32_t np[2] = {0, 0};      // softmax hand-offs consumed per tile
       uint32_t nact[2] = {0, 0};    // items in which the tile was active
-      for (int it = blockIdx.x, ic = 0; ok && it < items; it += gridDim.x, ++ic) {
+      for (int ic = 0, it = rank_of(0); ok && it >= 0; it = rank_of(++ic)) {
         int qt0, nba, nbb;
         item(it, qt0, nba, nbb);
         const int nb[2] = {nba, nbb};
@@ -691,7 +700,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
       return true;
     };
     uint32_t gs = 0, nact = 0;  // S blocks of this tile consumed; items it was active in
-    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+    for (int ic = 0, it = rank_of(0); ok && it >= 0; it = rank_of(++ic)) {
       int qt0, nba, nbb;
       const AttnHead &hd = item(it, qt0, nba, nbb);
       const int nb = x == 0 ? nba : nbb;
@@ -717,10 +726,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
           for (int i = 0; i < 128; ++i)
             if (i >= lim) v[i] = __float_as_uint(-INFINITY);
         }
-        float mx = __uint_as_float(v[127]);
+        // the row maximum as four independent chains over the key quarters
+        float mq[4];
 #pragma unroll
-        for (int i = 0; i < 126; i += 2) mx = max3f(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-        mx = fmaxf(mx, __uint_as_float(v[126]));
+        for (int q = 0; q < 4; ++q) {
+          mq[q] = __uint_as_float(v[32 * q + 31]);
+#pragma unroll
+          for (int i = 0; i < 30; i += 2)
+            mq[q] = max3f(mq[q], __uint_as_float(v[32 * q + i]), __uint_as_float(v[32 * q + i + 1]));
+          mq[q] = fmaxf(mq[q], __uint_as_float(v[32 * q + 30]));
+        }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         const float m_blk = mx * p.scale_log2;
         const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
         const float m_new = move ? m_blk : m;
@@ -728,9 +744,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
         // p = 2^(s*c - m), two keys at a time (packed f32x2 fma and sum), packed as
         // bf16 pairs into the first 64 columns of S, 16 columns at a time
         const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
-        uint64_t sum2 = pack2(0.f, 0.f);
+        uint64_t sumh[4];  // one running pair of sums per 32-key quarter
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
+          uint64_t &sum2 = sumh[h];
+          sum2 = pack2(0.f, 0.f);
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
@@ -745,7 +763,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
           ptx::tmem_st_16cols(sb + 16 * h, pk);
         }
         float s0, s1;
-        unpack2(sum2, s0, s1);
+        unpack2(add2(add2(sumh[0], sumh[1]), add2(sumh[2], sumh[3])), s0, s1);
         l = l * alpha + (s0 + s1);
         m = m_new;
         if (j > 0 && __any_sync(0xffffffffu, move)) {
