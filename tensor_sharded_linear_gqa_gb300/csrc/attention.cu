@@ -835,6 +835,401 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
   }
 }
 
+// ---------------------------------------------------------------------------
+// k_attention3: as k_attention2 (two query tiles of one head per work item, one
+// softmax thread per row, P in tensor memory), with blocks of 64 keys, so that
+// S, P and O of both tiles lie apart in TMEM: tile x has S at 256x, P at
+// 256x + 64 (64 bf16 keys, two per 32-bit column) and O at 256x + 128. The
+// softmax releases S as soon as it has loaded it, and the MMA warp issues the
+// tile's next S right away, so that S is ready when this block's softmax ends
+// and the softmax of consecutive blocks runs back to back; the next P is written
+// once the previous P V has read P (and updated O). Every barrier phase is
+// waited for exactly once, in order, by one side:
+//   s_full (MMA -> softmax: S ready), s_free (softmax -> MMA: S read),
+//   p_full (softmax -> MMA: P written), pv_done (MMA -> softmax: P V done, so P
+//   is free and O current), o_free (softmax -> MMA: O of the item read).
+// K tiles are 64 keys x 128 dims (two swizzled 8 KB k-tiles), V^T tiles 128 dims
+// x 64 keys (one 16 KB k-tile), in four-stage rings shared by both query tiles.
+// On causal attention over 4096 tokens (64 q heads) it takes 0.41 ms against
+// k_attention2's 0.25 ms, its tensor pipe active 30 % of the time (52 % for
+// k_attention2): k_attention2 stays the default, this kernel runs with
+// TPGQA_ATTN=3.
+// ---------------------------------------------------------------------------
+constexpr int kKb = 64;                        // keys per block
+constexpr uint32_t kKSub = 64u * 128u;         // one [64 keys x 64 dims] swizzled k-tile of K
+constexpr uint32_t kKTile = 2 * kKSub;         // a K block (all 128 dims)
+constexpr uint32_t kVTile = 128u * 128u;       // a V^T block: [128 dims x 64 keys]
+constexpr int k3Stages = 4;
+constexpr uint32_t k3SmemQ = 0, k3SmemK = 2 * kTile, k3SmemV = k3SmemK + k3Stages * kKTile;
+constexpr uint32_t k3SmemBar = k3SmemV + k3Stages * kVTile;  // 192 KB
+constexpr size_t kAttn3Smem = k3SmemBar + 256 + 1024;
+
+__global__ void __launch_bounds__(kAttnThreads, 1) k_attention3(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t sQ = sbase + k3SmemQ, sK0 = sbase + k3SmemK, sV0 = sbase + k3SmemV;
+  uint8_t *bar_area = smem + k3SmemBar;
+  const uint32_t bar0 = ptx::smem_addr(bar_area);
+  // ring barriers: k_full[4], k_empty[4], v_full[4], v_empty[4]; then per tile x:
+  // s_full, s_free, p_full, pv_done, o_free; q_full, q_empty, drain
+  auto k_full = [&](int s) { return bar0 + 8u * s; };
+  auto k_empty = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (8 + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (12 + s); };
+  auto tbar = [&](int x, int which) { return bar0 + 8u * (16 + 5 * x + which); };
+  constexpr int S_FULL = 0, S_FREE = 1, P_FULL = 2, PV_DONE = 3, O_FREE = 4;
+  const uint32_t q_full = bar0 + 8u * 26, q_empty = bar0 + 8u * 27, drain = bar0 + 8u * 28;
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * 29);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * 29 + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kv_blocks = (p.tokens + kKb - 1) / kKb;
+  const int pairs = (p.q_tiles + 1) / 2;
+  const int items = pairs * p.heads_total;
+  auto rank_of = [&](int r) {
+    const int pos = (r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                            : static_cast<int>(blockIdx.x);
+    const int k = r * static_cast<int>(gridDim.x) + pos;
+    return k < items ? k : -1;
+  };
+  // work item -> (first query tile, 64-key blocks of tile A and of tile B, head);
+  // causal ranks the longest pairs first; a tile past the sequence has no blocks
+  auto item = [&](int it, int &qt0, int &nba, int &nbb) -> const AttnHead & {
+    const int r = it / p.heads_total;
+    const int pi = p.causal ? pairs - 1 - r : r;
+    qt0 = 2 * pi;
+    const int nb_causal_a = ((qt0 + 1) * kTileQ < p.tokens ? (qt0 + 1) * kTileQ : p.tokens);
+    nba = p.causal ? (nb_causal_a + kKb - 1) / kKb : kv_blocks;
+    const int nb_causal_b = ((qt0 + 2) * kTileQ < p.tokens ? (qt0 + 2) * kTileQ : p.tokens);
+    nbb = qt0 + 1 < p.q_tiles ? (p.causal ? (nb_causal_b + kKb - 1) / kKb : kv_blocks) : 0;
+    return p.heads[it % p.heads_total];
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < k3Stages; ++s) {
+      ptx::mbar_init(k_full(s), 1);
+      ptx::mbar_init(k_empty(s), 1);
+      ptx::mbar_init(v_full(s), 1);
+      ptx::mbar_init(v_empty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(tbar(x, S_FULL), 1);
+      ptx::mbar_init(tbar(x, S_FREE), 128);
+      ptx::mbar_init(tbar(x, P_FULL), 128);
+      ptx::mbar_init(tbar(x, PV_DONE), 1);
+      ptx::mbar_init(tbar(x, O_FREE), 128);
+    }
+    ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+
+  int issued[k3Stages] = {0, 0, 0, 0};  // loads started per stage of this producer lane's ring
+  int q_loads = 0;
+  if (warp == 0) {
+    if (lane < 2) {
+      // lane 0: the Q tiles of each item, then the K ring; lane 1: the V^T ring
+      bool run = true;
+      int g = 0;
+      for (int ic = 0, it = rank_of(0); run && it >= 0; it = rank_of(++ic)) {
+        int qt0, nba, nbb;
+        const AttnHead &hd = item(it, qt0, nba, nbb);
+        const int nbm = nba > nbb ? nba : nbb;
+        if (lane == 0) {
+          if (*abort_flag || !ptx::mbar_wait(q_empty, (ic & 1) ^ 1, p.wait_ns)) {
+            if (!*abort_flag) record(p.status, kDevTimeoutProducer);
+            *abort_flag = 1;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(q_full, nbb > 0 ? 2 * kTile : kTile);
+          for (int t = 0; t < (nbb > 0 ? 2 : 1); ++t)
+            for (int c = 0; c < 2; ++c)
+              ptx::tma_load_2d(sQ + t * kTile + c * kSub, &p.maps[hd.q_map], hd.q_col + c * 64,
+                               (qt0 + t) * kTileQ, q_full);
+          ++q_loads;
+        }
+        for (int j = 0; j < nbm; ++j, ++g) {
+          const int s = g % k3Stages;
+          const uint32_t ph = (g / k3Stages) & 1;
+          const uint32_t full = lane == 0 ? k_full(s) : v_full(s), empty = lane == 0 ? k_empty(s) : v_empty(s);
+          if (*abort_flag || !ptx::mbar_wait(empty, ph ^ 1, p.wait_ns)) {
+            if (!*abort_flag) record(p.status, kDevTimeoutProducer);
+            *abort_flag = 1;
+            run = false;
+            break;
+          }
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(full, kKTile);
+            for (int c = 0; c < 2; ++c)
+              ptx::tma_load_2d(sK0 + s * kKTile + c * kKSub, &p.maps[hd.k_map], hd.kv_col + c * 64, j * kKb, full);
+          } else {
+            ptx::mbar_arrive_expect_tx(full, kVTile);
+            ptx::tma_load_2d(sV0 + s * kVTile, &p.maps[hd.v_map], j * kKb, hd.kv_col, full);
+          }
+          ++issued[s];
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(kTileQ, kKb);
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(kTileQ, kHd);
+      bool ok = true;
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (*abort_flag || !ptx::mbar_wait(bar, parity, p.wait_ns)) {
+          if (!*abort_flag) record(p.status, kDevTimeoutMma);
+          ok = false;
+          return false;
+        }
+        return true;
+      };
+      // S_x = Q_x K^T of the K stage holding block g (64 keys), into tile x's S
+      auto issue_s = [&](int x, int g) {
+        const uint32_t d = tmem + static_cast<uint32_t>(256 * x);
+        const uint32_t kq = sQ + static_cast<uint32_t>(x) * kTile, kk0 = sK0 + static_cast<uint32_t>(g % k3Stages) * kKTile;
+#pragma unroll
+        for (int kk = 0; kk < kHd / 16; ++kk) {
+          const uint64_t ad = ptx::smem_desc_sw128(kq + (kk >> 2) * kSub) + 2 * (kk & 3);
+          const uint64_t bd = ptx::smem_desc_sw128(kk0 + (kk >> 2) * kKSub) + 2 * (kk & 3);
+          ptx::mma_bf16(d, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(tbar(x, S_FULL));
+      };
+      // O_x += P_x V^T_g, P_x from tensor memory
+      auto issue_pv = [&](int x, int g, bool first) {
+        const uint32_t d = tmem + static_cast<uint32_t>(256 * x + 128);
+        const uint32_t a = tmem + static_cast<uint32_t>(256 * x + 64);
+        const uint32_t vv = sV0 + static_cast<uint32_t>(g % k3Stages) * kVTile;
+#pragma unroll
+        for (int kk = 0; kk < kKb / 16; ++kk) {
+          const uint64_t bd = ptx::smem_desc_sw128(vv) + 2 * kk;
+          ptx::mma_bf16_ts(d, a + 8u * kk, bd, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(tbar(x, PV_DONE));
+      };
+      int g = 0;                          // K / V blocks over all items
+      uint32_t ns[2] = {0, 0};            // S issued per tile (all items)
+      uint32_t np[2] = {0, 0};            // P hand-offs consumed per tile
+      uint32_t nact[2] = {0, 0};          // items in which the tile was active
+      for (int ic = 0, it = rank_of(0); ok && it >= 0; it = rank_of(++ic)) {
+        int qt0, nba, nbb;
+        item(it, qt0, nba, nbb);
+        const int nb[2] = {nba, nbb};
+        const int nbm = nba > nbb ? nba : nbb;
+        if (!wait(q_full, ic & 1)) break;
+        // S of block j of every active tile: after the softmax has read the tile's
+        // previous S (the first S of this CTA has none)
+        auto issue_block_s = [&](int j) {
+          const int gj = g + j;
+          if (!wait(k_full(gj % k3Stages), (gj / k3Stages) & 1)) return;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (j >= nb[x]) continue;
+            if (ns[x] > 0 && !wait(tbar(x, S_FREE), (ns[x] - 1) & 1)) return;
+            ptx::tc_fence_after();
+            issue_s(x, gj);
+            ++ns[x];
+          }
+          ptx::mma_commit(k_empty(gj % k3Stages));  // K of block j read by every S of it
+          if (j + 1 == nbm) ptx::mma_commit(q_empty);  // the item's last S is issued
+        };
+        issue_block_s(0);
+        for (int j = 0; ok && j < nbm; ++j) {
+          if (j + 1 < nbm) {
+            issue_block_s(j + 1);
+            if (!ok) break;
+          }
+          const int gj = g + j;
+          if (!wait(v_full(gj % k3Stages), (gj / k3Stages) & 1)) break;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (j >= nb[x]) continue;
+            if (!wait(tbar(x, P_FULL), np[x] & 1)) break;
+            ++np[x];
+            if (j == 0 && !wait(tbar(x, O_FREE), (nact[x] & 1) ^ 1)) break;
+            ptx::tc_fence_after();
+            issue_pv(x, gj, j == 0);
+          }
+          if (!ok) break;
+          ptx::mma_commit(v_empty(gj % k3Stages));  // V of block j read by every P V of it
+        }
+        for (int x = 0; x < 2; ++x)
+          if (nb[x] > 0) ++nact[x];
+        g += nbm;
+      }
+      if (!ok) *abort_flag = 1;
+      ptx::mma_commit(drain);
+      if (!ptx::mbar_wait(drain, 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    }
+  } else {
+    // ---- softmax: warps 2-5 tile A, 6-9 tile B; warp w reads TMEM lanes [32*(w%4), +32) ----
+    const int x = (warp - 2) >> 2;
+    const int qw = warp & 3;
+    const int row = qw * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(256 * x);
+    const uint32_t pb = sb + 64u, ob = sb + 128u;
+    bool ok = true;
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      const bool ready = ptx::mbar_wait(bar, parity, p.wait_ns);
+      if (!__all_sync(0xffffffffu, ready && *abort_flag == 0)) {
+        if (lane == 0) {
+          if (!ready) record(p.status, kDevTimeoutEpilogue);
+          *abort_flag = 1;
+        }
+        return false;
+      }
+      return true;
+    };
+    uint32_t gs = 0;  // S blocks of this tile consumed (all items); P V done waits follow the same count
+    for (int ic = 0, it = rank_of(0); ok && it >= 0; it = rank_of(++ic)) {
+      int qt0, nba, nbb;
+      const AttnHead &hd = item(it, qt0, nba, nbb);
+      const int nb = x == 0 ? nba : nbb;
+      if (nb == 0) continue;
+      const int qrow = (qt0 + x) * kTileQ + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nb; ++j, ++gs) {
+        if (!wait_all(tbar(x, S_FULL), gs & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const int k0 = j * kKb;
+        const int lim = min(p.causal ? qrow - k0 + 1 : kKb, p.tokens - k0);
+        uint32_t v[64];
+        {
+          uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+          uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+          ptx::tmem_ld_32cols(sb, v0);
+          ptx::tmem_ld_32cols(sb + 32, v1);
+          ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(v);
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tbar(x, S_FREE));  // S read: the tile's next S may be computed
+        if (!__all_sync(0xffffffffu, lim >= kKb)) {  // a masked key in this warp's rows
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i >= lim) v[i] = __float_as_uint(-INFINITY);
+        }
+        float mq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mq[q] = __uint_as_float(v[16 * q + 15]);
+#pragma unroll
+          for (int i = 0; i < 14; i += 2)
+            mq[q] = max3f(mq[q], __uint_as_float(v[16 * q + i]), __uint_as_float(v[16 * q + i + 1]));
+          mq[q] = fmaxf(mq[q], __uint_as_float(v[16 * q + 14]));
+        }
+        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        const float m_blk = mx * p.scale_log2;
+        const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
+        const float m_new = move ? m_blk : m;
+        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
+        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
+        uint64_t sumh[2];
+        uint32_t pk[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          sumh[h] = pack2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float y0, y1;
+            unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
+                    y1);
+            const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
+            sumh[h] = add2(sumh[h], pack2(a0, a1));
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
+            memcpy(&pk[h][i >> 1], &hb, 4);
+          }
+        }
+        float s0, s1;
+        unpack2(add2(sumh[0], sumh[1]), s0, s1);
+        l = l * alpha + (s0 + s1);
+        m = m_new;
+        // the previous P V has read P and brought O up to date
+        if (j > 0) {
+          if (!wait_all(tbar(x, PV_DONE), (gs - 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (__any_sync(0xffffffffu, move)) {  // rows keeping their maximum scale by 1
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              ptx::tmem_ld_32cols(ob + c * 32, o);
+              ptx::tmem_ld_wait();
+              ptx::tmem_regs_ready(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              ptx::tmem_st_32cols(ob + c * 32, o);
+            }
+          }
+        }
+        ptx::tmem_st_16cols(pb, pk[0]);
+        ptx::tmem_st_16cols(pb + 16, pk[1]);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tbar(x, P_FULL));
+      }
+      if (!ok) break;
+      // the item's output: O / l once its last P V has landed
+      if (!wait_all(tbar(x, PV_DONE), (gs - 1) & 1)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld_32cols(ob + c * 32, v);
+        ptx::tmem_ld_wait();
+        ptx::tmem_regs_ready(v);
+        if (qrow < p.tokens) {
+          __nv_bfloat16 *dst =
+              static_cast<__nv_bfloat16 *>(hd.out) + static_cast<long long>(qrow) * hd.out_ld + c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
+            memcpy(&w.x, &h0, 4);
+            memcpy(&w.y, &h1, 4);
+            memcpy(&w.z, &h2, 4);
+            memcpy(&w.w, &h3, 4);
+            *reinterpret_cast<uint4 *>(dst + i) = w;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tbar(x, O_FREE));  // O_x may be overwritten by the next item's first P V
+    }
+  }
+
+  // ---- teardown: every TMA load this CTA started has landed before it exits ----
+  __syncthreads();
+  if (warp == 0 && lane < 2) {
+    if (lane == 0 && q_loads > 0 && !ptx::mbar_wait(q_full, (q_loads - 1) & 1, p.wait_ns))
+      record(p.status, kDevTimeoutDrain);
+    for (int s = 0; s < k3Stages; ++s)
+      if (issued[s] > 0 && !ptx::mbar_wait(lane == 0 ? k_full(s) : v_full(s), (issued[s] - 1) & 1, p.wait_ns))
+        record(p.status, kDevTimeoutDrain);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // V [T x C] (row pitch ld_in) -> V^T [C x T] (row pitch ld_out) for every kv
 // source in one launch (grid z = source), 64 x 64 tiles through shared memory.
 __global__ void __launch_bounds__(256) k_transpose_bf16(TransposeArgs a) {
@@ -864,6 +1259,14 @@ tp_status launch_transpose_bf16(const TransposeArgs &a, int sources, cudaStream_
   return launch_checked(launch_kernel(k_transpose_bf16, grid, dim3(256), 0, s, 1, a));
 }
 
+int attention_variant() {
+  const char *env = getenv("TPGQA_ATTN");
+  if (env && (env[0] == '1' || env[0] == '3') && env[1] == 0) return env[0] - '0';
+  return 2;
+}
+
+int attention_k_box_rows(int variant) { return variant == 3 ? kKb : kTileK; }
+
 tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
   DevCtx ctx;
   cudaError_t e = get_dev_ctx(&ctx);
@@ -883,22 +1286,24 @@ tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attention2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kAttn2Smem));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attention3, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kAttn3Smem));
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 64) configured |= 1ULL << dev;
     }
   }
   p.heads_total = total_heads;
-  // Two query tiles per work item by default; TPGQA_ATTN=1 runs the kernel with
-  // one query tile per item (read on every call).
-  const char *env = getenv("TPGQA_ATTN");
-  if (env && env[0] == '1') {
+  if (p.variant == 1) {
     const long long items = static_cast<long long>(p.q_tiles) * total_heads;
     const dim3 grid(static_cast<unsigned>(items < num_sms() ? items : num_sms()));
     return launch_checked(launch_kernel(k_attention, grid, dim3(kAttnThreads), kAttnSmem, s, 1, p));
   }
   const long long items = static_cast<long long>((p.q_tiles + 1) / 2) * total_heads;
   const dim3 grid(static_cast<unsigned>(items < num_sms() ? items : num_sms()));
-  return launch_checked(launch_kernel(k_attention2, grid, dim3(kAttnThreads), kAttn2Smem, s, 1, p));
+  if (p.variant == 2)
+    return launch_checked(launch_kernel(k_attention2, grid, dim3(kAttnThreads), kAttn2Smem, s, 1, p));
+  return launch_checked(launch_kernel(k_attention3, grid, dim3(kAttnThreads), kAttn3Smem, s, 1, p));
 }
 
 }  // namespace tpgqa

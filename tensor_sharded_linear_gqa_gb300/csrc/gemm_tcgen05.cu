@@ -500,7 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
 constexpr int kPairABytes = 128 * BK * 2;  // one 64-wide k-tile of this CTA's 128 A rows
 // BN accumulator columns per tile: each CTA holds BN/2 rows of B (for SwiGLU,
 // BN/2 gate rows in CTA 0 and BN/2 up rows in CTA 1). BN is 256, or 224 when
-// narrower tiles fill the last wave better.
+// narrower tiles fill the last wave better. BN = 512 (SwiGLU only, one 64-wide
+// k-tile per stage): 256 gate and 256 up columns per tile, computed by two
+// N=256 MMAs per k-step into one 512-column accumulator; each CTA holds 128
+// gate rows and 128 up rows of B (its half of each MMA's N).
 template <int KSUB, int BN>
 struct PairCfg {
   static constexpr int kBRows = BN / 2;
@@ -535,8 +538,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   constexpr int kHalfB = PC::kBRows;  // B rows per CTA
   constexpr int kOutCols = (EPI == kEpiSwiGLU) ? BN / 2 : BN;
   const int kPrefetch = p.prefetch;
-  constexpr uint32_t kTmemCols = 512;  // two accumulators, at columns 0 and 256
+  constexpr uint32_t kTmemCols = 512;  // two accumulators, at columns 0 and 256 (one of 512 columns at BN 512)
   constexpr int S = kPairStages;
+  constexpr bool kWide = BN == 512;
+  static_assert(!kWide || (EPI == kEpiSwiGLU && KSUB == 1), "512-column tiles: SwiGLU, 64-wide stages");
+  constexpr int kAcc = kWide ? 1 : 2;          // accumulators in TMEM
+  constexpr int kMmaN = kWide ? 256 : BN;      // N of one MMA
+  constexpr uint32_t kWideUp = 128u * 128u;    // BN 512: up rows after the 128 gate rows of a k-tile
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -600,7 +608,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int kt = 0; kt < seg_stages<KSUB>(sg) && pre < S; ++kt, ++pre) {
         const uint32_t lead_full = ptx::mapa_shared(full_bar(pre), 0);
         if (leader) ptx::mbar_arrive_expect_tx(full_bar(pre), 2 * kPairStageBytes);
-        if (p.box_kt > 1) {
+        if constexpr (kWide) {
+          const int wrow = nt * 256 + static_cast<int>(rank) * 128;
+          ptx::tma_load_2d_pair(sB0 + pre * kPairBBytes, &p.maps[sg.b_map], kt * BK, wrow, lead_full);
+          ptx::tma_load_2d_pair(sB0 + pre * kPairBBytes + kWideUp, &p.maps[sg.b2_map], kt * BK, wrow, lead_full);
+        } else if (p.box_kt > 1) {
           ptx::tma_load_3d_pair(sB0 + pre * kPairSub * kPairBBytes, &p.maps[map], 0, row, kt * kPairSub, lead_full);
         } else {
 #pragma unroll
@@ -650,7 +662,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // This CTA's half of B: rows of its own map and offset.
       auto b_src = [&](const Cursor &c, int &map, int &row) {
         const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
-        if (EPI == kEpiSwiGLU || sg.b2_map >= 0) {  // two B matrices, one half of the tile each
+        if (kWide) {  // both B matrices in each CTA (the gate map is named here)
+          map = sg.b_map + c.moff;
+          row = c.brow + c.nt * 256 + static_cast<int>(rank) * 128;
+        } else if (EPI == kEpiSwiGLU || sg.b2_map >= 0) {  // two B matrices, one half of the tile each
           map = (leader ? sg.b_map : sg.b2_map) + c.moff;
           row = c.brow + c.nt * kHalfB;
         } else {
@@ -696,7 +711,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int m, r;
         b_src(ld, m, r);
         const int a_row = ld.mt * 256 + static_cast<int>(rank) * 128;
-        if (p.box_kt > 1) {
+        if constexpr (kWide) {
+          const int x = ld.kt * BK;
+          ptx::tma_load_2d_pair(sA0 + st * kPairABytes, &p.maps[sg.a_map], x, a_row, lead_full);
+          if (!early) {
+            ptx::tma_load_2d_pair(sB0 + st * kPairBBytes, &p.maps[m], x, r, lead_full);
+            ptx::tma_load_2d_pair(sB0 + st * kPairBBytes + kWideUp, &p.maps[sg.b2_map + ld.moff], x, r, lead_full);
+          }
+        } else if (p.box_kt > 1) {
           // one copy per operand brings the stage's KSUB k-tiles (3-D maps)
           ptx::tma_load_3d_pair(sA0 + st * kPairSub * kPairABytes, &p.maps[sg.a_map], 0, a_row,
                                 ld.kt * kPairSub, lead_full);
@@ -720,13 +742,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, BN);
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, kMmaN);
       int kb = 0;
       bool ok = true;
       for (int tile = live_tile(p, pair, npairs), j = 0; ok && tile < p.total_tiles;
            tile = live_tile(p, tile + npairs, npairs), ++j) {
-        const int a = j & 1;
-        const uint32_t use = static_cast<uint32_t>(j >> 1);
+        const int a = j % kAcc;
+        const uint32_t use = static_cast<uint32_t>(j / kAcc);
         if (*abort_flag || !ptx::mbar_wait(tempty_bar(a), (use & 1) ^ 1, p.wait_ns)) {
           if (!*abort_flag) record(p.status, kDevTimeoutMma);
           *abort_flag = 1;
@@ -751,8 +773,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t ad = ptx::smem_desc_sw128(sA0 + (st * kPairSub + j) * kPairABytes);
             const uint64_t bd = ptx::smem_desc_sw128(sB0 + (st * kPairSub + j) * kPairBBytes);
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k)
+            for (int k = 0; k < BK / UMMA_K; ++k) {
               ptx::mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (k0 | j | k) != 0 ? 1u : 0u);
+              if constexpr (kWide) {
+                const uint64_t ud = ptx::smem_desc_sw128(sB0 + (st * kPairSub + j) * kPairBBytes + kWideUp);
+                ptx::mma_bf16_pair(d + 256u, ad + 2 * k, ud + 2 * k, idesc, (k0 | j | k) != 0 ? 1u : 0u);
+              }
+            }
           }
           ptx::mma_commit_pair_multicast(empty_bar(st), 0x3);
         }
@@ -766,8 +793,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     for (int tile = live_tile(p, pair, npairs), j = 0; tile < p.total_tiles;
          tile = live_tile(p, tile + npairs, npairs), ++j) {
-      const int a = j & 1;
-      const uint32_t use = static_cast<uint32_t>(j >> 1);
+      const int a = j % kAcc;
+      const uint32_t use = static_cast<uint32_t>(j / kAcc);
       const bool ready = ptx::mbar_wait(tfull_bar(a), use & 1, p.wait_ns);
       if (!ready && lane == 0) record(p.status, kDevTimeoutEpilogue);
       ptx::tc_fence_after();
@@ -1246,7 +1273,7 @@ template <bool PAIR, int BN>
 struct SplitCfg {
   static constexpr int kSub = PAIR ? 2 : 1;  // 64-wide k-tiles per stage
   static constexpr int kABytes = 128 * BK * 2;
-  static constexpr int kBRows = PAIR ? 128 : BN;  // B rows per CTA per k-tile
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;  // B rows per CTA per k-tile
   static constexpr int kBBytes = kBRows * BK * 2;
   static constexpr int kStageBytes = kSub * (kABytes + kBBytes);
   static constexpr int kStages = (6 * 32768) / kStageBytes;  // 192 KB of stages
@@ -1256,7 +1283,7 @@ struct SplitCfg {
 template <bool PAIR, int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_constant__ GemmParams p) {
   using C = SplitCfg<PAIR, BN>;
-  static_assert(!PAIR || BN == 256, "SM pairs run 256-column tiles");
+  static_assert(!PAIR || BN == 256 || BN == 128, "SM pairs run 256- or 128-column tiles");
   constexpr int KS = C::kSub;
   // SM pairs: fixed stages of 128-row A k-tiles. Single CTAs: an A k-tile holds
   // the a_rows rows loaded and the stage count comes from the host.
@@ -1302,10 +1329,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   const int local = tile - pr.tile_begin;
   const int mt = local % pr.m_tiles;
   const int nt = local / pr.m_tiles;
-  int ns = 0;
-  for (int q = 0; q < pr.seg_count; ++q) ns += (p.seg[pr.seg_begin + q].k_tiles + KS - 1) / KS;
-  const int k_begin = (split * ns) / nsplit;
-  const int k_end = ((split + 1) * ns) / nsplit;
+  // Ring folding (ring_rows > 0): split s is segment (rank) s, whole. Otherwise
+  // the problem's stages are cut into nsplit near-equal ranges.
+  const bool ring = p.ring_rows > 0;
+  int k_begin = 0, k_end = 0;
+  {
+    int ns = 0;
+    for (int q = 0; q < pr.seg_count; ++q) {
+      const int n = (p.seg[pr.seg_begin + q].k_tiles + KS - 1) / KS;
+      if (ring && q == split) {
+        k_begin = ns;
+        k_end = ns + n;
+      }
+      ns += n;
+    }
+    if (!ring) {
+      k_begin = (split * ns) / nsplit;
+      k_end = ((split + 1) * ns) / nsplit;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -1365,9 +1407,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
       const int z = kt * KS;
       if (EPI == kEpiSwiGLU)
         ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[member == 0 ? sg.b_map : sg.b2_map], 0,
-                              nt * 128, z, fb);
+                              nt * (BN / 2), z, fb);
       else
-        ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[sg.b_map], 0, nt * BN + member * 128, z, fb);
+        ptx::tma_load_3d_pair(sB0 + st * KS * C::kBBytes, &p.maps[sg.b_map], 0, nt * BN + member * (BN / 2), z,
+                              fb);
       return;
     }
 #pragma unroll
@@ -1376,9 +1419,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
       const uint32_t db = sB0 + (st * KS + j) * C::kBBytes;
       if constexpr (PAIR) {
         if (EPI == kEpiSwiGLU)
-          ptx::tma_load_2d_pair(db, &p.maps[member == 0 ? sg.b_map : sg.b2_map], x, nt * 128, fb);
+          ptx::tma_load_2d_pair(db, &p.maps[member == 0 ? sg.b_map : sg.b2_map], x, nt * (BN / 2), fb);
         else
-          ptx::tma_load_2d_pair(db, &p.maps[sg.b_map], x, nt * BN + member * 128, fb);
+          ptx::tma_load_2d_pair(db, &p.maps[sg.b_map], x, nt * BN + member * (BN / 2), fb);
       } else {
         if (EPI == kEpiSwiGLU) {
           ptx::tma_load_2d(db, &p.maps[sg.b_map], x, nt * (BN / 2), fb);
@@ -1560,6 +1603,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
         const int lo = split * rows_per;
         const int row0 = PAIR ? mt * 256 + member * 128 : mt * 128;
         const OutDesc od{pr.out, pr.ldc, pr.n};
+        // ring folding: the tile's chunk c = row / ring_rows is summed in the ring's
+        // order c+1, c+2, ..., c (split t = rank t); otherwise splits 0..S-1
+        const int first = ring ? ((row0 + lo) / p.ring_rows + 1) % nsplit : 0;
         const int m_rows = pr.m;
         constexpr int kUnits = (EPI == kEpiSwiGLU) ? BN / 8 : BN / 4;
         constexpr int kBatch = (EPI == kEpiSwiGLU) ? 4 : 8;
@@ -1572,11 +1618,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
             if (t >= nsplit) break;
             float4 vg[kBatch], vu[kBatch];
 #pragma unroll
+            const int ts = ring ? (first + t) % nsplit : t;
             for (int b = 0; b < kBatch; ++b) {
               const int idx = base + b * kThreads < total ? base + b * kThreads : base;
               const int rl = idx / kUnits;
               const int c4 = idx % kUnits;
-              const int prow = (t == split) ? lo + rl : 128 + (t < split ? t : t - 1) * rows_per + rl;
+              const int prow = (ts == split) ? lo + rl : 128 + (ts < split ? ts : ts - 1) * rows_per + rl;
               const uint32_t rowa = red0 + static_cast<uint32_t>(prow * kRowBytes);
               vg[b] = ptx::ld_shared_f4(rowa + static_cast<uint32_t>(((c4 ^ (rl & 7)) * 16)));
               if (EPI == kEpiSwiGLU)
@@ -1601,7 +1648,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
             if (idx >= total) break;
             const int rl = idx / kUnits;
             const int grow = row0 + lo + rl;
-            if (grow < m_rows) store_unit<EPI, BN>(od, grow, nt, idx % kUnits, g[b], u[b]);
+            if (grow >= m_rows) continue;
+            if (ring) {
+              for (int c = 0; c < p.ring_copies; ++c)
+                store_unit<EPI, BN>(OutDesc{p.ring_dst[c], pr.ldc, pr.n}, grow, nt, idx % kUnits, g[b], u[b]);
+            } else {
+              store_unit<EPI, BN>(od, grow, nt, idx % kUnits, g[b], u[b]);
+            }
           }
         }
       }
@@ -1650,9 +1703,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
       if (!got && lane == 0) record(p.status, kDevTimeoutEpilogue);
       ptx::named_barrier(1, 128);  // local partial writes of all four epilogue warps
       if (got && *abort_flag == 0) {
-        // rows [lo, lo + rows_per) of this member's half, summed over splits in order 0..S-1
+        // rows [lo, lo + rows_per) of this member's half, summed over splits in order
+        // 0..S-1, or in the ring order of the tile's chunk when folding
         const int lo = split * rows_per;
         const int row0 = PAIR ? mt * 256 + member * 128 : mt * 128;
+        const int first = ring ? ((row0 + lo) / p.ring_rows + 1) % nsplit : 0;
         constexpr int kUnits = (EPI == kEpiSwiGLU) ? BN / 8 : BN / 4;  // output 16-byte units per row
         const int total = rows_per * kUnits;
         for (int idx = tid; idx < total; idx += 128) {
@@ -1661,7 +1716,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
           const int grow = row0 + lo + rl;
           float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
           for (int t = 0; t < nsplit; ++t) {
-            const uint8_t *rowp = smem + (t * rows_per + rl) * kRowBytes;
+            const int ts = ring ? (first + t) % nsplit : t;
+            const uint8_t *rowp = smem + (ts * rows_per + rl) * kRowBytes;
             const float4 vg = *reinterpret_cast<const float4 *>(rowp + ((c4 ^ (rl & 7)) * 16));
             if (t == 0) {
               g = vg;
@@ -1678,40 +1734,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
             }
           }
           if (grow >= pr.m) continue;
-          const float f[4] = {g.x, g.y, g.z, g.w};
-          if (EPI == kEpiF32) {
-            const int col = nt * BN + c4 * 4;
-            float *dst = static_cast<float *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
-            if (col + 4 <= pr.n) {
-              *reinterpret_cast<float4 *>(dst) = g;
-            } else {
-              for (int e = 0; e < 4; ++e)
-                if (col + e < pr.n) dst[e] = f[e];
-            }
+          if (ring) {
+            for (int c = 0; c < p.ring_copies; ++c)
+              store_unit<EPI, BN>(OutDesc{p.ring_dst[c], pr.ldc, pr.n}, grow, nt, c4, g, u);
           } else {
-            float o[4];
-            int col;
-            if (EPI == kEpiSwiGLU) {
-              const float uu[4] = {u.x, u.y, u.z, u.w};
-              for (int e = 0; e < 4; ++e) o[e] = silu(f[e]) * uu[e];
-              col = nt * (BN / 2) + c4 * 4;
-            } else {
-              for (int e = 0; e < 4; ++e) o[e] = f[e];
-              col = nt * BN + c4 * 4;
-            }
-            __nv_bfloat16 *dst =
-                static_cast<__nv_bfloat16 *>(pr.out) + static_cast<long long>(grow) * pr.ldc + col;
-            if (col + 4 <= pr.n) {
-              __nv_bfloat162 h0 = __floats2bfloat162_rn(o[0], o[1]);
-              __nv_bfloat162 h1 = __floats2bfloat162_rn(o[2], o[3]);
-              uint2 w;
-              memcpy(&w.x, &h0, 4);
-              memcpy(&w.y, &h1, 4);
-              *reinterpret_cast<uint2 *>(dst) = w;
-            } else {
-              for (int e = 0; e < 4; ++e)
-                if (col + e < pr.n) dst[e] = __float2bfloat16_rn(o[e]);
-            }
+            store_unit<EPI, BN>(OutDesc{pr.out, pr.ldc, pr.n}, grow, nt, c4, g, u);
           }
         }
       }
@@ -1814,6 +1841,12 @@ int pair_ksub() {
 
 template <int EPI>
 tp_status launch_pair(const GemmParams &p, int bn, cudaStream_t stream) {
+  if (bn == 512) {
+    if constexpr (EPI == kEpiSwiGLU)
+      return launch_pair_ks<EPI, 1, 512>(p, stream);
+    else
+      return TP_ERR_UNSUPPORTED;
+  }
   if (bn == 224) return launch_pair_ks<EPI, 2, 224>(p, stream);
   if (bn == 128) return launch_pair_ks<EPI, 2, 128>(p, stream);
   if (bn != 256) return TP_ERR_UNSUPPORTED;
@@ -1878,6 +1911,8 @@ tp_status launch_splitk(const GemmParams &p, cudaStream_t stream) {
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
+}  // namespace
+
 // Clusters of `csize` split-K CTAs that can be resident at once, or -1 if the
 // runtime cannot say. A cluster has to fit inside one GPC, so this can be well
 // below SMs / csize (on GB300: 36 clusters of 4 and 15 of 8 for 152 SMs). All
@@ -1912,8 +1947,6 @@ int max_active_clusters(int csize) {
   }
   return cache[dev][csize];
 }
-
-}  // namespace
 
 bool encode_bf16_map_2d(CUtensorMap *map, const void *base, long long rows, long long cols, long long ld,
                         int box_rows) {
@@ -2107,13 +2140,23 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
     }
     split = choose_split(p.total_tiles, pair, min_stages < 0 ? 0 : min_stages);
   }
+  if (ring_split) {
+    // one split per segment (rank) on 256 x 128 pair tiles, f32 sums in ring order
+    if (!pair || bn != 128 || epi != kEpiF32 || n_probs != 1 || p.prob[0].seg_count < 2 ||
+        p.prob[0].seg_count > 4 || p.ring_rows <= 0 || p.ring_rows % 256 != 0 || p.ring_copies < 1 ||
+        p.ring_copies > kMaxRingCopies)
+      return TP_ERR_UNSUPPORTED;
+    p.split = p.prob[0].seg_count;
+    p.box_kt = use_3d_boxes(SplitCfg<true, 128>::kSub);
+    return launch_splitk<true, kEpiF32, 128>(p, stream);
+  }
   if (split < 1 || (pair && bn != 256) || (!pair && bn != 256 && bn != 128) || ring || dual)
     split = 1;  // split-K runs 256-column pair tiles and 128/256-column single-CTA tiles
   p.split = split;
   // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand
   // and stage replaces KSUB 2-D copies. The single-CTA kernels load one k-tile
   // per stage and keep the 2-D maps.
-  p.box_kt = pair ? use_3d_boxes(split > 1 || bn != 256 ? SplitCfg<true, 256>::kSub : pair_ksub()) : 1;
+  p.box_kt = !pair || bn == 512 ? 1 : use_3d_boxes(split > 1 || bn != 256 ? SplitCfg<true, 256>::kSub : pair_ksub());
   if (ring) return launch_pair_ring(p, bn, stream);
   if (split > 1) {
     if (pair) {
@@ -2220,13 +2263,14 @@ int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu) {
 }
 
 int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, int *b_rows) {
-  // TPGQA_PAIR_BN=224|256 forces the SM-pair tile width (tuning override).
+  // TPGQA_PAIR_BN=128|224|256|512 forces the SM-pair tile width (tuning
+  // override; 512 applies to SwiGLU problems only).
   static const int forced = [] {
     const char *e = getenv("TPGQA_PAIR_BN");
     return e ? atoi(e) : 0;
   }();
   int best = 256;
-  if (forced == 128 || forced == 224 || forced == 256) {
+  if (forced == 128 || forced == 224 || forced == 256 || (forced == 512 && swiglu)) {
     best = forced;
   } else {
     // A tile's time goes with its stage bytes (the loads bound the pair's
@@ -2249,8 +2293,20 @@ int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, 
         best = bn;
       }
     }
+    // SwiGLU grids of more than one wave of 256-column tiles that fit one wave
+    // of 512-column tiles (256 gate and 256 up columns): one tile per SM pair,
+    // half the A bytes per MMA flop. The single accumulator leaves no epilogue
+    // overlap, which a single wave does not need.
+    if (swiglu && forced == 0) {
+      long long t256 = 0, t512 = 0;
+      for (int i = 0; i < nprob; ++i) {
+        t256 += mt * ((ncols[i] + 127) / 128);
+        t512 += mt * ((ncols[i] + 255) / 256);
+      }
+      if (t256 > pairs && t512 <= pairs) best = 512;
+    }
   }
-  *b_rows = best / 2;
+  *b_rows = best == 512 ? 128 : best / 2;
   return best;
 }
 

@@ -228,6 +228,39 @@ tp_status gemm_bf16_column_chunks(int32_t n, const tp_tensor *x_chunks, const tp
   return b.launch(s);
 }
 
+// Row-parallel shapes whose per-rank GEMM would split K over SM-pair clusters
+// (too few 256 x 256 tiles for every pair) while the per-rank partials fit one
+// wave of 256 x 128 pair tiles in clusters of 2N CTAs (N = 2 or 4, every
+// 256-row tile inside one ring chunk). With TPGQA_RANK_SPLIT=1 (read on every
+// call) these layers compute each rank's partial on 256 x 128 pair tiles
+// without split-K, whatever the combine, so that the ring fold with one cluster
+// split per rank gives the bits of the GEMM followed by the ring. Off by
+// default: at T = 512, N = 2 (the MLP block's down projection) the folded GEMM
+// took 24.4 us of the step against 23.0 us for the split-K GEMM and the
+// one-pass ring; a 256 x 128 tile loads 1.5 MB of operands per CTA there
+// against 1.0 MB for a split-K 256 x 256 tile, and both run at the rate the
+// shared-memory fill allows.
+bool rank_split_shape(int32_t n, const tp_tensor *x, const tp_tensor *w) {
+  const char *env = getenv("TPGQA_RANK_SPLIT");
+  if (!(env && env[0] == '1')) return false;
+  const long long T = x[0].rows, nout = w[0].rows;
+  if ((n != 2 && n != 4) || !choose_pair(T) || T % n != 0 || (T / n) % 256 != 0 || T > (1LL << 30)) return false;
+  if (nout < 1 || nout > (1LL << 30)) return false;
+  int b_rows = 0;
+  const std::vector<long long> nc(static_cast<size_t>(n), nout);
+  if (choose_pair_bn(T, nc.data(), n, false, &b_rows) != 256) return false;
+  long long min_stages = -1;
+  for (int32_t r = 0; r < n; ++r) {
+    const long long st = ((x[r].cols + 63) / 64 + 1) / 2;
+    if (min_stages < 0 || st < min_stages) min_stages = st;
+  }
+  const long long tiles256 = static_cast<long long>(n) * (T / 256) * ((nout + 255) / 256);
+  if (choose_split(tiles256, true, min_stages) == 1) return false;
+  const long long tiles128 = (T / 256) * ((nout + 127) / 128);
+  const int resident = max_active_clusters(2 * n);
+  return resident > 0 && tiles128 <= resident;
+}
+
 // Row-parallel: fused = one problem whose segments are the ranks; else one problem per rank.
 tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
                         bool fused, cudaStream_t s) {
@@ -248,6 +281,12 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
       b.bn = choose_bn(T, nc.data(), static_cast<int>(probs), false);
       b_rows = b.bn;
     }
+  }
+  if (!fused && rank_split_shape(n, x, w)) {
+    b.pair = true;
+    b.bn = 128;
+    b_rows = 64;
+    b.split = 1;
   }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
@@ -343,6 +382,48 @@ tp_status gemm_bf16_row_ring(int32_t n, const tp_tensor *x, const tp_tensor *w, 
   b.p.ring_rows = static_cast<int>(T / n);
   b.p.ring_out = first;
   b.p.ring_copies = copies;
+  return b.launch(s);
+}
+
+// Row-parallel GEMM with the ring all-reduce folded into the split-K SM-pair
+// kernel: one cluster per 256 x 128 tile, split s computing rank s's partial,
+// the owned rows summed in their chunk's ring order and written to
+// y[0..copies-1]. For the shapes of rank_split_shape; every output shares y[0]'s
+// row pitch.
+bool ring_split_ok(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y, int copies) {
+  const char *env = getenv("TPGQA_RING_EPILOGUE");
+  if (env && env[0] == '0') return false;
+  if (copies < 1 || copies > kMaxRingCopies) return false;
+  for (int r = 1; r < copies; ++r)
+    if (y[r].ld != y[0].ld) return false;
+  return rank_split_shape(n, x, w);
+}
+
+tp_status gemm_bf16_row_ring_split(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
+                                   int copies, cudaStream_t s) {
+  const long long T = x[0].rows, nout = w[0].rows;
+  GemmBuilder b;
+  b.epi = kEpiF32;
+  b.pair = true;
+  b.bn = 128;
+  b.ring_split = true;
+  b.a_rows = 128;
+  tp_status err = TP_OK;
+  std::vector<int> am(n), bm(n);
+  std::vector<long long> ks(n);
+  for (int32_t r = 0; r < n; ++r) {
+    am[r] = b.add_map(x[r].ptr, T, x[r].cols, x[r].ld, b.a_rows, &err);
+    if (am[r] < 0) return err;
+    bm[r] = b.add_map(w[r].ptr, nout, w[r].cols, w[r].ld, 64, &err);
+    if (bm[r] < 0) return err;
+    ks[r] = x[r].cols;
+  }
+  if (!b.add_problem(static_cast<int>(T), static_cast<int>(nout), y[0].ptr, y[0].ld, am.data(), bm.data(), nullptr,
+                     ks.data(), n))
+    return TP_ERR_UNSUPPORTED;
+  b.p.ring_rows = static_cast<int>(T / n);
+  b.p.ring_copies = copies;
+  for (int r = 0; r < copies; ++r) b.p.ring_dst[r] = y[r].ptr;
   return b.launch(s);
 }
 
@@ -445,6 +526,7 @@ tp_status row_linear_impl(int32_t n, const tp_tensor *x, const tp_tensor *w, con
   if (dt == TP_BF16 && (combine == TP_COMBINE_RING_FUSED || combine == TP_COMBINE_RING_SHARED)) {
     const int copies = combine == TP_COMBINE_RING_FUSED ? n : 1;
     if (ring_fold_ok(n, x, w, y, copies)) return gemm_bf16_row_ring(n, x, w, y, copies, s);
+    if (ring_split_ok(n, x, w, y, copies)) return gemm_bf16_row_ring_split(n, x, w, y, copies, s);
   }
   if (dt == TP_BF16)
     st = gemm_bf16_row(n, x, w, y, fused, s);
@@ -815,10 +897,12 @@ extern "C" tp_status tp_attn_core(const tp_plan *plan, const tp_tensor *q, const
   if ((st = launch_transpose_bf16(ta, nkv, s)) != TP_OK) return st;
   static thread_local AttnParams prm;  // ~22 KB: kept off the stack
   std::memset(&prm, 0, sizeof(prm));
+  prm.variant = attention_variant();
+  const int k_box = attention_k_box_rows(prm.variant);
   for (int32_t r = 0; r < n; ++r)
     if (!encode_bf16_map_2d(&prm.maps[r], q[r].ptr, T, q[r].cols, q[r].ld, 128)) return TP_ERR_INVALID_ARG;
   for (int32_t r = 0; r < nkv; ++r) {
-    if (!encode_bf16_map_2d(&prm.maps[n + r], k[r].ptr, T, kvc, k[r].ld, 128)) return TP_ERR_INVALID_ARG;
+    if (!encode_bf16_map_2d(&prm.maps[n + r], k[r].ptr, T, kvc, k[r].ld, k_box)) return TP_ERR_INVALID_ARG;
     if (!encode_bf16_map_2d(&prm.maps[n + nkv + r], static_cast<char *>(workspace) + r * vt, kvc, T, tp8, 128))
       return TP_ERR_INVALID_ARG;
   }
@@ -1053,10 +1137,15 @@ tp_status launch_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *
   const long long mt = (T + 127) / 128;
   (void)mt;
   b.pair = choose_pair(T);
+  int b_rows = 0;
   {
     const std::vector<long long> nc(static_cast<size_t>(n), Fr);
-    int b_rows = 0;
-    b.bn = b.pair ? choose_pair_bn(T, nc.data(), n, true, &b_rows) : choose_bn(T, nc.data(), n, true);
+    if (b.pair) {
+      b.bn = choose_pair_bn(T, nc.data(), n, true, &b_rows);
+    } else {
+      b.bn = choose_bn(T, nc.data(), n, true);
+      b_rows = b.bn / 2;
+    }
   }
   b.a_rows = b.pair ? 128 : a_box_rows(T);
   tp_status err = TP_OK;
@@ -1064,9 +1153,9 @@ tp_status launch_gate_up(const tp_dims &d, const tp_tensor *x, const tp_tensor *
   if (am < 0) return err;
   for (int32_t r = 0; r < n; ++r) {
     // gate and up each fill half of a tile's accumulator columns
-    const int gm = b.add_map(w_gate[r].ptr, Fr, D, w_gate[r].ld, b.bn / 2, &err);
+    const int gm = b.add_map(w_gate[r].ptr, Fr, D, w_gate[r].ld, b_rows, &err);
     if (gm < 0) return err;
-    const int um = b.add_map(w_up[r].ptr, Fr, D, w_up[r].ld, b.bn / 2, &err);
+    const int um = b.add_map(w_up[r].ptr, Fr, D, w_up[r].ld, b_rows, &err);
     if (um < 0) return err;
     const long long ks = D;
     if (!b.add_problem(static_cast<int>(T), static_cast<int>(Fr), h[r].ptr, h[r].ld, &am, &gm, &um,

@@ -87,6 +87,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // bf16 tensor-core grouped GEMM (tcgen05 + TMA), C = A * B^T, both K-major.
 // ---------------------------------------------------------------------------
 constexpr int kMaxMaps = 48;
+constexpr int kMaxRingCopies = 8;  // outputs of the split-K ring fold
 constexpr int kMaxProblems = 72;  // a column GEMM over reduce-scatter chunks has N*N problems
 constexpr int kMaxSegs = 80;
 
@@ -155,6 +156,11 @@ struct GemmParams {
   int ring_rows;
   int ring_out;
   int ring_copies;
+  // The same fold in the split-K SM-pair kernel (GemmBuilder::ring_split): split s
+  // of a cluster computes rank s's partial; the owned rows are summed in the
+  // chunk's ring order and stored to ring_dst[0 .. ring_copies - 1] (row pitch of
+  // the problem's output).
+  void *ring_dst[kMaxRingCopies];
   int *status;
   long long wait_ns;
 };
@@ -188,6 +194,9 @@ struct GemmBuilder {
   // map index or -1. Not re-encoded by use_3d_boxes.
   int add_out_map_f32(void *base, long long rows, long long cols, long long ld, tp_status *err);
   bool ring = false;  // launch the ring-folding pair kernel (see GemmParams::ring_rows)
+  // launch the split-K SM-pair kernel with one split per segment (rank) and the
+  // ring fold in its reduction (see GemmParams::ring_dst); 128-column tiles
+  bool ring_split = false;
   // Re-encodes every map as a 3-D map whose box spans kt k-tiles, if every
   // map's K is a multiple of 64 with at least kt k-tiles; returns kt, or 1 (the
   // 2-D maps kept) otherwise.
@@ -219,6 +228,9 @@ bool choose_pair(long long rows);
 // Split-K factor for `tiles` output tiles of `stages_per_tile` k-stages each
 // (1 = no split).
 int choose_split(long long tiles, bool pair, long long stages_per_tile);
+// Clusters of csize split-K CTAs that can be resident at once on the current
+// device, or -1 if the runtime cannot say.
+int max_active_clusters(int csize);
 
 // ---------------------------------------------------------------------------
 // Exact fp32 SIMT grouped GEMM, C = A * B^T with per-problem K segments.
@@ -319,11 +331,16 @@ struct AttnParams {
   CUtensorMap maps[kMaxAttnMaps];
   AttnHead heads[kMaxAttnHeads];
   int tokens, q_tiles, causal, heads_total;
+  int variant;              // kernel: 1 one query tile per item, 2 two tiles, 3 two tiles in 64-key blocks
   float scale_log2;         // log2(e) / sqrt(d)
   int *status;
   long long wait_ns;
 };
 tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s);
+// The attention kernel a call runs (2 by default; TPGQA_ATTN=1 or 3 selects
+// another, read on every call) and the rows of its K boxes (keys per block).
+int attention_variant();
+int attention_k_box_rows(int variant);
 // V [rows x cols] (pitch ld_in[z]) -> V^T [cols x rows] (pitch ld_out), bf16,
 // for sources z = 0..sources-1 in one launch.
 struct TransposeArgs {

@@ -178,3 +178,19 @@ def test_projection_attention_o_proj_chain(tp_size, hq, hkv):
     ref = sum(O.linear(att[r], f["wo"][:, slice(*oplan[r].ranges["o_proj"])]) for r in range(tp_size))
     for r in range(tp_size):
         assert_close(host_f64(ys[r]), ref, BF16_TOL, f"rank {r}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("kernel", ["1", "2", "3"])
+def test_every_attention_kernel_matches_the_oracle(kernel, causal, monkeypatch):
+    """The three attention kernels (TPGQA_ATTN=1: one 128-query tile per work item;
+    2, the default: two tiles over 128-key blocks; 3: two tiles over 64-key
+    blocks), each against the oracle, on a ragged sharded case and on peaked
+    scores whose row maxima move block after block."""
+    need_gpu()
+    monkeypatch.setenv("TPGQA_ATTN", kernel)
+    for m in (Attn(2, 8, 2, 300, seed=620), Attn(2, 4, 2, 700, seed=621, scale=4.0, key_ramp=3.0)):
+        got = m.run(causal)
+        ref = m.oracle(causal)
+        for r in range(m.n):
+            assert_close(host_f64(got[r]), ref[r], BF16_TOL, f"kernel {kernel} rank {r}")

@@ -30,7 +30,21 @@ CASES = [
     (1024, 4, 768, 320),
     (2048, 8, 1000, 200),
     (2048, 4, 4096, 1024),   # the attention projection's o_proj shape
+    # grids too small for one 256 x 256 tile per SM pair (the GEMM alone would
+    # split K): with TPGQA_RANK_SPLIT=1 the fold runs in the split-K pair kernel,
+    # one cluster split per rank; by default the GEMM splits K and the ring runs
+    # after it
+    (512, 2, 2048, 4096),    # the T=512 MLP block's down projection
+    (512, 2, 1000, 1000),
+    (1024, 4, 264, 2048),
 ]
+RANK_SPLIT = {(512, 2, 2048, 4096), (512, 2, 1000, 1000), (1024, 4, 264, 2048)}
+
+
+@pytest.fixture(params=["0", "1"], ids=["default", "rank_split"])
+def rank_split(request, monkeypatch):
+    monkeypatch.setenv("TPGQA_RANK_SPLIT", request.param)
+    return request.param == "1"
 
 
 def _torch():
@@ -66,8 +80,10 @@ def _run(xd, wd, combine, env=None):
 
 
 @pytest.mark.parametrize("T,n,D,K", CASES)
-def test_folded_ring_is_bit_identical_to_gemm_then_ring(T, n, D, K):
+def test_folded_ring_is_bit_identical_to_gemm_then_ring(T, n, D, K, rank_split):
     need_gpu()
+    if rank_split and (T, n, D, K) not in RANK_SPLIT:
+        pytest.skip("the rank-split setting changes nothing for this shape")
     x, w = _layer(T, n, D, K, seed=700 + T + n + D)
     xd = [dev_bf16(a) for a in x]
     wd = [dev_bf16(a) for a in w]
@@ -173,3 +189,23 @@ def test_early_weight_loads_change_no_bits(kind):
     f = inputs.bf16_bits_to_f64
     assert_close(host_f64(ys[0]), O.linear(f(x[0]), f(w[0])) if combine == tp.TP_COMBINE_NONE else
                  sum(O.linear(f(a), f(b)) for a, b in zip(x, w)), BF16_TOL, "result")
+
+
+@pytest.mark.parametrize("T,n,D,K", CASES)
+def test_folded_ring_is_one_kernel_launch(T, n, D, K, rank_split):
+    """With the fold the call is the GEMM alone; without it (TPGQA_RING_EPILOGUE=0,
+    or a split-K shape without TPGQA_RANK_SPLIT=1) the GEMM and the one-pass ring."""
+    need_gpu()
+    folds = (T, n, D, K) not in RANK_SPLIT or rank_split
+    if rank_split and (T, n, D, K) not in RANK_SPLIT:
+        pytest.skip("the rank-split setting changes nothing for this shape")
+    x, w = _layer(T, n, D, K, seed=900 + T + n + D)
+    xd = [dev_bf16(a) for a in x]
+    wd = [dev_bf16(a) for a in w]
+    c0 = tp.tp_launch_count()
+    _run(xd, wd, tp.TP_COMBINE_RING_FUSED)
+    c1 = tp.tp_launch_count()
+    _run(xd, wd, tp.TP_COMBINE_RING_FUSED, env="0")
+    c2 = tp.tp_launch_count()
+    assert c1 - c0 == (1 if folds else 2)
+    assert c2 - c1 == 2
