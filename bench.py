@@ -485,6 +485,7 @@ class DeviceSet:
             return slice(*shards[r]["ranges"][name])
 
         self.calls = []  # (phase name, callable)
+        self.step_calls = []  # block calls that replace the leading phase calls in the timed step
         self.x = to_dev(data["x"])
         self.e2e = {}
         if w["kind"] in ("attn", "layer"):
@@ -520,6 +521,12 @@ class DeviceSet:
             # fold the ring into the GEMM)
             self.calls.append(("o_proj", tp.Prepared("tp_row_linear", n, tp.arr(a_r), tp.arr(o_w), tp.arr(yo),
                                                      COMBINE_NAMES[mode], sptr)))
+            if not self.attention:
+                # the timed step makes the block call, q/k/v and o_proj in one
+                # (the phase pass times the two halves on their own)
+                self.step_calls = [("attn_proj", ("tp_attn_proj", tp.arr([self.x]), tp.arr(q_w), tp.arr(k_w),
+                                                  tp.arr(v_w), tp.arr(q), tp.arr(k), tp.arr(v), tp.arr(a_r),
+                                                  tp.arr(o_w), tp.arr(yo), COMBINE_NAMES[mode]))]
             self.e2e["attn"] = (q_w, k_w, v_w, q, k, v, a_r, o_w, yo)
         if w["kind"] in ("mlp", "layer"):
             F = w["ffn"]
@@ -783,9 +790,16 @@ def run_native(args):
     names = [nm for (nm, _c) in sets[0].calls]
 
     def step(s, ev=None):
-        # a1: the shard plan (host), then every device phase of the step in order
+        # a1: the shard plan (host), then every device phase of the step in order:
+        # the timed step makes the block calls (step_calls stand for the phase
+        # calls they cover); the phase pass (ev given) makes the phase calls
         plan = tp.tp_plan_create(*plan_args)
-        for i, (name, call) in enumerate(s.calls):
+        calls = s.calls
+        if ev is None and s.step_calls:
+            covered = {"attn_proj": ("qkv", "o_proj")}
+            skip = {nm for (b, _c) in s.step_calls for nm in covered[b]}
+            calls = s.step_calls + [(nm, c) for (nm, c) in s.calls if nm not in skip]
+        for i, (name, call) in enumerate(calls):
             if ev:
                 ev[i].record(stream)
             if isinstance(call, tuple):  # plan-bound call: marshal the fresh plan handle

@@ -282,8 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
       cursor_next(p, c);
     }
   }
-  // Prologue done: wait for the previous kernel in the stream, then let the next one launch.
-  ptx::griddep_wait();
+  // Prologue done: wait for the previous kernel in the stream, then let the next
+  // one launch. With defer_dep_wait the kernel shares no buffer with the previous
+  // kernel and waits for it only before exiting (below).
+  if (!p.defer_dep_wait) ptx::griddep_wait();
   ptx::griddep_launch_dependents();
 
   int issued = 0;  // k-blocks whose loads the producer started (thread 0 only)
@@ -480,6 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
+  // The grid completes only after the previous kernel has: kernels after this one
+  // that wait for it also see the previous kernel's writes.
+  if (p.defer_dep_wait && threadIdx.x == 0) ptx::griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -1617,8 +1622,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
           for (int t = 0; t < kMaxSplit; ++t) {
             if (t >= nsplit) break;
             float4 vg[kBatch], vu[kBatch];
-#pragma unroll
             const int ts = ring ? (first + t) % nsplit : t;
+#pragma unroll
             for (int b = 0; b < kBatch; ++b) {
               const int idx = base + b * kThreads < total ? base + b * kThreads : base;
               const int rl = idx / kUnits;
@@ -1795,7 +1800,8 @@ tp_status launch_one(const GemmParams &p, cudaStream_t stream) {
       if (dev < 32) configured_mask |= (1 << dev);
     }
   }
-  const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+  const int cap = p.max_ctas > 0 && p.max_ctas < num_sms() ? p.max_ctas : num_sms();
+  const int grid = p.total_tiles < cap ? p.total_tiles : cap;
   e = launch_kernel(k_gemm_bf16<BN, EPI>, dim3(grid), dim3(kThreads), one_smem_bytes(p.a_rows, BN, p.one_stages),
                     stream, 1, p);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -2101,6 +2107,7 @@ bool GemmBuilder::add_dual_problem(int m, int n, void *out, long long ldc, void 
 tp_status GemmBuilder::launch(cudaStream_t stream) {
   p.num_problems = n_probs;
   p.n_maps_used = n_maps;
+  ctas = 0;
   if (p.total_tiles == 0) return TP_OK;
   DevCtx ctx;
   cudaError_t e = get_dev_ctx(&ctx);
@@ -2152,7 +2159,23 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   }
   if (split < 1 || (pair && bn != 256) || (!pair && bn != 256 && bn != 128) || ring || dual)
     split = 1;  // split-K runs 256-column pair tiles and 128/256-column single-CTA tiles
+  if (defer_dep_wait || max_ctas > 0) split = 1;
   p.split = split;
+  // the deferred wait and the CTA cap are built into the persistent single-CTA kernel only
+  const bool one = !pair && split == 1;
+  p.defer_dep_wait = defer_dep_wait && one ? 1 : 0;
+  p.max_ctas = one ? max_ctas : 0;
+  {
+    const int sms = num_sms();
+    if (split > 1)
+      ctas = p.total_tiles * (pair ? 2 : 1) * split;
+    else if (pair)
+      ctas = 2 * (p.total_tiles < sms / 2 ? p.total_tiles : sms / 2);
+    else {
+      const int cap = p.max_ctas > 0 && p.max_ctas < sms ? p.max_ctas : sms;
+      ctas = p.total_tiles < cap ? p.total_tiles : cap;
+    }
+  }
   // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand
   // and stage replaces KSUB 2-D copies. The single-CTA kernels load one k-tile
   // per stage and keep the 2-D maps.
@@ -2233,7 +2256,7 @@ int choose_split(long long tiles, bool pair, long long stages_per_tile) {
   return s;
 }
 
-int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu) {
+int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu, long long max_ctas) {
   // TPGQA_BN=128|192|224|256 forces the tile width (tuning override).
   static const int forced = [] {
     const char *e = getenv("TPGQA_BN");
@@ -2243,8 +2266,8 @@ int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu) {
   // Single-CTA tiles stream the weights (few rows of activations): a tile's time
   // goes with its width, the kernel's with the waves of tiles over the SMs.
   // 128-column tiles need twice the operand bytes per MMA flop; grids small
-  // enough for split-K keep 256 columns.
-  const long long sms = num_sms();
+  // enough for split-K keep 256 columns. max_ctas > 0: the CTAs the launch may use.
+  const long long sms = max_ctas > 0 && max_ctas < num_sms() ? max_ctas : num_sms();
   const long long mt = (rows + 127) / 128;
   int best = 256;
   long long best_cost = -1;

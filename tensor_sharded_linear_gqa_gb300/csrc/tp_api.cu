@@ -139,7 +139,7 @@ struct ColOut {
 };
 
 tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, const ColOut *outs,
-                           int epi, cudaStream_t s) {
+                           int epi, cudaStream_t s, int *ctas_out = nullptr) {
   const long long T = x.rows, K = x.cols;
   long long t256 = 0, t128 = 0;
   for (int32_t r = 0; r < nb; ++r) {
@@ -175,7 +175,9 @@ tp_status gemm_bf16_column(const tp_tensor &x, int32_t nb, const tp_tensor *w, c
                        &am, &bm, nullptr, &ks, 1))
       return TP_ERR_UNSUPPORTED;
   }
-  return b.launch(s);
+  const tp_status st = b.launch(s);
+  if (ctas_out) *ctas_out = b.ctas;
+  return st;
 }
 
 // Column-parallel GEMM whose input rows come from N chunk buffers: rows
@@ -231,18 +233,17 @@ tp_status gemm_bf16_column_chunks(int32_t n, const tp_tensor *x_chunks, const tp
 // Row-parallel shapes whose per-rank GEMM would split K over SM-pair clusters
 // (too few 256 x 256 tiles for every pair) while the per-rank partials fit one
 // wave of 256 x 128 pair tiles in clusters of 2N CTAs (N = 2 or 4, every
-// 256-row tile inside one ring chunk). With TPGQA_RANK_SPLIT=1 (read on every
-// call) these layers compute each rank's partial on 256 x 128 pair tiles
-// without split-K, whatever the combine, so that the ring fold with one cluster
-// split per rank gives the bits of the GEMM followed by the ring. Off by
-// default: at T = 512, N = 2 (the MLP block's down projection) the folded GEMM
-// took 24.4 us of the step against 23.0 us for the split-K GEMM and the
-// one-pass ring; a 256 x 128 tile loads 1.5 MB of operands per CTA there
-// against 1.0 MB for a split-K 256 x 256 tile, and both run at the rate the
-// shared-memory fill allows.
+// 256-row tile inside one ring chunk). These layers compute each rank's partial
+// on 256 x 128 pair tiles without split-K, whatever the combine, so that the
+// ring fold with one cluster split per rank gives the bits of the GEMM followed
+// by the ring. At T = 512, N = 2 (the MLP block's down projection) the step
+// takes 49.0 us against 50.6 us for the split-K GEMM and the one-pass ring,
+// although a 256 x 128 tile loads 1.5 MB of operands per CTA there against
+// 1.0 MB for a split-K 256 x 256 tile. TPGQA_RANK_SPLIT=0 turns it off (read
+// on every call).
 bool rank_split_shape(int32_t n, const tp_tensor *x, const tp_tensor *w) {
   const char *env = getenv("TPGQA_RANK_SPLIT");
-  if (!(env && env[0] == '1')) return false;
+  if (env && env[0] == '0') return false;
   const long long T = x[0].rows, nout = w[0].rows;
   if ((n != 2 && n != 4) || !choose_pair(T) || T % n != 0 || (T / n) % 256 != 0 || T > (1LL << 30)) return false;
   if (nout < 1 || nout > (1LL << 30)) return false;
@@ -262,8 +263,9 @@ bool rank_split_shape(int32_t n, const tp_tensor *x, const tp_tensor *w) {
 }
 
 // Row-parallel: fused = one problem whose segments are the ranks; else one problem per rank.
+// max_ctas and defer_dep_wait: see GemmParams (single-CTA kernel, T <= 128).
 tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
-                        bool fused, cudaStream_t s) {
+                        bool fused, cudaStream_t s, int max_ctas = 0, bool defer_dep_wait = false) {
   const long long T = x[0].rows, nout = w[0].rows;
   const long long mt = (T + 127) / 128;
   const long long probs = fused ? 1 : n;
@@ -278,8 +280,10 @@ tp_status gemm_bf16_row(int32_t n, const tp_tensor *x, const tp_tensor *w, const
     if (b.pair) {
       b.bn = choose_pair_bn(T, nc.data(), static_cast<int>(probs), false, &b_rows);
     } else {
-      b.bn = choose_bn(T, nc.data(), static_cast<int>(probs), false);
+      b.bn = choose_bn(T, nc.data(), static_cast<int>(probs), false, max_ctas);
       b_rows = b.bn;
+      b.max_ctas = max_ctas;
+      b.defer_dep_wait = defer_dep_wait;
     }
   }
   if (!fused && rank_split_shape(n, x, w)) {
@@ -510,7 +514,8 @@ tp_status check_row_args(int32_t n, const tp_tensor *x, const tp_tensor *w, cons
 }
 
 tp_status row_linear_impl(int32_t n, const tp_tensor *x, const tp_tensor *w, const tp_tensor *y,
-                          int32_t combine, int32_t dt, cudaStream_t s) {
+                          int32_t combine, int32_t dt, cudaStream_t s, int max_ctas = 0,
+                          bool defer_dep_wait = false) {
   const long long T = x[0].rows, nout = w[0].rows;
   if (T == 0 || nout == 0) return TP_OK;
   const bool fused = combine == TP_COMBINE_FUSED;
@@ -529,7 +534,7 @@ tp_status row_linear_impl(int32_t n, const tp_tensor *x, const tp_tensor *w, con
     if (ring_split_ok(n, x, w, y, copies)) return gemm_bf16_row_ring_split(n, x, w, y, copies, s);
   }
   if (dt == TP_BF16)
-    st = gemm_bf16_row(n, x, w, y, fused, s);
+    st = gemm_bf16_row(n, x, w, y, fused, s, max_ctas, defer_dep_wait);
   else
     st = gemm_f32_row(n, x, w, y, fused, s);
   if (st != TP_OK) return st;
@@ -1310,7 +1315,7 @@ tp_status gemm_bf16_qkv_paired(int32_t n, int32_t nkv, const tp_tensor &x, const
 
 tp_status launch_qkv(const tp_dims &d, const tp_rank_shard &s0, const tp_tensor *x, const tp_tensor *w_q,
                      const tp_tensor *w_k, const tp_tensor *w_v, const tp_tensor *q, const tp_tensor *k,
-                     const tp_tensor *v, cudaStream_t s) {
+                     const tp_tensor *v, cudaStream_t s, int *ctas_out = nullptr) {
   const int32_t n = d.tp_size;
   const int32_t nkv = s0.kv_replicated ? 1 : n;
   {
@@ -1334,7 +1339,28 @@ tp_status launch_qkv(const tp_dims &d, const tp_rank_shard &s0, const tp_tensor 
     ws.push_back(w_v[r]);
     outs.push_back(ColOut{v[r].ptr, v[r].ld});
   }
-  return gemm_bf16_column(*x, static_cast<int32_t>(ws.size()), ws.data(), outs.data(), kEpiBF16, s);
+  return gemm_bf16_column(*x, static_cast<int32_t>(ws.size()), ws.data(), outs.data(), kEpiBF16, s, ctas_out);
+}
+
+// Bytes [begin, end) a tensor's elements span.
+struct Span {
+  uintptr_t begin, end;
+};
+Span tensor_span(const tp_tensor &t) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(t.ptr);
+  if (t.rows <= 0 || t.cols <= 0) return Span{b, b};
+  const long long es = t.dtype == TP_F32 ? 4 : 2;
+  return Span{b, b + static_cast<uintptr_t>(((t.rows - 1) * t.ld + t.cols) * es)};
+}
+bool spans_overlap(const tp_tensor *a, int na, const tp_tensor *b, int nb) {
+  for (int i = 0; i < na; ++i) {
+    const Span x = tensor_span(a[i]);
+    for (int j = 0; j < nb; ++j) {
+      const Span y = tensor_span(b[j]);
+      if (x.begin < y.end && y.begin < x.end) return true;
+    }
+  }
+  return false;
 }
 
 }  // namespace
@@ -1383,8 +1409,34 @@ extern "C" tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const
   if ((st = check_health(n)) != TP_OK) return st;
   if (T == 0) return TP_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = launch_qkv(d, s0, x, w_q, w_k, w_v, q, k, v, s)) != TP_OK) return st;
-  // o_proj row-parallel + combine.
+  int qkv_ctas = 0;
+  if ((st = launch_qkv(d, s0, x, w_q, w_k, w_v, q, k, v, s, &qkv_ctas)) != TP_OK) return st;
+  // o_proj row-parallel + combine. o_proj does not read what q/k/v write, so at
+  // decode sizes (T <= 128, where neither GEMM fills the GPU's HBM stream alone)
+  // it runs beside q/k/v on the SMs q/k/v leaves free, and waits for q/k/v only
+  // before it exits. Only where the GEMM alone would run one problem per rank
+  // without split-K (its partials then have the same bits on fewer CTAs), and
+  // not when its buffers overlap q/k/v's; TPGQA_CONCURRENT_OPROJ=0 turns it off
+  // (read on every call).
+  bool beside = false;
+  {
+    const char *env = getenv("TPGQA_CONCURRENT_OPROJ");
+    const int32_t nkv = s0.kv_replicated ? 1 : n;
+    const int32_t ny = combine == TP_COMBINE_FUSED ? 1 : n;
+    bool unsplit = false;
+    if (combine != TP_COMBINE_FUSED && T <= 128 && !choose_pair(T)) {
+      const std::vector<long long> nc(static_cast<size_t>(n), D);
+      const int bn = choose_bn(T, nc.data(), n, false);
+      const long long tiles = static_cast<long long>(n) * ((T + 127) / 128) * ((D + bn - 1) / bn);
+      unsplit = !(bn == 256 && tiles * 2 <= num_sms());
+    }
+    beside = !(env && env[0] == '0') && unsplit && qkv_ctas > 0 && qkv_ctas + 16 <= num_sms() &&
+             !spans_overlap(a, n, q, n) && !spans_overlap(a, n, k, nkv) && !spans_overlap(a, n, v, nkv) &&
+             !spans_overlap(y, ny, q, n) && !spans_overlap(y, ny, k, nkv) && !spans_overlap(y, ny, v, nkv) &&
+             !spans_overlap(y, ny, x, 1) && !spans_overlap(y, ny, w_q, n) && !spans_overlap(y, ny, w_k, nkv) &&
+             !spans_overlap(y, ny, w_v, nkv);
+  }
+  if (beside) return row_linear_impl(n, a, w_o, y, combine, TP_BF16, s, num_sms() - qkv_ctas, true);
   return row_linear_impl(n, a, w_o, y, combine, TP_BF16, s);
 }
 

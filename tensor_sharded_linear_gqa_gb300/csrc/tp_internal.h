@@ -161,6 +161,13 @@ struct GemmParams {
   // chunk's ring order and stored to ring_dst[0 .. ring_copies - 1] (row pitch of
   // the problem's output).
   void *ring_dst[kMaxRingCopies];
+  // Persistent single-CTA kernel only. max_ctas > 0 caps its grid (the other SMs
+  // are left to a kernel running beside it). defer_dep_wait = 1: the kernel
+  // reads nothing the previous kernel on its stream writes and writes nothing
+  // that kernel touches, so it starts at once, and waits for that kernel only
+  // before it exits (its completion still implies the previous kernel's).
+  int max_ctas;
+  int defer_dep_wait;
   int *status;
   long long wait_ns;
 };
@@ -211,12 +218,16 @@ struct GemmBuilder {
   bool add_dual_problem(int m, int n, void *out, long long ldc, void *out2, long long ldc2, int a_map,
                         int b_map, int b2_map, long long k);
   bool dual = false;  // some problem has two outputs (forces the SM-pair kernel, no split)
+  int max_ctas = 0;             // see GemmParams::max_ctas (forces no split)
+  bool defer_dep_wait = false;  // see GemmParams::defer_dep_wait (forces no split)
+  int ctas = 0;                 // after launch(): the CTAs the launch started
   tp_status launch(cudaStream_t stream);
 };
 
 // Tile width of the single-CTA kernels (256, 224 or 192 accumulator columns)
 // for problems of `rows` rows and ncols[i] output columns.
-int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu);
+// max_ctas > 0: the CTAs the launch may use (default: every SM).
+int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu, long long max_ctas = 0);
 // Rows of an A box for problems of `rows` rows on the single-CTA kernels.
 int a_box_rows(long long rows);
 // Tile width of the SM-pair kernel (256 or 224 accumulator columns) for

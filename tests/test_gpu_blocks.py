@@ -197,6 +197,55 @@ def test_decode_replicated_kv_tp8_t64(combine):
         assert_close(host_f64(y), ref["y"][0], BF16_TOL, "MLP Y")
 
 
+def _attn_then_core(L, combine):
+    """tp_attn_proj into NaN-filled q/k/v, then, on the same stream and with no
+    synchronisation between, the attention core over those q/k/v."""
+    t, n, T = L.t, L.n, L.T
+    D = L.w["hidden"]
+    rep = L.shards[0]["kv_replicated"]
+    kv_ranks = 1 if rep else n
+    wq = [L.dev["wq"][slice(*L.rng(r, "q_proj"))] for r in range(n)]
+    wk = [L.dev["wk"][slice(*L.rng(r, "k_proj"))] for r in range(kv_ranks)]
+    wv = [L.dev["wv"][slice(*L.rng(r, "v_proj"))] for r in range(kv_ranks)]
+    a = [L.dev["a"][:, slice(*L.rng(r, "o_proj"))] for r in range(n)]
+    wo = [L.dev["wo"][:, slice(*L.rng(r, "o_proj"))] for r in range(n)]
+    nan = float("nan")
+    q = [t.full((T, x.shape[0]), nan, dtype=t.bfloat16, device="cuda") for x in wq]
+    k = [t.full((T, x.shape[0]), nan, dtype=t.bfloat16, device="cuda") for x in wk]
+    v = [t.full((T, x.shape[0]), nan, dtype=t.bfloat16, device="cuda") for x in wv]
+    ys = [t.full((T, D), nan, device="cuda") for _ in range(1 if combine == tp.TP_COMBINE_FUSED else n)]
+    att = [t.full((T, x.shape[0]), nan, dtype=t.bfloat16, device="cuda") for x in wq]
+    ws = t.empty(max(1, tp.tp_attn_core_workspace_size(L.plan, T)), dtype=t.uint8, device="cuda")
+    t.cuda.synchronize()
+    tp.tp_attn_proj(L.plan, L.x, wq, wk, wv, q, k, v, a, wo, ys, combine)
+    tp.tp_attn_core(L.plan, q, k, v, att, True, ws)
+    t.cuda.synchronize()
+    assert tp.tp_device_status() == (tp.TP_OK, 0)
+    return [host_bits_f32(y) for y in ys], [host_f64(x) for x in q + k + v], [host_f64(x) for x in att]
+
+
+@pytest.mark.parametrize("combine", [tp.TP_COMBINE_RING_FUSED, tp.TP_COMBINE_RING, tp.TP_COMBINE_FUSED])
+def test_decode_oproj_beside_qkv(combine, monkeypatch):
+    """At decode sizes o_proj runs beside the q/k/v GEMM on the SMs it leaves
+    free and waits for it only before exiting (not with the FUSED combine, whose
+    single problem splits K). The results equal, bit for bit, those of the
+    serial order (TPGQA_CONCURRENT_OPROJ=0), and a kernel launched after the call
+    on the same stream (the attention core, reading q/k/v) sees q/k/v complete:
+    NaN-filled q/k/v read too early would spread into its output."""
+    need_gpu()
+    L, _f = layer("decode_gqa_rep_tp8_t64")
+    monkeypatch.setenv("TPGQA_CONCURRENT_OPROJ", "0")
+    y0, qkv0, att0 = _attn_then_core(L, combine)
+    monkeypatch.setenv("TPGQA_CONCURRENT_OPROJ", "1")
+    for _ in range(3):
+        y1, qkv1, att1 = _attn_then_core(L, combine)
+        for a_, b_ in zip(y0, y1):
+            assert np.array_equal(a_, b_)
+        for a_, b_ in zip(qkv0 + att0, qkv1 + att1):
+            assert np.isfinite(b_).all()
+            assert np.array_equal(a_, b_)
+
+
 @pytest.mark.parametrize("tp_size,hq,hkv", [(4, 8, 4), (8, 16, 2)])
 def test_qkv_proj_matches_oracle(tp_size, hq, hkv):
     need_gpu()

@@ -31,9 +31,8 @@ CASES = [
     (2048, 8, 1000, 200),
     (2048, 4, 4096, 1024),   # the attention projection's o_proj shape
     # grids too small for one 256 x 256 tile per SM pair (the GEMM alone would
-    # split K): with TPGQA_RANK_SPLIT=1 the fold runs in the split-K pair kernel,
-    # one cluster split per rank; by default the GEMM splits K and the ring runs
-    # after it
+    # split K): the fold runs in the split-K pair kernel, one cluster split per
+    # rank; with TPGQA_RANK_SPLIT=0 the GEMM splits K and the ring runs after it
     (512, 2, 2048, 4096),    # the T=512 MLP block's down projection
     (512, 2, 1000, 1000),
     (1024, 4, 264, 2048),
@@ -41,7 +40,7 @@ CASES = [
 RANK_SPLIT = {(512, 2, 2048, 4096), (512, 2, 1000, 1000), (1024, 4, 264, 2048)}
 
 
-@pytest.fixture(params=["0", "1"], ids=["default", "rank_split"])
+@pytest.fixture(params=["0", "1"], ids=["rank_split_off", "rank_split"])
 def rank_split(request, monkeypatch):
     monkeypatch.setenv("TPGQA_RANK_SPLIT", request.param)
     return request.param == "1"
@@ -194,7 +193,7 @@ def test_early_weight_loads_change_no_bits(kind):
 @pytest.mark.parametrize("T,n,D,K", CASES)
 def test_folded_ring_is_one_kernel_launch(T, n, D, K, rank_split):
     """With the fold the call is the GEMM alone; without it (TPGQA_RING_EPILOGUE=0,
-    or a split-K shape without TPGQA_RANK_SPLIT=1) the GEMM and the one-pass ring."""
+    or a split-K shape with TPGQA_RANK_SPLIT=0) the GEMM and the one-pass ring."""
     need_gpu()
     folds = (T, n, D, K) not in RANK_SPLIT or rank_split
     if rank_split and (T, n, D, K) not in RANK_SPLIT:
