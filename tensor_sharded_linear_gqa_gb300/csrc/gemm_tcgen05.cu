@@ -505,10 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
 constexpr int kPairABytes = 128 * BK * 2;  // one 64-wide k-tile of this CTA's 128 A rows
 // BN accumulator columns per tile: each CTA holds BN/2 rows of B (for SwiGLU,
 // BN/2 gate rows in CTA 0 and BN/2 up rows in CTA 1). BN is 256, or 224 when
-// narrower tiles fill the last wave better. BN = 512 (SwiGLU only, one 64-wide
-// k-tile per stage): 256 gate and 256 up columns per tile, computed by two
-// N=256 MMAs per k-step into one 512-column accumulator; each CTA holds 128
-// gate rows and 128 up rows of B (its half of each MMA's N).
+// narrower tiles fill the last wave better. BN = 512 or 448 (SwiGLU only, one
+// 64-wide k-tile per stage): BN/2 gate and BN/2 up columns per tile, computed by
+// two N = BN/2 MMAs per k-step into accumulators at TMEM columns 0 and 256; each
+// CTA holds BN/4 gate rows and BN/4 up rows of B (its half of each MMA's N).
 template <int KSUB, int BN>
 struct PairCfg {
   static constexpr int kBRows = BN / 2;
@@ -516,7 +516,9 @@ struct PairCfg {
   static constexpr int kStageBytes = KSUB * (kPairABytes + kBBytes);
   // as many stages as fit beside the barriers: 3 for 256- and 224-column tiles
   // of 128-deep stages, 4 for 128-column tiles
-  static constexpr int kStages = (kSmemLimit - 1280) / kStageBytes > 4 ? 4 : (kSmemLimit - 1280) / kStageBytes;
+  static constexpr int kMaxStages = KSUB == 1 ? 5 : 4;
+  static constexpr int kStages =
+      (kSmemLimit - 1280) / kStageBytes > kMaxStages ? kMaxStages : (kSmemLimit - 1280) / kStageBytes;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 256;
   static_assert(kBBytes % 1024 == 0, "B k-tiles must keep the 1024-byte swizzle alignment");
 };
@@ -545,11 +547,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int kPrefetch = p.prefetch;
   constexpr uint32_t kTmemCols = 512;  // two accumulators, at columns 0 and 256 (one of 512 columns at BN 512)
   constexpr int S = kPairStages;
-  constexpr bool kWide = BN == 512;
-  static_assert(!kWide || (EPI == kEpiSwiGLU && KSUB == 1), "512-column tiles: SwiGLU, 64-wide stages");
+  constexpr bool kWide = BN == 512 || BN == 448;
+  static_assert(!kWide || (EPI == kEpiSwiGLU && KSUB == 1), "wide tiles: SwiGLU, 64-wide stages");
   constexpr int kAcc = kWide ? 1 : 2;          // accumulators in TMEM
-  constexpr int kMmaN = kWide ? 256 : BN;      // N of one MMA
-  constexpr uint32_t kWideUp = 128u * 128u;    // BN 512: up rows after the 128 gate rows of a k-tile
+  constexpr int kMmaN = kWide ? BN / 2 : BN;   // N of one MMA
+  constexpr int kWideRows = BN / 4;            // wide tiles: gate (and up) rows of B per CTA
+  constexpr uint32_t kWideUp = static_cast<uint32_t>(kWideRows) * 128u;  // up rows after the gate rows
+  constexpr int kUpCol = kWide ? 256 : BN / 2;  // TMEM column of the up sums (SwiGLU)
+  static_assert(kWideUp % 1024 == 0, "up rows keep the 1024-byte swizzle alignment");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -614,7 +619,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t lead_full = ptx::mapa_shared(full_bar(pre), 0);
         if (leader) ptx::mbar_arrive_expect_tx(full_bar(pre), 2 * kPairStageBytes);
         if constexpr (kWide) {
-          const int wrow = nt * 256 + static_cast<int>(rank) * 128;
+          const int wrow = nt * (BN / 2) + static_cast<int>(rank) * kWideRows;
           ptx::tma_load_2d_pair(sB0 + pre * kPairBBytes, &p.maps[sg.b_map], kt * BK, wrow, lead_full);
           ptx::tma_load_2d_pair(sB0 + pre * kPairBBytes + kWideUp, &p.maps[sg.b2_map], kt * BK, wrow, lead_full);
         } else if (p.box_kt > 1) {
@@ -669,7 +674,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const GemmSeg &sg = p.seg[p.prob[c.prob].seg_begin + c.seg];
         if (kWide) {  // both B matrices in each CTA (the gate map is named here)
           map = sg.b_map + c.moff;
-          row = c.brow + c.nt * 256 + static_cast<int>(rank) * 128;
+          row = c.brow + c.nt * (BN / 2) + static_cast<int>(rank) * kWideRows;
         } else if (EPI == kEpiSwiGLU || sg.b2_map >= 0) {  // two B matrices, one half of the tile each
           map = (leader ? sg.b_map : sg.b2_map) + c.moff;
           row = c.brow + c.nt * kHalfB;
@@ -782,7 +787,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               ptx::mma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (k0 | j | k) != 0 ? 1u : 0u);
               if constexpr (kWide) {
                 const uint64_t ud = ptx::smem_desc_sw128(sB0 + (st * kPairSub + j) * kPairBBytes + kWideUp);
-                ptx::mma_bf16_pair(d + 256u, ad + 2 * k, ud + 2 * k, idesc, (k0 | j | k) != 0 ? 1u : 0u);
+                ptx::mma_bf16_pair(d + static_cast<uint32_t>(kUpCol), ad + 2 * k, ud + 2 * k, idesc,
+                                   (k0 | j | k) != 0 ? 1u : 0u);
               }
             }
           }
@@ -823,7 +829,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kFull; c += 32) {
           uint32_t g[32], u[32];
           ptx::tmem_ld_32cols(tbase + c, g);
-          ptx::tmem_ld_32cols(tbase + BN / 2 + c, u);
+          ptx::tmem_ld_32cols(tbase + kUpCol + c, u);
           ptx::tmem_ld_wait();
           ptx::tmem_regs_ready(g);
           ptx::tmem_regs_ready(u);
@@ -841,7 +847,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           static_assert(BN / 2 - kFull == 16, "a 16-column tail");
           uint32_t g[16], u[16];
           ptx::tmem_ld_16cols(tbase + kFull, g);
-          ptx::tmem_ld_16cols(tbase + BN / 2 + kFull, u);
+          ptx::tmem_ld_16cols(tbase + kUpCol + kFull, u);
           ptx::tmem_ld_wait();
           ptx::tmem_regs_ready(g);
           ptx::tmem_regs_ready(u);
@@ -1847,9 +1853,9 @@ int pair_ksub() {
 
 template <int EPI>
 tp_status launch_pair(const GemmParams &p, int bn, cudaStream_t stream) {
-  if (bn == 512) {
+  if (bn == 512 || bn == 448) {
     if constexpr (EPI == kEpiSwiGLU)
-      return launch_pair_ks<EPI, 1, 512>(p, stream);
+      return bn == 512 ? launch_pair_ks<EPI, 1, 512>(p, stream) : launch_pair_ks<EPI, 1, 448>(p, stream);
     else
       return TP_ERR_UNSUPPORTED;
   }
@@ -2179,7 +2185,7 @@ tp_status GemmBuilder::launch(cudaStream_t stream) {
   // The SM-pair kernels load KSUB k-tiles per stage; one 3-D copy per operand
   // and stage replaces KSUB 2-D copies. The single-CTA kernels load one k-tile
   // per stage and keep the 2-D maps.
-  p.box_kt = !pair || bn == 512 ? 1 : use_3d_boxes(split > 1 || bn != 256 ? SplitCfg<true, 256>::kSub : pair_ksub());
+  p.box_kt = !pair || bn == 512 || bn == 448 ? 1 : use_3d_boxes(split > 1 || bn != 256 ? SplitCfg<true, 256>::kSub : pair_ksub());
   if (ring) return launch_pair_ring(p, bn, stream);
   if (split > 1) {
     if (pair) {
@@ -2286,14 +2292,14 @@ int choose_bn(long long rows, const long long *ncols, int nprob, bool swiglu, lo
 }
 
 int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, int *b_rows) {
-  // TPGQA_PAIR_BN=128|224|256|512 forces the SM-pair tile width (tuning
-  // override; 512 applies to SwiGLU problems only).
+  // TPGQA_PAIR_BN=128|224|256|448|512 forces the SM-pair tile width (tuning
+  // override; 448 and 512 apply to SwiGLU problems only).
   static const int forced = [] {
     const char *e = getenv("TPGQA_PAIR_BN");
     return e ? atoi(e) : 0;
   }();
   int best = 256;
-  if (forced == 128 || forced == 224 || forced == 256 || (forced == 512 && swiglu)) {
+  if (forced == 128 || forced == 224 || forced == 256 || ((forced == 448 || forced == 512) && swiglu)) {
     best = forced;
   } else {
     // A tile's time goes with its stage bytes (the loads bound the pair's
@@ -2317,19 +2323,24 @@ int choose_pair_bn(long long m, const long long *ncols, int nprob, bool swiglu, 
       }
     }
     // SwiGLU grids of more than one wave of 256-column tiles that fit one wave
-    // of 512-column tiles (256 gate and 256 up columns): one tile per SM pair,
-    // half the A bytes per MMA flop. The single accumulator leaves no epilogue
-    // overlap, which a single wave does not need.
+    // of wide tiles (BN/2 gate and BN/2 up columns): one tile per SM pair, half
+    // the A bytes per MMA flop. A single wave's time goes with the tile width,
+    // so the narrower of 448 and 512 that fits wins. The single accumulator
+    // leaves no epilogue overlap, which a single wave does not need.
     if (swiglu && forced == 0) {
-      long long t256 = 0, t512 = 0;
+      long long t256 = 0, t448 = 0, t512 = 0;
       for (int i = 0; i < nprob; ++i) {
         t256 += mt * ((ncols[i] + 127) / 128);
+        t448 += mt * ((ncols[i] + 223) / 224);
         t512 += mt * ((ncols[i] + 255) / 256);
       }
-      if (t256 > pairs && t512 <= pairs) best = 512;
+      if (t256 > pairs && t448 <= pairs)
+        best = 448;
+      else if (t256 > pairs && t512 <= pairs)
+        best = 512;
     }
   }
-  *b_rows = best == 512 ? 128 : best / 2;
+  *b_rows = best == 512 || best == 448 ? best / 4 : best / 2;
   return best;
 }
 

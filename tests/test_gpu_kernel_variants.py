@@ -7,7 +7,7 @@ on the shape. The SM-pair kernels fetch each stage with one 3-D TMA copy per
 operand when every K is a multiple of 64, else with one 2-D copy per k-tile.
 Split-K reduces the splits' partials through the cluster's shared memory in a
 fixed order. The persistent SM-pair kernel runs 256-, 224- or 128-column tiles
-(and 512-column SwiGLU tiles: 256 gate and 256 up columns), the single-CTA
+(and 448- and 512-column SwiGLU tiles: half gate, half up columns), the single-CTA
 kernel 128- to 256-column ones. The tuning overrides TPGQA_PAIR,
 TPGQA_KSUB, TPGQA_SPLIT, TPGQA_TMA3D, TPGQA_PAIR_BN and TPGQA_BN force one
 variant, so each variant here reruns the linear-layer and MLP parity tests in a
@@ -33,7 +33,8 @@ TESTS = ["tests/test_gpu_linear.py",
     ("1", "1", "2", "0", "256", "256"), ("1", "1", "3", "0", "256", "256"), ("1", "1", "2", "1", "224", "256"),
     ("1", "1", "2", "0", "224", "256"), ("0", "2", "2", "1", "256", "256"), ("0", "4", "2", "1", "256", "256"),
     ("1", "2", "2", "1", "256", "256"), ("1", "4", "2", "1", "256", "256"), ("1", "2", "2", "0", "256", "256"),
-    ("1", "1", "2", "1", "128", "256"), ("1", "1", "2", "0", "128", "256"), ("1", "1", "2", "1", "512", "256")])
+    ("1", "1", "2", "1", "128", "256"), ("1", "1", "2", "0", "128", "256"), ("1", "1", "2", "1", "512", "256"),
+    ("1", "1", "2", "1", "448", "256")])
 def test_kernel_variant_parity(pair, split, ksub, tma3d, pair_bn, bn):
     from gpu_util import need_gpu
     need_gpu()
