@@ -23,7 +23,12 @@
 //     tile belongs to exactly one rank).
 //  4. k_moe_combine gives rank r's partial output: per token, the sum over its
 //     slots in slot order of weight * the slot's down-projection row, for the
-//     slots rank r ran. The caller's ring all-reduce then combines the ranks.
+//     slots rank r ran. The caller's ring all-reduce then combines the ranks;
+//     for the one-pass ring (every rank's output, or the shared one) the same
+//     kernel folds the ranks' partials in the ring's order instead (mlxcel
+//     manual "텐서 병렬화", 통신 패턴: chunk c of the flat output reduced as
+//     x_{c+1} + ... + x_c), so the partials are never written.
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -183,13 +188,86 @@ struct CombineArgs {
   long long y_ld[kMaxRanks];   // their row pitches (elements)
   long long tokens, d4;        // d4: float4 units per row
   int k, n, per_rank_src, ep_filter;
+  // 0: output o gets rank o's partial; 1: every output gets the ring all-reduce
+  // of the partials; 2: output 0 alone gets it. Outputs are contiguous ([T x D])
+  // when ring != 0.
+  int ring;
 };
 
+// Rank r's partial of token t, float4 unit v: the sum over the token's slots in
+// order of weight * the slot's down-projection row, over the slots rank r ran.
+__device__ __forceinline__ float4 moe_partial(const CombineArgs &a, int r, long long t, long long v) {
+  const float4 *src = reinterpret_cast<const float4 *>(a.yp[a.per_rank_src ? r : 0]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < a.k; ++j) {
+    const long long s = t * a.k + j;
+    const int p = __ldg(a.pos + s);
+    if (p < 0) continue;
+    if (a.ep_filter && __ldg(a.ids + s) % a.n != r) continue;
+    const float wt = __ldg(a.w + s);
+    const float4 x = src[p * a.d4 + v];
+    acc.x = fmaf(wt, x.x, acc.x);
+    acc.y = fmaf(wt, x.y, acc.y);
+    acc.z = fmaf(wt, x.z, acc.z);
+    acc.w = fmaf(wt, x.w, acc.w);
+  }
+  return acc;
+}
+
+// Ring chunk of flat element e of S: chunk c holds [floor(cS/N), floor((c+1)S/N)).
+__device__ __forceinline__ int ring_chunk(long long e, long long S, int n) {
+  return static_cast<int>(((e + 1) * n + S - 1) / S - 1);
+}
+
+__device__ __forceinline__ float lane_of(const float4 &x, int i) {
+  return i == 0 ? x.x : i == 1 ? x.y : i == 2 ? x.z : x.w;
+}
+
 // Grid (token CTAs, outputs). Output o sums, for each token, its slots in order
-// (weight * row pos of the slot) over the slots rank o ran.
+// (weight * row pos of the slot) over the slots rank o ran. With a.ring, one
+// grid row computes every rank's partial of an element and folds them in the
+// order of the element's ring chunk, rank c+1 first, as the one-pass ring adds
+// the stored partials.
 __global__ void __launch_bounds__(kThreads) k_moe_combine(CombineArgs a) {
   griddep_wait();
   griddep_launch_dependents();
+  if (a.ring) {
+    const int n = a.n;
+    const long long S = a.tokens * a.d4 * 4;
+    for (long long t = blockIdx.x; t < a.tokens; t += gridDim.x) {
+      for (long long v = threadIdx.x; v < a.d4; v += kThreads) {
+        const long long e = (t * a.d4 + v) * 4;
+        const int c = ring_chunk(e, S, n);
+        float4 sum;
+        if (c == ring_chunk(e + 3, S, n)) {
+          for (int j = 0; j < n; ++j) {
+            const float4 x = moe_partial(a, (c + 1 + j) % n, t, v);
+            if (j == 0) {
+              sum = x;
+            } else {
+              sum.x = sum.x + x.x;
+              sum.y = sum.y + x.y;
+              sum.z = sum.z + x.z;
+              sum.w = sum.w + x.w;
+            }
+          }
+        } else {  // the unit straddles two chunks: fold each element in its own order
+          float f[4];
+          for (int i = 0; i < 4; ++i) {
+            const int ci = ring_chunk(e + i, S, n);
+            for (int j = 0; j < n; ++j) {
+              const float x = lane_of(moe_partial(a, (ci + 1 + j) % n, t, v), i);
+              f[i] = j == 0 ? x : f[i] + x;
+            }
+          }
+          sum = make_float4(f[0], f[1], f[2], f[3]);
+        }
+        for (int o = 0; o < (a.ring == 1 ? n : 1); ++o)
+          reinterpret_cast<float4 *>(a.y[o] + t * a.y_ld[o])[v] = sum;
+      }
+    }
+    return;
+  }
   const int o = blockIdx.y;
   const float4 *src = reinterpret_cast<const float4 *>(a.yp[a.per_rank_src ? o : 0]);
   for (long long t = blockIdx.x; t < a.tokens; t += gridDim.x) {
@@ -240,6 +318,12 @@ MoeLayout moe_layout(int n, int mode, int experts, int k, long long tokens, long
   o += align256(static_cast<size_t>(ypart_copies * L.rows * hidden) * 4);
   L.total = o;
   return L;
+}
+
+bool moe_ring_folded(int32_t combine, int n) {
+  if (n < 2 || (combine != TP_COMBINE_RING_FUSED && combine != TP_COMBINE_RING_SHARED)) return false;
+  const char *env = getenv("TPGQA_MOE_RING_FOLD");
+  return !(env && env[0] == '0');
 }
 
 tp_status moe_forward(const MoeCall &c, cudaStream_t s) {
@@ -399,6 +483,15 @@ tp_status moe_forward(const MoeCall &c, cudaStream_t s) {
   ca.n = n;
   ca.per_rank_src = within && !fused;
   ca.ep_filter = !within && !fused;
+  // the one-pass ring folded into the combine (TPGQA_MOE_RING_FOLD=0 leaves it
+  // to the caller's all-reduce; read on every call)
+  ca.ring = moe_ring_folded(c.combine, n) ? (c.combine == TP_COMBINE_RING_FUSED ? 1 : 2) : 0;
+  if (ca.ring) {
+    long long gx = static_cast<long long>(num_sms()) * 8;
+    if (gx > T) gx = T;
+    return launch_checked(launch_kernel(k_moe_combine, dim3(static_cast<unsigned>(gx), 1), dim3(kThreads), 0, s, 1,
+                                        ca));
+  }
   long long gx = static_cast<long long>(num_sms()) * 8 / n_out;
   if (gx < 1) gx = 1;
   if (gx > T) gx = T;

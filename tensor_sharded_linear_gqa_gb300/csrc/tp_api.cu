@@ -11,6 +11,10 @@
 #include "tp_internal.h"
 
 namespace tpgqa {
+
+// moe.cu: whether moe_forward folds the one-pass ring (RING_FUSED or RING_SHARED)
+// into the MoE block's weighted combine, leaving no all-reduce to the caller.
+bool moe_ring_folded(int32_t combine, int n);
 namespace {
 
 __device__ int g_dev_status = 0;
@@ -1029,6 +1033,7 @@ extern "C" tp_status tp_moe_block(const tp_moe_dims *d, const tp_tensor *x, cons
   c.y = y;
   c.workspace = workspace;
   if ((st = moe_forward(c, s)) != TP_OK) return st;
+  if (moe_ring_folded(combine, n)) return TP_OK;  // the combine kernel ran the one-pass ring
   if (combine == TP_COMBINE_RING) return run_allreduce(n, y, TP_RING_STEPS, s);
   if (combine == TP_COMBINE_RING_FUSED) return run_allreduce(n, y, TP_RING_FUSED, s);
   if (combine == TP_COMBINE_RING_SHARED) return run_allreduce(n, y, TP_RING_FUSED_SHARED, s);

@@ -179,3 +179,29 @@ def test_moe_mixtral_tp8_t4096_sampled_rows():
                                [f(data["ed"][e])])
     for r in (0, n - 1):
         assert_close(host_f64(ys[r])[rows], ref, BF16_TOL, f"rank {r}")
+
+
+@pytest.mark.parametrize("mode", list(MODES))
+@pytest.mark.parametrize("n,E,k,T,D,F", [(4, 4, 2, 31, 200, 256), (8, 8, 2, 31, 200, 512), (2, 4, 2, 300, 256, 512)])
+def test_ring_folded_into_the_combine(mode, n, E, k, T, D, F, monkeypatch):
+    """RING_FUSED and RING_SHARED fold the ranks' partials inside the weighted
+    combine, each element in its ring chunk's order (31 x 200 outputs put chunk
+    boundaries inside float4 units). The bits equal the combine followed by the
+    one-pass ring (TPGQA_MOE_RING_FOLD=0) and the step ring, on every rank."""
+    need_gpu()
+    if mode == O.MOE_EXPERT_PARALLEL and E % n:
+        pytest.skip("expert parallel needs E divisible by N")
+    m = Moe(n, mode, E, k, T, D, F, seed=530 + n * 10 + E)
+    folded = m.run(tp.TP_COMBINE_RING_FUSED)
+    shared = m.run(tp.TP_COMBINE_RING_SHARED)
+    steps = m.run(tp.TP_COMBINE_RING)
+    monkeypatch.setenv("TPGQA_MOE_RING_FOLD", "0")
+    unfolded = m.run(tp.TP_COMBINE_RING_FUSED)
+    torch = _torch()
+    for r in range(n):
+        assert torch.equal(folded[r], unfolded[r]), f"rank {r}"
+        assert torch.equal(folded[r], steps[r]), f"rank {r}, step ring"
+    assert torch.equal(shared[0], folded[0])
+    ref = m.oracle()
+    assert_close(host_f64(folded[0]), ref["y"][0], BF16_TOL, "folded")
+    assert tp.tp_device_status() == (tp.TP_OK, 0)
