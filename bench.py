@@ -543,6 +543,12 @@ class DeviceSet:
                                            tp.arr(h))))
             self.calls.append(("down", tp.Prepared("tp_row_linear", n, tp.arr(h), tp.arr(dn), tp.arr(ym),
                                                    COMBINE_NAMES[mode], sptr)))
+            # the timed step makes the block call (gate/up and down with its combine)
+            self.mws = torch.empty(tp.tp_mlp_block_workspace_size(plan, T), dtype=torch.uint8, device=dev)
+            self.keep.append(self.mws)
+            self.step_calls.append(("mlp_block", ("tp_mlp_block", tp.arr([self.x]), tp.arr(g), tp.arr(u), tp.arr(dn),
+                                                  tp.arr(ym), COMBINE_NAMES[mode], self.mws.data_ptr(),
+                                                  self.mws.numel())))
             self.e2e["mlp"] = (g, u, dn, ym)
         if w["kind"] == "attn_core":
             hd = w["head_dim"]
@@ -796,9 +802,16 @@ def run_native(args):
         plan = tp.tp_plan_create(*plan_args)
         calls = s.calls
         if ev is None and s.step_calls:
-            covered = {"attn_proj": ("qkv", "o_proj")}
-            skip = {nm for (b, _c) in s.step_calls for nm in covered[b]}
-            calls = s.step_calls + [(nm, c) for (nm, c) in s.calls if nm not in skip]
+            covered = {"attn_proj": ("qkv", "o_proj"), "mlp_block": ("gate_up", "down")}
+            block_of = {nm: (b, c) for (b, c) in s.step_calls for nm in covered[b]}
+            # each block call where its first phase call stood, the other phase calls kept
+            calls, placed = [], set()
+            for nm, c in s.calls:
+                if nm not in block_of:
+                    calls.append((nm, c))
+                elif block_of[nm][0] not in placed:
+                    placed.add(block_of[nm][0])
+                    calls.append(block_of[nm])
         for i, (name, call) in enumerate(calls):
             if ev:
                 ev[i].record(stream)
