@@ -509,6 +509,10 @@ tp_status tp_qkv_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *
  *             context that feeds o_proj (attention itself is not part of this call).
  *  w_o[r]   : [D x (q heads of r) * hd] bf16 (columns plan.range(O) of Wo).
  *  y        : f32 [T x D]; y[0] for TP_COMBINE_FUSED, y[0..N-1] otherwise.
+ * Ordering: the call's results are complete for every kernel enqueued after it
+ * on the stream. At decode sizes (T <= 128) o_proj runs on the device beside
+ * the q/k/v GEMM, when a and y share no byte with q, k, v (nor y with x and the
+ * q/k/v weights); overlapping buffers are allowed and run the two in order.
  * Errors: as tp_mlp_block (no workspace). */
 tp_status tp_attn_proj(const tp_plan *plan, const tp_tensor *x, const tp_tensor *w_q,
                        const tp_tensor *w_k, const tp_tensor *w_v, tp_tensor *q, tp_tensor *k,
