@@ -83,3 +83,18 @@ def test_split_k_reduction_is_deterministic(split):
     r = subprocess.run([sys.executable, "-c", _REPEAT], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("pair_bn", ["448", "512"])
+def test_wide_swiglu_tiles_with_block_tables(pair_bn):
+    """The MoE block's gate/up GEMM takes each tile's expert weights through a
+    block table; with the wide SwiGLU tiles forced, every gate and up row of a
+    tile comes from its expert's slot. Reruns the MoE parity tests in a child
+    process with TPGQA_PAIR_BN set."""
+    from gpu_util import need_gpu
+    need_gpu()
+    env = dict(os.environ, TPGQA_PAIR_BN=pair_bn)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
+                        "tests/test_gpu_moe.py::test_moe_block_matches_the_oracle"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
