@@ -1230,6 +1230,550 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention3(const __grid_con
   }
 }
 
+// ---------------------------------------------------------------------------
+// k_attention4: one 256-query tile of one q head per work item, on an SM pair
+// (a cluster of two CTAs whose MMAs are cta_group::2). CTA c of the pair holds
+// query rows [128c, 128c + 128) of the tile, keys [64c, 64c + 64) of every
+// 128-key K block and head dims [64c, 64c + 64) of every V^T block, so each K
+// and V^T block is loaded once for 256 queries. In the leader CTA one thread
+// issues S = Q K^T (M = 256, N = 128 keys, K = 128 dims) and another O += P V
+// (M = 256, N = 128 dims, K = 128 keys, P read from tensor memory): the tensor
+// core queues little more than the MMA it runs, so a lone issuer leaves it idle
+// while it waits and commits; with two, one thread's bookkeeping overlaps the
+// other's MMAs.
+// TMEM of each CTA: O at columns 0-127, S buffers at 128 and 256, P buffers
+// (bf16, two keys per column) at 384 and 448; block g uses S and P buffers
+// g % 2. S of block g + 2 is issued as soon as the softmax has loaded S of block
+// g, P of block g is written once P V of block g - 2 is done.
+// Warp roles in each CTA:
+//   warp 0     TMA: lane 0 the item's Q rows (two buffers, so the next item's
+//              Q lands while this one's last S are issued) and the K ring, lane 1
+//              the V^T ring (four stages each). Every copy completes on the
+//              leader CTA's barrier, which the leader arms with both CTAs' bytes;
+//   warp 1     TMEM allocation; in the leader, the S thread; in the other CTA,
+//              one thread forwarding each P hand-off to the leader (a
+//              cluster-scope arrive costs a few hundred cycles, which no softmax
+//              thread should wait for);
+//   warps 2-9  softmax: two threads per query row, warps w and w+4 taking keys
+//              (and output columns) [0, 64) and [64, 128) of the row's TMEM
+//              lane; the row maximum and, at the end of an item, the row sum are
+//              combined through shared memory. The reference maximum moves only
+//              when a block's maximum exceeds it by more than 8 (log2 units);
+//              then the row of O is rescaled in TMEM once the previous P V has
+//              landed. At the end of an item O / l is stored; the next item's
+//              first P V, which overwrites O, waits for the same threads' next
+//              P hand-off;
+//   warp 10    in the leader, the P V thread; in the other CTA, the forwarder of
+//              the "S loaded" hand-offs.
+// Every wait is bounded; on a timeout the CTA records it, stops issuing, gives
+// copies in flight time to land, frees TMEM and returns.
+// ---------------------------------------------------------------------------
+constexpr int kAttn4Threads = 352;  // producer, S issuer, 8 softmax warps, P V issuer
+constexpr int k4Stages = 4;
+constexpr uint32_t k4KVSub = 64u * 128u;     // one [64 rows x 64 bf16] swizzled k-tile (8 KB)
+constexpr uint32_t k4KVStage = 2 * k4KVSub;  // this CTA's half of a K block or of a V^T block
+constexpr uint32_t k4SmemQ = 0, k4SmemK = 2 * kTile, k4SmemV = k4SmemK + k4Stages * k4KVStage;
+constexpr uint32_t k4SmemBar = k4SmemV + k4Stages * k4KVStage;  // 192 KB
+constexpr uint32_t k4SmemRed = k4SmemBar + 384;                 // row exchange, [2 buffers][2 halves][128] f32
+constexpr size_t kAttn4Smem = k4SmemRed + 2 * 2 * 128 * 4 + 1024;
+constexpr uint32_t k4ColS = 128, k4ColP = 384;  // TMEM columns of S buffer 0 and P buffer 0 (O at 0)
+// barrier slots (8 bytes each) from k4SmemBar
+enum : int {
+  k4QFull = 0, k4QEmpty = 2, k4KFull = 4, k4KEmpty = 8, k4VFull = 12, k4VEmpty = 16,
+  k4SFull = 20, k4SFree = 22, k4PFull = 24, k4PvDone = 26, k4XBar = 30, k4DrainS = 34, k4DrainPv = 35,
+  k4NumBars = 36
+};
+static_assert(8 * k4NumBars + 8 <= 384, "barriers, TMEM slot and abort flag fit before the exchange");
+
+// D (TMEM) (+)= A * B^T on the SM pair, A read from tensor memory: each CTA's
+// 128 rows of A on its own TMEM lanes, K bf16 values two per 32-bit column; B
+// halves from both CTAs' shared memory at the same offset.
+__device__ __forceinline__ void mma_bf16_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One arrival on an mbarrier of another CTA of the cluster (shared::cluster
+// address), without release semantics: the caller has already waited for what
+// the arrival announces (tcgen05 loads or stores completed, then a CTA-scope
+// barrier acquired), so it carries no data of its own and skips the
+// cluster-wide release, which costs a thousand cycles on a busy SM.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Bounded wait for an mbarrier phase whose common case, a phase already
+// complete, costs one try_wait: the timed retry loop is out of line.
+__device__ __noinline__ bool mbar_wait_retry(uint32_t bar, uint32_t parity, long long budget_ns) {
+  return ptx::mbar_wait(bar, parity, budget_ns);
+}
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, long long budget_ns) {
+  if (__builtin_expect(ptx::mbar_try_wait(bar, parity), 1)) return true;
+  return mbar_wait_retry(bar, parity, budget_ns);
+}
+
+// A position in a CTA pair's sequence of work items and their key blocks.
+struct Attn4Cursor {
+  int ic;                // items started
+  int j, nb, qt;         // key block in the item, blocks of the item, 256-query tile
+  const AttnHead *hd;    // null past the last item
+};
+
+__global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t sQ = sbase + k4SmemQ, sK = sbase + k4SmemK, sV = sbase + k4SmemV;
+  uint8_t *bar_area = smem + k4SmemBar;
+  const uint32_t bar0 = ptx::smem_addr(bar_area);
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bar_area + 8 * k4NumBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bar_area + 8 * k4NumBars + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = static_cast<int>(blockIdx.x >> 1), nclusters = static_cast<int>(gridDim.x >> 1);
+  const int kv_blocks = (p.tokens + kTileK - 1) / kTileK;
+  const int tiles = (p.tokens + 255) / 256;
+  const int items = tiles * p.heads_total;
+  // The pair's r-th item, in snake order over the pairs (longest items first
+  // when causal); -1 past the last.
+  auto rank_of = [&](int r) {
+    const int pos = (r & 1) ? nclusters - 1 - cluster : cluster;
+    const int k = r * nclusters + pos;
+    return k < items ? k : -1;
+  };
+  auto load = [&](Attn4Cursor &c) {
+    const int it = rank_of(c.ic);
+    c.j = 0;
+    if (it < 0) {
+      c.hd = nullptr;
+      c.nb = c.qt = 0;
+      return;
+    }
+    const int r = it / p.heads_total;
+    c.qt = p.causal ? tiles - 1 - r : r;
+    c.nb = p.causal ? min(2 * c.qt + 2, kv_blocks) : kv_blocks;
+    c.hd = &p.heads[it % p.heads_total];
+  };
+  auto advance = [&](Attn4Cursor &c) {
+    if (++c.j == c.nb) {
+      ++c.ic;
+      load(c);
+    }
+  };
+  // A bounded single-thread wait; on a timeout the thread records it and gives up.
+  auto wait1 = [&](int b, uint32_t parity, int code) {
+    if (mbar_wait_fast(bar(b), parity, p.wait_ns)) return true;
+    if (!*abort_flag) record(p.status, code);
+    *abort_flag = 1;
+    return false;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(bar(k4QFull + i), 1);
+      ptx::mbar_init(bar(k4QEmpty + i), 1);
+      // S of block g done, and P V of block g - 2 done (so P buffer g % 2 is free)
+      ptx::mbar_init(bar(k4SFull + i), 2);
+      // this CTA's 8 softmax warps, and in the leader the other CTA's forwarded hand-off
+      ptx::mbar_init(bar(k4SFree + i), leader ? 9 : 8);
+      ptx::mbar_init(bar(k4PFull + i), leader ? 9 : 8);
+    }
+    for (int s = 0; s < k4Stages; ++s) {
+      ptx::mbar_init(bar(k4KFull + s), 1);
+      ptx::mbar_init(bar(k4KEmpty + s), 1);
+      ptx::mbar_init(bar(k4VFull + s), 1);
+      ptx::mbar_init(bar(k4VEmpty + s), 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      ptx::mbar_init(bar(k4PvDone + i), 1);
+      ptx::mbar_init(bar(k4XBar + i), 64);  // the two warps sharing a quarter of the rows
+    }
+    ptx::mbar_init(bar(k4DrainS), 1);
+    ptx::mbar_init(bar(k4DrainPv), 1);
+    // blocks 0 and 1 have no P V two blocks back
+    ptx::mbar_arrive(bar(k4SFull));
+    ptx::mbar_arrive(bar(k4SFull + 1));
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_addr(const_cast<uint32_t *>(tmem_slot)), kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, 128);
+
+  if (warp == 0) {
+    if (lane < 2) {
+      // lane 0: each item's Q rows, then the K ring; lane 1: the V^T ring
+      Attn4Cursor c{0, 0, 0, 0, nullptr};
+      load(c);
+      uint32_t st = 0, ph = 0;  // ring stage and phase of block g
+      for (int g = 0; c.hd; ++g, advance(c)) {
+        const AttnHead &hd = *c.hd;
+        if (lane == 0 && c.j == 0) {
+          // Q buffer ic % 2: the last S of the item that used it before has read it
+          const int qb = c.ic & 1;
+          if (*abort_flag || !wait1(k4QEmpty + qb, ((c.ic >> 1) & 1) ^ 1, kDevTimeoutProducer)) break;
+          if (leader) ptx::mbar_arrive_expect_tx(bar(k4QFull + qb), 2 * kTile);
+          const uint32_t lead_full = ptx::mapa_shared(bar(k4QFull + qb), 0);
+          for (int sub = 0; sub < 2; ++sub)
+            ptx::tma_load_2d_pair(sQ + static_cast<uint32_t>(qb) * kTile + sub * kSub, &p.maps[hd.q_map],
+                                  hd.q_col + 64 * sub, c.qt * 256 + 128 * static_cast<int>(rank), lead_full);
+        }
+        const int full = (lane == 0 ? k4KFull : k4VFull) + static_cast<int>(st);
+        const int empty = (lane == 0 ? k4KEmpty : k4VEmpty) + static_cast<int>(st);
+        if (*abort_flag || !wait1(empty, ph ^ 1, kDevTimeoutProducer)) break;
+        if (leader) ptx::mbar_arrive_expect_tx(bar(full), 2 * k4KVStage);
+        const uint32_t lead_full = ptx::mapa_shared(bar(full), 0);
+        const uint32_t dst = (lane == 0 ? sK : sV) + st * k4KVStage;
+        for (int sub = 0; sub < 2; ++sub) {
+          if (lane == 0)  // keys [64 rank, +64) of the block, head dims [64 sub, +64)
+            ptx::tma_load_2d_pair(dst + sub * k4KVSub, &p.maps[hd.k_map], hd.kv_col + 64 * sub,
+                                  c.j * kTileK + 64 * static_cast<int>(rank), lead_full);
+          else  // head dims [64 rank, +64) of V^T, keys [64 sub, +64) of the block
+            ptx::tma_load_2d_pair(dst + sub * k4KVSub, &p.maps[hd.v_map], c.j * kTileK + 64 * sub,
+                                  hd.kv_col + 64 * static_cast<int>(rank), lead_full);
+        }
+        if (++st == k4Stages) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  } else if ((warp == 1 || warp == 10) && lane == 0) {
+    if (leader && warp == 1) {
+      // ---- S thread: S(g) = Q K^T into S buffer g % 2 ----
+      const uint64_t q_desc = ptx::smem_desc_sw128(sQ), k_desc = ptx::smem_desc_sw128(sK);
+      Attn4Cursor c{0, 0, 0, 0, nullptr};
+      load(c);
+      uint32_t b = 0, bph = 0, st = 0, kph = 0;  // S buffer and phase, K stage and phase
+      bool ok = true;
+      for (; c.hd; advance(c)) {
+        const int qb = c.ic & 1;
+        // the softmax has loaded S of block g - 2 out of this buffer (both CTAs)
+        if (!wait1(k4SFree + static_cast<int>(b), bph ^ 1, kDevTimeoutMma) ||
+            (c.j == 0 && !wait1(k4QFull + qb, (c.ic >> 1) & 1, kDevTimeoutMma)) ||
+            !wait1(k4KFull + static_cast<int>(st), kph, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + k4ColS + 128u * b;
+        const uint64_t ad = q_desc + ((static_cast<uint32_t>(qb) * kTile) >> 4);
+        const uint64_t bd = k_desc + ((st * k4KVStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kHd / 16; ++kk)
+          ptx::mma_bf16_pair(d, ad + (((kk >> 2) * kSub) >> 4) + 2 * (kk & 3),
+                             bd + (((kk >> 2) * k4KVSub) >> 4) + 2 * (kk & 3), idesc, kk > 0 ? 1u : 0u);
+        ptx::mma_commit_pair_multicast(bar(k4SFull + static_cast<int>(b)), 0x3);
+        ptx::mma_commit_pair_multicast(bar(k4KEmpty + static_cast<int>(st)), 0x3);
+        if (c.j + 1 == c.nb) ptx::mma_commit_pair_multicast(bar(k4QEmpty + qb), 0x3);  // the item's last S
+        if (++b == 2) {
+          b = 0;
+          bph ^= 1;
+        }
+        if (++st == k4Stages) {
+          st = 0;
+          kph ^= 1;
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      ptx::mma_commit_pair_multicast(bar(k4DrainS), 0x1);
+      if (!ptx::mbar_wait(bar(k4DrainS), 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    } else if (leader) {
+      // ---- P V thread: O += P(g) V(g), P from P buffer g % 2 ----
+      const uint64_t v_desc = ptx::smem_desc_sw128(sV);
+      Attn4Cursor c{0, 0, 0, 0, nullptr};
+      load(c);
+      uint32_t b = 0, bph = 0, st = 0, vph = 0, n = 0;  // P buffer and phase, V stage and phase, P V issued
+      bool ok = true;
+      for (; c.hd; advance(c), ++n) {
+        // P(g) in both CTAs (their O rescaled where it had to be) and V^T of block g
+        if (!wait1(k4PFull + static_cast<int>(b), bph, kDevTimeoutMma) ||
+            !wait1(k4VFull + static_cast<int>(st), vph, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t a = tmem + k4ColP + 64u * b;
+        const uint64_t bd = v_desc + ((st * k4KVStage) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTileK / 16; ++kk)
+          mma_bf16_pair_ts(tmem, a + 8u * static_cast<uint32_t>(kk), bd + (((kk >> 2) * k4KVSub) >> 4) + 2 * (kk & 3),
+                           idesc, (c.j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit_pair_multicast(bar(k4PvDone + static_cast<int>(n & 3)), 0x3);
+        // the second arrival on the S barrier of block g + 2: P buffer g % 2 is free
+        ptx::mma_commit_pair_multicast(bar(k4SFull + static_cast<int>(b)), 0x3);
+        ptx::mma_commit_pair_multicast(bar(k4VEmpty + static_cast<int>(st)), 0x3);
+        if (++b == 2) {
+          b = 0;
+          bph ^= 1;
+        }
+        if (++st == k4Stages) {
+          st = 0;
+          vph ^= 1;
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      ptx::mma_commit_pair_multicast(bar(k4DrainPv), 0x1);
+      if (!ptx::mbar_wait(bar(k4DrainPv), 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
+    } else {
+      // ---- the other CTA: forward its hand-offs (warp 1: P written, warp 10: S
+      // loaded) to the leader's barriers, one cluster-scope arrive per block ----
+      const int base = warp == 1 ? k4PFull : k4SFree;
+      const uint32_t lead = ptx::mapa_shared(bar(base), 0);
+      Attn4Cursor c{0, 0, 0, 0, nullptr};
+      load(c);
+      uint32_t b = 0, ph = 0;
+      for (; c.hd; advance(c)) {
+        if (!wait1(base + static_cast<int>(b), ph, kDevTimeoutMma)) break;
+        mbar_arrive_remote_relaxed(lead + 8u * b);
+        if (++b == 2) {
+          b = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  } else if (warp >= 2 && warp <= 9) {
+    // ---- softmax: warps w and w+4 read TMEM lanes [32*(w%4), +32), a thread pair per row ----
+    const int qw = warp & 3;
+    const int half = (warp - 2) >> 2;  // 0: keys / output columns [0, 64), 1: [64, 128)
+    const int row = qw * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t ob = tmem + lane_off + 64u * static_cast<uint32_t>(half);
+    const uint32_t xbar = bar(k4XBar + qw);
+    volatile float *red = reinterpret_cast<volatile float *>(smem + k4SmemRed);
+    bool ok = true;
+    // A bounded warp-wide wait: lane 0 polls and the warp converges on its answer;
+    // on a timeout (or another role's abort) the warp gives up.
+    auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+      int go = 0;
+      if (lane == 0) {
+        const bool ready = mbar_wait_fast(b, parity, p.wait_ns);
+        if (!ready) record(p.status, kDevTimeoutEpilogue);
+        if (!ready || *abort_flag) *abort_flag = 1;
+        else go = 1;
+      }
+      return __shfl_sync(0xffffffffu, go, 0) != 0;
+    };
+    // P V of block gq has landed: O is current up to it (four barriers in turn,
+    // so a phase waited for is never two behind the barrier's current one)
+    auto wait_pv = [&](int gq) -> bool {
+      if (!wait_all(bar(k4PvDone + (gq & 3)), (gq >> 2) & 1)) return false;
+      ptx::tc_fence_after();
+      return true;
+    };
+    // The partner thread's value for this row. Exchange x uses buffer x % 2 and
+    // phase x of the pair's barrier: the value written for exchange x + 2 can
+    // only be written after the partner has passed exchange x + 1, so after it
+    // has read the value of exchange x.
+    uint32_t xc = 0;
+    auto exchange = [&](float x, float &y) -> bool {
+      const int buf = static_cast<int>(xc & 1);
+      red[(buf * 2 + half) * 128 + row] = x;
+      ptx::mbar_arrive(xbar);
+      if (!wait_all(xbar, xc & 1)) return false;
+      y = red[(buf * 2 + (half ^ 1)) * 128 + row];
+      ++xc;
+      return true;
+    };
+    Attn4Cursor c{0, 0, 0, 0, nullptr};
+    load(c);
+    int g = 0;  // key blocks over all items
+    uint32_t b = 0, bph = 0;  // S / P buffer of block g and the S phase
+    while (ok && c.hd) {
+      const AttnHead &hd = *c.hd;
+      const int qrow = c.qt * 256 + 128 * static_cast<int>(rank) + row;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < c.nb; ++j, ++g) {
+        if (!wait_all(bar(k4SFull + static_cast<int>(b)), bph)) { ok = false; break; }
+        ptx::tc_fence_after();
+        // this thread's 64 keys, then the partner's 64 (for the row maximum only)
+        const uint32_t srow = tmem + lane_off + k4ColS + 128u * b;
+        const uint32_t sb = srow + 64u * static_cast<uint32_t>(half), so = srow + 64u * static_cast<uint32_t>(half ^ 1);
+        uint32_t v[64], w[32];
+        {
+          uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+          uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+          ptx::tmem_ld_32cols(sb, v0);
+          ptx::tmem_ld_32cols(sb + 32u, v1);
+          ptx::tmem_ld_32cols(so, w);
+          ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(v);
+          ptx::tmem_regs_ready(w);
+        }
+        const int k0 = j * kTileK + 64 * half, k1 = j * kTileK + 64 * (half ^ 1);
+        // keys past the query (causal) or past the sequence are masked
+        const int lim = min(p.causal ? qrow - k0 + 1 : 64, p.tokens - k0);
+        const int lim_o = min(p.causal ? qrow - k1 + 1 : 64, p.tokens - k1);
+        const bool masked = !__all_sync(0xffffffffu, lim >= 64 && lim_o >= 64);  // a masked key in this warp's rows
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i >= lim) v[i] = __float_as_uint(-INFINITY);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i >= lim_o) w[i] = __float_as_uint(-INFINITY);
+        }
+        float mq[6];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mq[q] = __uint_as_float(v[16 * q + 15]);
+#pragma unroll
+          for (int i = 0; i < 14; i += 2)
+            mq[q] = max3f(mq[q], __uint_as_float(v[16 * q + i]), __uint_as_float(v[16 * q + i + 1]));
+          mq[q] = fmaxf(mq[q], __uint_as_float(v[16 * q + 14]));
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          mq[4 + q] = __uint_as_float(w[16 * q + 15]);
+#pragma unroll
+          for (int i = 0; i < 14; i += 2)
+            mq[4 + q] = max3f(mq[4 + q], __uint_as_float(w[16 * q + i]), __uint_as_float(w[16 * q + i + 1]));
+          mq[4 + q] = fmaxf(mq[4 + q], __uint_as_float(w[16 * q + 14]));
+        }
+        {
+          ptx::tmem_ld_32cols(so + 32u, w);
+          ptx::tmem_ld_wait();
+          ptx::tmem_regs_ready(w);
+          if (masked) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 + i >= lim_o) w[i] = __float_as_uint(-INFINITY);
+          }
+        }
+        // S of this block is in registers: the S buffer may take block g + 2
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(k4SFree + static_cast<int>(b)));
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 2)
+            mq[4 + q] = max3f(mq[4 + q], __uint_as_float(w[16 * q + i]), __uint_as_float(w[16 * q + i + 1]));
+        }
+        const float m_blk = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(mq[4], mq[5])) * p.scale_log2;
+        const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
+        const float m_new = move ? m_blk : m;
+        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
+        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
+        uint64_t sumh[2];
+        uint32_t pk[2][16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          sumh[h] = pack2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float y0, y1;
+            unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
+                    y1);
+            const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
+            sumh[h] = add2(sumh[h], pack2(a0, a1));
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
+            memcpy(&pk[h][i >> 1], &hb, 4);
+          }
+        }
+        float s0, s1;
+        unpack2(add2(sumh[0], sumh[1]), s0, s1);
+        l = l * alpha + (s0 + s1);
+        m = m_new;
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          // O must hold P V up to block j - 1 before it is rescaled (rows keeping
+          // their maximum scale by 1)
+          if (!wait_pv(g - 1)) { ok = false; break; }
+#pragma unroll 1
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            ptx::tmem_ld_32cols(ob + 32u * static_cast<uint32_t>(cc), o);
+            ptx::tmem_ld_wait();
+            ptx::tmem_regs_ready(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            ptx::tmem_st_32cols(ob + 32u * static_cast<uint32_t>(cc), o);
+          }
+        }
+        // P over keys [64 half, +64): columns [32 half, +32) of the P buffer
+        const uint32_t pb = tmem + lane_off + k4ColP + 64u * b + 32u * static_cast<uint32_t>(half);
+        ptx::tmem_st_16cols(pb, pk[0]);
+        ptx::tmem_st_16cols(pb + 16u, pk[1]);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(k4PFull + static_cast<int>(b)));
+        if (++b == 2) {
+          b = 0;
+          bph ^= 1;
+        }
+      }
+      if (!ok) break;
+      // the item's output: O / l once its last P V has landed
+      if (!wait_pv(g - 1)) { ok = false; break; }
+      float l_other;
+      if (!exchange(l, l_other)) { ok = false; break; }
+      const float inv = 1.f / (l + l_other);
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t o[32];
+        ptx::tmem_ld_32cols(ob + 32u * static_cast<uint32_t>(cc), o);
+        ptx::tmem_ld_wait();
+        ptx::tmem_regs_ready(o);
+        if (qrow < p.tokens) {
+          __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(hd.out) + static_cast<long long>(qrow) * hd.out_ld +
+                               64 * half + 32 * cc;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
+            memcpy(&w.x, &h0, 4);
+            memcpy(&w.y, &h1, 4);
+            memcpy(&w.z, &h2, 4);
+            memcpy(&w.w, &h3, 4);
+            *reinterpret_cast<uint4 *>(dst + i) = w;
+          }
+        }
+      }
+      // O has been read before this thread's next P hand-off, after which the
+      // next item's first P V overwrites it
+      ptx::tc_fence_before();
+      ++c.ic;
+      load(c);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // A wait ran out somewhere in the pair: give copies already in flight (into
+    // either CTA) time to land before the pair's shared memory goes away.
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 2000000ull) {
+    }
+  }
+  ptx::cluster_sync();  // neither CTA leaves while the other may still touch its smem or TMEM
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
 // V [T x C] (row pitch ld_in) -> V^T [C x T] (row pitch ld_out) for every kv
 // source in one launch (grid z = source), 64 x 64 tiles through shared memory.
 __global__ void __launch_bounds__(256) k_transpose_bf16(TransposeArgs a) {
@@ -1261,11 +1805,14 @@ tp_status launch_transpose_bf16(const TransposeArgs &a, int sources, cudaStream_
 
 int attention_variant() {
   const char *env = getenv("TPGQA_ATTN");
-  if (env && (env[0] == '1' || env[0] == '3') && env[1] == 0) return env[0] - '0';
+  if (env && (env[0] == '1' || env[0] == '3' || env[0] == '4') && env[1] == 0) return env[0] - '0';
   return 2;
 }
 
-int attention_k_box_rows(int variant) { return variant == 3 ? kKb : kTileK; }
+int attention_k_box_rows(int variant) { return variant == 3 || variant == 4 ? kKb : kTileK; }
+
+// Rows of the V^T boxes: the SM-pair kernel loads half of the head dims per CTA.
+int attention_v_box_rows(int variant) { return variant == 4 ? 64 : kTileK; }
 
 tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
   DevCtx ctx;
@@ -1289,11 +1836,40 @@ tp_status launch_attention(AttnParams &p, int total_heads, cudaStream_t s) {
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attention3, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kAttn3Smem));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attention4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kAttn4Smem));
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 64) configured |= 1ULL << dev;
     }
   }
   p.heads_total = total_heads;
+  if (p.variant == 4) {
+    // one pair per 256-query item, at most as many pairs as are resident at once
+    static int resident[64] = {};
+    std::lock_guard<std::mutex> g(mu);
+    int pairs = dev < 64 ? resident[dev] : 0;
+    if (pairs <= 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(kAttn4Threads);
+      cfg.dynamicSmemBytes = kAttn4Smem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&pairs, k_attention4, &cfg) != cudaSuccess || pairs <= 0)
+        pairs = num_sms() / 2;
+      cudaGetLastError();  // a failed query leaves no sticky error behind
+      if (dev < 64) resident[dev] = pairs;
+    }
+    const long long items = static_cast<long long>((p.tokens + 255) / 256) * total_heads;
+    const dim3 grid(static_cast<unsigned>(2 * (items < pairs ? items : pairs)));
+    return launch_checked(launch_kernel(k_attention4, grid, dim3(kAttn4Threads), kAttn4Smem, s, 2, p));
+  }
   if (p.variant == 1) {
     const long long items = static_cast<long long>(p.q_tiles) * total_heads;
     const dim3 grid(static_cast<unsigned>(items < num_sms() ? items : num_sms()));

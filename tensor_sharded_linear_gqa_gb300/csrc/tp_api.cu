@@ -15,6 +15,8 @@ namespace tpgqa {
 // moe.cu: whether moe_forward folds the one-pass ring (RING_FUSED or RING_SHARED)
 // into the MoE block's weighted combine, leaving no all-reduce to the caller.
 bool moe_ring_folded(int32_t combine, int n);
+// attention.cu: rows of the V^T boxes the attention kernel of this variant loads.
+int attention_v_box_rows(int variant);
 namespace {
 
 __device__ int g_dev_status = 0;
@@ -912,7 +914,8 @@ extern "C" tp_status tp_attn_core(const tp_plan *plan, const tp_tensor *q, const
     if (!encode_bf16_map_2d(&prm.maps[r], q[r].ptr, T, q[r].cols, q[r].ld, 128)) return TP_ERR_INVALID_ARG;
   for (int32_t r = 0; r < nkv; ++r) {
     if (!encode_bf16_map_2d(&prm.maps[n + r], k[r].ptr, T, kvc, k[r].ld, k_box)) return TP_ERR_INVALID_ARG;
-    if (!encode_bf16_map_2d(&prm.maps[n + nkv + r], static_cast<char *>(workspace) + r * vt, kvc, T, tp8, 128))
+    if (!encode_bf16_map_2d(&prm.maps[n + nkv + r], static_cast<char *>(workspace) + r * vt, kvc, T, tp8,
+                            attention_v_box_rows(prm.variant)))
       return TP_ERR_INVALID_ARG;
   }
   int h = 0;

@@ -181,12 +181,13 @@ def test_projection_attention_o_proj_chain(tp_size, hq, hkv):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("kernel", ["1", "2", "3"])
+@pytest.mark.parametrize("kernel", ["1", "2", "3", "4"])
 def test_every_attention_kernel_matches_the_oracle(kernel, causal, monkeypatch):
-    """The three attention kernels (TPGQA_ATTN=1: one 128-query tile per work item;
+    """The four attention kernels (TPGQA_ATTN=1: one 128-query tile per work item;
     2, the default: two tiles over 128-key blocks; 3: two tiles over 64-key
-    blocks), each against the oracle, on a ragged sharded case and on peaked
-    scores whose row maxima move block after block."""
+    blocks; 4: a 256-query tile on an SM pair), each against the oracle, on a
+    ragged sharded case and on peaked scores whose row maxima move block after
+    block."""
     need_gpu()
     monkeypatch.setenv("TPGQA_ATTN", kernel)
     for m in (Attn(2, 8, 2, 300, seed=620), Attn(2, 4, 2, 700, seed=621, scale=4.0, key_ramp=3.0)):
