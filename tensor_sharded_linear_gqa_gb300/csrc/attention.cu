@@ -1243,45 +1243,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention3(const __grid_con
 // other's MMAs.
 // TMEM of each CTA: O at columns 0-127, S buffers at 128 and 256, P buffers
 // (bf16, two keys per column) at 384 and 448; block g uses S and P buffers
-// g % 2. S of block g + 2 is issued as soon as the softmax has loaded S of block
-// g, P of block g is written once P V of block g - 2 is done.
+// g % 2. S of block g + 2 is issued as soon as the softmax of both CTAs has
+// loaded S of block g; the S barrier of block g takes two arrivals, S of block g
+// done and P V of block g - 2 done (so P buffer g % 2 is free again).
 // Warp roles in each CTA:
 //   warp 0     TMA: lane 0 the item's Q rows (two buffers, so the next item's
 //              Q lands while this one's last S are issued) and the K ring, lane 1
 //              the V^T ring (four stages each). Every copy completes on the
 //              leader CTA's barrier, which the leader arms with both CTAs' bytes;
-//   warp 1     TMEM allocation; in the leader, the S thread; in the other CTA,
-//              one thread forwarding each P hand-off to the leader (a
-//              cluster-scope arrive costs a few hundred cycles, which no softmax
-//              thread should wait for);
-//   warps 2-9  softmax: two threads per query row, warps w and w+4 taking keys
-//              (and output columns) [0, 64) and [64, 128) of the row's TMEM
-//              lane; the row maximum and, at the end of an item, the row sum are
-//              combined through shared memory. The reference maximum moves only
-//              when a block's maximum exceeds it by more than 8 (log2 units);
-//              then the row of O is rescaled in TMEM once the previous P V has
-//              landed. At the end of an item O / l is stored; the next item's
-//              first P V, which overwrites O, waits for the same threads' next
-//              P hand-off;
-//   warp 10    in the leader, the P V thread; in the other CTA, the forwarder of
-//              the "S loaded" hand-offs.
+//   warp 1     TMEM allocation; in the leader, the S thread;
+//   warps 2-5  softmax: one thread per query row (its TMEM lane) over all 128
+//              keys of a block. The hand-offs ("S loaded", "P written") of both
+//              CTAs arrive on the leader's barriers with relaxed cluster-scope
+//              arrives: each follows the thread's own wait for its tcgen05 loads
+//              or stores, and the release form costs a thousand cycles on a busy
+//              SM. The reference maximum moves only when a block's maximum
+//              exceeds it by more than 8 (log2 units); then the row of O is
+//              rescaled in TMEM once the previous P V has landed. At the end of
+//              an item O / l is stored; the next item's first P V, which
+//              overwrites O, waits for the same threads' next P hand-off;
+//   warp 6     in the leader, the P V thread.
 // Every wait is bounded; on a timeout the CTA records it, stops issuing, gives
 // copies in flight time to land, frees TMEM and returns.
 // ---------------------------------------------------------------------------
-constexpr int kAttn4Threads = 352;  // producer, S issuer, 8 softmax warps, P V issuer
+constexpr int kAttn4Threads = 224;  // producer, S issuer, 4 softmax warps, P V issuer
 constexpr int k4Stages = 4;
 constexpr uint32_t k4KVSub = 64u * 128u;     // one [64 rows x 64 bf16] swizzled k-tile (8 KB)
 constexpr uint32_t k4KVStage = 2 * k4KVSub;  // this CTA's half of a K block or of a V^T block
 constexpr uint32_t k4SmemQ = 0, k4SmemK = 2 * kTile, k4SmemV = k4SmemK + k4Stages * k4KVStage;
 constexpr uint32_t k4SmemBar = k4SmemV + k4Stages * k4KVStage;  // 192 KB
-constexpr uint32_t k4SmemRed = k4SmemBar + 384;                 // row exchange, [2 buffers][2 halves][128] f32
-constexpr size_t kAttn4Smem = k4SmemRed + 2 * 2 * 128 * 4 + 1024;
+constexpr size_t kAttn4Smem = k4SmemBar + 384 + 1024;            // + barriers + alignment slack
 constexpr uint32_t k4ColS = 128, k4ColP = 384;  // TMEM columns of S buffer 0 and P buffer 0 (O at 0)
 // barrier slots (8 bytes each) from k4SmemBar
 enum : int {
   k4QFull = 0, k4QEmpty = 2, k4KFull = 4, k4KEmpty = 8, k4VFull = 12, k4VEmpty = 16,
-  k4SFull = 20, k4SFree = 22, k4PFull = 24, k4PvDone = 26, k4XBar = 30, k4DrainS = 34, k4DrainPv = 35,
-  k4NumBars = 36
+  k4SFull = 20, k4SFree = 22, k4PFull = 24, k4PvDone = 26, k4DrainS = 30, k4DrainPv = 31, k4NumBars = 32
 };
 static_assert(8 * k4NumBars + 8 <= 384, "barriers, TMEM slot and abort flag fit before the exchange");
 
@@ -1315,6 +1311,36 @@ __device__ __noinline__ bool mbar_wait_retry(uint32_t bar, uint32_t parity, long
 __device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity, long long budget_ns) {
   if (__builtin_expect(ptx::mbar_try_wait(bar, parity), 1)) return true;
   return mbar_wait_retry(bar, parity, budget_ns);
+}
+
+// Non-blocking test of an mbarrier phase (mbarrier.test_wait: never suspends
+// the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait that polls with test_wait, for the threads whose reaction time
+// is on the critical path (a suspended try_wait took about 500 cycles to see a
+// phase complete); the clock is read every 64 polls.
+__device__ __noinline__ bool mbar_spin_retry(uint32_t bar, uint32_t parity, long long budget_ns) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (static_cast<long long>(ptx::globaltimer_ns() - t0) > budget_ns) return false;
+  }
+}
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, long long budget_ns) {
+  if (__builtin_expect(mbar_test_wait(bar, parity), 1)) return true;
+  return mbar_spin_retry(bar, parity, budget_ns);
 }
 
 // A position in a CTA pair's sequence of work items and their key blocks.
@@ -1383,9 +1409,9 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
       ptx::mbar_init(bar(k4QEmpty + i), 1);
       // S of block g done, and P V of block g - 2 done (so P buffer g % 2 is free)
       ptx::mbar_init(bar(k4SFull + i), 2);
-      // this CTA's 8 softmax warps, and in the leader the other CTA's forwarded hand-off
-      ptx::mbar_init(bar(k4SFree + i), leader ? 9 : 8);
-      ptx::mbar_init(bar(k4PFull + i), leader ? 9 : 8);
+      // the 4 softmax warps of both CTAs (used in the leader only)
+      ptx::mbar_init(bar(k4SFree + i), 8);
+      ptx::mbar_init(bar(k4PFull + i), 8);
     }
     for (int s = 0; s < k4Stages; ++s) {
       ptx::mbar_init(bar(k4KFull + s), 1);
@@ -1395,7 +1421,6 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
     }
     for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(bar(k4PvDone + i), 1);
-      ptx::mbar_init(bar(k4XBar + i), 64);  // the two warps sharing a quarter of the rows
     }
     ptx::mbar_init(bar(k4DrainS), 1);
     ptx::mbar_init(bar(k4DrainPv), 1);
@@ -1455,7 +1480,7 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
         }
       }
     }
-  } else if ((warp == 1 || warp == 10) && lane == 0) {
+  } else if ((warp == 1 || warp == 6) && lane == 0) {
     if (leader && warp == 1) {
       // ---- S thread: S(g) = Q K^T into S buffer g % 2 ----
       const uint64_t q_desc = ptx::smem_desc_sw128(sQ), k_desc = ptx::smem_desc_sw128(sK);
@@ -1532,39 +1557,22 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
       if (!ok) *abort_flag = 1;
       ptx::mma_commit_pair_multicast(bar(k4DrainPv), 0x1);
       if (!ptx::mbar_wait(bar(k4DrainPv), 0, p.wait_ns)) record(p.status, kDevTimeoutDrain);
-    } else {
-      // ---- the other CTA: forward its hand-offs (warp 1: P written, warp 10: S
-      // loaded) to the leader's barriers, one cluster-scope arrive per block ----
-      const int base = warp == 1 ? k4PFull : k4SFree;
-      const uint32_t lead = ptx::mapa_shared(bar(base), 0);
-      Attn4Cursor c{0, 0, 0, 0, nullptr};
-      load(c);
-      uint32_t b = 0, ph = 0;
-      for (; c.hd; advance(c)) {
-        if (!wait1(base + static_cast<int>(b), ph, kDevTimeoutMma)) break;
-        mbar_arrive_remote_relaxed(lead + 8u * b);
-        if (++b == 2) {
-          b = 0;
-          ph ^= 1;
-        }
-      }
     }
-  } else if (warp >= 2 && warp <= 9) {
-    // ---- softmax: warps w and w+4 read TMEM lanes [32*(w%4), +32), a thread pair per row ----
+  } else if (warp >= 2 && warp <= 5) {
+    // ---- softmax: warp w reads TMEM lanes [32*(w%4), +32), one thread per query row ----
     const int qw = warp & 3;
-    const int half = (warp - 2) >> 2;  // 0: keys / output columns [0, 64), 1: [64, 128)
     const int row = qw * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    const uint32_t ob = tmem + lane_off + 64u * static_cast<uint32_t>(half);
-    const uint32_t xbar = bar(k4XBar + qw);
-    volatile float *red = reinterpret_cast<volatile float *>(smem + k4SmemRed);
+    const uint32_t ob = tmem + lane_off;
+    // hand-offs go to the leader CTA's barriers (the MMA threads live there)
+    const uint32_t lead_sfree = ptx::mapa_shared(bar(k4SFree), 0), lead_pfull = ptx::mapa_shared(bar(k4PFull), 0);
     bool ok = true;
     // A bounded warp-wide wait: lane 0 polls and the warp converges on its answer;
     // on a timeout (or another role's abort) the warp gives up.
-    auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+    auto wait_all = [&](uint32_t bb, uint32_t parity) -> bool {
       int go = 0;
       if (lane == 0) {
-        const bool ready = mbar_wait_fast(b, parity, p.wait_ns);
+        const bool ready = mbar_spin(bb, parity, p.wait_ns);
         if (!ready) record(p.status, kDevTimeoutEpilogue);
         if (!ready || *abort_flag) *abort_flag = 1;
         else go = 1;
@@ -1578,118 +1586,77 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
       ptx::tc_fence_after();
       return true;
     };
-    // The partner thread's value for this row. Exchange x uses buffer x % 2 and
-    // phase x of the pair's barrier: the value written for exchange x + 2 can
-    // only be written after the partner has passed exchange x + 1, so after it
-    // has read the value of exchange x.
-    uint32_t xc = 0;
-    auto exchange = [&](float x, float &y) -> bool {
-      const int buf = static_cast<int>(xc & 1);
-      red[(buf * 2 + half) * 128 + row] = x;
-      ptx::mbar_arrive(xbar);
-      if (!wait_all(xbar, xc & 1)) return false;
-      y = red[(buf * 2 + (half ^ 1)) * 128 + row];
-      ++xc;
-      return true;
-    };
     Attn4Cursor c{0, 0, 0, 0, nullptr};
     load(c);
-    int g = 0;  // key blocks over all items
+    int g = 0;                // key blocks over all items
     uint32_t b = 0, bph = 0;  // S / P buffer of block g and the S phase
     while (ok && c.hd) {
       const AttnHead &hd = *c.hd;
       const int qrow = c.qt * 256 + 128 * static_cast<int>(rank) + row;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < c.nb; ++j, ++g) {
+        // S of block g, and P V of block g - 2 done (P buffer b free)
         if (!wait_all(bar(k4SFull + static_cast<int>(b)), bph)) { ok = false; break; }
         ptx::tc_fence_after();
-        // this thread's 64 keys, then the partner's 64 (for the row maximum only)
-        const uint32_t srow = tmem + lane_off + k4ColS + 128u * b;
-        const uint32_t sb = srow + 64u * static_cast<uint32_t>(half), so = srow + 64u * static_cast<uint32_t>(half ^ 1);
-        uint32_t v[64], w[32];
-        {
-          uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-          uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-          ptx::tmem_ld_32cols(sb, v0);
-          ptx::tmem_ld_32cols(sb + 32u, v1);
-          ptx::tmem_ld_32cols(so, w);
-          ptx::tmem_ld_wait();
-          ptx::tmem_regs_ready(v);
-          ptx::tmem_regs_ready(w);
-        }
-        const int k0 = j * kTileK + 64 * half, k1 = j * kTileK + 64 * (half ^ 1);
-        // keys past the query (causal) or past the sequence are masked
-        const int lim = min(p.causal ? qrow - k0 + 1 : 64, p.tokens - k0);
-        const int lim_o = min(p.causal ? qrow - k1 + 1 : 64, p.tokens - k1);
-        const bool masked = !__all_sync(0xffffffffu, lim >= 64 && lim_o >= 64);  // a masked key in this warp's rows
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i >= lim) v[i] = __float_as_uint(-INFINITY);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i >= lim_o) w[i] = __float_as_uint(-INFINITY);
-        }
-        float mq[6];
+        const uint32_t sb = tmem + lane_off + k4ColS + 128u * b;
+        uint32_t v[128];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          mq[q] = __uint_as_float(v[16 * q + 15]);
-#pragma unroll
-          for (int i = 0; i < 14; i += 2)
-            mq[q] = max3f(mq[q], __uint_as_float(v[16 * q + i]), __uint_as_float(v[16 * q + i + 1]));
-          mq[q] = fmaxf(mq[q], __uint_as_float(v[16 * q + 14]));
+          uint32_t (&vq)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32 * q]);
+          ptx::tmem_ld_32cols(sb + 32u * static_cast<uint32_t>(q), vq);
         }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          mq[4 + q] = __uint_as_float(w[16 * q + 15]);
-#pragma unroll
-          for (int i = 0; i < 14; i += 2)
-            mq[4 + q] = max3f(mq[4 + q], __uint_as_float(w[16 * q + i]), __uint_as_float(w[16 * q + i + 1]));
-          mq[4 + q] = fmaxf(mq[4 + q], __uint_as_float(w[16 * q + 14]));
-        }
-        {
-          ptx::tmem_ld_32cols(so + 32u, w);
-          ptx::tmem_ld_wait();
-          ptx::tmem_regs_ready(w);
-          if (masked) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 + i >= lim_o) w[i] = __float_as_uint(-INFINITY);
-          }
-        }
+        ptx::tmem_ld_wait();
+        ptx::tmem_regs_ready(v);
         // S of this block is in registers: the S buffer may take block g + 2
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(k4SFree + static_cast<int>(b)));
+        if (lane == 0) mbar_arrive_remote_relaxed(lead_sfree + 8u * b);
+        const int k0 = j * kTileK;
+        // keys past the query (causal) or past the sequence are masked
+        const int lim = min(p.causal ? qrow - k0 + 1 : kTileK, p.tokens - k0);
+        if (!__all_sync(0xffffffffu, lim >= kTileK)) {  // a masked key in this warp's rows
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 2)
-            mq[4 + q] = max3f(mq[4 + q], __uint_as_float(w[16 * q + i]), __uint_as_float(w[16 * q + i + 1]));
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) v[i] = __float_as_uint(-INFINITY);
         }
-        const float m_blk = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(mq[4], mq[5])) * p.scale_log2;
+        // the row maximum as four independent chains over the key quarters
+        float mq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mq[q] = __uint_as_float(v[32 * q + 31]);
+#pragma unroll
+          for (int i = 0; i < 30; i += 2)
+            mq[q] = max3f(mq[q], __uint_as_float(v[32 * q + i]), __uint_as_float(v[32 * q + i + 1]));
+          mq[q] = fmaxf(mq[q], __uint_as_float(v[32 * q + 30]));
+        }
+        const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
         const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
         const float m_new = move ? m_blk : m;
         const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
+        // p = 2^(s*c - m), two keys at a time, packed as bf16 pairs into P buffer b,
+        // 16 columns (32 keys) at a time
         const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
-        uint64_t sumh[2];
-        uint32_t pk[2][16];
+        const uint32_t pb = tmem + lane_off + k4ColP + 64u * b;
+        uint64_t sumh[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          sumh[h] = pack2(0.f, 0.f);
+        for (int h = 0; h < 4; ++h) {
+          uint64_t &sum2 = sumh[h];
+          sum2 = pack2(0.f, 0.f);
+          uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             float y0, y1;
             unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
                     y1);
             const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
-            sumh[h] = add2(sumh[h], pack2(a0, a1));
+            sum2 = add2(sum2, pack2(a0, a1));
             const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
-            memcpy(&pk[h][i >> 1], &hb, 4);
+            memcpy(&pk[i >> 1], &hb, 4);
           }
+          ptx::tmem_st_16cols(pb + 16u * static_cast<uint32_t>(h), pk);
         }
         float s0, s1;
-        unpack2(add2(sumh[0], sumh[1]), s0, s1);
+        unpack2(add2(add2(sumh[0], sumh[1]), add2(sumh[2], sumh[3])), s0, s1);
         l = l * alpha + (s0 + s1);
         m = m_new;
         if (j > 0 && __any_sync(0xffffffffu, move)) {
@@ -1697,7 +1664,7 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
           // their maximum scale by 1)
           if (!wait_pv(g - 1)) { ok = false; break; }
 #pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
+          for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
             ptx::tmem_ld_32cols(ob + 32u * static_cast<uint32_t>(cc), o);
             ptx::tmem_ld_wait();
@@ -1707,14 +1674,10 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
             ptx::tmem_st_32cols(ob + 32u * static_cast<uint32_t>(cc), o);
           }
         }
-        // P over keys [64 half, +64): columns [32 half, +32) of the P buffer
-        const uint32_t pb = tmem + lane_off + k4ColP + 64u * b + 32u * static_cast<uint32_t>(half);
-        ptx::tmem_st_16cols(pb, pk[0]);
-        ptx::tmem_st_16cols(pb + 16u, pk[1]);
-        ptx::tmem_st_wait();
+        ptx::tmem_st_wait();  // P (and a rescaled O) in tensor memory before the hand-off
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(k4PFull + static_cast<int>(b)));
+        if (lane == 0) mbar_arrive_remote_relaxed(lead_pfull + 8u * b);
         if (++b == 2) {
           b = 0;
           bph ^= 1;
@@ -1723,18 +1686,16 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
       if (!ok) break;
       // the item's output: O / l once its last P V has landed
       if (!wait_pv(g - 1)) { ok = false; break; }
-      float l_other;
-      if (!exchange(l, l_other)) { ok = false; break; }
-      const float inv = 1.f / (l + l_other);
+      const float inv = 1.f / l;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t o[32];
         ptx::tmem_ld_32cols(ob + 32u * static_cast<uint32_t>(cc), o);
         ptx::tmem_ld_wait();
         ptx::tmem_regs_ready(o);
         if (qrow < p.tokens) {
-          __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(hd.out) + static_cast<long long>(qrow) * hd.out_ld +
-                               64 * half + 32 * cc;
+          __nv_bfloat16 *dst =
+              static_cast<__nv_bfloat16 *>(hd.out) + static_cast<long long>(qrow) * hd.out_ld + 32 * cc;
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
