@@ -149,6 +149,22 @@ __device__ __forceinline__ int find_problem(const GemmParams &p, int tile) {
   return lo;
 }
 
+// (m-tile, n-tile) of a problem's tile `local`: m fastest over the problem, or
+// over groups of m_group m-tiles (the last group may be shorter).
+__device__ __forceinline__ void tile_coords(const GemmProblem &pr, int local, int &mt, int &nt) {
+  const int g = pr.m_group;
+  if (g <= 0 || g >= pr.m_tiles) {
+    mt = local % pr.m_tiles;
+    nt = local / pr.m_tiles;
+    return;
+  }
+  const int per_group = g * pr.n_tiles;
+  const int grp = local / per_group, r = local - grp * per_group;
+  const int rows = min(g, pr.m_tiles - grp * g);
+  mt = grp * g + r % rows;
+  nt = r / rows;
+}
+
 // First tile at or after `tile`, stepping by `stride`, that its problem's block
 // table does not skip (every tile when there is no table). The producer, the
 // MMA issuer and the epilogue all step with it, so they see the same tiles.
@@ -156,7 +172,9 @@ __device__ __forceinline__ int live_tile(const GemmParams &p, int tile, int stri
   for (; tile < p.total_tiles; tile += stride) {
     const GemmProblem &pr = p.prob[find_problem(p, tile)];
     if (!pr.blk) break;
-    const int v = __ldg(pr.blk + (tile - pr.tile_begin) % pr.m_tiles);
+    int mt, nt;
+    tile_coords(pr, tile - pr.tile_begin, mt, nt);
+    const int v = __ldg(pr.blk + mt);
     if (v >= 0 && (v >> 16) < pr.n_moff) break;
   }
   return tile;
@@ -176,9 +194,7 @@ __device__ __forceinline__ void cursor_tile(const GemmParams &p, Cursor &c, int 
   if (!c.valid) return;
   c.prob = find_problem(p, tile);
   const GemmProblem &pr = p.prob[c.prob];
-  const int local = tile - pr.tile_begin;
-  c.mt = local % pr.m_tiles;
-  c.nt = local / pr.m_tiles;
+  tile_coords(pr, tile - pr.tile_begin, c.mt, c.nt);
   tile_b_origin(pr, c.mt, c.moff, c.brow);
   c.seg = 0;
   c.kt = 0;
@@ -394,9 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
         break;
       }
       const GemmProblem &pr = p.prob[find_problem(p, tile)];
-      const int local = tile - pr.tile_begin;
-      const int mt = local % pr.m_tiles;
-      const int nt = local / pr.m_tiles;
+      int mt, nt;
+      tile_coords(pr, tile - pr.tile_begin, mt, nt);
       const int row = mt * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(a) * kAccStride +
                              (static_cast<uint32_t>(q * 32) << 16);
@@ -609,7 +624,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int pre = 0;
   if (warp == 0 && lane == 0 && p.early_b && pair < p.total_tiles) {
     const GemmProblem &pr = p.prob[find_problem(p, pair)];
-    const int nt = (pair - pr.tile_begin) / pr.m_tiles;
+    int mt0, nt;
+    tile_coords(pr, pair - pr.tile_begin, mt0, nt);
     for (int sgi = 0; sgi < pr.seg_count && pre < S; ++sgi) {
       const GemmSeg &sg = p.seg[pr.seg_begin + sgi];
       const bool two_b = EPI == kEpiSwiGLU || sg.b2_map >= 0;
@@ -646,8 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!c.valid) return;
         c.prob = find_problem(p, t);
         const GemmProblem &pr = p.prob[c.prob];
-        c.mt = (t - pr.tile_begin) % pr.m_tiles;
-        c.nt = (t - pr.tile_begin) / pr.m_tiles;
+        tile_coords(pr, t - pr.tile_begin, c.mt, c.nt);
         tile_b_origin(pr, c.mt, c.moff, c.brow);
         c.seg = c.kt = c.kt_in_tile = 0;
       };
@@ -664,8 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!c.valid) return;
         c.prob = find_problem(p, t);
         const GemmProblem &q = p.prob[c.prob];
-        c.mt = (t - q.tile_begin) % q.m_tiles;
-        c.nt = (t - q.tile_begin) / q.m_tiles;
+        tile_coords(q, t - q.tile_begin, c.mt, c.nt);
         tile_b_origin(q, c.mt, c.moff, c.brow);
         c.seg = c.kt = c.kt_in_tile = 0;
       };
@@ -814,9 +828,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       const GemmProblem &pr = p.prob[find_problem(p, tile)];
-      const int local = tile - pr.tile_begin;
-      const int mt = local % pr.m_tiles;
-      const int nt = local / pr.m_tiles;
+      int mt, nt;
+      tile_coords(pr, tile - pr.tile_begin, mt, nt);
       const int row = mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * 256) +
                              (static_cast<uint32_t>(q * 32) << 16);
@@ -1005,7 +1018,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // tile's first stages start before the grid-dependency wait.
   int pre = 0;
   if (warp == 0 && lane == 0 && p.early_b && pair < p.total_tiles) {
-    const int mt = pair % pr.m_tiles, nt = pair / pr.m_tiles;
+    int mt, nt;
+    tile_coords(pr, pair, mt, nt);
     const int b_row = nt * BN + static_cast<int>(crank) * kHalfB;
     for (int s = 0; s < nrank && pre < S; ++s) {
       const GemmSeg &sg = p.seg[pr.seg_begin + fold_rank(mt, s)];
@@ -1031,7 +1045,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int kb = 0;
       bool go = true;
       for (int t = pair; go && t < p.total_tiles; t += npairs) {
-        const int mt = t % pr.m_tiles, nt = t / pr.m_tiles;
+        int mt, nt;
+        tile_coords(pr, t, mt, nt);
         const int a_row = mt * 256 + static_cast<int>(crank) * 128;
         const int b_row = nt * BN + static_cast<int>(crank) * kHalfB;
         for (int s = 0; go && s < nrank; ++s) {
@@ -1078,7 +1093,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t taken0 = 0, taken1 = 0;  // acquisitions of each TMEM region so far
       bool ok = true;
       for (int t = pair, jt = 0; ok && t < p.total_tiles; t += npairs, ++jt) {
-        const int mt = t % pr.m_tiles;
+        int mt, nt;
+        tile_coords(pr, t, mt, nt);
         for (int s = 0; ok && s < nrank; ++s) {
           const int reg = s == 0 ? (jt & 1) : ((jt & 1) ^ 1);
           uint32_t &taken = reg ? taken1 : taken0;
@@ -1142,7 +1158,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       return alive;
     };
     for (int t = pair, jt = 0; alive && t < p.total_tiles; t += npairs, ++jt) {
-      const int mt = t % pr.m_tiles, nt = t / pr.m_tiles;
+      int mt, nt;
+      tile_coords(pr, t, mt, nt);
       const int rs = jt & 1, ra = rs ^ 1;
       const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
       const uint32_t tsum = tmem_base + static_cast<uint32_t>(rs * 256) + lane_off;
@@ -1337,9 +1354,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
 
   const int pi = find_problem(p, tile);
   const GemmProblem &pr = p.prob[pi];
-  const int local = tile - pr.tile_begin;
-  const int mt = local % pr.m_tiles;
-  const int nt = local / pr.m_tiles;
+  int mt, nt;
+  tile_coords(pr, tile - pr.tile_begin, mt, nt);
   // Ring folding (ring_rows > 0): split s is segment (rank) s, whole. Otherwise
   // the problem's stages are cut into nsplit near-equal ranges.
   const bool ring = p.ring_rows > 0;
@@ -2081,6 +2097,7 @@ bool GemmBuilder::add_problem(int m, int n, void *out, long long ldc, const int 
   pr.blk = blk;
   pr.b_rows_per_blk = b_rows_per_blk;
   pr.n_moff = n_moff;
+  pr.m_group = m_group;
   if (blk) split = 1;  // block tables run on the persistent kernels only
   for (int s = 0; s < nseg; ++s) {
     GemmSeg &sg = p.seg[n_segs + s];

@@ -28,6 +28,7 @@
 //     kernel folds the ranks' partials in the ring's order instead (mlxcel
 //     manual "텐서 병렬화", 통신 패턴: chunk c of the flat output reduced as
 //     x_{c+1} + ... + x_c), so the partials are never written.
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <vector>
@@ -375,9 +376,15 @@ tp_status moe_forward(const MoeCall &c, cudaStream_t s) {
   // ---- gate/up with SwiGLU: H rows of the routed layout ----
   const long long Fs = within ? F / n : F;  // columns of H per problem
   const int nprob = within ? n : 1;
+  // Tiles in groups of about one expert's m-tiles, each group n-tile by n-tile:
+  // with the m-tile fastest over all routed rows, every wave of tiles read all
+  // of them and a slice of every expert's weights, about 3.6 times the operand
+  // bytes from DRAM on the Mixtral shape.
+  const int m_group = static_cast<int>(std::max<long long>(1, (T * k / E + L.bm - 1) / L.bm));
   {
     GemmBuilder b;
     b.epi = kEpiSwiGLU;
+    b.m_group = m_group;
     b.pair = L.pair;
     std::vector<long long> nc(nprob, Fs);
     int b_rows = 0;
@@ -419,6 +426,7 @@ tp_status moe_forward(const MoeCall &c, cudaStream_t s) {
   {
     GemmBuilder b;
     b.epi = kEpiF32;
+    b.m_group = m_group;
     b.pair = L.pair;
     const int dprob = within && !fused ? n : 1;
     std::vector<long long> nc(dprob, D);

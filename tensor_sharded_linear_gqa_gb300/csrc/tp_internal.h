@@ -114,7 +114,9 @@ struct GemmProblem {
   int b_rows_per_blk;    // with a block table: B rows per block slot
   int n_moff;            // with a block table: B maps per segment (entries whose
                          // map offset is not below it are skipped like -1)
-  int pad;
+  int m_group;           // tile order: 0 = m-tile fastest over the whole problem;
+                         // g > 0 = groups of g m-tiles, each group's tiles n-tile by
+                         // n-tile (keeps a group's A and B rows in L2 together)
   void *out;             // output base (row-major)
   long long ldc;         // elements
   // Two-output problem (SM-pair kernel, bf16 epilogue, 256-column tiles only):
@@ -183,6 +185,7 @@ struct GemmBuilder {
   int a_rows = 128;   // A box rows of the single-CTA kernels (see a_box_rows)
   int split = 0;      // 0: chosen at launch; >1: split-K over a cluster, reduced in fixed
                       // order through DSMEM; 1: the persistent kernels
+  int m_group = 0;    // tile order of the problems added after it is set (GemmProblem::m_group)
   // What each map was made from, so launch() can re-encode them as 3-D maps.
   struct MapArgs {
     const void *base;
