@@ -370,6 +370,13 @@ tp_status gemm_bf16_row_ring(int32_t n, const tp_tensor *x, const tp_tensor *w, 
     b.bn = choose_pair_bn(T, nc.data(), n, false, &b_rows);  // the width the unfolded GEMM takes
   }
   b.a_rows = 128;
+  // Tiles in groups of two ring chunks' row tiles: the tiles of one chunk fold
+  // the ranks in the same order, so with few chunks in flight fewer ranks' K
+  // slices are live in L2 at once. On the prefill layer's down projection
+  // (T = 4096, N = 8, K = 3584 per rank) DRAM reads drop from 4.64 to 3.77 GB
+  // and the launch from 1.297 to 1.264 ms; one or four chunks per group did less.
+  const long long chunk_tiles = (T / n) / 256;
+  b.m_group = chunk_tiles > 0 && chunk_tiles <= (1 << 20) ? static_cast<int>(2 * chunk_tiles) : 0;
   tp_status err = TP_OK;
   std::vector<int> am(n), bm(n);
   std::vector<long long> ks(n);
