@@ -351,6 +351,10 @@ size_t tp_attn_core_workspace_size(const tp_plan *plan, int64_t tokens);
  *  workspace : at least tp_attn_core_workspace_size bytes, 16-byte aligned.
  * d must be 128 and tp_size at most 32, with at most 256 q heads in all,
  * else TP_ERR_UNSUPPORTED.
+ * The kernel is chosen on every call by the environment variable TPGQA_ATTN:
+ * unset (or any other value), two 128-query tiles per CTA; 1, one tile per
+ * CTA; 3, two tiles over 64-key blocks; 4, a 256-query tile on an SM pair. All
+ * compute the same result within rounding (P and A are rounded to bf16).
  * Errors: TP_ERR_INVALID_ARG, TP_ERR_DTYPE, TP_ERR_ALIGNMENT, TP_ERR_WORKSPACE,
  * TP_ERR_UNSUPPORTED, TP_ERR_RANK_FAILED, TP_ERR_CUDA. */
 tp_status tp_attn_core(const tp_plan *plan, const tp_tensor *q, const tp_tensor *k, const tp_tensor *v,

@@ -104,11 +104,14 @@ def test_first_row_is_the_first_value_row():
         assert np.array_equal(host_f64(got[0])[0, h * HD:(h + 1) * HD], v0[0, kvh * HD:(kvh + 1) * HD])
 
 
-def test_attn_core_tp8_t4096_sampled_rows():
+@pytest.mark.parametrize("kernel", ["2", "4"])
+def test_attn_core_tp8_t4096_sampled_rows(kernel, monkeypatch):
     """The benchmarked configuration (TP=8, 64 q heads, 8 kv heads, 4096 tokens,
     causal), checked on a seeded sample of query rows of two heads per rank:
-    causal row i is the full softmax over keys 0..i."""
+    causal row i is the full softmax over keys 0..i. Run with the default
+    two-tile kernel and with the SM-pair kernel (TPGQA_ATTN=4)."""
     need_gpu()
+    monkeypatch.setenv("TPGQA_ATTN", kernel)
     torch = _torch()
     w = inputs.WORKLOADS["attn_core_tp8_t4096"]
     n, t = w["tp"], w["T"]
