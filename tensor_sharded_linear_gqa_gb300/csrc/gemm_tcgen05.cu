@@ -150,30 +150,37 @@ __device__ __forceinline__ int find_problem(const GemmParams &p, int tile) {
 }
 
 // (m-tile, n-tile) of a problem's tile `local`: m fastest over the problem, or
-// over groups of m_group m-tiles (the last group may be shorter).
+// with GROUPED over groups of m_group m-tiles (the last group may be shorter).
+// Only the kernels that take grouped problems compile the grouped form: its
+// mere presence in the other kernels cost 1.5-3 us per step of back-to-back
+// small GEMMs (the T=512 MLP block, decode), with m_group = 0 at run time.
+template <bool GROUPED>
 __device__ __forceinline__ void tile_coords(const GemmProblem &pr, int local, int &mt, int &nt) {
-  const int g = pr.m_group;
-  if (g <= 0 || g >= pr.m_tiles) {
-    mt = local % pr.m_tiles;
-    nt = local / pr.m_tiles;
-    return;
+  if constexpr (GROUPED) {
+    const int g = pr.m_group;
+    if (g > 0 && g < pr.m_tiles) {
+      const int per_group = g * pr.n_tiles;
+      const int grp = local / per_group, r = local - grp * per_group;
+      const int rows = min(g, pr.m_tiles - grp * g);
+      mt = grp * g + r % rows;
+      nt = r / rows;
+      return;
+    }
   }
-  const int per_group = g * pr.n_tiles;
-  const int grp = local / per_group, r = local - grp * per_group;
-  const int rows = min(g, pr.m_tiles - grp * g);
-  mt = grp * g + r % rows;
-  nt = r / rows;
+  mt = local % pr.m_tiles;
+  nt = local / pr.m_tiles;
 }
 
 // First tile at or after `tile`, stepping by `stride`, that its problem's block
 // table does not skip (every tile when there is no table). The producer, the
 // MMA issuer and the epilogue all step with it, so they see the same tiles.
+template <bool GROUPED = false>
 __device__ __forceinline__ int live_tile(const GemmParams &p, int tile, int stride) {
   for (; tile < p.total_tiles; tile += stride) {
     const GemmProblem &pr = p.prob[find_problem(p, tile)];
     if (!pr.blk) break;
     int mt, nt;
-    tile_coords(pr, tile - pr.tile_begin, mt, nt);
+    tile_coords<GROUPED>(pr, tile - pr.tile_begin, mt, nt);
     const int v = __ldg(pr.blk + mt);
     if (v >= 0 && (v >> 16) < pr.n_moff) break;
   }
@@ -194,7 +201,7 @@ __device__ __forceinline__ void cursor_tile(const GemmParams &p, Cursor &c, int 
   if (!c.valid) return;
   c.prob = find_problem(p, tile);
   const GemmProblem &pr = p.prob[c.prob];
-  tile_coords(pr, tile - pr.tile_begin, c.mt, c.nt);
+  tile_coords<false>(pr, tile - pr.tile_begin, c.mt, c.nt);
   tile_b_origin(pr, c.mt, c.moff, c.brow);
   c.seg = 0;
   c.kt = 0;
@@ -411,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16(const __grid_constant
       }
       const GemmProblem &pr = p.prob[find_problem(p, tile)];
       int mt, nt;
-      tile_coords(pr, tile - pr.tile_begin, mt, nt);
+      tile_coords<false>(pr, tile - pr.tile_begin, mt, nt);
       const int row = mt * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(a) * kAccStride +
                              (static_cast<uint32_t>(q * 32) << 16);
@@ -549,7 +556,8 @@ __device__ __forceinline__ int tile_stages(const GemmParams &p, int prob) {
   return n;
 }
 
-template <int EPI, int KSUB, int BN>
+// GROUPED: the problems may order their tiles in groups of m-tiles (m_group).
+template <int EPI, int KSUB, int BN, bool GROUPED = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_gemm_bf16_pair(const __grid_constant__ GemmParams p) {
   using PC = PairCfg<KSUB, BN>;
@@ -625,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0 && p.early_b && pair < p.total_tiles) {
     const GemmProblem &pr = p.prob[find_problem(p, pair)];
     int mt0, nt;
-    tile_coords(pr, pair - pr.tile_begin, mt0, nt);
+    tile_coords<GROUPED>(pr, pair - pr.tile_begin, mt0, nt);
     for (int sgi = 0; sgi < pr.seg_count && pre < S; ++sgi) {
       const GemmSeg &sg = p.seg[pr.seg_begin + sgi];
       const bool two_b = EPI == kEpiSwiGLU || sg.b2_map >= 0;
@@ -656,13 +664,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // Cursor over this pair's tiles: tiles pair, pair + npairs, ...
       auto first = [&](Cursor &c) {
-        const int t = live_tile(p, pair, npairs);
+        const int t = live_tile<GROUPED>(p, pair, npairs);
         c.tile = t;
         c.valid = t < p.total_tiles;
         if (!c.valid) return;
         c.prob = find_problem(p, t);
         const GemmProblem &pr = p.prob[c.prob];
-        tile_coords(pr, t - pr.tile_begin, c.mt, c.nt);
+        tile_coords<GROUPED>(pr, t - pr.tile_begin, c.mt, c.nt);
         tile_b_origin(pr, c.mt, c.moff, c.brow);
         c.seg = c.kt = c.kt_in_tile = 0;
       };
@@ -673,13 +681,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (c.kt < seg_stages<KSUB>(p.seg[pr.seg_begin + c.seg])) return;
         c.kt = 0;
         if (++c.seg < pr.seg_count) return;
-        const int t = live_tile(p, c.tile + npairs, npairs);
+        const int t = live_tile<GROUPED>(p, c.tile + npairs, npairs);
         c.tile = t;
         c.valid = t < p.total_tiles;
         if (!c.valid) return;
         c.prob = find_problem(p, t);
         const GemmProblem &q = p.prob[c.prob];
-        tile_coords(q, t - q.tile_begin, c.mt, c.nt);
+        tile_coords<GROUPED>(q, t - q.tile_begin, c.mt, c.nt);
         tile_b_origin(q, c.mt, c.moff, c.brow);
         c.seg = c.kt = c.kt_in_tile = 0;
       };
@@ -769,8 +777,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(256, kMmaN);
       int kb = 0;
       bool ok = true;
-      for (int tile = live_tile(p, pair, npairs), j = 0; ok && tile < p.total_tiles;
-           tile = live_tile(p, tile + npairs, npairs), ++j) {
+      for (int tile = live_tile<GROUPED>(p, pair, npairs), j = 0; ok && tile < p.total_tiles;
+           tile = live_tile<GROUPED>(p, tile + npairs, npairs), ++j) {
         const int a = j % kAcc;
         const uint32_t use = static_cast<uint32_t>(j / kAcc);
         if (*abort_flag || !ptx::mbar_wait(tempty_bar(a), (use & 1) ^ 1, p.wait_ns)) {
@@ -816,8 +824,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     const int q = warp & 3;
-    for (int tile = live_tile(p, pair, npairs), j = 0; tile < p.total_tiles;
-         tile = live_tile(p, tile + npairs, npairs), ++j) {
+    for (int tile = live_tile<GROUPED>(p, pair, npairs), j = 0; tile < p.total_tiles;
+         tile = live_tile<GROUPED>(p, tile + npairs, npairs), ++j) {
       const int a = j % kAcc;
       const uint32_t use = static_cast<uint32_t>(j / kAcc);
       const bool ready = ptx::mbar_wait(tfull_bar(a), use & 1, p.wait_ns);
@@ -829,7 +837,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const GemmProblem &pr = p.prob[find_problem(p, tile)];
       int mt, nt;
-      tile_coords(pr, tile - pr.tile_begin, mt, nt);
+      tile_coords<GROUPED>(pr, tile - pr.tile_begin, mt, nt);
       const int row = mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(a * 256) +
                              (static_cast<uint32_t>(q * 32) << 16);
@@ -1019,7 +1027,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int pre = 0;
   if (warp == 0 && lane == 0 && p.early_b && pair < p.total_tiles) {
     int mt, nt;
-    tile_coords(pr, pair, mt, nt);
+    tile_coords<true>(pr, pair, mt, nt);
     const int b_row = nt * BN + static_cast<int>(crank) * kHalfB;
     for (int s = 0; s < nrank && pre < S; ++s) {
       const GemmSeg &sg = p.seg[pr.seg_begin + fold_rank(mt, s)];
@@ -1046,7 +1054,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool go = true;
       for (int t = pair; go && t < p.total_tiles; t += npairs) {
         int mt, nt;
-        tile_coords(pr, t, mt, nt);
+        tile_coords<true>(pr, t, mt, nt);
         const int a_row = mt * 256 + static_cast<int>(crank) * 128;
         const int b_row = nt * BN + static_cast<int>(crank) * kHalfB;
         for (int s = 0; go && s < nrank; ++s) {
@@ -1094,7 +1102,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = pair, jt = 0; ok && t < p.total_tiles; t += npairs, ++jt) {
         int mt, nt;
-        tile_coords(pr, t, mt, nt);
+        tile_coords<true>(pr, t, mt, nt);
         for (int s = 0; ok && s < nrank; ++s) {
           const int reg = s == 0 ? (jt & 1) : ((jt & 1) ^ 1);
           uint32_t &taken = reg ? taken1 : taken0;
@@ -1159,7 +1167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
     for (int t = pair, jt = 0; alive && t < p.total_tiles; t += npairs, ++jt) {
       int mt, nt;
-      tile_coords(pr, t, mt, nt);
+      tile_coords<true>(pr, t, mt, nt);
       const int rs = jt & 1, ra = rs ^ 1;
       const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
       const uint32_t tsum = tmem_base + static_cast<uint32_t>(rs * 256) + lane_off;
@@ -1355,7 +1363,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_bf16_splitk(const __grid_c
   const int pi = find_problem(p, tile);
   const GemmProblem &pr = p.prob[pi];
   int mt, nt;
-  tile_coords(pr, tile - pr.tile_begin, mt, nt);
+  tile_coords<false>(pr, tile - pr.tile_begin, mt, nt);
   // Ring folding (ring_rows > 0): split s is segment (rank) s, whole. Otherwise
   // the problem's stages are cut into nsplit near-equal ranges.
   const bool ring = p.ring_rows > 0;
@@ -1830,7 +1838,7 @@ tp_status launch_one(const GemmParams &p, cudaStream_t stream) {
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
 
-template <int EPI, int KSUB, int BN>
+template <int EPI, int KSUB, int BN, bool GROUPED = false>
 tp_status launch_pair_ks(const GemmParams &p, cudaStream_t stream) {
   static int configured_mask = 0;
   static std::mutex mu;
@@ -1840,7 +1848,7 @@ tp_status launch_pair_ks(const GemmParams &p, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> g(mu);
     if (dev >= 32 || !(configured_mask & (1 << dev))) {
-      e = cudaFuncSetAttribute(k_gemm_bf16_pair<EPI, KSUB, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      e = cudaFuncSetAttribute(k_gemm_bf16_pair<EPI, KSUB, BN, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                PairCfg<KSUB, BN>::kSmem);
       if (e != cudaSuccess) return cuda_fail(e);
       if (dev < 32) configured_mask |= (1 << dev);
@@ -1848,8 +1856,8 @@ tp_status launch_pair_ks(const GemmParams &p, cudaStream_t stream) {
   }
   const int pairs_max = num_sms() / 2;
   const int pairs = p.total_tiles < pairs_max ? p.total_tiles : pairs_max;
-  e = launch_kernel(k_gemm_bf16_pair<EPI, KSUB, BN>, dim3(2 * pairs), dim3(kThreads), PairCfg<KSUB, BN>::kSmem,
-                    stream, 1, p);
+  e = launch_kernel(k_gemm_bf16_pair<EPI, KSUB, BN, GROUPED>, dim3(2 * pairs), dim3(kThreads),
+                    PairCfg<KSUB, BN>::kSmem, stream, 1, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? TP_OK : cuda_fail(e);
 }
@@ -1878,7 +1886,12 @@ tp_status launch_pair(const GemmParams &p, int bn, cudaStream_t stream) {
   if (bn == 224) return launch_pair_ks<EPI, 2, 224>(p, stream);
   if (bn == 128) return launch_pair_ks<EPI, 2, 128>(p, stream);
   if (bn != 256) return TP_ERR_UNSUPPORTED;
-  return pair_ksub() == 2 ? launch_pair_ks<EPI, 2, 256>(p, stream) : launch_pair_ks<EPI, 3, 256>(p, stream);
+  if (pair_ksub() != 2) return launch_pair_ks<EPI, 3, 256>(p, stream);
+  // The grouped tile order (MoE problems) has its own instantiation; other
+  // widths run every problem m-tile first, which changes no result.
+  bool grouped = false;
+  for (int i = 0; i < p.num_problems; ++i) grouped = grouped || p.prob[i].m_group > 0;
+  return grouped ? launch_pair_ks<EPI, 2, 256, true>(p, stream) : launch_pair_ks<EPI, 2, 256>(p, stream);
 }
 
 template <int KSUB, int BN>
