@@ -91,6 +91,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// The two-tile and SM-pair kernels take p = 2^(s*c - m) against the row's running
+// maximum m without first finding the maximum of each key block: softmax does not
+// change with the constant taken off a row's scores, so m only has to keep p and
+// the sums far inside the f32 range. p above 1 keeps the same relative precision
+// in bf16 P and in the f32 sums. The block's maximum is found (find_max) on an
+// item's first block, and on a later block only when the block's sum of p
+// passes kSumLimit or is not finite; then m moves to that maximum when it
+// exceeds m by more than 8 (log2 units), p is taken again, and the row of O is
+// rescaled by 2^(m_old - m_new). So p <= 2^64 always, and a row of O sums at
+// most 2^64 * T * max|v|, far inside the f32 range (2^128) for values of
+// ordinary size.
+constexpr float kSumLimit = 0x1p64f;
+
 tp_status launch_checked(cudaError_t e) {
   if (e != cudaSuccess) return cuda_fail(e);
   const cudaError_t l = cudaGetLastError();
@@ -460,10 +473,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention(const __grid_cons
 // S (two values per 32-bit column), and P V reads it from there as the A
 // operand (the tensor-memory form of tcgen05.mma), so P never goes through
 // shared memory. S of the next block is issued after P V of this one, which has
-// read P by then (the tensor core runs one issuer's MMAs in order). The
-// reference maximum moves only when a block's maximum exceeds it by more than
-// 8 (log2 units); then that row of O is rescaled in TMEM: O is current up to the
-// previous block whenever S of a block is complete, so no extra wait is needed.
+// read P by then (the tensor core runs one issuer's MMAs in order). p is taken
+// against the row's running maximum, which moves only as kSumLimit describes;
+// then that row of O is rescaled in TMEM: O is current up to the previous block
+// whenever S of a block is complete, so no extra wait is needed.
 // Every wait is bounded, as in k_attention.
 // ---------------------------------------------------------------------------
 constexpr uint32_t k2SmemQ = 0, k2SmemK = 2 * kTile, k2SmemV = 4 * kTile;  // Q_A, Q_B; K ring; V^T ring
@@ -726,44 +739,54 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention2(const __grid_con
           for (int i = 0; i < 128; ++i)
             if (i >= lim) v[i] = __float_as_uint(-INFINITY);
         }
-        // the row maximum as four independent chains over the key quarters
-        float mq[4];
+        // p = 2^(s*c - m) against the row's running maximum m (see find_max)
+        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
+        bool find_max = j == 0, move = false;
+        float m_new = m, s0, s1;
+#pragma unroll 1
+        for (;;) {
+          if (find_max) {
+            // the row maximum as four independent chains over the key quarters
+            float mq[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mq[q] = __uint_as_float(v[32 * q + 31]);
+            for (int q = 0; q < 4; ++q) {
+              mq[q] = __uint_as_float(v[32 * q + 31]);
 #pragma unroll
-          for (int i = 0; i < 30; i += 2)
-            mq[q] = max3f(mq[q], __uint_as_float(v[32 * q + i]), __uint_as_float(v[32 * q + i + 1]));
-          mq[q] = fmaxf(mq[q], __uint_as_float(v[32 * q + 30]));
-        }
-        const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-        const float m_blk = mx * p.scale_log2;
-        const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
-        const float m_new = move ? m_blk : m;
-        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
-        // p = 2^(s*c - m), two keys at a time (packed f32x2 fma and sum), packed as
-        // bf16 pairs into the first 64 columns of S, 16 columns at a time
-        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
-        uint64_t sumh[4];  // one running pair of sums per 32-key quarter
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint64_t &sum2 = sumh[h];
-          sum2 = pack2(0.f, 0.f);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float y0, y1;
-            unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
-                    y1);
-            const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
-            sum2 = add2(sum2, pack2(a0, a1));
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
-            memcpy(&pk[i >> 1], &hb, 4);
+              for (int i = 0; i < 30; i += 2)
+                mq[q] = max3f(mq[q], __uint_as_float(v[32 * q + i]), __uint_as_float(v[32 * q + i + 1]));
+              mq[q] = fmaxf(mq[q], __uint_as_float(v[32 * q + 30]));
+            }
+            const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
+            move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
+            m_new = move ? m_blk : m;
           }
-          ptx::tmem_st_16cols(sb + 16 * h, pk);
+          // two keys at a time (packed f32x2 fma and sum), packed as bf16 pairs
+          // into the first 64 columns of S, 16 columns at a time
+          const uint64_t nm2 = pack2(-m_new, -m_new);
+          uint64_t sumh[4];  // one running pair of sums per 32-key quarter
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint64_t &sum2 = sumh[h];
+            sum2 = pack2(0.f, 0.f);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float y0, y1;
+              unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
+                      y1);
+              const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
+              sum2 = add2(sum2, pack2(a0, a1));
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
+              memcpy(&pk[i >> 1], &hb, 4);
+            }
+            ptx::tmem_st_16cols(sb + 16 * h, pk);
+          }
+          unpack2(add2(add2(sumh[0], sumh[1]), add2(sumh[2], sumh[3])), s0, s1);
+          if (find_max || !__any_sync(0xffffffffu, !(s0 + s1 <= kSumLimit))) break;
+          find_max = true;
+          ptx::tmem_st_wait();  // this pass's P is written over before the next pass's
         }
-        float s0, s1;
-        unpack2(add2(add2(sumh[0], sumh[1]), add2(sumh[2], sumh[3])), s0, s1);
+        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
         l = l * alpha + (s0 + s1);
         m = m_new;
         if (j > 0 && __any_sync(0xffffffffu, move)) {
@@ -1257,9 +1280,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_attention3(const __grid_con
 //              CTAs arrive on the leader's barriers with relaxed cluster-scope
 //              arrives: each follows the thread's own wait for its tcgen05 loads
 //              or stores, and the release form costs a thousand cycles on a busy
-//              SM. The reference maximum moves only when a block's maximum
-//              exceeds it by more than 8 (log2 units); then the row of O is
-//              rescaled in TMEM once the previous P V has landed. At the end of
+//              SM. p is taken against the row's running maximum, which moves
+//              only as kSumLimit describes; then the row of O is rescaled in
+//              TMEM once the previous P V has landed. At the end of
 //              an item O / l is stored; the next item's first P V, which
 //              overwrites O, waits for the same threads' next P hand-off;
 //   warp 6     in the leader, the P V thread.
@@ -1619,44 +1642,55 @@ __global__ void __launch_bounds__(kAttn4Threads, 1) k_attention4(const __grid_co
           for (int i = 0; i < 128; ++i)
             if (i >= lim) v[i] = __float_as_uint(-INFINITY);
         }
-        // the row maximum as four independent chains over the key quarters
-        float mq[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mq[q] = __uint_as_float(v[32 * q + 31]);
-#pragma unroll
-          for (int i = 0; i < 30; i += 2)
-            mq[q] = max3f(mq[q], __uint_as_float(v[32 * q + i]), __uint_as_float(v[32 * q + i + 1]));
-          mq[q] = fmaxf(mq[q], __uint_as_float(v[32 * q + 30]));
-        }
-        const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
-        const bool move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
-        const float m_new = move ? m_blk : m;
-        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
-        // p = 2^(s*c - m), two keys at a time, packed as bf16 pairs into P buffer b,
-        // 16 columns (32 keys) at a time
-        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2), nm2 = pack2(-m_new, -m_new);
+        // p = 2^(s*c - m) against the row's running maximum m (see find_max)
+        const uint64_t c2 = pack2(p.scale_log2, p.scale_log2);
         const uint32_t pb = tmem + lane_off + k4ColP + 64u * b;
-        uint64_t sumh[4];
+        bool find_max = j == 0, move = false;
+        float m_new = m, s0, s1;
+#pragma unroll 1
+        for (;;) {
+          if (find_max) {
+            // the row maximum as four independent chains over the key quarters
+            float mq[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint64_t &sum2 = sumh[h];
-          sum2 = pack2(0.f, 0.f);
-          uint32_t pk[16];
+            for (int q = 0; q < 4; ++q) {
+              mq[q] = __uint_as_float(v[32 * q + 31]);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float y0, y1;
-            unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
-                    y1);
-            const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
-            sum2 = add2(sum2, pack2(a0, a1));
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
-            memcpy(&pk[i >> 1], &hb, 4);
+              for (int i = 0; i < 30; i += 2)
+                mq[q] = max3f(mq[q], __uint_as_float(v[32 * q + i]), __uint_as_float(v[32 * q + i + 1]));
+              mq[q] = fmaxf(mq[q], __uint_as_float(v[32 * q + 30]));
+            }
+            const float m_blk = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * p.scale_log2;
+            move = m_blk > m + 8.f;  // always on the item's first block (m = -inf)
+            m_new = move ? m_blk : m;
           }
-          ptx::tmem_st_16cols(pb + 16u * static_cast<uint32_t>(h), pk);
+          // two keys at a time, packed as bf16 pairs into P buffer b, 16 columns
+          // (32 keys) at a time
+          const uint64_t nm2 = pack2(-m_new, -m_new);
+          uint64_t sumh[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint64_t &sum2 = sumh[h];
+            sum2 = pack2(0.f, 0.f);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float y0, y1;
+              unpack2(fma2(pack2(__uint_as_float(v[32 * h + i]), __uint_as_float(v[32 * h + i + 1])), c2, nm2), y0,
+                      y1);
+              const float a0 = ex2_approx(y0), a1 = ex2_approx(y1);
+              sum2 = add2(sum2, pack2(a0, a1));
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(a0, a1);
+              memcpy(&pk[i >> 1], &hb, 4);
+            }
+            ptx::tmem_st_16cols(pb + 16u * static_cast<uint32_t>(h), pk);
+          }
+          unpack2(add2(add2(sumh[0], sumh[1]), add2(sumh[2], sumh[3])), s0, s1);
+          if (find_max || !__any_sync(0xffffffffu, !(s0 + s1 <= kSumLimit))) break;
+          find_max = true;
+          ptx::tmem_st_wait();  // this pass's P is written over before the next pass's
         }
-        float s0, s1;
-        unpack2(add2(add2(sumh[0], sumh[1]), add2(sumh[2], sumh[3])), s0, s1);
+        const float alpha = move ? exp2f(m - m_new) : 1.f;  // 0 on the first block
         l = l * alpha + (s0 + s1);
         m = m_new;
         if (j > 0 && __any_sync(0xffffffffu, move)) {
