@@ -184,6 +184,32 @@ def test_projection_attention_o_proj_chain(tp_size, hq, hkv):
 
 
 @pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("kernel", ["2", "4"])
+def test_running_maximum_lags_then_moves(kernel, causal, monkeypatch):
+    """The kernels take p against the row's running maximum and look for a block's
+    own maximum only when the block's sum of p passes 2^64. Keys of the second
+    128-key block scaled by 8 put each row's maximum 15 to 30 (log2 units, for
+    the first head of rank 0) above the first block's, so p reaches 2^15 to 2^30
+    with the maximum left where it is; keys of the third block scaled by 30 put
+    it 70 to 110 above, so the maximum moves, p is taken again and O is rescaled;
+    the fourth block is back to ordinary scores. The result must still be the
+    softmax of the oracle."""
+    need_gpu()
+    monkeypatch.setenv("TPGQA_ATTN", kernel)
+    m = Attn(2, 4, 2, 512, seed=622)
+    factor = np.ones((512, 1), dtype=np.float32)
+    factor[128:256] = 8.0
+    factor[256:384] = 30.0
+    for r in range(len(m.k)):
+        kb = inputs.normal_f32(622, 300 + r, m.k[r].shape) * factor
+        m.k[r] = inputs.f32_to_bf16_bits(kb)
+    got = m.run(causal)
+    ref = m.oracle(causal)
+    for r in range(m.n):
+        assert_close(host_f64(got[r]), ref[r], BF16_TOL, f"kernel {kernel} rank {r}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("kernel", ["1", "2", "3", "4"])
 def test_every_attention_kernel_matches_the_oracle(kernel, causal, monkeypatch):
     """The four attention kernels (TPGQA_ATTN=1: one 128-query tile per work item;
